@@ -1,0 +1,294 @@
+"""Python entry to the fp64 CPU oracle (``sa_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` are the only callers.  The product library never
+imports this package, and this package imports nothing from the product.
+
+Arguments are torch CPU tensors (or numpy arrays) in their storage dtype; the
+C code widens them exactly to double itself.  Results come back as float64
+numpy arrays.  Every call releases the GIL (ctypes), so disjoint row subsets
+can be evaluated from several Python threads at once.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sa_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, F16, BF16, FP8REC = 0, 1, 2, 3
+IDX_OK = 0
+IDX_BELOW_SENTINEL = 1
+IDX_AFTER_PADDING = 2
+IDX_OUT_OF_RANGE = 4
+IDX_NOT_INCREASING = 8
+IDX_DUPLICATE = 16
+IDX_ALL_PADDING = 32
+
+_i64 = C.c_int64
+_p = C.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler (plain -O2, no fast-math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+                   check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _SparseArgs(C.Structure):
+    _fields_ = [
+        ("q", _p), ("q_dtype", C.c_int), ("k", _p), ("v", _p), ("kv_dtype", C.c_int),
+        ("idx", _p), ("idx_is_i64", C.c_int),
+        ("B", _i64), ("Hq", _i64), ("Hkv", _i64), ("Sq", _i64), ("D", _i64), ("Dv", _i64),
+        ("T", _i64), ("I", _i64), ("K", _i64),
+        ("kv_len", _p), ("past_len", _i64), ("causal", C.c_int),
+        ("scale", C.c_double), ("softcap", C.c_double), ("window", _i64), ("sink", _p),
+        ("record_bytes", _i64), ("n_rope", _i64),
+    ]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = C.CDLL(build())
+            L.orc_f16_to_double.restype = C.c_double
+            L.orc_f16_to_double.argtypes = [C.c_uint16]
+            L.orc_bf16_to_double.restype = C.c_double
+            L.orc_bf16_to_double.argtypes = [C.c_uint16]
+            L.orc_e4m3fn_to_double.restype = C.c_double
+            L.orc_e4m3fn_to_double.argtypes = [C.c_uint8]
+            L.orc_e8m0_to_double.restype = C.c_double
+            L.orc_e8m0_to_double.argtypes = [C.c_uint8]
+            L.orc_decode_fp8_record.restype = None
+            L.orc_decode_fp8_record.argtypes = [_p, _i64, _i64, _p]
+            L.orc_validate_row.restype = C.c_int
+            L.orc_validate_row.argtypes = [_p, C.c_int, _i64, _i64, C.POINTER(_i64)]
+            L.orc_validate_indices.restype = None
+            L.orc_validate_indices.argtypes = [_p, C.c_int, _i64, _i64, _i64, _i64, _p, _i64,
+                                               _p, _p]
+            L.orc_present_concat.restype = None
+            L.orc_present_concat.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64,
+                                             _i64]
+            L.orc_present_append.restype = None
+            L.orc_present_append.argtypes = [_p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _p]
+            L.orc_sparse_attention.restype = C.c_int
+            L.orc_sparse_attention.argtypes = [C.POINTER(_SparseArgs), _p, _i64, _p]
+            L.orc_prefill.restype = C.c_int
+            L.orc_prefill.argtypes = [_p, _p, _p, C.c_int, _i64, _i64, _i64, _i64, _i64,
+                                      C.c_int, C.c_double, C.c_double, _p, _i64, _p]
+            L.orc_paged_decode.restype = C.c_int
+            L.orc_paged_decode.argtypes = [_p, _p, _p, C.c_int, _p, _p, _i64, _i64, _i64,
+                                           _i64, _i64, _i64, C.c_double, _p, _i64, _p]
+            _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def _host(x):
+    """Contiguous CPU torch tensor (kept alive by the caller's reference)."""
+    if isinstance(x, np.ndarray):
+        x = torch.from_numpy(np.ascontiguousarray(x))
+    return x.detach().to("cpu").contiguous()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    return {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}[t.dtype]
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _rows_arg(rows):
+    if rows is None:
+        return None, 0
+    r = torch.as_tensor(np.asarray(rows, dtype=np.int64)).contiguous()
+    return r, int(r.numel())
+
+
+# ---------------------------------------------------------------------------
+# scalar decoders
+# ---------------------------------------------------------------------------
+
+def f16_to_double(bits: int) -> float:
+    return lib().orc_f16_to_double(bits)
+
+
+def bf16_to_double(bits: int) -> float:
+    return lib().orc_bf16_to_double(bits)
+
+
+def e4m3fn_to_double(code: int) -> float:
+    return lib().orc_e4m3fn_to_double(code)
+
+
+def e8m0_to_double(b: int) -> float:
+    return lib().orc_e8m0_to_double(b)
+
+
+def decode_fp8_record(rec, n_nope: int, n_rope: int) -> np.ndarray:
+    r = _host(torch.as_tensor(rec, dtype=torch.uint8))
+    out = np.zeros(n_nope + n_rope, dtype=np.float64)
+    lib().orc_decode_fp8_record(r.data_ptr(), n_nope, n_rope, out.ctypes.data)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# index validation / present KV
+# ---------------------------------------------------------------------------
+
+def validate_row(row, bound: int):
+    r = _host(torch.as_tensor(row, dtype=torch.int64))
+    col = _i64(-1)
+    code = lib().orc_validate_row(r.data_ptr(), 1, r.numel(), bound, C.byref(col))
+    return code, col.value
+
+
+def validate_indices(idx, bound: int = 0, bound_per_batch=None):
+    """idx ``[B, I, Sq, K]`` int32/int64 → (status uint8 ``[B*I*Sq]``, err)."""
+    t = _host(idx)
+    B, I, Sq, K = t.shape
+    bb = None if bound_per_batch is None else _host(torch.as_tensor(bound_per_batch,
+                                                                    dtype=torch.int64))
+    status = np.zeros(B * I * Sq, dtype=np.uint8)
+    err = C.c_uint32(0)
+    lib().orc_validate_indices(t.data_ptr(), int(t.dtype == torch.int64), B, I, Sq, K,
+                               _ptr(bb), bound, status.ctypes.data, C.addressof(err))
+    return status, err.value
+
+
+def present_concat(past, cur, out_stride=None):
+    """past ``[B,H,P,D]`` (or None), cur ``[B,H,C,D]`` → ``[B,H,stride,D]``
+    (positions beyond P+C are zero)."""
+    c = _host(cur)
+    B, H, Cn, D = c.shape
+    if past is None:
+        p = torch.empty((B, H, 0, D), dtype=c.dtype)
+    else:
+        p = _host(past)
+    P = p.shape[2]
+    stride = P + Cn if out_stride is None else out_stride
+    out = torch.zeros((B, H, stride, D), dtype=c.dtype)
+    lib().orc_present_concat(p.data_ptr(), c.data_ptr(), out.data_ptr(), c.element_size(),
+                             B, H, P, Cn, D, stride)
+    return out
+
+
+def present_append(cache, cur, write_pos):
+    """Returns a copy of ``cache [B,H,cap,D]`` with ``cur [B,H,C,D]`` written
+    at ``write_pos[b]``."""
+    out = _host(cache).clone()
+    c = _host(cur)
+    B, H, Cn, D = c.shape
+    wp = _host(torch.as_tensor(write_pos, dtype=torch.int64))
+    lib().orc_present_append(c.data_ptr(), out.data_ptr(), c.element_size(), B, H, Cn, D,
+                             out.shape[2], wp.data_ptr())
+    return out
+
+
+# ---------------------------------------------------------------------------
+# attention
+# ---------------------------------------------------------------------------
+
+def sparse_attention(q, idx, k=None, v=None, records=None, *, scale: float,
+                     softcap: float = 0.0, window: int = 0, kv_len=None,
+                     past_len: int = 0, causal: bool = False, sink=None,
+                     n_rope: int = 0, Dv=None, rows=None) -> np.ndarray:
+    """Selected-token attention; see ``orc_sparse_attention``.
+
+    Dense cache: ``k``/``v`` ``[B, Hkv, T, D]``.  FP8: ``records``
+    ``[B, Hkv, T, record_bytes]`` uint8 (K and V are the decoded record),
+    ``n_rope`` the bf16 tail width, logical ``D = 64*blocks + n_rope``."""
+    qh = _host(q)
+    B, Hq, Sq, D = qh.shape
+    ih = _host(idx)
+    _, I, _, K = ih.shape
+    a = _SparseArgs()
+    a.q, a.q_dtype = qh.data_ptr(), _dtype_code(qh)
+    keep = [qh, ih]
+    if records is not None:
+        rh = _host(records)
+        keep.append(rh)
+        a.k = a.v = rh.data_ptr()
+        a.kv_dtype = FP8REC
+        a.Hkv, a.T = rh.shape[1], rh.shape[2]
+        a.record_bytes = rh.shape[3]
+        a.n_rope = n_rope
+        a.Dv = D if Dv is None else Dv
+    else:
+        kh, vh = _host(k), _host(v)
+        keep += [kh, vh]
+        a.k, a.v, a.kv_dtype = kh.data_ptr(), vh.data_ptr(), _dtype_code(kh)
+        a.Hkv, a.T = kh.shape[1], kh.shape[2]
+        a.Dv = vh.shape[3]
+    a.idx, a.idx_is_i64 = ih.data_ptr(), int(ih.dtype == torch.int64)
+    a.B, a.Hq, a.Sq, a.D, a.I, a.K = B, Hq, Sq, D, I, K
+    kl = None if kv_len is None else _host(torch.as_tensor(kv_len, dtype=torch.int64))
+    a.kv_len = _ptr(kl)
+    a.past_len, a.causal = past_len, int(causal)
+    a.scale, a.softcap, a.window = scale, softcap, window
+    sk = None if sink is None else _host(torch.as_tensor(sink, dtype=torch.float64))
+    a.sink = _ptr(sk)
+    r, nr = _rows_arg(rows)
+    n = nr if r is not None else B * Hq * Sq
+    y = np.zeros((n, a.Dv), dtype=np.float64)
+    rc = lib().orc_sparse_attention(C.byref(a), _ptr(r), nr, y.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the sparse attention shape")
+    return y
+
+
+def prefill(q, k, v, *, scale: float, causal: bool = True, softcap: float = 0.0,
+            rows=None) -> np.ndarray:
+    qh, kh, vh = _host(q), _host(k), _host(v)
+    B, Hq, S, D = qh.shape
+    Hkv = kh.shape[1]
+    r, nr = _rows_arg(rows)
+    n = nr if r is not None else B * Hq * S
+    y = np.zeros((n, D), dtype=np.float64)
+    rc = lib().orc_prefill(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), _dtype_code(qh), B,
+                           Hq, Hkv, S, D, int(causal), scale, softcap, _ptr(r), nr,
+                           y.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the prefill shape")
+    return y
+
+
+def paged_decode(q, k_pool, v_pool, block_table, ctx_len, *, page_tokens: int,
+                 scale: float, rows=None) -> np.ndarray:
+    qh, kp, vp = _host(q), _host(k_pool), _host(v_pool)
+    bt = _host(block_table).to(torch.int32)
+    cl = _host(ctx_len).to(torch.int32)
+    B, Hq = qh.shape[0], qh.shape[1]
+    D = qh.shape[-1]
+    Hkv = kp.shape[1]
+    r, nr = _rows_arg(rows)
+    n = nr if r is not None else B * Hq
+    y = np.zeros((n, D), dtype=np.float64)
+    rc = lib().orc_paged_decode(qh.data_ptr(), kp.data_ptr(), vp.data_ptr(), _dtype_code(qh),
+                                bt.data_ptr(), cl.data_ptr(), B, Hq, Hkv, D, page_tokens,
+                                bt.shape[1], scale, _ptr(r), nr, y.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the paged shape")
+    return y

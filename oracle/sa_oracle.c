@@ -1,0 +1,569 @@
+/*
+ * sa_oracle.c -- plain, slow, fp64 CPU oracle for KV-cache attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do.  It shares no code, header, table or helper with the CUDA
+ * library: storage decoding, FP8 decoding, index validation, present-KV
+ * construction and attention are all written out again here, directly from
+ * the definitions, with no blocking, fusion or reordering.
+ *
+ * Sources (the pages' titles and sections):
+ *   [IS]  onnx-runtime-ep-cuda, src/kernels/index_share.rs -- IndexShare:
+ *         module docs (selected-token attention), `validate_indices`,
+ *         `build_present`, `index_share_row`.
+ *   [SA]  onnx-runtime-ep-cuda, src/kernels/standard_attention.rs -- ONNX
+ *         Attention: module docs "Semantics", `attention_row`,
+ *         `attention_combine` (fully-masked row gives 0).
+ *   [CSA] onnx-runtime-ep-cpu, src/kernels/compressed_sparse_attention.rs --
+ *         `CacheFormat` (hybrid FP8 record), `dequantize_cache`; and
+ *         onnx-runtime-ep-cuda compressed_sparse_attention.rs,
+ *         `csa_ratio128_sink_attention` (dense window + records, sink).
+ *   [PG]  ferrum-kernels, vnext_ops/transformer/causal_attention.rs --
+ *         16-token KV blocks addressed through a table.
+ *   OCP 8-bit floating point specification (E4M3FN) and the OCP MX
+ *   specification (E8M0 scale) for the FP8 record decode.
+ *
+ * Every floating-point step runs in double.  Inputs are widened exactly from
+ * their storage type (f32, f16, bf16, FP8 record).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_F32 0
+#define ORC_F16 1
+#define ORC_BF16 2
+#define ORC_FP8REC 3
+
+/* ------------------------------------------------------------------------ */
+/* Exact widening of storage types.                                          */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE 754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double orc_f16_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int ex = (h >> 10) & 0x1f;
+  int fr = h & 0x3ff;
+  double v;
+  if (ex == 0) {
+    v = ldexp((double)fr, -24); /* subnormal: fr * 2^-14 * 2^-10 */
+  } else if (ex == 31) {
+    v = fr ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(fr | 0x400), ex - 25); /* 1.fr * 2^(ex-15) */
+  }
+  return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+double orc_bf16_to_double(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+static double load_elem(const void* base, int64_t i, int dtype) {
+  if (dtype == ORC_F32) {
+    return (double)((const float*)base)[i];
+  }
+  if (dtype == ORC_F16) {
+    return orc_f16_to_double(((const uint16_t*)base)[i]);
+  }
+  return orc_bf16_to_double(((const uint16_t*)base)[i]);
+}
+
+/* OCP E4M3FN: 1 sign, 4 exponent (bias 7), 3 mantissa bits, no infinity;
+ * S.1111.111 is NaN; exponent field 0 is subnormal m * 2^-9. */
+double orc_e4m3fn_to_double(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int ex = (c >> 3) & 0xf;
+  int m = c & 0x7;
+  double v;
+  if (ex == 0xf && m == 0x7) {
+    return NAN;
+  }
+  if (ex == 0) {
+    v = ldexp((double)m, -9);
+  } else {
+    v = ldexp((double)(8 + m), ex - 10); /* (1 + m/8) * 2^(ex-7) */
+  }
+  return sign ? -v : v;
+}
+
+/* OCP MX E8M0 scale: 2^(b - 127); 0xFF is NaN. */
+double orc_e8m0_to_double(uint8_t b) {
+  if (b == 0xff) {
+    return NAN;
+  }
+  return ldexp(1.0, (int)b - 127);
+}
+
+/* Decode one hybrid FP8 record into `out[n_nope + n_rope]`:
+ * n_nope/64 blocks of [E8M0 scale byte, 64 E4M3FN codes], then n_rope
+ * little-endian bf16 values ([CSA] CacheFormat::Fp8E4m3Block64 and
+ * dequantize_cache). */
+void orc_decode_fp8_record(const uint8_t* rec, int64_t n_nope, int64_t n_rope, double* out) {
+  int64_t nb = n_nope / 64;
+  for (int64_t blk = 0; blk < nb; ++blk) {
+    const uint8_t* p = rec + blk * 65;
+    double s = orc_e8m0_to_double(p[0]);
+    for (int64_t d = 0; d < 64; ++d) {
+      out[blk * 64 + d] = orc_e4m3fn_to_double(p[1 + d]) * s;
+    }
+  }
+  const uint8_t* tail = rec + nb * 65;
+  for (int64_t r = 0; r < n_rope; ++r) {
+    uint16_t bits = (uint16_t)(tail[2 * r] | ((uint16_t)tail[2 * r + 1] << 8));
+    out[n_nope + r] = orc_bf16_to_double(bits);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Index validation ([IS] validate_indices).                                 */
+/* ------------------------------------------------------------------------ */
+
+#define ORC_IDX_OK 0
+#define ORC_IDX_BELOW_SENTINEL 1
+#define ORC_IDX_AFTER_PADDING 2
+#define ORC_IDX_OUT_OF_RANGE 4
+#define ORC_IDX_NOT_INCREASING 8
+#define ORC_IDX_DUPLICATE 16
+#define ORC_IDX_ALL_PADDING 32
+
+static int64_t load_index(const void* idx, int64_t i, int is_i64) {
+  return is_i64 ? ((const int64_t*)idx)[i] : (int64_t)((const int32_t*)idx)[i];
+}
+
+/* Scan one row left to right.  A -1 marks padding and is skipped; any other
+ * value is checked in this order: below the -1 sentinel, after padding, out
+ * of [0, bound), equal to the previous kept index, smaller than it.  The first
+ * failing column decides the status.  A row with no kept index is all
+ * padding. */
+int orc_validate_row(const void* row, int is_i64, int64_t K, int64_t bound,
+                     int64_t* bad_col) {
+  int padding = 0;
+  int have_prev = 0;
+  int64_t prev = 0;
+  int64_t count = 0;
+  for (int64_t col = 0; col < K; ++col) {
+    int64_t v = load_index(row, col, is_i64);
+    int code = ORC_IDX_OK;
+    if (v == -1) {
+      padding = 1;
+      continue;
+    }
+    if (v < -1) {
+      code = ORC_IDX_BELOW_SENTINEL;
+    } else if (padding) {
+      code = ORC_IDX_AFTER_PADDING;
+    } else if (v >= bound) {
+      code = ORC_IDX_OUT_OF_RANGE;
+    } else if (have_prev && v == prev) {
+      code = ORC_IDX_DUPLICATE;
+    } else if (have_prev && v < prev) {
+      code = ORC_IDX_NOT_INCREASING;
+    }
+    if (code != ORC_IDX_OK) {
+      if (bad_col) {
+        *bad_col = col;
+      }
+      return code;
+    }
+    prev = v;
+    have_prev = 1;
+    count += 1;
+  }
+  if (count == 0) {
+    if (bad_col) {
+      *bad_col = -1;
+    }
+    return ORC_IDX_ALL_PADDING;
+  }
+  if (bad_col) {
+    *bad_col = -1;
+  }
+  return ORC_IDX_OK;
+}
+
+/* Rows are [B, I, Sq] of K columns; batch b is bounded by bound_b[b] when
+ * given, else by `bound`.  Fills status[row] and ORs every status into *err. */
+void orc_validate_indices(const void* idx, int is_i64, int64_t B, int64_t I, int64_t Sq,
+                          int64_t K, const int64_t* bound_b, int64_t bound,
+                          uint8_t* status, uint32_t* err) {
+  uint32_t acc = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    int64_t bnd = bound_b ? bound_b[b] : bound;
+    for (int64_t h = 0; h < I; ++h) {
+      for (int64_t q = 0; q < Sq; ++q) {
+        int64_t row = (b * I + h) * Sq + q;
+        const char* base = (const char*)idx + row * K * (is_i64 ? 8 : 4);
+        int s = orc_validate_row(base, is_i64, K, bnd, NULL);
+        if (status) {
+          status[row] = (uint8_t)s;
+        }
+        acc |= (uint32_t)s;
+      }
+    }
+  }
+  if (err) {
+    *err = acc;
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Present KV ([IS] build_present; [SA] build_kv capacity append).           */
+/* ------------------------------------------------------------------------ */
+
+/* present[b,h,t,:] = past[b,h,t,:] for t < P, cur[b,h,t-P,:] for P <= t < P+C;
+ * present rows have stride `out_stride` positions (>= P+C).  Byte copy of
+ * `esz`-byte elements. */
+void orc_present_concat(const void* past, const void* cur, void* out, int64_t esz,
+                        int64_t B, int64_t H, int64_t P, int64_t C, int64_t D,
+                        int64_t out_stride) {
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t h = 0; h < H; ++h) {
+      for (int64_t t = 0; t < P + C; ++t) {
+        const char* src;
+        if (t < P) {
+          src = (const char*)past + (((b * H + h) * P + t) * D) * esz;
+        } else {
+          src = (const char*)cur + (((b * H + h) * C + (t - P)) * D) * esz;
+        }
+        char* dst = (char*)out + (((b * H + h) * out_stride + t) * D) * esz;
+        memcpy(dst, src, (size_t)(D * esz));
+      }
+    }
+  }
+}
+
+/* Append: cache[b,h,write_pos[b]+c,:] = cur[b,h,c,:]; all other positions of
+ * the capacity-`cap` cache are left as they are. */
+void orc_present_append(const void* cur, void* cache, int64_t esz, int64_t B, int64_t H,
+                        int64_t C, int64_t D, int64_t cap, const int64_t* write_pos) {
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t h = 0; h < H; ++h) {
+      for (int64_t c = 0; c < C; ++c) {
+        int64_t t = write_pos[b] + c;
+        const char* src = (const char*)cur + (((b * H + h) * C + c) * D) * esz;
+        char* dst = (char*)cache + (((b * H + h) * cap + t) * D) * esz;
+        memcpy(dst, src, (size_t)(D * esz));
+      }
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Attention over an explicit candidate key set.                             */
+/* ------------------------------------------------------------------------ */
+
+/* KV storage accessor: either a dense [B, Hkv, stride, D] tensor of f32/f16/
+ * bf16, or hybrid FP8 records [B, Hkv, stride, record_bytes] where K and V are
+ * the same decoded record (V optionally its first Dv dims). */
+typedef struct {
+  const void* k;
+  const void* v;
+  int dtype;
+  int64_t Hkv;
+  int64_t stride;       /* positions between consecutive (b, kvh) slabs */
+  int64_t D;
+  int64_t Dv;
+  int64_t record_bytes; /* FP8 only */
+  int64_t n_rope;       /* FP8 only */
+} orc_kv;
+
+static void get_k(const orc_kv* kv, int64_t b, int64_t h, int64_t t, double* out) {
+  if (kv->dtype == ORC_FP8REC) {
+    const uint8_t* rec = (const uint8_t*)kv->k +
+                         ((b * kv->Hkv + h) * kv->stride + t) * kv->record_bytes;
+    orc_decode_fp8_record(rec, kv->D - kv->n_rope, kv->n_rope, out);
+    return;
+  }
+  int64_t base = ((b * kv->Hkv + h) * kv->stride + t) * kv->D;
+  for (int64_t d = 0; d < kv->D; ++d) {
+    out[d] = load_elem(kv->k, base + d, kv->dtype);
+  }
+}
+
+static void get_v(const orc_kv* kv, int64_t b, int64_t h, int64_t t, double* out,
+                  double* tmp) {
+  if (kv->dtype == ORC_FP8REC) {
+    const uint8_t* rec = (const uint8_t*)kv->v +
+                         ((b * kv->Hkv + h) * kv->stride + t) * kv->record_bytes;
+    orc_decode_fp8_record(rec, kv->D - kv->n_rope, kv->n_rope, tmp);
+    for (int64_t d = 0; d < kv->Dv; ++d) {
+      out[d] = tmp[d];
+    }
+    return;
+  }
+  int64_t base = ((b * kv->Hkv + h) * kv->stride + t) * kv->Dv;
+  for (int64_t d = 0; d < kv->Dv; ++d) {
+    out[d] = load_elem(kv->v, base + d, kv->dtype);
+  }
+}
+
+/* One output row ([SA] Semantics; [IS] index_share_row):
+ *   s_j = scale * sum_d q_d k_{j,d}
+ *   s_j = softcap * tanh(s_j / softcap)            if softcap != 0
+ *   s_j = -inf  if masked[j]                         (causal / pad / not a key)
+ *   M = max_j s_j;  M == -inf  =>  y = 0
+ *   L = sum_j exp(s_j - M)  (+ exp(sink - M) if a sink logit is given)
+ *   y = sum_j exp(s_j - M) / L * v_j
+ * `keys` lists n candidate positions, `masked` flags the ones that take -inf.
+ */
+static void attend_row(const orc_kv* kv, int64_t b, int64_t kvh, const double* q,
+                       const int64_t* keys, const int* masked, int64_t n, double scale,
+                       double softcap, const double* sink, double* y) {
+  double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double* krow = (double*)malloc(sizeof(double) * (size_t)kv->D);
+  double* vrow = (double*)malloc(sizeof(double) * (size_t)kv->D);
+  double* tmp = (double*)malloc(sizeof(double) * (size_t)kv->D);
+  double M = -INFINITY;
+  for (int64_t j = 0; j < n; ++j) {
+    if (masked[j]) {
+      s[j] = -INFINITY;
+      continue;
+    }
+    get_k(kv, b, kvh, keys[j], krow);
+    double dot = 0.0;
+    for (int64_t d = 0; d < kv->D; ++d) {
+      dot += q[d] * krow[d];
+    }
+    double sj = scale * dot;
+    if (softcap != 0.0) {
+      sj = softcap * tanh(sj / softcap);
+    }
+    s[j] = sj;
+    if (sj > M) {
+      M = sj;
+    }
+  }
+  for (int64_t d = 0; d < kv->Dv; ++d) {
+    y[d] = 0.0;
+  }
+  if (M == -INFINITY) {
+    free(s);
+    free(krow);
+    free(vrow);
+    free(tmp);
+    return;
+  }
+  double L = 0.0;
+  for (int64_t j = 0; j < n; ++j) {
+    if (s[j] != -INFINITY) {
+      L += exp(s[j] - M);
+    }
+  }
+  if (sink) {
+    L += exp(*sink - M);
+  }
+  for (int64_t j = 0; j < n; ++j) {
+    if (s[j] == -INFINITY) {
+      continue;
+    }
+    double p = exp(s[j] - M) / L;
+    get_v(kv, b, kvh, keys[j], vrow, tmp);
+    for (int64_t d = 0; d < kv->Dv; ++d) {
+      y[d] += p * vrow[d];
+    }
+  }
+  free(s);
+  free(krow);
+  free(vrow);
+  free(tmp);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sparse selected-token decode ([IS] index_share_row; [CSA] window).        */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const void* q;        /* [B, Hq, Sq, D] in q_dtype */
+  int q_dtype;          /* f32 / f16 / bf16 */
+  const void* k;        /* dense: [B, Hkv, T, D]; FP8: records [B, Hkv, T, rb] */
+  const void* v;        /* dense: [B, Hkv, T, Dv]; FP8: same records as k */
+  int kv_dtype;         /* f32 / f16 / bf16 / FP8 record */
+  const void* idx;      /* [B, I, Sq, K] */
+  int idx_is_i64;
+  int64_t B, Hq, Hkv, Sq, D, Dv, T, I, K;
+  const int64_t* kv_len; /* nullable: per-batch valid length (pad frontier) */
+  int64_t past_len;     /* causal frontier offset: query i sees j <= past_len + i */
+  int causal;
+  double scale;
+  double softcap;
+  int64_t window;       /* 0, or W: the W positions before the valid length */
+  const double* sink;   /* nullable: per-query-head logit added to the denominator */
+  int64_t record_bytes; /* FP8 only */
+  int64_t n_rope;       /* FP8 only */
+} orc_sparse_args;
+
+/* Candidate set of one row:
+ *   the valid prefix of idx[b, ih, i, :] (take while != -1), and with a
+ *   window W additionally every t in [len_b - W, len_b), the selected entries
+ *   then being kept only below len_b - W so that each key counts once.
+ * A kept key is masked when causal and j > past_len + i, or when j >= len_b.
+ * Rows are flattened (b, h, i); `rows` selects which to compute (NULL: all),
+ * y gets one Dv-vector per computed row.  Returns 0, or -1 on a bad shape. */
+int orc_sparse_attention(const orc_sparse_args* a, const int64_t* rows, int64_t nrows,
+                         double* y) {
+  if (a->Hkv <= 0 || a->Hq % a->Hkv != 0) {
+    return -1;
+  }
+  if (!(a->I == 1 || a->I == a->Hkv || a->I == a->Hq)) {
+    return -1;
+  }
+  int64_t g = a->Hq / a->Hkv;
+  int64_t total = a->B * a->Hq * a->Sq;
+  int64_t count = rows ? nrows : total;
+  orc_kv kv = {a->k, a->v, a->kv_dtype, a->Hkv, a->T, a->D, a->Dv, a->record_bytes,
+               a->n_rope};
+  int64_t cap = a->K + a->window;
+  int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)(cap > 0 ? cap : 1));
+  int* masked = (int*)malloc(sizeof(int) * (size_t)(cap > 0 ? cap : 1));
+  double* q = (double*)malloc(sizeof(double) * (size_t)a->D);
+  for (int64_t r = 0; r < count; ++r) {
+    int64_t row = rows ? rows[r] : r;
+    int64_t i = row % a->Sq;
+    int64_t h = (row / a->Sq) % a->Hq;
+    int64_t b = row / (a->Sq * a->Hq);
+    int64_t kvh = h / g;
+    int64_t ih = (a->I == 1) ? 0 : (a->I == a->Hkv ? kvh : h);
+    int64_t len = a->kv_len ? a->kv_len[b] : a->T;
+    for (int64_t d = 0; d < a->D; ++d) {
+      q[d] = load_elem(a->q, ((b * a->Hq + h) * a->Sq + i) * a->D + d, a->q_dtype);
+    }
+    int64_t n = 0;
+    int64_t wstart = len - a->window;
+    if (a->window > 0) {
+      for (int64_t t = (wstart > 0 ? wstart : 0); t < len; ++t) {
+        keys[n++] = t;
+      }
+    }
+    const char* irow = (const char*)a->idx +
+                       (((b * a->I + ih) * a->Sq + i) * a->K) * (a->idx_is_i64 ? 8 : 4);
+    for (int64_t c = 0; c < a->K; ++c) {
+      int64_t j = load_index(irow, c, a->idx_is_i64);
+      if (j == -1) {
+        break;
+      }
+      if (a->window > 0 && j >= wstart) {
+        continue;
+      }
+      keys[n++] = j;
+    }
+    for (int64_t j = 0; j < n; ++j) {
+      int m = 0;
+      if (a->causal && keys[j] > a->past_len + i) {
+        m = 1;
+      }
+      if (keys[j] >= len || keys[j] < 0) {
+        m = 1;
+      }
+      masked[j] = m;
+    }
+    attend_row(&kv, b, kvh, q, keys, masked, n, a->scale, a->softcap,
+               a->sink ? &a->sink[h] : NULL, y + r * a->Dv);
+  }
+  free(keys);
+  free(masked);
+  free(q);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dense prefill ([SA] Semantics, attention_row), no past.                   */
+/* ------------------------------------------------------------------------ */
+
+/* Q [B, Hq, S, D], K/V [B, Hkv, S, D]; query i sees keys 0..i when causal,
+ * all S keys otherwise.  Rows flattened (b, h, i). */
+int orc_prefill(const void* q, const void* k, const void* v, int dtype, int64_t B,
+                int64_t Hq, int64_t Hkv, int64_t S, int64_t D, int causal, double scale,
+                double softcap, const int64_t* rows, int64_t nrows, double* y) {
+  if (Hkv <= 0 || Hq % Hkv != 0) {
+    return -1;
+  }
+  int64_t g = Hq / Hkv;
+  int64_t total = B * Hq * S;
+  int64_t count = rows ? nrows : total;
+  orc_kv kv = {k, v, dtype, Hkv, S, D, D, 0, 0};
+  int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)S);
+  int* masked = (int*)malloc(sizeof(int) * (size_t)S);
+  double* qr = (double*)malloc(sizeof(double) * (size_t)D);
+  for (int64_t r = 0; r < count; ++r) {
+    int64_t row = rows ? rows[r] : r;
+    int64_t i = row % S;
+    int64_t h = (row / S) % Hq;
+    int64_t b = row / (S * Hq);
+    for (int64_t d = 0; d < D; ++d) {
+      qr[d] = load_elem(q, ((b * Hq + h) * S + i) * D + d, dtype);
+    }
+    for (int64_t j = 0; j < S; ++j) {
+      keys[j] = j;
+      masked[j] = (causal && j > i) ? 1 : 0;
+    }
+    attend_row(&kv, b, h / g, qr, keys, masked, S, scale, softcap, NULL, y + r * D);
+  }
+  free(keys);
+  free(masked);
+  free(qr);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged causal decode ([PG] 16-token blocks through a table).               */
+/* ------------------------------------------------------------------------ */
+
+/* Pools [num_pages, Hkv, page_tokens, D]; token t of sequence b lives at
+ * page block_table[b * max_pages + t / page_tokens], slot t % page_tokens.
+ * The single new query of sequence b sits at position ctx_len[b] - 1 and
+ * sees all ctx_len[b] tokens.  Gathers the sequence's keys into a contiguous
+ * copy, then applies the dense formula.  Rows flattened (b, h). */
+int orc_paged_decode(const void* q, const void* k_pool, const void* v_pool, int dtype,
+                     const int32_t* block_table, const int32_t* ctx_len, int64_t B,
+                     int64_t Hq, int64_t Hkv, int64_t D, int64_t page_tokens,
+                     int64_t max_pages, double scale, const int64_t* rows, int64_t nrows,
+                     double* y) {
+  if (Hkv <= 0 || Hq % Hkv != 0) {
+    return -1;
+  }
+  int64_t g = Hq / Hkv;
+  int64_t total = B * Hq;
+  int64_t count = rows ? nrows : total;
+  size_t esz = dtype == ORC_F32 ? 4 : 2;
+  double* qr = (double*)malloc(sizeof(double) * (size_t)D);
+  for (int64_t r = 0; r < count; ++r) {
+    int64_t row = rows ? rows[r] : r;
+    int64_t h = row % Hq;
+    int64_t b = row / Hq;
+    int64_t kvh = h / g;
+    int64_t n = ctx_len[b];
+    /* contiguous copy of this (b, kvh)'s keys/values, as [1, 1, n, D] */
+    char* kc = (char*)malloc(esz * (size_t)(n * D > 0 ? n * D : 1));
+    char* vc = (char*)malloc(esz * (size_t)(n * D > 0 ? n * D : 1));
+    for (int64_t t = 0; t < n; ++t) {
+      int64_t page = block_table[b * max_pages + t / page_tokens];
+      int64_t slot = t % page_tokens;
+      size_t src = (size_t)(((page * Hkv + kvh) * page_tokens + slot) * D) * esz;
+      memcpy(kc + (size_t)(t * D) * esz, (const char*)k_pool + src, esz * (size_t)D);
+      memcpy(vc + (size_t)(t * D) * esz, (const char*)v_pool + src, esz * (size_t)D);
+    }
+    for (int64_t d = 0; d < D; ++d) {
+      qr[d] = load_elem(q, (b * Hq + h) * D + d, dtype);
+    }
+    orc_kv kv = {kc, vc, dtype, 1, n, D, D, 0, 0};
+    int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    int* masked = (int*)calloc((size_t)(n > 0 ? n : 1), sizeof(int));
+    for (int64_t t = 0; t < n; ++t) {
+      keys[t] = t;
+    }
+    attend_row(&kv, 0, 0, qr, keys, masked, n, scale, 0.0, NULL, y + r * D);
+    free(keys);
+    free(masked);
+    free(kc);
+    free(vc);
+  }
+  free(qr);
+  return 0;
+}

@@ -1,0 +1,346 @@
+"""Seeded synthetic inputs for the KV-cache attention hot path.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic. Both the oracle tests and the CUDA path take their
+inputs from here, so the two sides see identical bytes.
+
+Every generator is deterministic in ``seed``. Large tensors are drawn with a
+``torch.Generator`` on the requested device (so an 8 GB paged pool does not
+have to be produced on the host); small ones may be drawn on the CPU.
+
+Workload shapes follow the five decode/prefill cases of the problem statement:
+
+* ``tiny_sparse``      fp32 selected-token decode, B1 Hq4 Hkv1 D64, past 256 + 1
+* ``sparse_bf16``      bf16 selected-token decode, B32 Hq64 Hkv8 D128 T8192 K2048
+* ``csa_fp8``          FP8 block-64 latent cache, B16 Hq128 MQA D576, T65536,
+                       window 128 united with top-k 2048
+* ``prefill_bf16``     dense causal prefill, B4 S4096 Hq32 Hkv8 D128, softcap 50
+* ``paged_fp16``       paged causal decode, B128, ctx ~ U[1024, 32768], 16-token pages
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+import torch
+
+__all__ = [
+    "normal",
+    "sorted_sample_rows",
+    "pad_tails",
+    "quantize_fp8_block64_records",
+    "paged_layout",
+    "SparseCase",
+    "PrefillCase",
+    "PagedCase",
+    "tiny_sparse",
+    "sparse_bf16",
+    "csa_fp8",
+    "prefill_bf16",
+    "paged_fp16",
+    "make_sparse_inputs",
+    "make_prefill_inputs",
+    "make_paged_inputs",
+]
+
+_TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) & 0x7FFF_FFFF_FFFF_FFFF)
+    return g
+
+
+def normal(shape, dtype: str, seed: int, device="cpu") -> torch.Tensor:
+    """N(0, 1) values drawn in fp32 and rounded (RNE) to the storage dtype."""
+    g = _gen(seed, device)
+    x = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+    return x.to(_TORCH_DT[dtype])
+
+
+def sorted_sample_rows(rows: int, low: int, high: int, k: int, seed: int,
+                       device="cpu") -> torch.Tensor:
+    """``rows`` rows of ``k`` distinct integers drawn uniformly from
+    ``[low, high)`` without replacement, each row sorted ascending (int64)."""
+    n = high - low
+    if k > n:
+        raise ValueError(f"cannot draw {k} distinct values from a range of {n}")
+    g = _gen(seed, device)
+    out = torch.empty((rows, k), dtype=torch.int64, device=device)
+    # Random keys per candidate, keep the k smallest keys: a uniform k-subset.
+    step = max(1, (1 << 26) // max(n, 1))
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        keys = torch.rand((r1 - r0, n), generator=g, device=device)
+        pick = torch.topk(keys, k, dim=1, largest=False, sorted=False).indices
+        out[r0:r1] = torch.sort(pick, dim=1).values + low
+    return out
+
+
+def pad_tails(idx: torch.Tensor, seed: int, prob: float, max_pad: int,
+              min_pad: int = 1) -> torch.Tensor:
+    """Replace a seeded trailing run of each selected row by ``-1``.
+
+    A row is chosen with probability ``prob``; its pad count is uniform in
+    ``[min_pad, max_pad]`` (never the whole row). The largest indices are the
+    ones dropped, so the remaining prefix stays strictly increasing.
+    """
+    rows, k = idx.shape
+    rng = np.random.default_rng(seed)
+    chosen = rng.random(rows) < prob
+    counts = rng.integers(min_pad, max_pad + 1, size=rows)
+    counts = np.minimum(counts, k - 1)
+    out = idx.clone()
+    col = torch.arange(k, device=idx.device)
+    lim = torch.tensor(np.where(chosen, k - counts, k), device=idx.device)
+    out[col[None, :] >= lim[:, None]] = -1
+    return out
+
+
+def quantize_fp8_block64_records(nope: torch.Tensor, rope: torch.Tensor,
+                                 record_stride: int | None = None) -> torch.Tensor:
+    """Pack rows into hybrid FP8 records (test-data generation only).
+
+    ``nope`` is ``[..., n_nope]`` (n_nope a multiple of 64), ``rope`` is
+    ``[..., n_rope]`` bf16. Each record is ``n_nope/64`` blocks of
+    ``[E8M0 scale byte, 64 E4M3FN codes]`` followed by the RoPE dims as
+    little-endian bf16. The block exponent is the smallest ``e`` with
+    ``amax / 2**e <= 448`` (an all-zero block gets byte 127); codes are the
+    round-to-nearest-even E4M3FN encoding of ``x / 2**e``.
+    """
+    lead = nope.shape[:-1]
+    n_nope = nope.shape[-1]
+    n_rope = rope.shape[-1]
+    if n_nope % 64:
+        raise ValueError("non-RoPE width must be a multiple of 64")
+    nb = n_nope // 64
+    width = nb * 65 + 2 * n_rope
+    stride = width if record_stride is None else record_stride
+    if stride < width:
+        raise ValueError("record stride smaller than the record")
+    x = nope.to(torch.float32).reshape(-1, nb, 64)
+    amax = x.abs().amax(dim=2)
+    e = torch.zeros_like(amax, dtype=torch.int32)
+    nz = amax > 0
+    e[nz] = torch.ceil(torch.log2(amax[nz] / 448.0)).to(torch.int32)
+    # Correct for log2 rounding so that amax / 2**e <= 448 holds exactly.
+    for _ in range(2):
+        too_big = nz & (amax / torch.exp2(e.to(torch.float32)) > 448.0)
+        e = e + too_big.to(torch.int32)
+    e = torch.clamp(e, -127, 127)
+    scaled = x / torch.exp2(e.to(torch.float32))[:, :, None]
+    codes = scaled.to(torch.float8_e4m3fn).view(torch.uint8)
+    n = x.shape[0]
+    rec = torch.zeros((n, stride), dtype=torch.uint8, device=nope.device)
+    blocks = rec[:, : nb * 65].view(n, nb, 65)
+    blocks[:, :, 0] = (e + 127).to(torch.uint8)
+    blocks[:, :, 1:] = codes
+    rb = rope.to(torch.bfloat16).reshape(n, n_rope).contiguous().view(torch.int16)
+    rb = rb.to(torch.int32) & 0xFFFF
+    tail = rec[:, nb * 65: nb * 65 + 2 * n_rope].view(n, n_rope, 2)
+    tail[:, :, 0] = (rb & 0xFF).to(torch.uint8)
+    tail[:, :, 1] = (rb >> 8).to(torch.uint8)
+    return rec.reshape(*lead, stride)
+
+
+def paged_layout(B: int, ctx_low: int, ctx_high: int, page_tokens: int,
+                 seed: int, extra_pages: int = 0):
+    """Per-sequence context lengths ~ U[ctx_low, ctx_high] and a block table
+    that maps each sequence's logical pages onto a seeded random permutation
+    of one shared page pool. Returns ``(ctx_len i32 [B], block_table i32
+    [B, max_pages], num_pages)``; unused table slots hold ``-1``."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(ctx_low, ctx_high + 1, size=B).astype(np.int32)
+    pages = (ctx + page_tokens - 1) // page_tokens
+    max_pages = int(math.ceil(ctx_high / page_tokens))
+    num_pages = int(pages.sum()) + extra_pages
+    perm = rng.permutation(num_pages).astype(np.int32)
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    off = 0
+    for b in range(B):
+        table[b, : pages[b]] = perm[off: off + pages[b]]
+        off += pages[b]
+    return torch.from_numpy(ctx), torch.from_numpy(table), num_pages
+
+
+# --------------------------------------------------------------------------
+# Workload descriptions
+# --------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class SparseCase:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    T: int                 # cache length (past + current), also the row stride
+    K: int                 # selected-index width
+    I: int                 # index heads: 1, Hkv or Hq
+    dtype: str             # "f32", "f16", "bf16" or "fp8" (hybrid records)
+    pad_prob: float = 0.0  # probability that a row gets a -1 tail
+    pad_max: int = 0
+    pad_min: int = 1
+    window: int = 0        # dense window of recent tokens united with the top-k
+    n_rope: int = 0        # FP8 only: bf16 RoPE dims at the end of a record
+    record_stride: int = 0 # FP8 only: bytes between records (0 = packed)
+    softcap: float = 0.0
+    scale: float = 0.0     # 0 => 1/sqrt(D)
+    idx_i64: bool = False
+    cur: int = 1           # tokens appended this step
+
+    @property
+    def g(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.Hq
+
+    def eff_scale(self) -> float:
+        return self.scale if self.scale else 1.0 / math.sqrt(self.D)
+
+
+@dataclass(frozen=True)
+class PrefillCase:
+    name: str
+    B: int
+    S: int
+    Hq: int
+    Hkv: int
+    D: int
+    causal: bool = True
+    softcap: float = 0.0
+    scale: float = 0.0
+    dtype: str = "bf16"
+
+    def eff_scale(self) -> float:
+        return self.scale if self.scale else 1.0 / math.sqrt(self.D)
+
+
+@dataclass(frozen=True)
+class PagedCase:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    ctx_low: int
+    ctx_high: int
+    page_tokens: int = 16
+    dtype: str = "f16"
+    scale: float = 0.0
+
+    def eff_scale(self) -> float:
+        return self.scale if self.scale else 1.0 / math.sqrt(self.D)
+
+
+def tiny_sparse(**kw) -> SparseCase:
+    """fp32, B1 Hq4 Hkv1 D64, past 256 + 1 current, per-head rows of 32
+    indices from [0, 257) with 0..8 trailing -1 pads, scale 1/8."""
+    base = SparseCase("tiny_sparse_f32", B=1, Hq=4, Hkv=1, D=64, T=257, K=32, I=4,
+                      dtype="f32", pad_prob=1.0, pad_max=8, pad_min=0, scale=0.125)
+    return replace(base, **kw)
+
+
+def sparse_bf16(**kw) -> SparseCase:
+    """bf16, B32 Hq64 Hkv8 D128, cache 8192 (8191 past + 1 current), 2048
+    indices per (batch, KV head) row, about 5% rows padded."""
+    base = SparseCase("sparse_bf16_b32_h64_kv8_d128_t8192_k2048", B=32, Hq=64, Hkv=8,
+                      D=128, T=8192, K=2048, I=8, dtype="bf16", pad_prob=0.05,
+                      pad_max=256)
+    return replace(base, **kw)
+
+
+def csa_fp8(**kw) -> SparseCase:
+    """FP8 hybrid latent cache, B16 Hq128 over one latent head, 512 E4M3
+    dims + 64 bf16 RoPE dims (648-byte records), T 65536, window 128 united
+    with 2048 sorted uniform indices, scale 1/sqrt(576)."""
+    base = SparseCase("csa_fp8_b16_h128_d576_t65536_k2048_w128", B=16, Hq=128, Hkv=1,
+                      D=576, T=65536, K=2048, I=1, dtype="fp8", window=128, n_rope=64,
+                      record_stride=648)
+    return replace(base, **kw)
+
+
+def prefill_bf16(**kw) -> PrefillCase:
+    base = PrefillCase("prefill_bf16_b4_s4096_h32_kv8_d128_causal_softcap50", B=4, S=4096,
+                       Hq=32, Hkv=8, D=128, causal=True, softcap=50.0)
+    return replace(base, **kw)
+
+
+def paged_fp16(**kw) -> PagedCase:
+    base = PagedCase("paged_fp16_b128_h32_kv8_d128_ctx1k-32k_p16", B=128, Hq=32, Hkv=8,
+                     D=128, ctx_low=1024, ctx_high=32768)
+    return replace(base, **kw)
+
+
+# --------------------------------------------------------------------------
+# Input builders
+# --------------------------------------------------------------------------
+
+def make_sparse_inputs(c: SparseCase, seed: int, device="cpu") -> dict:
+    """Q ``[B,Hq,1,D]``, a KV cache of ``T`` positions whose last ``cur`` are
+    the current token(s) (also returned separately as ``k_cur``/``v_cur``), and
+    ``selected_indices`` ``[B, I, 1, K]``.
+
+    For the FP8 case the cache is ``[B, 1, T, record_stride]`` bytes (K and V
+    are the same latent record) and Q is bf16."""
+    out = {}
+    qdt = "bf16" if c.dtype == "fp8" else c.dtype
+    out["q"] = normal((c.B, c.Hq, 1, c.D), qdt, seed * 7919 + 1, device)
+    if c.dtype == "fp8":
+        n_nope = c.D - c.n_rope
+        stride = c.record_stride or (n_nope // 64 * 65 + 2 * c.n_rope)
+        nope = normal((c.B, c.T, n_nope), "f32", seed * 7919 + 2, device)
+        rope = normal((c.B, c.T, c.n_rope), "bf16", seed * 7919 + 3, device)
+        rec = quantize_fp8_block64_records(nope, rope, stride)
+        out["kv_records"] = rec.reshape(c.B, 1, c.T, stride)
+    else:
+        out["k_cache"] = normal((c.B, c.Hkv, c.T, c.D), c.dtype, seed * 7919 + 2, device)
+        out["v_cache"] = normal((c.B, c.Hkv, c.T, c.D), c.dtype, seed * 7919 + 3, device)
+        out["k_cur"] = out["k_cache"][:, :, c.T - c.cur:, :].clone()
+        out["v_cur"] = out["v_cache"][:, :, c.T - c.cur:, :].clone()
+    rows = c.B * c.I
+    if c.window:
+        high = c.T - c.window
+    else:
+        high = c.T
+    idx = sorted_sample_rows(rows, 0, high, c.K, seed * 7919 + 4, device)
+    if c.pad_prob > 0 and c.pad_max > 0:
+        idx = pad_tails(idx, seed * 7919 + 5, c.pad_prob, c.pad_max, c.pad_min)
+    idx = idx.reshape(c.B, c.I, 1, c.K)
+    out["idx"] = idx if c.idx_i64 else idx.to(torch.int32)
+    return out
+
+
+def make_prefill_inputs(c: PrefillCase, seed: int, device="cpu") -> dict:
+    return {
+        "q": normal((c.B, c.Hq, c.S, c.D), c.dtype, seed * 104729 + 1, device),
+        "k": normal((c.B, c.Hkv, c.S, c.D), c.dtype, seed * 104729 + 2, device),
+        "v": normal((c.B, c.Hkv, c.S, c.D), c.dtype, seed * 104729 + 3, device),
+    }
+
+
+def make_paged_inputs(c: PagedCase, seed: int, device="cpu") -> dict:
+    """Pools ``[num_pages, Hkv, page_tokens, D]``; ``ctx_len`` counts the new
+    token, whose K/V (``k_new``/``v_new`` ``[B, Hkv, D]``) also sit in the
+    pool at slot ``ctx - 1``."""
+    ctx, table, num_pages = paged_layout(c.B, c.ctx_low, c.ctx_high, c.page_tokens,
+                                         seed * 15485863 + 1)
+    shape = (num_pages, c.Hkv, c.page_tokens, c.D)
+    k_pool = normal(shape, c.dtype, seed * 15485863 + 2, device)
+    v_pool = normal(shape, c.dtype, seed * 15485863 + 3, device)
+    ctx_d = ctx.to(device)
+    table_d = table.to(device)
+    last = (ctx_d - 1).long()
+    page = table_d.long().gather(1, (last // c.page_tokens)[:, None])[:, 0]
+    slot = last % c.page_tokens
+    k_new = k_pool[page, :, slot, :].clone()
+    v_new = v_pool[page, :, slot, :].clone()
+    return {
+        "q": normal((c.B, c.Hq, 1, c.D), c.dtype, seed * 15485863 + 4, device),
+        "k_pool": k_pool, "v_pool": v_pool, "k_new": k_new, "v_new": v_new,
+        "ctx_len": ctx_d, "block_table": table_d, "num_pages": num_pages,
+    }
