@@ -1,0 +1,250 @@
+/*
+ * sa.h -- C ABI of the GB300 KV-cache attention library (libsa.so).
+ *
+ * Five operations, all computed on the GPU on the caller's stream:
+ *
+ *   validate_indices     index-row validation with a device error word
+ *   build_present_kv     present K/V = past ++ current (concat or in-place append)
+ *   sparse_attn_decode   selected-token attention (dense or FP8 hybrid cache)
+ *   attn_prefill         dense (causal) prefill with softcap, present K/V out
+ *   paged_attn_decode    causal decode over a 16-token page table
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *    library never allocates, frees or synchronises; scratch comes from a
+ *    caller-provided workspace whose size is given by the matching
+ *    *_workspace() query.  Tensors are dense and row-major in the stated
+ *    shape (no strides other than the stated capacity strides).
+ *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *    stream.  All work is enqueued on it; the calls return before it runs.
+ *  - Host-side argument errors return a negative status before anything is
+ *    enqueued.  Data-dependent problems (malformed index rows, out-of-range
+ *    page table entries or write positions) never fail the call: they OR bits
+ *    into a caller-zeroed device word `err_word` (read it after your own
+ *    synchronisation), and the kernels keep every load in bounds.
+ *  - The calls are stateless and thread-safe.  No kernel spins or traps.
+ *
+ * Sources of the semantics (page title, section):
+ *  [IS]  onnx-runtime-ep-cuda src/kernels/index_share.rs (IndexShare):
+ *        module docs, validate_indices, build_present, index_share_row.
+ *  [SA]  onnx-runtime-ep-cuda src/kernels/standard_attention.rs (ONNX
+ *        Attention): module docs "Semantics", build_kv, attention_row,
+ *        attention_split / attention_combine (FlashDecoding split-KV).
+ *  [CSA] onnx-runtime-ep-cpu src/kernels/compressed_sparse_attention.rs:
+ *        CacheFormat (hybrid FP8 record), dequantize_cache; onnx-runtime-ep-cuda
+ *        compressed_sparse_attention.rs, csa_ratio128_sink_attention.
+ *  [PG]  ferrum-kernels vnext_ops/transformer/causal_attention.rs: paged KV
+ *        blocks of 16 tokens addressed through a table.
+ */
+#ifndef SA_H
+#define SA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (return values) ------------------------------------ */
+#define SA_OK 0
+#define SA_ERR_NULL (-1)        /* a required pointer is NULL                 */
+#define SA_ERR_SHAPE (-2)       /* a size is non-positive or inconsistent     */
+#define SA_ERR_DTYPE (-3)       /* unsupported dtype or dtype combination     */
+#define SA_ERR_ALIGN (-4)       /* a pointer is not 16-byte aligned           */
+#define SA_ERR_WORKSPACE (-5)   /* workspace missing or too small             */
+#define SA_ERR_OVERLAP (-6)     /* an output overlaps an input illegally      */
+#define SA_ERR_UNSUPPORTED (-7) /* valid request this build does not serve    */
+#define SA_ERR_LAUNCH (-8)      /* the CUDA runtime refused a launch          */
+
+/* ---- storage dtypes --------------------------------------------------- */
+#define SA_F32 0
+#define SA_F16 1
+#define SA_BF16 2
+#define SA_FP8_E4M3_B64 3 /* hybrid record: blocks of [E8M0, 64 x E4M3FN] + bf16 tail */
+
+/* ---- index-row status codes (row_status bytes; OR-ed into err_word) --- */
+#define SA_IDX_BELOW_SENTINEL 1  /* a value below -1                          */
+#define SA_IDX_AFTER_PADDING 2   /* a non -1 value after a -1                 */
+#define SA_IDX_OUT_OF_RANGE 4    /* a value >= the row's bound                */
+#define SA_IDX_NOT_INCREASING 8  /* a value smaller than its predecessor      */
+#define SA_IDX_DUPLICATE 16      /* a value equal to its predecessor          */
+#define SA_IDX_ALL_PADDING 32    /* the row holds only -1                     */
+/* other err_word bits */
+#define SA_ERRBIT_WRITE_POS 64   /* build_present_kv: write_pos[b] out of range */
+#define SA_ERRBIT_PAGE 128       /* paged: ctx_len or block-table entry invalid */
+#define SA_ERRBIT_TIMEOUT 256    /* a kernel's bounded wait for a copy ran out  */
+
+/* Human-readable name of a status code (static string). */
+const char* sa_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int sa_version(void);
+
+/*
+ * validate_indices -- [IS] validate_indices / validate_index_rows.
+ *
+ * idx: [B, I, Sq, K] int32 (idx_is_i64 = 0) or int64 (idx_is_i64 = 1).
+ * Each row is scanned left to right: -1 marks padding; any other value is
+ * checked, in this order, for being below -1, following padding, being
+ * >= bound, equal to its predecessor, smaller than it.  The first failing
+ * column decides the row's code; a row of only -1 is SA_IDX_ALL_PADDING.
+ * bound_per_batch: nullable device int64 [B]; when NULL every row is bounded
+ * by `bound`.
+ * row_status: nullable device uint8 [B*I*Sq], written with each row's code
+ * (0 = valid).  err_word: device uint32, OR-ed with every row's code (the
+ * caller zeroes it).  Bit-exact with the definition.
+ */
+int validate_indices(const void* idx, int idx_is_i64, int64_t B, int64_t I, int64_t Sq,
+                     int64_t K, const int64_t* bound_per_batch, int64_t bound,
+                     uint8_t* row_status, uint32_t* err_word, void* stream);
+
+/*
+ * build_present_kv -- [IS] build_present, [SA] build_kv.  A pure copy
+ * (bit-exact), for K and (optionally) V in one launch.
+ *
+ * Concat mode (write_pos == NULL):
+ *   present[b,h,t,:] = past[b,h,t,:]      for t <  P   (past is [B,H,P,D])
+ *                    = cur[b,h,t-P,:]     for P <= t < P+C (cur is [B,H,C,D])
+ *   present is [B, H, present_stride, D] with present_stride >= P + C;
+ *   positions >= P + C are not written.  past may be NULL only when P == 0.
+ *   present must not overlap past or cur (SA_ERR_OVERLAP).
+ * Append mode (write_pos != NULL, device int64 [B]):
+ *   present is a capacity cache [B, H, present_stride, D]; cur[b,h,c,:] is
+ *   written at position write_pos[b] + c.  past must be NULL or equal to
+ *   present (in place: nothing else moves); another past [B,H,present_stride,D]
+ *   is first copied whole.  A write_pos outside [0, present_stride - C] skips
+ *   that batch and sets SA_ERRBIT_WRITE_POS in err_word (nullable).
+ * past_v/cur_v/present_v: the same for V; present_v NULL means K only.
+ * dtype: SA_F32, SA_F16 or SA_BF16 (any 2/4-byte element copies exactly).
+ */
+int build_present_kv(const void* past_k, const void* cur_k, void* present_k,
+                     const void* past_v, const void* cur_v, void* present_v, int dtype,
+                     int64_t B, int64_t H, int64_t P, int64_t C, int64_t D,
+                     int64_t present_stride, const int64_t* write_pos, uint32_t* err_word,
+                     void* stream);
+
+/*
+ * Selected-token attention -- [IS] index_share_row (semantics), [SA]
+ * Semantics + attention_split/attention_combine (split-KV, fixed-order
+ * combine), [CSA] dense window + FP8 records + sink.
+ *
+ * For every output row (b, h, i) with kvh = h / (Hq/Hkv) and index head
+ * ih = 0 (I == 1), kvh (I == Hkv) or h (I == Hq):
+ *   C = valid prefix of idx[b, ih, i, :] (entries before the first -1);
+ *   with window W > 0: C = [len_b - W, len_b) united with {j in C : j < len_b - W};
+ *   s_j = scale * q . k_j;  s_j = softcap * tanh(s_j / softcap) if softcap != 0;
+ *   s_j = -inf when j >= len_b (len_b = kv_len[b], or T), or causal and
+ *         j > past_len + i;
+ *   y = sum_j softmax(s)_j v_j, with exp(sink[h] - max) added to the
+ *   denominator when sink != NULL; a row whose scores are all -inf gives 0.
+ * Layouts:
+ *   q  [B, Hq, Sq, D] in q_dtype (F32, F16, BF16);  y [B, Hq, Sq, Dv] same dtype.
+ *   dense cache (kv_dtype == q_dtype): k_cache [B, Hkv, T, D], v_cache [B, Hkv, T, Dv].
+ *   FP8 cache (kv_dtype SA_FP8_E4M3_B64, q_dtype BF16): k_cache is
+ *     [B, Hkv, T, record_stride] bytes, each record (D - n_rope)/64 blocks of
+ *     [E8M0 scale, 64 E4M3FN codes] then n_rope little-endian bf16 values;
+ *     V is the same decoded record (its first Dv dims); v_cache is ignored.
+ *   idx [B, I, Sq, K] int32 or int64.  kv_len: nullable device int64 [B].
+ *   sink: nullable device float [Hq] (natural-log logits).
+ * scale: 0 means 1/sqrt(D).  Index rows are validated on the device against
+ * len_b when err_word != NULL (row_status nullable, as in validate_indices);
+ * malformed rows never fault: negative entries are skipped and entries
+ * >= len_b are masked.
+ * Workspace: sparse_attn_decode_workspace(p) bytes, 256-byte aligned.
+ */
+typedef struct {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const void* idx;
+  const float* sink;
+  void* y;
+  int32_t q_dtype;
+  int32_t kv_dtype;
+  int32_t idx_is_i64;
+  int32_t causal;
+  int64_t B, Hq, Hkv, Sq, D, Dv, T, I, K;
+  const int64_t* kv_len;
+  int64_t past_len;
+  float scale;
+  float softcap;
+  int64_t window;
+  int64_t record_stride;
+  int64_t n_rope;
+  uint32_t* err_word;
+  uint8_t* row_status;
+  void* workspace;
+  size_t workspace_bytes;
+} sa_sparse_params;
+
+size_t sparse_attn_decode_workspace(const sa_sparse_params* p);
+int sparse_attn_decode(const sa_sparse_params* p, void* stream);
+
+/*
+ * attn_prefill -- [SA] Semantics with no past: q [B, Hq, S, D],
+ * k/v [B, Hkv, S, D] (GQA, Hq % Hkv == 0), y [B, Hq, S, D]; query i sees
+ * keys 0..i when causal; softcap as above, applied before the mask; fp32
+ * softmax.  present_k / present_v (nullable, [B, Hkv, S, D]) receive exact
+ * copies of k / v (past ++ current with an empty past).  dtype: SA_BF16 or
+ * SA_F16 (tensor-core path, D == 128), or SA_F32 (reference-speed path).
+ */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* y;
+  void* present_k;
+  void* present_v;
+  int32_t dtype;
+  int32_t causal;
+  int64_t B, Hq, Hkv, S, D;
+  float scale;
+  float softcap;
+  void* workspace;
+  size_t workspace_bytes;
+} sa_prefill_params;
+
+size_t attn_prefill_workspace(const sa_prefill_params* p);
+int attn_prefill(const sa_prefill_params* p, void* stream);
+
+/*
+ * paged_attn_decode -- [PG] paged causal decode.  One new query per
+ * sequence: q [B, Hq, D], y [B, Hq, D].  Pools k_pool / v_pool are
+ * [num_pages, Hkv, page_tokens, D]; token t of sequence b lives at page
+ * block_table[b * max_pages + t / page_tokens], slot t % page_tokens.
+ * ctx_len[b] (device int32) counts the new token, which attends to all
+ * ctx_len[b] tokens.  If k_new / v_new ([B, Hkv, D]) are given they are first
+ * written into the pool at token ctx_len[b] - 1.  A ctx_len outside
+ * [1, max_pages*page_tokens] or a table entry outside [0, num_pages) sets
+ * SA_ERRBIT_PAGE (err_word nullable) and is never dereferenced.
+ * dtype SA_F16 / SA_BF16 / SA_F32; scale 0 means 1/sqrt(D).
+ */
+typedef struct {
+  const void* q;
+  void* k_pool;
+  void* v_pool;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* block_table;
+  const int32_t* ctx_len;
+  void* y;
+  int32_t dtype;
+  int32_t pad_;
+  int64_t B, Hq, Hkv, D, page_tokens, max_pages, num_pages;
+  float scale;
+  float pad2_;
+  uint32_t* err_word;
+  void* workspace;
+  size_t workspace_bytes;
+} sa_paged_params;
+
+size_t paged_attn_decode_workspace(const sa_paged_params* p);
+int paged_attn_decode(const sa_paged_params* p, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_H */

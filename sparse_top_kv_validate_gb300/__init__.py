@@ -1,0 +1,384 @@
+"""GB300 KV-cache attention library: Python binding of ``libsa.so``.
+
+This module only marshals arguments: it turns torch CUDA tensors into the
+device pointers and sizes of the C ABI declared in ``include/sa.h`` and
+passes torch's current stream.  Every step of the computation runs in the
+library's CUDA kernels; if ``libsa.so`` is missing the calls raise instead of
+falling back to anything else.
+
+Entry points (same names as the C ABI):
+    validate_indices, build_present_kv, sparse_attn_decode, attn_prefill,
+    paged_attn_decode
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "load", "lib_path", "SAError", "status_string",
+    "validate_indices", "build_present_kv", "sparse_attn_decode", "attn_prefill",
+    "paged_attn_decode", "sparse_attn_decode_workspace", "attn_prefill_workspace",
+    "paged_attn_decode_workspace",
+    "F32", "F16", "BF16", "FP8_E4M3_B64",
+    "IDX_BELOW_SENTINEL", "IDX_AFTER_PADDING", "IDX_OUT_OF_RANGE", "IDX_NOT_INCREASING",
+    "IDX_DUPLICATE", "IDX_ALL_PADDING", "ERRBIT_WRITE_POS", "ERRBIT_PAGE", "ERRBIT_TIMEOUT",
+    "SparseParams", "PrefillParams", "PagedParams",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = os.path.join(_HERE, "_build", "libsa.so")
+
+F32, F16, BF16, FP8_E4M3_B64 = 0, 1, 2, 3
+IDX_BELOW_SENTINEL, IDX_AFTER_PADDING, IDX_OUT_OF_RANGE = 1, 2, 4
+IDX_NOT_INCREASING, IDX_DUPLICATE, IDX_ALL_PADDING = 8, 16, 32
+ERRBIT_WRITE_POS, ERRBIT_PAGE, ERRBIT_TIMEOUT = 64, 128, 256
+
+_p = C.c_void_p
+_i64 = C.c_int64
+_i32 = C.c_int32
+
+
+class SparseParams(C.Structure):
+    _fields_ = [
+        ("q", _p), ("k_cache", _p), ("v_cache", _p), ("idx", _p), ("sink", _p), ("y", _p),
+        ("q_dtype", _i32), ("kv_dtype", _i32), ("idx_is_i64", _i32), ("causal", _i32),
+        ("B", _i64), ("Hq", _i64), ("Hkv", _i64), ("Sq", _i64), ("D", _i64), ("Dv", _i64),
+        ("T", _i64), ("I", _i64), ("K", _i64),
+        ("kv_len", _p), ("past_len", _i64),
+        ("scale", C.c_float), ("softcap", C.c_float),
+        ("window", _i64), ("record_stride", _i64), ("n_rope", _i64),
+        ("err_word", _p), ("row_status", _p), ("workspace", _p), ("workspace_bytes", C.c_size_t),
+    ]
+
+
+class PrefillParams(C.Structure):
+    _fields_ = [
+        ("q", _p), ("k", _p), ("v", _p), ("y", _p), ("present_k", _p), ("present_v", _p),
+        ("dtype", _i32), ("causal", _i32),
+        ("B", _i64), ("Hq", _i64), ("Hkv", _i64), ("S", _i64), ("D", _i64),
+        ("scale", C.c_float), ("softcap", C.c_float),
+        ("workspace", _p), ("workspace_bytes", C.c_size_t),
+    ]
+
+
+class PagedParams(C.Structure):
+    _fields_ = [
+        ("q", _p), ("k_pool", _p), ("v_pool", _p), ("k_new", _p), ("v_new", _p),
+        ("block_table", _p), ("ctx_len", _p), ("y", _p),
+        ("dtype", _i32), ("pad_", _i32),
+        ("B", _i64), ("Hq", _i64), ("Hkv", _i64), ("D", _i64), ("page_tokens", _i64),
+        ("max_pages", _i64), ("num_pages", _i64),
+        ("scale", C.c_float), ("pad2_", C.c_float),
+        ("err_word", _p), ("workspace", _p), ("workspace_bytes", C.c_size_t),
+    ]
+
+
+class SAError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _LIB
+
+
+def load():
+    """Load ``libsa.so`` (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB):
+            raise RuntimeError(
+                f"{_LIB} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = C.CDLL(_LIB)
+        L.sa_status_string.restype = C.c_char_p
+        L.sa_status_string.argtypes = [C.c_int]
+        L.sa_version.restype = C.c_int
+        L.sa_version.argtypes = []
+        L.validate_indices.restype = C.c_int
+        L.validate_indices.argtypes = [_p, C.c_int, _i64, _i64, _i64, _i64, _p, _i64, _p, _p, _p]
+        L.build_present_kv.restype = C.c_int
+        L.build_present_kv.argtypes = [_p, _p, _p, _p, _p, _p, C.c_int, _i64, _i64, _i64, _i64,
+                                       _i64, _i64, _p, _p, _p]
+        L.sparse_attn_decode_workspace.restype = C.c_size_t
+        L.sparse_attn_decode_workspace.argtypes = [C.POINTER(SparseParams)]
+        L.sparse_attn_decode.restype = C.c_int
+        L.sparse_attn_decode.argtypes = [C.POINTER(SparseParams), _p]
+        L.attn_prefill_workspace.restype = C.c_size_t
+        L.attn_prefill_workspace.argtypes = [C.POINTER(PrefillParams)]
+        L.attn_prefill.restype = C.c_int
+        L.attn_prefill.argtypes = [C.POINTER(PrefillParams), _p]
+        L.paged_attn_decode_workspace.restype = C.c_size_t
+        L.paged_attn_decode_workspace.argtypes = [C.POINTER(PagedParams)]
+        L.paged_attn_decode.restype = C.c_int
+        L.paged_attn_decode.argtypes = [C.POINTER(PagedParams), _p]
+        _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return load().sa_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+_DT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _dev(t, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(call, rc):
+    if rc != 0:
+        raise SAError(call, rc)
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes: int, device, workspace=None):
+    """Caller-owned scratch: the given tensor, or a cached torch allocation."""
+    if nbytes == 0:
+        return None, 0
+    if workspace is not None:
+        return workspace, workspace.numel() * workspace.element_size()
+    key = (device, torch.cuda.current_stream(device).cuda_stream)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf, buf.numel()
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def validate_indices(idx: torch.Tensor, bound: int = 0, bound_per_batch=None, *,
+                     row_status: torch.Tensor | None = None,
+                     err_word: torch.Tensor | None = None, stream=None):
+    """Validate ``idx`` ``[B, I, Sq, K]`` (int32/int64) on the device.
+
+    Returns ``(row_status uint8 [B*I*Sq], err_word uint32 [1])`` device tensors;
+    ``err_word`` is zeroed here unless passed in."""
+    L = load()
+    _dev(idx, "idx")
+    B, I, Sq, K = idx.shape
+    if row_status is None:
+        row_status = torch.empty(B * I * Sq, dtype=torch.uint8, device=idx.device)
+    if err_word is None:
+        err_word = torch.zeros(1, dtype=torch.int32, device=idx.device)
+    bb = _dev(bound_per_batch, "bound_per_batch")
+    rc = L.validate_indices(idx.data_ptr(), int(idx.dtype == torch.int64), B, I, Sq, K, _ptr(bb),
+                            int(bound), _ptr(row_status), err_word.data_ptr(), _stream(stream))
+    _check("validate_indices", rc)
+    return row_status, err_word
+
+
+def build_present_kv(cur_k, present_k, past_k=None, cur_v=None, present_v=None, past_v=None, *,
+                     write_pos=None, err_word=None, stream=None):
+    """Present K/V: concat (``write_pos`` None: present = past ++ cur along the
+    sequence axis, present ``[B,H,stride,D]``) or append (cur written at
+    ``write_pos[b]`` of the capacity cache ``present``)."""
+    L = load()
+    for n, t in (("cur_k", cur_k), ("present_k", present_k), ("past_k", past_k), ("cur_v", cur_v),
+                 ("present_v", present_v), ("past_v", past_v), ("write_pos", write_pos),
+                 ("err_word", err_word)):
+        _dev(t, n)
+    B, H, Cn, D = cur_k.shape
+    P = 0 if (past_k is None or write_pos is not None) else past_k.shape[2]
+    rc = L.build_present_kv(_ptr(past_k), cur_k.data_ptr(), present_k.data_ptr(), _ptr(past_v),
+                            _ptr(cur_v), _ptr(present_v), _dt(cur_k), B, H, P, Cn, D,
+                            present_k.shape[2], _ptr(write_pos), _ptr(err_word), _stream(stream))
+    _check("build_present_kv", rc)
+    return present_k, present_v
+
+
+def _sparse_params(q, k_cache, v_cache, idx, y, *, scale, softcap, window, kv_len, past_len,
+                   causal, sink, err_word, row_status, n_rope=0, Dv=None):
+    p = SparseParams()
+    B, Hq, Sq, D = q.shape
+    p.q, p.y = q.data_ptr(), _ptr(y)
+    p.q_dtype = _dt(q)
+    if k_cache.dtype == torch.uint8:
+        p.k_cache = k_cache.data_ptr()
+        p.v_cache = None
+        p.kv_dtype = FP8_E4M3_B64
+        p.record_stride = k_cache.shape[3]
+        p.n_rope = n_rope
+        p.Dv = D if Dv is None else Dv
+    else:
+        p.k_cache, p.v_cache = k_cache.data_ptr(), _ptr(v_cache)
+        p.kv_dtype = _dt(k_cache)
+        p.Dv = v_cache.shape[3]
+    p.Hkv, p.T = k_cache.shape[1], k_cache.shape[2]
+    if idx is not None:
+        p.idx = idx.data_ptr()
+        p.idx_is_i64 = int(idx.dtype == torch.int64)
+        p.I, p.K = idx.shape[1], idx.shape[3]
+    else:
+        p.idx, p.I, p.K = None, 1, 0
+    p.B, p.Hq, p.Sq, p.D = B, Hq, Sq, D
+    p.sink = _ptr(sink)
+    p.kv_len = _ptr(kv_len)
+    p.past_len = int(past_len)
+    p.causal = int(bool(causal))
+    p.scale = float(scale)
+    p.softcap = float(softcap)
+    p.window = int(window)
+    p.err_word = _ptr(err_word)
+    p.row_status = _ptr(row_status)
+    return p
+
+
+def sparse_attn_decode_workspace(q, k_cache, v_cache, idx, **kw) -> int:
+    p = _sparse_params(q, k_cache, v_cache, idx, None, **_sparse_defaults(kw))
+    return int(load().sparse_attn_decode_workspace(C.byref(p)))
+
+
+def _sparse_defaults(kw):
+    d = dict(scale=0.0, softcap=0.0, window=0, kv_len=None, past_len=0, causal=False, sink=None,
+             err_word=None, row_status=None, n_rope=0, Dv=None)
+    d.update(kw)
+    return d
+
+
+def sparse_attn_decode(q, k_cache, v_cache, idx, *, y=None, workspace=None, stream=None, **kw):
+    """Selected-token attention.  ``q [B,Hq,Sq,D]``; dense cache
+    ``k_cache/v_cache [B,Hkv,T,D]`` (same dtype as q) or FP8 hybrid records
+    ``k_cache uint8 [B,Hkv,T,record_stride]`` (``v_cache`` None, pass
+    ``n_rope``); ``idx [B,I,Sq,K]`` int32/int64.  Keyword options: scale,
+    softcap, window, kv_len (int64 [B]), past_len, causal, sink (float32
+    [Hq]), err_word (int32 [1], caller-zeroed), row_status (uint8 [B*I*Sq]),
+    n_rope, Dv.  Returns ``y [B,Hq,Sq,Dv]``."""
+    L = load()
+    kw = _sparse_defaults(kw)
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("idx", idx),
+                 ("kv_len", kw["kv_len"]), ("sink", kw["sink"]), ("err_word", kw["err_word"]),
+                 ("row_status", kw["row_status"])):
+        _dev(t, n)
+    B, Hq, Sq, D = q.shape
+    Dv = kw["Dv"] if k_cache.dtype == torch.uint8 else v_cache.shape[3]
+    if Dv is None:
+        Dv = D
+    if y is None:
+        y = torch.empty((B, Hq, Sq, Dv), dtype=q.dtype, device=q.device)
+    p = _sparse_params(q, k_cache, v_cache, idx, y, **kw)
+    need = int(L.sparse_attn_decode_workspace(C.byref(p)))
+    ws, nb = _workspace(need, q.device, workspace)
+    p.workspace, p.workspace_bytes = _ptr(ws), nb
+    _check("sparse_attn_decode", L.sparse_attn_decode(C.byref(p), _stream(stream)))
+    return y
+
+
+def _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap):
+    p = PrefillParams()
+    B, Hq, S, D = q.shape
+    p.q, p.k, p.v, p.y = q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(y)
+    p.present_k, p.present_v = _ptr(present_k), _ptr(present_v)
+    p.dtype, p.causal = _dt(q), int(bool(causal))
+    p.B, p.Hq, p.Hkv, p.S, p.D = B, Hq, k.shape[1], S, D
+    p.scale, p.softcap = float(scale), float(softcap)
+    return p
+
+
+def attn_prefill_workspace(q, k, v, causal=True, scale=0.0, softcap=0.0) -> int:
+    p = _prefill_params(q, k, v, None, None, None, causal, scale, softcap)
+    return int(load().attn_prefill_workspace(C.byref(p)))
+
+
+def attn_prefill(q, k, v, *, causal=True, scale=0.0, softcap=0.0, y=None, present_k=None,
+                 present_v=None, workspace=None, stream=None):
+    """Dense prefill, ``q [B,Hq,S,D]``, ``k/v [B,Hkv,S,D]``; optional exact
+    present K/V copies.  Returns ``y``."""
+    L = load()
+    for n, t in (("q", q), ("k", k), ("v", v), ("present_k", present_k),
+                 ("present_v", present_v)):
+        _dev(t, n)
+    if y is None:
+        y = torch.empty_like(q)
+    p = _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap)
+    need = int(L.attn_prefill_workspace(C.byref(p)))
+    ws, nb = _workspace(need, q.device, workspace)
+    p.workspace, p.workspace_bytes = _ptr(ws), nb
+    _check("attn_prefill", L.attn_prefill(C.byref(p), _stream(stream)))
+    return y
+
+
+def _paged_params(q, k_pool, v_pool, block_table, ctx_len, y, k_new, v_new, scale, err_word):
+    p = PagedParams()
+    B, Hq = q.shape[0], q.shape[1]
+    D = q.shape[-1]
+    p.q, p.k_pool, p.v_pool = q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr()
+    p.k_new, p.v_new = _ptr(k_new), _ptr(v_new)
+    p.block_table, p.ctx_len, p.y = block_table.data_ptr(), ctx_len.data_ptr(), _ptr(y)
+    p.dtype = _dt(q)
+    p.B, p.Hq, p.Hkv, p.D = B, Hq, k_pool.shape[1], D
+    p.page_tokens, p.max_pages, p.num_pages = k_pool.shape[2], block_table.shape[1], k_pool.shape[0]
+    p.scale = float(scale)
+    p.err_word = _ptr(err_word)
+    return p
+
+
+def paged_attn_decode_workspace(q, k_pool, v_pool, block_table, ctx_len, scale=0.0) -> int:
+    p = _paged_params(q, k_pool, v_pool, block_table, ctx_len, None, None, None, scale, None)
+    return int(load().paged_attn_decode_workspace(C.byref(p)))
+
+
+def paged_attn_decode(q, k_pool, v_pool, block_table, ctx_len, *, k_new=None, v_new=None,
+                      scale=0.0, err_word=None, y=None, workspace=None, stream=None):
+    """Paged causal decode: ``q [B,Hq,1,D]`` (or ``[B,Hq,D]``), pools
+    ``[num_pages,Hkv,page_tokens,D]``, ``block_table int32 [B,max_pages]``,
+    ``ctx_len int32 [B]``; optional ``k_new/v_new [B,Hkv,D]`` written at token
+    ``ctx_len-1`` first.  Returns ``y`` shaped like ``q``."""
+    L = load()
+    for n, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("block_table", block_table),
+                 ("ctx_len", ctx_len), ("k_new", k_new), ("v_new", v_new),
+                 ("err_word", err_word)):
+        _dev(t, n)
+    if block_table.dtype != torch.int32 or ctx_len.dtype != torch.int32:
+        raise TypeError("block_table and ctx_len must be int32")
+    if y is None:
+        y = torch.empty_like(q)
+    p = _paged_params(q, k_pool, v_pool, block_table, ctx_len, y, k_new, v_new, scale, err_word)
+    need = int(L.paged_attn_decode_workspace(C.byref(p)))
+    ws, nb = _workspace(need, q.device, workspace)
+    p.workspace, p.workspace_bytes = _ptr(ws), nb
+    _check("paged_attn_decode", L.paged_attn_decode(C.byref(p), _stream(stream)))
+    return y

@@ -1,0 +1,101 @@
+// kernels.h -- argument blocks and launchers shared between the host entry
+// points (sa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sa {
+
+// ---- index validation --------------------------------------------------------
+struct ValidateArgs {
+  const void* idx;
+  int is_i64;
+  int vec_ok;                 // 16-byte vector loads are legal
+  int64_t rows;               // B * I * Sq
+  int64_t rows_per_batch;     // I * Sq
+  int64_t K;
+  const int64_t* bound_per_batch;
+  int64_t bound;
+  uint8_t* row_status;
+  uint32_t* err_word;
+};
+int launch_validate(const ValidateArgs& a, cudaStream_t st);
+
+// ---- present KV --------------------------------------------------------------
+struct PresentArgs {
+  const void* past[2];
+  const void* cur[2];
+  void* present[2];
+  int n_tensors;              // 1 (K) or 2 (K and V)
+  int esz;                    // element bytes
+  int64_t B, H, P, C, D;
+  int64_t stride;             // present positions per (b, h)
+  const int64_t* write_pos;   // append mode when non-null
+  int copy_past;              // append mode: copy past wholly first
+  uint32_t* err_word;
+};
+int launch_present(const PresentArgs& a, cudaStream_t st);
+
+// ---- gather decode (sparse and paged) ------------------------------------------
+enum KeySource : int { kSparse = 0, kPaged = 1, kDense = 2 };
+
+struct GatherArgs {
+  // tensors
+  const void* q;              // [B, Hq, Sq, D]
+  const void* k;              // dense cache or page pool
+  const void* v;
+  void* y;                    // [B, Hq, Sq, Dv]
+  const float* sink;          // nullable [Hq]
+  float* part_o;              // [units, splits, hpu, Dv] unnormalised partial outputs
+  float* part_ml;             // [units, splits, hpu, 2] running max (log2 units), sum
+  uint32_t* err_word;
+  // geometry
+  int source;                 // KeySource
+  int64_t B, Hq, Hkv, Sq, D, Dv;
+  int64_t g;                  // Hq / Hkv
+  int64_t hpu;                // heads served per unit
+  int64_t n_groups;           // units per (b, i): Hkv, or Hq when rows are per head
+  int64_t units;              // B * n_groups * Sq
+  int64_t splits;             // key splits per unit
+  int64_t chunk;              // candidates per split
+  int64_t n_cand;             // candidates per unit (upper bound for paged)
+  // sparse source
+  const void* idx;
+  int idx_is_i64;
+  int64_t I, K, T;            // index heads, index width, cache stride
+  int64_t window;
+  const int64_t* kv_len;      // nullable
+  int64_t past_len;
+  int causal;
+  // paged source
+  const int32_t* block_table;
+  const int32_t* ctx_len;
+  int64_t page_tokens, max_pages, num_pages;
+  // math
+  float scale_log2;           // scale * log2(e)
+  float softcap;              // 0 = off
+  float inv_softcap;
+};
+
+int launch_gather_decode(const GatherArgs& a, int dtype, cudaStream_t st);
+bool gather_uses_mma(const GatherArgs& a, int dtype);
+// Resident CTAs per SM of the tensor-core gather kernel for this request.
+int gather_mma_occupancy(const GatherArgs& a, int dtype);
+int launch_combine(const GatherArgs& a, int dtype, cudaStream_t st);
+
+// ---- paged: write the new token into the pool -----------------------------------
+struct PagedAppendArgs {
+  void* k_pool;
+  void* v_pool;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* block_table;
+  const int32_t* ctx_len;
+  int64_t B, Hkv, D, page_tokens, max_pages, num_pages;
+  int esz;
+  uint32_t* err_word;
+};
+int launch_paged_append(const PagedAppendArgs& a, cudaStream_t st);
+
+}  // namespace sa

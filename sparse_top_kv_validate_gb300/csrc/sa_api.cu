@@ -1,0 +1,527 @@
+// sa_api.cu -- the library's C ABI: host-side argument checks, work planning
+// (units, splits, workspace carving) and kernel launches.  Nothing here
+// allocates, frees or synchronises; everything is enqueued on the caller's
+// stream.
+#include <cuda_runtime.h>
+#include <cmath>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/sa.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t dtype_bytes(int dt) {
+  switch (dt) {
+    case SA_F32: return 4;
+    case SA_F16: return 2;
+    case SA_BF16: return 2;
+    default: return 0;
+  }
+}
+
+// Half-open byte ranges [a, a+na) and [b, b+nb) intersect.
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+struct DeviceShape {
+  int sms = 152;
+};
+
+DeviceShape device_shape() {
+  DeviceShape d;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      d.sms = n;
+  }
+  return d;
+}
+
+// Splits of `n_cand` candidates per unit for the tensor-core kernel: chunks
+// are whole 64-key stages (at most 1024 keys); among the candidate chunk
+// sizes, pick the one whose CTA count fills the machine's resident slots in
+// the most even number of waves, preferring fewer splits on ties.
+void plan_mma_splits(int64_t units, int64_t n_cand, int64_t slots, int64_t* chunk_out,
+                     int64_t* splits_out) {
+  if (n_cand <= 0) {
+    *chunk_out = 64;
+    *splits_out = 1;
+    return;
+  }
+  double best = -1.0;
+  int64_t best_chunk = 64, best_splits = 1;
+  for (int64_t chunk = 64; chunk <= 1024; chunk += 64) {
+    const int64_t splits = (n_cand + chunk - 1) / chunk;
+    if (splits > 64) continue;
+    const double waves = static_cast<double>(units * splits) / static_cast<double>(slots);
+    const double eff = waves / ceil(waves);
+    // Few CTAs per SM leave latency uncovered; many splits cost combine traffic.
+    const double score = eff - 0.004 * static_cast<double>(splits) -
+                         (waves < 2.0 ? 0.25 * (2.0 - waves) : 0.0);
+    if (score > best + 1e-9) {
+      best = score;
+      best_chunk = chunk;
+      best_splits = splits;
+    }
+    if (chunk >= n_cand) break;
+  }
+  *chunk_out = best_chunk;
+  *splits_out = best_splits;
+}
+
+void plan_simt_splits(int64_t n_cand, int64_t* chunk_out, int64_t* splits_out) {
+  int64_t splits = (n_cand + 255) / 256;
+  if (splits < 1) splits = 1;
+  if (splits > 64) splits = 64;
+  int64_t chunk = (n_cand + splits - 1) / splits;
+  if (chunk < 1) chunk = 1;
+  *chunk_out = chunk;
+  *splits_out = (n_cand + chunk - 1) / chunk > 0 ? (n_cand + chunk - 1) / chunk : 1;
+}
+
+// Fill the geometry / split plan of a gather request whose source, shape and
+// tensor fields are already set.  Returns SA_OK or an error status.
+int plan_gather(sa::GatherArgs& g, int dtype) {
+  g.g = g.Hq / g.Hkv;
+  if (g.source == sa::kSparse && g.I == g.Hq && g.g > 1) {
+    g.n_groups = g.Hq;  // each query head has its own index row
+    g.hpu = 1;
+  } else {
+    g.n_groups = g.Hkv;
+    g.hpu = g.g;
+  }
+  g.units = g.B * g.n_groups * g.Sq;
+  if (sa::gather_uses_mma(g, dtype)) {
+    g.chunk = 1024;  // occupancy is insensitive to the few KB of index staging
+    const int64_t per_sm = sa::gather_mma_occupancy(g, dtype);
+    const int64_t slots = static_cast<int64_t>(device_shape().sms) * per_sm;
+    plan_mma_splits(g.units, g.n_cand, slots, &g.chunk, &g.splits);
+  } else {
+    if ((g.D + 31) / 32 > 16) return SA_ERR_UNSUPPORTED;
+    plan_simt_splits(g.n_cand, &g.chunk, &g.splits);
+  }
+  return SA_OK;
+}
+
+size_t gather_workspace(const sa::GatherArgs& g) {
+  if (g.splits <= 1) return 0;
+  const size_t parts = static_cast<size_t>(g.units * g.splits * g.hpu);
+  return align_up(parts * g.Dv * sizeof(float)) + align_up(parts * 2 * sizeof(float));
+}
+
+void carve_gather_workspace(sa::GatherArgs& g, void* ws) {
+  if (g.splits <= 1) {
+    g.part_o = nullptr;
+    g.part_ml = nullptr;
+    return;
+  }
+  const size_t parts = static_cast<size_t>(g.units * g.splits * g.hpu);
+  char* base = static_cast<char*>(ws);
+  g.part_o = reinterpret_cast<float*>(base);
+  g.part_ml = reinterpret_cast<float*>(base + align_up(parts * g.Dv * sizeof(float)));
+}
+
+int run_gather(const sa::GatherArgs& g, int dtype, cudaStream_t st) {
+  if (sa::launch_gather_decode(g, dtype, st) != 0) return SA_ERR_LAUNCH;
+  if (sa::launch_combine(g, dtype, st) != 0) return SA_ERR_LAUNCH;
+  return SA_OK;
+}
+
+// ---- sparse decode: checks + plan ----------------------------------------------
+
+int check_sparse(const sa_sparse_params* p) {
+  if (!p || !p->q || !p->k_cache || !p->y) return SA_ERR_NULL;
+  if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->Sq <= 0 || p->D <= 0 || p->T <= 0)
+    return SA_ERR_SHAPE;
+  if (p->Hq % p->Hkv != 0) return SA_ERR_SHAPE;
+  if (!(p->I == 1 || p->I == p->Hkv || p->I == p->Hq)) return SA_ERR_SHAPE;
+  if (p->K < 0 || p->window < 0 || p->past_len < 0) return SA_ERR_SHAPE;
+  if (p->K == 0 && p->window == 0) return SA_ERR_SHAPE;
+  if (p->K > 0 && !p->idx) return SA_ERR_NULL;
+  if (p->kv_dtype == SA_FP8_E4M3_B64) return SA_ERR_UNSUPPORTED;  // served by the FP8 path
+  if (p->kv_dtype != p->q_dtype || dtype_bytes(p->q_dtype) == 0) return SA_ERR_DTYPE;
+  if (!p->v_cache) return SA_ERR_NULL;
+  if (p->Dv != p->D) return SA_ERR_UNSUPPORTED;
+  if (p->B * p->Hkv * p->T >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
+  if (!std::isfinite(p->scale) || !std::isfinite(p->softcap) || p->softcap < 0.f)
+    return SA_ERR_SHAPE;
+  const size_t es = dtype_bytes(p->q_dtype);
+  const size_t qbytes = static_cast<size_t>(p->B * p->Hq * p->Sq * p->D) * es;
+  const size_t ybytes = static_cast<size_t>(p->B * p->Hq * p->Sq * p->Dv) * es;
+  const size_t kvbytes = static_cast<size_t>(p->B * p->Hkv * p->T * p->D) * es;
+  const size_t ibytes = static_cast<size_t>(p->B * p->I * p->Sq * p->K) * (p->idx_is_i64 ? 8 : 4);
+  if (overlaps(p->y, ybytes, p->q, qbytes) || overlaps(p->y, ybytes, p->k_cache, kvbytes) ||
+      overlaps(p->y, ybytes, p->v_cache, kvbytes) || overlaps(p->y, ybytes, p->idx, ibytes))
+    return SA_ERR_OVERLAP;
+  if ((reinterpret_cast<uintptr_t>(p->q) | reinterpret_cast<uintptr_t>(p->y)) % es) return SA_ERR_ALIGN;
+  return SA_OK;
+}
+
+int sparse_plan(const sa_sparse_params* p, sa::GatherArgs& g) {
+  memset(&g, 0, sizeof(g));
+  g.q = p->q;
+  g.k = p->k_cache;
+  g.v = p->v_cache;
+  g.y = p->y;
+  g.sink = p->sink;
+  g.err_word = p->err_word;
+  g.source = sa::kSparse;
+  g.B = p->B;
+  g.Hq = p->Hq;
+  g.Hkv = p->Hkv;
+  g.Sq = p->Sq;
+  g.D = p->D;
+  g.Dv = p->Dv;
+  g.idx = p->idx;
+  g.idx_is_i64 = p->idx_is_i64;
+  g.I = p->I;
+  g.K = p->K;
+  g.T = p->T;
+  g.window = p->window;
+  g.kv_len = p->kv_len;
+  g.past_len = p->past_len;
+  g.causal = p->causal;
+  g.n_cand = p->window + p->K;
+  const float scale = p->scale != 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->D));
+  g.scale_log2 = scale * 1.4426950408889634f;
+  g.softcap = p->softcap;
+  g.inv_softcap = p->softcap != 0.f ? 1.0f / p->softcap : 0.f;
+  int rc = plan_gather(g, p->q_dtype);
+  if (rc != SA_OK) return rc;
+  if (sa::gather_uses_mma(g, p->q_dtype) &&
+      !(aligned16(p->k_cache) && aligned16(p->v_cache)))
+    return SA_ERR_ALIGN;
+  return SA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sa_status_string(int status) {
+  switch (status) {
+    case SA_OK: return "ok";
+    case SA_ERR_NULL: return "a required pointer is NULL";
+    case SA_ERR_SHAPE: return "a size is non-positive or inconsistent";
+    case SA_ERR_DTYPE: return "unsupported dtype or dtype combination";
+    case SA_ERR_ALIGN: return "a pointer is not suitably aligned";
+    case SA_ERR_WORKSPACE: return "workspace missing or too small";
+    case SA_ERR_OVERLAP: return "an output overlaps an input";
+    case SA_ERR_UNSUPPORTED: return "request not served by this build";
+    case SA_ERR_LAUNCH: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+int sa_version(void) { return 100; }
+
+int validate_indices(const void* idx, int idx_is_i64, int64_t B, int64_t I, int64_t Sq,
+                     int64_t K, const int64_t* bound_per_batch, int64_t bound,
+                     uint8_t* row_status, uint32_t* err_word, void* stream) {
+  if (!idx || !err_word) return SA_ERR_NULL;
+  if (B <= 0 || I <= 0 || Sq <= 0 || K <= 0 || bound < 0) return SA_ERR_SHAPE;
+  const size_t esz = idx_is_i64 ? 8 : 4;
+  if (reinterpret_cast<uintptr_t>(idx) % esz) return SA_ERR_ALIGN;
+  sa::ValidateArgs a;
+  a.idx = idx;
+  a.is_i64 = idx_is_i64 ? 1 : 0;
+  a.vec_ok = aligned16(idx) && ((K * static_cast<int64_t>(esz)) % 16 == 0);
+  a.rows = B * I * Sq;
+  a.rows_per_batch = I * Sq;
+  a.K = K;
+  a.bound_per_batch = bound_per_batch;
+  a.bound = bound;
+  a.row_status = row_status;
+  a.err_word = err_word;
+  return sa::launch_validate(a, as_stream(stream)) == 0 ? SA_OK : SA_ERR_LAUNCH;
+}
+
+int build_present_kv(const void* past_k, const void* cur_k, void* present_k, const void* past_v,
+                     const void* cur_v, void* present_v, int dtype, int64_t B, int64_t H,
+                     int64_t P, int64_t C, int64_t D, int64_t present_stride,
+                     const int64_t* write_pos, uint32_t* err_word, void* stream) {
+  const size_t es = dtype_bytes(dtype);
+  if (es == 0) return SA_ERR_DTYPE;
+  if (!cur_k || !present_k) return SA_ERR_NULL;
+  if (present_v && !cur_v) return SA_ERR_NULL;
+  if (B <= 0 || H <= 0 || C <= 0 || D <= 0 || P < 0) return SA_ERR_SHAPE;
+  sa::PresentArgs a;
+  memset(&a, 0, sizeof(a));
+  a.n_tensors = present_v ? 2 : 1;
+  a.esz = static_cast<int>(es);
+  a.B = B;
+  a.H = H;
+  a.P = P;
+  a.C = C;
+  a.D = D;
+  a.stride = present_stride;
+  a.write_pos = write_pos;
+  a.err_word = err_word;
+  const void* pasts[2] = {past_k, past_v};
+  const void* curs[2] = {cur_k, cur_v};
+  void* outs[2] = {present_k, present_v};
+  const size_t row = static_cast<size_t>(D) * es;
+  const size_t out_bytes = static_cast<size_t>(B * H * present_stride) * row;
+  const size_t cur_bytes = static_cast<size_t>(B * H * C) * row;
+  if (write_pos == nullptr) {
+    if (present_stride < P + C) return SA_ERR_SHAPE;
+    if (P > 0 && (!past_k || (present_v && !past_v))) return SA_ERR_NULL;
+    const size_t past_bytes = static_cast<size_t>(B * H * P) * row;
+    for (int t = 0; t < a.n_tensors; ++t) {
+      for (int s = 0; s < 2; ++s) {  // against both tensors' inputs
+        if (overlaps(outs[t], out_bytes, curs[s], cur_bytes) ||
+            overlaps(outs[t], out_bytes, pasts[s], P > 0 ? past_bytes : 0))
+          return SA_ERR_OVERLAP;
+      }
+    }
+    if (overlaps(outs[0], out_bytes, outs[1], out_bytes)) return SA_ERR_OVERLAP;
+  } else {
+    if (present_stride < C) return SA_ERR_SHAPE;
+    for (int t = 0; t < a.n_tensors; ++t) {
+      if (pasts[t] && pasts[t] != outs[t]) {
+        a.copy_past = 1;
+        if (overlaps(outs[t], out_bytes, pasts[t], out_bytes)) return SA_ERR_OVERLAP;
+      }
+      for (int s = 0; s < a.n_tensors; ++s)
+        if (overlaps(outs[t], out_bytes, curs[s], cur_bytes)) return SA_ERR_OVERLAP;
+    }
+    if (a.copy_past) {
+      for (int t = 0; t < a.n_tensors; ++t)
+        if (!pasts[t] || pasts[t] == outs[t]) return SA_ERR_UNSUPPORTED;  // mixed modes
+    }
+    if (overlaps(outs[0], out_bytes, outs[1], out_bytes)) return SA_ERR_OVERLAP;
+  }
+  for (int t = 0; t < a.n_tensors; ++t) {
+    a.past[t] = pasts[t] ? pasts[t] : curs[t];
+    a.cur[t] = curs[t];
+    a.present[t] = outs[t];
+    if (reinterpret_cast<uintptr_t>(outs[t]) % es || reinterpret_cast<uintptr_t>(curs[t]) % es)
+      return SA_ERR_ALIGN;
+  }
+  return sa::launch_present(a, as_stream(stream)) == 0 ? SA_OK : SA_ERR_LAUNCH;
+}
+
+size_t sparse_attn_decode_workspace(const sa_sparse_params* p) {
+  if (check_sparse(p) != SA_OK) return 0;
+  sa::GatherArgs g;
+  if (sparse_plan(p, g) != SA_OK) return 0;
+  return gather_workspace(g);
+}
+
+int sparse_attn_decode(const sa_sparse_params* p, void* stream) {
+  int rc = check_sparse(p);
+  if (rc != SA_OK) return rc;
+  sa::GatherArgs g;
+  rc = sparse_plan(p, g);
+  if (rc != SA_OK) return rc;
+  const size_t need = gather_workspace(g);
+  if (need > 0 && (!p->workspace || p->workspace_bytes < need)) return SA_ERR_WORKSPACE;
+  if (need > 0 && reinterpret_cast<uintptr_t>(p->workspace) % kAlign) return SA_ERR_ALIGN;
+  carve_gather_workspace(g, p->workspace);
+  cudaStream_t st = as_stream(stream);
+  if (p->K > 0 && (p->err_word || p->row_status)) {
+    sa::ValidateArgs v;
+    v.idx = p->idx;
+    v.is_i64 = p->idx_is_i64 ? 1 : 0;
+    const size_t esz = p->idx_is_i64 ? 8 : 4;
+    v.vec_ok = aligned16(p->idx) && ((p->K * static_cast<int64_t>(esz)) % 16 == 0);
+    v.rows = p->B * p->I * p->Sq;
+    v.rows_per_batch = p->I * p->Sq;
+    v.K = p->K;
+    v.bound_per_batch = p->kv_len;
+    v.bound = p->T;
+    v.row_status = p->row_status;
+    v.err_word = p->err_word;
+    if (sa::launch_validate(v, st) != 0) return SA_ERR_LAUNCH;
+  }
+  return run_gather(g, p->q_dtype, st);
+}
+
+// ---- prefill ---------------------------------------------------------------------
+
+static int check_prefill(const sa_prefill_params* p) {
+  if (!p || !p->q || !p->k || !p->v || !p->y) return SA_ERR_NULL;
+  if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->S <= 0 || p->D <= 0) return SA_ERR_SHAPE;
+  if (p->Hq % p->Hkv != 0) return SA_ERR_SHAPE;
+  if (dtype_bytes(p->dtype) == 0) return SA_ERR_DTYPE;
+  if (p->B * p->Hkv * p->S >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
+  if (!std::isfinite(p->scale) || !std::isfinite(p->softcap) || p->softcap < 0.f)
+    return SA_ERR_SHAPE;
+  const size_t es = dtype_bytes(p->dtype);
+  const size_t qb = static_cast<size_t>(p->B * p->Hq * p->S * p->D) * es;
+  const size_t kb = static_cast<size_t>(p->B * p->Hkv * p->S * p->D) * es;
+  const void* ins[3] = {p->q, p->k, p->v};
+  const size_t inb[3] = {qb, kb, kb};
+  for (int i = 0; i < 3; ++i) {
+    if (overlaps(p->y, qb, ins[i], inb[i])) return SA_ERR_OVERLAP;
+    if (overlaps(p->present_k, kb, ins[i], inb[i])) return SA_ERR_OVERLAP;
+    if (overlaps(p->present_v, kb, ins[i], inb[i])) return SA_ERR_OVERLAP;
+  }
+  if (overlaps(p->y, qb, p->present_k, kb) || overlaps(p->y, qb, p->present_v, kb) ||
+      overlaps(p->present_k, kb, p->present_v, kb))
+    return SA_ERR_OVERLAP;
+  return SA_OK;
+}
+
+static void prefill_plan(const sa_prefill_params* p, sa::GatherArgs& g) {
+  memset(&g, 0, sizeof(g));
+  g.q = p->q;
+  g.k = p->k;
+  g.v = p->v;
+  g.y = p->y;
+  g.source = sa::kDense;
+  g.B = p->B;
+  g.Hq = p->Hq;
+  g.Hkv = p->Hkv;
+  g.Sq = p->S;
+  g.D = p->D;
+  g.Dv = p->D;
+  g.T = p->S;
+  g.I = p->Hkv;
+  g.causal = p->causal;
+  g.past_len = 0;
+  g.n_cand = p->S;
+  const float scale = p->scale != 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->D));
+  g.scale_log2 = scale * 1.4426950408889634f;
+  g.softcap = p->softcap;
+  g.inv_softcap = p->softcap != 0.f ? 1.0f / p->softcap : 0.f;
+}
+
+size_t attn_prefill_workspace(const sa_prefill_params* p) {
+  if (check_prefill(p) != SA_OK) return 0;
+  sa::GatherArgs g;
+  prefill_plan(p, g);
+  if (plan_gather(g, p->dtype) != SA_OK) return 0;
+  return gather_workspace(g);
+}
+
+int attn_prefill(const sa_prefill_params* p, void* stream) {
+  int rc = check_prefill(p);
+  if (rc != SA_OK) return rc;
+  cudaStream_t st = as_stream(stream);
+  sa::GatherArgs g;
+  prefill_plan(p, g);
+  rc = plan_gather(g, p->dtype);
+  if (rc != SA_OK) return rc;
+  if (sa::gather_uses_mma(g, p->dtype) && !(aligned16(p->k) && aligned16(p->v)))
+    return SA_ERR_ALIGN;
+  const size_t need = gather_workspace(g);
+  if (need > 0 && (!p->workspace || p->workspace_bytes < need)) return SA_ERR_WORKSPACE;
+  if (need > 0 && reinterpret_cast<uintptr_t>(p->workspace) % kAlign) return SA_ERR_ALIGN;
+  carve_gather_workspace(g, p->workspace);
+  if (p->present_k || p->present_v) {
+    const void* cur_k = p->present_k ? p->k : p->v;
+    void* out_k = p->present_k ? p->present_k : p->present_v;
+    const void* cur_v = (p->present_k && p->present_v) ? p->v : nullptr;
+    void* out_v = (p->present_k && p->present_v) ? p->present_v : nullptr;
+    rc = build_present_kv(nullptr, cur_k, out_k, nullptr, cur_v, out_v, p->dtype, p->B, p->Hkv,
+                          0, p->S, p->D, p->S, nullptr, nullptr, stream);
+    if (rc != SA_OK) return rc;
+  }
+  return run_gather(g, p->dtype, st);
+}
+
+// ---- paged decode ------------------------------------------------------------------
+
+static int check_paged(const sa_paged_params* p) {
+  if (!p || !p->q || !p->k_pool || !p->v_pool || !p->block_table || !p->ctx_len || !p->y)
+    return SA_ERR_NULL;
+  if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0 || p->page_tokens <= 0 ||
+      p->max_pages <= 0 || p->num_pages <= 0)
+    return SA_ERR_SHAPE;
+  if (p->Hq % p->Hkv != 0) return SA_ERR_SHAPE;
+  if (dtype_bytes(p->dtype) == 0) return SA_ERR_DTYPE;
+  if (p->num_pages * p->Hkv * p->page_tokens >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
+  if (!std::isfinite(p->scale)) return SA_ERR_SHAPE;
+  const size_t es = dtype_bytes(p->dtype);
+  const size_t yb = static_cast<size_t>(p->B * p->Hq * p->D) * es;
+  const size_t pool = static_cast<size_t>(p->num_pages * p->Hkv * p->page_tokens * p->D) * es;
+  if (overlaps(p->y, yb, p->q, yb) || overlaps(p->y, yb, p->k_pool, pool) ||
+      overlaps(p->y, yb, p->v_pool, pool) || overlaps(p->k_pool, pool, p->v_pool, pool))
+    return SA_ERR_OVERLAP;
+  return SA_OK;
+}
+
+static void paged_plan(const sa_paged_params* p, sa::GatherArgs& g) {
+  memset(&g, 0, sizeof(g));
+  g.q = p->q;
+  g.k = p->k_pool;
+  g.v = p->v_pool;
+  g.y = p->y;
+  g.err_word = p->err_word;
+  g.source = sa::kPaged;
+  g.B = p->B;
+  g.Hq = p->Hq;
+  g.Hkv = p->Hkv;
+  g.Sq = 1;
+  g.D = p->D;
+  g.Dv = p->D;
+  g.I = p->Hkv;
+  g.block_table = p->block_table;
+  g.ctx_len = p->ctx_len;
+  g.page_tokens = p->page_tokens;
+  g.max_pages = p->max_pages;
+  g.num_pages = p->num_pages;
+  g.n_cand = p->max_pages * p->page_tokens;
+  const float scale = p->scale != 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->D));
+  g.scale_log2 = scale * 1.4426950408889634f;
+}
+
+size_t paged_attn_decode_workspace(const sa_paged_params* p) {
+  if (check_paged(p) != SA_OK) return 0;
+  sa::GatherArgs g;
+  paged_plan(p, g);
+  if (plan_gather(g, p->dtype) != SA_OK) return 0;
+  return gather_workspace(g);
+}
+
+int paged_attn_decode(const sa_paged_params* p, void* stream) {
+  int rc = check_paged(p);
+  if (rc != SA_OK) return rc;
+  cudaStream_t st = as_stream(stream);
+  sa::GatherArgs g;
+  paged_plan(p, g);
+  rc = plan_gather(g, p->dtype);
+  if (rc != SA_OK) return rc;
+  if (sa::gather_uses_mma(g, p->dtype) && !(aligned16(p->k_pool) && aligned16(p->v_pool)))
+    return SA_ERR_ALIGN;
+  const size_t need = gather_workspace(g);
+  if (need > 0 && (!p->workspace || p->workspace_bytes < need)) return SA_ERR_WORKSPACE;
+  if (need > 0 && reinterpret_cast<uintptr_t>(p->workspace) % kAlign) return SA_ERR_ALIGN;
+  carve_gather_workspace(g, p->workspace);
+  if (p->k_new || p->v_new) {
+    sa::PagedAppendArgs a;
+    a.k_pool = p->k_pool;
+    a.v_pool = p->v_pool;
+    a.k_new = p->k_new;
+    a.v_new = p->v_new;
+    a.block_table = p->block_table;
+    a.ctx_len = p->ctx_len;
+    a.B = p->B;
+    a.Hkv = p->Hkv;
+    a.D = p->D;
+    a.page_tokens = p->page_tokens;
+    a.max_pages = p->max_pages;
+    a.num_pages = p->num_pages;
+    a.esz = static_cast<int>(dtype_bytes(p->dtype));
+    a.err_word = p->err_word;
+    if (sa::launch_paged_append(a, st) != 0) return SA_ERR_LAUNCH;
+  }
+  return run_gather(g, p->dtype, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,116 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function
+that include/sa.h declares, the Python structs match the C layout, and the
+host-side argument checks reject bad requests before anything is launched."""
+import ctypes as C
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+import sparse_top_kv_validate_gb300 as sa
+from sparse_top_kv_validate_gb300 import build as sa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sa_build.build()
+    return sa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_five_operations():
+    names = declared_functions()
+    for n in ("validate_indices", "build_present_kv", "sparse_attn_decode", "attn_prefill",
+              "paged_attn_decode"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", sa.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+
+
+def _c_layout(struct_name, fields):
+    src = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"', "int main(void){",
+           f'printf("%zu\\n", sizeof({struct_name}));']
+    for f in fields:
+        src.append(f'printf("%zu\\n", offsetof({struct_name}, {f}));')
+    src.append("return 0;}")
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        exe = os.path.join(d, "t")
+        open(c, "w").write("\n".join(src))
+        subprocess.run(["gcc", "-o", exe, c], check=True)
+        vals = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
+                                               check=True).stdout.split()]
+    return vals[0], vals[1:]
+
+
+@pytest.mark.parametrize("cname,py", [("sa_sparse_params", sa.SparseParams),
+                                      ("sa_prefill_params", sa.PrefillParams),
+                                      ("sa_paged_params", sa.PagedParams)])
+def test_struct_layout_matches_header(cname, py):
+    fields = [f for f, _ in py._fields_]
+    size, offs = _c_layout(cname, fields)
+    assert C.sizeof(py) == size
+    assert [getattr(py, f).offset for f in fields] == offs
+
+
+def test_status_strings(lib):
+    assert sa.status_string(0) == "ok"
+    assert "NULL" in sa.status_string(-1)
+    assert lib.sa_version() >= 100
+
+
+def test_host_checks_reject_bad_requests_without_launching(lib):
+    # validate_indices: null pointers, bad shapes
+    assert lib.validate_indices(None, 0, 1, 1, 1, 4, None, 10, None, None, None) == -1
+    fake = C.c_void_p(0x1000)
+    word = C.c_void_p(0x2000)
+    assert lib.validate_indices(fake, 0, 0, 1, 1, 4, None, 10, None, word, None) == -2
+    assert lib.validate_indices(C.c_void_p(0x1002), 0, 1, 1, 1, 4, None, 10, None, word,
+                                None) == -4
+    # sparse decode
+    p = sa.SparseParams()
+    assert lib.sparse_attn_decode(C.byref(p), None) == -1
+    p.q, p.k_cache, p.v_cache, p.y, p.idx = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+    p.B, p.Hq, p.Hkv, p.Sq, p.D, p.Dv, p.T, p.I, p.K = 1, 6, 4, 1, 64, 64, 32, 4, 8
+    p.q_dtype = p.kv_dtype = sa.BF16
+    assert lib.sparse_attn_decode(C.byref(p), None) == -2   # Hq % Hkv
+    p.Hkv = 2
+    p.I = 3
+    assert lib.sparse_attn_decode(C.byref(p), None) == -2   # I not in {1, Hkv, Hq}
+    p.I = 2
+    p.kv_dtype = sa.F16
+    assert lib.sparse_attn_decode(C.byref(p), None) == -3   # q/kv dtype mismatch
+    p.kv_dtype = sa.BF16
+    p.y = 0x10000 + 64                                       # y overlaps q
+    assert lib.sparse_attn_decode(C.byref(p), None) == -6
+    p.y = 0x40000
+    p.K, p.window = 0, 0
+    assert lib.sparse_attn_decode(C.byref(p), None) == -2   # no candidates at all
+    # present: concat output overlapping an input
+    assert lib.build_present_kv(None, C.c_void_p(0x1000), C.c_void_p(0x1000), None, None, None,
+                                sa.BF16, 1, 1, 0, 4, 8, 4, None, None, None) == -6
+    assert lib.build_present_kv(None, C.c_void_p(0x1000), C.c_void_p(0x9000), None, None, None,
+                                7, 1, 1, 0, 4, 8, 4, None, None, None) == -3
+    # prefill / paged
+    q = sa.PrefillParams()
+    assert lib.attn_prefill(C.byref(q), None) == -1
+    g = sa.PagedParams()
+    assert lib.paged_attn_decode(C.byref(g), None) == -1

@@ -1,0 +1,267 @@
+"""GPU parity of index validation, present-KV and selected-token decode
+against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import assert_close, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _run_sparse(sa, c, inp, **kw):
+    q = inp["q"].to(DEV)
+    k = inp["k_cache"].to(DEV)
+    v = inp["v_cache"].to(DEV)
+    idx = inp["idx"].to(DEV)
+    return sa.sparse_attn_decode(q, k, v, idx, scale=c.eff_scale(), **kw)
+
+
+def _oracle_sparse(c, inp, **kw):
+    return oracle.sparse_attention(inp["q"], inp["idx"], inp["k_cache"], inp["v_cache"],
+                                   scale=c.eff_scale(), **kw)
+
+
+# ---------------------------------------------------------------------------
+# index validation (bit-exact)
+# ---------------------------------------------------------------------------
+
+def _mutated_rows(rows, K, T, seed):
+    """Valid rows plus one planted fault per faulty row (each rule)."""
+    rng = np.random.default_rng(seed)
+    idx = synth.sorted_sample_rows(rows, 0, T, K, seed).numpy()
+    kinds = rng.integers(0, 8, size=rows)
+    for r in range(rows):
+        col = int(rng.integers(1, K))
+        k = kinds[r]
+        if k == 1:
+            idx[r, col] = -int(rng.integers(2, 1000))           # below sentinel
+        elif k == 2:
+            idx[r, col - 1] = -1                                  # value after padding
+        elif k == 3:
+            idx[r, col] = T + int(rng.integers(0, 5))             # out of range
+        elif k == 4:
+            idx[r, col] = idx[r, col - 1]                         # duplicate
+        elif k == 5 and idx[r, col - 1] > 0:
+            idx[r, col] = idx[r, col - 1] - 1                     # decreasing
+        elif k == 6:
+            idx[r, :] = -1                                        # all padding
+        elif k == 7:
+            idx[r, col:] = -1                                     # valid tail
+    return torch.from_numpy(idx)
+
+
+@pytest.mark.parametrize("K", [1, 7, 32, 129, 300, 2048, 2500, 5000])
+@pytest.mark.parametrize("i64", [False, True])
+def test_validate_indices_bit_exact(cuda_lib, K, i64):
+    sa = cuda_lib
+    B, I, Sq, T = 3, 4, 2, 6000
+    rows = B * I * Sq
+    idx = _mutated_rows(rows, K, T, seed=K + 17 * i64) if K > 1 else \
+        torch.tensor([[3], [-1], [-5], [7000], [0], [5999]] * 4)[:rows]
+    idx = idx.reshape(B, I, Sq, K).to(torch.int64 if i64 else torch.int32)
+    bpb = torch.tensor([T, T - 100, T], dtype=torch.int64)
+    st_o, err_o = oracle.validate_indices(idx, bound=0, bound_per_batch=bpb)
+    st_g, err_g = sa.validate_indices(idx.to(DEV), 0, bpb.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(st_g.cpu().numpy(), st_o)
+    assert int(err_g.item()) == err_o
+
+
+def test_validate_indices_unaligned_width_scalar_path(cuda_lib):
+    idx = _mutated_rows(40, 13, 100, seed=5).reshape(2, 2, 10, 13).to(torch.int32)
+    st_o, err_o = oracle.validate_indices(idx, bound=100)
+    st_g, err_g = cuda_lib.validate_indices(idx.to(DEV), 100)
+    torch.cuda.synchronize()
+    assert np.array_equal(st_g.cpu().numpy(), st_o) and int(err_g.item()) == err_o
+
+
+# ---------------------------------------------------------------------------
+# present KV (bit-exact)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128, 3])
+def test_present_concat_bit_exact(cuda_lib, dt, D):
+    past_k, past_v = synth.normal((2, 3, 37, D), dt, 1), synth.normal((2, 3, 37, D), dt, 2)
+    cur_k, cur_v = synth.normal((2, 3, 2, D), dt, 3), synth.normal((2, 3, 2, D), dt, 4)
+    pk = torch.zeros((2, 3, 41, D), dtype=past_k.dtype, device=DEV)
+    pv = torch.zeros_like(pk)
+    cuda_lib.build_present_kv(cur_k.to(DEV), pk, past_k.to(DEV), cur_v.to(DEV), pv, past_v.to(DEV))
+    torch.cuda.synchronize()
+    ek = oracle.present_concat(past_k, cur_k, out_stride=41)
+    ev = oracle.present_concat(past_v, cur_v, out_stride=41)
+    assert torch.equal(pk.cpu().view(torch.uint8), ek.view(torch.uint8))
+    assert torch.equal(pv.cpu().view(torch.uint8), ev.view(torch.uint8))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_present_append_in_place_touches_only_the_slot(cuda_lib, dt):
+    cache_k = synth.normal((4, 2, 64, 128), dt, 7)
+    cache_v = synth.normal((4, 2, 64, 128), dt, 8)
+    cur_k = synth.normal((4, 2, 1, 128), dt, 9)
+    cur_v = synth.normal((4, 2, 1, 128), dt, 10)
+    wp = torch.tensor([0, 17, 63, 70], dtype=torch.int64)   # last one is out of range
+    gk, gv = cache_k.to(DEV), cache_v.to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cuda_lib.build_present_kv(cur_k.to(DEV), gk, gk, cur_v.to(DEV), gv, gv, write_pos=wp.to(DEV),
+                              err_word=err)
+    torch.cuda.synchronize()
+    ok_wp = wp.clone()
+    ok_wp[3] = 0
+    ek = oracle.present_append(cache_k, cur_k, ok_wp)
+    ev = oracle.present_append(cache_v, cur_v, ok_wp)
+    ek[3] = cache_k[3]
+    ev[3] = cache_v[3]
+    assert torch.equal(gk.cpu().view(torch.uint8), ek.view(torch.uint8))
+    assert torch.equal(gv.cpu().view(torch.uint8), ev.view(torch.uint8))
+    assert int(err.item()) == cuda_lib.ERRBIT_WRITE_POS
+
+
+def test_present_append_with_separate_past(cuda_lib):
+    past = synth.normal((2, 2, 16, 64), "f16", 11)
+    cur = synth.normal((2, 2, 3, 64), "f16", 12)
+    out = torch.full((2, 2, 16, 64), 7.0, dtype=torch.float16, device=DEV)
+    wp = torch.tensor([2, 13], dtype=torch.int64)
+    cuda_lib.build_present_kv(cur.to(DEV), out, past.to(DEV), write_pos=wp.to(DEV))
+    torch.cuda.synchronize()
+    exp = oracle.present_append(past, cur, wp)
+    assert torch.equal(out.cpu().view(torch.int16), exp.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# selected-token decode
+# ---------------------------------------------------------------------------
+
+def test_tiny_fp32_sparse_decode_matches_oracle(cuda_lib):
+    c = synth.tiny_sparse()
+    for seed in (1, 2):
+        inp = synth.make_sparse_inputs(c, seed)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        y = _run_sparse(cuda_lib, c, inp, err_word=err)
+        torch.cuda.synchronize()
+        assert_close(to64(y), _oracle_sparse(c, inp), torch.float32, "tiny fp32")
+        assert int(err.item()) == 0
+
+
+CASES = [
+    # name, case overrides
+    ("gqa8_rows_per_kvhead", dict(B=2, Hq=16, Hkv=2, T=700, K=300, I=2)),
+    ("rows_per_query_head", dict(B=2, Hq=8, Hkv=2, T=500, K=130, I=8)),
+    ("one_shared_row", dict(B=3, Hq=12, Hkv=3, T=400, K=77, I=1)),
+    ("mha_g1", dict(B=2, Hq=4, Hkv=4, T=300, K=65, I=4)),
+    ("g16_two_ntiles", dict(B=1, Hq=32, Hkv=2, T=600, K=200, I=2)),
+    ("d64", dict(B=2, Hq=8, Hkv=1, T=350, K=100, I=1, D=64)),
+    ("d256", dict(B=1, Hq=8, Hkv=1, T=300, K=140, I=1, D=256)),
+    ("d96_simt", dict(B=1, Hq=4, Hkv=1, T=300, K=100, I=1, D=96)),
+    ("single_key_rows", dict(B=2, Hq=8, Hkv=1, T=100, K=1, I=1)),
+]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("name,over", CASES, ids=[c[0] for c in CASES])
+def test_sparse_decode_matches_oracle(cuda_lib, dt, name, over):
+    c = synth.sparse_bf16(dtype=dt, pad_prob=0.3, pad_max=40, **over)
+    inp = synth.make_sparse_inputs(c, seed=11)
+    y = _run_sparse(cuda_lib, c, inp)
+    torch.cuda.synchronize()
+    assert_close(to64(y), _oracle_sparse(c, inp), y.dtype, name)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_sparse_decode_options(cuda_lib, dt):
+    """window, per-batch kv_len, causal frontier, softcap, sink, int64 indices,
+    several query positions."""
+    c = synth.sparse_bf16(dtype=dt, B=3, Hq=16, Hkv=2, T=520, K=150, I=2, pad_prob=0.4,
+                          pad_max=30, idx_i64=True)
+    inp = synth.make_sparse_inputs(c, seed=21)
+    # Sq = 2 query positions: reuse the index rows for both
+    q2 = synth.normal((c.B, c.Hq, 2, c.D), dt, 22)
+    idx2 = inp["idx"].repeat(1, 1, 2, 1)
+    kv_len = torch.tensor([520, 431, 200], dtype=torch.int64)
+    sink = torch.linspace(-1.0, 2.0, c.Hq, dtype=torch.float32)
+    for opts in (dict(window=64), dict(softcap=1.5), dict(causal=True, past_len=300),
+                 dict(sink=sink), dict(kv_len=kv_len, window=32, softcap=3.0)):
+        inp2 = dict(inp, q=q2, idx=idx2)
+        gkw = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in opts.items()}
+        y = _run_sparse(cuda_lib, c, inp2, **gkw)
+        torch.cuda.synchronize()
+        okw = dict(opts)
+        if "sink" in okw:
+            okw["sink"] = okw["sink"].double()
+        ref = _oracle_sparse(c, inp2, **okw)
+        assert_close(to64(y), ref, y.dtype, str(list(opts)))
+
+
+def test_fully_masked_rows_give_zero(cuda_lib):
+    c = synth.sparse_bf16(B=2, Hq=8, Hkv=1, T=200, K=50, I=1)
+    inp = synth.make_sparse_inputs(c, seed=31)
+    kv_len = torch.tensor([0, 200], dtype=torch.int64, device=DEV)
+    y = _run_sparse(cuda_lib, c, inp, kv_len=kv_len)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y[0]) == 0
+    assert torch.count_nonzero(y[1]) > 0
+
+
+def test_garbage_beyond_valid_length_does_not_change_output(cuda_lib):
+    c = synth.sparse_bf16(B=2, Hq=16, Hkv=2, T=400, K=100, I=2, window=16)
+    inp = synth.make_sparse_inputs(c, seed=41)
+    kv_len = torch.tensor([300, 350], dtype=torch.int64, device=DEV)
+    y1 = _run_sparse(cuda_lib, c, inp, kv_len=kv_len)
+    k2, v2 = inp["k_cache"].clone(), inp["v_cache"].clone()
+    k2[0, :, 300:] = 1e4
+    v2[0, :, 300:] = float("nan")
+    k2[1, :, 350:] = -3e3
+    y2 = _run_sparse(cuda_lib, c, dict(inp, k_cache=k2, v_cache=v2), kv_len=kv_len)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_malformed_rows_latch_error_and_stay_finite(cuda_lib):
+    c = synth.sparse_bf16(B=2, Hq=16, Hkv=2, T=300, K=64, I=2, pad_prob=0.0)
+    inp = synth.make_sparse_inputs(c, seed=51)
+    idx = inp["idx"].clone()
+    idx[0, 0, 0, 5] = 10_000          # out of range
+    idx[1, 1, 0, 3] = idx[1, 1, 0, 2]  # duplicate
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    st = torch.full((4,), 255, dtype=torch.uint8, device=DEV)
+    y = _run_sparse(cuda_lib, c, dict(inp, idx=idx), err_word=err, row_status=st)
+    torch.cuda.synchronize()
+    assert int(err.item()) == (4 | 16)
+    assert st.cpu().tolist() == [4, 0, 0, 16]
+    assert torch.isfinite(y.float()).all()
+
+
+def test_decode_is_deterministic(cuda_lib):
+    c = synth.sparse_bf16(B=4, Hq=64, Hkv=8, T=4096, K=1024, I=8)
+    inp = {k: v.to(DEV) for k, v in synth.make_sparse_inputs(c, seed=61).items()}
+    ys = [cuda_lib.sparse_attn_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["idx"],
+                                      scale=c.eff_scale()) for _ in range(4)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(ys[0], y)
+
+
+def test_full_size_sparse_bf16_sampled_rows(cuda_lib):
+    """B32 Hq64 Hkv8 D128 T8192 K2048 in the benchmark's launch configuration,
+    checked on sampled (batch, KV head) groups against the oracle."""
+    c = synth.sparse_bf16()
+    inp = synth.make_sparse_inputs(c, seed=1, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = cuda_lib.sparse_attn_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["idx"],
+                                    scale=c.eff_scale(), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rng = np.random.default_rng(0)
+    for _ in range(12):
+        b, kvh = int(rng.integers(c.B)), int(rng.integers(c.Hkv))
+        hs = slice(kvh * c.g, (kvh + 1) * c.g)
+        ref = oracle.sparse_attention(inp["q"][b:b + 1, hs].cpu(),
+                                      inp["idx"][b:b + 1, kvh:kvh + 1].cpu(),
+                                      inp["k_cache"][b:b + 1, kvh:kvh + 1].cpu(),
+                                      inp["v_cache"][b:b + 1, kvh:kvh + 1].cpu(),
+                                      scale=c.eff_scale())
+        assert_close(to64(y[b, hs]), ref, y.dtype, f"b={b} kvh={kvh}")
