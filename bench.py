@@ -2,8 +2,9 @@
 
 Default workload: selected-token decode, bf16, B32 Hq64 Hkv8 D128, cache
 8192 tokens, 2048 selected indices per (batch, KV head) row (about 5% of rows
-padded).  One step = append the current token's K/V into the cache, validate
-the index rows on the device, and run the split-K gather decode + combine.
+padded).  One step = one sparse_attn_decode call that appends the current
+token's K/V into the cache, validates the index rows on the device, gathers
+the selected K/V rows and merges the partial softmax results (one kernel).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
@@ -146,16 +147,19 @@ class SparseDecode:
         self.status = torch.empty(c.B * c.I, dtype=torch.uint8, device=dev)
         self.y = torch.empty((c.B, c.Hq, 1, c.D), dtype=self.q.dtype, device=dev)
         nws = sa.sparse_attn_decode_workspace(self.q, self.k, self.v, self.idx,
-                                              scale=c.eff_scale())
-        self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+                                              scale=c.eff_scale(), k_cur=self.k_cur,
+                                              v_cur=self.v_cur, write_pos=self.write_pos,
+                                              err_word=self.err, row_status=self.status)
+        self.ws = sa.new_workspace(nws, dev)
         self.rows = c.B * c.Hq
         self.valid = int((self.idx >= 0).sum().item())
         es = self.q.element_size()
         # algorithmic bytes of the decode call: each valid selected K and V row
-        # once, the index rows, Q and Y.
+        # once, the index rows, Q, Y, and the current token read + written.
+        cur_bytes = 2 * self.k_cur.numel() * es
         self.decode_bytes = (self.valid * 2 * c.D * es + self.idx.numel() * self.idx.element_size()
-                             + self.q.numel() * es + self.y.numel() * es)
-        self.launches_per_step = 4  # present, validate, gather, combine
+                             + self.q.numel() * es + self.y.numel() * es + 2 * cur_bytes)
+        self.launches_per_step = 1  # one fused kernel (plus a small counter memset)
         # host copies for the end-to-end leg
         self.h_q = self.q.cpu().pin_memory()
         self.h_idx = self.idx.cpu().pin_memory()
@@ -166,13 +170,12 @@ class SparseDecode:
 
     def step(self, ev=None):
         sa, c = self.sa, self.c
-        sa.build_present_kv(self.k_cur, self.k, self.k, self.v_cur, self.v, self.v,
-                            write_pos=self.write_pos, err_word=self.err)
-        sa.validate_indices(self.idx, c.T, row_status=self.status, err_word=self.err)
         if ev is not None:
             ev[0].record()
         sa.sparse_attn_decode(self.q, self.k, self.v, self.idx, scale=c.eff_scale(), y=self.y,
-                              workspace=self.ws)
+                              workspace=self.ws, k_cur=self.k_cur, v_cur=self.v_cur,
+                              write_pos=self.write_pos, err_word=self.err,
+                              row_status=self.status)
         if ev is not None:
             ev[1].record()
 
@@ -194,8 +197,8 @@ class SparseDecode:
         return {"workload": c.name, "batch": c.B, "q_heads": c.Hq, "kv_heads": c.Hkv,
                 "head_dim": c.D, "cache_tokens": c.T, "top_k": c.K, "index_heads": c.I,
                 "padded_row_prob": c.pad_prob, "valid_selected": self.valid,
-                "step": "append current K/V + device index validation + split-K gather "
-                        "decode + combine"}
+                "step": "sparse_attn_decode: append current K/V + device index validation + "
+                        "stream-K gather decode + in-kernel combine (1 kernel + counter memset)"}
 
     def oracle_rows(self, rows):
         import oracle
@@ -209,7 +212,7 @@ class SparseDecode:
 
     def roofline(self, decode_ms, peaks):
         achieved = self.decode_bytes / (decode_ms * 1e-3) / 1e9
-        return {"bound": "hbm", "kernel": "sparse_attn_decode (gather + combine)",
+        return {"bound": "hbm", "kernel": "gather_stream_kernel (whole sparse_attn_decode call)",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),

@@ -152,7 +152,16 @@ int build_present_kv(const void* past_k, const void* cur_k, void* present_k,
  * len_b when err_word != NULL (row_status nullable, as in validate_indices);
  * malformed rows never fault: negative entries are skipped and entries
  * >= len_b are masked.
- * Workspace: sparse_attn_decode_workspace(p) bytes, 256-byte aligned.
+ * Fused append (dense cache only): when k_cur != NULL, the current token(s)
+ * k_cur / v_cur [B, Hkv, cur_len, D] are first written into the cache at
+ * positions write_pos[b] .. write_pos[b] + cur_len - 1 (write_pos: nullable
+ * device int64 [B], NULL meaning T - cur_len) -- build_present_kv's append
+ * mode -- and attention sees them there.  A write position outside
+ * [0, T - cur_len] sets SA_ERRBIT_WRITE_POS and skips that batch's write.
+ * Workspace: sparse_attn_decode_workspace(p) bytes, 256-byte aligned; its
+ * contents on entry do not matter (the call clears the counters it keeps
+ * there with an asynchronous memset).  Calls that share a workspace must not
+ * overlap on the GPU.
  */
 typedef struct {
   const void* q;
@@ -175,6 +184,10 @@ typedef struct {
   int64_t n_rope;
   uint32_t* err_word;
   uint8_t* row_status;
+  const void* k_cur;
+  const void* v_cur;
+  const int64_t* write_pos;
+  int64_t cur_len;
   void* workspace;
   size_t workspace_bytes;
 } sa_sparse_params;
@@ -188,7 +201,7 @@ int sparse_attn_decode(const sa_sparse_params* p, void* stream);
  * keys 0..i when causal; softcap as above, applied before the mask; fp32
  * softmax.  present_k / present_v (nullable, [B, Hkv, S, D]) receive exact
  * copies of k / v (past ++ current with an empty past).  dtype: SA_BF16 or
- * SA_F16 (tensor-core path, D == 128), or SA_F32 (reference-speed path).
+ * SA_F16, or SA_F32.  Workspace rules as for sparse_attn_decode.
  */
 typedef struct {
   const void* q;
@@ -219,7 +232,8 @@ int attn_prefill(const sa_prefill_params* p, void* stream);
  * written into the pool at token ctx_len[b] - 1.  A ctx_len outside
  * [1, max_pages*page_tokens] or a table entry outside [0, num_pages) sets
  * SA_ERRBIT_PAGE (err_word nullable) and is never dereferenced.
- * dtype SA_F16 / SA_BF16 / SA_F32; scale 0 means 1/sqrt(D).
+ * dtype SA_F16 / SA_BF16 / SA_F32; scale 0 means 1/sqrt(D).  Workspace rules
+ * as for sparse_attn_decode.
  */
 typedef struct {
   const void* q;

@@ -22,7 +22,7 @@ __all__ = [
     "load", "lib_path", "SAError", "status_string",
     "validate_indices", "build_present_kv", "sparse_attn_decode", "attn_prefill",
     "paged_attn_decode", "sparse_attn_decode_workspace", "attn_prefill_workspace",
-    "paged_attn_decode_workspace",
+    "paged_attn_decode_workspace", "new_workspace",
     "F32", "F16", "BF16", "FP8_E4M3_B64",
     "IDX_BELOW_SENTINEL", "IDX_AFTER_PADDING", "IDX_OUT_OF_RANGE", "IDX_NOT_INCREASING",
     "IDX_DUPLICATE", "IDX_ALL_PADDING", "ERRBIT_WRITE_POS", "ERRBIT_PAGE", "ERRBIT_TIMEOUT",
@@ -51,7 +51,9 @@ class SparseParams(C.Structure):
         ("kv_len", _p), ("past_len", _i64),
         ("scale", C.c_float), ("softcap", C.c_float),
         ("window", _i64), ("record_stride", _i64), ("n_rope", _i64),
-        ("err_word", _p), ("row_status", _p), ("workspace", _p), ("workspace_bytes", C.c_size_t),
+        ("err_word", _p), ("row_status", _p),
+        ("k_cur", _p), ("v_cur", _p), ("write_pos", _p), ("cur_len", _i64),
+        ("workspace", _p), ("workspace_bytes", C.c_size_t),
     ]
 
 
@@ -172,16 +174,22 @@ def _check(call, rc):
 _ws_cache: dict = {}
 
 
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A caller-owned workspace of at least ``nbytes`` (contents irrelevant)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
 def _workspace(nbytes: int, device, workspace=None):
-    """Caller-owned scratch: the given tensor, or a cached torch allocation."""
+    """Caller-owned scratch: the given tensor, or a cached torch allocation
+    per (device, stream)."""
     if nbytes == 0:
         return None, 0
     if workspace is not None:
         return workspace, workspace.numel() * workspace.element_size()
-    key = (device, torch.cuda.current_stream(device).cuda_stream)
+    key = (str(device), torch.cuda.current_stream(device).cuda_stream)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        buf = new_workspace(max(nbytes, 1 << 20), device)
         _ws_cache[key] = buf
     return buf, buf.numel()
 
@@ -231,7 +239,8 @@ def build_present_kv(cur_k, present_k, past_k=None, cur_v=None, present_v=None, 
 
 
 def _sparse_params(q, k_cache, v_cache, idx, y, *, scale, softcap, window, kv_len, past_len,
-                   causal, sink, err_word, row_status, n_rope=0, Dv=None):
+                   causal, sink, err_word, row_status, n_rope=0, Dv=None, k_cur=None,
+                   v_cur=None, write_pos=None):
     p = SparseParams()
     B, Hq, Sq, D = q.shape
     p.q, p.y = q.data_ptr(), _ptr(y)
@@ -264,6 +273,8 @@ def _sparse_params(q, k_cache, v_cache, idx, y, *, scale, softcap, window, kv_le
     p.window = int(window)
     p.err_word = _ptr(err_word)
     p.row_status = _ptr(row_status)
+    p.k_cur, p.v_cur, p.write_pos = _ptr(k_cur), _ptr(v_cur), _ptr(write_pos)
+    p.cur_len = 0 if k_cur is None else k_cur.shape[2]
     return p
 
 
@@ -274,7 +285,8 @@ def sparse_attn_decode_workspace(q, k_cache, v_cache, idx, **kw) -> int:
 
 def _sparse_defaults(kw):
     d = dict(scale=0.0, softcap=0.0, window=0, kv_len=None, past_len=0, causal=False, sink=None,
-             err_word=None, row_status=None, n_rope=0, Dv=None)
+             err_word=None, row_status=None, n_rope=0, Dv=None, k_cur=None, v_cur=None,
+             write_pos=None)
     d.update(kw)
     return d
 
@@ -286,12 +298,14 @@ def sparse_attn_decode(q, k_cache, v_cache, idx, *, y=None, workspace=None, stre
     ``n_rope``); ``idx [B,I,Sq,K]`` int32/int64.  Keyword options: scale,
     softcap, window, kv_len (int64 [B]), past_len, causal, sink (float32
     [Hq]), err_word (int32 [1], caller-zeroed), row_status (uint8 [B*I*Sq]),
-    n_rope, Dv.  Returns ``y [B,Hq,Sq,Dv]``."""
+    n_rope, Dv, and the fused append k_cur / v_cur ([B,Hkv,C,D]) with
+    write_pos (int64 [B], default T - C).  Returns ``y [B,Hq,Sq,Dv]``."""
     L = load()
     kw = _sparse_defaults(kw)
     for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("idx", idx),
                  ("kv_len", kw["kv_len"]), ("sink", kw["sink"]), ("err_word", kw["err_word"]),
-                 ("row_status", kw["row_status"])):
+                 ("row_status", kw["row_status"]), ("k_cur", kw["k_cur"]), ("v_cur", kw["v_cur"]),
+                 ("write_pos", kw["write_pos"])):
         _dev(t, n)
     B, Hq, Sq, D = q.shape
     Dv = kw["Dv"] if k_cache.dtype == torch.uint8 else v_cache.shape[3]

@@ -7,19 +7,33 @@
 // predecessor, in that order; the first failing column decides the code; a
 // row of only -1 is "all padding".
 //
-// GB300 mapping: one warp per row.  A chunk of 32*E columns sits in
-// registers (lane l owns E consecutive columns, loaded with 16-byte vector
-// loads when aligned), so every load of a row up to 32*E columns is in flight
-// at once.  The left-to-right scan becomes: a per-lane sequential scan of its
-// E columns given (a) whether any earlier lane saw a -1 (ballot prefix) and
-// (b) the previous lane's last value (shuffle); the row's first failing
-// column is the warp-wide minimum.  Codes are bit-identical to the
-// definition.
+// GB300 mapping: the left-to-right scan is evaluated in its exact per-column
+// form.  Assuming every earlier column passed, column j fails iff:
+//   v < -1                          -> below sentinel
+//   j > 0 and v[j-1] == -1          -> after padding
+//   v >= bound                      -> out of range
+//   j > 0 and v == v[j-1] / v < v[j-1] -> duplicate / not increasing
+// (a -1 passes).  The row's status is the code of the smallest failing
+// column, and "all padding" when no column fails and v[0] == -1.  Columns are
+// therefore independent: one warp per row loads its columns with 16-byte
+// vector loads, all in flight at once, and a warp max-reduction of the key
+// ~(column << 8 | code) picks the first failure.  Bit-identical codes.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace sa {
 
+__device__ __forceinline__ int column_rule(int64_t v, int64_t prev, int64_t col, int64_t bound) {
+  if (v == -1) return 0;
+  if (v < -1) return SA_IDX_BELOW_SENTINEL;
+  if (col > 0 && prev == -1) return SA_IDX_AFTER_PADDING;
+  if (v >= bound) return SA_IDX_OUT_OF_RANGE;
+  if (col > 0 && v == prev) return SA_IDX_DUPLICATE;
+  if (col > 0 && v < prev) return SA_IDX_NOT_INCREASING;
+  return 0;
+}
+
+// E consecutive columns per lane per step; 32*E columns per warp step.
 template <int E>
 __global__ void __launch_bounds__(256) validate_rows_kernel(ValidateArgs a) {
   const int lane = threadIdx.x & 31;
@@ -29,32 +43,27 @@ __global__ void __launch_bounds__(256) validate_rows_kernel(ValidateArgs a) {
   const int64_t b = row / a.rows_per_batch;
   const int64_t bound = a.bound_per_batch ? a.bound_per_batch[b] : a.bound;
   const int64_t base = row * K;
+  unsigned long long best = 0;  // max of ~key over failing columns (0 = none)
 
-  bool pad_seen = false;   // a -1 appeared in an earlier chunk
-  bool any_kept = false;   // a non -1 value appeared (row not all padding)
-  int64_t prev_last = 0;   // value of the column just before this chunk
-  int code = 0;
-
-  for (int64_t c0 = 0; c0 < K; c0 += 32 * E) {
-    const int64_t lc0 = c0 + static_cast<int64_t>(lane) * E;
+#pragma unroll 2
+  for (int64_t c0 = static_cast<int64_t>(lane) * E; c0 < K; c0 += 32 * E) {
     int64_t v[E];
-    const bool full = lc0 + E <= K;
-    if (full && a.vec_ok) {
+    if (c0 + E <= K && a.vec_ok) {
       if (a.is_i64) {
-        const int4* p = reinterpret_cast<const int4*>(static_cast<const int64_t*>(a.idx) + base + lc0);
+        const int4* p = reinterpret_cast<const int4*>(static_cast<const int64_t*>(a.idx) + base + c0);
 #pragma unroll
         for (int e = 0; e < E / 2; ++e) {
-          int4 w = __ldg(p + e);
-          v[2 * e] = (static_cast<int64_t>(static_cast<uint32_t>(w.y)) << 32) |
-                     static_cast<uint32_t>(w.x);
-          v[2 * e + 1] = (static_cast<int64_t>(static_cast<uint32_t>(w.w)) << 32) |
-                         static_cast<uint32_t>(w.z);
+          const int4 w = __ldg(p + e);
+          v[2 * e] = static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(w.y)) << 32) |
+                                          static_cast<uint32_t>(w.x));
+          v[2 * e + 1] = static_cast<int64_t>(
+              (static_cast<uint64_t>(static_cast<uint32_t>(w.w)) << 32) | static_cast<uint32_t>(w.z));
         }
       } else {
-        const int4* p = reinterpret_cast<const int4*>(static_cast<const int32_t*>(a.idx) + base + lc0);
+        const int4* p = reinterpret_cast<const int4*>(static_cast<const int32_t*>(a.idx) + base + c0);
 #pragma unroll
         for (int e = 0; e < E / 4; ++e) {
-          int4 w = __ldg(p + e);
+          const int4 w = __ldg(p + e);
           v[4 * e] = w.x;
           v[4 * e + 1] = w.y;
           v[4 * e + 2] = w.z;
@@ -63,67 +72,30 @@ __global__ void __launch_bounds__(256) validate_rows_kernel(ValidateArgs a) {
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        v[e] = (lc0 + e < K) ? load_index(a.idx, base + lc0 + e, a.is_i64) : -1;
-      }
+      for (int e = 0; e < E; ++e) v[e] = (c0 + e < K) ? load_index(a.idx, base + c0 + e, a.is_i64) : -1;
     }
-    int n_here = 0;  // columns this lane owns in this chunk
-    if (lc0 < K) n_here = static_cast<int>(K - lc0 < E ? K - lc0 : E);
-    bool has_pad = false, has_kept = false;
+    const int64_t before = c0 > 0 ? load_index(a.idx, base + c0 - 1, a.is_i64) : 0;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      if (e < n_here) {
-        has_pad |= (v[e] == -1);
-        has_kept |= (v[e] != -1);
-      }
-    }
-    const uint32_t pad_mask = __ballot_sync(0xffffffffu, has_pad);
-    const uint32_t kept_mask = __ballot_sync(0xffffffffu, has_kept);
-    // Value of the column before this lane's first column.
-    int64_t before = __shfl_up_sync(0xffffffffu, v[E - 1], 1);
-    if (lane == 0) before = prev_last;
-    const bool have_before = (lc0 > 0);
-    bool p = pad_seen || (pad_mask & ((1u << lane) - 1u)) != 0;
-
-    int my_code = 0;
-    int64_t my_col = INT64_MAX;
-    int64_t pv = before;
-    bool have_pv = have_before;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      if (e < n_here && my_code == 0) {
-        const int64_t x = v[e];
-        if (x == -1) {
-          p = true;
-        } else {
-          int c = 0;
-          if (x < -1) c = SA_IDX_BELOW_SENTINEL;
-          else if (p) c = SA_IDX_AFTER_PADDING;
-          else if (x >= bound) c = SA_IDX_OUT_OF_RANGE;
-          else if (have_pv && x == pv) c = SA_IDX_DUPLICATE;
-          else if (have_pv && x < pv) c = SA_IDX_NOT_INCREASING;
-          if (c) {
-            my_code = c;
-            my_col = lc0 + e;
-          }
-          pv = x;
-          have_pv = true;
+      const int64_t col = c0 + e;
+      if (col < K) {
+        const int code = column_rule(v[e], e == 0 ? before : v[e - 1], col, bound);
+        if (code) {
+          const unsigned long long k = ~((static_cast<unsigned long long>(col) << 8) |
+                                         static_cast<unsigned long long>(code));
+          best = best > k ? best : k;
         }
       }
     }
-    // First failing column across the warp.
-    const uint32_t fail_mask = __ballot_sync(0xffffffffu, my_code != 0);
-    if (fail_mask) {
-      const int first = __ffs(fail_mask) - 1;  // lanes own increasing columns
-      code = __shfl_sync(0xffffffffu, my_code, first);
-      break;
-    }
-    pad_seen = pad_seen || pad_mask != 0;
-    any_kept = any_kept || kept_mask != 0;
-    prev_last = __shfl_sync(0xffffffffu, v[E - 1], 31);
   }
-  if (code == 0 && !any_kept) code = SA_IDX_ALL_PADDING;
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, sh);
+    best = best > o ? best : o;
+  }
   if (lane == 0) {
+    int code = best ? static_cast<int>((~best) & 0xff) : 0;
+    if (code == 0 && load_index(a.idx, base, a.is_i64) == -1) code = SA_IDX_ALL_PADDING;
     if (a.row_status) a.row_status[row] = static_cast<uint8_t>(code);
     if (code && a.err_word) atomicOr(a.err_word, static_cast<uint32_t>(code));
   }
@@ -133,15 +105,8 @@ int launch_validate(const ValidateArgs& a, cudaStream_t st) {
   if (a.rows == 0) return 0;
   const int warps = 8;
   const unsigned grid = static_cast<unsigned>((a.rows + warps - 1) / warps);
-  if (a.K <= 32 * 4) {
-    validate_rows_kernel<4><<<grid, 32 * warps, 0, st>>>(a);
-  } else if (a.K <= 32 * 16) {
-    validate_rows_kernel<16><<<grid, 32 * warps, 0, st>>>(a);
-  } else if (a.is_i64 || a.K <= 32 * 32) {
-    validate_rows_kernel<32><<<grid, 32 * warps, 0, st>>>(a);
-  } else {
-    validate_rows_kernel<64><<<grid, 32 * warps, 0, st>>>(a);
-  }
+  if (a.K <= 32 * 4 || a.is_i64) validate_rows_kernel<4><<<grid, 32 * warps, 0, st>>>(a);
+  else validate_rows_kernel<8><<<grid, 32 * warps, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -47,9 +47,12 @@ struct GatherArgs {
   const void* v;
   void* y;                    // [B, Hq, Sq, Dv]
   const float* sink;          // nullable [Hq]
-  float* part_o;              // [units, splits, hpu, Dv] unnormalised partial outputs
-  float* part_ml;             // [units, splits, hpu, 2] running max (log2 units), sum
+  float* part_o;              // unnormalised partial outputs (layout per kernel)
+  float* part_ml;             // partial running max (log2 units) and sum
   uint32_t* err_word;
+  uint8_t* row_status;        // fused validation: per index row status (nullable)
+  unsigned long long* vword;  // fused validation words, one per index row (zeroed)
+  unsigned int* ticket;       // stream kernel: per-unit arrival counters (zeroed)
   // geometry
   int source;                 // KeySource
   int64_t B, Hq, Hkv, Sq, D, Dv;
@@ -57,9 +60,11 @@ struct GatherArgs {
   int64_t hpu;                // heads served per unit
   int64_t n_groups;           // units per (b, i): Hkv, or Hq when rows are per head
   int64_t units;              // B * n_groups * Sq
-  int64_t splits;             // key splits per unit
-  int64_t chunk;              // candidates per split
+  int64_t splits;             // SIMT path: key splits per unit
+  int64_t chunk;              // SIMT path: candidates per split
   int64_t n_cand;             // candidates per unit (upper bound for paged)
+  int64_t tiles_per_unit;     // stream kernel, sparse/dense: ceil(n_cand / 16)
+  int64_t tiles_per_warp;     // stream kernel, sparse/dense: tiles per warp range
   // sparse source
   const void* idx;
   int idx_is_i64;
@@ -68,6 +73,11 @@ struct GatherArgs {
   const int64_t* kv_len;      // nullable
   int64_t past_len;
   int causal;
+  // fused current-token append (sparse source; k_cur nullable)
+  const void* k_cur;          // [B, Hkv, C, D]
+  const void* v_cur;
+  const int64_t* write_pos;   // nullable: T - C
+  int64_t C;
   // paged source
   const int32_t* block_table;
   const int32_t* ctx_len;
@@ -78,11 +88,16 @@ struct GatherArgs {
   float inv_softcap;
 };
 
-int launch_gather_decode(const GatherArgs& a, int dtype, cudaStream_t st);
-bool gather_uses_mma(const GatherArgs& a, int dtype);
-// Resident CTAs per SM of the tensor-core gather kernel for this request.
-int gather_mma_occupancy(const GatherArgs& a, int dtype);
+// SIMT split-K kernel (any dtype, D <= 512) + its combine kernel.
+int launch_gather_simt(const GatherArgs& a, int dtype, cudaStream_t st);
 int launch_combine(const GatherArgs& a, int dtype, cudaStream_t st);
+// Whether the persistent tensor-core stream kernel serves this request.
+bool gather_uses_mma(const GatherArgs& a, int dtype);
+// Persistent tensor-core stream kernel (f16/bf16, D in {64,128,256}).
+size_t stream_smem_bytes(int D, int source, int64_t B);
+int stream_warps(int D);
+int stream_max_batch_paged();
+int launch_gather_stream(const GatherArgs& a, int dtype, int grid, cudaStream_t st);
 
 // ---- paged: write the new token into the pool -----------------------------------
 struct PagedAppendArgs {

@@ -51,38 +51,6 @@ DeviceShape device_shape() {
   return d;
 }
 
-// Splits of `n_cand` candidates per unit for the tensor-core kernel: chunks
-// are whole 64-key stages (at most 1024 keys); among the candidate chunk
-// sizes, pick the one whose CTA count fills the machine's resident slots in
-// the most even number of waves, preferring fewer splits on ties.
-void plan_mma_splits(int64_t units, int64_t n_cand, int64_t slots, int64_t* chunk_out,
-                     int64_t* splits_out) {
-  if (n_cand <= 0) {
-    *chunk_out = 64;
-    *splits_out = 1;
-    return;
-  }
-  double best = -1.0;
-  int64_t best_chunk = 64, best_splits = 1;
-  for (int64_t chunk = 64; chunk <= 1024; chunk += 64) {
-    const int64_t splits = (n_cand + chunk - 1) / chunk;
-    if (splits > 64) continue;
-    const double waves = static_cast<double>(units * splits) / static_cast<double>(slots);
-    const double eff = waves / ceil(waves);
-    // Few CTAs per SM leave latency uncovered; many splits cost combine traffic.
-    const double score = eff - 0.004 * static_cast<double>(splits) -
-                         (waves < 2.0 ? 0.25 * (2.0 - waves) : 0.0);
-    if (score > best + 1e-9) {
-      best = score;
-      best_chunk = chunk;
-      best_splits = splits;
-    }
-    if (chunk >= n_cand) break;
-  }
-  *chunk_out = best_chunk;
-  *splits_out = best_splits;
-}
-
 void plan_simt_splits(int64_t n_cand, int64_t* chunk_out, int64_t* splits_out) {
   int64_t splits = (n_cand + 255) / 256;
   if (splits < 1) splits = 1;
@@ -93,9 +61,29 @@ void plan_simt_splits(int64_t n_cand, int64_t* chunk_out, int64_t* splits_out) {
   *splits_out = (n_cand + chunk - 1) / chunk > 0 ? (n_cand + chunk - 1) / chunk : 1;
 }
 
-// Fill the geometry / split plan of a gather request whose source, shape and
-// tensor fields are already set.  Returns SA_OK or an error status.
-int plan_gather(sa::GatherArgs& g, int dtype) {
+// A gather request after planning: which kernel runs, its grid, and where
+// its scratch lives inside the caller's workspace.  The counter region
+// [0, clear_bytes) is cleared by the call itself.
+struct Plan {
+  sa::GatherArgs g;
+  bool stream = false;
+  int grid = 0;
+  bool fuse_validate = false;
+  size_t off_ticket = 0, off_vword = 0, clear_bytes = 0;
+  size_t off_part_o = 0, off_part_ml = 0, bytes = 0;
+};
+
+int stream_grid(const sa::GatherArgs& g, int dtype) {
+  static_cast<void>(dtype);
+  const int sms = device_shape().sms;
+  // one CTA per SM: the kernel's shared-memory ring fills the SM
+  return sms > 0 ? sms : 152;
+}
+
+// Fill the unit geometry, pick the kernel and lay out the workspace for a
+// request whose source, shape and tensor fields are set.
+int plan_gather(Plan& pl, int dtype, bool want_validate) {
+  sa::GatherArgs& g = pl.g;
   g.g = g.Hq / g.Hkv;
   if (g.source == sa::kSparse && g.I == g.Hq && g.g > 1) {
     g.n_groups = g.Hq;  // each query head has its own index row
@@ -105,46 +93,71 @@ int plan_gather(sa::GatherArgs& g, int dtype) {
     g.hpu = g.g;
   }
   g.units = g.B * g.n_groups * g.Sq;
-  if (sa::gather_uses_mma(g, dtype)) {
-    g.chunk = 1024;  // occupancy is insensitive to the few KB of index staging
-    const int64_t per_sm = sa::gather_mma_occupancy(g, dtype);
-    const int64_t slots = static_cast<int64_t>(device_shape().sms) * per_sm;
-    plan_mma_splits(g.units, g.n_cand, slots, &g.chunk, &g.splits);
+  pl.stream = sa::gather_uses_mma(g, dtype) &&
+              (g.source != sa::kPaged || g.B <= sa::stream_max_batch_paged());
+  const int64_t irows = g.B * g.I * g.Sq;
+  if (pl.stream) {
+    pl.grid = stream_grid(g, dtype);
+    const int64_t gw = static_cast<int64_t>(pl.grid) * sa::stream_warps(static_cast<int>(g.D));
+    g.tiles_per_unit = (g.n_cand + 15) / 16;
+    if (g.source != sa::kPaged) {
+      const int64_t nt = g.units * g.tiles_per_unit;
+      g.tiles_per_warp = (nt + gw - 1) / gw;
+      if (g.tiles_per_warp < 1) g.tiles_per_warp = 1;
+    }
+    pl.fuse_validate = want_validate && g.source == sa::kSparse && g.K > 0;
+    pl.off_ticket = 0;
+    pl.off_vword = align_up(static_cast<size_t>(g.units) * 4);
+    pl.clear_bytes = pl.off_vword + (pl.fuse_validate ? static_cast<size_t>(irows) * 8 : 0);
+    pl.off_part_o = align_up(pl.clear_bytes);
+    const size_t parts = static_cast<size_t>(gw) * 2 * g.hpu;
+    pl.off_part_ml = pl.off_part_o + align_up(parts * g.D * sizeof(float));
+    pl.bytes = pl.off_part_ml + align_up(parts * 2 * sizeof(float));
   } else {
     if ((g.D + 31) / 32 > 16) return SA_ERR_UNSUPPORTED;
     plan_simt_splits(g.n_cand, &g.chunk, &g.splits);
+    if (g.splits > 1) {
+      const size_t parts = static_cast<size_t>(g.units * g.splits * g.hpu);
+      pl.off_part_o = 0;
+      pl.off_part_ml = align_up(parts * g.Dv * sizeof(float));
+      pl.bytes = pl.off_part_ml + align_up(parts * 2 * sizeof(float));
+    }
   }
   return SA_OK;
 }
 
-size_t gather_workspace(const sa::GatherArgs& g) {
-  if (g.splits <= 1) return 0;
-  const size_t parts = static_cast<size_t>(g.units * g.splits * g.hpu);
-  return align_up(parts * g.Dv * sizeof(float)) + align_up(parts * 2 * sizeof(float));
+int check_workspace(const Plan& pl, void* ws, size_t ws_bytes) {
+  if (pl.bytes == 0) return SA_OK;
+  if (!ws || ws_bytes < pl.bytes) return SA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return SA_ERR_ALIGN;
+  return SA_OK;
 }
 
-void carve_gather_workspace(sa::GatherArgs& g, void* ws) {
-  if (g.splits <= 1) {
-    g.part_o = nullptr;
-    g.part_ml = nullptr;
-    return;
-  }
-  const size_t parts = static_cast<size_t>(g.units * g.splits * g.hpu);
+int run_plan(Plan& pl, void* ws, int dtype, cudaStream_t st) {
+  sa::GatherArgs& g = pl.g;
   char* base = static_cast<char*>(ws);
-  g.part_o = reinterpret_cast<float*>(base);
-  g.part_ml = reinterpret_cast<float*>(base + align_up(parts * g.Dv * sizeof(float)));
-}
-
-int run_gather(const sa::GatherArgs& g, int dtype, cudaStream_t st) {
-  if (sa::launch_gather_decode(g, dtype, st) != 0) return SA_ERR_LAUNCH;
+  if (pl.bytes > 0) {
+    g.part_o = reinterpret_cast<float*>(base + pl.off_part_o);
+    g.part_ml = reinterpret_cast<float*>(base + pl.off_part_ml);
+  }
+  if (pl.stream) {
+    g.ticket = reinterpret_cast<unsigned int*>(base + pl.off_ticket);
+    g.vword = pl.fuse_validate ? reinterpret_cast<unsigned long long*>(base + pl.off_vword)
+                               : nullptr;
+    if (pl.clear_bytes && cudaMemsetAsync(base, 0, pl.clear_bytes, st) != cudaSuccess)
+      return SA_ERR_LAUNCH;
+    return sa::launch_gather_stream(g, dtype, pl.grid, st) == 0 ? SA_OK : SA_ERR_LAUNCH;
+  }
+  if (sa::launch_gather_simt(g, dtype, st) != 0) return SA_ERR_LAUNCH;
   if (sa::launch_combine(g, dtype, st) != 0) return SA_ERR_LAUNCH;
   return SA_OK;
 }
 
 // ---- sparse decode: checks + plan ----------------------------------------------
 
-int check_sparse(const sa_sparse_params* p) {
-  if (!p || !p->q || !p->k_cache || !p->y) return SA_ERR_NULL;
+// `query` = 1 for a workspace-size query, which needs no output pointer.
+int check_sparse(const sa_sparse_params* p, int query = 0) {
+  if (!p || !p->q || !p->k_cache || (!p->y && !query)) return SA_ERR_NULL;
   if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->Sq <= 0 || p->D <= 0 || p->T <= 0)
     return SA_ERR_SHAPE;
   if (p->Hq % p->Hkv != 0) return SA_ERR_SHAPE;
@@ -159,6 +172,7 @@ int check_sparse(const sa_sparse_params* p) {
   if (p->B * p->Hkv * p->T >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
   if (!std::isfinite(p->scale) || !std::isfinite(p->softcap) || p->softcap < 0.f)
     return SA_ERR_SHAPE;
+  if (p->k_cur && (!p->v_cur || p->cur_len <= 0 || p->cur_len > p->T)) return SA_ERR_SHAPE;
   const size_t es = dtype_bytes(p->q_dtype);
   const size_t qbytes = static_cast<size_t>(p->B * p->Hq * p->Sq * p->D) * es;
   const size_t ybytes = static_cast<size_t>(p->B * p->Hq * p->Sq * p->Dv) * es;
@@ -171,7 +185,8 @@ int check_sparse(const sa_sparse_params* p) {
   return SA_OK;
 }
 
-int sparse_plan(const sa_sparse_params* p, sa::GatherArgs& g) {
+int sparse_plan(const sa_sparse_params* p, Plan& pl) {
+  sa::GatherArgs& g = pl.g;
   memset(&g, 0, sizeof(g));
   g.q = p->q;
   g.k = p->k_cache;
@@ -200,10 +215,16 @@ int sparse_plan(const sa_sparse_params* p, sa::GatherArgs& g) {
   g.scale_log2 = scale * 1.4426950408889634f;
   g.softcap = p->softcap;
   g.inv_softcap = p->softcap != 0.f ? 1.0f / p->softcap : 0.f;
-  int rc = plan_gather(g, p->q_dtype);
+  g.k_cur = p->k_cur;
+  g.v_cur = p->v_cur;
+  g.write_pos = p->write_pos;
+  g.C = p->k_cur ? p->cur_len : 0;
+  g.row_status = p->row_status;
+  int rc = plan_gather(pl, p->q_dtype, p->err_word || p->row_status);
   if (rc != SA_OK) return rc;
-  if (sa::gather_uses_mma(g, p->q_dtype) &&
-      !(aligned16(p->k_cache) && aligned16(p->v_cache)))
+  if (pl.stream && !(aligned16(p->k_cache) && aligned16(p->v_cache)))
+    return SA_ERR_ALIGN;
+  if (pl.stream && p->k_cur && !(aligned16(p->k_cur) && aligned16(p->v_cur)))
     return SA_ERR_ALIGN;
   return SA_OK;
 }
@@ -316,45 +337,65 @@ int build_present_kv(const void* past_k, const void* cur_k, void* present_k, con
 }
 
 size_t sparse_attn_decode_workspace(const sa_sparse_params* p) {
-  if (check_sparse(p) != SA_OK) return 0;
-  sa::GatherArgs g;
-  if (sparse_plan(p, g) != SA_OK) return 0;
-  return gather_workspace(g);
+  if (check_sparse(p, 1) != SA_OK) return 0;
+  Plan pl;
+  if (sparse_plan(p, pl) != SA_OK) return 0;
+  return pl.bytes;
 }
 
 int sparse_attn_decode(const sa_sparse_params* p, void* stream) {
   int rc = check_sparse(p);
   if (rc != SA_OK) return rc;
-  sa::GatherArgs g;
-  rc = sparse_plan(p, g);
+  Plan pl;
+  rc = sparse_plan(p, pl);
   if (rc != SA_OK) return rc;
-  const size_t need = gather_workspace(g);
-  if (need > 0 && (!p->workspace || p->workspace_bytes < need)) return SA_ERR_WORKSPACE;
-  if (need > 0 && reinterpret_cast<uintptr_t>(p->workspace) % kAlign) return SA_ERR_ALIGN;
-  carve_gather_workspace(g, p->workspace);
+  rc = check_workspace(pl, p->workspace, p->workspace_bytes);
+  if (rc != SA_OK) return rc;
   cudaStream_t st = as_stream(stream);
-  if (p->K > 0 && (p->err_word || p->row_status)) {
-    sa::ValidateArgs v;
-    v.idx = p->idx;
-    v.is_i64 = p->idx_is_i64 ? 1 : 0;
-    const size_t esz = p->idx_is_i64 ? 8 : 4;
-    v.vec_ok = aligned16(p->idx) && ((p->K * static_cast<int64_t>(esz)) % 16 == 0);
-    v.rows = p->B * p->I * p->Sq;
-    v.rows_per_batch = p->I * p->Sq;
-    v.K = p->K;
-    v.bound_per_batch = p->kv_len;
-    v.bound = p->T;
-    v.row_status = p->row_status;
-    v.err_word = p->err_word;
-    if (sa::launch_validate(v, st) != 0) return SA_ERR_LAUNCH;
+  if (!pl.stream) {
+    // separate steps on the SIMT path: append, then validation, then gather
+    if (p->k_cur) {
+      sa::PresentArgs a;
+      memset(&a, 0, sizeof(a));
+      a.past[0] = a.present[0] = const_cast<void*>(p->k_cache);
+      a.past[1] = a.present[1] = const_cast<void*>(p->v_cache);
+      a.cur[0] = p->k_cur;
+      a.cur[1] = p->v_cur;
+      a.n_tensors = 2;
+      a.esz = static_cast<int>(dtype_bytes(p->q_dtype));
+      a.B = p->B;
+      a.H = p->Hkv;
+      a.C = p->cur_len;
+      a.D = p->D;
+      a.stride = p->T;
+      a.write_pos = p->write_pos;
+      a.err_word = p->err_word;
+      if (!p->write_pos) return SA_ERR_UNSUPPORTED;  // SIMT path appends at explicit positions
+      if (sa::launch_present(a, st) != 0) return SA_ERR_LAUNCH;
+    }
+    if (p->K > 0 && (p->err_word || p->row_status)) {
+      sa::ValidateArgs v;
+      v.idx = p->idx;
+      v.is_i64 = p->idx_is_i64 ? 1 : 0;
+      const size_t esz = p->idx_is_i64 ? 8 : 4;
+      v.vec_ok = aligned16(p->idx) && ((p->K * static_cast<int64_t>(esz)) % 16 == 0);
+      v.rows = p->B * p->I * p->Sq;
+      v.rows_per_batch = p->I * p->Sq;
+      v.K = p->K;
+      v.bound_per_batch = p->kv_len;
+      v.bound = p->T;
+      v.row_status = p->row_status;
+      v.err_word = p->err_word;
+      if (sa::launch_validate(v, st) != 0) return SA_ERR_LAUNCH;
+    }
   }
-  return run_gather(g, p->q_dtype, st);
+  return run_plan(pl, p->workspace, p->q_dtype, st);
 }
 
 // ---- prefill ---------------------------------------------------------------------
 
-static int check_prefill(const sa_prefill_params* p) {
-  if (!p || !p->q || !p->k || !p->v || !p->y) return SA_ERR_NULL;
+static int check_prefill(const sa_prefill_params* p, int query = 0) {
+  if (!p || !p->q || !p->k || !p->v || (!p->y && !query)) return SA_ERR_NULL;
   if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->S <= 0 || p->D <= 0) return SA_ERR_SHAPE;
   if (p->Hq % p->Hkv != 0) return SA_ERR_SHAPE;
   if (dtype_bytes(p->dtype) == 0) return SA_ERR_DTYPE;
@@ -377,7 +418,7 @@ static int check_prefill(const sa_prefill_params* p) {
   return SA_OK;
 }
 
-static void prefill_plan(const sa_prefill_params* p, sa::GatherArgs& g) {
+static void prefill_args(const sa_prefill_params* p, sa::GatherArgs& g) {
   memset(&g, 0, sizeof(g));
   g.q = p->q;
   g.k = p->k;
@@ -402,27 +443,24 @@ static void prefill_plan(const sa_prefill_params* p, sa::GatherArgs& g) {
 }
 
 size_t attn_prefill_workspace(const sa_prefill_params* p) {
-  if (check_prefill(p) != SA_OK) return 0;
-  sa::GatherArgs g;
-  prefill_plan(p, g);
-  if (plan_gather(g, p->dtype) != SA_OK) return 0;
-  return gather_workspace(g);
+  if (check_prefill(p, 1) != SA_OK) return 0;
+  Plan pl;
+  prefill_args(p, pl.g);
+  if (plan_gather(pl, p->dtype, false) != SA_OK) return 0;
+  return pl.bytes;
 }
 
 int attn_prefill(const sa_prefill_params* p, void* stream) {
   int rc = check_prefill(p);
   if (rc != SA_OK) return rc;
   cudaStream_t st = as_stream(stream);
-  sa::GatherArgs g;
-  prefill_plan(p, g);
-  rc = plan_gather(g, p->dtype);
+  Plan pl;
+  prefill_args(p, pl.g);
+  rc = plan_gather(pl, p->dtype, false);
   if (rc != SA_OK) return rc;
-  if (sa::gather_uses_mma(g, p->dtype) && !(aligned16(p->k) && aligned16(p->v)))
-    return SA_ERR_ALIGN;
-  const size_t need = gather_workspace(g);
-  if (need > 0 && (!p->workspace || p->workspace_bytes < need)) return SA_ERR_WORKSPACE;
-  if (need > 0 && reinterpret_cast<uintptr_t>(p->workspace) % kAlign) return SA_ERR_ALIGN;
-  carve_gather_workspace(g, p->workspace);
+  if (pl.stream && !(aligned16(p->k) && aligned16(p->v))) return SA_ERR_ALIGN;
+  rc = check_workspace(pl, p->workspace, p->workspace_bytes);
+  if (rc != SA_OK) return rc;
   if (p->present_k || p->present_v) {
     const void* cur_k = p->present_k ? p->k : p->v;
     void* out_k = p->present_k ? p->present_k : p->present_v;
@@ -432,13 +470,14 @@ int attn_prefill(const sa_prefill_params* p, void* stream) {
                           0, p->S, p->D, p->S, nullptr, nullptr, stream);
     if (rc != SA_OK) return rc;
   }
-  return run_gather(g, p->dtype, st);
+  return run_plan(pl, p->workspace, p->dtype, st);
 }
 
 // ---- paged decode ------------------------------------------------------------------
 
-static int check_paged(const sa_paged_params* p) {
-  if (!p || !p->q || !p->k_pool || !p->v_pool || !p->block_table || !p->ctx_len || !p->y)
+static int check_paged(const sa_paged_params* p, int query = 0) {
+  if (!p || !p->q || !p->k_pool || !p->v_pool || !p->block_table || !p->ctx_len ||
+      (!p->y && !query))
     return SA_ERR_NULL;
   if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0 || p->page_tokens <= 0 ||
       p->max_pages <= 0 || p->num_pages <= 0)
@@ -456,7 +495,7 @@ static int check_paged(const sa_paged_params* p) {
   return SA_OK;
 }
 
-static void paged_plan(const sa_paged_params* p, sa::GatherArgs& g) {
+static void paged_args(const sa_paged_params* p, sa::GatherArgs& g) {
   memset(&g, 0, sizeof(g));
   g.q = p->q;
   g.k = p->k_pool;
@@ -482,27 +521,24 @@ static void paged_plan(const sa_paged_params* p, sa::GatherArgs& g) {
 }
 
 size_t paged_attn_decode_workspace(const sa_paged_params* p) {
-  if (check_paged(p) != SA_OK) return 0;
-  sa::GatherArgs g;
-  paged_plan(p, g);
-  if (plan_gather(g, p->dtype) != SA_OK) return 0;
-  return gather_workspace(g);
+  if (check_paged(p, 1) != SA_OK) return 0;
+  Plan pl;
+  paged_args(p, pl.g);
+  if (plan_gather(pl, p->dtype, false) != SA_OK) return 0;
+  return pl.bytes;
 }
 
 int paged_attn_decode(const sa_paged_params* p, void* stream) {
   int rc = check_paged(p);
   if (rc != SA_OK) return rc;
   cudaStream_t st = as_stream(stream);
-  sa::GatherArgs g;
-  paged_plan(p, g);
-  rc = plan_gather(g, p->dtype);
+  Plan pl;
+  paged_args(p, pl.g);
+  rc = plan_gather(pl, p->dtype, false);
   if (rc != SA_OK) return rc;
-  if (sa::gather_uses_mma(g, p->dtype) && !(aligned16(p->k_pool) && aligned16(p->v_pool)))
-    return SA_ERR_ALIGN;
-  const size_t need = gather_workspace(g);
-  if (need > 0 && (!p->workspace || p->workspace_bytes < need)) return SA_ERR_WORKSPACE;
-  if (need > 0 && reinterpret_cast<uintptr_t>(p->workspace) % kAlign) return SA_ERR_ALIGN;
-  carve_gather_workspace(g, p->workspace);
+  if (pl.stream && !(aligned16(p->k_pool) && aligned16(p->v_pool))) return SA_ERR_ALIGN;
+  rc = check_workspace(pl, p->workspace, p->workspace_bytes);
+  if (rc != SA_OK) return rc;
   if (p->k_new || p->v_new) {
     sa::PagedAppendArgs a;
     a.k_pool = p->k_pool;
@@ -521,7 +557,7 @@ int paged_attn_decode(const sa_paged_params* p, void* stream) {
     a.err_word = p->err_word;
     if (sa::launch_paged_append(a, st) != 0) return SA_ERR_LAUNCH;
   }
-  return run_gather(g, p->dtype, st);
+  return run_plan(pl, p->workspace, p->dtype, st);
 }
 
 }  // extern "C"

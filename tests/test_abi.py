@@ -114,3 +114,11 @@ def test_host_checks_reject_bad_requests_without_launching(lib):
     assert lib.attn_prefill(C.byref(q), None) == -1
     g = sa.PagedParams()
     assert lib.paged_attn_decode(C.byref(g), None) == -1
+
+
+def test_workspace_query_needs_no_output_pointer(lib):
+    p = sa.SparseParams()
+    p.q, p.k_cache, p.v_cache, p.idx = 0x10000, 0x20000, 0x30000, 0x50000
+    p.B, p.Hq, p.Hkv, p.Sq, p.D, p.Dv, p.T, p.I, p.K = 4, 64, 8, 1, 128, 128, 8192, 8, 2048
+    p.q_dtype = p.kv_dtype = sa.BF16
+    assert lib.sparse_attn_decode_workspace(C.byref(p)) > 0

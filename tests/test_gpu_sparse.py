@@ -265,3 +265,55 @@ def test_full_size_sparse_bf16_sampled_rows(cuda_lib):
                                       inp["v_cache"][b:b + 1, kvh:kvh + 1].cpu(),
                                       scale=c.eff_scale())
         assert_close(to64(y[b, hs]), ref, y.dtype, f"b={b} kvh={kvh}")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_fused_append_matches_append_then_decode(cuda_lib, dt):
+    """k_cur/v_cur written at write_pos inside the decode call: the output equals
+    the oracle over the appended cache, and the cache holds the new rows."""
+    c = synth.sparse_bf16(dtype=dt, B=3, Hq=16, Hkv=2, T=600, K=200, I=2, pad_prob=0.2,
+                          pad_max=30)
+    inp = synth.make_sparse_inputs(c, seed=71)
+    k_cur = synth.normal((c.B, c.Hkv, 2, c.D), dt, 72)
+    v_cur = synth.normal((c.B, c.Hkv, 2, c.D), dt, 73)
+    wp = torch.tensor([598, 100, 0], dtype=torch.int64)
+    # make sure the selected sets include the appended positions
+    idx = inp["idx"].clone()
+    for b, w in enumerate(wp.tolist()):
+        row = sorted(set(idx[b, 0, 0][idx[b, 0, 0] >= 0].tolist()[:-2]) | {w, w + 1})
+        idx[b, 0, 0] = -1
+        idx[b, 0, 0, :len(row)] = torch.tensor(row)
+    kc, vc = inp["k_cache"].to(DEV), inp["v_cache"].to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = cuda_lib.sparse_attn_decode(inp["q"].to(DEV), kc, vc, idx.to(DEV), scale=c.eff_scale(),
+                                    k_cur=k_cur.to(DEV), v_cur=v_cur.to(DEV),
+                                    write_pos=wp.to(DEV), err_word=err)
+    torch.cuda.synchronize()
+    ek = oracle.present_append(inp["k_cache"], k_cur, wp)
+    ev = oracle.present_append(inp["v_cache"], v_cur, wp)
+    assert torch.equal(kc.cpu(), ek) and torch.equal(vc.cpu(), ev)
+    ref = oracle.sparse_attention(inp["q"], idx, ek, ev, scale=c.eff_scale())
+    assert_close(to64(y), ref, y.dtype, "fused append")
+    assert int(err.item()) == 0
+
+
+def test_workspace_contents_on_entry_do_not_matter(cuda_lib):
+    c = synth.sparse_bf16(B=4, Hq=64, Hkv=8, T=2048, K=700, I=8, pad_prob=0.3, pad_max=100)
+    inp = {k: v.to(DEV) for k, v in synth.make_sparse_inputs(c, seed=81).items()}
+    err0 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    st0 = torch.zeros(c.B * c.I, dtype=torch.uint8, device=DEV)
+    need = cuda_lib.sparse_attn_decode_workspace(inp["q"], inp["k_cache"], inp["v_cache"],
+                                                 inp["idx"], scale=c.eff_scale(), err_word=err0,
+                                                 row_status=st0)
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device=DEV)
+    ys = []
+    for fill in (0xAB, 0x00, 0xFF):
+        ws.fill_(fill)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        st = torch.full((c.B * c.I,), 99, dtype=torch.uint8, device=DEV)
+        ys.append(cuda_lib.sparse_attn_decode(inp["q"], inp["k_cache"], inp["v_cache"],
+                                              inp["idx"], scale=c.eff_scale(), workspace=ws,
+                                              err_word=err, row_status=st))
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0 and int(st.max().item()) == 0
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
