@@ -4,7 +4,7 @@ Default workload: selected-token decode, bf16, B32 Hq64 Hkv8 D128, cache
 8192 tokens, 2048 selected indices per (batch, KV head) row (about 5% of rows
 padded).  One step = one sparse_attn_decode call that appends the current
 token's K/V into the cache, validates the index rows on the device, gathers
-the selected K/V rows and merges the partial softmax results (one kernel).
+the selected K/V rows and merges the partial softmax results (three kernels).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
@@ -159,7 +159,7 @@ class SparseDecode:
         cur_bytes = 2 * self.k_cur.numel() * es
         self.decode_bytes = (self.valid * 2 * c.D * es + self.idx.numel() * self.idx.element_size()
                              + self.q.numel() * es + self.y.numel() * es + 2 * cur_bytes)
-        self.launches_per_step = 1  # one fused kernel (plus a small counter memset)
+        self.launches_per_step = 3  # plan (validate + positions + append), gather, combine
         # host copies for the end-to-end leg
         self.h_q = self.q.cpu().pin_memory()
         self.h_idx = self.idx.cpu().pin_memory()
@@ -197,8 +197,9 @@ class SparseDecode:
         return {"workload": c.name, "batch": c.B, "q_heads": c.Hq, "kv_heads": c.Hkv,
                 "head_dim": c.D, "cache_tokens": c.T, "top_k": c.K, "index_heads": c.I,
                 "padded_row_prob": c.pad_prob, "valid_selected": self.valid,
-                "step": "sparse_attn_decode: append current K/V + device index validation + "
-                        "stream-K gather decode + in-kernel combine (1 kernel + counter memset)"}
+                "step": "one sparse_attn_decode call: plan kernel (index validation, candidate "
+                        "positions, current-token append) + stream-K gather decode + combine of "
+                        "split units (3 kernels)"}
 
     def oracle_rows(self, rows):
         import oracle
@@ -212,7 +213,7 @@ class SparseDecode:
 
     def roofline(self, decode_ms, peaks):
         achieved = self.decode_bytes / (decode_ms * 1e-3) / 1e9
-        return {"bound": "hbm", "kernel": "gather_stream_kernel (whole sparse_attn_decode call)",
+        return {"bound": "hbm", "kernel": "sparse_attn_decode call (plan + gather_stream + combine)",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),

@@ -37,6 +37,32 @@ struct PresentArgs {
 };
 int launch_present(const PresentArgs& a, cudaStream_t st);
 
+// ---- per index row plan: validation + candidate positions + append ----------------
+struct PlanArgs {
+  const void* idx;            // [B, I, Sq, K]
+  int idx_is_i64;
+  int vec_ok;                 // 16-byte vector loads are legal
+  int plan_rows;              // 0: append blocks only
+  int validate;               // write row_status / err_word
+  int causal;
+  int64_t B, I, Sq, K, T, window, past_len;
+  int64_t n_cand_pad;         // positions per row: (window + K) rounded up to 16
+  const int64_t* kv_len;      // nullable
+  int32_t* pos;               // [B*I*Sq, n_cand_pad] cache positions or -1
+  uint8_t* row_status;
+  uint32_t* err_word;
+  // fused append of the current token(s) (append_blocks == 0: none)
+  const void* k_cur;
+  const void* v_cur;
+  void* k_cache;
+  void* v_cache;
+  const int64_t* write_pos;   // nullable: T - C
+  int64_t Hkv, C, D;
+  int esz;
+  int append_blocks;
+};
+int launch_plan(const PlanArgs& a, cudaStream_t st);
+
 // ---- gather decode (sparse and paged) ------------------------------------------
 enum KeySource : int { kSparse = 0, kPaged = 1, kDense = 2 };
 
@@ -50,9 +76,6 @@ struct GatherArgs {
   float* part_o;              // unnormalised partial outputs (layout per kernel)
   float* part_ml;             // partial running max (log2 units) and sum
   uint32_t* err_word;
-  uint8_t* row_status;        // fused validation: per index row status (nullable)
-  unsigned long long* vword;  // fused validation words, one per index row (zeroed)
-  unsigned int* ticket;       // stream kernel: per-unit arrival counters (zeroed)
   // geometry
   int source;                 // KeySource
   int64_t B, Hq, Hkv, Sq, D, Dv;
@@ -65,6 +88,10 @@ struct GatherArgs {
   int64_t n_cand;             // candidates per unit (upper bound for paged)
   int64_t tiles_per_unit;     // stream kernel, sparse/dense: ceil(n_cand / 16)
   int64_t tiles_per_warp;     // stream kernel, sparse/dense: tiles per warp range
+  const int32_t* pos;         // stream kernel, sparse: planned cache positions
+  int64_t n_cand_pad;         // positions per planned row
+  int64_t* meta;              // stream kernel -> combine: [0] tiles per warp
+  int32_t* pref_out;          // stream kernel -> combine (paged): tile prefix [B+1]
   // sparse source
   const void* idx;
   int idx_is_i64;
@@ -98,6 +125,8 @@ size_t stream_smem_bytes(int D, int source, int64_t B);
 int stream_warps(int D);
 int stream_max_batch_paged();
 int launch_gather_stream(const GatherArgs& a, int dtype, int grid, cudaStream_t st);
+// Merge of the units the stream kernel split across warps.
+int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st);
 
 // ---- paged: write the new token into the pool -----------------------------------
 struct PagedAppendArgs {

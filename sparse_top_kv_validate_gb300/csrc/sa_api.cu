@@ -62,27 +62,24 @@ void plan_simt_splits(int64_t n_cand, int64_t* chunk_out, int64_t* splits_out) {
 }
 
 // A gather request after planning: which kernel runs, its grid, and where
-// its scratch lives inside the caller's workspace.  The counter region
-// [0, clear_bytes) is cleared by the call itself.
+// its scratch lives inside the caller's workspace (nothing in it needs to be
+// initialised: every word is written before it is read).
 struct Plan {
   sa::GatherArgs g;
   bool stream = false;
   int grid = 0;
-  bool fuse_validate = false;
-  size_t off_ticket = 0, off_vword = 0, clear_bytes = 0;
-  size_t off_part_o = 0, off_part_ml = 0, bytes = 0;
+  size_t off_pos = 0, off_meta = 0, off_part_o = 0, off_part_ml = 0, bytes = 0;
 };
 
-int stream_grid(const sa::GatherArgs& g, int dtype) {
-  static_cast<void>(dtype);
+int stream_grid() {
   const int sms = device_shape().sms;
-  // one CTA per SM: the kernel's shared-memory ring fills the SM
+  // one CTA per SM: the kernel's shared-memory rings fill the SM
   return sms > 0 ? sms : 152;
 }
 
 // Fill the unit geometry, pick the kernel and lay out the workspace for a
 // request whose source, shape and tensor fields are set.
-int plan_gather(Plan& pl, int dtype, bool want_validate) {
+int plan_gather(Plan& pl, int dtype) {
   sa::GatherArgs& g = pl.g;
   g.g = g.Hq / g.Hkv;
   if (g.source == sa::kSparse && g.I == g.Hq && g.g > 1) {
@@ -97,22 +94,32 @@ int plan_gather(Plan& pl, int dtype, bool want_validate) {
               (g.source != sa::kPaged || g.B <= sa::stream_max_batch_paged());
   const int64_t irows = g.B * g.I * g.Sq;
   if (pl.stream) {
-    pl.grid = stream_grid(g, dtype);
+    pl.grid = stream_grid();
     const int64_t gw = static_cast<int64_t>(pl.grid) * sa::stream_warps(static_cast<int>(g.D));
     g.tiles_per_unit = (g.n_cand + 15) / 16;
+    g.n_cand_pad = g.tiles_per_unit * 16;
+    if (g.units * g.tiles_per_unit >= (int64_t(1) << 31) ||
+        g.B * g.Hkv * ((g.max_pages * g.page_tokens + 15) / 16) >= (int64_t(1) << 31) ||
+        irows * g.n_cand_pad >= (int64_t(1) << 40))
+      return SA_ERR_UNSUPPORTED;
     if (g.source != sa::kPaged) {
       const int64_t nt = g.units * g.tiles_per_unit;
       g.tiles_per_warp = (nt + gw - 1) / gw;
       if (g.tiles_per_warp < 1) g.tiles_per_warp = 1;
     }
-    pl.fuse_validate = want_validate && g.source == sa::kSparse && g.K > 0;
-    pl.off_ticket = 0;
-    pl.off_vword = align_up(static_cast<size_t>(g.units) * 4);
-    pl.clear_bytes = pl.off_vword + (pl.fuse_validate ? static_cast<size_t>(irows) * 8 : 0);
-    pl.off_part_o = align_up(pl.clear_bytes);
+    size_t off = 0;
+    if (g.source == sa::kSparse) {
+      pl.off_pos = off;
+      off += align_up(static_cast<size_t>(irows * g.n_cand_pad) * sizeof(int32_t));
+    }
+    pl.off_meta = off;
+    off += align_up(sizeof(int64_t) + static_cast<size_t>(g.B + 1) * sizeof(int32_t));
     const size_t parts = static_cast<size_t>(gw) * 2 * g.hpu;
-    pl.off_part_ml = pl.off_part_o + align_up(parts * g.D * sizeof(float));
-    pl.bytes = pl.off_part_ml + align_up(parts * 2 * sizeof(float));
+    pl.off_part_o = off;
+    off += align_up(parts * g.D * sizeof(float));
+    pl.off_part_ml = off;
+    off += align_up(parts * 2 * sizeof(float));
+    pl.bytes = off;
   } else {
     if ((g.D + 31) / 32 > 16) return SA_ERR_UNSUPPORTED;
     plan_simt_splits(g.n_cand, &g.chunk, &g.splits);
@@ -133,20 +140,26 @@ int check_workspace(const Plan& pl, void* ws, size_t ws_bytes) {
   return SA_OK;
 }
 
-int run_plan(Plan& pl, void* ws, int dtype, cudaStream_t st) {
+// Carve the workspace; for the stream path return the planned-position area.
+void carve(Plan& pl, void* ws) {
   sa::GatherArgs& g = pl.g;
   char* base = static_cast<char*>(ws);
-  if (pl.bytes > 0) {
-    g.part_o = reinterpret_cast<float*>(base + pl.off_part_o);
-    g.part_ml = reinterpret_cast<float*>(base + pl.off_part_ml);
-  }
+  if (pl.bytes == 0) return;
+  g.part_o = reinterpret_cast<float*>(base + pl.off_part_o);
+  g.part_ml = reinterpret_cast<float*>(base + pl.off_part_ml);
   if (pl.stream) {
-    g.ticket = reinterpret_cast<unsigned int*>(base + pl.off_ticket);
-    g.vword = pl.fuse_validate ? reinterpret_cast<unsigned long long*>(base + pl.off_vword)
-                               : nullptr;
-    if (pl.clear_bytes && cudaMemsetAsync(base, 0, pl.clear_bytes, st) != cudaSuccess)
-      return SA_ERR_LAUNCH;
-    return sa::launch_gather_stream(g, dtype, pl.grid, st) == 0 ? SA_OK : SA_ERR_LAUNCH;
+    g.meta = reinterpret_cast<int64_t*>(base + pl.off_meta);
+    g.pref_out = reinterpret_cast<int32_t*>(base + pl.off_meta + sizeof(int64_t));
+    if (g.source == sa::kSparse) g.pos = reinterpret_cast<const int32_t*>(base + pl.off_pos);
+  }
+}
+
+int run_plan(Plan& pl, int dtype, cudaStream_t st) {
+  sa::GatherArgs& g = pl.g;
+  if (pl.stream) {
+    if (sa::launch_gather_stream(g, dtype, pl.grid, st) != 0) return SA_ERR_LAUNCH;
+    if (sa::launch_stream_combine(g, dtype, st) != 0) return SA_ERR_LAUNCH;
+    return SA_OK;
   }
   if (sa::launch_gather_simt(g, dtype, st) != 0) return SA_ERR_LAUNCH;
   if (sa::launch_combine(g, dtype, st) != 0) return SA_ERR_LAUNCH;
@@ -219,8 +232,7 @@ int sparse_plan(const sa_sparse_params* p, Plan& pl) {
   g.v_cur = p->v_cur;
   g.write_pos = p->write_pos;
   g.C = p->k_cur ? p->cur_len : 0;
-  g.row_status = p->row_status;
-  int rc = plan_gather(pl, p->q_dtype, p->err_word || p->row_status);
+  int rc = plan_gather(pl, p->q_dtype);
   if (rc != SA_OK) return rc;
   if (pl.stream && !(aligned16(p->k_cache) && aligned16(p->v_cache)))
     return SA_ERR_ALIGN;
@@ -352,44 +364,64 @@ int sparse_attn_decode(const sa_sparse_params* p, void* stream) {
   rc = check_workspace(pl, p->workspace, p->workspace_bytes);
   if (rc != SA_OK) return rc;
   cudaStream_t st = as_stream(stream);
-  if (!pl.stream) {
-    // separate steps on the SIMT path: append, then validation, then gather
-    if (p->k_cur) {
-      sa::PresentArgs a;
-      memset(&a, 0, sizeof(a));
-      a.past[0] = a.present[0] = const_cast<void*>(p->k_cache);
-      a.past[1] = a.present[1] = const_cast<void*>(p->v_cache);
-      a.cur[0] = p->k_cur;
-      a.cur[1] = p->v_cur;
-      a.n_tensors = 2;
-      a.esz = static_cast<int>(dtype_bytes(p->q_dtype));
-      a.B = p->B;
-      a.H = p->Hkv;
-      a.C = p->cur_len;
-      a.D = p->D;
-      a.stride = p->T;
-      a.write_pos = p->write_pos;
-      a.err_word = p->err_word;
-      if (!p->write_pos) return SA_ERR_UNSUPPORTED;  // SIMT path appends at explicit positions
-      if (sa::launch_present(a, st) != 0) return SA_ERR_LAUNCH;
-    }
-    if (p->K > 0 && (p->err_word || p->row_status)) {
-      sa::ValidateArgs v;
-      v.idx = p->idx;
-      v.is_i64 = p->idx_is_i64 ? 1 : 0;
-      const size_t esz = p->idx_is_i64 ? 8 : 4;
-      v.vec_ok = aligned16(p->idx) && ((p->K * static_cast<int64_t>(esz)) % 16 == 0);
-      v.rows = p->B * p->I * p->Sq;
-      v.rows_per_batch = p->I * p->Sq;
-      v.K = p->K;
-      v.bound_per_batch = p->kv_len;
-      v.bound = p->T;
-      v.row_status = p->row_status;
-      v.err_word = p->err_word;
-      if (sa::launch_validate(v, st) != 0) return SA_ERR_LAUNCH;
-    }
+  carve(pl, p->workspace);
+  // Plan kernel: per index row validation + planned positions (stream path),
+  // and the current-token append (either path).
+  sa::PlanArgs pa;
+  memset(&pa, 0, sizeof(pa));
+  pa.idx = p->idx;
+  pa.idx_is_i64 = p->idx_is_i64 ? 1 : 0;
+  const size_t iesz = p->idx_is_i64 ? 8 : 4;
+  pa.vec_ok = p->idx && aligned16(p->idx) && ((p->K * static_cast<int64_t>(iesz)) % 16 == 0);
+  pa.plan_rows = pl.stream ? 1 : 0;
+  pa.validate = pl.stream && p->K > 0 && (p->err_word || p->row_status);
+  pa.causal = p->causal;
+  pa.B = p->B;
+  pa.I = p->I;
+  pa.Sq = p->Sq;
+  pa.K = p->K;
+  pa.T = p->T;
+  pa.window = p->window;
+  pa.past_len = p->past_len;
+  pa.n_cand_pad = pl.g.n_cand_pad;
+  pa.kv_len = p->kv_len;
+  pa.pos = const_cast<int32_t*>(pl.g.pos);
+  pa.row_status = p->row_status;
+  pa.err_word = p->err_word;
+  if (p->k_cur) {
+    pa.k_cur = p->k_cur;
+    pa.v_cur = p->v_cur;
+    pa.k_cache = const_cast<void*>(p->k_cache);
+    pa.v_cache = const_cast<void*>(p->v_cache);
+    pa.write_pos = p->write_pos;
+    pa.Hkv = p->Hkv;
+    pa.C = p->cur_len;
+    pa.D = p->D;
+    pa.esz = static_cast<int>(dtype_bytes(p->q_dtype));
+    if ((p->D * pa.esz) % 16 || !aligned16(p->k_cur) || !aligned16(p->v_cur) ||
+        !aligned16(p->k_cache) || !aligned16(p->v_cache))
+      return SA_ERR_ALIGN;
+    const int64_t n16 = p->B * p->Hkv * p->cur_len * (p->D * pa.esz / 16);
+    int64_t blocks = (n16 + 127) / 128;
+    if (blocks > 152 * 4) blocks = 152 * 4;
+    pa.append_blocks = static_cast<int>(blocks);
   }
-  return run_plan(pl, p->workspace, p->q_dtype, st);
+  if ((pa.plan_rows || pa.append_blocks) && sa::launch_plan(pa, st) != 0) return SA_ERR_LAUNCH;
+  if (!pl.stream && p->K > 0 && (p->err_word || p->row_status)) {
+    sa::ValidateArgs v;
+    v.idx = p->idx;
+    v.is_i64 = p->idx_is_i64 ? 1 : 0;
+    v.vec_ok = pa.vec_ok;
+    v.rows = p->B * p->I * p->Sq;
+    v.rows_per_batch = p->I * p->Sq;
+    v.K = p->K;
+    v.bound_per_batch = p->kv_len;
+    v.bound = p->T;
+    v.row_status = p->row_status;
+    v.err_word = p->err_word;
+    if (sa::launch_validate(v, st) != 0) return SA_ERR_LAUNCH;
+  }
+  return run_plan(pl, p->q_dtype, st);
 }
 
 // ---- prefill ---------------------------------------------------------------------
@@ -446,7 +478,7 @@ size_t attn_prefill_workspace(const sa_prefill_params* p) {
   if (check_prefill(p, 1) != SA_OK) return 0;
   Plan pl;
   prefill_args(p, pl.g);
-  if (plan_gather(pl, p->dtype, false) != SA_OK) return 0;
+  if (plan_gather(pl, p->dtype) != SA_OK) return 0;
   return pl.bytes;
 }
 
@@ -456,7 +488,7 @@ int attn_prefill(const sa_prefill_params* p, void* stream) {
   cudaStream_t st = as_stream(stream);
   Plan pl;
   prefill_args(p, pl.g);
-  rc = plan_gather(pl, p->dtype, false);
+  rc = plan_gather(pl, p->dtype);
   if (rc != SA_OK) return rc;
   if (pl.stream && !(aligned16(p->k) && aligned16(p->v))) return SA_ERR_ALIGN;
   rc = check_workspace(pl, p->workspace, p->workspace_bytes);
@@ -470,7 +502,8 @@ int attn_prefill(const sa_prefill_params* p, void* stream) {
                           0, p->S, p->D, p->S, nullptr, nullptr, stream);
     if (rc != SA_OK) return rc;
   }
-  return run_plan(pl, p->workspace, p->dtype, st);
+  carve(pl, p->workspace);
+  return run_plan(pl, p->dtype, st);
 }
 
 // ---- paged decode ------------------------------------------------------------------
@@ -524,7 +557,7 @@ size_t paged_attn_decode_workspace(const sa_paged_params* p) {
   if (check_paged(p, 1) != SA_OK) return 0;
   Plan pl;
   paged_args(p, pl.g);
-  if (plan_gather(pl, p->dtype, false) != SA_OK) return 0;
+  if (plan_gather(pl, p->dtype) != SA_OK) return 0;
   return pl.bytes;
 }
 
@@ -534,7 +567,7 @@ int paged_attn_decode(const sa_paged_params* p, void* stream) {
   cudaStream_t st = as_stream(stream);
   Plan pl;
   paged_args(p, pl.g);
-  rc = plan_gather(pl, p->dtype, false);
+  rc = plan_gather(pl, p->dtype);
   if (rc != SA_OK) return rc;
   if (pl.stream && !(aligned16(p->k_pool) && aligned16(p->v_pool))) return SA_ERR_ALIGN;
   rc = check_workspace(pl, p->workspace, p->workspace_bytes);
@@ -557,7 +590,8 @@ int paged_attn_decode(const sa_paged_params* p, void* stream) {
     a.err_word = p->err_word;
     if (sa::launch_paged_append(a, st) != 0) return SA_ERR_LAUNCH;
   }
-  return run_plan(pl, p->workspace, p->dtype, st);
+  carve(pl, p->workspace);
+  return run_plan(pl, p->dtype, st);
 }
 
 }  // extern "C"
