@@ -57,6 +57,8 @@ extern "C" {
 #define SA_ERR_OVERLAP (-6)     /* an output overlaps an input illegally      */
 #define SA_ERR_UNSUPPORTED (-7) /* valid request this build does not serve    */
 #define SA_ERR_LAUNCH (-8)      /* the CUDA runtime refused a launch          */
+#define SA_ERR_SCRATCH_LIMIT (-9) /* sparse_attn_decode_noalloc: scratch needed
+                                     exceeds SA_NOALLOC_SCRATCH_BYTES          */
 
 /* ---- storage dtypes --------------------------------------------------- */
 #define SA_F32 0
@@ -194,6 +196,31 @@ typedef struct {
 
 size_t sparse_attn_decode_workspace(const sa_sparse_params* p);
 int sparse_attn_decode(const sa_sparse_params* p, void* stream);
+
+/*
+ * sparse_attn_decode_noalloc -- the same operation as sparse_attn_decode for
+ * callers that cannot allocate device memory themselves: runtimes that own a
+ * fixed device-memory budget and account for every byte, plugins whose host
+ * framework passes them inputs and outputs but no scratch, or code that must
+ * not set off cudaMalloc's implicit device synchronisation (or be refused it
+ * during a global-mode stream capture).  The pages have no counterpart: it is
+ * a deployment variant of this library's own entry point.
+ *
+ * p->workspace / p->workspace_bytes are ignored.  Scratch comes from one
+ * built-in device buffer of SA_NOALLOC_SCRATCH_BYTES, which every GPU that
+ * loads the library holds until the process exits; a request needing more
+ * (sparse_attn_decode_workspace(p) > SA_NOALLOC_SCRATCH_BYTES) returns
+ * SA_ERR_SCRATCH_LIMIT before anything is enqueued.  Nothing is allocated or
+ * freed.  The first call on each device looks up that buffer's device
+ * address (once, with that device current); make that first call before any
+ * stream capture.  Every call shares the buffer and it keeps the last call's
+ * contents (the call needs none of it cleared: all scratch is written before
+ * it is read), so calls that overlap on the GPU -- on different streams, or
+ * from different threads, of the same device -- race and must be serialised
+ * by the caller.
+ */
+#define SA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int sparse_attn_decode_noalloc(const sa_sparse_params* p, void* stream);
 
 /*
  * attn_prefill -- [SA] Semantics with no past: q [B, Hq, S, D],

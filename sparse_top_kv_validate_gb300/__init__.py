@@ -22,7 +22,8 @@ __all__ = [
     "load", "lib_path", "SAError", "status_string",
     "validate_indices", "build_present_kv", "sparse_attn_decode", "attn_prefill",
     "paged_attn_decode", "sparse_attn_decode_workspace", "attn_prefill_workspace",
-    "paged_attn_decode_workspace", "new_workspace",
+    "paged_attn_decode_workspace", "new_workspace", "sparse_attn_decode_noalloc",
+    "NOALLOC_SCRATCH_BYTES", "ERR_SCRATCH_LIMIT",
     "F32", "F16", "BF16", "FP8_E4M3_B64",
     "IDX_BELOW_SENTINEL", "IDX_AFTER_PADDING", "IDX_OUT_OF_RANGE", "IDX_NOT_INCREASING",
     "IDX_DUPLICATE", "IDX_ALL_PADDING", "ERRBIT_WRITE_POS", "ERRBIT_PAGE", "ERRBIT_TIMEOUT",
@@ -36,6 +37,8 @@ F32, F16, BF16, FP8_E4M3_B64 = 0, 1, 2, 3
 IDX_BELOW_SENTINEL, IDX_AFTER_PADDING, IDX_OUT_OF_RANGE = 1, 2, 4
 IDX_NOT_INCREASING, IDX_DUPLICATE, IDX_ALL_PADDING = 8, 16, 32
 ERRBIT_WRITE_POS, ERRBIT_PAGE, ERRBIT_TIMEOUT = 64, 128, 256
+ERR_SCRATCH_LIMIT = -9
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _p = C.c_void_p
 _i64 = C.c_int64
@@ -117,6 +120,8 @@ def load():
         L.sparse_attn_decode_workspace.argtypes = [C.POINTER(SparseParams)]
         L.sparse_attn_decode.restype = C.c_int
         L.sparse_attn_decode.argtypes = [C.POINTER(SparseParams), _p]
+        L.sparse_attn_decode_noalloc.restype = C.c_int
+        L.sparse_attn_decode_noalloc.argtypes = [C.POINTER(SparseParams), _p]
         L.attn_prefill_workspace.restype = C.c_size_t
         L.attn_prefill_workspace.argtypes = [C.POINTER(PrefillParams)]
         L.attn_prefill.restype = C.c_int
@@ -395,4 +400,26 @@ def paged_attn_decode(q, k_pool, v_pool, block_table, ctx_len, *, k_new=None, v_
     ws, nb = _workspace(need, q.device, workspace)
     p.workspace, p.workspace_bytes = _ptr(ws), nb
     _check("paged_attn_decode", L.paged_attn_decode(C.byref(p), _stream(stream)))
+    return y
+
+
+def sparse_attn_decode_noalloc(q, k_cache, v_cache, idx, *, y=None, stream=None, **kw):
+    """``sparse_attn_decode`` without caller-provided scratch: the library's
+    built-in device buffer (``NOALLOC_SCRATCH_BYTES``) serves every call, so
+    calls must not overlap on the GPU.  Same arguments, minus ``workspace``."""
+    L = load()
+    kw = _sparse_defaults(kw)
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("idx", idx),
+                 ("kv_len", kw["kv_len"]), ("sink", kw["sink"]), ("err_word", kw["err_word"]),
+                 ("row_status", kw["row_status"]), ("k_cur", kw["k_cur"]), ("v_cur", kw["v_cur"]),
+                 ("write_pos", kw["write_pos"])):
+        _dev(t, n)
+    B, Hq, Sq, D = q.shape
+    Dv = kw["Dv"] if k_cache.dtype == torch.uint8 else v_cache.shape[3]
+    if Dv is None:
+        Dv = D
+    if y is None:
+        y = torch.empty((B, Hq, Sq, Dv), dtype=q.dtype, device=q.device)
+    p = _sparse_params(q, k_cache, v_cache, idx, y, **kw)
+    _check("sparse_attn_decode_noalloc", L.sparse_attn_decode_noalloc(C.byref(p), _stream(stream)))
     return y

@@ -3,7 +3,9 @@
 // allocates, frees or synchronises; everything is enqueued on the caller's
 // stream.
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cmath>
+#include <mutex>
 #include <stdint.h>
 #include <string.h>
 
@@ -256,6 +258,7 @@ const char* sa_status_string(int status) {
     case SA_ERR_OVERLAP: return "an output overlaps an input";
     case SA_ERR_UNSUPPORTED: return "request not served by this build";
     case SA_ERR_LAUNCH: return "CUDA launch failed";
+    case SA_ERR_SCRATCH_LIMIT: return "request needs more scratch than the built-in no-allocation buffer holds";
     default: return "unknown status";
   }
 }
@@ -595,3 +598,61 @@ int paged_attn_decode(const sa_paged_params* p, void* stream) {
 }
 
 }  // extern "C"
+
+// ---- sparse decode without caller-provided scratch ------------------------------------
+//
+// For callers that may not allocate device memory: a runtime that owns a fixed
+// device-memory budget and accounts for every byte, a plugin whose host
+// framework hands it inputs and outputs but no scratch, or code that must not
+// trigger cudaMalloc's implicit device synchronisation (or its refusal during
+// a global-mode stream capture).  The scratch lives in one file-scope device
+// array that every GPU loading this library holds until the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // SA_NOALLOC_SCRATCH_BYTES
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_noalloc_ptr[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name only stands in for the symbol, so the address is looked up
+// once per device (with that device current) and cached.
+void* noalloc_scratch(int* status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *status = SA_ERR_LAUNCH;
+    return nullptr;
+  }
+  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  p = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      *status = SA_ERR_LAUNCH;
+      return nullptr;
+    }
+    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+}  // namespace
+
+extern "C" int sparse_attn_decode_noalloc(const sa_sparse_params* p, void* stream) {
+  int rc = check_sparse(p);
+  if (rc != SA_OK) return rc;
+  Plan pl;
+  rc = sparse_plan(p, pl);
+  if (rc != SA_OK) return rc;
+  if (pl.bytes > kNoAllocScratchBytes) return SA_ERR_SCRATCH_LIMIT;
+  void* scratch = noalloc_scratch(&rc);
+  if (!scratch) return rc;
+  sa_sparse_params q = *p;
+  q.workspace = scratch;
+  q.workspace_bytes = kNoAllocScratchBytes;
+  return sparse_attn_decode(&q, stream);
+}
