@@ -232,6 +232,18 @@ __device__ __forceinline__ void mma16816<__half>(float (&d)[4], uint32_t a0, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---- programmatic dependent launch --------------------------------------------------
+
+// Let the next kernel in the stream (launched with programmatic stream
+// serialisation) start launching; it still waits for this grid's results.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding kernel in the stream has completed and its memory
+// is visible (a no-op when this grid was launched without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- index loads ----------------------------------------------------------------
 
 __device__ __forceinline__ int64_t load_index(const void* idx, int64_t off, int is_i64) {

@@ -9,7 +9,7 @@
 // tokens united with the selected ones as in the compressed sparse attention
 // pages (`csa_ratio128_sink_attention`).
 //
-// GB300 mapping: one 128-thread block per index row (b, ih, i).  Every column
+// GB300 mapping: one 256-thread block per index row (b, ih, i).  Every column
 // is checked in its exact per-column form (a column's rule depends only on its
 // value and its left neighbour's; the first failing column wins through a
 // block max of ~(column << 8 | code)), so the row needs no sequential scan.
@@ -33,7 +33,8 @@ __device__ __forceinline__ int plan_column_code(int64_t v, int64_t prev, int64_t
   return 0;
 }
 
-__global__ void __launch_bounds__(128) plan_rows_kernel(PlanArgs a) {
+__global__ void __launch_bounds__(256) plan_rows_kernel(PlanArgs a) {
+  pdl_launch_dependents();  // the gather kernel may start its set-up now
   const int64_t irows = a.plan_rows ? a.B * a.I * a.Sq : 0;
   if (static_cast<int64_t>(blockIdx.x) >= irows) {
     // ---- append blocks: cur [B, Hkv, C, D] -> cache rows write_pos[b] + c --------
@@ -80,37 +81,42 @@ __global__ void __launch_bounds__(128) plan_rows_kernel(PlanArgs a) {
   // padding of the last tile
   for (int64_t c = ncand + threadIdx.x; c < a.n_cand_pad; c += blockDim.x) pos[c] = -1;
 
-  // selected columns, 4 consecutive per thread per step
+  // selected columns: 8 consecutive per thread per step, every load of the
+  // step issued before any is used
   const int64_t base = irow * a.K;
   unsigned long long best = 0;  // max over failing columns of ~(col << 8 | code)
-  for (int64_t c0 = static_cast<int64_t>(threadIdx.x) * 4; c0 < a.K; c0 += blockDim.x * 4) {
-    int64_t v[4];
-    if (c0 + 4 <= a.K && a.vec_ok) {
+  for (int64_t c0 = static_cast<int64_t>(threadIdx.x) * 8; c0 < a.K; c0 += blockDim.x * 8) {
+    int64_t v[8];
+    if (c0 + 8 <= a.K && a.vec_ok) {
       if (a.idx_is_i64) {
         const int4* p = reinterpret_cast<const int4*>(static_cast<const int64_t*>(a.idx) + base + c0);
-        const int4 w0 = __ldg(p), w1 = __ldg(p + 1);
-        v[0] = static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(w0.y)) << 32) | static_cast<uint32_t>(w0.x));
-        v[1] = static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(w0.w)) << 32) | static_cast<uint32_t>(w0.z));
-        v[2] = static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(w1.y)) << 32) | static_cast<uint32_t>(w1.x));
-        v[3] = static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(w1.w)) << 32) | static_cast<uint32_t>(w1.z));
+        int4 w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = __ldg(p + q);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          v[2 * q] = static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(w[q].y)) << 32) |
+                                          static_cast<uint32_t>(w[q].x));
+          v[2 * q + 1] = static_cast<int64_t>(
+              (static_cast<uint64_t>(static_cast<uint32_t>(w[q].w)) << 32) | static_cast<uint32_t>(w[q].z));
+        }
       } else {
-        const int4 w = __ldg(reinterpret_cast<const int4*>(static_cast<const int32_t*>(a.idx) + base + c0));
-        v[0] = w.x;
-        v[1] = w.y;
-        v[2] = w.z;
-        v[3] = w.w;
+        const int4* p = reinterpret_cast<const int4*>(static_cast<const int32_t*>(a.idx) + base + c0);
+        const int4 w0 = __ldg(p), w1 = __ldg(p + 1);
+        v[0] = w0.x; v[1] = w0.y; v[2] = w0.z; v[3] = w0.w;
+        v[4] = w1.x; v[5] = w1.y; v[6] = w1.z; v[7] = w1.w;
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = (c0 + e < a.K) ? load_index(a.idx, base + c0 + e, a.idx_is_i64) : -1;
+      for (int e = 0; e < 8; ++e) v[e] = (c0 + e < a.K) ? load_index(a.idx, base + c0 + e, a.idx_is_i64) : -1;
     }
     const int64_t before = c0 > 0 ? load_index(a.idx, base + c0 - 1, a.idx_is_i64) : 0;
+    int32_t out[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 8; ++e) {
       const int64_t col = c0 + e;
-      if (col >= a.K) break;
       const int64_t t = v[e];
-      if (a.validate) {
+      if (a.validate && col < a.K) {
         const int code = plan_column_code(t, e == 0 ? before : v[e - 1], col, len);
         if (code) {
           const unsigned long long key =
@@ -121,12 +127,21 @@ __global__ void __launch_bounds__(128) plan_rows_kernel(PlanArgs a) {
       }
       bool keep = t >= 0 && t < len && t <= causal_lim;
       if (a.window > 0 && t >= wstart) keep = false;  // already a window candidate
-      pos[a.window + col] = keep ? static_cast<int32_t>(t) : -1;
+      out[e] = keep ? static_cast<int32_t>(t) : -1;
+    }
+    int32_t* dst = pos + a.window + c0;
+    if (c0 + 8 <= a.K && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+      reinterpret_cast<int4*>(dst)[0] = make_int4(out[0], out[1], out[2], out[3]);
+      reinterpret_cast<int4*>(dst)[1] = make_int4(out[4], out[5], out[6], out[7]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (c0 + e < a.K) dst[e] = out[e];
     }
   }
   if (!a.validate) return;
   // block max of the failure keys
-  __shared__ unsigned long long red[4];
+  __shared__ unsigned long long red[8];
 #pragma unroll
   for (int sh = 16; sh > 0; sh >>= 1) {
     const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, sh);
@@ -147,7 +162,7 @@ int launch_plan(const PlanArgs& a, cudaStream_t st) {
   const int64_t irows = a.plan_rows ? a.B * a.I * a.Sq : 0;
   const int64_t blocks = irows + a.append_blocks;
   if (blocks == 0) return 0;
-  plan_rows_kernel<<<static_cast<unsigned>(blocks), 128, 0, st>>>(a);
+  plan_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -170,6 +170,29 @@ __global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(Gat
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
 
+  // ---- barriers and ring init --------------------------------------------------------
+  if (threadIdx.x < NW) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + threadIdx.x * G::kWarpBytes + G::kBarOff);
+#pragma unroll
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+  }
+  // V rows of every slot start at zero: a masked key's row is never fetched,
+  // and its probability 0 must multiply finite values.
+  constexpr int kVz = 16 * G::kRowStride / 16;  // int4 per slot's V rows
+  for (int e = threadIdx.x; e < NW * S * kVz; e += blockDim.x) {
+    const int w = e / (S * kVz), r = e % (S * kVz);
+    uint4* vz = reinterpret_cast<uint4*>(smem + w * G::kWarpBytes + (r / kVz) * G::kSlotBytes +
+                                         16 * G::kRowStride);
+    vz[r % kVz] = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  fence_mbar_init();
+  // Everything above is independent of the previous kernel in the stream
+  // (plan / append); from here on its results are read.
+  pdl_wait();
+  pdl_launch_dependents();  // the combine kernel may start launching
+  __syncthreads();
+
   // ---- tile space -----------------------------------------------------------------
   int32_t* pref = reinterpret_cast<int32_t*>(smem + NW * G::kWarpBytes);
   int64_t NTt, R;
@@ -217,25 +240,6 @@ __global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(Gat
     R = a.tiles_per_warp;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) a.meta[0] = R;
-
-  // ---- barriers and ring init --------------------------------------------------------
-  if (threadIdx.x < NW) {
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + threadIdx.x * G::kWarpBytes + G::kBarOff);
-#pragma unroll
-    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
-  }
-  // V rows of every slot start at zero: a masked key's row is never fetched,
-  // and its probability 0 must multiply finite values.
-  constexpr int kVz = 16 * G::kRowStride / 16;  // int4 per slot's V rows
-  for (int e = threadIdx.x; e < NW * S * kVz; e += blockDim.x) {
-    const int w = e / (S * kVz), r = e % (S * kVz);
-    uint4* vz = reinterpret_cast<uint4*>(smem + w * G::kWarpBytes + (r / kVz) * G::kSlotBytes +
-                                         16 * G::kRowStride);
-    vz[r % kVz] = make_uint4(0, 0, 0, 0);
-  }
-  fence_proxy_async_smem();
-  fence_mbar_init();
-  __syncthreads();
 
   // ---- this warp's tile range ----------------------------------------------------------
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * NW + warp;
@@ -470,6 +474,8 @@ __global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(Gat
 // its slot 0 when the unit begins inside w's range, else in slot 1.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) stream_combine_kernel(GatherArgs a) {
+  constexpr int kMaxW = 64;  // partials merged per pass
+  pdl_wait();  // the stream kernel's partials and tile space
   const int64_t u = blockIdx.x;
   const int64_t R = a.meta[0];
   int64_t off, tu;
@@ -485,52 +491,93 @@ __global__ void __launch_bounds__(128) stream_combine_kernel(GatherArgs a) {
   const int64_t w_lo = off / R, w_hi = (off + tu - 1) / R;
   if (w_lo == w_hi) return;  // written directly by the stream kernel
   const UnitInfo ui = unit_info(a, u);
-  __shared__ float sM[16], sInv[16];
   const int hpu = static_cast<int>(a.hpu);
+  const int64_t nw = w_hi - w_lo + 1;
+  __shared__ float sm_m[kMaxW][16], sm_l[kMaxW][16];
+  __shared__ float sM[16], sL[16];
   if (threadIdx.x < hpu) {
-    const int hh = threadIdx.x;
-    float M = SA_NEG_INF;
-    for (int64_t w = w_lo; w <= w_hi; ++w) {
-      const int sl = (w * R >= off) ? 0 : 1;
-      M = fmaxf(M, __ldg(a.part_ml + 2 * ((w * 2 + sl) * a.hpu + hh)));
+    sM[threadIdx.x] = SA_NEG_INF;
+    sL[threadIdx.x] = 0.f;
+  }
+  constexpr int kG = (16 * D / 4 + 127) / 128;  // float4 groups per thread (hpu <= 16)
+  float4 acc[kG];
+#pragma unroll
+  for (int g = 0; g < kG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // Partials are merged in warp order, kMaxW at a time, as a running
+  // (max, sum, output) exactly like the online softmax.
+  for (int64_t w0 = 0; w0 < nw; w0 += kMaxW) {
+    const int nwp = static_cast<int>(nw - w0 < kMaxW ? nw - w0 : kMaxW);
+    __syncthreads();
+    for (int t = threadIdx.x; t < nwp * hpu; t += blockDim.x) {
+      const int wi = t / hpu, hh = t % hpu;
+      const int64_t w = w_lo + w0 + wi;
+      const int sl = (w * R >= off) ? 0 : 1;  // the unit begins inside w's range
+      const float2 ml =
+          __ldg(reinterpret_cast<const float2*>(a.part_ml) + (w * 2 + sl) * a.hpu + hh);
+      sm_m[wi][hh] = ml.x;
+      sm_l[wi][hh] = ml.y;
     }
-    float L = 0.f;
-    if (M != SA_NEG_INF) {
-      for (int64_t w = w_lo; w <= w_hi; ++w) {
-        const int sl = (w * R >= off) ? 0 : 1;
-        const float2 ml = __ldg(reinterpret_cast<const float2*>(a.part_ml) + (w * 2 + sl) * a.hpu + hh);
-        if (ml.x != SA_NEG_INF) L += ml.y * ex2(ml.x - M);
+    __syncthreads();
+    // new running max per head, rescale of what is accumulated so far
+    __shared__ float sScale[16];
+    if (threadIdx.x < hpu) {
+      const int hh = threadIdx.x;
+      float M = sM[hh];
+      for (int wi = 0; wi < nwp; ++wi) M = fmaxf(M, sm_m[wi][hh]);
+      const float Mu = (M == SA_NEG_INF) ? 0.f : M;
+      const float old = ex2(sM[hh] - Mu);
+      float L = sL[hh] * old;
+      for (int wi = 0; wi < nwp; ++wi) {
+        const float f = ex2(sm_m[wi][hh] - Mu);
+        sm_m[wi][hh] = f;  // now the partial's weight
+        L += sm_l[wi][hh] * f;
       }
-      if (a.sink) L += ex2(a.sink[ui.h0 + hh] * kLog2e - M);
+      sScale[hh] = old;
+      sM[hh] = M;
+      sL[hh] = L;
     }
-    sM[hh] = M;
-    sInv[hh] = (M == SA_NEG_INF || L == 0.f) ? 0.f : 1.0f / L;
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      const int e = threadIdx.x + 128 * g;
+      if (e >= hpu * D / 4) break;
+      const int hh = (e * 4) / D, d = (e * 4) % D;
+      float4 s4 = acc[g];
+      const float sc = sScale[hh];
+      s4.x *= sc;
+      s4.y *= sc;
+      s4.z *= sc;
+      s4.w *= sc;
+#pragma unroll 4
+      for (int wi = 0; wi < nwp; ++wi) {
+        const int64_t w = w_lo + w0 + wi;
+        const int sl = (w * R >= off) ? 0 : 1;
+        const float f = sm_m[wi][hh];
+        const float4 v = __ldg(reinterpret_cast<const float4*>(
+            a.part_o + ((w * 2 + sl) * a.hpu + hh) * D + d));
+        s4.x += v.x * f;
+        s4.y += v.y * f;
+        s4.z += v.z * f;
+        s4.w += v.w * f;
+      }
+      acc[g] = s4;
+    }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < hpu * D / 4; e += blockDim.x) {
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    const int e = threadIdx.x + 128 * g;
+    if (e >= hpu * D / 4) break;
     const int hh = (e * 4) / D, d = (e * 4) % D;
     const float M = sM[hh];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != SA_NEG_INF) {
-      for (int64_t w = w_lo; w <= w_hi; ++w) {
-        const int sl = (w * R >= off) ? 0 : 1;
-        const int64_t pi = (w * 2 + sl) * a.hpu + hh;
-        const float m = __ldg(a.part_ml + 2 * pi);
-        if (m == SA_NEG_INF) continue;
-        const float f = ex2(m - M);
-        const float4 v = __ldg(reinterpret_cast<const float4*>(a.part_o + pi * D + d));
-        acc.x += v.x * f;
-        acc.y += v.y * f;
-        acc.z += v.z * f;
-        acc.w += v.w * f;
-      }
-    }
-    const float inv = sInv[hh];
+    float L = sL[hh];
+    if (a.sink && M != SA_NEG_INF) L += ex2(a.sink[ui.h0 + hh] * kLog2e - M);
+    const float inv = (M == SA_NEG_INF || L == 0.f) ? 0.f : 1.0f / L;
     T* yp = static_cast<T*>(a.y) + ((ui.b * a.Hq + ui.h0 + hh) * a.Sq + ui.i) * D + d;
-    yp[0] = from_f32<T>(acc.x * inv);
-    yp[1] = from_f32<T>(acc.y * inv);
-    yp[2] = from_f32<T>(acc.z * inv);
-    yp[3] = from_f32<T>(acc.w * inv);
+    yp[0] = from_f32<T>(acc[g].x * inv);
+    yp[1] = from_f32<T>(acc[g].y * inv);
+    yp[2] = from_f32<T>(acc[g].z * inv);
+    yp[3] = from_f32<T>(acc[g].w * inv);
   }
 }
 
@@ -538,14 +585,33 @@ __global__ void __launch_bounds__(128) stream_combine_kernel(GatherArgs a) {
 // launchers
 // ---------------------------------------------------------------------------
 
+// Launch with programmatic stream serialisation: the kernel may begin while
+// the previous kernel in the stream finishes, and waits for its results
+// itself (griddepcontrol.wait) before reading them.
+template <typename K>
+static int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      const GatherArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a) == cudaSuccess ? 0 : -1;
+}
+
 template <typename T, int D, int NT>
 static int launch_stream_t(const GatherArgs& a, int grid, size_t smem, cudaStream_t st) {
   if (cudaFuncSetAttribute(gather_stream_kernel<T, D, NT>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return -1;
-  gather_stream_kernel<T, D, NT><<<grid, SGeo<D>::kThreads, smem, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return launch_pdl(gather_stream_kernel<T, D, NT>, dim3(grid), dim3(SGeo<D>::kThreads), smem,
+                    st, a);
 }
 
 int launch_gather_stream(const GatherArgs& a, int dtype, int grid, cudaStream_t st) {
@@ -567,17 +633,15 @@ int launch_gather_stream(const GatherArgs& a, int dtype, int grid, cudaStream_t 
 
 int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st) {
   if (a.units == 0) return 0;
-  const unsigned grid = static_cast<unsigned>(a.units);
+  const dim3 grid(static_cast<unsigned>(a.units)), blk(128);
   if (dtype == SA_BF16) {
-    if (a.D == 64) stream_combine_kernel<__nv_bfloat16, 64><<<grid, 128, 0, st>>>(a);
-    else if (a.D == 128) stream_combine_kernel<__nv_bfloat16, 128><<<grid, 128, 0, st>>>(a);
-    else stream_combine_kernel<__nv_bfloat16, 256><<<grid, 128, 0, st>>>(a);
-  } else {
-    if (a.D == 64) stream_combine_kernel<__half, 64><<<grid, 128, 0, st>>>(a);
-    else if (a.D == 128) stream_combine_kernel<__half, 128><<<grid, 128, 0, st>>>(a);
-    else stream_combine_kernel<__half, 256><<<grid, 128, 0, st>>>(a);
+    if (a.D == 64) return launch_pdl(stream_combine_kernel<__nv_bfloat16, 64>, grid, blk, 0, st, a);
+    if (a.D == 128) return launch_pdl(stream_combine_kernel<__nv_bfloat16, 128>, grid, blk, 0, st, a);
+    return launch_pdl(stream_combine_kernel<__nv_bfloat16, 256>, grid, blk, 0, st, a);
   }
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  if (a.D == 64) return launch_pdl(stream_combine_kernel<__half, 64>, grid, blk, 0, st, a);
+  if (a.D == 128) return launch_pdl(stream_combine_kernel<__half, 128>, grid, blk, 0, st, a);
+  return launch_pdl(stream_combine_kernel<__half, 256>, grid, blk, 0, st, a);
 }
 
 }  // namespace sa
