@@ -137,6 +137,8 @@ class ClockSampler:
 class SparseDecode:
     """Selected-token decode step (append + validate + gather decode)."""
 
+    metric = METRIC
+
     def __init__(self, sa, c: synth.SparseCase, dev, seed=1001):
         self.sa, self.c, self.dev = sa, c, dev
         inp = synth.make_sparse_inputs(c, seed, device=dev)
@@ -222,10 +224,176 @@ class SparseDecode:
                 "decode_us": round(decode_ms * 1e3, 2), "traffic": TRAFFIC.get(self.c.name)}
 
 
+class PagedDecode:
+    """Paged causal decode step: write the new token into the page pool and
+    attend over each sequence's whole context (one query per sequence)."""
+
+    metric = METRIC
+
+    def __init__(self, sa, c: synth.PagedCase, dev, seed=1005):
+        self.sa, self.c, self.dev = sa, c, dev
+        inp = synth.make_paged_inputs(c, seed, device=dev)
+        self.inp = inp
+        self.q = inp["q"]
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.y = torch.empty_like(self.q)
+        nws = sa.paged_attn_decode_workspace(self.q, inp["k_pool"], inp["v_pool"],
+                                             inp["block_table"], inp["ctx_len"],
+                                             scale=c.eff_scale())
+        self.ws = sa.new_workspace(nws, dev)
+        self.rows = c.B * c.Hq
+        es = self.q.element_size()
+        tokens = int(inp["ctx_len"].sum().item())
+        self.tokens = tokens
+        self.decode_bytes = (tokens * c.Hkv * c.D * es * 2 + inp["block_table"].numel() * 4
+                             + 2 * self.q.numel() * es + 2 * inp["k_new"].numel() * es * 2)
+        self.launches_per_step = 4  # append, gather, combine (+ nothing else)
+        self.h_q = self.q.cpu().pin_memory()
+        self.h_kn = inp["k_new"].cpu().pin_memory()
+        self.h_vn = inp["v_new"].cpu().pin_memory()
+        self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
+
+    def step(self, ev=None):
+        i = self.inp
+        if ev is not None:
+            ev[0].record()
+        self.sa.paged_attn_decode(self.q, i["k_pool"], i["v_pool"], i["block_table"],
+                                  i["ctx_len"], k_new=i["k_new"], v_new=i["v_new"],
+                                  scale=self.c.eff_scale(), err_word=self.err, y=self.y,
+                                  workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    def h2d(self):
+        self.q.copy_(self.h_q, non_blocking=True)
+        self.inp["k_new"].copy_(self.h_kn, non_blocking=True)
+        self.inp["v_new"].copy_(self.h_vn, non_blocking=True)
+        return sum(t.numel() * t.element_size() for t in (self.h_q, self.h_kn, self.h_vn))
+
+    def d2h(self):
+        self.h_y.copy_(self.y, non_blocking=True)
+        return self.h_y.numel() * self.h_y.element_size()
+
+    def config(self):
+        c = self.c
+        return {"workload": c.name, "batch": c.B, "q_heads": c.Hq, "kv_heads": c.Hkv,
+                "head_dim": c.D, "ctx_range": [c.ctx_low, c.ctx_high], "page_tokens":
+                c.page_tokens, "context_tokens": self.tokens,
+                "step": "paged_attn_decode: new-token append + stream-K gather over pages "
+                        "+ combine"}
+
+    def oracle_rows(self, rows):
+        import oracle
+        c, i = self.c, self.inp
+        out = []
+        if not hasattr(self, "_host"):
+            self._host = {}
+        for r in rows:
+            b, h = divmod(r, c.Hq)
+            if b not in self._host:
+                n = int(i["ctx_len"][b])
+                pages = i["block_table"][b, : (n + c.page_tokens - 1) // c.page_tokens].long()
+                self._host[b] = (i["q"][b:b + 1].cpu(), i["k_pool"][pages].cpu(),
+                                 i["v_pool"][pages].cpu(), n)
+            q, kp, vp, n = self._host[b]
+            table = torch.arange(kp.shape[0], dtype=torch.int32)[None]
+            y = oracle.paged_decode(q, kp, vp, table, torch.tensor([n], dtype=torch.int32),
+                                    page_tokens=c.page_tokens, scale=c.eff_scale(), rows=[h])
+            out.append(y[0])
+        return np.stack(out)
+
+    def roofline(self, decode_ms, peaks):
+        achieved = self.decode_bytes / (decode_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": "paged_attn_decode call (append + gather_stream + "
+                "combine)", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                "peak_source": peaks["source"] + " (copy bandwidth, burst)",
+                "algorithmic_bytes": int(self.decode_bytes),
+                "decode_us": round(decode_ms * 1e3, 2), "traffic": TRAFFIC.get(self.c.name)}
+
+
+class Prefill:
+    """Dense causal prefill step with present K/V emission."""
+
+    metric = "dense causal prefill tokens/s and tensor-core TFLOP/s (1 GB300)"
+
+    def __init__(self, sa, c: synth.PrefillCase, dev, seed=1004):
+        self.sa, self.c, self.dev = sa, c, dev
+        inp = synth.make_prefill_inputs(c, seed, device=dev)
+        self.q, self.k, self.v = inp["q"], inp["k"], inp["v"]
+        self.pk, self.pv = torch.empty_like(self.k), torch.empty_like(self.v)
+        self.y = torch.empty_like(self.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        nws = sa.attn_prefill_workspace(self.q, self.k, self.v, True, c.eff_scale(), c.softcap)
+        self.ws = sa.new_workspace(nws, dev)
+        self.rows = c.B * c.S  # tokens
+        S = c.S
+        pairs = S * (S + 1) // 2 if c.causal else S * S
+        self.flops = 4.0 * c.D * pairs * c.B * c.Hq
+        self.launches_per_step = 3
+        self.h = {n: getattr(self, n).cpu().pin_memory() for n in ("q", "k", "v")}
+        self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
+
+    def step(self, ev=None):
+        c = self.c
+        if ev is not None:
+            ev[0].record()
+        self.sa.attn_prefill(self.q, self.k, self.v, causal=c.causal, scale=c.eff_scale(),
+                             softcap=c.softcap, y=self.y, present_k=self.pk, present_v=self.pv,
+                             workspace=self.ws)
+        if ev is not None:
+            ev[1].record()
+
+    def h2d(self):
+        for n in ("q", "k", "v"):
+            getattr(self, n).copy_(self.h[n], non_blocking=True)
+        return sum(t.numel() * t.element_size() for t in self.h.values())
+
+    def d2h(self):
+        self.h_y.copy_(self.y, non_blocking=True)
+        return self.h_y.numel() * self.h_y.element_size()
+
+    def config(self):
+        c = self.c
+        return {"workload": c.name, "batch": c.B, "seq_len": c.S, "q_heads": c.Hq,
+                "kv_heads": c.Hkv, "head_dim": c.D, "causal": c.causal, "softcap": c.softcap,
+                "step": "attn_prefill with present K/V"}
+
+    def oracle_rows(self, rows):
+        import oracle
+        c = self.c
+        if not hasattr(self, "_host"):
+            self._host = (self.q.cpu(), self.k.cpu(), self.v.cpu())
+        q, k, v = self._host
+        # each requested unit is one token (all its query heads), spread over
+        # the batch and positions
+        stride = max(1, (c.B * c.S) // max(len(rows), 1))
+        picked = []
+        for r in rows:
+            tok = (r * stride) % (c.B * c.S)
+            b, i = divmod(tok, c.S)
+            picked += [(b * c.Hq + h) * c.S + i for h in range(c.Hq)]
+        return oracle.prefill(q, k, v, scale=c.eff_scale(), causal=c.causal, softcap=c.softcap,
+                              rows=picked)
+
+    def roofline(self, ms, peaks):
+        tf = self.flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": "attn_prefill call", "achieved": round(tf, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(tf / peaks["bf16_tflops"], 4),
+                "peak_source": peaks["source"] + " (cuBLAS bf16, burst)",
+                "algorithmic_flops": self.flops, "call_us": round(ms * 1e3, 2),
+                "traffic": TRAFFIC.get(self.c.name)}
+
+
 # DRAM bytes (read + write) per decode launch from an ncu capture of the
 # dominant kernel, keyed by workload; None until a capture of the current
 # kernel exists.
-TRAFFIC: dict = {}
+TRAFFIC: dict = {
+    # plan + gather_stream + combine kernels of one call, ncu dram read + write
+    "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 279922176,
+}
 
 
 def make_workload(sa, name, dev):
@@ -233,6 +401,10 @@ def make_workload(sa, name, dev):
         return SparseDecode(sa, synth.sparse_bf16(), dev)
     if name == "tiny_sparse":
         return SparseDecode(sa, synth.tiny_sparse(), dev)
+    if name == "paged_fp16":
+        return PagedDecode(sa, synth.paged_fp16(), dev)
+    if name == "prefill_bf16":
+        return Prefill(sa, synth.prefill_bf16(), dev)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -310,9 +482,9 @@ def run_gpu(args):
     if rank == 0:
         peaks = measured_peaks()
         line = {
-            "metric": METRIC,
+            "metric": wl.metric,
             "value": round(value, 1),
-            "unit": "query-rows/s",
+            "unit": "tokens/s" if isinstance(wl, Prefill) else "query-rows/s",
             "n_gpus": ws,
             "steps": steps,
             "warmup": max(args.warmup, 3),
@@ -326,7 +498,8 @@ def run_gpu(args):
                            l2="flushed between steps (512 MB write outside the step events)",
                            timing="sum of per-step CUDA events on the launching stream"),
             "roofline": wl.roofline(statistics.median(dec_ms), peaks),
-            "e2e": {"value": round(wl.rows * ws / (e2e_ms * 1e-3), 1), "unit": "query-rows/s",
+            "e2e": {"value": round(wl.rows * ws / (e2e_ms * 1e-3), 1),
+                    "unit": "tokens/s" if isinstance(wl, Prefill) else "query-rows/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "ms_per_step": round(e2e_ms, 5)},
             "gpu_launches": wl.launches_per_step * steps,
@@ -374,8 +547,9 @@ def cpu_baseline(wl, args, budget_s: float = 10.0):
         _oracle_threads(wl, rows_all[:n2], cores)
         dt = time.perf_counter() - t0
         n = n2
-    return {"value": round(n / dt, 2), "unit": "query-rows/s", "cores": cores,
-            "kind": "oracle", "sample": f"{n} of {wl.rows} query rows of one step",
+    unit = "tokens/s" if isinstance(wl, Prefill) else "query-rows/s"
+    return {"value": round(n / dt, 2), "unit": unit, "cores": cores,
+            "kind": "oracle", "sample": f"{n} of {wl.rows} {unit.split('/')[0]} of one step",
             "seconds": round(dt, 3)}
 
 
