@@ -387,6 +387,94 @@ class Prefill:
                 "traffic": TRAFFIC.get(self.c.name)}
 
 
+class CsaFp8Decode:
+    """Selected-token decode over the hybrid FP8 latent cache: a dense window of
+    the last 128 tokens united with 2048 selected indices, 128 query heads on
+    one 576-dim latent head (512 E4M3 + 64 bf16 dims, 648-byte records)."""
+
+    metric = METRIC
+
+    def __init__(self, sa, c: synth.SparseCase, dev, seed=1003):
+        self.sa, self.c, self.dev = sa, c, dev
+        inp = synth.make_sparse_inputs(c, seed, device=dev)
+        self.q, self.rec, self.idx = inp["q"], inp["kv_records"], inp["idx"]
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.status = torch.empty(c.B * c.I, dtype=torch.uint8, device=dev)
+        self.y = torch.empty_like(self.q)
+        nws = sa.sparse_attn_decode_workspace(self.q, self.rec, None, self.idx,
+                                              scale=c.eff_scale(), window=c.window,
+                                              n_rope=c.n_rope, err_word=self.err,
+                                              row_status=self.status)
+        self.ws = sa.new_workspace(nws, dev)
+        self.rows = c.B * c.Hq
+        valid = int((self.idx >= 0).sum().item())       # selected below the window
+        self.keys = valid + c.B * c.window
+        self.decode_bytes = (self.keys * c.record_stride + self.idx.numel() * 4
+                             + 2 * self.q.numel() * 2)
+        self.flops = 4.0 * c.Hq * c.D * self.keys
+        self.launches_per_step = 3  # plan, fp8 decode, combine
+        self.h_q = self.q.cpu().pin_memory()
+        self.h_idx = self.idx.cpu().pin_memory()
+        self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
+
+    def step(self, ev=None):
+        c = self.c
+        if ev is not None:
+            ev[0].record()
+        self.sa.sparse_attn_decode(self.q, self.rec, None, self.idx, scale=c.eff_scale(),
+                                   window=c.window, n_rope=c.n_rope, y=self.y,
+                                   workspace=self.ws, err_word=self.err, row_status=self.status)
+        if ev is not None:
+            ev[1].record()
+
+    def h2d(self):
+        self.q.copy_(self.h_q, non_blocking=True)
+        self.idx.copy_(self.h_idx, non_blocking=True)
+        return sum(t.numel() * t.element_size() for t in (self.h_q, self.h_idx))
+
+    def d2h(self):
+        self.h_y.copy_(self.y, non_blocking=True)
+        return self.h_y.numel() * self.h_y.element_size()
+
+    def config(self):
+        c = self.c
+        return {"workload": c.name, "batch": c.B, "q_heads": c.Hq, "latent_heads": c.Hkv,
+                "head_dim": c.D, "fp8_dims": c.D - c.n_rope, "rope_dims": c.n_rope,
+                "record_bytes": c.record_stride, "cache_tokens": c.T, "top_k": c.K,
+                "window": c.window, "keys_attended": self.keys,
+                "step": "sparse_attn_decode on FP8 records: plan kernel (validation, window "
+                        "union positions) + FP8 decode/attention kernel + combine"}
+
+    def oracle_rows(self, rows):
+        import oracle
+        c = self.c
+        if not hasattr(self, "_host"):
+            self._host = {}
+        out = []
+        for r in rows:
+            b, h = divmod(r, c.Hq)
+            if b not in self._host:
+                self._host[b] = (self.q[b:b + 1].cpu(), self.idx[b:b + 1].cpu(),
+                                 self.rec[b:b + 1].cpu())
+            q, idx, rec = self._host[b]
+            out.append(oracle.sparse_attention(q, idx, records=rec, n_rope=c.n_rope,
+                                               scale=c.eff_scale(), window=c.window,
+                                               rows=[h])[0])
+        return np.stack(out)
+
+    def roofline(self, ms, peaks):
+        gbs = self.decode_bytes / (ms * 1e-3) / 1e9
+        tf = self.flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": "sparse_attn_decode call on FP8 records "
+                "(plan + fp8_decode + combine)", "achieved": round(tf, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(tf / peaks["bf16_tflops"], 4),
+                "peak_source": peaks["source"] + " (cuBLAS bf16, burst)",
+                "algorithmic_flops": self.flops, "algorithmic_bytes": int(self.decode_bytes),
+                "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                "call_us": round(ms * 1e3, 2), "traffic": TRAFFIC.get(self.c.name)}
+
+
 # DRAM bytes (read + write) per decode launch from an ncu capture of the
 # dominant kernel, keyed by workload; None until a capture of the current
 # kernel exists.
@@ -403,6 +491,8 @@ def make_workload(sa, name, dev):
         return SparseDecode(sa, synth.tiny_sparse(), dev)
     if name == "paged_fp16":
         return PagedDecode(sa, synth.paged_fp16(), dev)
+    if name == "csa_fp8":
+        return CsaFp8Decode(sa, synth.csa_fp8(), dev)
     if name == "prefill_bf16":
         return Prefill(sa, synth.prefill_bf16(), dev)
     raise SystemExit(f"unknown workload {name}")

@@ -109,6 +109,8 @@ struct GatherArgs {
   const int32_t* block_table;
   const int32_t* ctx_len;
   int64_t page_tokens, max_pages, num_pages;
+  // FP8 hybrid records (sparse source)
+  int64_t record_stride;      // bytes between records
   // math
   float scale_log2;           // scale * log2(e)
   float softcap;              // 0 = off
@@ -125,6 +127,10 @@ size_t stream_smem_bytes(int D, int source, int64_t B);
 int stream_warps(int D);
 int stream_max_batch_paged();
 int launch_gather_stream(const GatherArgs& a, int dtype, int grid, cudaStream_t st);
+// FP8 hybrid-record decode (MQA, D = 512 E4M3 + 64 bf16, bf16 Q/Y).
+size_t fp8_smem_bytes();
+int fp8_chunk_tiles_max();
+int launch_fp8_decode(const GatherArgs& a, cudaStream_t st);
 // Merge of the units the stream kernel split across warps.
 int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st);
 

@@ -69,6 +69,7 @@ void plan_simt_splits(int64_t n_cand, int64_t* chunk_out, int64_t* splits_out) {
 struct Plan {
   sa::GatherArgs g;
   bool stream = false;
+  bool fp8 = false;
   int grid = 0;
   size_t off_pos = 0, off_meta = 0, off_part_o = 0, off_part_ml = 0, bytes = 0;
 };
@@ -135,6 +136,43 @@ int plan_gather(Plan& pl, int dtype) {
   return SA_OK;
 }
 
+// FP8 hybrid-record decode: planned positions (as the stream path), one CTA
+// per (unit, 32-head block, key chunk), partials merged by the combine kernel.
+int plan_fp8(Plan& pl) {
+  sa::GatherArgs& g = pl.g;
+  pl.fp8 = true;
+  g.g = g.Hq / g.Hkv;
+  g.n_groups = g.Hkv;  // 1: every query head shares the latent head
+  g.hpu = g.g;
+  g.units = g.B * g.n_groups * g.Sq;
+  g.tiles_per_unit = (g.n_cand + 15) / 16;
+  g.n_cand_pad = g.tiles_per_unit * 16;
+  const int64_t blocks = g.units * (g.Hq / 32);
+  const int64_t slots = static_cast<int64_t>(device_shape().sms) * 2;  // 2 CTAs per SM
+  int64_t splits = slots / (blocks > 0 ? blocks : 1);
+  const int64_t min_splits = (g.tiles_per_unit + sa::fp8_chunk_tiles_max() - 1) /
+                             sa::fp8_chunk_tiles_max();
+  if (splits < min_splits) splits = min_splits;
+  if (splits < 1) splits = 1;
+  if (splits > g.tiles_per_unit) splits = g.tiles_per_unit > 0 ? g.tiles_per_unit : 1;
+  g.chunk = (g.tiles_per_unit + splits - 1) / splits;  // tiles per chunk
+  g.splits = (g.tiles_per_unit + g.chunk - 1) / g.chunk;
+  if (g.splits < 1) g.splits = 1;
+  const int64_t irows = g.B * g.I * g.Sq;
+  size_t off = 0;
+  pl.off_pos = off;
+  off += align_up(static_cast<size_t>(irows * g.n_cand_pad) * sizeof(int32_t));
+  if (g.splits > 1) {
+    const size_t parts = static_cast<size_t>(g.units * g.splits * g.hpu);
+    pl.off_part_o = off;
+    off += align_up(parts * g.Dv * sizeof(float));
+    pl.off_part_ml = off;
+    off += align_up(parts * 2 * sizeof(float));
+  }
+  pl.bytes = off;
+  return SA_OK;
+}
+
 int check_workspace(const Plan& pl, void* ws, size_t ws_bytes) {
   if (pl.bytes == 0) return SA_OK;
   if (!ws || ws_bytes < pl.bytes) return SA_ERR_WORKSPACE;
@@ -147,6 +185,14 @@ void carve(Plan& pl, void* ws) {
   sa::GatherArgs& g = pl.g;
   char* base = static_cast<char*>(ws);
   if (pl.bytes == 0) return;
+  if (pl.fp8) {
+    g.pos = reinterpret_cast<const int32_t*>(base + pl.off_pos);
+    if (g.splits > 1) {
+      g.part_o = reinterpret_cast<float*>(base + pl.off_part_o);
+      g.part_ml = reinterpret_cast<float*>(base + pl.off_part_ml);
+    }
+    return;
+  }
   g.part_o = reinterpret_cast<float*>(base + pl.off_part_o);
   g.part_ml = reinterpret_cast<float*>(base + pl.off_part_ml);
   if (pl.stream) {
@@ -158,6 +204,11 @@ void carve(Plan& pl, void* ws) {
 
 int run_plan(Plan& pl, int dtype, cudaStream_t st) {
   sa::GatherArgs& g = pl.g;
+  if (pl.fp8) {
+    if (sa::launch_fp8_decode(g, st) != 0) return SA_ERR_LAUNCH;
+    if (sa::launch_combine(g, SA_BF16, st) != 0) return SA_ERR_LAUNCH;
+    return SA_OK;
+  }
   if (pl.stream) {
     if (sa::launch_gather_stream(g, dtype, pl.grid, st) != 0) return SA_ERR_LAUNCH;
     if (sa::launch_stream_combine(g, dtype, st) != 0) return SA_ERR_LAUNCH;
@@ -180,7 +231,26 @@ int check_sparse(const sa_sparse_params* p, int query = 0) {
   if (p->K < 0 || p->window < 0 || p->past_len < 0) return SA_ERR_SHAPE;
   if (p->K == 0 && p->window == 0) return SA_ERR_SHAPE;
   if (p->K > 0 && !p->idx) return SA_ERR_NULL;
-  if (p->kv_dtype == SA_FP8_E4M3_B64) return SA_ERR_UNSUPPORTED;  // served by the FP8 path
+  if (!std::isfinite(p->scale) || !std::isfinite(p->softcap) || p->softcap < 0.f)
+    return SA_ERR_SHAPE;
+  if (p->kv_dtype == SA_FP8_E4M3_B64) {
+    // hybrid records: bf16 Q/Y, one latent head, 512 E4M3 dims + 64 bf16 dims
+    if (p->q_dtype != SA_BF16) return SA_ERR_DTYPE;
+    if (p->D != 576 || p->n_rope != 64 || p->Dv != p->D || p->Hkv != 1 || p->I != 1 ||
+        p->Hq % 32 != 0 || p->k_cur)
+      return SA_ERR_UNSUPPORTED;
+    if (p->record_stride < 648 || p->record_stride % 8 != 0) return SA_ERR_SHAPE;
+    if (p->B * p->T >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(p->k_cache) % 8 || !aligned16(p->q) || !aligned16(p->y ? p->y : p->q))
+      return SA_ERR_ALIGN;
+    const size_t qbytes = static_cast<size_t>(p->B * p->Hq * p->Sq * p->D) * 2;
+    const size_t rbytes = static_cast<size_t>(p->B * p->T * p->record_stride);
+    const size_t ibytes = static_cast<size_t>(p->B * p->I * p->Sq * p->K) * (p->idx_is_i64 ? 8 : 4);
+    if (overlaps(p->y, qbytes, p->q, qbytes) || overlaps(p->y, qbytes, p->k_cache, rbytes) ||
+        overlaps(p->y, qbytes, p->idx, ibytes))
+      return SA_ERR_OVERLAP;
+    return SA_OK;
+  }
   if (p->kv_dtype != p->q_dtype || dtype_bytes(p->q_dtype) == 0) return SA_ERR_DTYPE;
   if (!p->v_cache) return SA_ERR_NULL;
   if (p->Dv != p->D) return SA_ERR_UNSUPPORTED;
@@ -234,6 +304,10 @@ int sparse_plan(const sa_sparse_params* p, Plan& pl) {
   g.v_cur = p->v_cur;
   g.write_pos = p->write_pos;
   g.C = p->k_cur ? p->cur_len : 0;
+  if (p->kv_dtype == SA_FP8_E4M3_B64) {
+    g.record_stride = p->record_stride;
+    return plan_fp8(pl);
+  }
   int rc = plan_gather(pl, p->q_dtype);
   if (rc != SA_OK) return rc;
   if (pl.stream && !(aligned16(p->k_cache) && aligned16(p->v_cache)))
@@ -376,8 +450,8 @@ int sparse_attn_decode(const sa_sparse_params* p, void* stream) {
   pa.idx_is_i64 = p->idx_is_i64 ? 1 : 0;
   const size_t iesz = p->idx_is_i64 ? 8 : 4;
   pa.vec_ok = p->idx && aligned16(p->idx) && ((p->K * static_cast<int64_t>(iesz)) % 16 == 0);
-  pa.plan_rows = pl.stream ? 1 : 0;
-  pa.validate = pl.stream && p->K > 0 && (p->err_word || p->row_status);
+  pa.plan_rows = (pl.stream || pl.fp8) ? 1 : 0;
+  pa.validate = pa.plan_rows && p->K > 0 && (p->err_word || p->row_status);
   pa.causal = p->causal;
   pa.B = p->B;
   pa.I = p->I;
@@ -410,7 +484,7 @@ int sparse_attn_decode(const sa_sparse_params* p, void* stream) {
     pa.append_blocks = static_cast<int>(blocks);
   }
   if ((pa.plan_rows || pa.append_blocks) && sa::launch_plan(pa, st) != 0) return SA_ERR_LAUNCH;
-  if (!pl.stream && p->K > 0 && (p->err_word || p->row_status)) {
+  if (!pa.plan_rows && p->K > 0 && (p->err_word || p->row_status)) {
     sa::ValidateArgs v;
     v.idx = p->idx;
     v.is_i64 = p->idx_is_i64 ? 1 : 0;

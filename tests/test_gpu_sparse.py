@@ -317,3 +317,68 @@ def test_workspace_contents_on_entry_do_not_matter(cuda_lib):
         torch.cuda.synchronize()
         assert int(err.item()) == 0 and int(st.max().item()) == 0
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+
+
+# ---------------------------------------------------------------------------
+# FP8 hybrid-record latent cache (MQA, 512 E4M3 + 64 bf16 dims)
+# ---------------------------------------------------------------------------
+
+def _fp8_case(**over):
+    base = dict(B=2, Hq=64, T=3000, K=300, window=128, pad_prob=0.5, pad_max=60)
+    base.update(over)
+    return synth.csa_fp8(**base)
+
+
+def _run_fp8(sa, c, inp, **kw):
+    return sa.sparse_attn_decode(inp["q"].to(DEV), inp["kv_records"].to(DEV), None,
+                                 inp["idx"].to(DEV), scale=c.eff_scale(), window=c.window,
+                                 n_rope=c.n_rope, **kw)
+
+
+@pytest.mark.parametrize("over", [dict(), dict(record_stride=656), dict(Hq=32, K=40, T=500),
+                                  dict(window=0, K=700), dict(B=3, Hq=128, T=5000, K=1000)])
+def test_fp8_records_match_oracle(cuda_lib, over):
+    c = _fp8_case(**over)
+    inp = synth.make_sparse_inputs(c, seed=91)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = _run_fp8(cuda_lib, c, inp, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.sparse_attention(inp["q"], inp["idx"], records=inp["kv_records"],
+                                  n_rope=c.n_rope, scale=c.eff_scale(), window=c.window)
+    assert_close(to64(y), ref, y.dtype, f"fp8 {over}")
+
+
+def test_fp8_options_kv_len_softcap_sink_and_query_positions(cuda_lib):
+    c = _fp8_case(B=2, Hq=32, T=2000, K=200)
+    inp = synth.make_sparse_inputs(c, seed=92)
+    q2 = synth.normal((c.B, c.Hq, 2, c.D), "bf16", 93)
+    idx2 = inp["idx"].repeat(1, 1, 2, 1)
+    kv_len = torch.tensor([2000, 1500], dtype=torch.int64)
+    sink = torch.linspace(-2.0, 1.0, c.Hq, dtype=torch.float32)
+    inp2 = dict(inp, q=q2, idx=idx2)
+    y = _run_fp8(cuda_lib, c, inp2, kv_len=kv_len.to(DEV), softcap=4.0, sink=sink.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.sparse_attention(q2, idx2, records=inp["kv_records"], n_rope=c.n_rope,
+                                  scale=c.eff_scale(), window=c.window, kv_len=kv_len,
+                                  softcap=4.0, sink=sink.double())
+    assert_close(to64(y), ref, y.dtype, "fp8 options")
+
+
+def test_full_size_fp8_sampled_rows(cuda_lib):
+    """B16 Hq128 MQA D576 (648-byte records) T65536, window 128 + top-k 2048,
+    the benchmark's launch configuration, checked on sampled batches."""
+    c = synth.csa_fp8()
+    inp = synth.make_sparse_inputs(c, seed=1, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = cuda_lib.sparse_attn_decode(inp["q"], inp["kv_records"], None, inp["idx"],
+                                    scale=c.eff_scale(), window=c.window, n_rope=c.n_rope,
+                                    err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for b in (0, 11):
+        heads = list(range(0, c.Hq, 9))
+        ref = oracle.sparse_attention(inp["q"][b:b + 1].cpu(), inp["idx"][b:b + 1].cpu(),
+                                      records=inp["kv_records"][b:b + 1].cpu(), n_rope=c.n_rope,
+                                      scale=c.eff_scale(), window=c.window, rows=heads)
+        assert_close(to64(y[b, heads]), ref, y.dtype, f"fp8 full b={b}")
