@@ -229,6 +229,11 @@ int sparse_attn_decode_noalloc(const sa_sparse_params* p, void* stream);
  * softmax.  present_k / present_v (nullable, [B, Hkv, S, D]) receive exact
  * copies of k / v (past ++ current with an empty past).  dtype: SA_BF16 or
  * SA_F16, or SA_F32.  Workspace rules as for sparse_attn_decode.
+ * bf16 / f16 with D in {64, 128}, a positive scale and 16-byte aligned
+ * q / k / v / y run on the tcgen05 tensor-core kernel and need no workspace
+ * (a misaligned y there is SA_ERR_ALIGN); other shapes take the general
+ * kernel.  err_word (nullable) receives SA_ERRBIT_TIMEOUT if the tensor-core
+ * pipeline stalled, in which case y is unspecified.
  */
 typedef struct {
   const void* q;
@@ -244,6 +249,7 @@ typedef struct {
   float softcap;
   void* workspace;
   size_t workspace_bytes;
+  uint32_t* err_word;   /* nullable: SA_ERRBIT_TIMEOUT if a tensor-core pipeline stalled */
 } sa_prefill_params;
 
 size_t attn_prefill_workspace(const sa_prefill_params* p);

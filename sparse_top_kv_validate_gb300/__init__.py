@@ -66,7 +66,7 @@ class PrefillParams(C.Structure):
         ("dtype", _i32), ("causal", _i32),
         ("B", _i64), ("Hq", _i64), ("Hkv", _i64), ("S", _i64), ("D", _i64),
         ("scale", C.c_float), ("softcap", C.c_float),
-        ("workspace", _p), ("workspace_bytes", C.c_size_t),
+        ("workspace", _p), ("workspace_bytes", C.c_size_t), ("err_word", _p),
     ]
 
 
@@ -326,7 +326,7 @@ def sparse_attn_decode(q, k_cache, v_cache, idx, *, y=None, workspace=None, stre
     return y
 
 
-def _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap):
+def _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap, err_word=None):
     p = PrefillParams()
     B, Hq, S, D = q.shape
     p.q, p.k, p.v, p.y = q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(y)
@@ -334,6 +334,7 @@ def _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap):
     p.dtype, p.causal = _dt(q), int(bool(causal))
     p.B, p.Hq, p.Hkv, p.S, p.D = B, Hq, k.shape[1], S, D
     p.scale, p.softcap = float(scale), float(softcap)
+    p.err_word = _ptr(err_word)
     return p
 
 
@@ -343,7 +344,7 @@ def attn_prefill_workspace(q, k, v, causal=True, scale=0.0, softcap=0.0) -> int:
 
 
 def attn_prefill(q, k, v, *, causal=True, scale=0.0, softcap=0.0, y=None, present_k=None,
-                 present_v=None, workspace=None, stream=None):
+                 present_v=None, err_word=None, workspace=None, stream=None):
     """Dense prefill, ``q [B,Hq,S,D]``, ``k/v [B,Hkv,S,D]``; optional exact
     present K/V copies.  Returns ``y``."""
     L = load()
@@ -352,7 +353,7 @@ def attn_prefill(q, k, v, *, causal=True, scale=0.0, softcap=0.0, y=None, presen
         _dev(t, n)
     if y is None:
         y = torch.empty_like(q)
-    p = _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap)
+    p = _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap, err_word)
     need = int(L.attn_prefill_workspace(C.byref(p)))
     ws, nb = _workspace(need, q.device, workspace)
     p.workspace, p.workspace_bytes = _ptr(ws), nb

@@ -134,6 +134,22 @@ int launch_fp8_decode(const GatherArgs& a, cudaStream_t st);
 // Merge of the units the stream kernel split across warps.
 int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st);
 
+// ---- dense prefill on the fifth-generation tensor cores (tcgen05 + TMEM + TMA) ------
+struct PrefillTcArgs {
+  const void* q;              // [B, Hq, S, D]
+  const void* k;              // [B, Hkv, S, D]
+  const void* v;
+  void* y;                    // [B, Hq, S, D]
+  int dtype;                  // SA_BF16 or SA_F16
+  int causal;
+  int64_t B, Hq, Hkv, S, D;
+  float scale;                // > 0
+  float softcap;              // 0 = off
+  uint32_t* err_word;         // nullable: SA_ERRBIT_TIMEOUT on a stalled pipeline
+};
+bool prefill_tc_supported(const PrefillTcArgs& a);
+int launch_prefill_tc(const PrefillTcArgs& a, cudaStream_t st);
+
 // ---- paged: write the new token into the pool -----------------------------------
 struct PagedAppendArgs {
   void* k_pool;

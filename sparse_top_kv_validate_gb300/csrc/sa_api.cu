@@ -551,18 +551,66 @@ static void prefill_args(const sa_prefill_params* p, sa::GatherArgs& g) {
   g.inv_softcap = p->softcap != 0.f ? 1.0f / p->softcap : 0.f;
 }
 
+static void prefill_tc_args(const sa_prefill_params* p, sa::PrefillTcArgs& a) {
+  memset(&a, 0, sizeof(a));
+  a.q = p->q;
+  a.k = p->k;
+  a.v = p->v;
+  a.y = p->y;
+  a.dtype = p->dtype;
+  a.causal = p->causal;
+  a.B = p->B;
+  a.Hq = p->Hq;
+  a.Hkv = p->Hkv;
+  a.S = p->S;
+  a.D = p->D;
+  a.scale = p->scale != 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->D));
+  a.softcap = p->softcap;
+  a.err_word = p->err_word;
+}
+
+// Whether the tcgen05 kernel serves this call (bf16/f16, D in {64, 128},
+// positive scale, 16-byte aligned q / k / v); it needs no workspace.  The
+// output's alignment is not part of the choice (the workspace query has no
+// output): a misaligned y on this path is SA_ERR_ALIGN.
+static bool prefill_on_tc(const sa_prefill_params* p) {
+  sa::PrefillTcArgs a;
+  prefill_tc_args(p, a);
+  a.y = const_cast<void*>(a.q);
+  return sa::prefill_tc_supported(a);
+}
+
 size_t attn_prefill_workspace(const sa_prefill_params* p) {
   if (check_prefill(p, 1) != SA_OK) return 0;
+  if (prefill_on_tc(p)) return 0;
   Plan pl;
   prefill_args(p, pl.g);
   if (plan_gather(pl, p->dtype) != SA_OK) return 0;
   return pl.bytes;
 }
 
+static int copy_present(const sa_prefill_params* p, void* stream) {
+  if (!p->present_k && !p->present_v) return SA_OK;
+  const void* cur_k = p->present_k ? p->k : p->v;
+  void* out_k = p->present_k ? p->present_k : p->present_v;
+  const void* cur_v = (p->present_k && p->present_v) ? p->v : nullptr;
+  void* out_v = (p->present_k && p->present_v) ? p->present_v : nullptr;
+  return build_present_kv(nullptr, cur_k, out_k, nullptr, cur_v, out_v, p->dtype, p->B, p->Hkv, 0,
+                          p->S, p->D, p->S, nullptr, nullptr, stream);
+}
+
 int attn_prefill(const sa_prefill_params* p, void* stream) {
   int rc = check_prefill(p);
   if (rc != SA_OK) return rc;
   cudaStream_t st = as_stream(stream);
+  if (prefill_on_tc(p)) {
+    if (!aligned16(p->y)) return SA_ERR_ALIGN;
+    rc = copy_present(p, stream);
+    if (rc != SA_OK) return rc;
+    sa::PrefillTcArgs a;
+    prefill_tc_args(p, a);
+    return sa::launch_prefill_tc(a, st) == 0 ? SA_OK : SA_ERR_LAUNCH;
+  }
   Plan pl;
   prefill_args(p, pl.g);
   rc = plan_gather(pl, p->dtype);
@@ -570,15 +618,8 @@ int attn_prefill(const sa_prefill_params* p, void* stream) {
   if (pl.stream && !(aligned16(p->k) && aligned16(p->v))) return SA_ERR_ALIGN;
   rc = check_workspace(pl, p->workspace, p->workspace_bytes);
   if (rc != SA_OK) return rc;
-  if (p->present_k || p->present_v) {
-    const void* cur_k = p->present_k ? p->k : p->v;
-    void* out_k = p->present_k ? p->present_k : p->present_v;
-    const void* cur_v = (p->present_k && p->present_v) ? p->v : nullptr;
-    void* out_v = (p->present_k && p->present_v) ? p->present_v : nullptr;
-    rc = build_present_kv(nullptr, cur_k, out_k, nullptr, cur_v, out_v, p->dtype, p->B, p->Hkv,
-                          0, p->S, p->D, p->S, nullptr, nullptr, stream);
-    if (rc != SA_OK) return rc;
-  }
+  rc = copy_present(p, stream);
+  if (rc != SA_OK) return rc;
   carve(pl, p->workspace);
   return run_plan(pl, p->dtype, st);
 }

@@ -84,7 +84,10 @@ def test_full_size_paged_fp16_sampled_sequences(cuda_lib):
 
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("over", [dict(), dict(causal=False), dict(softcap=0.0),
-                                  dict(S=200, Hq=8, Hkv=8), dict(S=77, Hq=4, Hkv=1, D=64)])
+                                  dict(S=200, Hq=8, Hkv=8), dict(S=77, Hq=4, Hkv=1, D=64),
+                                  dict(S=1, Hq=4, Hkv=2), dict(S=256, Hq=6, Hkv=2),
+                                  dict(B=1, S=129, Hq=3, Hkv=1, causal=False),
+                                  dict(S=300, D=64, softcap=0.0, causal=False)])
 def test_prefill_matches_oracle_and_present_is_exact(cuda_lib, dt, over):
     base = dict(B=2, S=333, Hq=16, Hkv=4, D=128, causal=True, softcap=50.0, dtype=dt)
     base.update(over)
@@ -99,6 +102,17 @@ def test_prefill_matches_oracle_and_present_is_exact(cuda_lib, dt, over):
     ref = oracle.prefill(inp["q"], inp["k"], inp["v"], scale=c.eff_scale(), causal=c.causal,
                          softcap=c.softcap)
     assert_close(to64(y), ref, y.dtype, f"prefill {dt} {over}")
+
+
+def test_prefill_reports_no_timeout_and_is_deterministic(cuda_lib):
+    c = synth.PrefillCase("small", B=2, S=700, Hq=8, Hkv=2, D=128, causal=True, softcap=50.0)
+    inp = synth.make_prefill_inputs(c, seed=9, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ys = [cuda_lib.attn_prefill(inp["q"], inp["k"], inp["v"], causal=True, scale=c.eff_scale(),
+                                softcap=c.softcap, err_word=err) for _ in range(2)]
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(ys[0], ys[1])
 
 
 def test_full_size_prefill_sampled_rows(cuda_lib):
