@@ -9,25 +9,41 @@
 // set, then the causal mask, an fp32 softmax, and the probability-weighted
 // sum of V rows.
 //
-// GB300 design (one persistent CTA per SM, 12 warps):
-//  * A work item is two 128-row query tiles that read the same K/V stream:
-//    two query heads of one GQA group at the same positions, or (odd group
-//    sizes) neighbouring entries of the group's (position tile, head) list.
-//    Items go to CTAs in a snake order of decreasing causal length.
-//  * Warp 0 (one lane) is the TMA producer: the two Q tiles, then K_0, V_0,
-//    K_1, V_1, ... through a ring of 32 KB slots, every tile a set of
-//    128-byte-swizzled 64-column slabs.
-//  * Warp 1 owns the 512 TMEM columns and one lane issues every MMA:
-//    S_x = Q_x K_j^T (128 x 128 x D, both operands K-major from shared
-//    memory) and O_x += P_x V_j (P from tensor memory, V MN-major).
-//  * Warps 4-7 and 8-11 are the softmax warpgroups of tiles a and b; thread
-//    r owns row r (TMEM lane r).  Per KV tile it loads its S row, applies the
-//    scale / softcap (tanh.approx) / mask, keeps a running maximum that is
-//    raised only when a new score exceeds it by more than 2^8 (rescaling its
-//    O row in TMEM then), writes P = 2^(s - m) as 16-bit pairs over the S
-//    columns, and finally normalises its O row and stores it.
-//  * P aliases S: the MMA issuing order PV_x(j) -> S_x(j+1) keeps the read of
-//    P ahead of the next write of S.
+// GB300 design (one persistent CTA per SM; warps 0-3 service, 4.. softmax):
+//  * A work item is one 128-row query tile of one head; items go to CTAs in a
+//    snake order of decreasing causal length, neighbouring heads of a GQA
+//    group side by side so that their K/V reads meet in L2.
+//  * Warp 0 (one lane) is the TMA producer: the item's Q tile (two buffers,
+//    so the next item's Q arrives early), then the 128-key K and V tiles in
+//    the order the MMA lane consumes them through a ring of slots; every tile
+//    is a set of 128-byte-swizzled 64-column slabs.
+//  * Warp 1 owns the tensor memory -- three 128-column score buffers and the
+//    O accumulator -- and one lane issues every MMA: S(0), S(1), then per KV
+//    tile j: S(j+2) into buffer (j+2) % 3, O += P(j) V_j.  S = Q K^T (128 x
+//    128 x D) takes both operands K-major from shared memory; PV takes P from
+//    tensor memory and V MN-major.  Issuing two score tiles ahead keeps the
+//    tensor core fed while the lane waits for a P.  (tcgen05.mma issue
+//    returns only once the previous MMA has nearly finished, so every cycle
+//    this lane spends elsewhere is tensor-core idle time; a 128 x 64 MMA
+//    costs as long as a 128 x 128 one, so score tiles stay 128 keys wide.)
+//  * Warp 2 (one lane) writes the present K/V outputs: the item that reads all
+//    tiles of a (b, KV head) stores them from the ring with TMA.
+//  * The softmax warpgroup(s) split each row's keys (one group by default:
+//    thread r owns row r = TMEM lane r and all 128 keys of a tile).  Per tile
+//    a thread loads its scores, applies scale, softcap and mask, and writes
+//    P = 2^(s - m) as 16-bit pairs over its own score columns; at the end it
+//    normalises its O row and stores it.  With a softcap the logits are
+//    bounded and m is the constant 0 (exact: softmax is shift-invariant, and
+//    the bound keeps 2^logit and the row sums inside fp32's normal range);
+//    otherwise m is a running maximum raised only when a tile's maximum
+//    exceeds it by more than 2^8, O then rescaled in TMEM after the previous
+//    PV has completed.
+//  * The softcap's tanh runs on the FMA pipes as a fitted odd polynomial
+//    (paired fp32 arithmetic) for about two thirds of every thread's scores
+//    and on the MUFU tanh for the rest, so that neither pipe -- the MUFU one
+//    also carries the exponentials -- bounds the kernel; a warp whose tile
+//    holds a |score / softcap| outside the fitted range uses the MUFU tanh
+//    throughout.
 //  * Every mbarrier wait is bounded; a stalled pipeline sets
 //    SA_ERRBIT_TIMEOUT, stops every role, and still frees the tensor memory.
 #include <cuda.h>
@@ -35,6 +51,7 @@
 #include <cmath>
 #include <mutex>
 #include <type_traits>
+#include <utility>
 
 #include "kernels.h"
 #include "tc05.cuh"
@@ -43,31 +60,56 @@ namespace sa {
 
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kTile = 128;          // query rows and keys per tile
+#ifndef SA_PREFILL_GROUPS
+#define SA_PREFILL_GROUPS 1
+#endif
+constexpr int kGroups = SA_PREFILL_GROUPS;  // softmax warpgroups, each a share of every key tile
+constexpr int kThreads = 128 * (1 + kGroups);
+constexpr int kTile = 128;               // query rows per tile; keys per K/V tile
+constexpr int kGroupKeys = kTile / kGroups;  // keys of a tile per softmax warpgroup
 constexpr int kSlabBytes = kTile * 128;  // 128 rows x 64 sixteen-bit columns
 constexpr float kRescaleLog2 = 8.0f;     // lazy-maximum slack (factor 256)
+constexpr int kSBufs = 3;                // score buffers in tensor memory
+constexpr int kLead = kSBufs - 1;        // S(j + kLead) is issued before PV(j)
+constexpr int kTanhTerms = 5;            // tanh(x) ~= x * sum_k c_k (x^2)^k
+constexpr float kTanhPolyBound = 0.625f; // |x| range of the fit (abs error ~1e-7)
+// Largest softcap * log2(e) for which 2^(logit) needs no offset: logits in
+// [-97, 97] keep every probability a normal fp32 number and row sums over up
+// to 2^30 keys below 2^127.
+constexpr float kFixedOffsetMaxLog2 = 97.0f;
 
 template <int D>
 struct PGeo {
   static constexpr int kSlabs = D / 64;
   static constexpr int kTileBytes = kSlabs * kSlabBytes;        // 16 or 32 KB
-  static constexpr int kStages = D == 128 ? 4 : 8;              // K/V ring slots
-  static constexpr int kOffQ = 0;                               // Q_a, Q_b
-  static constexpr int kOffRing = 2 * kTileBytes;
-  static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
-  // barriers: q_full, q_empty, kv_full[kStages], kv_empty[kStages],
-  // s_full[2], p_full[2], o_full[2], done
-  static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2,
-                       kBarKvEmpty = 2 + kStages, kBarS = 2 + 2 * kStages,
-                       kBarP = kBarS + 2, kBarO = kBarP + 2, kBarDone = kBarO + 2,
-                       kNumBars = kBarDone + 1;
+#ifndef SA_PREFILL_QBUF
+#define SA_PREFILL_QBUF 2
+#endif
+#ifndef SA_PREFILL_STAGES128
+#define SA_PREFILL_STAGES128 4
+#endif
+  static constexpr int kQBufs = SA_PREFILL_QBUF;                // Q buffers (next item's Q early)
+  static constexpr int kStages = D == 128 ? SA_PREFILL_STAGES128 : 8;  // K/V ring slots
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffRing = kQBufs * kTileBytes;
+  static constexpr int kOffXch = kOffRing + kStages * kTileBytes;  // [2 rounds][groups][128] f32
+  static constexpr int kOffBar = kOffXch + 2 * kGroups * kTile * 4;
+  // barriers: q_full[2], q_empty[2] (per Q buffer), kv_full[kStages],
+  // kv_empty[kStages], s_full[3], p_full[3] (per score buffer), pv_done[2]
+  // (PV of even / odd tiles), o_full, xch[2] (softmax groups, per exchange
+  // round parity), done.  A buffer is refilled only after its previous
+  // contents were consumed, so no barrier that is waited on phase by phase
+  // ever has two phases outstanding.
+  static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKvFull = 4,
+                       kBarKvEmpty = kBarKvFull + kStages, kBarS = kBarKvEmpty + kStages,
+                       kBarP = kBarS + kSBufs, kBarPv = kBarP + kSBufs, kBarO = kBarPv + 2,
+                       kBarXch = kBarO + 1, kBarDone = kBarXch + 2, kNumBars = kBarDone + 1;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemUsed = kOffAbort + 4;
   static constexpr int kSmem = kSmemUsed + 1024;                // 1024-byte alignment slack
-  // tensor memory columns
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  // tensor memory columns: score buffers 0, 1, 2, then O
+  static constexpr uint32_t kColS = 0, kColO = kSBufs * kTile;
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -75,45 +117,32 @@ struct PGeo {
 struct PrefillKParams {
   void* y;
   uint32_t* err_word;
+  int write_present;  // bit 0: present_k, bit 1: present_v (through their tensor maps)
   int B, Hq, Hkv, S, g;
   int nq;             // query / key tiles per head: ceil(S / 128)
-  int pairs;          // items per (b, kvh): ceil(nq * g / 2)
-  int n_items;        // B * Hkv * pairs
+  int n_items;        // B * Hq * nq
   int causal;
-  int softcap_on;     // selects the kernel instantiation
-  float k1;           // score multiplier before tanh (scale / softcap), or 1
-  float c_log2;       // log2-domain multiplier after it (softcap * log2e or scale * log2e)
+  int softcap_on;     // 0 none, 1 softcap with a running maximum, 2 softcap, constant offset
+  float k1;           // x = score * k1 (scale / softcap), or the raw score
+  float c_log2;       // log2-domain multiplier of tanh(x) (softcap * log2e) or of x (scale * log2e)
+  float tq[kTanhTerms];  // c_log2 * c_k: the tanh polynomial already in log2 units
 };
 
 struct Item {
-  int b, kvh;
-  int head[2], qt[2], n[2];
-  int has_b;
-  int n_max;
+  int b, h, kvh, qt, n;   // n: KV tiles the query tile reads
 };
 
-// Item w: (b, kvh) = w % (B * Hkv); its pair index counts down with w / (B *
-// Hkv) so that longer causal items come first.  The group's query tiles are
-// listed position-tile major, (qt, hh) -> qt * g + hh, and paired in order.
+// Item w: (b, h) = w % (B * Hq), query tile counting down with w / (B * Hq) so
+// that longer causal items come first.
 __device__ __forceinline__ Item item_of(int w, const PrefillKParams& p) {
   Item it;
-  const int bk_n = p.B * p.Hkv;
-  const int bk = w % bk_n;
-  const int pair = p.pairs - 1 - w / bk_n;
-  it.b = bk / p.Hkv;
-  it.kvh = bk % p.Hkv;
-  const int total = p.nq * p.g;
-#pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    const int e = 2 * pair + x;
-    const int ee = e < total ? e : total - 1;
-    it.qt[x] = ee / p.g;
-    it.head[x] = it.kvh * p.g + ee % p.g;
-    it.n[x] = p.causal ? it.qt[x] + 1 : p.nq;
-  }
-  it.has_b = (2 * pair + 1) < total;
-  if (!it.has_b) it.n[1] = 0;
-  it.n_max = it.n[0] > it.n[1] ? it.n[0] : it.n[1];
+  const int bh_n = p.B * p.Hq;
+  const int bh = w % bh_n;
+  it.qt = p.nq - 1 - w / bh_n;
+  it.b = bh / p.Hq;
+  it.h = bh % p.Hq;
+  it.kvh = it.h / p.g;
+  it.n = p.causal ? it.qt + 1 : p.nq;
   return it;
 }
 
@@ -127,8 +156,9 @@ __device__ __forceinline__ int item_index(int k, int G) {
 // Bounded wait that turns a timeout into a CTA-wide abort.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
                                               volatile int* abort_flag, uint32_t* err_word) {
+  if (mbar_try_wait(bar, parity)) return true;  // the common case: no flag read
   if (*abort_flag) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (mbar_wait_sleep(bar, parity)) return true;
   *abort_flag = 1;
   if (err_word) atomicOr(err_word, static_cast<uint32_t>(SA_ERRBIT_TIMEOUT));
   return false;
@@ -142,10 +172,43 @@ __device__ __forceinline__ bool wait_or_abort_warp(uint64_t* bar, uint32_t parit
   return __all_sync(0xffffffffu, ok);
 }
 
+// ---- scalar and paired fp32 arithmetic -----------------------------------------------------
+
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two fp32 lanes in one 64-bit register (Blackwell paired FMA / ADD / MUL).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 }  // namespace
@@ -163,52 +226,130 @@ __device__ void prefill_producer(const CUtensorMap* tq, const CUtensorMap* tk,
   tc05::prefetch_tmap(tk);
   tc05::prefetch_tmap(tv);
   uint32_t kv_cnt = 0, q_cnt = 0;
-  for (int k = 0;; ++k) {
+  bool stop = false;
+  for (int k = 0; !stop; ++k) {
     const int w = item_index(k, static_cast<int>(gridDim.x));
     if (w >= p.n_items) break;
     const Item it = item_of(w, p);
-    if (q_cnt > 0 && !wait_or_abort(&bars[G::kBarQEmpty], (q_cnt - 1) & 1, abort_flag, p.err_word))
+    // Q buffer qb is free once the last S MMA of its previous item has completed.
+    const uint32_t qb = q_cnt % G::kQBufs, quse = q_cnt / G::kQBufs;
+    if (quse > 0 &&
+        !wait_or_abort(&bars[G::kBarQEmpty + qb], (quse - 1) & 1, abort_flag, p.err_word))
       break;
-    mbar_arrive_expect_tx(&bars[G::kBarQFull], (it.has_b ? 2u : 1u) * G::kTileBytes);
+    mbar_arrive_expect_tx(&bars[G::kBarQFull + qb], G::kTileBytes);
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      if (x == 1 && !it.has_b) break;
+    for (int s = 0; s < G::kSlabs; ++s)
+      tc05::tma_load3(sm + G::kOffQ + qb * G::kTileBytes + s * kSlabBytes, tq, s * 64,
+                      it.qt * kTile, it.b * p.Hq + it.h, &bars[G::kBarQFull + qb]);
+    ++q_cnt;
+    // K/V tiles in the order the MMA lane consumes them: K_0 .. K_(kLead-1),
+    // then per tile j: K_(j+kLead) (if any), V_j.
+    const int z = it.b * p.Hkv + it.kvh;
+    const int n = it.n;
+    for (int e = 0; e < 2 * n && !stop; ++e) {
+      // entry e -> (is_v, t): the first kLead entries are K tiles; after them
+      // the pairs (K_(j+kLead), V_j) while j + kLead < n, then the last V's.
+      bool is_v;
+      int t;
+      const int nk0 = n < kLead ? n : kLead;
+      if (e < nk0) {
+        is_v = false;
+        t = e;
+      } else if (e < nk0 + 2 * (n - nk0)) {
+        const int r = e - nk0;
+        is_v = (r & 1) != 0;
+        t = is_v ? r / 2 : r / 2 + kLead;
+      } else {
+        is_v = true;
+        t = e - n;
+      }
+      const uint32_t slot = kv_cnt % G::kStages, use = kv_cnt / G::kStages;
+      if (use > 0 && !wait_or_abort(&bars[G::kBarKvEmpty + slot], (use - 1) & 1, abort_flag,
+                                    p.err_word)) {
+        stop = true;
+        break;
+      }
+      mbar_arrive_expect_tx(&bars[G::kBarKvFull + slot], G::kTileBytes);
 #pragma unroll
       for (int s = 0; s < G::kSlabs; ++s)
-        tc05::tma_load3(sm + G::kOffQ + x * G::kTileBytes + s * kSlabBytes, tq, s * 64,
-                        it.qt[x] * kTile, it.b * p.Hq + it.head[x], &bars[G::kBarQFull]);
+        tc05::tma_load3(sm + G::kOffRing + slot * G::kTileBytes + s * kSlabBytes,
+                        is_v ? tv : tk, s * 64, t * kTile, z, &bars[G::kBarKvFull + slot]);
+      ++kv_cnt;
     }
-    ++q_cnt;
-    const int z = it.b * p.Hkv + it.kvh;
-    bool stop = false;
-    for (int j = 0; j < it.n_max && !stop; ++j) {
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        const uint32_t slot = kv_cnt % G::kStages, use = kv_cnt / G::kStages;
-        if (use > 0 && !wait_or_abort(&bars[G::kBarKvEmpty + slot], (use - 1) & 1, abort_flag,
-                                      p.err_word)) {
-          stop = true;
-          break;
-        }
-        mbar_arrive_expect_tx(&bars[G::kBarKvFull + slot], G::kTileBytes);
-#pragma unroll
-        for (int s = 0; s < G::kSlabs; ++s)
-          tc05::tma_load3(sm + G::kOffRing + slot * G::kTileBytes + s * kSlabBytes,
-                          kv ? tv : tk, s * 64, j * kTile, z, &bars[G::kBarKvFull + slot]);
-        ++kv_cnt;
-      }
-    }
-    if (stop) break;
   }
   if (*abort_flag) {
     // Let every copy already issued land before the CTA can exit.
-    if (q_cnt > 0) mbar_wait(&bars[G::kBarQFull], (q_cnt - 1) & 1);
+    for (uint32_t qb = 0; qb < G::kQBufs; ++qb) {
+      if (q_cnt <= qb) break;
+      const uint32_t issued = (q_cnt - qb + G::kQBufs - 1) / G::kQBufs;
+      mbar_wait(&bars[G::kBarQFull + qb], (issued - 1) & 1);
+    }
     for (uint32_t s = 0; s < G::kStages; ++s) {
       if (kv_cnt <= s) break;
       const uint32_t issued = (kv_cnt - s + G::kStages - 1) / G::kStages;
       mbar_wait(&bars[G::kBarKvFull + s], (issued - 1) & 1);
     }
   }
+}
+
+// ---- role: present-KV writer (one lane) --------------------------------------------------
+
+// Present K/V are exact copies of the inputs (there is no past).  K/V tile t
+// of a (b, kvh) is read by the item of query tile t of the group's first
+// head (its last tile when causal), which stores it from the ring to
+// present_k / present_v -- one tile pair per item, so the stores spread over
+// the whole grid.  Every ring slot takes two arrivals before it is refilled:
+// the MMA lane's and this lane's, given once the store (if any) has finished
+// reading shared memory.
+template <int D>
+__device__ void prefill_writer(const CUtensorMap* tpk, const CUtensorMap* tpv,
+                               const PrefillKParams& p, uint8_t* sm, uint64_t* bars,
+                               volatile int* abort_flag) {
+  using G = PGeo<D>;
+  uint32_t kv_cnt = 0;
+  bool stop = false;
+  for (int k = 0; !stop; ++k) {
+    const int w = item_index(k, static_cast<int>(gridDim.x));
+    if (w >= p.n_items) break;
+    const Item it = item_of(w, p);
+    const int n = it.n;
+    const bool owner = p.write_present != 0 && it.h % p.g == 0;
+    const int z = it.b * p.Hkv + it.kvh;
+    const int nk0 = n < kLead ? n : kLead;
+    for (int e = 0; e < 2 * n; ++e) {
+      // the producer's entry order: K_0 .. K_(kLead-1), then (K_(j+kLead), V_j) pairs, then V's
+      bool is_v;
+      int t;
+      if (e < nk0) {
+        is_v = false;
+        t = e;
+      } else if (e < nk0 + 2 * (n - nk0)) {
+        const int r = e - nk0;
+        is_v = (r & 1) != 0;
+        t = is_v ? r / 2 : r / 2 + kLead;
+      } else {
+        is_v = true;
+        t = e - n;
+      }
+      const uint32_t slot = kv_cnt % G::kStages;
+      if (!wait_or_abort(&bars[G::kBarKvFull + slot], (kv_cnt / G::kStages) & 1, abort_flag,
+                         p.err_word)) {
+        stop = true;
+        break;
+      }
+      ++kv_cnt;
+      if (owner && t == it.qt && ((p.write_present >> (is_v ? 1 : 0)) & 1)) {
+        const uint8_t* src = sm + G::kOffRing + slot * G::kTileBytes;
+#pragma unroll
+        for (int s2 = 0; s2 < G::kSlabs; ++s2)
+          tc05::tma_store3(is_v ? tpv : tpk, s2 * 64, t * kTile, z, src + s2 * kSlabBytes);
+        tc05::bulk_commit_group();
+        tc05::bulk_wait_group_read0();
+      }
+      mbar_arrive(&bars[G::kBarKvEmpty + slot]);
+    }
+  }
+  tc05::bulk_wait_group0();  // every store has reached global memory
 }
 
 // ---- role: MMA issuer (one lane) ----------------------------------------------------
@@ -219,91 +360,90 @@ __device__ void prefill_mma(const PrefillKParams& p, uint8_t* sm, uint64_t* bars
   using G = PGeo<D>;
   constexpr uint32_t id_s = tc05::idesc_f16(kTile, kTile, kBf16, false, false);
   constexpr uint32_t id_o = tc05::idesc_f16(kTile, D, kBf16, false, true);
-  const uint32_t sQ = smem_u32(sm + G::kOffQ), sRing = smem_u32(sm + G::kOffRing);
-  const uint32_t colS[2] = {G::kColS0, G::kColS1}, colO[2] = {G::kColO0, G::kColO1};
+  // Descriptors of Q buffer 0 and of ring slot 0; the start-address field
+  // (16-byte units, bits 0-13) then only advances by the byte offset / 16.
+  const uint64_t dQ = tc05::sw128_desc(smem_u32(sm + G::kOffQ), 16, 1024);
+  const uint64_t dK = tc05::sw128_desc(smem_u32(sm + G::kOffRing), 16, 1024);
+  const uint64_t dV = tc05::sw128_desc(smem_u32(sm + G::kOffRing), kSlabBytes, 1024);
 
-  auto issue_s = [&](int x, uint32_t slot) {
-    const uint32_t a0 = sQ + x * G::kTileBytes, b0 = sRing + slot * G::kTileBytes;
+  // S(j) = Q . K_j^T into score buffer j % 2
+  auto issue_s = [&](uint32_t qb, uint32_t slot, int buf) {
+    const uint64_t a0 = dQ + ((qb * G::kTileBytes) >> 4), b0 = dK + ((slot * G::kTileBytes) >> 4);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk / 4) * kSlabBytes + (kk % 4) * 32;
-      tc05::mma_ss(tmem + colS[x], tc05::sw128_desc(a0 + off, 16, 1024),
-                   tc05::sw128_desc(b0 + off, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+      const uint32_t off = ((kk / 4) * kSlabBytes + (kk % 4) * 32) >> 4;
+      tc05::mma_ss(tmem + G::kColS + buf * kTile, a0 + off, b0 + off, id_s, kk > 0 ? 1u : 0u);
     }
   };
-  auto issue_pv = [&](int x, uint32_t slot, bool acc) {
-    const uint32_t v0 = sRing + slot * G::kTileBytes;
+  // O += P(j) . V_j; P of group q's keys sits in the first half of that
+  // group's score columns (each softmax group writes over its own scores).
+  auto issue_pv = [&](uint32_t slot, int buf, bool acc) {
+    const uint64_t v0 = dV + ((slot * G::kTileBytes) >> 4);
+    const uint32_t a = tmem + G::kColS + buf * kTile;
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk)
-      tc05::mma_ts(tmem + colO[x], tmem + colS[x] + kk * 8,
-                   tc05::sw128_desc(v0 + kk * 2048, kSlabBytes, 1024), id_o,
-                   (acc || kk > 0) ? 1u : 0u);
+      tc05::mma_ts(tmem + G::kColO,
+                   a + (kk / (kGroupKeys / 16)) * kGroupKeys + (kk % (kGroupKeys / 16)) * 8,
+                   v0 + ((kk * 2048) >> 4), id_o, (acc || kk > 0) ? 1u : 0u);
   };
 
-  uint32_t kv_cnt = 0, q_cnt = 0, p_cnt[2] = {0, 0};
-  for (int k = 0;; ++k) {
+  uint32_t kv_cnt = 0, q_cnt = 0;
+  uint32_t p_par = 0;  // bit b: parity of the next p_full[b] phase
+  bool stop = false;
+  for (int k = 0; !stop; ++k) {
     const int w = item_index(k, static_cast<int>(gridDim.x));
     if (w >= p.n_items) break;
     const Item it = item_of(w, p);
-    if (!wait_or_abort(&bars[G::kBarQFull], q_cnt & 1, abort_flag, p.err_word)) break;
-    ++q_cnt;
-    uint32_t slotK = kv_cnt % G::kStages;
-    if (!wait_or_abort(&bars[G::kBarKvFull + slotK], (kv_cnt / G::kStages) & 1, abort_flag,
-                       p.err_word))
+    const uint32_t qb = q_cnt % G::kQBufs;
+    if (!wait_or_abort(&bars[G::kBarQFull + qb], (q_cnt / G::kQBufs) & 1, abort_flag, p.err_word))
       break;
-    ++kv_cnt;
-    tc05::fence_after_sync();
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      if (it.n[x] > 0) {
-        issue_s(x, slotK);
-        tc05::commit(&bars[G::kBarS + x]);
-      }
-    }
-    tc05::commit(&bars[G::kBarKvEmpty + slotK]);
-    bool stop = false;
-    for (int j = 0; j < it.n_max && !stop; ++j) {
-      const uint32_t slotV = kv_cnt % G::kStages;
-      if (!wait_or_abort(&bars[G::kBarKvFull + slotV], (kv_cnt / G::kStages) & 1, abort_flag,
-                         p.err_word)) {
+    ++q_cnt;
+    // Ring entries of this item, in consumption order: K_0 .. K_(kLead-1), then
+    // per tile j: K_(j+kLead) (if any), V_j.
+    const uint32_t base = kv_cnt;
+    const int n = it.n;
+    kv_cnt += 2 * n;
+    auto kidx = [&](int t) { return base + static_cast<uint32_t>(t < kLead ? t : 2 * t - kLead); };
+    auto vidx = [&](int t) {
+      return base + static_cast<uint32_t>(t < n - kLead ? kLead + 2 * t + 1 : n + t);
+    };
+    auto full = [&](uint32_t idx) {
+      return wait_or_abort(&bars[G::kBarKvFull + idx % G::kStages], (idx / G::kStages) & 1,
+                           abort_flag, p.err_word);
+    };
+    auto release = [&](uint32_t idx) { tc05::commit(&bars[G::kBarKvEmpty + idx % G::kStages]); };
+    // S(t) into buffer t % 3, then free its K tile; the item's last S frees Q.
+    auto score_tile = [&](int t) -> bool {
+      const uint32_t ki = kidx(t);
+      if (!full(ki)) return false;
+      tc05::fence_after_sync();
+      issue_s(qb, ki % G::kStages, t % kSBufs);
+      tc05::commit(&bars[G::kBarS + t % kSBufs]);
+      release(ki);
+      if (t == n - 1) tc05::commit(&bars[G::kBarQEmpty + qb]);
+      return true;
+    };
+
+    for (int t = 0; t < kLead && t < n && !stop; ++t) stop = !score_tile(t);
+    for (int j = 0; j < n && !stop; ++j) {
+      if (j + kLead < n && !score_tile(j + kLead)) {
         stop = true;
         break;
       }
-      ++kv_cnt;
-      const bool has_next = j + 1 < it.n_max;
-      if (has_next) {
-        slotK = kv_cnt % G::kStages;
-        if (!wait_or_abort(&bars[G::kBarKvFull + slotK], (kv_cnt / G::kStages) & 1, abort_flag,
-                           p.err_word)) {
-          stop = true;
-          break;
-        }
-        ++kv_cnt;
+      const uint32_t vi = vidx(j);
+      const int buf = j % kSBufs;
+      if (!full(vi) ||
+          !wait_or_abort(&bars[G::kBarP + buf], (p_par >> buf) & 1, abort_flag, p.err_word)) {
+        stop = true;
+        break;
       }
+      p_par ^= 1u << buf;
       tc05::fence_after_sync();
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (j < it.n[x]) {
-          if (!wait_or_abort(&bars[G::kBarP + x], p_cnt[x] & 1, abort_flag, p.err_word)) {
-            stop = true;
-            break;
-          }
-          ++p_cnt[x];
-          tc05::fence_after_sync();
-          issue_pv(x, slotV, j > 0);
-          if (j == it.n[x] - 1) tc05::commit(&bars[G::kBarO + x]);
-        }
-        if (has_next && j + 1 < it.n[x]) {
-          issue_s(x, slotK);
-          tc05::commit(&bars[G::kBarS + x]);
-        }
-      }
-      if (stop) break;
-      tc05::commit(&bars[G::kBarKvEmpty + slotV]);
-      if (has_next) tc05::commit(&bars[G::kBarKvEmpty + slotK]);
+      issue_pv(vi % G::kStages, buf, j > 0);
+      tc05::commit(&bars[G::kBarPv + (j & 1)]);
+      release(vi);
+      if (j == n - 1) tc05::commit(&bars[G::kBarO]);
     }
-    if (stop) break;
-    tc05::commit(&bars[G::kBarQEmpty]);
   }
   // Every MMA issued above completes before the tensor memory is released.
   tc05::commit(&bars[G::kBarDone]);
@@ -314,141 +454,286 @@ __device__ void prefill_mma(const PrefillKParams& p, uint8_t* sm, uint64_t* bars
 
 namespace {
 
-// ---- role: softmax warpgroup (tile x; thread = one query row) ---------------------------
+// ---- role: softmax warpgroups (group q owns keys [q, q + 1) * kGroupKeys of every tile) ----
 
-// O row *= alpha, in tensor memory (warp-collective).
-template <int D>
-__device__ __forceinline__ void rescale_o_row(uint32_t tO, float alpha) {
+// kCols columns of this thread's O row *= alpha, in tensor memory (warp-collective).
+template <int kCols>
+__device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
+  const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t o[32];
-    tc05::tmem_ld32(tO + c * 32, o);
+  for (int c = 0; c < kCols / 16; ++c) {
+    uint32_t o[16];
+    tc05::tmem_ld16(tO + c * 16, o);
     tc05::tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-    tc05::tmem_st32(tO + c * 32, o);
+    for (int i = 0; i < 8; ++i) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2), lo,
+                hi);
+      o[2 * i] = __float_as_uint(lo);
+      o[2 * i + 1] = __float_as_uint(hi);
+    }
+    tc05::tmem_st16(tO + c * 16, o);
   }
   tc05::tmem_st_wait();
 }
 
-// In place over the 128 raw scores of a row: t = tanh(s * k1) (softcap) or
-// t = s, masked columns (> rel) to -inf; returns max t.
-template <bool kSoftcap, bool kMask>
-__device__ __forceinline__ float score_pass(uint32_t (&r)[4][32], float k1, int rel) {
-  float mx[4] = {SA_NEG_INF, SA_NEG_INF, SA_NEG_INF, SA_NEG_INF};
+// Pass 1 over a thread's 32 raw scores: x = s * k1 in place (softcap; else
+// x = s); xmax = max of the unmasked x (columns <= rel; kNeedMax), amax =
+// max |x| (softcap).
+template <bool kSoftcap, bool kMask, bool kNeedMax>
+__device__ __forceinline__ void score_pass(uint32_t (&r)[kGroupKeys], float k1, int rel,
+                                           float& xmax, float& amax) {
+  const uint64_t k1x2 = f2_pack(k1, k1);
+  float mx[2] = {SA_NEG_INF, SA_NEG_INF}, ax[2] = {0.0f, 0.0f};
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float t = __uint_as_float(r[c][i]);
-      if (kSoftcap) t = tanh_approx(t * k1);
-      if (kMask && c * 32 + i > rel) t = SA_NEG_INF;
-      r[c][i] = __float_as_uint(t);
-      mx[i & 3] = fmaxf(mx[i & 3], t);
+  for (int i = 0; i < kGroupKeys / 2; ++i) {
+    float a = __uint_as_float(r[2 * i]), b = __uint_as_float(r[2 * i + 1]);
+    if (kSoftcap) {
+      f2_unpack(f2_mul(f2_pack(a, b), k1x2), a, b);
+      r[2 * i] = __float_as_uint(a);
+      r[2 * i + 1] = __float_as_uint(b);
+      ax[i & 1] = max3(ax[i & 1], fabsf(a), fabsf(b));
+    }
+    if (kNeedMax) {
+      if (kMask) {
+        if (2 * i > rel) a = SA_NEG_INF;
+        if (2 * i + 1 > rel) b = SA_NEG_INF;
+      }
+      mx[i & 1] = max3(mx[i & 1], a, b);
     }
   }
-  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  xmax = fmaxf(mx[0], mx[1]);
+  amax = fmaxf(ax[0], ax[1]);
 }
 
-template <int D, typename T, bool kSoftcap>
-__device__ void prefill_softmax(const PrefillKParams& p, uint64_t* bars, uint32_t tmem,
-                                volatile int* abort_flag) {
+// How the log2-domain logit of x is formed: c_log2 * x (no softcap), or
+// c_log2 * tanh(x) with the first kPolyPairs pairs of a thread's scores on
+// the polynomial and the rest on the MUFU tanh (kSplit: the two pipes then
+// carry about the same load), or all on the MUFU tanh (a score outside the
+// polynomial's range).
+enum ScoreMode { kPlain = 0, kSplit = 1, kMufu = 2 };
+constexpr int kPolyPairs = kGroupKeys * 11 / 32;  // of kGroupKeys / 2
+
+__device__ __forceinline__ float poly_logit(float x, const float (&tq)[kTanhTerms]) {
+  const float y = x * x;
+  float q = tq[kTanhTerms - 1];
+#pragma unroll
+  for (int k = kTanhTerms - 2; k >= 0; --k) q = fmaf(q, y, tq[k]);
+  return x * q;
+}
+
+// Pass 2: p = 2^(logit(x) - m), masked columns 0, written to tensor memory at
+// tP as 16 columns of 16-bit pairs; returns the two partial sums.
+template <int kMode, bool kMask, typename T>
+__device__ __forceinline__ uint64_t exp_pass(const uint32_t (&r)[kGroupKeys], uint32_t tP, float c2,
+                                             float neg_m, const float (&tq)[kTanhTerms], int rel) {
+  const uint64_t c2x2 = f2_pack(c2, c2), nm2 = f2_pack(neg_m, neg_m);
+  uint64_t ls[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
+  uint32_t pk[kGroupKeys / 2];
+#pragma unroll
+  for (int i = 0; i < kGroupKeys / 2; ++i) {
+    const float x0 = __uint_as_float(r[2 * i]), x1 = __uint_as_float(r[2 * i + 1]);
+    uint64_t v;
+    if (kMode == kPlain) {
+      v = f2_fma(f2_pack(x0, x1), c2x2, nm2);
+    } else if (kMode == kMufu || i >= kPolyPairs) {
+      v = f2_fma(f2_pack(tanh_approx(x0), tanh_approx(x1)), c2x2, nm2);
+    } else {
+      const uint64_t xx = f2_pack(x0, x1);
+      const uint64_t y = f2_mul(xx, xx);
+      uint64_t q = f2_fma(f2_pack(tq[4], tq[4]), y, f2_pack(tq[3], tq[3]));
+      q = f2_fma(q, y, f2_pack(tq[2], tq[2]));
+      q = f2_fma(q, y, f2_pack(tq[1], tq[1]));
+      q = f2_fma(q, y, f2_pack(tq[0], tq[0]));
+      v = f2_fma(xx, q, nm2);
+    }
+    float a, b;
+    f2_unpack(v, a, b);
+    if (kMask) {
+      if (2 * i > rel) a = SA_NEG_INF;
+      if (2 * i + 1 > rel) b = SA_NEG_INF;
+    }
+    a = ex2(a);
+    b = ex2(b);
+    ls[i & 1] = f2_add(ls[i & 1], f2_pack(a, b));
+    pk[i] = pack2<T>(a, b);
+  }
+#pragma unroll
+  for (int c = 0; c < kGroupKeys / 32; ++c)
+    tc05::tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
+  return f2_add(ls[0], ls[1]);
+}
+
+// Score variants: no softcap; softcap with a running maximum; softcap with the
+// constant offset 0.  With |softcap| * log2(e) <= kFixedOffsetMaxLog2 every
+// log2-domain logit lies within +-97, so 2^logit neither overflows nor
+// underflows fp32, nor does a row sum over up to 2^30 keys: the shift-
+// invariant softmax then needs no maximum at all (no cross-group exchange,
+// no O rescale).
+enum ScoreVariant { kVarPlain = 0, kVarSoftcapMax = 1, kVarSoftcapFixed = 2 };
+
+template <int D, typename T, int kVariant>
+__device__ void prefill_softmax(const PrefillKParams& p, uint8_t* sm, uint64_t* bars,
+                                uint32_t tmem, volatile int* abort_flag) {
   using G = PGeo<D>;
+  constexpr bool kSoftcap = kVariant != kVarPlain;
+  constexpr bool kFixed = kVariant == kVarSoftcapFixed;
+  constexpr int kOCols = D / kGroups;  // O columns normalised and stored by each group
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
-  const int x = (warp - 4) >> 2;
+  const int q = (warp - 4) >> 2;  // keys [q, q + 1) * kGroupKeys of every tile
   const int row = ((warp & 3) << 5) | lane;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t tS = tmem + lane_base + (x ? G::kColS1 : G::kColS0);
-  const uint32_t tO = tmem + lane_base + (x ? G::kColO1 : G::kColO0);
-  uint64_t* s_full = &bars[G::kBarS + x];
-  uint64_t* p_full = &bars[G::kBarP + x];
-  uint64_t* o_full = &bars[G::kBarO + x];
-  const float c2 = p.c_log2;
-  uint32_t s_cnt = 0, o_cnt = 0;
+  const uint32_t tS = tmem + lane_base + G::kColS + q * kGroupKeys;  // + buffer * 128
+  const uint32_t tO = tmem + lane_base + G::kColO + q * kOCols;
+  float* xch = reinterpret_cast<float*>(sm + G::kOffXch);
+  const float c2 = p.c_log2, k1 = p.k1;
+  float tq[kTanhTerms];
+#pragma unroll
+  for (int k = 0; k < kTanhTerms; ++k) tq[k] = p.tq[k];
+  // Phase parities as bit masks (bit b: next phase of barrier b): s_full per
+  // score buffer; pv_done per tile parity, flipped when this thread hands a P
+  // to the MMA lane (the PV it starts then completes that barrier's next phase).
+  uint32_t s_par = 0, pv_par = 0, o_cnt = 0, x_cnt = 0;
+  bool stop = false;
 
-  for (int k = 0;; ++k) {
+  // Share a value with the other groups of the same row (bounded; false on
+  // abort); returns their maximum (kMax) or sum.
+  auto exchange = [&](float v, bool kMax, float& out) -> bool {
+    if (kGroups == 1) {  // the whole row is this thread's
+      out = v;
+      return true;
+    }
+    const uint32_t slot = x_cnt & 1;
+    xch[(slot * kGroups + q) * kTile + row] = v;
+    mbar_arrive(&bars[G::kBarXch + slot]);
+    if (!wait_or_abort_warp(&bars[G::kBarXch + slot], (x_cnt >> 1) & 1, abort_flag, p.err_word))
+      return false;
+    ++x_cnt;
+    const float* e = &xch[slot * kGroups * kTile + row];
+    float acc = e[0];
+#pragma unroll
+    for (int g2 = 1; g2 < kGroups; ++g2) acc = kMax ? fmaxf(acc, e[g2 * kTile]) : acc + e[g2 * kTile];
+    out = acc;
+    return true;
+  };
+
+  for (int k = 0; !stop; ++k) {
     const int w = item_index(k, static_cast<int>(gridDim.x));
     if (w >= p.n_items) break;
     const Item it = item_of(w, p);
-    const int n = it.n[x];
-    if (n == 0) continue;
-    const int qi = it.qt[x] * kTile + row;
+    const int qi = it.qt * kTile + row;
     const int lim = p.causal ? min(qi, p.S - 1) : p.S - 1;  // last visible key
     float m = SA_NEG_INF, l = 0.0f;
-    bool stop = false;
-    for (int j = 0; j < n; ++j) {
-      if (!wait_or_abort_warp(s_full, s_cnt & 1, abort_flag, p.err_word)) {
+    for (int j = 0; j < it.n; ++j) {
+      const int buf = j % kSBufs;
+      if (!wait_or_abort_warp(&bars[G::kBarS + buf], (s_par >> buf) & 1, abort_flag, p.err_word)) {
         stop = true;
         break;
       }
-      ++s_cnt;
+      s_par ^= 1u << buf;
       tc05::fence_after_sync();
-      uint32_t r[4][32];
+      const uint32_t tSb = tS + buf * kTile;
+      uint32_t r[kGroupKeys];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc05::tmem_ld32(tS + c * 32, r[c]);
+      for (int c = 0; c < kGroupKeys / 32; ++c)
+        tc05::tmem_ld32(tSb + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
       tc05::tmem_ld_wait();
 
-      // scores -> (softcap) -> mask; row maximum
-      const int rel = lim - j * kTile;  // columns above rel are masked
-      const float mt =
-          (rel < kTile - 1 ? score_pass<kSoftcap, true>(r, p.k1, rel)
-                           : score_pass<kSoftcap, false>(r, p.k1, rel)) * c2;
-
-      // lazy maximum: raise it only when the tile's maximum exceeds it by the slack
-      const bool raise = mt > m + kRescaleLog2;
-      const bool any_raise = __any_sync(0xffffffffu, raise);
+      // pass 1: x, its masked maximum and its largest magnitude
+      const int rel = lim - j * kTile - q * kGroupKeys;  // columns above rel are masked
+      const bool masked = __any_sync(0xffffffffu, rel < kGroupKeys - 1);
+      float xmax, amax;
+      if (masked)
+        score_pass<kSoftcap, true, !kFixed>(r, k1, rel, xmax, amax);
+      else
+        score_pass<kSoftcap, false, !kFixed>(r, k1, rel, xmax, amax);
+      const int mode =
+          !kSoftcap ? kPlain
+                    : (__any_sync(0xffffffffu, amax > kTanhPolyBound) ? kMufu : kSplit);
+      bool any_raise = false;
       float alpha = 1.0f;
-      if (raise) {
-        alpha = ex2(m - mt);
-        l *= alpha;
-        m = mt;
-      }
-      const float neg_m = m == SA_NEG_INF ? 0.0f : -m;
-
-      // probabilities, written over the S columns as 16-bit pairs
-      float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(r[c][2 * i]), c2, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(r[c][2 * i + 1]), c2, neg_m));
-          ls[i & 3] += p0 + p1;
-          pk[i] = pack2<T>(p0, p1);
+      if (!kFixed) {
+        float mt = SA_NEG_INF;
+        if (xmax != SA_NEG_INF)
+          mt = mode == kPlain   ? xmax * c2
+               : mode == kSplit ? poly_logit(xmax, tq)
+                                : tanh_approx(xmax) * c2;
+        if (!exchange(mt, true, mt)) {
+          stop = true;
+          break;
         }
-        tc05::tmem_st16(tS + c * 16, pk);
+        // lazy maximum (every group takes the same decision from the same values)
+        const bool raise = mt > m + kRescaleLog2;
+        any_raise = __any_sync(0xffffffffu, raise);
+        if (raise) {
+          alpha = ex2(m - mt);
+          l *= alpha;
+          m = mt;
+        }
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // O (complete up to tile j - 1: its MMA preceded this S) follows the new maximum
-      if (any_raise && j > 0) rescale_o_row<D>(tO, alpha);
+      const float neg_m = (kFixed || m == SA_NEG_INF) ? 0.0f : -m;
+
+      // pass 2: probabilities over this group's own score columns
+      uint64_t ls;
+      if (mode == kPlain)
+        ls = masked ? exp_pass<kPlain, true, T>(r, tSb, c2, neg_m, tq, rel)
+                    : exp_pass<kPlain, false, T>(r, tSb, c2, neg_m, tq, rel);
+      else if (mode == kSplit)
+        ls = masked ? exp_pass<kSplit, true, T>(r, tSb, c2, neg_m, tq, rel)
+                    : exp_pass<kSplit, false, T>(r, tSb, c2, neg_m, tq, rel);
+      else
+        ls = masked ? exp_pass<kMufu, true, T>(r, tSb, c2, neg_m, tq, rel)
+                    : exp_pass<kMufu, false, T>(r, tSb, c2, neg_m, tq, rel);
+      {
+        float a, b;
+        f2_unpack(ls, a, b);
+        l += a + b;
+      }
+      // O follows the new maximum once PV(j - 1) has completed.  PVs of odd and
+      // even tiles complete on separate barriers; on PV(j - 1)'s barrier the
+      // phase before it, PV(j - 3), is complete (S(j) was issued after it), so
+      // only PV(j - 1)'s phase can be outstanding.
+      if (!kFixed && any_raise && j > 0) {
+        const int pb = (j - 1) & 1;
+        if (!wait_or_abort_warp(&bars[G::kBarPv + pb], ((pv_par >> pb) & 1) ^ 1u, abort_flag,
+                                p.err_word)) {
+          stop = true;
+          break;
+        }
+        tc05::fence_after_sync();
+        rescale_o<kOCols>(tO, alpha);
+      }
       tc05::tmem_st_wait();
       tc05::fence_before_sync();
-      mbar_arrive(p_full);
+      mbar_arrive(&bars[G::kBarP + buf]);
+      pv_par ^= 1u << (j & 1);
     }
     if (stop) break;
 
-    // epilogue: O row / l -> y
-    if (!wait_or_abort_warp(o_full, o_cnt & 1, abort_flag, p.err_word)) break;
+    // epilogue: the row sum is the groups' sums; this group stores O columns
+    // [q * D / 4, (q + 1) * D / 4) / l
+    float lt;
+    if (!exchange(l, false, lt)) break;
+    if (!wait_or_abort_warp(&bars[G::kBarO], o_cnt & 1, abort_flag, p.err_word)) break;
     ++o_cnt;
     tc05::fence_after_sync();
-    const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+    const float inv_l = lt > 0.0f ? 1.0f / lt : 0.0f;
     T* yrow = static_cast<T*>(p.y) +
-              ((static_cast<int64_t>(it.b) * p.Hq + it.head[x]) * p.S + qi) * D;
+              ((static_cast<int64_t>(it.b) * p.Hq + it.h) * p.S + qi) * D + q * kOCols;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      tc05::tmem_ld32(tO + c * 32, o);
+    for (int c = 0; c < kOCols / 16; ++c) {
+      uint32_t o[16];
+      tc05::tmem_ld16(tO + c * 16, o);
       tc05::tmem_ld_wait();
       if (qi < p.S) {
-        uint32_t pk[16];
+        uint32_t pk[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 8; ++i)
           pk[i] = pack2<T>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        uint4* dst = reinterpret_cast<uint4*>(yrow + c * 16);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
     }
   }
@@ -456,10 +741,11 @@ __device__ void prefill_softmax(const PrefillKParams& p, uint64_t* bars, uint32_
 
 // ---- kernel -------------------------------------------------------------------------------
 
-template <int D, typename T, bool kSoftcap>
+template <int D, typename T, int kVariant>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc05_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                        const __grid_constant__ CUtensorMap tv, const PrefillKParams p) {
+                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tpk,
+                        const __grid_constant__ CUtensorMap tpv, const PrefillKParams p) {
   using G = PGeo<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -470,17 +756,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[G::kBarQFull], 1);
-    mbar_init(&bars[G::kBarQEmpty], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[G::kBarQFull + i], 1);
+      mbar_init(&bars[G::kBarQEmpty + i], 1);
+      mbar_init(&bars[G::kBarPv + i], 1);
+      mbar_init(&bars[G::kBarXch + i], 128 * kGroups);
+    }
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(&bars[G::kBarS + i], 1);
+      mbar_init(&bars[G::kBarP + i], 128 * kGroups);
+    }
     for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&bars[G::kBarKvFull + s], 1);
-      mbar_init(&bars[G::kBarKvEmpty + s], 1);
+      mbar_init(&bars[G::kBarKvEmpty + s], 2);  // MMA lane + present writer
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars[G::kBarS + x], 1);
-      mbar_init(&bars[G::kBarP + x], 128);
-      mbar_init(&bars[G::kBarO + x], 1);
-    }
+    mbar_init(&bars[G::kBarO], 1);
     mbar_init(&bars[G::kBarDone], 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -499,8 +789,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0)
       prefill_mma<D, std::is_same<T, __nv_bfloat16>::value>(p, sm, bars, tmem, abort_flag);
+  } else if (warp == 2) {
+    if (lane == 0) prefill_writer<D>(&tpk, &tpv, p, sm, bars, abort_flag);
   } else if (warp >= 4) {
-    prefill_softmax<D, T, kSoftcap>(p, bars, tmem, abort_flag);
+    prefill_softmax<D, T, kVariant>(p, sm, bars, tmem, abort_flag);
   }
   __syncwarp();
   tc05::fence_before_sync();
@@ -555,60 +847,117 @@ static bool make_tile_map(CUtensorMap* m, const void* base, int dtype, int64_t D
 
 static bool al16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
 
+// Least-squares fit of tanh(x) / x = sum_k c_k (x^2)^k over 0 < x <= B
+// (Chebyshev nodes in x; normal equations in u = x^2 / B^2, solved in double
+// by Gaussian elimination with partial pivoting).  Evaluated in fp32 with
+// fused multiply-adds the polynomial stays within about 1e-7 of tanh on
+// |x| <= B = kTanhPolyBound, below the MUFU tanh's own error.
+static void fit_tanh_poly(double (&c)[kTanhTerms]) {
+  constexpr int kNodes = 2048;
+  const double B = kTanhPolyBound;
+  const double pi = 3.14159265358979323846;
+  double A[kTanhTerms][kTanhTerms + 1] = {};
+  for (int i = 0; i < kNodes; ++i) {
+    const double x = B * std::cos(pi * (i + 0.5) / (2.0 * kNodes));
+    const double u = x * x / (B * B), f = std::tanh(x) / x;
+    double pw[kTanhTerms];
+    pw[0] = 1.0;
+    for (int k = 1; k < kTanhTerms; ++k) pw[k] = pw[k - 1] * u;
+    for (int r = 0; r < kTanhTerms; ++r) {
+      for (int q = 0; q < kTanhTerms; ++q) A[r][q] += pw[r] * pw[q];
+      A[r][kTanhTerms] += pw[r] * f;
+    }
+  }
+  for (int col = 0; col < kTanhTerms; ++col) {
+    int piv = col;
+    for (int r = col + 1; r < kTanhTerms; ++r)
+      if (std::fabs(A[r][col]) > std::fabs(A[piv][col])) piv = r;
+    for (int q = 0; q <= kTanhTerms; ++q) std::swap(A[col][q], A[piv][q]);
+    for (int r = 0; r < kTanhTerms; ++r) {
+      if (r == col) continue;
+      const double f = A[r][col] / A[col][col];
+      for (int q = col; q <= kTanhTerms; ++q) A[r][q] -= f * A[col][q];
+    }
+  }
+  double scale = 1.0;  // 1 / B^(2k): back from u to x^2
+  for (int k = 0; k < kTanhTerms; ++k) {
+    c[k] = A[k][kTanhTerms] / A[k][k] * scale;
+    scale /= B * B;
+  }
+}
+
+static const double* tanh_poly() {
+  static std::once_flag once;
+  static double c[kTanhTerms];
+  std::call_once(once, [] { fit_tanh_poly(c); });
+  return c;
+}
+
 bool prefill_tc_supported(const PrefillTcArgs& a) {
   if (a.dtype != SA_BF16 && a.dtype != SA_F16) return false;
   if (a.D != 64 && a.D != 128) return false;
   if (!(a.scale > 0.0f) || !std::isfinite(a.scale) || !std::isfinite(a.softcap)) return false;
-  if (!al16(a.q) || !al16(a.k) || !al16(a.v) || !al16(a.y)) return false;
+  if (!al16(a.q) || !al16(a.k) || !al16(a.v) || !al16(a.y) || !al16(a.present_k) ||
+      !al16(a.present_v))
+    return false;
   if (a.S < 1 || a.S > (int64_t(1) << 30)) return false;
   const int64_t nq = (a.S + kTile - 1) / kTile;
-  const int64_t g = a.Hq / a.Hkv;
-  const int64_t items = a.B * a.Hkv * ((nq * g + 1) / 2);
-  if (items >= (int64_t(1) << 30) || a.B * a.Hq >= (int64_t(1) << 30)) return false;
+  if (a.B * a.Hq * nq >= (int64_t(1) << 30)) return false;  // item indices in int
   return encode_tiled() != nullptr;
 }
 
 template <int D, typename T>
 static int launch_prefill_t(const PrefillTcArgs& a, cudaStream_t st) {
   using G = PGeo<D>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tpk, tpv;
   if (!make_tile_map(&tq, a.q, a.dtype, D, a.S, a.B * a.Hq) ||
       !make_tile_map(&tk, a.k, a.dtype, D, a.S, a.B * a.Hkv) ||
       !make_tile_map(&tv, a.v, a.dtype, D, a.S, a.B * a.Hkv))
     return -1;
+  tpk = tk;  // placeholders when no present output is requested
+  tpv = tv;
+  if ((a.present_k && !make_tile_map(&tpk, a.present_k, a.dtype, D, a.S, a.B * a.Hkv)) ||
+      (a.present_v && !make_tile_map(&tpv, a.present_v, a.dtype, D, a.S, a.B * a.Hkv)))
+    return -1;
   PrefillKParams p;
   p.y = a.y;
   p.err_word = a.err_word;
+  p.write_present = (a.present_k ? 1 : 0) | (a.present_v ? 2 : 0);
   p.B = static_cast<int>(a.B);
   p.Hq = static_cast<int>(a.Hq);
   p.Hkv = static_cast<int>(a.Hkv);
   p.S = static_cast<int>(a.S);
   p.g = static_cast<int>(a.Hq / a.Hkv);
   p.nq = static_cast<int>((a.S + kTile - 1) / kTile);
-  p.pairs = (p.nq * p.g + 1) / 2;
-  p.n_items = p.B * p.Hkv * p.pairs;
+  p.n_items = p.B * p.Hq * p.nq;
   p.causal = a.causal ? 1 : 0;
   const float log2e = 1.4426950408889634f;
   if (a.softcap != 0.0f) {
     const float cap = std::fabs(a.softcap);
-    p.softcap_on = 1;
     p.k1 = a.scale / cap;
     p.c_log2 = cap * log2e;
+    p.softcap_on = p.c_log2 <= kFixedOffsetMaxLog2 ? 2 : 1;
+    const double* c = tanh_poly();
+    for (int k = 0; k < kTanhTerms; ++k)
+      p.tq[k] = static_cast<float>(c[k] * static_cast<double>(cap) * 1.4426950408889634);
   } else {
     p.softcap_on = 0;
     p.k1 = 1.0f;
     p.c_log2 = a.scale * log2e;
+    for (int k = 0; k < kTanhTerms; ++k) p.tq[k] = 0.0f;
   }
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return -1;
   const int grid = p.n_items < sms ? p.n_items : sms;
-  auto kern = p.softcap_on ? prefill_tc05_kernel<D, T, true> : prefill_tc05_kernel<D, T, false>;
+  auto kern = p.softcap_on == 0   ? prefill_tc05_kernel<D, T, kVarPlain>
+              : p.softcap_on == 1 ? prefill_tc05_kernel<D, T, kVarSoftcapMax>
+                                  : prefill_tc05_kernel<D, T, kVarSoftcapFixed>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem) !=
       cudaSuccess)
     return -1;
-  kern<<<grid, kThreads, G::kSmem, st>>>(tq, tk, tv, p);
+  kern<<<grid, kThreads, G::kSmem, st>>>(tq, tk, tv, tpk, tpv, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -140,6 +140,8 @@ struct PrefillTcArgs {
   const void* k;              // [B, Hkv, S, D]
   const void* v;
   void* y;                    // [B, Hq, S, D]
+  void* present_k;            // nullable: [B, Hkv, S, D] copy of k, written by the kernel
+  void* present_v;            // nullable: copy of v
   int dtype;                  // SA_BF16 or SA_F16
   int causal;
   int64_t B, Hq, Hkv, S, D;

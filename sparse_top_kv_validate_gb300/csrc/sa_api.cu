@@ -557,6 +557,8 @@ static void prefill_tc_args(const sa_prefill_params* p, sa::PrefillTcArgs& a) {
   a.k = p->k;
   a.v = p->v;
   a.y = p->y;
+  a.present_k = p->present_k;
+  a.present_v = p->present_v;
   a.dtype = p->dtype;
   a.causal = p->causal;
   a.B = p->B;
@@ -577,6 +579,7 @@ static bool prefill_on_tc(const sa_prefill_params* p) {
   sa::PrefillTcArgs a;
   prefill_tc_args(p, a);
   a.y = const_cast<void*>(a.q);
+  a.present_k = a.present_v = nullptr;  // checked per call, like y
   return sa::prefill_tc_supported(a);
 }
 
@@ -604,10 +607,9 @@ int attn_prefill(const sa_prefill_params* p, void* stream) {
   if (rc != SA_OK) return rc;
   cudaStream_t st = as_stream(stream);
   if (prefill_on_tc(p)) {
-    if (!aligned16(p->y)) return SA_ERR_ALIGN;
-    rc = copy_present(p, stream);
-    if (rc != SA_OK) return rc;
-    sa::PrefillTcArgs a;
+    if (!aligned16(p->y) || !aligned16(p->present_k) || !aligned16(p->present_v))
+      return SA_ERR_ALIGN;
+    sa::PrefillTcArgs a;  // present K/V are written by the kernel itself
     prefill_tc_args(p, a);
     return sa::launch_prefill_tc(a, st) == 0 ? SA_OK : SA_ERR_LAUNCH;
   }

@@ -87,7 +87,9 @@ def test_full_size_paged_fp16_sampled_sequences(cuda_lib):
                                   dict(S=200, Hq=8, Hkv=8), dict(S=77, Hq=4, Hkv=1, D=64),
                                   dict(S=1, Hq=4, Hkv=2), dict(S=256, Hq=6, Hkv=2),
                                   dict(B=1, S=129, Hq=3, Hkv=1, causal=False),
-                                  dict(S=300, D=64, softcap=0.0, causal=False)])
+                                  dict(S=300, D=64, softcap=0.0, causal=False),
+                                  dict(S=260, softcap=5.0), dict(S=260, softcap=2.0, causal=False),
+                                  dict(S=300, softcap=100.0), dict(S=129, softcap=80.0, causal=False)])
 def test_prefill_matches_oracle_and_present_is_exact(cuda_lib, dt, over):
     base = dict(B=2, S=333, Hq=16, Hkv=4, D=128, causal=True, softcap=50.0, dtype=dt)
     base.update(over)
@@ -95,9 +97,11 @@ def test_prefill_matches_oracle_and_present_is_exact(cuda_lib, dt, over):
     inp = synth.make_prefill_inputs(c, seed=5)
     q, k, v = (inp[n].to(DEV) for n in ("q", "k", "v"))
     pk, pv = torch.empty_like(k), torch.empty_like(v)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
     y = cuda_lib.attn_prefill(q, k, v, causal=c.causal, scale=c.eff_scale(), softcap=c.softcap,
-                              present_k=pk, present_v=pv)
+                              present_k=pk, present_v=pv, err_word=err)
     torch.cuda.synchronize()
+    assert int(err.item()) == 0
     assert torch.equal(pk.cpu(), inp["k"]) and torch.equal(pv.cpu(), inp["v"])
     ref = oracle.prefill(inp["q"], inp["k"], inp["v"], scale=c.eff_scale(), causal=c.causal,
                          softcap=c.softcap)
