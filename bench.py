@@ -331,7 +331,7 @@ class Prefill:
         S = c.S
         pairs = S * (S + 1) // 2 if c.causal else S * S
         self.flops = 4.0 * c.D * pairs * c.B * c.Hq
-        self.launches_per_step = 3
+        self.launches_per_step = 1  # one tensor-core kernel; present K/V written inside it
         self.h = {n: getattr(self, n).cpu().pin_memory() for n in ("q", "k", "v")}
         self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
 
@@ -481,6 +481,8 @@ class CsaFp8Decode:
 TRAFFIC: dict = {
     # plan + gather_stream + combine kernels of one call, ncu dram read + write
     "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 279922176,
+    # prefill_tc05_kernel, one launch (Q, K, V read; Y and present K/V written)
+    "prefill_bf16_b4_s4096_h32_kv8_d128_causal_softcap50": 441644032,
 }
 
 
