@@ -186,37 +186,75 @@ __global__ void __launch_bounds__(128) gather_simt_kernel(GatherArgs a) {
 // combine: y = sum_s o_s 2^(m_s - M) / (sum_s l_s 2^(m_s - M) [+ sink term])
 // ---------------------------------------------------------------------------
 
+constexpr int kCombineMaxSplits = 512;  // split weights kept in shared memory
+
 template <typename T>
 __global__ void __launch_bounds__(128) combine_kernel(GatherArgs a) {
+  __shared__ float w_s[kCombineMaxSplits];
+  __shared__ float inv_s;
   const int64_t hh = blockIdx.x % a.hpu;
   const int64_t unit = blockIdx.x / a.hpu;
   const UnitInfo u = unit_info(a, unit);
   const int64_t h = u.h0 + hh;
   const int64_t D = a.Dv;
+  const int splits = static_cast<int>(a.splits);
   const float* ml = a.part_ml + (unit * a.splits * a.hpu + hh) * 2;
   const int64_t mstride = a.hpu * 2;
-  float M = SA_NEG_INF;
-  for (int64_t s = 0; s < a.splits; ++s) M = fmaxf(M, ml[s * mstride]);
-  float L = 0.f;
-  if (M != SA_NEG_INF) {
-    for (int64_t s = 0; s < a.splits; ++s) {
+  // Split weights w_s = 2^(m_s - M) (0 for an empty split) and 1 / L, by warp 0.
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float M = SA_NEG_INF;
+    for (int s = lane; s < splits; s += 32) M = fmaxf(M, ml[s * mstride]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int s = lane; s < splits; s += 32) {
       const float ms = ml[s * mstride];
-      if (ms != SA_NEG_INF) L += ml[s * mstride + 1] * ex2(ms - M);
+      const float w = (M == SA_NEG_INF || ms == SA_NEG_INF) ? 0.f : ex2(ms - M);
+      if (s < kCombineMaxSplits) w_s[s] = w;
+      L += ml[s * mstride + 1] * w;
     }
-    if (a.sink) L += ex2(a.sink[h] * kLog2e - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) {
+      if (a.sink && M != SA_NEG_INF) L += ex2(a.sink[h] * kLog2e - M);
+      inv_s = (M == SA_NEG_INF || L == 0.f) ? 0.f : 1.0f / L;
+    }
   }
-  const float inv = (M == SA_NEG_INF || L == 0.f) ? 0.f : 1.0f / L;
+  __syncthreads();
+  const float inv = inv_s;
   T* yp = static_cast<T*>(a.y) + ((u.b * a.Hq + h) * a.Sq + u.i) * D;
-  for (int64_t d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.f;
-    if (M != SA_NEG_INF) {
-      for (int64_t s = 0; s < a.splits; ++s) {
-        const float ms = ml[s * mstride];
-        if (ms == SA_NEG_INF) continue;
-        acc += a.part_o[((unit * a.splits + s) * a.hpu + hh) * D + d] * ex2(ms - M);
+  const float* po = a.part_o + (unit * a.splits * a.hpu + hh) * D;
+  const int64_t pstride = a.hpu * D;  // between splits
+  if (splits <= kCombineMaxSplits && (D & 3) == 0) {
+    for (int64_t d = 4 * threadIdx.x; d < D; d += 4 * blockDim.x) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < splits; ++s) {
+        const float w = w_s[s];
+        if (w == 0.f) continue;
+        const float4 v = *reinterpret_cast<const float4*>(po + s * pstride + d);
+        acc.x = fmaf(v.x, w, acc.x);
+        acc.y = fmaf(v.y, w, acc.y);
+        acc.z = fmaf(v.z, w, acc.z);
+        acc.w = fmaf(v.w, w, acc.w);
       }
+      yp[d] = from_f32<T>(acc.x * inv);
+      yp[d + 1] = from_f32<T>(acc.y * inv);
+      yp[d + 2] = from_f32<T>(acc.z * inv);
+      yp[d + 3] = from_f32<T>(acc.w * inv);
     }
-    yp[d] = from_f32<T>(acc * inv);
+  } else {
+    float M = SA_NEG_INF;
+    for (int s = 0; s < splits; ++s) M = fmaxf(M, ml[s * mstride]);
+    for (int64_t d = threadIdx.x; d < D; d += blockDim.x) {
+      float acc = 0.f;
+      for (int s = 0; s < splits; ++s) {
+        const float ms = ml[s * mstride];
+        if (M == SA_NEG_INF || ms == SA_NEG_INF) continue;
+        acc += po[s * pstride + d] * ex2(ms - M);
+      }
+      yp[d] = from_f32<T>(acc * inv);
+    }
   }
 }
 

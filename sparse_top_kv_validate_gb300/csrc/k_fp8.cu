@@ -45,7 +45,7 @@ constexpr int kMaxChunkTiles = 64;
 constexpr int kOffQ = 0;                                   // [32][kRowStride]
 constexpr int kOffDec = kOffQ + kHeads * kRowStride;       // [16][kRowStride]
 constexpr int kOffRaw = kOffDec + 16 * kRowStride;         // [2][kRawStage]
-constexpr int kOffX = kOffRaw + 2 * kRawStage;             // [2 hg][4 q][32 lanes][8] f32
+constexpr int kOffX = kOffRaw + 2 * kRawStage;             // [2 hg][4 q][8 values][32 lanes] f32
 constexpr int kOffPos = kOffX + 2 * 4 * 32 * 8 * 4;        // [kMaxChunkTiles * 16] i32
 constexpr int kSmem = kOffPos + kMaxChunkTiles * 16 * 4;
 
@@ -72,6 +72,12 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t b) {
   if (b == 0u) return __int_as_float(0x00400000);  // 2^-127, a subnormal float
   return __int_as_float(static_cast<int>(b) << 23);
 }
+
+// The decoded tile keeps 16-byte chunk c of a row at chunk c ^ ((c >> 3) & 7)
+// (within its group of eight): the decode's stores, 16 lanes of one record
+// writing chunks 4p + i, then fall on distinct bank groups, while ldmatrix,
+// 8 rows at one chunk, stays conflict-free through the 73-chunk row stride.
+__device__ __forceinline__ int dec_chunk(int c) { return c ^ ((c >> 3) & 7); }
 
 }  // namespace
 
@@ -166,19 +172,19 @@ __global__ void __launch_bounds__(256, 2) fp8_decode_kernel(GatherArgs a) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) outw[i] = 0u;
       }
-      uint4* dst = reinterpret_cast<uint4*>(drow + (64 * k + 32 * h) * 2);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        dst[i] = make_uint4(outw[4 * i], outw[4 * i + 1], outw[4 * i + 2], outw[4 * i + 3]);
+        *reinterpret_cast<uint4*>(drow + dec_chunk(p * 4 + i) * 16) =
+            make_uint4(outw[4 * i], outw[4 * i + 1], outw[4 * i + 2], outw[4 * i + 3]);
       // RoPE tail: 64 little-endian bf16 = 128 bytes, two threads per record
       if (p < 2) {
-        uint4* rdst = reinterpret_cast<uint4*>(drow + kNope * 2 + 64 * p);
         const uint2* rsrc = reinterpret_cast<const uint2*>(raw + kNope / 64 * 65 + 64 * p);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint2 lo = valid ? rsrc[2 * i] : make_uint2(0, 0);
           const uint2 hi = valid ? rsrc[2 * i + 1] : make_uint2(0, 0);
-          rdst[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          *reinterpret_cast<uint4*>(drow + dec_chunk(kNope / 8 + 4 * p + i) * 16) =
+              make_uint4(lo.x, lo.y, hi.x, hi.y);
         }
       }
     }
@@ -194,23 +200,24 @@ __global__ void __launch_bounds__(256, 2) fp8_decode_kernel(GatherArgs a) {
       const uint32_t qa = smem_u32(sq) + (hg * 16 + (lane & 15)) * kRowStride +
                           (qd * kQuarter + 8 * (lane >> 4)) * 2;
       const int jm = lane >> 3, rr = lane & 7;
-      const uint32_t kbse = smem_u32(sdec) + (rr + 8 * (jm >> 1)) * kRowStride +
-                            (qd * kQuarter + 8 * (jm & 1)) * 2;
+      const uint32_t krow = smem_u32(sdec) + (rr + 8 * (jm >> 1)) * kRowStride;
+      const int kc0 = (qd * kQuarter) / 8 + (jm & 1);  // this lane's chunk at k-step 0
 #pragma unroll
       for (int kk = 0; kk < kKS; ++kk) {
         uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
         ldsm_x4(qa + kk * 32, a0, a1, a2, a3);
-        ldsm_x4(kbse + kk * 32, b0, b1, b2, b3);
+        ldsm_x4(krow + dec_chunk(kc0 + 2 * kk) * 16, b0, b1, b2, b3);
         mma16816<__nv_bfloat16>(s[0], a0, a1, a2, a3, b0, b1);
         mma16816<__nv_bfloat16>(s[1], a0, a1, a2, a3, b2, b3);
       }
     }
-    // sum the four quarters' partial scores of this head group
-    float* myx = sx + ((hg * 4 + qd) * 32 + lane) * 8;
+    // sum the four quarters' partial scores of this head group; sx is
+    // [hg][quarter][value][lane] so that every access is one word per lane
+    float* myx = sx + (hg * 4 + qd) * 8 * 32 + lane;
 #pragma unroll
     for (int n = 0; n < 2; ++n)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) myx[n * 4 + e] = s[n][e];
+      for (int e = 0; e < 4; ++e) myx[(n * 4 + e) * 32] = s[n][e];
     named_bar(1 + hg, 128);
 #pragma unroll
     for (int n = 0; n < 2; ++n)
@@ -218,7 +225,7 @@ __global__ void __launch_bounds__(256, 2) fp8_decode_kernel(GatherArgs a) {
       for (int e = 0; e < 4; ++e) {
         float acc = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc += sx[((hg * 4 + q) * 32 + lane) * 8 + n * 4 + e];
+        for (int q = 0; q < 4; ++q) acc += sx[((hg * 4 + q) * 8 + n * 4 + e) * 32 + lane];
         s[n][e] = acc;
       }
     // ---- online softmax (rows = heads gid, gid+8; columns = keys) -------------------------
@@ -242,14 +249,20 @@ __global__ void __launch_bounds__(256, 2) fp8_decode_kernel(GatherArgs a) {
       mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 1));
       mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 2));
     }
+    // Lazy running maximum: raised only when the tile's maximum exceeds it by
+    // more than 2^8 (probabilities up to 256 are exact enough in bf16), so the
+    // O accumulators are rescaled only on such tiles.
     float mu[2], al[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const float mn = fmaxf(m_run[j], mx[j]);
-      mu[j] = (mn == SA_NEG_INF) ? 0.f : mn;
-      al[j] = ex2(m_run[j] - mu[j]);
-      m_run[j] = mn;
+      al[j] = 1.0f;
+      if (mx[j] > m_run[j] + 8.0f) {  // also the first finite maximum
+        al[j] = ex2(m_run[j] - mx[j]);
+        m_run[j] = mx[j];
+      }
+      mu[j] = (m_run[j] == SA_NEG_INF) ? 0.f : m_run[j];
     }
+    const bool rescale = __any_sync(0xffffffffu, al[0] != 1.0f || al[1] != 1.0f);
     float ps[2] = {0.f, 0.f};
     uint32_t pa[4];
 #pragma unroll
@@ -263,22 +276,24 @@ __global__ void __launch_bounds__(256, 2) fp8_decode_kernel(GatherArgs a) {
     }
     l_run[0] = l_run[0] * al[0] + ps[0];
     l_run[1] = l_run[1] * al[1] + ps[1];
+    if (rescale) {
 #pragma unroll
-    for (int n = 0; n < kNT; ++n) {
-      o[n][0] *= al[0];
-      o[n][1] *= al[0];
-      o[n][2] *= al[1];
-      o[n][3] *= al[1];
+      for (int n = 0; n < kNT; ++n) {
+        o[n][0] *= al[0];
+        o[n][1] *= al[0];
+        o[n][2] *= al[1];
+        o[n][3] *= al[1];
+      }
     }
     // ---- O += P . V over this warp's quarter --------------------------------------------
     {
       const int jm = lane >> 3, rr = lane & 7;
-      const uint32_t vb = smem_u32(sdec) + (rr + 8 * (jm & 1)) * kRowStride +
-                          (qd * kQuarter + 8 * (jm >> 1)) * 2;
+      const uint32_t vrow = smem_u32(sdec) + (rr + 8 * (jm & 1)) * kRowStride;
+      const int vc0 = (qd * kQuarter) / 8 + (jm >> 1);
 #pragma unroll
       for (int n2 = 0; n2 < kNT / 2; ++n2) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + n2 * 32, b0, b1, b2, b3);
+        ldsm_x4_t(vrow + dec_chunk(vc0 + 2 * n2) * 16, b0, b1, b2, b3);
         mma16816<__nv_bfloat16>(o[2 * n2], pa[0], pa[1], pa[2], pa[3], b0, b1);
         mma16816<__nv_bfloat16>(o[2 * n2 + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
       }
