@@ -61,7 +61,7 @@ namespace sa {
 namespace {
 
 #ifndef SA_PREFILL_GROUPS
-#define SA_PREFILL_GROUPS 1
+#define SA_PREFILL_GROUPS 2
 #endif
 constexpr int kGroups = SA_PREFILL_GROUPS;  // softmax warpgroups, each a share of every key tile
 constexpr int kThreads = 128 * (1 + kGroups);
@@ -95,15 +95,15 @@ struct PGeo {
   static constexpr int kOffXch = kOffRing + kStages * kTileBytes;  // [2 rounds][groups][128] f32
   static constexpr int kOffBar = kOffXch + 2 * kGroups * kTile * 4;
   // barriers: q_full[2], q_empty[2] (per Q buffer), kv_full[kStages],
-  // kv_empty[kStages], s_full[3], p_full[3] (per score buffer), pv_done[2]
-  // (PV of even / odd tiles), o_full, xch[2] (softmax groups, per exchange
-  // round parity), done.  A buffer is refilled only after its previous
-  // contents were consumed, so no barrier that is waited on phase by phase
-  // ever has two phases outstanding.
+  // kv_empty[kStages], s_full[3], p_full[3], pv_free[3] (per score buffer:
+  // the PV that read its P has completed), o_full, xch[2] (softmax groups, per
+  // exchange round parity), done[2] (per MMA lane).  A buffer is refilled
+  // only after its previous contents were consumed, so no barrier that is
+  // waited on phase by phase ever has two phases outstanding.
   static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKvFull = 4,
                        kBarKvEmpty = kBarKvFull + kStages, kBarS = kBarKvEmpty + kStages,
-                       kBarP = kBarS + kSBufs, kBarPv = kBarP + kSBufs, kBarO = kBarPv + 2,
-                       kBarXch = kBarO + 1, kBarDone = kBarXch + 2, kNumBars = kBarDone + 1;
+                       kBarP = kBarS + kSBufs, kBarPv = kBarP + kSBufs, kBarO = kBarPv + kSBufs,
+                       kBarXch = kBarO + 1, kBarDone = kBarXch + 2, kNumBars = kBarDone + 2;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemUsed = kOffAbort + 4;
@@ -354,7 +354,14 @@ __device__ void prefill_writer(const CUtensorMap* tpk, const CUtensorMap* tpv,
 
 // ---- role: MMA issuer (one lane) ----------------------------------------------------
 
-template <int D, bool kBf16>
+// Two lanes issue the MMAs, on different warps (and so different schedulers):
+// the score lane S(g) for every KV tile g, as soon as its K tile is in and
+// the buffer's previous P has been consumed; the PV lane O += P(g) V_g as soon
+// as P(g) and V_g are in.  (tcgen05.mma issue returns only when the tensor
+// core can take the instruction, so each lane waits only on its own
+// dependencies while the other keeps the queue fed.)  Score buffers rotate
+// with a tile count g that runs on across the CTA's items.
+template <int D, bool kBf16, bool kScoreLane>
 __device__ void prefill_mma(const PrefillKParams& p, uint8_t* sm, uint64_t* bars, uint32_t tmem,
                             volatile int* abort_flag) {
   using G = PGeo<D>;
@@ -366,7 +373,7 @@ __device__ void prefill_mma(const PrefillKParams& p, uint8_t* sm, uint64_t* bars
   const uint64_t dK = tc05::sw128_desc(smem_u32(sm + G::kOffRing), 16, 1024);
   const uint64_t dV = tc05::sw128_desc(smem_u32(sm + G::kOffRing), kSlabBytes, 1024);
 
-  // S(j) = Q . K_j^T into score buffer j % 2
+  // S = Q . K^T into score buffer buf
   auto issue_s = [&](uint32_t qb, uint32_t slot, int buf) {
     const uint64_t a0 = dQ + ((qb * G::kTileBytes) >> 4), b0 = dK + ((slot * G::kTileBytes) >> 4);
 #pragma unroll
@@ -375,8 +382,8 @@ __device__ void prefill_mma(const PrefillKParams& p, uint8_t* sm, uint64_t* bars
       tc05::mma_ss(tmem + G::kColS + buf * kTile, a0 + off, b0 + off, id_s, kk > 0 ? 1u : 0u);
     }
   };
-  // O += P(j) . V_j; P of group q's keys sits in the first half of that
-  // group's score columns (each softmax group writes over its own scores).
+  // O += P . V; P of group q's keys sits in the first half of that group's
+  // score columns (each softmax group writes over its own scores).
   auto issue_pv = [&](uint32_t slot, int buf, bool acc) {
     const uint64_t v0 = dV + ((slot * G::kTileBytes) >> 4);
     const uint32_t a = tmem + G::kColS + buf * kTile;
@@ -387,19 +394,20 @@ __device__ void prefill_mma(const PrefillKParams& p, uint8_t* sm, uint64_t* bars
                    v0 + ((kk * 2048) >> 4), id_o, (acc || kk > 0) ? 1u : 0u);
   };
 
-  uint32_t kv_cnt = 0, q_cnt = 0;
-  uint32_t p_par = 0;  // bit b: parity of the next p_full[b] phase
+  uint32_t kv_cnt = 0, q_cnt = 0, g = 0;
+  uint32_t par = 0;  // bit b: parity of the next awaited phase of this lane's barrier b
   bool stop = false;
   for (int k = 0; !stop; ++k) {
     const int w = item_index(k, static_cast<int>(gridDim.x));
     if (w >= p.n_items) break;
     const Item it = item_of(w, p);
     const uint32_t qb = q_cnt % G::kQBufs;
-    if (!wait_or_abort(&bars[G::kBarQFull + qb], (q_cnt / G::kQBufs) & 1, abort_flag, p.err_word))
+    if (kScoreLane &&
+        !wait_or_abort(&bars[G::kBarQFull + qb], (q_cnt / G::kQBufs) & 1, abort_flag, p.err_word))
       break;
     ++q_cnt;
-    // Ring entries of this item, in consumption order: K_0 .. K_(kLead-1), then
-    // per tile j: K_(j+kLead) (if any), V_j.
+    // Ring entries of this item, in the producer's order: K_0 .. K_(kLead-1),
+    // then per tile j: K_(j+kLead) (if any), V_j.
     const uint32_t base = kv_cnt;
     const int n = it.n;
     kv_cnt += 2 * n;
@@ -412,42 +420,44 @@ __device__ void prefill_mma(const PrefillKParams& p, uint8_t* sm, uint64_t* bars
                            abort_flag, p.err_word);
     };
     auto release = [&](uint32_t idx) { tc05::commit(&bars[G::kBarKvEmpty + idx % G::kStages]); };
-    // S(t) into buffer t % 3, then free its K tile; the item's last S frees Q.
-    auto score_tile = [&](int t) -> bool {
-      const uint32_t ki = kidx(t);
-      if (!full(ki)) return false;
-      tc05::fence_after_sync();
-      issue_s(qb, ki % G::kStages, t % kSBufs);
-      tc05::commit(&bars[G::kBarS + t % kSBufs]);
-      release(ki);
-      if (t == n - 1) tc05::commit(&bars[G::kBarQEmpty + qb]);
-      return true;
-    };
 
-    for (int t = 0; t < kLead && t < n && !stop; ++t) stop = !score_tile(t);
-    for (int j = 0; j < n && !stop; ++j) {
-      if (j + kLead < n && !score_tile(j + kLead)) {
-        stop = true;
-        break;
+    for (int j = 0; j < n; ++j, ++g) {
+      const int buf = static_cast<int>(g % kSBufs);
+      if (kScoreLane) {
+        // the buffer's previous P (tile g - 3) must have been read by its PV
+        const uint32_t ki = kidx(j);
+        if ((g >= kSBufs &&
+             !wait_or_abort(&bars[G::kBarPv + buf], (par >> buf) & 1, abort_flag, p.err_word)) ||
+            !full(ki)) {
+          stop = true;
+          break;
+        }
+        if (g >= kSBufs) par ^= 1u << buf;
+        tc05::fence_after_sync();
+        issue_s(qb, ki % G::kStages, buf);
+        tc05::commit(&bars[G::kBarS + buf]);
+        release(ki);
+        if (j == n - 1) tc05::commit(&bars[G::kBarQEmpty + qb]);
+      } else {
+        const uint32_t vi = vidx(j);
+        if (!full(vi) ||
+            !wait_or_abort(&bars[G::kBarP + buf], (par >> buf) & 1, abort_flag, p.err_word)) {
+          stop = true;
+          break;
+        }
+        par ^= 1u << buf;
+        tc05::fence_after_sync();
+        issue_pv(vi % G::kStages, buf, j > 0);
+        tc05::commit(&bars[G::kBarPv + buf]);
+        release(vi);
+        if (j == n - 1) tc05::commit(&bars[G::kBarO]);
       }
-      const uint32_t vi = vidx(j);
-      const int buf = j % kSBufs;
-      if (!full(vi) ||
-          !wait_or_abort(&bars[G::kBarP + buf], (p_par >> buf) & 1, abort_flag, p.err_word)) {
-        stop = true;
-        break;
-      }
-      p_par ^= 1u << buf;
-      tc05::fence_after_sync();
-      issue_pv(vi % G::kStages, buf, j > 0);
-      tc05::commit(&bars[G::kBarPv + (j & 1)]);
-      release(vi);
-      if (j == n - 1) tc05::commit(&bars[G::kBarO]);
     }
   }
-  // Every MMA issued above completes before the tensor memory is released.
-  tc05::commit(&bars[G::kBarDone]);
-  mbar_wait(&bars[G::kBarDone], 0);
+  // Every MMA this lane issued completes before the tensor memory is released.
+  uint64_t* done = &bars[G::kBarDone + (kScoreLane ? 0 : 1)];
+  tc05::commit(done);
+  mbar_wait(done, 0);
 }
 
 }  // namespace
@@ -591,10 +601,11 @@ __device__ void prefill_softmax(const PrefillKParams& p, uint8_t* sm, uint64_t* 
   float tq[kTanhTerms];
 #pragma unroll
   for (int k = 0; k < kTanhTerms; ++k) tq[k] = p.tq[k];
-  // Phase parities as bit masks (bit b: next phase of barrier b): s_full per
-  // score buffer; pv_done per tile parity, flipped when this thread hands a P
-  // to the MMA lane (the PV it starts then completes that barrier's next phase).
-  uint32_t s_par = 0, pv_par = 0, o_cnt = 0, x_cnt = 0;
+  // Phase parities as bit masks (bit b: next phase of buffer b's barrier):
+  // s_full; pv_free, flipped when this thread hands a P to the PV lane (the PV
+  // it starts then completes that barrier's next phase).  Score buffers rotate
+  // with the tile count g across the CTA's items, as in the MMA lanes.
+  uint32_t s_par = 0, pv_par = 0, o_cnt = 0, x_cnt = 0, g = 0;
   bool stop = false;
 
   // Share a value with the other groups of the same row (bounded; false on
@@ -625,8 +636,8 @@ __device__ void prefill_softmax(const PrefillKParams& p, uint8_t* sm, uint64_t* 
     const int qi = it.qt * kTile + row;
     const int lim = p.causal ? min(qi, p.S - 1) : p.S - 1;  // last visible key
     float m = SA_NEG_INF, l = 0.0f;
-    for (int j = 0; j < it.n; ++j) {
-      const int buf = j % kSBufs;
+    for (int j = 0; j < it.n; ++j, ++g) {
+      const int buf = static_cast<int>(g % kSBufs);
       if (!wait_or_abort_warp(&bars[G::kBarS + buf], (s_par >> buf) & 1, abort_flag, p.err_word)) {
         stop = true;
         break;
@@ -690,12 +701,12 @@ __device__ void prefill_softmax(const PrefillKParams& p, uint8_t* sm, uint64_t* 
         f2_unpack(ls, a, b);
         l += a + b;
       }
-      // O follows the new maximum once PV(j - 1) has completed.  PVs of odd and
-      // even tiles complete on separate barriers; on PV(j - 1)'s barrier the
-      // phase before it, PV(j - 3), is complete (S(j) was issued after it), so
-      // only PV(j - 1)'s phase can be outstanding.
+      // O follows the new maximum once PV(g - 1) has completed.  On its
+      // buffer's pv_free barrier the phase before it, PV(g - 4), is complete
+      // (the score lane waited for it before issuing S(g - 1)), so only
+      // PV(g - 1)'s phase can be outstanding.
       if (!kFixed && any_raise && j > 0) {
-        const int pb = (j - 1) & 1;
+        const int pb = static_cast<int>((g + kSBufs - 1) % kSBufs);
         if (!wait_or_abort_warp(&bars[G::kBarPv + pb], ((pv_par >> pb) & 1) ^ 1u, abort_flag,
                                 p.err_word)) {
           stop = true;
@@ -707,7 +718,7 @@ __device__ void prefill_softmax(const PrefillKParams& p, uint8_t* sm, uint64_t* 
       tc05::tmem_st_wait();
       tc05::fence_before_sync();
       mbar_arrive(&bars[G::kBarP + buf]);
-      pv_par ^= 1u << (j & 1);
+      pv_par ^= 1u << buf;
     }
     if (stop) break;
 
@@ -759,19 +770,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[G::kBarQFull + i], 1);
       mbar_init(&bars[G::kBarQEmpty + i], 1);
-      mbar_init(&bars[G::kBarPv + i], 1);
       mbar_init(&bars[G::kBarXch + i], 128 * kGroups);
+      mbar_init(&bars[G::kBarDone + i], 1);
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&bars[G::kBarS + i], 1);
       mbar_init(&bars[G::kBarP + i], 128 * kGroups);
+      mbar_init(&bars[G::kBarPv + i], 1);
     }
     for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&bars[G::kBarKvFull + s], 1);
       mbar_init(&bars[G::kBarKvEmpty + s], 2);  // MMA lane + present writer
     }
     mbar_init(&bars[G::kBarO], 1);
-    mbar_init(&bars[G::kBarDone], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -788,7 +799,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) prefill_producer<D>(&tq, &tk, &tv, p, sm, bars, abort_flag);
   } else if (warp == 1) {
     if (lane == 0)
-      prefill_mma<D, std::is_same<T, __nv_bfloat16>::value>(p, sm, bars, tmem, abort_flag);
+      prefill_mma<D, std::is_same<T, __nv_bfloat16>::value, true>(p, sm, bars, tmem, abort_flag);
+  } else if (warp == 3) {
+    if (lane == 0)
+      prefill_mma<D, std::is_same<T, __nv_bfloat16>::value, false>(p, sm, bars, tmem, abort_flag);
   } else if (warp == 2) {
     if (lane == 0) prefill_writer<D>(&tpk, &tpv, p, sm, bars, abort_flag);
   } else if (warp >= 4) {
