@@ -9,35 +9,37 @@
 // set, then the causal mask, an fp32 softmax, and the probability-weighted
 // sum of V rows.
 //
-// GB300 design (one persistent CTA per SM; warps 0-3 service, 4.. softmax):
+// GB300 design (one persistent CTA per SM; warps 0-3 service, 4-11 softmax):
 //  * A work item is one 128-row query tile of one head; items go to CTAs in a
 //    snake order of decreasing causal length, neighbouring heads of a GQA
 //    group side by side so that their K/V reads meet in L2.
 //  * Warp 0 (one lane) is the TMA producer: the item's Q tile (two buffers,
 //    so the next item's Q arrives early), then the 128-key K and V tiles in
-//    the order the MMA lane consumes them through a ring of slots; every tile
+//    the order the MMA lanes consume them through a ring of slots; every tile
 //    is a set of 128-byte-swizzled 64-column slabs.
 //  * Warp 1 owns the tensor memory -- three 128-column score buffers and the
-//    O accumulator -- and one lane issues every MMA: S(0), S(1), then per KV
-//    tile j: S(j+2) into buffer (j+2) % 3, O += P(j) V_j.  S = Q K^T (128 x
-//    128 x D) takes both operands K-major from shared memory; PV takes P from
-//    tensor memory and V MN-major.  Issuing two score tiles ahead keeps the
-//    tensor core fed while the lane waits for a P.  (tcgen05.mma issue
-//    returns only once the previous MMA has nearly finished, so every cycle
-//    this lane spends elsewhere is tensor-core idle time; a 128 x 64 MMA
-//    costs as long as a 128 x 128 one, so score tiles stay 128 keys wide.)
-//  * Warp 2 (one lane) writes the present K/V outputs: the item that reads all
-//    tiles of a (b, KV head) stores them from the ring with TMA.
-//  * The softmax warpgroup(s) split each row's keys (one group by default:
-//    thread r owns row r = TMEM lane r and all 128 keys of a tile).  Per tile
-//    a thread loads its scores, applies scale, softcap and mask, and writes
-//    P = 2^(s - m) as 16-bit pairs over its own score columns; at the end it
-//    normalises its O row and stores it.  With a softcap the logits are
-//    bounded and m is the constant 0 (exact: softmax is shift-invariant, and
-//    the bound keeps 2^logit and the row sums inside fp32's normal range);
-//    otherwise m is a running maximum raised only when a tile's maximum
-//    exceeds it by more than 2^8, O then rescaled in TMEM after the previous
-//    PV has completed.
+//    O accumulator.  Two lanes issue the MMAs: warp 1's lane issues S(g) =
+//    Q K_g^T (128 x 128 x D, both operands K-major from shared memory) into
+//    buffer g % 3 once K_g is in and the buffer's previous P has been read;
+//    warp 3's lane issues O += P(g) V_g (P from tensor memory, V MN-major)
+//    once P(g) and V_g are in.  tcgen05.mma issue returns only when the
+//    tensor core can take the instruction, so with one issuing lane every
+//    wait or commit of that lane was tensor-idle time; with two, each waits
+//    only on its own inputs while the other keeps the queue fed.  (A 128 x 64
+//    MMA costs as long as a 128 x 128 one, so score tiles stay 128 keys
+//    wide.)
+//  * Warp 2 (one lane) writes the present K/V outputs: the item that reads
+//    K/V tile t as its last (diagonal) tile stores it from the ring with TMA.
+//  * Two softmax warpgroups split each row's keys (keys 0-63 and 64-127 of a
+//    tile); thread r of a group owns row r = TMEM lane r.  Per tile a thread
+//    loads its scores, applies scale, softcap and mask, and writes
+//    P = 2^(s - m) as 16-bit pairs over its own score columns; at the end the
+//    groups add their row sums and each normalises and stores half the O
+//    row.  With a softcap the logits are bounded and m is the constant 0
+//    (exact: softmax is shift-invariant, and the bound keeps 2^logit and the
+//    row sums inside fp32's normal range); otherwise m is a running maximum
+//    shared by the groups and raised only when a tile's maximum exceeds it by
+//    more than 2^8, O then rescaled in TMEM after the previous PV completed.
 //  * The softcap's tanh runs on the FMA pipes as a fitted odd polynomial
 //    (paired fp32 arithmetic) for about two thirds of every thread's scores
 //    and on the MUFU tanh for the rest, so that neither pipe -- the MUFU one
