@@ -475,6 +475,7 @@ __global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(Gat
 template <typename T, int D>
 __global__ void __launch_bounds__(128) stream_combine_kernel(GatherArgs a) {
   constexpr int kMaxW = 64;  // partials merged per pass
+  constexpr int kRegW = 8;   // up to this many partials: merged in registers
   pdl_wait();  // the stream kernel's partials and tile space
   const int64_t u = blockIdx.x;
   const int64_t R = a.meta[0];
@@ -493,6 +494,55 @@ __global__ void __launch_bounds__(128) stream_combine_kernel(GatherArgs a) {
   const UnitInfo ui = unit_info(a, u);
   const int hpu = static_cast<int>(a.hpu);
   const int64_t nw = w_hi - w_lo + 1;
+  if (nw <= kRegW) {
+    // Few partials: every thread loads all it needs at once -- its float4 of
+    // each partial and its head's (m, l) of each -- then merges in registers:
+    // one round trip to L2 after the stream kernel ends.
+    constexpr int kG2 = (16 * D / 4 + 127) / 128;
+#pragma unroll
+    for (int g = 0; g < kG2; ++g) {
+      const int e = threadIdx.x + 128 * g;
+      if (e >= hpu * D / 4) break;
+      const int hh = (e * 4) / D, d = (e * 4) % D;
+      float4 v[kRegW];
+      float2 ml[kRegW];
+#pragma unroll
+      for (int wi = 0; wi < kRegW; ++wi) {
+        if (wi < nw) {
+          const int64_t w = w_lo + wi;
+          const int64_t sb = (w * 2 + ((w * R >= off) ? 0 : 1)) * a.hpu + hh;
+          v[wi] = __ldg(reinterpret_cast<const float4*>(a.part_o + sb * D + d));
+          ml[wi] = __ldg(reinterpret_cast<const float2*>(a.part_ml) + sb);
+        }
+      }
+      float M = SA_NEG_INF;
+#pragma unroll
+      for (int wi = 0; wi < kRegW; ++wi)
+        if (wi < nw) M = fmaxf(M, ml[wi].x);
+      const float Mu = (M == SA_NEG_INF) ? 0.f : M;
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int wi = 0; wi < kRegW; ++wi) {
+        if (wi < nw && ml[wi].x != SA_NEG_INF) {
+          const float f = ex2(ml[wi].x - Mu);
+          L += ml[wi].y * f;
+          acc.x = fmaf(v[wi].x, f, acc.x);
+          acc.y = fmaf(v[wi].y, f, acc.y);
+          acc.z = fmaf(v[wi].z, f, acc.z);
+          acc.w = fmaf(v[wi].w, f, acc.w);
+        }
+      }
+      if (a.sink && M != SA_NEG_INF) L += ex2(a.sink[ui.h0 + hh] * kLog2e - M);
+      const float inv = (M == SA_NEG_INF || L == 0.f) ? 0.f : 1.0f / L;
+      T* yp = static_cast<T*>(a.y) + ((ui.b * a.Hq + ui.h0 + hh) * a.Sq + ui.i) * D + d;
+      yp[0] = from_f32<T>(acc.x * inv);
+      yp[1] = from_f32<T>(acc.y * inv);
+      yp[2] = from_f32<T>(acc.z * inv);
+      yp[3] = from_f32<T>(acc.w * inv);
+    }
+    return;
+  }
   __shared__ float sm_m[kMaxW][16], sm_l[kMaxW][16];
   __shared__ float sM[16], sL[16];
   if (threadIdx.x < hpu) {
