@@ -493,6 +493,9 @@ def make_workload(sa, name, dev):
         return SparseDecode(sa, synth.tiny_sparse(), dev)
     if name == "paged_fp16":
         return PagedDecode(sa, synth.paged_fp16(), dev)
+    if name == "paged_fp16_b16":  # the same sequences' distribution at 1/8 the batch (ncu-sized)
+        return PagedDecode(sa, synth.paged_fp16(
+            B=16, name="paged_fp16_b16_h32_kv8_d128_ctx1k-32k_p16"), dev)
     if name == "csa_fp8":
         return CsaFp8Decode(sa, synth.csa_fp8(), dev)
     if name == "prefill_bf16":
