@@ -1,0 +1,695 @@
+// k_fp8_tc.cu -- selected-token decode over the hybrid FP8 latent cache on the
+// fifth-generation tensor cores (tcgen05 + TMEM + TMA), for blocks of 128
+// query heads.
+//
+// Semantics: as k_fp8.cu -- the hybrid record of the compressed sparse
+// attention pages (onnx-runtime-ep-cpu compressed_sparse_attention.rs,
+// `CacheFormat::Fp8E4m3Block64`, `dequantize_cache`: blocks of [E8M0 scale
+// byte, 64 E4M3FN codes] then the RoPE dims as little-endian bf16), and
+// IndexShare's `index_share_row` over the candidates planned by k_plan.cu,
+// with K and V both the decoded 576-dim record.
+//
+// GB300 design: two kernels.
+//  1. fp8_gather_decode_kernel: one warp per planned candidate reads the
+//     record with coalesced 8-byte loads (three per warp), stages it in
+//     shared memory and writes the exact bf16 decode (e4m3 x 2^(scale-127);
+//     the RoPE tail copied) as row [unit, candidate] of a [units, n_cand_pad,
+//     576] bf16 buffer; masked candidates are zero rows.  Each record is
+//     decoded once, and the buffer (40 MB for 16 queries of 2176 keys) stays
+//     in L2 for the attention kernel.
+//  2. fp8_tc05_kernel: the 128 heads of a head block are the M of every MMA.
+//     The 128 x 576 fp32 output block (288 KB) is larger than one SM's tensor
+//     memory, so three CTAs share each (query position, head block, key
+//     split): each owns a third of the output dims (three 64-dim chunks) and
+//     computes the full 128-key score tiles itself.
+//      * Q (128 heads x 576) stays in shared memory for the whole CTA as nine
+//        128-byte-swizzled 64-dim slabs; warp 0's lane streams the decoded
+//        keys by TMA into a five-slot ring: for every 128-key tile the nine
+//        64-dim chunks for the scores, then the CTA's three chunks again as V.
+//      * Warp 1's lane issues S = Q K^T chunk by chunk into one of two TMEM
+//        score buffers; warp 2's lane issues O += P V (P from TMEM, V
+//        MN-major, N = 64 per chunk).  (Two lanes: tcgen05.mma issue returns
+//        only when the tensor core can take the instruction, so each lane
+//        should wait only on its own inputs.)
+//      * Warps 4-7 are the softmax warpgroup; thread r owns head r (TMEM lane
+//        r).  Per tile: the maximum raw score over the valid keys (scale and
+//        softcap are monotonic), a running maximum raised only by more than
+//        2^8 (O then rescaled in TMEM), then P as bf16 pairs written over the
+//        tile's own score columns.  At the end it writes the CTA's 192 output
+//        dims, normalised, or a partial (m, l, O) for the split combine.
+//      * Every mbarrier wait is bounded: a stalled pipeline sets
+//        SA_ERRBIT_TIMEOUT, stops every role and still frees the tensor
+//        memory.
+#include <cuda.h>
+#include <cuda_fp8.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+
+#include "kernels.h"
+#include "tc05.cuh"
+
+namespace sa {
+
+namespace {
+
+constexpr int kD = 576;
+constexpr int kRowBytes = kD * 2;        // decoded row: 576 bf16
+constexpr int kChunks = 9;               // 64-dim chunks: 8 FP8 blocks + the RoPE tail
+constexpr int kHeads = 128;              // M of every MMA
+constexpr int kKeys = 128;               // keys per tile (N of the score MMA)
+constexpr int kParts = 3;                // CTAs sharing a head block's output dims
+constexpr int kPartChunks = kChunks / kParts;  // 64-dim output chunks per CTA
+constexpr int kPartDims = kPartChunks * 64;    // 192
+constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 bf16, 128-byte swizzled
+constexpr int kStages = 5;               // ring of key chunks
+constexpr int kWarpLoad = 0, kWarpS = 1, kWarpPv = 2, kWarpSoftmax = 4;
+constexpr int kThreads = 256;
+constexpr int kMaxTiles = 48;            // tiles per CTA (validity staged in shared memory)
+constexpr int kRecRope = 8 * 65;         // byte offset of the RoPE tail in a record
+constexpr float kRescaleLog2 = 8.0f;
+
+// shared memory (bytes)
+constexpr int kOffQ = 0;                                    // 9 slabs [128 heads][64 dims]
+constexpr int kOffRing = kChunks * kChunkBytes;             // [kStages] key chunks
+constexpr int kOffValid = kOffRing + kStages * kChunkBytes; // [kMaxTiles][4] u32 bit masks
+constexpr int kOffBar = kOffValid + kMaxTiles * 16;
+// barriers: q_full, full_s[kStages], full_pv[kStages], empty[kStages],
+// s_full[2], p_full[2], pv_free[2], o_full, done[2].  A filled slot is
+// announced on full_s or full_pv by the lane that will read it: each of those
+// barriers then has one waiter that takes its phases in order (one ring
+// barrier shared by both lanes would let the PV lane, running ahead of the
+// fill, meet a phase two ahead of the barrier's and take it as complete).
+constexpr int kBarQ = 0, kBarFullS = 1, kBarFullPv = kBarFullS + kStages,
+              kBarEmpty = kBarFullPv + kStages, kBarS = kBarEmpty + kStages,
+              kBarP = kBarS + 2, kBarPv = kBarP + 2, kBarO = kBarPv + 2, kBarDone = kBarO + 1,
+              kNumBars = kBarDone + 2;
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+constexpr int kSmem = kOffAbort + 4 + 1024;                 // + alignment slack
+static_assert(kSmem <= 232448, "shared memory");
+// tensor memory: score buffers 0 and 1, then this CTA's output dims
+constexpr uint32_t kColS = 0, kColO = 2 * kKeys, kTmemCols = 512;
+static_assert(kColO + kPartDims <= kTmemCols, "tensor memory");
+
+struct Fp8TcParams {
+  const int32_t* pos;        // [units, n_cand_pad] planned cache positions or -1
+  int64_t n_cand_pad;        // multiple of 128
+  void* y;                   // [B, Hq, Sq, 576] bf16
+  float* part_o;             // splits > 1: [units * splits * Hq, 576] partial outputs
+  float* part_ml;            //             [units * splits * Hq, 2] (max, sum)
+  const float* sink;         // nullable [Hq]
+  uint32_t* err_word;
+  int B, Sq, Hq, hblocks, splits, chunk_tiles, tiles;
+  float scale_log2;          // scale * log2(e)
+  float k1, c_log2;          // softcap: logit2 = c_log2 * tanh(s * k1)
+};
+
+struct DecodeParams {
+  const char* recs;          // k_cache base: [B, 1, T, record_stride] bytes
+  int64_t record_stride;
+  int64_t T;
+  const int32_t* pos;        // [units, n_cand_pad]
+  int64_t rows;              // units * n_cand_pad
+  int64_t n_cand_pad;
+  int Sq;
+  __nv_bfloat16* kdec;       // [units, n_cand_pad, 576]
+};
+
+// The ring's entries, in order: the nine score chunks of tile 0, then for
+// each tile j: the nine score chunks of tile j + 1 (if any) and the CTA's
+// three output chunks of tile j.
+__device__ __forceinline__ uint32_t s_entry(int j, int c) {
+  return j == 0 ? static_cast<uint32_t>(c) : static_cast<uint32_t>(9 + 12 * (j - 1) + c);
+}
+__device__ __forceinline__ uint32_t pv_entry(int j, int k, int nt) {
+  return static_cast<uint32_t>(9 + 12 * j + (j + 1 < nt ? 9 : 0) + k);
+}
+// Entry e -> (tile j, chunk c, read by the score lane?).
+__device__ __forceinline__ void entry_of(int e, int nt, int part, int& j, int& c, bool& score) {
+  if (e < 9) {
+    j = 0;
+    c = e;
+    score = true;
+    return;
+  }
+  const int q = e - 9, blk = q / 12, rr = q % 12;
+  const bool more = blk + 1 < nt;
+  score = more && rr < 9;
+  if (score) {
+    j = blk + 1;
+    c = rr;
+  } else {
+    j = blk;
+    c = part * kPartChunks + (rr - (more ? 9 : 0));
+  }
+}
+
+// Two E4M3FN codes -> two floats, exactly (via the f16x2 conversion).
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
+  const __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// E8M0 scale byte -> 2^(b - 127); 255 is NaN in the format.
+__device__ __forceinline__ float e8m0_scale(uint32_t b) {
+  if (b == 255u) return __int_as_float(0x7fc00000);
+  if (b == 0u) return __int_as_float(0x00400000);  // 2^-127, a subnormal float
+  return __int_as_float(static_cast<int>(b) << 23);
+}
+
+}  // namespace
+
+namespace {
+
+// ---- kernel 1: gather + exact decode of the planned candidates' records ------------------
+
+// One warp per row [unit, candidate] of the decoded buffer (8 rows per CTA).
+__global__ void __launch_bounds__(256) fp8_gather_decode_kernel(const DecodeParams p) {
+  __shared__ __align__(16) uint2 stage[8][82];  // one 648-byte record per warp
+  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (row >= p.rows) return;
+  const int32_t pos = __ldg(p.pos + row);
+  uint4* out = reinterpret_cast<uint4*>(p.kdec + row * kD);  // 72 x 16 bytes
+  if (pos < 0) {
+    for (int i = lane; i < kRowBytes / 16; i += 32) out[i] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const int64_t b = (row / p.n_cand_pad) / p.Sq;
+  const uint2* rec = reinterpret_cast<const uint2*>(
+      p.recs + (b * p.T + pos) * p.record_stride);  // 8-byte aligned
+  uint2* st = stage[warp];
+  for (int i = lane; i < 81; i += 32) st[i] = __ldg(rec + i);
+  __syncwarp();
+  // FP8 dims: lane l decodes codes [16q, 16q + 16) of block c = l / 4, q = l % 4,
+  // record bytes 65c + 1 + 16q ..; the scale is byte 65c.
+  const int c = lane >> 2, q = lane & 3;
+  const unsigned char* sb = reinterpret_cast<const unsigned char*>(st);
+  const uint32_t* sw = reinterpret_cast<const uint32_t*>(st);
+  const float sc = e8m0_scale(sb[65 * c]);
+  const uint64_t sc2 = f2_pack(sc, sc);
+  const int first = 65 * c + 1 + 16 * q;
+  const int w0 = first >> 2, sh = (first & 3) * 8;
+  uint32_t w[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) w[i] = sw[w0 + i];
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t codes = sh ? __funnelshift_r(w[i], w[i + 1], sh) : w[i];
+    const float2 lo = e4m3x2_to_f2(codes & 0xffffu), hi = e4m3x2_to_f2(codes >> 16);
+    float a0, a1, b0, b1;
+    f2_unpack(f2_mul(f2_pack(lo.x, lo.y), sc2), a0, a1);
+    f2_unpack(f2_mul(f2_pack(hi.x, hi.y), sc2), b0, b1);
+    o[2 * i] = pack2<__nv_bfloat16>(a0, a1);
+    o[2 * i + 1] = pack2<__nv_bfloat16>(b0, b1);
+  }
+  out[8 * c + 2 * q] = make_uint4(o[0], o[1], o[2], o[3]);
+  out[8 * c + 2 * q + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  // RoPE dims 512 .. 575: the 128 bytes from record byte 520, as they are
+  if (lane < 8) {
+    const uint2 lo = st[kRecRope / 8 + 2 * lane], hi = st[kRecRope / 8 + 2 * lane + 1];
+    out[64 + lane] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+  }
+}
+
+}  // namespace
+
+namespace {
+
+// ---- kernel 2 roles: the TMA lane, the MMA issue lanes -------------------------------------
+
+// Q rows (b, hb * 128 + r, i) -> nine 128-byte-swizzled slabs; then the ring
+// entries in order, each a 128-key x 64-dim box of the decoded buffer.
+__device__ void fp8tc_producer(const CUtensorMap* tq, const CUtensorMap* tk, const Fp8TcParams& p,
+                               int unit, int hb, int t0, int nt, int part, uint8_t* sm,
+                               uint64_t* bars, volatile int* abort_flag) {
+  const int b = unit / p.Sq, i = unit % p.Sq;
+  tc05::prefetch_tmap(tq);
+  tc05::prefetch_tmap(tk);
+  mbar_arrive_expect_tx(&bars[kBarQ], kChunks * kChunkBytes);
+#pragma unroll 1
+  for (int c = 0; c < kChunks; ++c)
+    tc05::tma_load3(sm + kOffQ + c * kChunkBytes, tq, 64 * c, i, b * p.Hq + hb * kHeads,
+                    &bars[kBarQ]);
+  // per slot: armed at all, last fill read by the score lane, its parity;
+  // and the parity of the next phase of full_s / full_pv
+  uint32_t armed = 0, last_score = 0, last_par = 0, par_s = 0, par_pv = 0;
+  const int total = 12 * nt;
+  for (int e = 0; e < total; ++e) {
+    int j, c;
+    bool score;
+    entry_of(e, nt, part, j, c, score);
+    const uint32_t slot = static_cast<uint32_t>(e) % kStages, use = static_cast<uint32_t>(e) / kStages;
+    if (use > 0 && !wait_or_abort(&bars[kBarEmpty + slot], (use - 1) & 1, abort_flag, p.err_word))
+      break;
+    uint32_t& par = score ? par_s : par_pv;
+    const uint32_t ph = (par >> slot) & 1;
+    par ^= 1u << slot;
+    armed |= 1u << slot;
+    last_score = (last_score & ~(1u << slot)) | ((score ? 1u : 0u) << slot);
+    last_par = (last_par & ~(1u << slot)) | (ph << slot);
+    uint64_t* full = &bars[(score ? kBarFullS : kBarFullPv) + slot];
+    mbar_arrive_expect_tx(full, kChunkBytes);
+    tc05::tma_load3(sm + kOffRing + slot * kChunkBytes, tk, 64 * c, (t0 + j) * kKeys, unit, full);
+  }
+  // no copy may still be landing when the CTA exits
+  mbar_wait(&bars[kBarQ], 0);
+  for (int s = 0; s < kStages; ++s)
+    if ((armed >> s) & 1)
+      mbar_wait(&bars[(((last_score >> s) & 1) ? kBarFullS : kBarFullPv) + s], (last_par >> s) & 1);
+}
+
+// Every MMA this lane issued completes before the tensor memory is released.
+__device__ __forceinline__ void drain_lane(uint64_t* done) {
+  tc05::commit(done);
+  mbar_wait(done, 0);
+}
+
+// S_j = Q K_j^T into score buffer j & 1, one 64-dim chunk (4 k-steps) at a time.
+__device__ void fp8tc_score_lane(const Fp8TcParams& p, int nt, uint8_t* sm, uint64_t* bars,
+                                 uint32_t tmem, volatile int* abort_flag) {
+  constexpr uint32_t id_s = tc05::idesc_f16(kHeads, kKeys, true, false, false);
+  const uint64_t dQ = tc05::sw128_desc(smem_u32(sm + kOffQ), 16, 1024);
+  const uint64_t dK = tc05::sw128_desc(smem_u32(sm + kOffRing), 16, 1024);
+  bool ok = wait_or_abort(&bars[kBarQ], 0, abort_flag, p.err_word);
+  uint32_t par = 0;  // bit s: parity of the next awaited phase of full_s[s]
+  for (int j = 0; ok && j < nt; ++j) {
+    const int buf = j & 1;
+    // the buffer's previous P (tile j - 2) must have been read by its PV
+    if (j >= 2 && !wait_or_abort(&bars[kBarPv + buf], ((j - 2) >> 1) & 1, abort_flag, p.err_word))
+      break;
+    for (int c = 0; c < kChunks; ++c) {
+      const uint32_t e = s_entry(j, c), slot = e % kStages;
+      if (!wait_or_abort(&bars[kBarFullS + slot], (par >> slot) & 1, abort_flag, p.err_word)) {
+        ok = false;
+        break;
+      }
+      par ^= 1u << slot;
+      tc05::fence_after_sync();
+      const uint64_t a0 = dQ + ((static_cast<uint32_t>(c) * kChunkBytes) >> 4);
+      const uint64_t b0 = dK + ((slot * kChunkBytes) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc05::mma_ss(tmem + kColS + buf * kKeys, a0 + kk * 2, b0 + kk * 2, id_s,
+                     (c > 0 || kk > 0) ? 1u : 0u);
+      tc05::commit(&bars[kBarEmpty + slot]);
+    }
+    if (!ok) break;
+    tc05::commit(&bars[kBarS + buf]);
+  }
+  drain_lane(&bars[kBarDone + 0]);
+}
+
+// O[:, 64k .. 64k + 64) += P_j V_j[:, chunk part * 3 + k] for the CTA's three
+// output chunks; P_j is the bf16 pairs over score buffer j & 1's first 64
+// columns (keys 2i, 2i + 1 in column i).
+__device__ void fp8tc_pv_lane(const Fp8TcParams& p, int nt, uint8_t* sm, uint64_t* bars,
+                              uint32_t tmem, volatile int* abort_flag) {
+  constexpr uint32_t id_o = tc05::idesc_f16(kHeads, 64, true, false, true);
+  const uint64_t dV = tc05::sw128_desc(smem_u32(sm + kOffRing), kChunkBytes, 1024);
+  bool ok = true;
+  uint32_t par = 0;  // bit s: parity of the next awaited phase of full_pv[s]
+  for (int j = 0; ok && j < nt; ++j) {
+    const int buf = j & 1;
+    if (!wait_or_abort(&bars[kBarP + buf], (j >> 1) & 1, abort_flag, p.err_word)) break;
+    tc05::fence_after_sync();
+    for (int k = 0; k < kPartChunks; ++k) {
+      const uint32_t e = pv_entry(j, k, nt), slot = e % kStages;
+      if (!wait_or_abort(&bars[kBarFullPv + slot], (par >> slot) & 1, abort_flag, p.err_word)) {
+        ok = false;
+        break;
+      }
+      par ^= 1u << slot;
+      tc05::fence_after_sync();
+      const uint64_t v0 = dV + ((slot * kChunkBytes) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < kKeys / 16; ++kk)
+        tc05::mma_ts(tmem + kColO + 64 * k, tmem + kColS + buf * kKeys + 8 * kk,
+                     v0 + ((kk * 2048) >> 4), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+      tc05::commit(&bars[kBarEmpty + slot]);
+    }
+    if (!ok) break;
+    tc05::commit(&bars[kBarPv + buf]);
+    if (j == nt - 1) tc05::commit(&bars[kBarO]);
+  }
+  drain_lane(&bars[kBarDone + 1]);
+}
+
+}  // namespace
+
+namespace {
+
+// ---- kernel 2 role: softmax warpgroup (warps 4-7; thread r = head r = TMEM lane r) -------
+
+// kCols columns of this thread's O row *= alpha, in tensor memory (warp-collective).
+__device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
+  const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+  for (int c = 0; c < kPartDims / 32; ++c) {
+    uint32_t o[32];
+    tc05::tmem_ld32(tO + c * 32, o);
+    tc05::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2), lo,
+                hi);
+      o[2 * i] = __float_as_uint(lo);
+      o[2 * i + 1] = __float_as_uint(hi);
+    }
+    tc05::tmem_st32(tO + c * 32, o);
+  }
+  tc05::tmem_st_wait();
+}
+
+// Log2-domain logit of a raw score.
+template <bool kCap>
+__device__ __forceinline__ float logit2(float s, const Fp8TcParams& p) {
+  return kCap ? p.c_log2 * tanh_approx(s * p.k1) : s * p.scale_log2;
+}
+
+template <bool kCap>
+__device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split, int nt,
+                              int part, const uint32_t* valid, uint64_t* bars, uint32_t tmem,
+                              volatile int* abort_flag) {
+  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  float m_run = SA_NEG_INF, l_run = 0.0f;
+  bool ok = true;
+  for (int j = 0; j < nt; ++j) {
+    const int buf = j & 1;
+    // validity of the tile's keys 32k + bit (kept in scalars: the loops over k
+    // below are not unrolled)
+    const uint4 vm = reinterpret_cast<const uint4*>(valid)[j];
+    const uint32_t vm0 = vm.x, vm1 = vm.y, vm2 = vm.z, vm3 = vm.w;
+    auto valid_bits = [&](int k) { return k == 0 ? vm0 : k == 1 ? vm1 : k == 2 ? vm2 : vm3; };
+    if (!wait_or_abort_warp(&bars[kBarS + buf], (j >> 1) & 1, abort_flag, p.err_word)) {
+      ok = false;
+      break;
+    }
+    tc05::fence_after_sync();
+    const uint32_t tS = tl + kColS + buf * kKeys;
+    // pass 1: the largest raw score over the valid keys
+    float mx = SA_NEG_INF;
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+      uint32_t s[32];
+      tc05::tmem_ld32(tS + 32 * k, s);
+      tc05::tmem_ld_wait();
+      const uint32_t vk = valid_bits(k);
+      if (vk == 0xffffffffu) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mx = max3(mx, __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = ((vk >> (2 * i)) & 1u) ? __uint_as_float(s[2 * i]) : SA_NEG_INF;
+          const float c = ((vk >> (2 * i + 1)) & 1u) ? __uint_as_float(s[2 * i + 1]) : SA_NEG_INF;
+          mx = max3(mx, a, c);
+        }
+      }
+    }
+    // the lazy running maximum (log2 units): raised only past 2^8
+    const float mt = mx == SA_NEG_INF ? SA_NEG_INF : logit2<kCap>(mx, p);
+    float alpha = 1.0f;
+    if (mt > m_run + kRescaleLog2) {  // also the first finite maximum
+      alpha = ex2(m_run - mt);
+      m_run = mt;
+    }
+    const float mu = m_run == SA_NEG_INF ? 0.0f : m_run;
+    // O *= alpha before PV_j accumulates into it (PV_(j-1) must be complete)
+    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+      if (!wait_or_abort_warp(&bars[kBarPv + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag,
+                              p.err_word)) {
+        ok = false;
+        break;
+      }
+      tc05::fence_after_sync();
+      rescale_o(tl + kColO, alpha);
+    }
+    // pass 2: P = 2^(logit - mu) as bf16 pairs over the buffer's first 64 columns
+    float ls0 = 0.0f, ls1 = 0.0f;
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+      uint32_t s[32];
+      tc05::tmem_ld32(tS + 32 * k, s);
+      tc05::tmem_ld_wait();
+      const uint32_t vk = valid_bits(k);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float p0 = ex2(logit2<kCap>(__uint_as_float(s[2 * i]), p) - mu);
+        float p1 = ex2(logit2<kCap>(__uint_as_float(s[2 * i + 1]), p) - mu);
+        if (!((vk >> (2 * i)) & 1u)) p0 = 0.0f;
+        if (!((vk >> (2 * i + 1)) & 1u)) p1 = 0.0f;
+        ls0 += p0;
+        ls1 += p1;
+        pk[i] = pack2<__nv_bfloat16>(p0, p1);
+      }
+      tc05::tmem_st16(tS + 16 * k, pk);
+    }
+    tc05::tmem_st_wait();
+    l_run = l_run * alpha + (ls0 + ls1);
+    tc05::fence_before_sync();
+    mbar_arrive(&bars[kBarP + buf]);
+  }
+
+  // ---- epilogue: this CTA's 192 output dims of head row ----------------------------------
+  const int h = hb * kHeads + row;
+  const int b = unit / p.Sq, i = unit % p.Sq;
+  const bool have = nt > 0 && ok && wait_or_abort_warp(&bars[kBarO], 0, abort_flag, p.err_word);
+  if (have) tc05::fence_after_sync();
+  if (p.splits == 1) {
+    float L = l_run;
+    if (p.sink && m_run != SA_NEG_INF) L += ex2(p.sink[h] * kLog2e - m_run);
+    const float inv = (!have || m_run == SA_NEG_INF || L == 0.0f) ? 0.0f : 1.0f / L;
+    __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(p.y) +
+                        ((static_cast<int64_t>(b) * p.Hq + h) * p.Sq + i) * kD + part * kPartDims;
+#pragma unroll 1
+    for (int c = 0; c < kPartDims / 32; ++c) {
+      uint32_t o[32];
+      if (have) {
+        tc05::tmem_ld32(tl + kColO + c * 32, o);
+        tc05::tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = pack2<__nv_bfloat16>(__uint_as_float(o[8 * q + 2 * e]) * inv,
+                                      __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+        *reinterpret_cast<uint4*>(yp + c * 32 + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  } else {
+    const int64_t pidx = (static_cast<int64_t>(unit) * p.splits + split) * p.Hq + h;
+    float* po = p.part_o + pidx * kD + part * kPartDims;
+#pragma unroll 1
+    for (int c = 0; c < kPartDims / 32; ++c) {
+      uint32_t o[32];
+      if (have) {
+        tc05::tmem_ld32(tl + kColO + c * 32, o);
+        tc05::tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(po + c * 32 + 4 * q) =
+            make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    }
+    if (part == 0) {
+      p.part_ml[2 * pidx] = have ? m_run : SA_NEG_INF;
+      p.part_ml[2 * pidx + 1] = have ? l_run : 0.0f;
+    }
+  }
+}
+
+}  // namespace
+
+
+// One CTA per (unit = (batch, query position), 128-head block, key split,
+// third of the output dims): blockIdx.x = ((unit * hblocks + hb) * splits +
+// split) * 3 + part, so the three CTAs reading the same keys run together.
+template <bool kCap>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_tc05_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const Fp8TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffAbort);
+  uint32_t* valid = reinterpret_cast<uint32_t*>(sm + kOffValid);
+  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
+  int cta = static_cast<int>(blockIdx.x);
+  const int part = cta % kParts;
+  cta /= kParts;
+  const int split = cta % p.splits;
+  cta /= p.splits;
+  const int hb = cta % p.hblocks;
+  const int unit = cta / p.hblocks;
+  const int t0 = split * p.chunk_tiles;
+  int nt = p.tiles - t0;
+  if (nt > p.chunk_tiles) nt = p.chunk_tiles;  // chunk_tiles <= kMaxTiles (host)
+  if (nt < 0) nt = 0;
+
+  if (warp == kWarpS) {
+    tc05::tmem_alloc(tslot, kTmemCols);
+    tc05::tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[kBarQ], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[kBarFullS + s], 1);
+      mbar_init(&bars[kBarFullPv + s], 1);
+      mbar_init(&bars[kBarEmpty + s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kBarS + s], 1);
+      mbar_init(&bars[kBarP + s], 128);
+      mbar_init(&bars[kBarPv + s], 1);
+      mbar_init(&bars[kBarDone + s], 1);
+    }
+    mbar_init(&bars[kBarO], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // validity bit masks of this split's tiles: word 4j + k, bit i = key 32k + i
+  const int32_t* prow = p.pos + static_cast<int64_t>(unit) * p.n_cand_pad +
+                        static_cast<int64_t>(t0) * kKeys;
+  for (int w = warp; w < 4 * nt; w += kThreads / 32) {
+    const uint32_t m = __ballot_sync(0xffffffffu, __ldg(prow + 32 * w + lane) >= 0);
+    if (lane == 0) valid[w] = m;
+  }
+  tc05::fence_before_sync();
+  __syncthreads();
+  tc05::fence_after_sync();
+  const uint32_t tmem = *tslot;
+
+  if (warp == kWarpLoad) {
+    if (lane == 0) fp8tc_producer(&tq, &tk, p, unit, hb, t0, nt, part, sm, bars, abort_flag);
+  } else if (warp == kWarpS) {
+    if (lane == 0) fp8tc_score_lane(p, nt, sm, bars, tmem, abort_flag);
+  } else if (warp == kWarpPv) {
+    if (lane == 0) fp8tc_pv_lane(p, nt, sm, bars, tmem, abort_flag);
+  } else if (warp >= kWarpSoftmax) {
+    fp8tc_softmax<kCap>(p, unit, hb, split, nt, part, valid, bars, tmem, abort_flag);
+  }
+
+  tc05::fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpS) {
+    tc05::fence_after_sync();
+    tc05::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---- host side -----------------------------------------------------------------------------
+
+// SA_FP8_KERNEL=mma selects the warp-level MMA kernel for every head count.
+static bool tc_disabled() {
+  const char* v = std::getenv("SA_FP8_KERNEL");
+  return v && std::strcmp(v, "mma") == 0;
+}
+
+int fp8_tc_max_tiles() { return kMaxTiles; }
+size_t fp8_tc_decoded_row_bytes() { return kRowBytes; }
+
+bool fp8_tc_supported(const GatherArgs& g) {
+  if (tc_disabled()) return false;
+  if (g.D != kD || g.Dv != kD || g.Hkv != 1 || g.Hq % kHeads != 0) return false;
+  if (!(g.scale_log2 > 0.0f) || !std::isfinite(g.scale_log2)) return false;  // monotone logits
+  if (g.n_cand < 1 || g.record_stride < 648 || g.record_stride % 8 != 0) return false;
+  if (g.B * g.Hq * g.Sq >= (int64_t(1) << 31)) return false;
+  return encode_tiled() != nullptr;
+}
+
+static bool bf16_map(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[3],
+                     const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_tiled()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kCap>
+static int launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const Fp8TcParams& p,
+                    int64_t grid, cudaStream_t st) {
+  if (cudaFuncSetAttribute(fp8_tc05_kernel<kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmem) != cudaSuccess)
+    return -1;
+  fp8_tc05_kernel<kCap><<<static_cast<unsigned>(grid), kThreads, kSmem, st>>>(tq, tk, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
+  if (!fp8_tc_supported(g) || !g.fp8_kdec) return -1;
+  if (g.n_cand_pad % kKeys != 0 || g.chunk > kMaxTiles || g.chunk < 1) return -1;
+  const int64_t rows = g.units * g.n_cand_pad;
+  if (rows <= 0) return 0;
+  // kernel 1: decoded rows [units, n_cand_pad, 576]
+  DecodeParams d;
+  d.recs = static_cast<const char*>(g.k);
+  d.record_stride = g.record_stride;
+  d.T = g.T;
+  d.pos = g.pos;
+  d.rows = rows;
+  d.n_cand_pad = g.n_cand_pad;
+  d.Sq = static_cast<int>(g.Sq);
+  d.kdec = static_cast<__nv_bfloat16*>(g.fp8_kdec);
+  fp8_gather_decode_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(d);
+  if (cudaGetLastError() != cudaSuccess) return -1;
+  // kernel 2: Q as [B * Hq][Sq][576] in boxes of 64 dims x 1 position x 128
+  // heads; decoded keys as [units][n_cand_pad][576] in boxes of 64 dims x 128 keys
+  CUtensorMap tq, tk;
+  const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(g.Sq),
+                               static_cast<cuuint64_t>(g.B * g.Hq)};
+  const cuuint64_t qstr[2] = {static_cast<cuuint64_t>(kRowBytes),
+                              static_cast<cuuint64_t>(g.Sq * kRowBytes)};
+  const cuuint32_t qbox[3] = {64, 1, static_cast<cuuint32_t>(kHeads)};
+  const cuuint64_t kdims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(g.n_cand_pad),
+                               static_cast<cuuint64_t>(g.units)};
+  const cuuint64_t kstr[2] = {static_cast<cuuint64_t>(kRowBytes),
+                              static_cast<cuuint64_t>(g.n_cand_pad * kRowBytes)};
+  const cuuint32_t kbox[3] = {64, static_cast<cuuint32_t>(kKeys), 1};
+  if (!bf16_map(&tq, g.q, qdims, qstr, qbox) || !bf16_map(&tk, g.fp8_kdec, kdims, kstr, kbox))
+    return -1;
+  Fp8TcParams p;
+  p.pos = g.pos;
+  p.n_cand_pad = g.n_cand_pad;
+  p.y = g.y;
+  p.part_o = g.part_o;
+  p.part_ml = g.part_ml;
+  p.sink = g.sink;
+  p.err_word = g.err_word;
+  p.B = static_cast<int>(g.B);
+  p.Sq = static_cast<int>(g.Sq);
+  p.Hq = static_cast<int>(g.Hq);
+  p.hblocks = static_cast<int>(g.Hq / kHeads);
+  p.splits = static_cast<int>(g.splits);
+  p.chunk_tiles = static_cast<int>(g.chunk);
+  p.tiles = static_cast<int>(g.tiles_per_unit);
+  p.scale_log2 = g.scale_log2;
+  const float log2e = 1.4426950408889634f;
+  p.k1 = g.softcap != 0.0f ? (g.scale_log2 / log2e) * g.inv_softcap : 0.0f;
+  p.c_log2 = g.softcap * log2e;
+  const int64_t grid = g.units * p.hblocks * g.splits * kParts;
+  return g.softcap != 0.0f ? launch_t<true>(tq, tk, p, grid, st)
+                           : launch_t<false>(tq, tk, p, grid, st);
+}
+
+}  // namespace sa

@@ -155,64 +155,6 @@ __device__ __forceinline__ int item_index(int k, int G) {
   return k * G + ((k & 1) ? G - 1 - c : c);
 }
 
-// Bounded wait that turns a timeout into a CTA-wide abort.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
-                                              volatile int* abort_flag, uint32_t* err_word) {
-  if (mbar_try_wait(bar, parity)) return true;  // the common case: no flag read
-  if (*abort_flag) return false;
-  if (mbar_wait_sleep(bar, parity)) return true;
-  *abort_flag = 1;
-  if (err_word) atomicOr(err_word, static_cast<uint32_t>(SA_ERRBIT_TIMEOUT));
-  return false;
-}
-
-// The same, with one verdict for the whole warp (its lanes then stay converged
-// for the warp-collective tensor-memory instructions that follow).
-__device__ __forceinline__ bool wait_or_abort_warp(uint64_t* bar, uint32_t parity,
-                                                   volatile int* abort_flag, uint32_t* err_word) {
-  const bool ok = wait_or_abort(bar, parity, abort_flag, err_word);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// ---- scalar and paired fp32 arithmetic -----------------------------------------------------
-
-__device__ __forceinline__ float tanh_approx(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// Two fp32 lanes in one 64-bit register (Blackwell paired FMA / ADD / MUL).
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
 }  // namespace
 
 namespace {
@@ -823,12 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side -----------------------------------------------------------------------------
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_tiled() {
+EncodeTiledFn encode_tiled() {
   static std::once_flag once;
   static EncodeTiledFn fn = nullptr;
   std::call_once(once, [] {

@@ -111,6 +111,7 @@ struct GatherArgs {
   int64_t page_tokens, max_pages, num_pages;
   // FP8 hybrid records (sparse source)
   int64_t record_stride;      // bytes between records
+  void* fp8_kdec;             // tcgen05 FP8 path: decoded rows [units, n_cand_pad, 576] bf16
   // math
   float scale_log2;           // scale * log2(e)
   float softcap;              // 0 = off
@@ -131,6 +132,14 @@ int launch_gather_stream(const GatherArgs& a, int dtype, int grid, cudaStream_t 
 size_t fp8_smem_bytes();
 int fp8_chunk_tiles_max();
 int launch_fp8_decode(const GatherArgs& a, cudaStream_t st);
+// The same on the fifth-generation tensor cores for blocks of 128 query heads:
+// a gather kernel decodes the planned candidates' records into fp8_kdec, then
+// the attention kernel streams them by TMA (planned positions padded to
+// 128-key tiles, at most fp8_tc_max_tiles() tiles per key split).
+bool fp8_tc_supported(const GatherArgs& a);
+int fp8_tc_max_tiles();
+size_t fp8_tc_decoded_row_bytes();
+int launch_fp8_tc(const GatherArgs& a, cudaStream_t st);
 // Merge of the units the stream kernel split across warps.
 int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st);
 

@@ -70,8 +70,9 @@ struct Plan {
   sa::GatherArgs g;
   bool stream = false;
   bool fp8 = false;
+  bool fp8_tc = false;  // the tcgen05 kernel (128-key tiles)
   int grid = 0;
-  size_t off_pos = 0, off_meta = 0, off_part_o = 0, off_part_ml = 0, bytes = 0;
+  size_t off_pos = 0, off_meta = 0, off_part_o = 0, off_part_ml = 0, off_kdec = 0, bytes = 0;
 };
 
 int stream_grid() {
@@ -136,8 +137,10 @@ int plan_gather(Plan& pl, int dtype) {
   return SA_OK;
 }
 
-// FP8 hybrid-record decode: planned positions (as the stream path), one CTA
-// per (unit, 32-head block, key chunk), partials merged by the combine kernel.
+// FP8 hybrid-record decode: planned positions (as the stream path), then the
+// tcgen05 kernel (128-head blocks, 128-key tiles, three CTAs per output block)
+// or the warp-level MMA kernel (32-head blocks, 16-key tiles); key splits are
+// merged by the combine kernel.
 int plan_fp8(Plan& pl) {
   sa::GatherArgs& g = pl.g;
   pl.fp8 = true;
@@ -145,18 +148,35 @@ int plan_fp8(Plan& pl) {
   g.n_groups = g.Hkv;  // 1: every query head shares the latent head
   g.hpu = g.g;
   g.units = g.B * g.n_groups * g.Sq;
-  g.tiles_per_unit = (g.n_cand + 15) / 16;
-  g.n_cand_pad = g.tiles_per_unit * 16;
-  const int64_t blocks = g.units * (g.Hq / 32);
-  const int64_t slots = static_cast<int64_t>(device_shape().sms) * 2;  // 2 CTAs per SM
-  int64_t splits = slots / (blocks > 0 ? blocks : 1);
-  const int64_t min_splits = (g.tiles_per_unit + sa::fp8_chunk_tiles_max() - 1) /
-                             sa::fp8_chunk_tiles_max();
-  if (splits < min_splits) splits = min_splits;
-  if (splits < 1) splits = 1;
-  if (splits > g.tiles_per_unit) splits = g.tiles_per_unit > 0 ? g.tiles_per_unit : 1;
-  g.chunk = (g.tiles_per_unit + splits - 1) / splits;  // tiles per chunk
-  g.splits = (g.tiles_per_unit + g.chunk - 1) / g.chunk;
+  pl.fp8_tc = sa::fp8_tc_supported(g);
+  const int64_t sms = device_shape().sms > 0 ? device_shape().sms : 152;
+  if (pl.fp8_tc) {
+    // 128-key tiles; (unit, 128-head block, split) x 3 dim parts, one CTA per SM
+    g.tiles_per_unit = (g.n_cand + 127) / 128;
+    g.n_cand_pad = g.tiles_per_unit * 128;
+    const int64_t blocks = g.units * (g.Hq / 128) * 3;
+    int64_t splits = sms / (blocks > 0 ? blocks : 1);
+    const int64_t min_splits = (g.tiles_per_unit + sa::fp8_tc_max_tiles() - 1) / sa::fp8_tc_max_tiles();
+    if (splits < min_splits) splits = min_splits;
+    if (splits < 1) splits = 1;
+    if (splits > g.tiles_per_unit) splits = g.tiles_per_unit;
+    g.chunk = (g.tiles_per_unit + splits - 1) / splits;
+    g.splits = (g.tiles_per_unit + g.chunk - 1) / g.chunk;
+    if (g.units * (g.Hq / 128) * g.splits * 3 >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
+  } else {
+    g.tiles_per_unit = (g.n_cand + 15) / 16;
+    g.n_cand_pad = g.tiles_per_unit * 16;
+    const int64_t blocks = g.units * (g.Hq / 32);
+    const int64_t slots = sms * 2;  // 2 CTAs per SM
+    int64_t splits = slots / (blocks > 0 ? blocks : 1);
+    const int64_t min_splits = (g.tiles_per_unit + sa::fp8_chunk_tiles_max() - 1) /
+                               sa::fp8_chunk_tiles_max();
+    if (splits < min_splits) splits = min_splits;
+    if (splits < 1) splits = 1;
+    if (splits > g.tiles_per_unit) splits = g.tiles_per_unit > 0 ? g.tiles_per_unit : 1;
+    g.chunk = (g.tiles_per_unit + splits - 1) / splits;  // tiles per chunk
+    g.splits = (g.tiles_per_unit + g.chunk - 1) / g.chunk;
+  }
   if (g.splits < 1) g.splits = 1;
   const int64_t irows = g.B * g.I * g.Sq;
   size_t off = 0;
@@ -168,6 +188,10 @@ int plan_fp8(Plan& pl) {
     off += align_up(parts * g.Dv * sizeof(float));
     pl.off_part_ml = off;
     off += align_up(parts * 2 * sizeof(float));
+  }
+  if (pl.fp8_tc) {
+    pl.off_kdec = off;
+    off += align_up(static_cast<size_t>(g.units * g.n_cand_pad) * sa::fp8_tc_decoded_row_bytes());
   }
   pl.bytes = off;
   return SA_OK;
@@ -191,6 +215,7 @@ void carve(Plan& pl, void* ws) {
       g.part_o = reinterpret_cast<float*>(base + pl.off_part_o);
       g.part_ml = reinterpret_cast<float*>(base + pl.off_part_ml);
     }
+    if (pl.fp8_tc) g.fp8_kdec = base + pl.off_kdec;
     return;
   }
   g.part_o = reinterpret_cast<float*>(base + pl.off_part_o);
@@ -205,7 +230,8 @@ void carve(Plan& pl, void* ws) {
 int run_plan(Plan& pl, int dtype, cudaStream_t st) {
   sa::GatherArgs& g = pl.g;
   if (pl.fp8) {
-    if (sa::launch_fp8_decode(g, st) != 0) return SA_ERR_LAUNCH;
+    if ((pl.fp8_tc ? sa::launch_fp8_tc(g, st) : sa::launch_fp8_decode(g, st)) != 0)
+      return SA_ERR_LAUNCH;
     if (sa::launch_combine(g, SA_BF16, st) != 0) return SA_ERR_LAUNCH;
     return SA_OK;
   }

@@ -365,6 +365,71 @@ def test_fp8_options_kv_len_softcap_sink_and_query_positions(cuda_lib):
     assert_close(to64(y), ref, y.dtype, "fp8 options")
 
 
+# Blocks of 128 query heads run on the tcgen05 kernel (128-key tiles, three
+# CTAs per output block): every option, several head blocks, many key splits.
+@pytest.mark.parametrize("over", [dict(Hq=128), dict(Hq=128, record_stride=656),
+                                  dict(Hq=128, window=0, K=700, pad_prob=0.0),
+                                  dict(Hq=256, B=1, T=4000, K=900),
+                                  dict(Hq=128, B=1, T=30000, K=6000),
+                                  dict(Hq=128, B=5, T=700, K=60, window=16)])
+def test_fp8_tc05_head_blocks_match_oracle(cuda_lib, over):
+    c = _fp8_case(**over)
+    inp = synth.make_sparse_inputs(c, seed=94)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = _run_fp8(cuda_lib, c, inp, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.sparse_attention(inp["q"], inp["idx"], records=inp["kv_records"],
+                                  n_rope=c.n_rope, scale=c.eff_scale(), window=c.window)
+    assert_close(to64(y), ref, y.dtype, f"fp8 tc05 {over}")
+
+
+@pytest.mark.parametrize("over", [dict(B=16, T=3000, K=1000),   # 3 splits of 3 tiles
+                                  dict(B=52, T=900, K=400)])    # 1 split of 5 tiles
+def test_fp8_tc05_several_tiles_per_cta(cuda_lib, over):
+    c = _fp8_case(Hq=128, **over)
+    inp = synth.make_sparse_inputs(c, seed=98)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = _run_fp8(cuda_lib, c, inp, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = list(range(0, c.B * c.Hq, 5))
+    ref = oracle.sparse_attention(inp["q"], inp["idx"], records=inp["kv_records"],
+                                  n_rope=c.n_rope, scale=c.eff_scale(), window=c.window,
+                                  rows=rows)
+    assert_close(to64(y.reshape(-1, c.D)[rows]), ref, y.dtype, f"fp8 tc05 tiles {over}")
+
+
+def test_fp8_tc05_options_kv_len_softcap_sink_and_query_positions(cuda_lib):
+    c = _fp8_case(B=2, Hq=128, T=2500, K=400)
+    inp = synth.make_sparse_inputs(c, seed=95)
+    q2 = synth.normal((c.B, c.Hq, 2, c.D), "bf16", 96)
+    idx2 = inp["idx"].repeat(1, 1, 2, 1)
+    kv_len = torch.tensor([2500, 1300], dtype=torch.int64)
+    sink = torch.linspace(-2.0, 1.0, c.Hq, dtype=torch.float32)
+    inp2 = dict(inp, q=q2, idx=idx2)
+    for softcap in (0.0, 4.0):
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        y = _run_fp8(cuda_lib, c, inp2, kv_len=kv_len.to(DEV), softcap=softcap,
+                     sink=sink.to(DEV), err_word=err)
+        torch.cuda.synchronize()
+        # indices at or past kv_len[1] are flagged (and masked), nothing else
+        assert int(err.item()) == 4
+        ref = oracle.sparse_attention(q2, idx2, records=inp["kv_records"], n_rope=c.n_rope,
+                                      scale=c.eff_scale(), window=c.window, kv_len=kv_len,
+                                      softcap=softcap, sink=sink.double())
+        assert_close(to64(y), ref, y.dtype, f"fp8 tc05 options softcap={softcap}")
+
+
+def test_fp8_tc05_is_deterministic(cuda_lib):
+    c = _fp8_case(B=2, Hq=128, T=6000, K=1500)
+    inp = synth.make_sparse_inputs(c, seed=97)
+    y1 = _run_fp8(cuda_lib, c, inp)
+    y2 = _run_fp8(cuda_lib, c, inp)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
 def test_full_size_fp8_sampled_rows(cuda_lib):
     """B16 Hq128 MQA D576 (648-byte records) T65536, window 128 + top-k 2048,
     the benchmark's launch configuration, checked on sampled batches."""
