@@ -46,6 +46,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "kernels.h"
 #include "tc05.cuh"
@@ -88,6 +89,14 @@ constexpr int kBarQ = 0, kBarFullS = 1, kBarFullPv = kBarFullS + kStages,
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kSmem = kOffAbort + 4 + 1024;                 // + alignment slack
+// The split merge reuses the Q area once every score MMA has completed: the
+// CTA's O rows (fp32, padded rows), its (max, sum) per row, the merge weights.
+constexpr int kMaxClusterSplits = 8;
+constexpr int kOStride = kPartDims + 4;                     // floats per O row
+constexpr int kOffMO = kOffQ;
+constexpr int kOffMMl = kOffMO + kHeads * kOStride * 4;
+constexpr int kOffMW = kOffMMl + kHeads * 8;
+static_assert(kOffMW + kHeads * kMaxClusterSplits * 4 <= kOffRing, "merge area");
 static_assert(kSmem <= 232448, "shared memory");
 // tensor memory: score buffers 0 and 1, then this CTA's output dims
 constexpr uint32_t kColS = 0, kColO = 2 * kKeys, kTmemCols = 512;
@@ -102,6 +111,7 @@ struct Fp8TcParams {
   const float* sink;         // nullable [Hq]
   uint32_t* err_word;
   int B, Sq, Hq, hblocks, splits, chunk_tiles, tiles;
+  int cluster_merge;         // the splits of an output block form a cluster and merge on chip
   float scale_log2;          // scale * log2(e)
   float k1, c_log2;          // softcap: logit2 = c_log2 * tanh(s * k1)
 };
@@ -146,6 +156,42 @@ __device__ __forceinline__ void entry_of(int e, int nt, int part, int& j, int& c
   }
 }
 
+// Barrier `id` over the first `threads` threads that reach it (a warpgroup).
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---- thread-block cluster helpers ----
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; release / acquire of shared memory.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// This CTA's shared address -> the same offset in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
 // Two E4M3FN codes -> two floats, exactly (via the f16x2 conversion).
 __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
   const __half2_raw h =
@@ -166,26 +212,13 @@ namespace {
 
 // ---- kernel 1: gather + exact decode of the planned candidates' records ------------------
 
-// One warp per row [unit, candidate] of the decoded buffer (8 rows per CTA).
-__global__ void __launch_bounds__(256) fp8_gather_decode_kernel(const DecodeParams p) {
-  __shared__ __align__(16) uint2 stage[8][82];  // one 648-byte record per warp
-  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (row >= p.rows) return;
-  const int32_t pos = __ldg(p.pos + row);
-  uint4* out = reinterpret_cast<uint4*>(p.kdec + row * kD);  // 72 x 16 bytes
-  if (pos < 0) {
-    for (int i = lane; i < kRowBytes / 16; i += 32) out[i] = make_uint4(0u, 0u, 0u, 0u);
-    return;
-  }
-  const int64_t b = (row / p.n_cand_pad) / p.Sq;
-  const uint2* rec = reinterpret_cast<const uint2*>(
-      p.recs + (b * p.T + pos) * p.record_stride);  // 8-byte aligned
-  uint2* st = stage[warp];
-  for (int i = lane; i < 81; i += 32) st[i] = __ldg(rec + i);
-  __syncwarp();
-  // FP8 dims: lane l decodes codes [16q, 16q + 16) of block c = l / 4, q = l % 4,
-  // record bytes 65c + 1 + 16q ..; the scale is byte 65c.
+constexpr int kDecRecs = 4;  // records per warp, all in flight together
+
+// Row r of the decoded buffer from a staged 648-byte record: lane l decodes
+// codes [16q, 16q + 16) of FP8 block c = l / 4, q = l % 4 (record bytes
+// 65c + 1 + 16q ..; the scale is byte 65c), lanes 0-7 copy 16 bytes each of
+// the RoPE tail (from record byte 520).
+__device__ __forceinline__ void decode_row(const uint2* st, uint4* out, int lane) {
   const int c = lane >> 2, q = lane & 3;
   const unsigned char* sb = reinterpret_cast<const unsigned char*>(st);
   const uint32_t* sw = reinterpret_cast<const uint32_t*>(st);
@@ -209,10 +242,55 @@ __global__ void __launch_bounds__(256) fp8_gather_decode_kernel(const DecodePara
   }
   out[8 * c + 2 * q] = make_uint4(o[0], o[1], o[2], o[3]);
   out[8 * c + 2 * q + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-  // RoPE dims 512 .. 575: the 128 bytes from record byte 520, as they are
   if (lane < 8) {
     const uint2 lo = st[kRecRope / 8 + 2 * lane], hi = st[kRecRope / 8 + 2 * lane + 1];
     out[64 + lane] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+  }
+}
+
+// Each warp decodes kDecRecs consecutive rows [unit, candidate] of the buffer
+// (8 warps per CTA): the rows' positions, then all their record loads, then
+// the decodes.
+__global__ void __launch_bounds__(256) fp8_gather_decode_kernel(const DecodeParams p) {
+  __shared__ __align__(16) uint2 stage[8][kDecRecs][82];  // 648-byte records
+  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
+  pdl_wait();                // the planned positions
+  pdl_launch_dependents();   // the attention kernel may start its set-up
+  const int64_t row0 = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * kDecRecs;
+  if (row0 >= p.rows) return;
+  const int32_t mine = (lane < kDecRecs && row0 + lane < p.rows) ? __ldg(p.pos + row0 + lane) : -1;
+  int32_t pos[kDecRecs];
+  uint2 v[kDecRecs][3];
+#pragma unroll
+  for (int r = 0; r < kDecRecs; ++r) {
+    pos[r] = __shfl_sync(0xffffffffu, mine, r);
+    if (pos[r] >= 0) {
+      const int64_t b = ((row0 + r) / p.n_cand_pad) / p.Sq;
+      const uint2* rec = reinterpret_cast<const uint2*>(
+          p.recs + (b * p.T + pos[r]) * p.record_stride);  // 8-byte aligned
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        if (lane + 32 * k < 81) v[r][k] = __ldg(rec + lane + 32 * k);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kDecRecs; ++r)
+    if (pos[r] >= 0) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        if (lane + 32 * k < 81) stage[warp][r][lane + 32 * k] = v[r][k];
+    }
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < kDecRecs; ++r) {
+    const int64_t row = row0 + r;
+    if (row >= p.rows) break;
+    uint4* out = reinterpret_cast<uint4*>(p.kdec + row * kD);  // 72 x 16 bytes
+    if (pos[r] < 0) {
+      for (int i = lane; i < kRowBytes / 16; i += 32) out[i] = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      decode_row(stage[warp][r], out, lane);
+    }
   }
 }
 
@@ -222,19 +300,12 @@ namespace {
 
 // ---- kernel 2 roles: the TMA lane, the MMA issue lanes -------------------------------------
 
-// Q rows (b, hb * 128 + r, i) -> nine 128-byte-swizzled slabs; then the ring
-// entries in order, each a 128-key x 64-dim box of the decoded buffer.
-__device__ void fp8tc_producer(const CUtensorMap* tq, const CUtensorMap* tk, const Fp8TcParams& p,
-                               int unit, int hb, int t0, int nt, int part, uint8_t* sm,
+// The ring entries in order, each a 128-key x 64-dim box of the decoded buffer
+// (Q's nine slabs were requested in the prologue).
+__device__ void fp8tc_producer(const CUtensorMap* tk, const Fp8TcParams& p,
+                               int unit, int t0, int nt, int part, uint8_t* sm,
                                uint64_t* bars, volatile int* abort_flag) {
-  const int b = unit / p.Sq, i = unit % p.Sq;
-  tc05::prefetch_tmap(tq);
   tc05::prefetch_tmap(tk);
-  mbar_arrive_expect_tx(&bars[kBarQ], kChunks * kChunkBytes);
-#pragma unroll 1
-  for (int c = 0; c < kChunks; ++c)
-    tc05::tma_load3(sm + kOffQ + c * kChunkBytes, tq, 64 * c, i, b * p.Hq + hb * kHeads,
-                    &bars[kBarQ]);
   // per slot: armed at all, last fill read by the score lane, its parity;
   // and the parity of the next phase of full_s / full_pv
   uint32_t armed = 0, last_score = 0, last_par = 0, par_s = 0, par_pv = 0;
@@ -461,16 +532,21 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
   }
 
   // ---- epilogue: this CTA's 192 output dims of head row ----------------------------------
+  // Each thread stages its row in the Q area (free: every score MMA has
+  // completed) and, for y or the partials, copies it out with one bulk copy
+  // (row-per-thread global stores would be 48 scattered 16-byte writes each).
   const int h = hb * kHeads + row;
   const int b = unit / p.Sq, i = unit % p.Sq;
   const bool have = nt > 0 && ok && wait_or_abort_warp(&bars[kBarO], 0, abort_flag, p.err_word);
   if (have) tc05::fence_after_sync();
+  mbar_wait(&bars[kBarQ], 0);  // (no tile at all: Q's load must have landed before its area is reused)
+  uint8_t* sm = reinterpret_cast<uint8_t*>(bars) - kOffBar;
+  float* orow = reinterpret_cast<float*>(sm + kOffMO) + row * kOStride;
   if (p.splits == 1) {
     float L = l_run;
     if (p.sink && m_run != SA_NEG_INF) L += ex2(p.sink[h] * kLog2e - m_run);
     const float inv = (!have || m_run == SA_NEG_INF || L == 0.0f) ? 0.0f : 1.0f / L;
-    __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(p.y) +
-                        ((static_cast<int64_t>(b) * p.Hq + h) * p.Sq + i) * kD + part * kPartDims;
+    uint32_t* yrow = reinterpret_cast<uint32_t*>(orow);  // 192 bf16 = 384 bytes
 #pragma unroll 1
     for (int c = 0; c < kPartDims / 32; ++c) {
       uint32_t o[32];
@@ -488,40 +564,122 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
         for (int e = 0; e < 4; ++e)
           w[e] = pack2<__nv_bfloat16>(__uint_as_float(o[8 * q + 2 * e]) * inv,
                                       __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-        *reinterpret_cast<uint4*>(yp + c * 32 + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(yrow + c * 16 + 4 * q) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-  } else {
-    const int64_t pidx = (static_cast<int64_t>(unit) * p.splits + split) * p.Hq + h;
-    float* po = p.part_o + pidx * kD + part * kPartDims;
+    fence_proxy_async_smem();
+    tc05::bulk_s2g(static_cast<__nv_bfloat16*>(p.y) +
+                       ((static_cast<int64_t>(b) * p.Hq + h) * p.Sq + i) * kD + part * kPartDims,
+                   yrow, kPartDims * 2);
+    tc05::bulk_commit_group();
+    tc05::bulk_wait_group_read0();
+    return;
+  }
+  // splits > 1: the row's unnormalised O and (max, sum)
 #pragma unroll 1
-    for (int c = 0; c < kPartDims / 32; ++c) {
-      uint32_t o[32];
-      if (have) {
-        tc05::tmem_ld32(tl + kColO + c * 32, o);
-        tc05::tmem_ld_wait();
-      } else {
+  for (int c = 0; c < kPartDims / 32; ++c) {
+    uint32_t o[32];
+    if (have) {
+      tc05::tmem_ld32(tl + kColO + c * 32, o);
+      tc05::tmem_ld_wait();
+    } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      for (int e = 0; e < 32; ++e) o[e] = 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<uint4*>(orow + c * 32 + 4 * q) =
+          make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+  }
+  const float m_out = have ? m_run : SA_NEG_INF, l_out = have ? l_run : 0.0f;
+  if (p.cluster_merge) {  // merged on chip after the cluster barrier
+    float* ml = reinterpret_cast<float*>(sm + kOffMMl);
+    ml[2 * row] = m_out;
+    ml[2 * row + 1] = l_out;
+    return;
+  }
+  const int64_t pidx = (static_cast<int64_t>(unit) * p.splits + split) * p.Hq + h;
+  fence_proxy_async_smem();
+  tc05::bulk_s2g(p.part_o + pidx * kD + part * kPartDims, orow, kPartDims * 4);
+  tc05::bulk_commit_group();
+  if (part == 0) {  // the same (max, sum) in every part: the combine kernel's layout
+    p.part_ml[2 * pidx] = m_out;
+    p.part_ml[2 * pidx + 1] = l_out;
+  }
+  tc05::bulk_wait_group_read0();
+}
+
+// The splits of one (unit, head block, part) are the CTAs of a cluster (rank =
+// split).  Cluster CTA s merges head rows [128 s / C, 128 (s + 1) / C) of the
+// part's dims, reading every CTA's staged O rows and (max, sum) through
+// distributed shared memory:
+//   y = sum_c 2^(m_c - M) O_c / (sum_c 2^(m_c - M) l_c [+ 2^(sink - M)]).
+__device__ void fp8tc_cluster_merge(const Fp8TcParams& p, int unit, int hb, int part, uint8_t* sm) {
+  const int C = p.splits;
+  const uint32_t rank = cluster_rank();
+  const int r0 = static_cast<int>(rank) * kHeads / C, r1 = (static_cast<int>(rank) + 1) * kHeads / C;
+  const uint32_t o_base = smem_u32(sm + kOffMO), ml_base = smem_u32(sm + kOffMMl);
+  float* wts = reinterpret_cast<float*>(sm + kOffMW);  // [128][kMaxClusterSplits]
+  const int tid = static_cast<int>(threadIdx.x);
+  const int b = unit / p.Sq, i = unit % p.Sq;
+  if (tid < r1 - r0) {
+    const int r = r0 + tid;
+    float m[kMaxClusterSplits], l[kMaxClusterSplits];
+    float M = SA_NEG_INF;
+#pragma unroll
+    for (int c = 0; c < kMaxClusterSplits; ++c) {
+      m[c] = SA_NEG_INF;
+      l[c] = 0.0f;
+      if (c < C) {
+        const float2 v = ld_cluster_f2(map_rank(ml_base + 8u * r, c));
+        m[c] = v.x;
+        l[c] = v.y;
+        M = fmaxf(M, v.x);
       }
+    }
+    float L = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(po + c * 32 + 4 * q) =
-            make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    for (int c = 0; c < kMaxClusterSplits; ++c) {
+      m[c] = (M == SA_NEG_INF || m[c] == SA_NEG_INF) ? 0.0f : ex2(m[c] - M);  // weight
+      L += m[c] * l[c];
     }
-    if (part == 0) {
-      p.part_ml[2 * pidx] = have ? m_run : SA_NEG_INF;
-      p.part_ml[2 * pidx + 1] = have ? l_run : 0.0f;
+    if (p.sink && M != SA_NEG_INF) L += ex2(p.sink[hb * kHeads + r] * kLog2e - M);
+    const float inv = (M == SA_NEG_INF || L == 0.0f) ? 0.0f : 1.0f / L;
+#pragma unroll
+    for (int c = 0; c < kMaxClusterSplits; ++c) wts[r * kMaxClusterSplits + c] = m[c] * inv;
+  }
+  __syncthreads();
+  const int n = (r1 - r0) * (kPartDims / 4);
+  for (int it = tid; it < n; it += kThreads) {
+    const int r = r0 + it / (kPartDims / 4), k = it % (kPartDims / 4);
+    const uint32_t src = o_base + static_cast<uint32_t>((r * kOStride + 4 * k) * 4);
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int c = 0; c < kMaxClusterSplits; ++c) {
+      if (c >= C) break;
+      const float w = wts[r * kMaxClusterSplits + c];
+      if (w == 0.0f) continue;
+      const float4 v = ld_cluster_f4(map_rank(src, c));
+      acc.x = fmaf(v.x, w, acc.x);
+      acc.y = fmaf(v.y, w, acc.y);
+      acc.z = fmaf(v.z, w, acc.z);
+      acc.w = fmaf(v.w, w, acc.w);
     }
+    __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(p.y) +
+                        ((static_cast<int64_t>(b) * p.Hq + hb * kHeads + r) * p.Sq + i) * kD +
+                        part * kPartDims + 4 * k;
+    *reinterpret_cast<uint2*>(yp) =
+        make_uint2(pack2<__nv_bfloat16>(acc.x, acc.y), pack2<__nv_bfloat16>(acc.z, acc.w));
   }
 }
 
 }  // namespace
 
 
-// One CTA per (unit = (batch, query position), 128-head block, key split,
-// third of the output dims): blockIdx.x = ((unit * hblocks + hb) * splits +
-// split) * 3 + part, so the three CTAs reading the same keys run together.
+// One CTA per (unit = (batch, query position), 128-head block, third of the
+// output dims, key split): blockIdx.x = ((unit * hblocks + hb) * 3 + part) *
+// splits + split, the splits of one output block adjacent (a cluster when
+// they merge on chip).
 template <bool kCap>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_tc05_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -535,10 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* valid = reinterpret_cast<uint32_t*>(sm + kOffValid);
   const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
   int cta = static_cast<int>(blockIdx.x);
-  const int part = cta % kParts;
-  cta /= kParts;
   const int split = cta % p.splits;
   cta /= p.splits;
+  const int part = cta % kParts;
+  cta /= kParts;
   const int hb = cta % p.hblocks;
   const int unit = cta / p.hblocks;
   const int t0 = split * p.chunk_tiles;
@@ -566,7 +724,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarO], 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // Q is an input of the call: its load may start before the kernels this
+    // one depends on have finished
+    tc05::prefetch_tmap(&tq);
+    mbar_arrive_expect_tx(&bars[kBarQ], kChunks * kChunkBytes);
+    const int b = unit / p.Sq, i = unit % p.Sq;
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c)
+      tc05::tma_load3(sm + kOffQ + c * kChunkBytes, &tq, 64 * c, i, b * p.Hq + hb * kHeads,
+                      &bars[kBarQ]);
   }
+  pdl_wait();  // the planned positions and the decoded keys
   // validity bit masks of this split's tiles: word 4j + k, bit i = key 32k + i
   const int32_t* prow = p.pos + static_cast<int64_t>(unit) * p.n_cand_pad +
                         static_cast<int64_t>(t0) * kKeys;
@@ -580,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tslot;
 
   if (warp == kWarpLoad) {
-    if (lane == 0) fp8tc_producer(&tq, &tk, p, unit, hb, t0, nt, part, sm, bars, abort_flag);
+    if (lane == 0) fp8tc_producer(&tk, p, unit, t0, nt, part, sm, bars, abort_flag);
   } else if (warp == kWarpS) {
     if (lane == 0) fp8tc_score_lane(p, nt, sm, bars, tmem, abort_flag);
   } else if (warp == kWarpPv) {
@@ -590,7 +758,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc05::fence_before_sync();
-  __syncthreads();
+  __syncwarp();
+  if (p.splits > 1 && p.cluster_merge) {
+    cluster_sync();  // every CTA's O rows staged
+    fp8tc_cluster_merge(p, unit, hb, part, sm);
+    cluster_sync();  // no CTA leaves while another reads its shared memory
+  } else {
+    __syncthreads();
+  }
   if (warp == kWarpS) {
     tc05::fence_after_sync();
     tc05::tmem_dealloc(tmem, kTmemCols);
@@ -626,18 +801,78 @@ static bool bf16_map(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch that may begin while the previous kernel in the stream finishes
+// (programmatic dependent launch; the kernel waits for that kernel's results
+// itself, griddepcontrol.wait, before reading them), optionally as clusters
+// of `cluster` CTAs.
+template <typename K, typename... Args>
+static int launch_pdl(K kernel, unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                      unsigned cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  unsigned n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? 0 : -1;
+}
+
 template <bool kCap>
-static int launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const Fp8TcParams& p,
-                    int64_t grid, cudaStream_t st) {
-  if (cudaFuncSetAttribute(fp8_tc05_kernel<kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmem) != cudaSuccess)
-    return -1;
-  fp8_tc05_kernel<kCap><<<static_cast<unsigned>(grid), kThreads, kSmem, st>>>(tq, tk, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+static bool set_smem() {
+  return cudaFuncSetAttribute(fp8_tc05_kernel<kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmem) == cudaSuccess;
+}
+
+// How many clusters of `c` CTAs of the attention kernel can be resident at
+// once on this device (a cluster needs c SMs of one GPC)?  Asked once per size.
+static int max_active_clusters(int c) {
+  static std::once_flag once[kMaxClusterSplits + 1];
+  static int ok[kMaxClusterSplits + 1];
+  std::call_once(once[c], [c] {
+    ok[c] = 0;
+    if (!set_smem<false>() || !set_smem<true>()) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(c));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_tc05_kernel<false>, &cfg) == cudaSuccess) ok[c] = n;
+    cudaGetLastError();  // a refused query leaves no sticky error behind
+  });
+  return ok[c];
+}
+
+// The splits of each output block merge on chip when they can form clusters
+// and all `blocks` clusters are resident at once (a second wave of clusters
+// would cost more than the separate combine).
+bool fp8_tc_cluster_merge(int64_t splits, int64_t blocks) {
+  if (splits < 2 || splits > kMaxClusterSplits) return false;
+  return max_active_clusters(static_cast<int>(splits)) >= blocks;
 }
 
 int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   if (!fp8_tc_supported(g) || !g.fp8_kdec) return -1;
+  const bool cluster = fp8_tc_cluster_merge(g.splits, g.units * (g.Hq / kHeads) * kParts);
+  if (g.splits > 1 && !cluster && (!g.part_o || !g.part_ml)) return -1;
   if (g.n_cand_pad % kKeys != 0 || g.chunk > kMaxTiles || g.chunk < 1) return -1;
   const int64_t rows = g.units * g.n_cand_pad;
   if (rows <= 0) return 0;
@@ -651,8 +886,10 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   d.n_cand_pad = g.n_cand_pad;
   d.Sq = static_cast<int>(g.Sq);
   d.kdec = static_cast<__nv_bfloat16*>(g.fp8_kdec);
-  fp8_gather_decode_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(d);
-  if (cudaGetLastError() != cudaSuccess) return -1;
+  const int64_t per_cta = 8 * kDecRecs;
+  if (launch_pdl(fp8_gather_decode_kernel, static_cast<unsigned>((rows + per_cta - 1) / per_cta), 256,
+                 0, st, 1u, d) != 0)
+    return -1;
   // kernel 2: Q as [B * Hq][Sq][576] in boxes of 64 dims x 1 position x 128
   // heads; decoded keys as [units][n_cand_pad][576] in boxes of 64 dims x 128 keys
   CUtensorMap tq, tk;
@@ -683,13 +920,18 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   p.splits = static_cast<int>(g.splits);
   p.chunk_tiles = static_cast<int>(g.chunk);
   p.tiles = static_cast<int>(g.tiles_per_unit);
+  p.cluster_merge = cluster ? 1 : 0;
   p.scale_log2 = g.scale_log2;
   const float log2e = 1.4426950408889634f;
   p.k1 = g.softcap != 0.0f ? (g.scale_log2 / log2e) * g.inv_softcap : 0.0f;
   p.c_log2 = g.softcap * log2e;
-  const int64_t grid = g.units * p.hblocks * g.splits * kParts;
-  return g.softcap != 0.0f ? launch_t<true>(tq, tk, p, grid, st)
-                           : launch_t<false>(tq, tk, p, grid, st);
+  const unsigned grid = static_cast<unsigned>(g.units * p.hblocks * kParts * g.splits);
+  const unsigned cl = cluster ? static_cast<unsigned>(g.splits) : 1u;
+  if (g.softcap != 0.0f)
+    return set_smem<true>() ? launch_pdl(fp8_tc05_kernel<true>, grid, kThreads, kSmem, st, cl, tq, tk, p)
+                            : -1;
+  return set_smem<false>() ? launch_pdl(fp8_tc05_kernel<false>, grid, kThreads, kSmem, st, cl, tq, tk, p)
+                           : -1;
 }
 
 }  // namespace sa

@@ -139,6 +139,10 @@ int launch_fp8_decode(const GatherArgs& a, cudaStream_t st);
 bool fp8_tc_supported(const GatherArgs& a);
 int fp8_tc_max_tiles();
 size_t fp8_tc_decoded_row_bytes();
+// Key splits that the attention kernel merges itself (a cluster of `splits`
+// CTAs per output block, `blocks` such clusters resident at once); otherwise
+// partials for launch_combine.
+bool fp8_tc_cluster_merge(int64_t splits, int64_t blocks);
 int launch_fp8_tc(const GatherArgs& a, cudaStream_t st);
 // Merge of the units the stream kernel split across warps.
 int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st);

@@ -70,7 +70,8 @@ struct Plan {
   sa::GatherArgs g;
   bool stream = false;
   bool fp8 = false;
-  bool fp8_tc = false;  // the tcgen05 kernel (128-key tiles)
+  bool fp8_tc = false;       // the tcgen05 kernels (128-key tiles)
+  bool fp8_combine = false;  // FP8 key splits merged by launch_combine
   int grid = 0;
   size_t off_pos = 0, off_meta = 0, off_part_o = 0, off_part_ml = 0, off_kdec = 0, bytes = 0;
 };
@@ -182,7 +183,8 @@ int plan_fp8(Plan& pl) {
   size_t off = 0;
   pl.off_pos = off;
   off += align_up(static_cast<size_t>(irows * g.n_cand_pad) * sizeof(int32_t));
-  if (g.splits > 1) {
+  pl.fp8_combine = g.splits > 1 && !(pl.fp8_tc && sa::fp8_tc_cluster_merge(g.splits, g.units * (g.Hq / 128) * 3));
+  if (pl.fp8_combine) {
     const size_t parts = static_cast<size_t>(g.units * g.splits * g.hpu);
     pl.off_part_o = off;
     off += align_up(parts * g.Dv * sizeof(float));
@@ -211,7 +213,7 @@ void carve(Plan& pl, void* ws) {
   if (pl.bytes == 0) return;
   if (pl.fp8) {
     g.pos = reinterpret_cast<const int32_t*>(base + pl.off_pos);
-    if (g.splits > 1) {
+    if (pl.fp8_combine) {
       g.part_o = reinterpret_cast<float*>(base + pl.off_part_o);
       g.part_ml = reinterpret_cast<float*>(base + pl.off_part_ml);
     }
@@ -232,7 +234,7 @@ int run_plan(Plan& pl, int dtype, cudaStream_t st) {
   if (pl.fp8) {
     if ((pl.fp8_tc ? sa::launch_fp8_tc(g, st) : sa::launch_fp8_decode(g, st)) != 0)
       return SA_ERR_LAUNCH;
-    if (sa::launch_combine(g, SA_BF16, st) != 0) return SA_ERR_LAUNCH;
+    if (pl.fp8_combine && sa::launch_combine(g, SA_BF16, st) != 0) return SA_ERR_LAUNCH;
     return SA_OK;
   }
   if (pl.stream) {
