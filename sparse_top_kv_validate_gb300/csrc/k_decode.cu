@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(128) combine_kernel(GatherArgs a) {
   const int64_t h = u.h0 + hh;
   const int64_t D = a.Dv;
   const int splits = static_cast<int>(a.splits);
+  pdl_wait();  // the partials of the kernel before (launched as its dependent)
   const float* ml = a.part_ml + (unit * a.splits * a.hpu + hh) * 2;
   const int64_t mstride = a.hpu * 2;
   // Split weights w_s = 2^(m_s - M) (0 for an empty split) and 1 / L, by warp 0.
@@ -339,13 +340,29 @@ int launch_gather_simt(const GatherArgs& a, int dtype, cudaStream_t st) {
   return -2;
 }
 
+// Launched as a programmatic dependent of the partials' kernel: its CTAs may
+// be scheduled while that kernel drains, and wait for it (griddepcontrol.wait)
+// before reading the partials.
+template <typename T>
+static int launch_combine_t(const GatherArgs& a, unsigned grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<T>, a) == cudaSuccess ? 0 : -1;
+}
+
 int launch_combine(const GatherArgs& a, int dtype, cudaStream_t st) {
   if (a.splits <= 1 || a.units == 0) return 0;
   const unsigned grid = static_cast<unsigned>(a.units * a.hpu);
-  if (dtype == SA_F32) combine_kernel<float><<<grid, 128, 0, st>>>(a);
-  else if (dtype == SA_F16) combine_kernel<__half><<<grid, 128, 0, st>>>(a);
-  else combine_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  if (dtype == SA_F32) return launch_combine_t<float>(a, grid, st);
+  if (dtype == SA_F16) return launch_combine_t<__half>(a, grid, st);
+  return launch_combine_t<__nv_bfloat16>(a, grid, st);
 }
 
 }  // namespace sa

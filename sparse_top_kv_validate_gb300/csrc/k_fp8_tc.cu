@@ -212,36 +212,46 @@ namespace {
 
 // ---- kernel 1: gather + exact decode of the planned candidates' records ------------------
 
-constexpr int kDecRecs = 4;  // records per warp, all in flight together
+constexpr int kDecRecs = 8;  // records per warp, all in flight together
 
-// Row r of the decoded buffer from a staged 648-byte record: lane l decodes
-// codes [16q, 16q + 16) of FP8 block c = l / 4, q = l % 4 (record bytes
-// 65c + 1 + 16q ..; the scale is byte 65c), lanes 0-7 copy 16 bytes each of
-// the RoPE tail (from record byte 520).
-__device__ __forceinline__ void decode_row(const uint2* st, uint4* out, int lane) {
-  const int c = lane >> 2, q = lane & 3;
-  const unsigned char* sb = reinterpret_cast<const unsigned char*>(st);
-  const uint32_t* sw = reinterpret_cast<const uint32_t*>(st);
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Eight decoded bf16 values (16 bytes) of FP8 block c, codes [8g, 8g + 8):
+// record bytes 65c + 1 + 8g .. (read as aligned words of the staged record),
+// scaled by the block's E8M0 byte 65c.
+__device__ __forceinline__ uint4 decode8(const uint32_t* sw, const unsigned char* sb, int c, int g) {
   const float sc = e8m0_scale(sb[65 * c]);
   const uint64_t sc2 = f2_pack(sc, sc);
-  const int first = 65 * c + 1 + 16 * q;
+  const int first = 65 * c + 1 + 8 * g;
   const int w0 = first >> 2, sh = (first & 3) * 8;
-  uint32_t w[5];
+  const uint32_t a = sw[w0], b = sw[w0 + 1], d = sw[w0 + 2];
+  const uint32_t lo = sh ? __funnelshift_r(a, b, sh) : a;
+  const uint32_t hi = sh ? __funnelshift_r(b, d, sh) : b;
+  uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 5; ++i) w[i] = sw[w0 + i];
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t codes = sh ? __funnelshift_r(w[i], w[i + 1], sh) : w[i];
-    const float2 lo = e4m3x2_to_f2(codes & 0xffffu), hi = e4m3x2_to_f2(codes >> 16);
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t codes = i ? hi : lo;
+    const float2 x = e4m3x2_to_f2(codes & 0xffffu), y = e4m3x2_to_f2(codes >> 16);
     float a0, a1, b0, b1;
-    f2_unpack(f2_mul(f2_pack(lo.x, lo.y), sc2), a0, a1);
-    f2_unpack(f2_mul(f2_pack(hi.x, hi.y), sc2), b0, b1);
+    f2_unpack(f2_mul(f2_pack(x.x, x.y), sc2), a0, a1);
+    f2_unpack(f2_mul(f2_pack(y.x, y.y), sc2), b0, b1);
     o[2 * i] = pack2<__nv_bfloat16>(a0, a1);
     o[2 * i + 1] = pack2<__nv_bfloat16>(b0, b1);
   }
-  out[8 * c + 2 * q] = make_uint4(o[0], o[1], o[2], o[3]);
-  out[8 * c + 2 * q + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One decoded row (72 x 16 bytes) from a staged 648-byte record: lane l writes
+// 16-byte chunks l and l + 32 (FP8 blocks l / 8 and 4 + l / 8, codes
+// [8 (l % 8), 8 (l % 8) + 8)), so that every warp store is 512 contiguous
+// bytes; lanes 0-7 copy the RoPE tail (record bytes 520 ..) to chunks 64-71.
+__device__ __forceinline__ void decode_row(const uint2* st, uint4* out, int lane) {
+  const unsigned char* sb = reinterpret_cast<const unsigned char*>(st);
+  const uint32_t* sw = reinterpret_cast<const uint32_t*>(st);
+  out[lane] = decode8(sw, sb, lane >> 3, lane & 7);
+  out[32 + lane] = decode8(sw, sb, 4 + (lane >> 3), lane & 7);
   if (lane < 8) {
     const uint2 lo = st[kRecRope / 8 + 2 * lane], hi = st[kRecRope / 8 + 2 * lane + 1];
     out[64 + lane] = make_uint4(lo.x, lo.y, hi.x, hi.y);
@@ -249,47 +259,40 @@ __device__ __forceinline__ void decode_row(const uint2* st, uint4* out, int lane
 }
 
 // Each warp decodes kDecRecs consecutive rows [unit, candidate] of the buffer
-// (8 warps per CTA): the rows' positions, then all their record loads, then
-// the decodes.
+// (8 warps per CTA): the rows' positions, then all their records copied
+// (8 bytes per lane per copy) straight into shared memory, then the decodes.
 __global__ void __launch_bounds__(256) fp8_gather_decode_kernel(const DecodeParams p) {
-  __shared__ __align__(16) uint2 stage[8][kDecRecs][82];  // 648-byte records
+  extern __shared__ __align__(16) uint2 stage[];  // [8 warps][kDecRecs][82] 648-byte records
   const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
   pdl_wait();                // the planned positions
   pdl_launch_dependents();   // the attention kernel may start its set-up
   const int64_t row0 = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * kDecRecs;
   if (row0 >= p.rows) return;
+  uint2* st = stage + warp * kDecRecs * 82;
   const int32_t mine = (lane < kDecRecs && row0 + lane < p.rows) ? __ldg(p.pos + row0 + lane) : -1;
-  int32_t pos[kDecRecs];
-  uint2 v[kDecRecs][3];
 #pragma unroll
   for (int r = 0; r < kDecRecs; ++r) {
-    pos[r] = __shfl_sync(0xffffffffu, mine, r);
-    if (pos[r] >= 0) {
+    const int32_t pr = __shfl_sync(0xffffffffu, mine, r);
+    if (pr >= 0) {
       const int64_t b = ((row0 + r) / p.n_cand_pad) / p.Sq;
       const uint2* rec = reinterpret_cast<const uint2*>(
-          p.recs + (b * p.T + pos[r]) * p.record_stride);  // 8-byte aligned
+          p.recs + (b * p.T + pr) * p.record_stride);  // 8-byte aligned
 #pragma unroll
       for (int k = 0; k < 3; ++k)
-        if (lane + 32 * k < 81) v[r][k] = __ldg(rec + lane + 32 * k);
+        if (lane + 32 * k < 81) cp_async8(st + r * 82 + lane + 32 * k, rec + lane + 32 * k);
     }
   }
-#pragma unroll
-  for (int r = 0; r < kDecRecs; ++r)
-    if (pos[r] >= 0) {
-#pragma unroll
-      for (int k = 0; k < 3; ++k)
-        if (lane + 32 * k < 81) stage[warp][r][lane + 32 * k] = v[r][k];
-    }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
   __syncwarp();
-#pragma unroll
+#pragma unroll 1
   for (int r = 0; r < kDecRecs; ++r) {
     const int64_t row = row0 + r;
     if (row >= p.rows) break;
     uint4* out = reinterpret_cast<uint4*>(p.kdec + row * kD);  // 72 x 16 bytes
-    if (pos[r] < 0) {
+    if (__shfl_sync(0xffffffffu, mine, r) < 0) {
       for (int i = lane; i < kRowBytes / 16; i += 32) out[i] = make_uint4(0u, 0u, 0u, 0u);
     } else {
-      decode_row(stage[warp][r], out, lane);
+      decode_row(st + r * 82, out, lane);
     }
   }
 }
@@ -532,6 +535,7 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
   }
 
   // ---- epilogue: this CTA's 192 output dims of head row ----------------------------------
+  pdl_launch_dependents();  // the combine kernel may start launching
   // Each thread stages its row in the Q area (free: every score MMA has
   // completed) and, for y or the partials, copies it out with one bulk copy
   // (row-per-thread global stores would be 48 scattered 16-byte writes each).
@@ -887,8 +891,11 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   d.Sq = static_cast<int>(g.Sq);
   d.kdec = static_cast<__nv_bfloat16*>(g.fp8_kdec);
   const int64_t per_cta = 8 * kDecRecs;
-  if (launch_pdl(fp8_gather_decode_kernel, static_cast<unsigned>((rows + per_cta - 1) / per_cta), 256,
-                 0, st, 1u, d) != 0)
+  const size_t dsmem = 8 * kDecRecs * 82 * sizeof(uint2);
+  if (cudaFuncSetAttribute(fp8_gather_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(dsmem)) != cudaSuccess ||
+      launch_pdl(fp8_gather_decode_kernel, static_cast<unsigned>((rows + per_cta - 1) / per_cta), 256,
+                 dsmem, st, 1u, d) != 0)
     return -1;
   // kernel 2: Q as [B * Hq][Sq][576] in boxes of 64 dims x 1 position x 128
   // heads; decoded keys as [units][n_cand_pad][576] in boxes of 64 dims x 128 keys
