@@ -340,21 +340,98 @@ int launch_gather_simt(const GatherArgs& a, int dtype, cudaStream_t st) {
   return -2;
 }
 
+// The same merge for at most kFlatSplits splits, D % 4 == 0 and y aligned to
+// four elements, one thread per four output dims of one head: every split's
+// (max, sum) and O values are requested together, so the merge costs one
+// round trip to L2.
+constexpr int kFlatSplits = 8;
+
+template <typename T>
+__device__ __forceinline__ void store4(T* p, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<__half>(__half* p, float a, float b, float c, float d) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack2<__half>(a, b), pack2<__half>(c, d));
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float a, float b, float c,
+                                                      float d) {
+  *reinterpret_cast<uint2*>(p) =
+      make_uint2(pack2<__nv_bfloat16>(a, b), pack2<__nv_bfloat16>(c, d));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) combine_flat_kernel(GatherArgs a) {
+  pdl_wait();  // the partials of the kernel before (launched as its dependent)
+  const int64_t q4 = a.Dv / 4;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (item >= a.units * a.hpu * q4) return;
+  const int64_t uh = item / q4, d = 4 * (item - uh * q4);
+  const int64_t unit = uh / a.hpu, hh = uh - unit * a.hpu;
+  const UnitInfo u = unit_info(a, unit);
+  const int64_t h = u.h0 + hh;
+  const int splits = static_cast<int>(a.splits);
+  const int64_t row0 = unit * a.splits * a.hpu + hh;  // (unit, split 0, head)
+  float m[kFlatSplits], l[kFlatSplits];
+  float4 o[kFlatSplits];
+#pragma unroll
+  for (int s = 0; s < kFlatSplits; ++s) {
+    if (s < splits) {
+      const int64_t r = row0 + s * a.hpu;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + r);
+      m[s] = ml.x;
+      l[s] = ml.y;
+      o[s] = __ldcg(reinterpret_cast<const float4*>(a.part_o + r * a.Dv + d));
+    } else {
+      m[s] = SA_NEG_INF;
+      l[s] = 0.f;
+      o[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  float M = SA_NEG_INF;
+#pragma unroll
+  for (int s = 0; s < kFlatSplits; ++s) M = fmaxf(M, m[s]);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int s = 0; s < kFlatSplits; ++s) {
+    const float w = (M == SA_NEG_INF || m[s] == SA_NEG_INF) ? 0.f : ex2(m[s] - M);
+    L += l[s] * w;
+    acc.x = fmaf(o[s].x, w, acc.x);
+    acc.y = fmaf(o[s].y, w, acc.y);
+    acc.z = fmaf(o[s].z, w, acc.z);
+    acc.w = fmaf(o[s].w, w, acc.w);
+  }
+  if (a.sink && M != SA_NEG_INF) L += ex2(a.sink[h] * kLog2e - M);
+  const float inv = (M == SA_NEG_INF || L == 0.f) ? 0.f : 1.0f / L;
+  T* yp = static_cast<T*>(a.y) + ((u.b * a.Hq + h) * a.Sq + u.i) * a.Dv + d;
+  store4<T>(yp, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
 // Launched as a programmatic dependent of the partials' kernel: its CTAs may
 // be scheduled while that kernel drains, and wait for it (griddepcontrol.wait)
 // before reading the partials.
 template <typename T>
 static int launch_combine_t(const GatherArgs& a, unsigned grid, cudaStream_t st) {
+  const bool flat = a.splits <= kFlatSplits && a.Dv % 4 == 0 &&
+                    reinterpret_cast<uintptr_t>(a.y) % (4 * sizeof(T)) == 0;  // vector stores
+  const int64_t items = a.units * a.hpu * (a.Dv / 4);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(flat ? static_cast<unsigned>((items + 255) / 256) : grid);
+  cfg.blockDim = dim3(flat ? 256 : 128);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<T>, a) == cudaSuccess ? 0 : -1;
+  return cudaLaunchKernelEx(&cfg, flat ? combine_flat_kernel<T> : combine_kernel<T>, a) ==
+                 cudaSuccess
+             ? 0
+             : -1;
 }
 
 int launch_combine(const GatherArgs& a, int dtype, cudaStream_t st) {
