@@ -412,7 +412,9 @@ class CsaFp8Decode:
         self.decode_bytes = (self.keys * c.record_stride + self.idx.numel() * 4
                              + 2 * self.q.numel() * 2)
         self.flops = 4.0 * c.Hq * c.D * self.keys
-        self.launches_per_step = 3  # plan, fp8 decode, combine
+        # plan, gather-decode, tcgen05 attention, combine (when the splits are not
+        # merged on chip; 128-head blocks) -- else plan, warp-MMA kernel, combine
+        self.launches_per_step = 4 if c.Hq % 128 == 0 else 3
         self.h_q = self.q.cpu().pin_memory()
         self.h_idx = self.idx.cpu().pin_memory()
         self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
@@ -443,7 +445,8 @@ class CsaFp8Decode:
                 "record_bytes": c.record_stride, "cache_tokens": c.T, "top_k": c.K,
                 "window": c.window, "keys_attended": self.keys,
                 "step": "sparse_attn_decode on FP8 records: plan kernel (validation, window "
-                        "union positions) + FP8 decode/attention kernel + combine"}
+                        "union positions) + gather-decode kernel (exact bf16 rows) + tcgen05 "
+                        "attention kernel + split combine"}
 
     def oracle_rows(self, rows):
         import oracle
@@ -466,7 +469,7 @@ class CsaFp8Decode:
         gbs = self.decode_bytes / (ms * 1e-3) / 1e9
         tf = self.flops / (ms * 1e-3) / 1e12
         return {"bound": "tensor", "kernel": "sparse_attn_decode call on FP8 records "
-                "(plan + fp8_decode + combine)", "achieved": round(tf, 2),
+                "(plan + fp8_gather_decode + fp8_tc05 + combine)", "achieved": round(tf, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(tf / peaks["bf16_tflops"], 4),
                 "peak_source": peaks["source"] + " (cuBLAS bf16, burst)",
