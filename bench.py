@@ -484,6 +484,9 @@ class CsaFp8Decode:
 TRAFFIC: dict = {
     # plan + gather_stream + combine kernels of one call, ncu dram read + write
     "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 279922176,
+    # plan + gather-decode + tcgen05 attention + combine of one call, ncu dram read + write
+    # (cold: the decoded rows and split partials, L2-resident live, count again)
+    "csa_fp8_b16_h128_d576_t65536_k2048_w128": 83579616,
     # prefill_tc05_kernel, one launch (Q, K, V read; Y and present K/V written)
     "prefill_bf16_b4_s4096_h32_kv8_d128_causal_softcap50": 441644032,
 }
