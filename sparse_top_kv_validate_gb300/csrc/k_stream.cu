@@ -16,7 +16,11 @@
 //  * Each warp runs its own 3-deep ring: a tile's 16 K rows and 16 V rows are
 //    fetched by one bulk async copy per lane (a row each), completion counted
 //    on the slot's mbarrier; rows are padded by 16 bytes so ldmatrix is
-//    conflict-free; masked keys are not fetched.  The cache positions of a
+//    conflict-free; masked keys are not fetched.  Paged tiles (16 tokens of
+//    one page, contiguous in the pool) instead arrive as D/64 TMA boxes of K
+//    and of V in the 128-byte-swizzled layout (kTma): 4 copies per tile in
+//    place of 32, which the per-row copies were bound by; rows of the page
+//    past the context are zeroed in shared memory after the load.  The cache positions of a
 //    tile (planned per index row by k_plan.cu, or read from the page table)
 //    are prefetched one iteration ahead.  No CTA-wide barrier in the loop.
 //  * Per tile: S^T = K . Q^T and O^T += V^T . P^T on the m16n8k16 tensor-core
@@ -25,34 +29,53 @@
 //  * A unit inside one warp's range is written directly; a unit split across
 //    warps leaves one partial per warp, merged by stream_combine_kernel in
 //    warp order (deterministic).
+#include <cstring>
+
 #include "gather_common.cuh"
+#include "tc05.cuh"
 
 namespace sa {
 
-template <int D>
+// kTma: the slot holds K then V as D/64 slabs of 16 rows x 128 bytes in the
+// 128-byte swizzle (TMA boxes), every slot 1024-byte aligned; else rows padded
+// to kRowStride.
+template <int D, bool kTma = false>
 struct SGeo {
   static constexpr int kRowBytes = D * 2;
   static constexpr int kRowStride = kRowBytes + 16;        // padding: conflict-free ldmatrix
-  static constexpr int kSlotBytes = 2 * 16 * kRowStride;   // 16 K rows then 16 V rows
+  static constexpr int kSlabs = D / 64;                    // kTma: 64-dim swizzled slabs
+  static constexpr int kSlabBytes = 16 * 128;
+  static constexpr int kHalfBytes = kTma ? kSlabs * kSlabBytes : 16 * kRowStride;
+  static constexpr int kSlotBytes = 2 * kHalfBytes;        // 16 K rows then 16 V rows
   static constexpr int kWarps = (D <= 128) ? 8 : 4;        // warps per CTA
   static constexpr int kStages = (D == 64) ? 4 : 3;        // ring slots per warp
   static constexpr int kRingBytes = kStages * kSlotBytes;
   // per warp: ring | slot masks | full barriers
   static constexpr int kMaskOff = kRingBytes;
   static constexpr int kBarOff = (kMaskOff + kStages * 4 + 7) / 8 * 8;
-  static constexpr int kWarpBytes = (kBarOff + kStages * 8 + 15) / 16 * 16;
+  static constexpr int kAlign = kTma ? 1024 : 16;
+  static constexpr int kWarpBytes = (kBarOff + kStages * 8 + kAlign - 1) / kAlign * kAlign;
   static constexpr int kThreads = kWarps * 32;
 };
 
-size_t stream_smem_bytes(int D, int source, int64_t B) {
-  size_t s = 0;
-  switch (D) {
-    case 64: s = static_cast<size_t>(SGeo<64>::kWarps) * SGeo<64>::kWarpBytes; break;
-    case 128: s = static_cast<size_t>(SGeo<128>::kWarps) * SGeo<128>::kWarpBytes; break;
-    default: s = static_cast<size_t>(SGeo<256>::kWarps) * SGeo<256>::kWarpBytes; break;
-  }
+template <int D, bool kTma>
+static size_t smem_bytes_t(int source, int64_t B) {
+  size_t s = static_cast<size_t>(SGeo<D, kTma>::kWarps) * SGeo<D, kTma>::kWarpBytes;
   if (source == kPaged) s += static_cast<size_t>(B + 1) * 4;
-  return s;
+  return s + (kTma ? 1024 : 0);  // + alignment of the dynamic base
+}
+
+size_t stream_smem_bytes(int D, int source, int64_t B) {
+  switch (D) {
+    case 64: return smem_bytes_t<64, false>(source, B);
+    case 128: return smem_bytes_t<128, false>(source, B);
+    default: return smem_bytes_t<256, false>(source, B);
+  }
+}
+
+// Byte offset of 16-byte chunk c (of D / 8) of row r (< 16) in a kTma half.
+__device__ __forceinline__ uint32_t swz_off(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 int stream_warps(int D) { return D <= 128 ? 8 : 4; }
@@ -161,12 +184,18 @@ __device__ __forceinline__ int64_t key_row(const GatherArgs& a, const KeyRef& k)
   return static_cast<int64_t>(k.raw) * a.Hkv * a.page_tokens + k.base;
 }
 
-template <typename T, int D, int NT>
-__global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(GatherArgs a) {
-  using G = SGeo<D>;
+template <typename T, int D, int NT, bool kTma>
+__global__ void __launch_bounds__(SGeo<D, kTma>::kThreads, 1)
+    gather_stream_kernel(const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv, GatherArgs a) {
+  using G = SGeo<D, kTma>;
   constexpr int KS = D / 16;
   constexpr int NW = G::kWarps, S = G::kStages;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem =
+      kTma ? reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023))
+           : smem_raw;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
 
@@ -177,14 +206,16 @@ __global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(Gat
     for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
   }
   // V rows of every slot start at zero: a masked key's row is never fetched,
-  // and its probability 0 must multiply finite values.
-  constexpr int kVz = 16 * G::kRowStride / 16;  // int4 per slot's V rows
-  for (int e = threadIdx.x; e < NW * S * kVz; e += blockDim.x) {
-    const int w = e / (S * kVz), r = e % (S * kVz);
-    uint4* vz = reinterpret_cast<uint4*>(smem + w * G::kWarpBytes + (r / kVz) * G::kSlotBytes +
-                                         16 * G::kRowStride);
-    vz[r % kVz] = make_uint4(0, 0, 0, 0);
-  }
+  // and its probability 0 must multiply finite values.  (kTma slots get their
+  // masked V rows zeroed after each load instead.)
+  constexpr int kVz = G::kHalfBytes / 16;  // int4 per slot's V rows
+  if (!kTma)
+    for (int e = threadIdx.x; e < NW * S * kVz; e += blockDim.x) {
+      const int w = e / (S * kVz), r = e % (S * kVz);
+      uint4* vz = reinterpret_cast<uint4*>(smem + w * G::kWarpBytes + (r / kVz) * G::kSlotBytes +
+                                           G::kHalfBytes);
+      vz[r % kVz] = make_uint4(0, 0, 0, 0);
+    }
   fence_proxy_async_smem();
   fence_mbar_init();
   // Everything above is independent of the previous kernel in the stream
@@ -269,6 +300,26 @@ __global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(Gat
     const int64_t row = key_row(a, kr);
     const uint32_t m = __ballot_sync(0xffffffffu, row >= 0) & 0xffffu;
     fence_proxy_async_smem();  // this warp's reads of the slot precede the refill
+    if (kTma) {
+      // the tile's 16 rows are consecutive in the pool (one page): row(l) = row(0) + l
+      const int first = m ? __ffs(m) - 1 : 0;
+      const long long rf = __shfl_sync(0xffffffffu, static_cast<long long>(row), first);
+      if (lane == 0) {
+        smask[slot] = m;
+        mbar_arrive_expect_tx(&full[slot], m ? 2u * 16u * G::kRowBytes : 0u);
+        if (m) {
+          const int y = static_cast<int>(rf - first);
+          unsigned char* kd = wbase + slot * G::kSlotBytes;
+#pragma unroll
+          for (int h = 0; h < G::kSlabs; ++h) {
+            tc05::tma_load2(kd + h * G::kSlabBytes, &tk, 64 * h, y, &full[slot]);
+            tc05::tma_load2(kd + G::kHalfBytes + h * G::kSlabBytes, &tv, 64 * h, y, &full[slot]);
+          }
+        }
+      }
+      __syncwarp();
+      return;
+    }
     if (lane == 0) {
       smask[slot] = m;
       mbar_arrive_expect_tx(&full[slot], __popc(m) * 2u * G::kRowBytes);
@@ -394,7 +445,18 @@ __global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(Gat
     if (mask == 0u) continue;
     const bool v_lo = (mask >> gid) & 1u, v_hi = (mask >> (gid + 8)) & 1u;
     const uint32_t kt = ring_s + slot * G::kSlotBytes;
-    const uint32_t vt = kt + 16 * G::kRowStride;
+    const uint32_t vt = kt + G::kHalfBytes;
+    if (kTma && mask != 0xffffu) {
+      // rows of the page past the context: V must hold finite values (zeros)
+      unsigned char* vrow = wbase + slot * G::kSlotBytes + G::kHalfBytes;
+      for (int e = lane; e < 16 * G::kSlabs * 8; e += 32) {
+        const int r = e / (G::kSlabs * 8), rest = e % (G::kSlabs * 8);
+        if (!((mask >> r) & 1u))
+          *reinterpret_cast<uint4*>(vrow + (rest >> 3) * G::kSlabBytes + r * 128 + (rest & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
     // S^T = K . Q^T
     float s[NT][4];
 #pragma unroll
@@ -406,7 +468,8 @@ __global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(Gat
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(rbase + kk * 32, a0, a1, a2, a3);
+        ldsm_x4(kTma ? kt + swz_off(lane & 15, 2 * kk + (lane >> 4)) : rbase + kk * 32, a0, a1, a2,
+                a3);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           mma16816<T>(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
@@ -450,12 +513,13 @@ __global__ void __launch_bounds__(SGeo<D>::kThreads, 1) gather_stream_kernel(Gat
     }
     // O^T += V^T . P^T
     {
-      const uint32_t rbase = vt + ((lane & 7) + ((lane >> 4) << 3)) * G::kRowStride +
-                             ((lane >> 3) & 1) * 16;
+      const int vr = (lane & 7) + ((lane >> 4) << 3);
+      const uint32_t rbase = vt + vr * G::kRowStride + ((lane >> 3) & 1) * 16;
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(rbase + mt * 32, a0, a1, a2, a3);
+        ldsm_x4_t(kTma ? vt + swz_off(vr, 2 * mt + ((lane >> 3) & 1)) : rbase + mt * 32, a0, a1,
+                  a2, a3);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
           mma16816<T>(o[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
@@ -638,9 +702,9 @@ __global__ void __launch_bounds__(128) stream_combine_kernel(GatherArgs a) {
 // Launch with programmatic stream serialisation: the kernel may begin while
 // the previous kernel in the stream finishes, and waits for its results
 // itself (griddepcontrol.wait) before reading them.
-template <typename K>
+template <typename K, typename... Args>
 static int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                      const GatherArgs& a) {
+                      Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -651,34 +715,73 @@ static int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a) == cudaSuccess ? 0 : -1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? 0 : -1;
+}
+
+// Paged pools [num_pages, Hkv, page_tokens, D] as 2-D tensors of 16-bit rows,
+// boxes of 64 dims x 16 rows in the 128-byte swizzle.  False when the pools
+// cannot be described (then the per-row copies are used).
+static bool paged_maps(const GatherArgs& a, int dtype, CUtensorMap* tk, CUtensorMap* tv) {
+  if (a.source != kPaged || a.page_tokens % 16 != 0 || (a.D != 64 && a.D != 128 && a.D != 256))
+    return false;
+  const int64_t rows = a.num_pages * a.Hkv * a.page_tokens;
+  if (rows < 16 || rows >= (int64_t(1) << 31)) return false;
+  if ((reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v)) & 15) return false;
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.D), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.D * 2)};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t es[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == SA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const void* base[2] = {a.k, a.v};
+  CUtensorMap* out[2] = {tk, tv};
+  for (int i = 0; i < 2; ++i)
+    if (enc(out[i], dt, 2, const_cast<void*>(base[i]), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  return true;
 }
 
 template <typename T, int D, int NT>
-static int launch_stream_t(const GatherArgs& a, int grid, size_t smem, cudaStream_t st) {
-  if (cudaFuncSetAttribute(gather_stream_kernel<T, D, NT>,
+static int launch_stream_t(const GatherArgs& a, int dtype, int grid, cudaStream_t st) {
+  CUtensorMap tk, tv;
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  if (paged_maps(a, dtype, &tk, &tv)) {
+    const size_t smem = smem_bytes_t<D, true>(a.source, a.B);
+    if (cudaFuncSetAttribute(gather_stream_kernel<T, D, NT, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return -1;
+    return launch_pdl(gather_stream_kernel<T, D, NT, true>, dim3(grid),
+                      dim3(SGeo<D, true>::kThreads), smem, st, tk, tv, a);
+  }
+  const size_t smem = smem_bytes_t<D, false>(a.source, a.B);
+  if (cudaFuncSetAttribute(gather_stream_kernel<T, D, NT, false>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return -1;
-  return launch_pdl(gather_stream_kernel<T, D, NT>, dim3(grid), dim3(SGeo<D>::kThreads), smem,
-                    st, a);
+  return launch_pdl(gather_stream_kernel<T, D, NT, false>, dim3(grid),
+                    dim3(SGeo<D, false>::kThreads), smem, st, tk, tv, a);
 }
 
 int launch_gather_stream(const GatherArgs& a, int dtype, int grid, cudaStream_t st) {
-  const size_t smem = stream_smem_bytes(static_cast<int>(a.D), a.source, a.B);
   const bool two = a.hpu > 8;
   if (dtype == SA_BF16) {
-    if (a.D == 64) return two ? launch_stream_t<__nv_bfloat16, 64, 2>(a, grid, smem, st)
-                              : launch_stream_t<__nv_bfloat16, 64, 1>(a, grid, smem, st);
-    if (a.D == 128) return two ? launch_stream_t<__nv_bfloat16, 128, 2>(a, grid, smem, st)
-                               : launch_stream_t<__nv_bfloat16, 128, 1>(a, grid, smem, st);
-    return launch_stream_t<__nv_bfloat16, 256, 1>(a, grid, smem, st);
+    if (a.D == 64) return two ? launch_stream_t<__nv_bfloat16, 64, 2>(a, dtype, grid, st)
+                              : launch_stream_t<__nv_bfloat16, 64, 1>(a, dtype, grid, st);
+    if (a.D == 128) return two ? launch_stream_t<__nv_bfloat16, 128, 2>(a, dtype, grid, st)
+                               : launch_stream_t<__nv_bfloat16, 128, 1>(a, dtype, grid, st);
+    return launch_stream_t<__nv_bfloat16, 256, 1>(a, dtype, grid, st);
   }
-  if (a.D == 64) return two ? launch_stream_t<__half, 64, 2>(a, grid, smem, st)
-                            : launch_stream_t<__half, 64, 1>(a, grid, smem, st);
-  if (a.D == 128) return two ? launch_stream_t<__half, 128, 2>(a, grid, smem, st)
-                             : launch_stream_t<__half, 128, 1>(a, grid, smem, st);
-  return launch_stream_t<__half, 256, 1>(a, grid, smem, st);
+  if (a.D == 64) return two ? launch_stream_t<__half, 64, 2>(a, dtype, grid, st)
+                            : launch_stream_t<__half, 64, 1>(a, dtype, grid, st);
+  if (a.D == 128) return two ? launch_stream_t<__half, 128, 2>(a, dtype, grid, st)
+                             : launch_stream_t<__half, 128, 1>(a, dtype, grid, st);
+  return launch_stream_t<__half, 256, 1>(a, dtype, grid, st);
 }
 
 int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st) {

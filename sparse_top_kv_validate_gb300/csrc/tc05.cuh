@@ -194,6 +194,17 @@ __device__ __forceinline__ void tma_load3(void* dst, const CUtensorMap* m, int x
       : "memory");
 }
 
+// 2-D tiled load of the box at (x, y) into `dst`, completing on `bar`.
+// x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load2(void* dst, const CUtensorMap* m, int x, int y,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 3-D tiled store of the box at (x, y, z) from `src` (bulk-group completion);
 // rows or columns outside the tensor are not written.
 __device__ __forceinline__ void tma_store3(const CUtensorMap* m, int x, int y, int z,
