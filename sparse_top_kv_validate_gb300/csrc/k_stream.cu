@@ -16,11 +16,12 @@
 //  * Each warp runs its own 3-deep ring: a tile's 16 K rows and 16 V rows are
 //    fetched by one bulk async copy per lane (a row each), completion counted
 //    on the slot's mbarrier; rows are padded by 16 bytes so ldmatrix is
-//    conflict-free; masked keys are not fetched.  Paged tiles (16 tokens of
-//    one page, contiguous in the pool) instead arrive as D/64 TMA boxes of K
-//    and of V in the 128-byte-swizzled layout (kTma): 4 copies per tile in
-//    place of 32, which the per-row copies were bound by; rows of the page
-//    past the context are zeroed in shared memory after the load.  The cache positions of a
+//    conflict-free; masked keys are not fetched.  With tensor maps (kTma) the
+//    slots hold the 128-byte-swizzled layout instead: paged and dense tiles
+//    (16 consecutive rows) arrive as D/64 TMA boxes of K and of V, selected
+//    rows as tile::gather4 loads of four rows each, so a tile takes 4 or 16
+//    copies in place of 32 (the per-row copies bounded the paged data path);
+//    masked rows of a loaded tile get their V zeroed in shared memory.  The cache positions of a
 //    tile (planned per index row by k_plan.cu, or read from the page table)
 //    are prefetched one iteration ahead.  No CTA-wide barrier in the loop.
 //  * Per tile: S^T = K . Q^T and O^T += V^T . P^T on the m16n8k16 tensor-core
@@ -301,20 +302,34 @@ __global__ void __launch_bounds__(SGeo<D, kTma>::kThreads, 1)
     const uint32_t m = __ballot_sync(0xffffffffu, row >= 0) & 0xffffu;
     fence_proxy_async_smem();  // this warp's reads of the slot precede the refill
     if (kTma) {
-      // the tile's 16 rows are consecutive in the pool (one page): row(l) = row(0) + l
       const int first = m ? __ffs(m) - 1 : 0;
       const long long rf = __shfl_sync(0xffffffffu, static_cast<long long>(row), first);
       if (lane == 0) {
         smask[slot] = m;
         mbar_arrive_expect_tx(&full[slot], m ? 2u * 16u * G::kRowBytes : 0u);
-        if (m) {
-          const int y = static_cast<int>(rf - first);
-          unsigned char* kd = wbase + slot * G::kSlotBytes;
+      }
+      __syncwarp();
+      unsigned char* kd = wbase + slot * G::kSlotBytes;
+      if (a.source == kSparse) {
+        // scattered rows: op o = lane (< 8 * kSlabs) fetches rows 4q .. 4q + 3 of
+        // slab h of K (kv = 0) or V; a masked key fetches the tile's first
+        // valid row instead (its V row is zeroed after the load)
+        const int q = lane & 3, h = (lane >> 2) % G::kSlabs, kv = lane / (4 * G::kSlabs);
+        const int mine = static_cast<int>(row >= 0 ? row : rf);
+        const int y0 = __shfl_sync(0xffffffffu, mine, 4 * q);
+        const int y1 = __shfl_sync(0xffffffffu, mine, 4 * q + 1);
+        const int y2 = __shfl_sync(0xffffffffu, mine, 4 * q + 2);
+        const int y3 = __shfl_sync(0xffffffffu, mine, 4 * q + 3);
+        if (m && lane < 8 * G::kSlabs)
+          tc05::tma_gather4(kd + kv * G::kHalfBytes + h * G::kSlabBytes + q * 512, kv ? &tv : &tk,
+                            64 * h, y0, y1, y2, y3, &full[slot]);
+      } else if (m && lane == 0) {
+        // consecutive rows (a page, or positions of a dense cache): row(l) = row(0) + l
+        const int y = static_cast<int>(rf - first);
 #pragma unroll
-          for (int h = 0; h < G::kSlabs; ++h) {
-            tc05::tma_load2(kd + h * G::kSlabBytes, &tk, 64 * h, y, &full[slot]);
-            tc05::tma_load2(kd + G::kHalfBytes + h * G::kSlabBytes, &tv, 64 * h, y, &full[slot]);
-          }
+        for (int h = 0; h < G::kSlabs; ++h) {
+          tc05::tma_load2(kd + h * G::kSlabBytes, &tk, 64 * h, y, &full[slot]);
+          tc05::tma_load2(kd + G::kHalfBytes + h * G::kSlabBytes, &tv, 64 * h, y, &full[slot]);
         }
       }
       __syncwarp();
@@ -718,20 +733,23 @@ static int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? 0 : -1;
 }
 
-// Paged pools [num_pages, Hkv, page_tokens, D] as 2-D tensors of 16-bit rows,
-// boxes of 64 dims x 16 rows in the 128-byte swizzle.  False when the pools
-// cannot be described (then the per-row copies are used).
-static bool paged_maps(const GatherArgs& a, int dtype, CUtensorMap* tk, CUtensorMap* tv) {
-  if (a.source != kPaged || a.page_tokens % 16 != 0 || (a.D != 64 && a.D != 128 && a.D != 256))
-    return false;
-  const int64_t rows = a.num_pages * a.Hkv * a.page_tokens;
+// K and V as 2-D tensors of 16-bit rows for the TMA-fed slots: page pools
+// [num_pages, Hkv, page_tokens, D] and dense caches [B, Hkv, T, D] in boxes of
+// 64 dims x 16 rows (a tile's rows are consecutive), selected-token caches in
+// boxes one row high for tile::gather4.  All in the 128-byte swizzle.  False
+// when the tensors cannot be described (then the per-row copies are used).
+static bool kv_maps(const GatherArgs& a, int dtype, CUtensorMap* tk, CUtensorMap* tv) {
+  if (a.D != 64 && a.D != 128 && a.D != 256) return false;
+  if (a.source == kPaged && a.page_tokens % 16 != 0) return false;
+  const int64_t rows =
+      a.source == kPaged ? a.num_pages * a.Hkv * a.page_tokens : a.B * a.Hkv * a.T;
   if (rows < 16 || rows >= (int64_t(1) << 31)) return false;
   if ((reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v)) & 15) return false;
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.D), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.D * 2)};
-  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t box[2] = {64, a.source == kSparse ? 1u : 16u};
   const cuuint32_t es[2] = {1, 1};
   const CUtensorMapDataType dt =
       dtype == SA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -750,7 +768,7 @@ static int launch_stream_t(const GatherArgs& a, int dtype, int grid, cudaStream_
   CUtensorMap tk, tv;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
-  if (paged_maps(a, dtype, &tk, &tv)) {
+  if (kv_maps(a, dtype, &tk, &tv)) {
     const size_t smem = smem_bytes_t<D, true>(a.source, a.B);
     if (cudaFuncSetAttribute(gather_stream_kernel<T, D, NT, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,

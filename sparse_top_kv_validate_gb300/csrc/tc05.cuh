@@ -205,6 +205,18 @@ __device__ __forceinline__ void tma_load2(void* dst, const CUtensorMap* m, int x
       : "memory");
 }
 
+// Four rows y0..y3 (columns [x, x + box width)) of a 2-D tensor whose map has
+// a box one row high, into four consecutive rows at `dst`, completing on `bar`.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, int x, int y0, int y1,
+                                            int y2, int y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 3-D tiled store of the box at (x, y, z) from `src` (bulk-group completion);
 // rows or columns outside the tensor are not written.
 __device__ __forceinline__ void tma_store3(const CUtensorMap* m, int x, int y, int z,
