@@ -10,7 +10,8 @@ the selected K/V rows and merges the partial softmax results (three kernels).
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
 
 Prints one JSON line.  Timing: CUDA events around each step on the launching
-stream, with an L2 flush (a 512 MB write) between steps outside the events;
+stream, with an L2 flush (a 512 MB write, then a 256 MB read that writes the
+flush's dirty lines back) between steps outside the events;
 the decode call itself is bracketed by its own events for the roofline.
 """
 from __future__ import annotations
@@ -523,11 +524,20 @@ def run_gpu(args):
     import sparse_top_kv_validate_gb300 as sa
     sa.load()
     wl = make_workload(sa, args.workload, dev)
+    # L2 flush between steps, outside the events: a 512 MB write evicts the
+    # step's inputs, then a 256 MB read of another buffer writes the flush's own
+    # dirty lines back, so that this write-back does not land in the next step
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    clean = torch.ones(128 * 1024 * 1024, dtype=torch.float16, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        sink.copy_(clean.sum(dtype=torch.float32))
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(args.warmup, 3)):
-        flush.zero_()
+        flush_l2()
         wl.step()
     torch.cuda.synchronize(dev)
 
@@ -542,7 +552,7 @@ def run_gpu(args):
     with ClockSampler(dev) as clk:
         t0 = time.perf_counter()
         for i in range(steps):
-            flush.zero_()
+            flush_l2()
             starts[i].record(stream)
             wl.step(dec[i])
             ends[i].record(stream)
@@ -566,7 +576,7 @@ def run_gpu(args):
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     h2d = d2h = 0
     for i in range(e2e_steps):
-        flush.zero_()
+        flush_l2()
         e_s[i].record(stream)
         h2d = wl.h2d()
         wl.step()
@@ -596,7 +606,8 @@ def run_gpu(args):
             "dtype": str(wl.q.dtype).replace("torch.", "").replace("bfloat16", "bf16"),
             "data": "synthetic (seeded N(0,1) Q/K/V, uniform sorted top-k indices)",
             "config": dict(wl.config(), parallelism=f"replicas x{ws}" if ws > 1 else "single GPU",
-                           l2="flushed between steps (512 MB write outside the step events)",
+                           l2="flushed between steps outside the step events: a 512 MB write, "
+                              "then a 256 MB read that writes the flush's dirty lines back",
                            timing="sum of per-step CUDA events on the launching stream"),
             "roofline": wl.roofline(statistics.median(dec_ms), peaks),
             "e2e": {"value": round(wl.rows * ws / (e2e_ms * 1e-3), 1),
