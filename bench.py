@@ -484,7 +484,7 @@ class CsaFp8Decode:
 # kernel exists.
 TRAFFIC: dict = {
     # plan + gather_stream + combine kernels of one call, ncu dram read + write
-    "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 279922176,
+    "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 279921053,
     # plan + gather-decode + tcgen05 attention + combine of one call, ncu dram read + write
     # (cold: the decoded rows and split partials, L2-resident live, count again)
     "csa_fp8_b16_h128_d576_t65536_k2048_w128": 83579616,
