@@ -43,6 +43,33 @@ def test_paged_decode_matches_oracle(cuda_lib, dt, over):
     assert_close(to64(y), ref, y.dtype, f"paged {dt} {over}")
 
 
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("page_tokens", [16, 32])
+def test_paged_slots_past_the_context_never_reach_the_output(cuda_lib, dt, page_tokens):
+    """Pool slots past each sequence's context, in its last page, hold NaN: the
+    tensor-core path loads whole pages, so those rows must be masked in K and
+    zeroed in V before P.V."""
+    c, inp = _paged_small(dt, seed=6, page_tokens=page_tokens, ctx_high=700)
+    pool_k, pool_v = inp["k_pool"].clone(), inp["v_pool"].clone()
+    for b in range(c.B):
+        n = int(inp["ctx_len"][b])
+        last_page = int(inp["block_table"][b, (n - 1) // c.page_tokens])
+        first_free = n % c.page_tokens
+        if first_free:
+            pool_k[last_page, :, first_free:, :] = float("nan")
+            pool_v[last_page, :, first_free:, :] = float("nan")
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = cuda_lib.paged_attn_decode(inp["q"].to(DEV), pool_k.to(DEV), pool_v.to(DEV),
+                                   inp["block_table"].to(DEV), inp["ctx_len"].to(DEV),
+                                   scale=c.eff_scale(), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.isfinite(y.float()).all()
+    ref = oracle.paged_decode(inp["q"], inp["k_pool"], inp["v_pool"], inp["block_table"],
+                              inp["ctx_len"], page_tokens=c.page_tokens, scale=c.eff_scale())
+    assert_close(to64(y), ref, y.dtype, f"paged NaN tail {dt} p{page_tokens}")
+
+
 def test_paged_bad_table_entry_latches_and_skips(cuda_lib):
     c, inp = _paged_small("f16", seed=4)
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
@@ -89,7 +116,11 @@ def test_full_size_paged_fp16_sampled_sequences(cuda_lib):
                                   dict(B=1, S=129, Hq=3, Hkv=1, causal=False),
                                   dict(S=300, D=64, softcap=0.0, causal=False),
                                   dict(S=260, softcap=5.0), dict(S=260, softcap=2.0, causal=False),
-                                  dict(S=300, softcap=100.0), dict(S=129, softcap=80.0, causal=False)])
+                                  dict(S=300, softcap=100.0), dict(S=129, softcap=80.0, causal=False),
+                                  # D = 256: the stream kernel's dense source (TMA boxes of
+                                  # consecutive rows) instead of the tcgen05 prefill
+                                  dict(B=1, S=150, Hq=4, Hkv=2, D=256),
+                                  dict(B=2, S=70, Hq=2, Hkv=2, D=256, causal=False)])
 def test_prefill_matches_oracle_and_present_is_exact(cuda_lib, dt, over):
     base = dict(B=2, S=333, Hq=16, Hkv=4, D=128, causal=True, softcap=50.0, dtype=dt)
     base.update(over)
