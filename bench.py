@@ -11,8 +11,10 @@ the selected K/V rows and merges the partial softmax results (three kernels).
 
 Prints one JSON line.  Timing: CUDA events around each step on the launching
 stream, with an L2 flush (a 512 MB write, then a 256 MB read that writes the
-flush's dirty lines back) between steps outside the events;
-the decode call itself is bracketed by its own events for the roofline.
+flush's dirty lines back) between steps outside the events.  The roofline
+divides the dominant kernel's algorithmic bytes (or flops) by its live
+duration, taken in a separate pass in which the library records CUDA events
+around that one kernel (sa.kernel_events); the whole call's figures sit beside.
 """
 from __future__ import annotations
 
@@ -214,15 +216,12 @@ class SparseDecode:
         return oracle.sparse_attention(h["q"], h["idx"], h["k"], h["v"], scale=c.eff_scale(),
                                        rows=rows)
 
-    def roofline(self, decode_ms, peaks):
-        achieved = self.decode_bytes / (decode_ms * 1e-3) / 1e9
-        return {"bound": "hbm", "kernel": "sparse_attn_decode call (plan + gather_stream + combine)",
-                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-                "peak_source": peaks["source"] + " (copy bandwidth, burst)",
-                "algorithmic_bytes": int(self.decode_bytes),
-                "decode_us": round(decode_ms * 1e3, 2), "traffic": TRAFFIC.get(self.c.name)}
+    def roofline(self, decode_ms, kernel_ms, peaks):
+        # the gather kernel: each valid selected K and V row once, Q read, Y written
+        es = self.q.element_size()
+        kbytes = self.valid * 2 * self.c.D * es + self.q.numel() * es + self.y.numel() * es
+        return hbm_roofline("gather_stream_kernel", kbytes, kernel_ms, self.decode_bytes,
+                            decode_ms, peaks, TRAFFIC.get(self.c.name))
 
 
 class PagedDecode:
@@ -303,15 +302,13 @@ class PagedDecode:
             out.append(y[0])
         return np.stack(out)
 
-    def roofline(self, decode_ms, peaks):
-        achieved = self.decode_bytes / (decode_ms * 1e-3) / 1e9
-        return {"bound": "hbm", "kernel": "paged_attn_decode call (append + gather_stream + "
-                "combine)", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-                "peak_source": peaks["source"] + " (copy bandwidth, burst)",
-                "algorithmic_bytes": int(self.decode_bytes),
-                "decode_us": round(decode_ms * 1e3, 2), "traffic": TRAFFIC.get(self.c.name)}
+    def roofline(self, decode_ms, kernel_ms, peaks):
+        # the gather kernel: every context token's K and V rows, the table, Q and Y
+        es = self.q.element_size()
+        kbytes = (self.tokens * self.c.Hkv * self.c.D * es * 2 + self.inp["block_table"].numel() * 4
+                  + 2 * self.q.numel() * es)
+        return hbm_roofline("gather_stream_kernel (paged)", kbytes, kernel_ms, self.decode_bytes,
+                            decode_ms, peaks, TRAFFIC.get(self.c.name))
 
 
 class Prefill:
@@ -378,14 +375,9 @@ class Prefill:
         return oracle.prefill(q, k, v, scale=c.eff_scale(), causal=c.causal, softcap=c.softcap,
                               rows=picked)
 
-    def roofline(self, ms, peaks):
-        tf = self.flops / (ms * 1e-3) / 1e12
-        return {"bound": "tensor", "kernel": "attn_prefill call", "achieved": round(tf, 2),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(tf / peaks["bf16_tflops"], 4),
-                "peak_source": peaks["source"] + " (cuBLAS bf16, burst)",
-                "algorithmic_flops": self.flops, "call_us": round(ms * 1e3, 2),
-                "traffic": TRAFFIC.get(self.c.name)}
+    def roofline(self, ms, kernel_ms, peaks):
+        return tensor_roofline("prefill_tc05_kernel", self.flops, kernel_ms, ms, peaks,
+                               TRAFFIC.get(self.c.name))
 
 
 class CsaFp8Decode:
@@ -466,31 +458,55 @@ class CsaFp8Decode:
                                                rows=[h])[0])
         return np.stack(out)
 
-    def roofline(self, ms, peaks):
+    def roofline(self, ms, kernel_ms, peaks):
+        # every flop of the call is in the tensor-core attention kernel
+        line = tensor_roofline("fp8_tc05_kernel" if self.c.Hq % 128 == 0 else "fp8_decode_kernel",
+                               self.flops, kernel_ms, ms, peaks, TRAFFIC.get(self.c.name))
         gbs = self.decode_bytes / (ms * 1e-3) / 1e9
-        tf = self.flops / (ms * 1e-3) / 1e12
-        return {"bound": "tensor", "kernel": "sparse_attn_decode call on FP8 records "
-                "(plan + fp8_gather_decode + fp8_tc05 + combine)", "achieved": round(tf, 2),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(tf / peaks["bf16_tflops"], 4),
-                "peak_source": peaks["source"] + " (cuBLAS bf16, burst)",
-                "algorithmic_flops": self.flops, "algorithmic_bytes": int(self.decode_bytes),
-                "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
-                "call_us": round(ms * 1e3, 2), "traffic": TRAFFIC.get(self.c.name)}
+        line.update(algorithmic_bytes=int(self.decode_bytes), call_hbm_gbs=round(gbs, 1),
+                    call_hbm_frac=round(gbs / peaks["hbm_gbs"], 4))
+        return line
 
 
 # DRAM bytes (read + write) per decode launch from an ncu capture of the
 # dominant kernel, keyed by workload; None until a capture of the current
 # kernel exists.
 TRAFFIC: dict = {
-    # plan + gather_stream + combine kernels of one call, ncu dram read + write
-    "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 279921053,
-    # plan + gather-decode + tcgen05 attention + combine of one call, ncu dram read + write
-    # (cold: the decoded rows and split partials, L2-resident live, count again)
-    "csa_fp8_b16_h128_d576_t65536_k2048_w128": 83579616,
+    # gather_stream_kernel (TMA gather4), one launch, ncu dram read + write
+    "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 271466338,
+    # fp8_tc05_kernel, one launch, ncu dram read + write (ncu flushes caches between
+    # kernels, so the 40 MB of decoded rows count from DRAM; live they come from L2)
+    "csa_fp8_b16_h128_d576_t65536_k2048_w128": 42660960,
     # prefill_tc05_kernel, one launch (Q, K, V read; Y and present K/V written)
     "prefill_bf16_b4_s4096_h32_kv8_d128_causal_softcap50": 441644032,
 }
+
+
+def hbm_roofline(kernel, kbytes, kernel_ms, call_bytes, call_ms, peaks, traffic):
+    """HBM roofline of the dominant kernel (its algorithmic bytes over its live
+    event-bracketed duration), with the whole call's figures beside it."""
+    achieved = kbytes / (kernel_ms * 1e-3) / 1e9
+    call = call_bytes / (call_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": traffic, "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "peak_source": peaks["source"] + " (copy bandwidth, burst)",
+            "algorithmic_bytes": int(kbytes), "kernel_us": round(kernel_ms * 1e3, 2),
+            "call_algorithmic_bytes": int(call_bytes), "call_us": round(call_ms * 1e3, 2),
+            "call_achieved": round(call, 1), "call_frac": round(call / peaks["hbm_gbs"], 4)}
+
+
+def tensor_roofline(kernel, flops, kernel_ms, call_ms, peaks, traffic):
+    """Tensor roofline of the dominant kernel, with the whole call beside it."""
+    tf = flops / (kernel_ms * 1e-3) / 1e12
+    call = flops / (call_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "kernel": kernel, "achieved": round(tf, 2),
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(tf / peaks["bf16_tflops"], 4), "traffic": traffic,
+            "peak_source": peaks["source"] + " (cuBLAS bf16, burst)",
+            "algorithmic_flops": flops, "kernel_us": round(kernel_ms * 1e3, 2),
+            "call_us": round(call_ms * 1e3, 2), "call_achieved": round(call, 2),
+            "call_frac": round(call / peaks["bf16_tflops"], 4)}
 
 
 def make_workload(sa, name, dev):
@@ -588,6 +604,18 @@ def run_gpu(args):
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
+    # dominant-kernel leg: the library records events around its dominant
+    # kernel (sa.kernel_events); same flush protocol, separate from the timed
+    # steps because recording between kernels removes their launch overlap
+    k_steps = max(3, min(steps, 50))
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(k_steps)]
+    for i in range(k_steps):
+        flush_l2()
+        with sa.kernel_events(*kev[i]):
+            wl.step()
+    torch.cuda.synchronize(dev)
+    kernel_ms = statistics.median(a.elapsed_time(b) for a, b in kev)
     err = int(wl.err.item())
 
     if rank == 0:
@@ -609,7 +637,7 @@ def run_gpu(args):
                            l2="flushed between steps outside the step events: a 512 MB write, "
                               "then a 256 MB read that writes the flush's dirty lines back",
                            timing="sum of per-step CUDA events on the launching stream"),
-            "roofline": wl.roofline(statistics.median(dec_ms), peaks),
+            "roofline": wl.roofline(statistics.median(dec_ms), kernel_ms, peaks),
             "e2e": {"value": round(wl.rows * ws / (e2e_ms * 1e-3), 1),
                     "unit": "tokens/s" if isinstance(wl, Prefill) else "query-rows/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),

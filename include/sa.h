@@ -85,6 +85,22 @@ const char* sa_status_string(int status);
 int sa_version(void);
 
 /*
+ * sa_set_kernel_events -- measurement hook (no counterpart on the pages).
+ *
+ * before, after: cudaEvent_t handles (created by the caller, with timing
+ * enabled), or both NULL to turn the hook off.  While set, every call made
+ * from this host thread records `before` on its stream immediately before it
+ * launches its dominant kernel (the gather kernel of a decode, the tensor-core
+ * attention kernel of an FP8 decode, the prefill kernel) and `after`
+ * immediately after it, so that the events bracket that one kernel.  The
+ * handles are not owned; the caller keeps them alive while the hook is set.
+ * Recording between two kernels removes their launch overlap, so timings of
+ * whole calls are taken with the hook off.
+ * Returns SA_OK, or SA_ERR_NULL if exactly one of the two is NULL.
+ */
+int sa_set_kernel_events(void* before, void* after);
+
+/*
  * validate_indices -- [IS] validate_indices / validate_index_rows.
  *
  * idx: [B, I, Sq, K] int32 (idx_is_i64 = 0) or int64 (idx_is_i64 = 1).

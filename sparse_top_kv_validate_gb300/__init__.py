@@ -27,7 +27,7 @@ __all__ = [
     "F32", "F16", "BF16", "FP8_E4M3_B64",
     "IDX_BELOW_SENTINEL", "IDX_AFTER_PADDING", "IDX_OUT_OF_RANGE", "IDX_NOT_INCREASING",
     "IDX_DUPLICATE", "IDX_ALL_PADDING", "ERRBIT_WRITE_POS", "ERRBIT_PAGE", "ERRBIT_TIMEOUT",
-    "SparseParams", "PrefillParams", "PagedParams",
+    "SparseParams", "PrefillParams", "PagedParams", "kernel_events",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -111,6 +111,8 @@ def load():
         L.sa_status_string.argtypes = [C.c_int]
         L.sa_version.restype = C.c_int
         L.sa_version.argtypes = []
+        L.sa_set_kernel_events.restype = C.c_int
+        L.sa_set_kernel_events.argtypes = [_p, _p]
         L.validate_indices.restype = C.c_int
         L.validate_indices.argtypes = [_p, C.c_int, _i64, _i64, _i64, _i64, _p, _i64, _p, _p, _p]
         L.build_present_kv.restype = C.c_int
@@ -132,6 +134,31 @@ def load():
         L.paged_attn_decode.argtypes = [C.POINTER(PagedParams), _p]
         _lib = L
         return _lib
+
+
+class kernel_events:
+    """Measurement hook: within the ``with`` block, every call of this library
+    from this host thread records ``before`` / ``after`` (timing
+    ``torch.cuda.Event`` objects, recorded once here so that they exist) on its
+    stream around its dominant kernel; ``before.elapsed_time(after)`` is then
+    that kernel's duration for the last call."""
+
+    def __init__(self, before, after):
+        self.before, self.after = before, after
+
+    def __enter__(self):
+        for ev in (self.before, self.after):
+            if not ev.cuda_event:
+                ev.record()
+        torch.cuda.synchronize()
+        _check("sa_set_kernel_events",
+               load().sa_set_kernel_events(C.c_void_p(self.before.cuda_event),
+                                           C.c_void_p(self.after.cuda_event)))
+        return self
+
+    def __exit__(self, *exc):
+        load().sa_set_kernel_events(None, None)
+        return False
 
 
 def status_string(status: int) -> str:

@@ -934,11 +934,14 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   p.c_log2 = g.softcap * log2e;
   const unsigned grid = static_cast<unsigned>(g.units * p.hblocks * kParts * g.splits);
   const unsigned cl = cluster ? static_cast<unsigned>(g.splits) : 1u;
-  if (g.softcap != 0.0f)
-    return set_smem<true>() ? launch_pdl(fp8_tc05_kernel<true>, grid, kThreads, kSmem, st, cl, tq, tk, p)
-                            : -1;
-  return set_smem<false>() ? launch_pdl(fp8_tc05_kernel<false>, grid, kThreads, kSmem, st, cl, tq, tk, p)
-                           : -1;
+  if (!(g.softcap != 0.0f ? set_smem<true>() : set_smem<false>())) return -1;
+  mark_event(g.ev_before, st);
+  const int rc =
+      g.softcap != 0.0f
+          ? launch_pdl(fp8_tc05_kernel<true>, grid, kThreads, kSmem, st, cl, tq, tk, p)
+          : launch_pdl(fp8_tc05_kernel<false>, grid, kThreads, kSmem, st, cl, tq, tk, p);
+  mark_event(g.ev_after, st);
+  return rc;
 }
 
 }  // namespace sa

@@ -112,6 +112,8 @@ struct GatherArgs {
   // FP8 hybrid records (sparse source)
   int64_t record_stride;      // bytes between records
   void* fp8_kdec;             // tcgen05 FP8 path: decoded rows [units, n_cand_pad, 576] bf16
+  void* ev_before;            // nullable cudaEvent_t pair recorded around the dominant kernel
+  void* ev_after;
   // math
   float scale_log2;           // scale * log2(e)
   float softcap;              // 0 = off
@@ -148,6 +150,11 @@ int launch_fp8_tc(const GatherArgs& a, cudaStream_t st);
 int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st);
 
 // ---- dense prefill on the fifth-generation tensor cores (tcgen05 + TMEM + TMA) ------
+// Records ev (a cudaEvent_t, nullable) on st: the measurement hook.
+inline void mark_event(void* ev, cudaStream_t st) {
+  if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev), st);
+}
+
 struct PrefillTcArgs {
   const void* q;              // [B, Hq, S, D]
   const void* k;              // [B, Hkv, S, D]

@@ -229,20 +229,39 @@ void carve(Plan& pl, void* ws) {
   }
 }
 
+// Measurement hook: events recorded around the dominant kernel of each call
+// made from this host thread (sa_set_kernel_events).
+thread_local void* t_ev_before = nullptr;
+thread_local void* t_ev_after = nullptr;
+
 int run_plan(Plan& pl, int dtype, cudaStream_t st) {
   sa::GatherArgs& g = pl.g;
+  g.ev_before = t_ev_before;
+  g.ev_after = t_ev_after;
   if (pl.fp8) {
-    if ((pl.fp8_tc ? sa::launch_fp8_tc(g, st) : sa::launch_fp8_decode(g, st)) != 0)
-      return SA_ERR_LAUNCH;
+    if (pl.fp8_tc) {
+      if (sa::launch_fp8_tc(g, st) != 0) return SA_ERR_LAUNCH;  // brackets its attention kernel
+    } else {
+      sa::mark_event(g.ev_before, st);
+      const int rc = sa::launch_fp8_decode(g, st);
+      sa::mark_event(g.ev_after, st);
+      if (rc != 0) return SA_ERR_LAUNCH;
+    }
     if (pl.fp8_combine && sa::launch_combine(g, SA_BF16, st) != 0) return SA_ERR_LAUNCH;
     return SA_OK;
   }
   if (pl.stream) {
-    if (sa::launch_gather_stream(g, dtype, pl.grid, st) != 0) return SA_ERR_LAUNCH;
+    sa::mark_event(g.ev_before, st);
+    const int rc = sa::launch_gather_stream(g, dtype, pl.grid, st);
+    sa::mark_event(g.ev_after, st);
+    if (rc != 0) return SA_ERR_LAUNCH;
     if (sa::launch_stream_combine(g, dtype, st) != 0) return SA_ERR_LAUNCH;
     return SA_OK;
   }
-  if (sa::launch_gather_simt(g, dtype, st) != 0) return SA_ERR_LAUNCH;
+  sa::mark_event(g.ev_before, st);
+  const int rc = sa::launch_gather_simt(g, dtype, st);
+  sa::mark_event(g.ev_after, st);
+  if (rc != 0) return SA_ERR_LAUNCH;
   if (sa::launch_combine(g, dtype, st) != 0) return SA_ERR_LAUNCH;
   return SA_OK;
 }
@@ -348,6 +367,13 @@ int sparse_plan(const sa_sparse_params* p, Plan& pl) {
 }  // namespace
 
 extern "C" {
+
+int sa_set_kernel_events(void* before, void* after) {
+  if ((before == nullptr) != (after == nullptr)) return SA_ERR_NULL;
+  t_ev_before = before;
+  t_ev_after = after;
+  return SA_OK;
+}
 
 const char* sa_status_string(int status) {
   switch (status) {
@@ -639,7 +665,10 @@ int attn_prefill(const sa_prefill_params* p, void* stream) {
       return SA_ERR_ALIGN;
     sa::PrefillTcArgs a;  // present K/V are written by the kernel itself
     prefill_tc_args(p, a);
-    return sa::launch_prefill_tc(a, st) == 0 ? SA_OK : SA_ERR_LAUNCH;
+    sa::mark_event(t_ev_before, st);
+    const int lrc = sa::launch_prefill_tc(a, st);
+    sa::mark_event(t_ev_after, st);
+    return lrc == 0 ? SA_OK : SA_ERR_LAUNCH;
   }
   Plan pl;
   prefill_args(p, pl.g);
