@@ -77,6 +77,12 @@ def test_status_strings(lib):
     assert lib.sa_version() >= 100
 
 
+def test_kernel_event_hook_needs_both_events_or_none(lib):
+    assert lib.sa_set_kernel_events(C.c_void_p(0x1000), None) == -1
+    assert lib.sa_set_kernel_events(None, C.c_void_p(0x1000)) == -1
+    assert lib.sa_set_kernel_events(None, None) == 0
+
+
 def test_host_checks_reject_bad_requests_without_launching(lib):
     # validate_indices: null pointers, bad shapes
     assert lib.validate_indices(None, 0, 1, 1, 1, 4, None, 10, None, None, None) == -1

@@ -319,6 +319,27 @@ def test_workspace_contents_on_entry_do_not_matter(cuda_lib):
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
 
 
+def test_kernel_events_bracket_the_gather_kernel_only(cuda_lib):
+    c = synth.sparse_bf16(B=4, T=3000, K=700)
+    inp = synth.make_sparse_inputs(c, seed=31, device=DEV)
+    y = torch.empty_like(inp["q"])
+    run = lambda: cuda_lib.sparse_attn_decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["idx"],
+                                              scale=c.eff_scale(), y=y)
+    run()
+    call0, call1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with cuda_lib.kernel_events(k0, k1):
+        call0.record()
+        run()
+        call1.record()
+    torch.cuda.synchronize()
+    kernel_ms, call_ms = k0.elapsed_time(k1), call0.elapsed_time(call1)
+    assert 0.0 < kernel_ms < call_ms
+    ref = oracle.sparse_attention(inp["q"].cpu(), inp["idx"].cpu(), inp["k_cache"].cpu(),
+                                  inp["v_cache"].cpu(), scale=c.eff_scale())
+    assert_close(to64(y), ref, y.dtype, "hooked call")
+
+
 # ---------------------------------------------------------------------------
 # FP8 hybrid-record latent cache (MQA, 512 E4M3 + 64 bf16 dims)
 # ---------------------------------------------------------------------------
