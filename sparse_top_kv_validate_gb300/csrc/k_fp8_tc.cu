@@ -270,6 +270,8 @@ __global__ void __launch_bounds__(256) fp8_gather_decode_kernel(const DecodePara
   if (row0 >= p.rows) return;
   uint2* st = stage + warp * kDecRecs * 82;
   const int32_t mine = (lane < kDecRecs && row0 + lane < p.rows) ? __ldg(p.pos + row0 + lane) : -1;
+  // two commit groups of kDecRecs / 2 records: the first half is decoded
+  // while the second half's copies are still landing
 #pragma unroll
   for (int r = 0; r < kDecRecs; ++r) {
     const int32_t pr = __shfl_sync(0xffffffffu, mine, r);
@@ -281,18 +283,24 @@ __global__ void __launch_bounds__(256) fp8_gather_decode_kernel(const DecodePara
       for (int k = 0; k < 3; ++k)
         if (lane + 32 * k < 81) cp_async8(st + r * 82 + lane + 32 * k, rec + lane + 32 * k);
     }
+    if (r == kDecRecs / 2 - 1 || r == kDecRecs - 1)
+      asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  __syncwarp();
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    if (half == 0) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
 #pragma unroll 1
-  for (int r = 0; r < kDecRecs; ++r) {
-    const int64_t row = row0 + r;
-    if (row >= p.rows) break;
-    uint4* out = reinterpret_cast<uint4*>(p.kdec + row * kD);  // 72 x 16 bytes
-    if (__shfl_sync(0xffffffffu, mine, r) < 0) {
-      for (int i = lane; i < kRowBytes / 16; i += 32) out[i] = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-      decode_row(st + r * 82, out, lane);
+    for (int r = half * (kDecRecs / 2); r < (half + 1) * (kDecRecs / 2); ++r) {
+      const int64_t row = row0 + r;
+      if (row >= p.rows) break;
+      uint4* out = reinterpret_cast<uint4*>(p.kdec + row * kD);  // 72 x 16 bytes
+      if (__shfl_sync(0xffffffffu, mine, r) < 0) {
+        for (int i = lane; i < kRowBytes / 16; i += 32) out[i] = make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        decode_row(st + r * 82, out, lane);
+      }
     }
   }
 }
