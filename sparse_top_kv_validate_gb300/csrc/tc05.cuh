@@ -276,7 +276,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
   return false;
 }
 
-// The same, with one verdict for the whole warp (its lanes then stay converged
+// The same, with one outcome for the whole warp (its lanes then stay converged
 // for the warp-collective tensor-memory instructions that follow).
 __device__ __forceinline__ bool wait_or_abort_warp(uint64_t* bar, uint32_t parity,
                                                    volatile int* abort_flag, uint32_t* err_word) {
