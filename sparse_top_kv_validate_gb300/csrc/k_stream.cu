@@ -30,6 +30,7 @@
 //  * A unit inside one warp's range is written directly; a unit split across
 //    warps leaves one partial per warp, merged by stream_combine_kernel in
 //    warp order (deterministic).
+#include <cstdlib>
 #include <cstring>
 
 #include "gather_common.cuh"
@@ -739,6 +740,8 @@ static int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t
 // boxes one row high for tile::gather4.  All in the 128-byte swizzle.  False
 // when the tensors cannot be described (then the per-row copies are used).
 static bool kv_maps(const GatherArgs& a, int dtype, CUtensorMap* tk, CUtensorMap* tv) {
+  const char* env = std::getenv("SA_STREAM_TMA");  // "0": the per-row copies for every source
+  if (env && std::strcmp(env, "0") == 0) return false;
   if (a.D != 64 && a.D != 128 && a.D != 256) return false;
   if (a.source == kPaged && a.page_tokens % 16 != 0) return false;
   const int64_t rows =

@@ -319,6 +319,21 @@ def test_workspace_contents_on_entry_do_not_matter(cuda_lib):
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_stream_row_copy_path_matches_oracle(cuda_lib, dt, monkeypatch):
+    """SA_STREAM_TMA=0: the stream kernel's per-row bulk copies (the path taken
+    when the caches cannot be described by tensor maps) for selected rows."""
+    monkeypatch.setenv("SA_STREAM_TMA", "0")
+    c = synth.sparse_bf16(B=3, T=2000, K=500, dtype=dt, pad_prob=0.5, pad_max=100)
+    inp = synth.make_sparse_inputs(c, seed=33)
+    y = cuda_lib.sparse_attn_decode(inp["q"].to(DEV), inp["k_cache"].to(DEV), inp["v_cache"].to(DEV),
+                                    inp["idx"].to(DEV), scale=c.eff_scale())
+    torch.cuda.synchronize()
+    ref = oracle.sparse_attention(inp["q"], inp["idx"], inp["k_cache"], inp["v_cache"],
+                                  scale=c.eff_scale())
+    assert_close(to64(y), ref, y.dtype, f"row copies {dt}")
+
+
 def test_kernel_events_bracket_the_gather_kernel_only(cuda_lib):
     c = synth.sparse_bf16(B=4, T=3000, K=700)
     inp = synth.make_sparse_inputs(c, seed=31, device=DEV)
