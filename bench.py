@@ -137,6 +137,37 @@ class ClockSampler:
 # workloads
 # ---------------------------------------------------------------------------
 
+class Staging:
+    """Several tensors as 256-byte-aligned slices of one device buffer, with a
+    pinned host twin: a step's inputs (or outputs) cross in one copy.  The
+    device slices replace the original tensors (same shapes, dtypes, data)."""
+
+    def __init__(self, tensors, dev):
+        offs, off = [], 0
+        for t in tensors:
+            off = (off + 255) // 256 * 256
+            offs.append(off)
+            off += t.numel() * t.element_size()
+        self.nbytes = off
+        self.dev = torch.empty(max(off, 1), dtype=torch.uint8, device=dev)
+        self.host = torch.empty(max(off, 1), dtype=torch.uint8).pin_memory()
+        self.views = []
+        for t, o in zip(tensors, offs):
+            n = t.numel() * t.element_size()
+            v = self.dev[o:o + n].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            self.host[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+            self.views.append(v)
+
+    def h2d(self):
+        self.dev.copy_(self.host, non_blocking=True)
+        return self.nbytes
+
+    def d2h(self):
+        self.host.copy_(self.dev, non_blocking=True)
+        return self.nbytes
+
+
 class SparseDecode:
     """Selected-token decode step (append + validate + gather decode)."""
 
@@ -145,12 +176,15 @@ class SparseDecode:
     def __init__(self, sa, c: synth.SparseCase, dev, seed=1001):
         self.sa, self.c, self.dev = sa, c, dev
         inp = synth.make_sparse_inputs(c, seed, device=dev)
-        self.q, self.k, self.v, self.idx = inp["q"], inp["k_cache"], inp["v_cache"], inp["idx"]
-        self.k_cur, self.v_cur = inp["k_cur"], inp["v_cur"]
+        self.k, self.v = inp["k_cache"], inp["v_cache"]
+        # the step's inputs and outputs in one staging buffer each (e2e leg)
+        self.s_in = Staging([inp["q"], inp["idx"], inp["k_cur"], inp["v_cur"]], dev)
+        self.q, self.idx, self.k_cur, self.v_cur = self.s_in.views
         self.write_pos = torch.full((c.B,), c.T - c.cur, dtype=torch.int64, device=dev)
-        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.s_out = Staging([torch.empty((c.B, c.Hq, 1, c.D), dtype=self.q.dtype, device=dev),
+                              torch.zeros(1, dtype=torch.int32, device=dev)], dev)
+        self.y, self.err = self.s_out.views
         self.status = torch.empty(c.B * c.I, dtype=torch.uint8, device=dev)
-        self.y = torch.empty((c.B, c.Hq, 1, c.D), dtype=self.q.dtype, device=dev)
         nws = sa.sparse_attn_decode_workspace(self.q, self.k, self.v, self.idx,
                                               scale=c.eff_scale(), k_cur=self.k_cur,
                                               v_cur=self.v_cur, write_pos=self.write_pos,
@@ -165,13 +199,6 @@ class SparseDecode:
         self.decode_bytes = (self.valid * 2 * c.D * es + self.idx.numel() * self.idx.element_size()
                              + self.q.numel() * es + self.y.numel() * es + 2 * cur_bytes)
         self.launches_per_step = 3  # plan (validate + positions + append), gather, combine
-        # host copies for the end-to-end leg
-        self.h_q = self.q.cpu().pin_memory()
-        self.h_idx = self.idx.cpu().pin_memory()
-        self.h_kc = self.k_cur.cpu().pin_memory()
-        self.h_vc = self.v_cur.cpu().pin_memory()
-        self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
-        self.h_err = torch.empty(1, dtype=torch.int32).pin_memory()
 
     def step(self, ev=None):
         sa, c = self.sa, self.c
@@ -185,17 +212,10 @@ class SparseDecode:
             ev[1].record()
 
     def h2d(self):
-        self.q.copy_(self.h_q, non_blocking=True)
-        self.idx.copy_(self.h_idx, non_blocking=True)
-        self.k_cur.copy_(self.h_kc, non_blocking=True)
-        self.v_cur.copy_(self.h_vc, non_blocking=True)
-        return sum(t.numel() * t.element_size() for t in (self.h_q, self.h_idx, self.h_kc,
-                                                           self.h_vc))
+        return self.s_in.h2d()  # Q, indices, current token's K and V
 
     def d2h(self):
-        self.h_y.copy_(self.y, non_blocking=True)
-        self.h_err.copy_(self.err, non_blocking=True)
-        return self.h_y.numel() * self.h_y.element_size() + 4
+        return self.s_out.d2h()  # Y and the error word
 
     def config(self):
         c = self.c
@@ -234,9 +254,11 @@ class PagedDecode:
         self.sa, self.c, self.dev = sa, c, dev
         inp = synth.make_paged_inputs(c, seed, device=dev)
         self.inp = inp
-        self.q = inp["q"]
+        self.s_in = Staging([inp["q"], inp["k_new"], inp["v_new"]], dev)
+        self.q, inp["k_new"], inp["v_new"] = self.s_in.views
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.y = torch.empty_like(self.q)
+        self.s_out = Staging([torch.empty_like(self.q)], dev)
+        self.y = self.s_out.views[0]
         nws = sa.paged_attn_decode_workspace(self.q, inp["k_pool"], inp["v_pool"],
                                              inp["block_table"], inp["ctx_len"],
                                              scale=c.eff_scale())
@@ -248,10 +270,6 @@ class PagedDecode:
         self.decode_bytes = (tokens * c.Hkv * c.D * es * 2 + inp["block_table"].numel() * 4
                              + 2 * self.q.numel() * es + 2 * inp["k_new"].numel() * es * 2)
         self.launches_per_step = 4  # append, gather, combine (+ nothing else)
-        self.h_q = self.q.cpu().pin_memory()
-        self.h_kn = inp["k_new"].cpu().pin_memory()
-        self.h_vn = inp["v_new"].cpu().pin_memory()
-        self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
 
     def step(self, ev=None):
         i = self.inp
@@ -265,14 +283,10 @@ class PagedDecode:
             ev[1].record()
 
     def h2d(self):
-        self.q.copy_(self.h_q, non_blocking=True)
-        self.inp["k_new"].copy_(self.h_kn, non_blocking=True)
-        self.inp["v_new"].copy_(self.h_vn, non_blocking=True)
-        return sum(t.numel() * t.element_size() for t in (self.h_q, self.h_kn, self.h_vn))
+        return self.s_in.h2d()  # Q and the new token's K and V
 
     def d2h(self):
-        self.h_y.copy_(self.y, non_blocking=True)
-        return self.h_y.numel() * self.h_y.element_size()
+        return self.s_out.d2h()  # Y
 
     def config(self):
         c = self.c
@@ -319,9 +333,11 @@ class Prefill:
     def __init__(self, sa, c: synth.PrefillCase, dev, seed=1004):
         self.sa, self.c, self.dev = sa, c, dev
         inp = synth.make_prefill_inputs(c, seed, device=dev)
-        self.q, self.k, self.v = inp["q"], inp["k"], inp["v"]
+        self.s_in = Staging([inp["q"], inp["k"], inp["v"]], dev)
+        self.q, self.k, self.v = self.s_in.views
         self.pk, self.pv = torch.empty_like(self.k), torch.empty_like(self.v)
-        self.y = torch.empty_like(self.q)
+        self.s_out = Staging([torch.empty_like(self.q)], dev)
+        self.y = self.s_out.views[0]
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         nws = sa.attn_prefill_workspace(self.q, self.k, self.v, True, c.eff_scale(), c.softcap)
         self.ws = sa.new_workspace(nws, dev)
@@ -330,8 +346,6 @@ class Prefill:
         pairs = S * (S + 1) // 2 if c.causal else S * S
         self.flops = 4.0 * c.D * pairs * c.B * c.Hq
         self.launches_per_step = 1  # one tensor-core kernel; present K/V written inside it
-        self.h = {n: getattr(self, n).cpu().pin_memory() for n in ("q", "k", "v")}
-        self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
 
     def step(self, ev=None):
         c = self.c
@@ -344,13 +358,10 @@ class Prefill:
             ev[1].record()
 
     def h2d(self):
-        for n in ("q", "k", "v"):
-            getattr(self, n).copy_(self.h[n], non_blocking=True)
-        return sum(t.numel() * t.element_size() for t in self.h.values())
+        return self.s_in.h2d()  # Q, K, V
 
     def d2h(self):
-        self.h_y.copy_(self.y, non_blocking=True)
-        return self.h_y.numel() * self.h_y.element_size()
+        return self.s_out.d2h()  # Y
 
     def config(self):
         c = self.c
@@ -390,10 +401,13 @@ class CsaFp8Decode:
     def __init__(self, sa, c: synth.SparseCase, dev, seed=1003):
         self.sa, self.c, self.dev = sa, c, dev
         inp = synth.make_sparse_inputs(c, seed, device=dev)
-        self.q, self.rec, self.idx = inp["q"], inp["kv_records"], inp["idx"]
+        self.rec = inp["kv_records"]
+        self.s_in = Staging([inp["q"], inp["idx"]], dev)
+        self.q, self.idx = self.s_in.views
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.status = torch.empty(c.B * c.I, dtype=torch.uint8, device=dev)
-        self.y = torch.empty_like(self.q)
+        self.s_out = Staging([torch.empty_like(self.q)], dev)
+        self.y = self.s_out.views[0]
         nws = sa.sparse_attn_decode_workspace(self.q, self.rec, None, self.idx,
                                               scale=c.eff_scale(), window=c.window,
                                               n_rope=c.n_rope, err_word=self.err,
@@ -408,9 +422,6 @@ class CsaFp8Decode:
         # plan, gather-decode, tcgen05 attention, combine (when the splits are not
         # merged on chip; 128-head blocks) -- else plan, warp-MMA kernel, combine
         self.launches_per_step = 4 if c.Hq % 128 == 0 else 3
-        self.h_q = self.q.cpu().pin_memory()
-        self.h_idx = self.idx.cpu().pin_memory()
-        self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
 
     def step(self, ev=None):
         c = self.c
@@ -423,13 +434,10 @@ class CsaFp8Decode:
             ev[1].record()
 
     def h2d(self):
-        self.q.copy_(self.h_q, non_blocking=True)
-        self.idx.copy_(self.h_idx, non_blocking=True)
-        return sum(t.numel() * t.element_size() for t in (self.h_q, self.h_idx))
+        return self.s_in.h2d()  # Q and the indices
 
     def d2h(self):
-        self.h_y.copy_(self.y, non_blocking=True)
-        return self.h_y.numel() * self.h_y.element_size()
+        return self.s_out.d2h()  # Y
 
     def config(self):
         c = self.c
