@@ -177,9 +177,12 @@ int build_present_kv(const void* past_k, const void* cur_k, void* present_k,
  * mode -- and attention sees them there.  A write position outside
  * [0, T - cur_len] sets SA_ERRBIT_WRITE_POS and skips that batch's write.
  * Workspace: sparse_attn_decode_workspace(p) bytes, 256-byte aligned; its
- * contents on entry do not matter (the call clears the counters it keeps
- * there with an asynchronous memset).  Calls that share a workspace must not
- * overlap on the GPU.
+ * contents on entry do not matter (every word is written before it is read).
+ * It holds the planned candidate positions and the key splits' partial
+ * results; for the FP8 cache with Hq a multiple of 128 also the decoded
+ * candidates (B * Sq * ceil((window + K) / 128) * 128 rows of D bf16 values,
+ * e.g. 40 MB for B 16, 2176 candidates, D 576).  Calls that share a workspace
+ * must not overlap on the GPU.
  */
 typedef struct {
   const void* q;
