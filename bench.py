@@ -53,6 +53,24 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of the ranks' values, returned on every rank (replicas: the
+    job takes as long as its slowest rank); x itself when not distributed."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    if torch.distributed.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank_step: float, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (weak scaling: every rank runs the same per-rank work)."""
+    return units_per_rank_step * world * steps / (total_ms * 1e-3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -606,13 +624,9 @@ def run_gpu(args):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     # the call alone: the step with a graph, else the events inside step()
     dec_ms = step_ms if graph is not None else [a.elapsed_time(b) for a, b in dec]
-    total_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / steps
-    value = wl.rows * ws * steps / (total_ms * 1e-3)
+    value = job_rate(wl.rows, ws, steps, total_ms)
 
     # end-to-end leg: host buffers, copies inside the timed region
     e2e_steps = max(3, min(steps, 200))
@@ -627,11 +641,7 @@ def run_gpu(args):
         d2h = wl.d2h()
         e_e[i].record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps, dev)
     # dominant-kernel leg: the library records events around its dominant
     # kernel (sa.kernel_events); same flush protocol, separate from the timed
     # steps because recording between kernels removes their launch overlap
@@ -668,7 +678,7 @@ def run_gpu(args):
                            launch="CUDA graph replay of one library call per step"
                            if graph is not None else "direct library call per step"),
             "roofline": wl.roofline(statistics.median(dec_ms), kernel_ms, peaks),
-            "e2e": {"value": round(wl.rows * ws / (e2e_ms * 1e-3), 1),
+            "e2e": {"value": round(job_rate(wl.rows, ws, 1, e2e_ms), 1),
                     "unit": "tokens/s" if isinstance(wl, Prefill) else "query-rows/s",
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "ms_per_step": round(e2e_ms, 5)},
