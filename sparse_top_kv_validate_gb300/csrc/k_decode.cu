@@ -366,15 +366,16 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float a,
 template <typename T>
 __global__ void __launch_bounds__(256) combine_flat_kernel(GatherArgs a) {
   pdl_wait();  // the partials of the kernel before (launched as its dependent)
-  const int64_t q4 = a.Dv / 4;
-  const int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (item >= a.units * a.hpu * q4) return;
-  const int64_t uh = item / q4, d = 4 * (item - uh * q4);
-  const int64_t unit = uh / a.hpu, hh = uh - unit * a.hpu;
+  // item counts stay below 2^31 on this path (checked on the host): 32-bit division
+  const uint32_t q4 = static_cast<uint32_t>(a.Dv / 4), hpu = static_cast<uint32_t>(a.hpu);
+  const uint32_t item = blockIdx.x * blockDim.x + threadIdx.x;
+  if (static_cast<int64_t>(item) >= a.units * a.hpu * q4) return;
+  const uint32_t uh = item / q4, d = 4 * (item - uh * q4);
+  const uint32_t unit = uh / hpu, hh = uh - unit * hpu;
   const UnitInfo u = unit_info(a, unit);
   const int64_t h = u.h0 + hh;
   const int splits = static_cast<int>(a.splits);
-  const int64_t row0 = unit * a.splits * a.hpu + hh;  // (unit, split 0, head)
+  const int64_t row0 = static_cast<int64_t>(unit) * a.splits * a.hpu + hh;  // (unit, split 0, head)
   float m[kFlatSplits], l[kFlatSplits];
   float4 o[kFlatSplits];
 #pragma unroll
@@ -416,9 +417,9 @@ __global__ void __launch_bounds__(256) combine_flat_kernel(GatherArgs a) {
 // before reading the partials.
 template <typename T>
 static int launch_combine_t(const GatherArgs& a, unsigned grid, cudaStream_t st) {
-  const bool flat = a.splits <= kFlatSplits && a.Dv % 4 == 0 &&
-                    reinterpret_cast<uintptr_t>(a.y) % (4 * sizeof(T)) == 0;  // vector stores
   const int64_t items = a.units * a.hpu * (a.Dv / 4);
+  const bool flat = a.splits <= kFlatSplits && a.Dv % 4 == 0 && items < (int64_t(1) << 31) &&
+                    reinterpret_cast<uintptr_t>(a.y) % (4 * sizeof(T)) == 0;  // vector stores
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(flat ? static_cast<unsigned>((items + 255) / 256) : grid);
   cfg.blockDim = dim3(flat ? 256 : 128);

@@ -213,6 +213,7 @@ namespace {
 // ---- kernel 1: gather + exact decode of the planned candidates' records ------------------
 
 constexpr int kDecRecs = 8;  // records per warp, all in flight together
+static_assert(128 % kDecRecs == 0, "a warp's rows must lie in one unit");
 
 __device__ __forceinline__ void cp_async8(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -270,15 +271,17 @@ __global__ void __launch_bounds__(256) fp8_gather_decode_kernel(const DecodePara
   if (row0 >= p.rows) return;
   uint2* st = stage + warp * kDecRecs * 82;
   const int32_t mine = (lane < kDecRecs && row0 + lane < p.rows) ? __ldg(p.pos + row0 + lane) : -1;
+  // The warp's rows share one unit (kDecRecs divides n_cand_pad, a multiple
+  // of 128, and row0 is a multiple of kDecRecs): one division per warp.
+  const char* batch_recs = p.recs + ((row0 / p.n_cand_pad) / p.Sq) * p.T * p.record_stride;
   // two commit groups of kDecRecs / 2 records: the first half is decoded
   // while the second half's copies are still landing
 #pragma unroll
   for (int r = 0; r < kDecRecs; ++r) {
     const int32_t pr = __shfl_sync(0xffffffffu, mine, r);
     if (pr >= 0) {
-      const int64_t b = ((row0 + r) / p.n_cand_pad) / p.Sq;
       const uint2* rec = reinterpret_cast<const uint2*>(
-          p.recs + (b * p.T + pr) * p.record_stride);  // 8-byte aligned
+          batch_recs + static_cast<int64_t>(pr) * p.record_stride);  // 8-byte aligned
 #pragma unroll
       for (int k = 0; k < 3; ++k)
         if (lane + 32 * k < 81) cp_async8(st + r * 82 + lane + 32 * k, rec + lane + 32 * k);

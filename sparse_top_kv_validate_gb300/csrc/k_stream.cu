@@ -165,10 +165,13 @@ __device__ __forceinline__ KeyRef key_load(const GatherArgs& a, const Cursor& cu
     k.base = cu.rowbase;
     k.raw = (c < cu.nc && !(a.causal && c > a.past_len + cu.ui.i)) ? static_cast<int32_t>(c) : -1;
   } else {
-    k.base = cu.ui.kvh * a.page_tokens + c % a.page_tokens;
+    // c < max_pages * page_tokens < 2^31 (checked on the host): 32-bit division
+    const uint32_t c32 = static_cast<uint32_t>(c), pt = static_cast<uint32_t>(a.page_tokens);
+    const uint32_t pi = c32 / pt;
+    k.base = cu.ui.kvh * a.page_tokens + (c32 - pi * pt);
     k.raw = -1;
     if (c < cu.nc) {
-      const int32_t pg = __ldg(a.block_table + cu.ui.b * a.max_pages + c / a.page_tokens);
+      const int32_t pg = __ldg(a.block_table + cu.ui.b * a.max_pages + pi);
       k.raw = pg < 0 ? -2 : pg;  // -2: a bad table entry
     }
   }

@@ -96,7 +96,8 @@ int plan_gather(Plan& pl, int dtype) {
   }
   g.units = g.B * g.n_groups * g.Sq;
   pl.stream = sa::gather_uses_mma(g, dtype) &&
-              (g.source != sa::kPaged || g.B <= sa::stream_max_batch_paged());
+              (g.source != sa::kPaged || (g.B <= sa::stream_max_batch_paged() &&
+                                          g.max_pages * g.page_tokens < (int64_t(1) << 31)));
   const int64_t irows = g.B * g.I * g.Sq;
   if (pl.stream) {
     pl.grid = stream_grid();
