@@ -10,9 +10,9 @@
 // with K and V both the decoded 576-dim record.
 //
 // GB300 design: two kernels.
-//  1. fp8_gather_decode_kernel: one warp per planned candidate reads the
-//     record with coalesced 8-byte loads (three per warp), stages it in
-//     shared memory and writes the exact bf16 decode (e4m3 x 2^(scale-127);
+//  1. fp8_gather_decode_kernel: each warp takes eight planned candidates,
+//     fetches each record as one bulk copy (its 16-byte-aligned 656-byte
+//     window) into shared memory and writes the exact bf16 decode (e4m3 x 2^(scale-127);
 //     the RoPE tail copied) as row [unit, candidate] of a [units, n_cand_pad,
 //     576] bf16 buffer; masked candidates are zero rows.  Each record is
 //     decoded once, and the buffer (40 MB for 16 queries of 2176 keys) stays
@@ -125,6 +125,7 @@ struct DecodeParams {
   int64_t n_cand_pad;
   int Sq;
   __nv_bfloat16* kdec;       // [units, n_cand_pad, 576]
+  uint32_t* err_word;        // nullable: SA_ERRBIT_TIMEOUT if a copy never lands
 };
 
 // The ring's entries, in order: the nine score chunks of tile 0, then for
@@ -214,18 +215,21 @@ namespace {
 
 constexpr int kDecRecs = 8;  // records per warp, all in flight together
 static_assert(128 % kDecRecs == 0, "a warp's rows must lie in one unit");
-
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
+// A record is fetched as the 16-byte-aligned window around it: records are
+// 8-byte aligned (checked on the host), so the window starts 0 or 8 bytes
+// before the record and is 656 bytes long; it never leaves the 16-byte
+// granules that hold the record.
+constexpr int kDecSlot = 656;
+constexpr size_t kDecSmem = 8 * kDecRecs * kDecSlot + 8 * 2 * sizeof(uint64_t);
 
 // Eight decoded bf16 values (16 bytes) of FP8 block c, codes [8g, 8g + 8):
-// record bytes 65c + 1 + 8g .. (read as aligned words of the staged record),
-// scaled by the block's E8M0 byte 65c.
-__device__ __forceinline__ uint4 decode8(const uint32_t* sw, const unsigned char* sb, int c, int g) {
-  const float sc = e8m0_scale(sb[65 * c]);
+// record bytes 65c + 1 + 8g .. (read as aligned words of the staged window,
+// the record starting `off` bytes into it), scaled by the block's E8M0 byte.
+__device__ __forceinline__ uint4 decode8(const uint32_t* sw, const unsigned char* sb, int off,
+                                         int c, int g) {
+  const float sc = e8m0_scale(sb[off + 65 * c]);
   const uint64_t sc2 = f2_pack(sc, sc);
-  const int first = 65 * c + 1 + 8 * g;
+  const int first = off + 65 * c + 1 + 8 * g;
   const int w0 = first >> 2, sh = (first & 3) * 8;
   const uint32_t a = sw[w0], b = sw[w0 + 1], d = sw[w0 + 2];
   const uint32_t lo = sh ? __funnelshift_r(a, b, sh) : a;
@@ -244,67 +248,84 @@ __device__ __forceinline__ uint4 decode8(const uint32_t* sw, const unsigned char
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// One decoded row (72 x 16 bytes) from a staged 648-byte record: lane l writes
-// 16-byte chunks l and l + 32 (FP8 blocks l / 8 and 4 + l / 8, codes
-// [8 (l % 8), 8 (l % 8) + 8)), so that every warp store is 512 contiguous
-// bytes; lanes 0-7 copy the RoPE tail (record bytes 520 ..) to chunks 64-71.
-__device__ __forceinline__ void decode_row(const uint2* st, uint4* out, int lane) {
-  const unsigned char* sb = reinterpret_cast<const unsigned char*>(st);
-  const uint32_t* sw = reinterpret_cast<const uint32_t*>(st);
-  out[lane] = decode8(sw, sb, lane >> 3, lane & 7);
-  out[32 + lane] = decode8(sw, sb, 4 + (lane >> 3), lane & 7);
+// One decoded row (72 x 16 bytes) from a staged record window, or zeros when
+// the candidate is masked: lane l writes 16-byte chunks l and l + 32 (FP8
+// blocks l / 8 and 4 + l / 8, codes [8 (l % 8), 8 (l % 8) + 8)), so that every
+// warp store is 512 contiguous bytes; lanes 0-7 copy the RoPE tail (record
+// bytes 520 ..) to chunks 64-71.
+__device__ __forceinline__ void decode_row(const unsigned char* slot, int off, uint4* out, int lane,
+                                           bool valid) {
+  const uint32_t* sw = reinterpret_cast<const uint32_t*>(slot);
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  const uint4 lo = decode8(sw, slot, off, lane >> 3, lane & 7);
+  const uint4 hi = decode8(sw, slot, off, 4 + (lane >> 3), lane & 7);
+  out[lane] = valid ? lo : z;
+  out[32 + lane] = valid ? hi : z;
   if (lane < 8) {
-    const uint2 lo = st[kRecRope / 8 + 2 * lane], hi = st[kRecRope / 8 + 2 * lane + 1];
-    out[64 + lane] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    const uint2* rope = reinterpret_cast<const uint2*>(slot + off + kRecRope);  // 8-byte aligned
+    const uint2 r0 = rope[2 * lane], r1 = rope[2 * lane + 1];
+    out[64 + lane] = valid ? make_uint4(r0.x, r0.y, r1.x, r1.y) : z;
   }
 }
 
 // Each warp decodes kDecRecs consecutive rows [unit, candidate] of the buffer
-// (8 warps per CTA): the rows' positions, then all their records copied
-// (8 bytes per lane per copy) straight into shared memory, then the decodes.
-__global__ void __launch_bounds__(256) fp8_gather_decode_kernel(const DecodeParams p) {
-  extern __shared__ __align__(16) uint2 stage[];  // [8 warps][kDecRecs][82] 648-byte records
+// (8 warps per CTA): the rows' positions, then one bulk copy per record
+// window into shared memory (lanes 0-7; the two halves complete on their own
+// mbarriers), then the decodes, the four rows of a half interleaved.  A
+// masked candidate is not fetched; its row is written as zeros.
+__global__ void __launch_bounds__(256, 4) fp8_gather_decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(16) unsigned char stage[];  // [8 warps][kDecRecs][kDecSlot], barriers
   const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
-  pdl_wait();                // the planned positions
-  pdl_launch_dependents();   // the attention kernel may start its set-up
+  // rows = units * n_cand_pad is a multiple of kDecRecs: a warp's rows are all in range
   const int64_t row0 = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * kDecRecs;
   if (row0 >= p.rows) return;
-  uint2* st = stage + warp * kDecRecs * 82;
-  const int32_t mine = (lane < kDecRecs && row0 + lane < p.rows) ? __ldg(p.pos + row0 + lane) : -1;
+  unsigned char* st = stage + warp * kDecRecs * kDecSlot;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + 8 * kDecRecs * kDecSlot) + 2 * warp;
+  if (lane == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+  }
+  fence_proxy_async_smem();
+  fence_mbar_init();
+  __syncwarp();
+  pdl_wait();                // the planned positions
+  pdl_launch_dependents();   // the attention kernel may start its set-up
+  const int32_t mine = (lane < kDecRecs) ? __ldg(p.pos + row0 + lane) : -1;
   // The warp's rows share one unit (kDecRecs divides n_cand_pad, a multiple
   // of 128, and row0 is a multiple of kDecRecs): one division per warp.
   const char* batch_recs = p.recs + ((row0 / p.n_cand_pad) / p.Sq) * p.T * p.record_stride;
-  // two commit groups of kDecRecs / 2 records: the first half is decoded
-  // while the second half's copies are still landing
-#pragma unroll
-  for (int r = 0; r < kDecRecs; ++r) {
-    const int32_t pr = __shfl_sync(0xffffffffu, mine, r);
-    if (pr >= 0) {
-      const uint2* rec = reinterpret_cast<const uint2*>(
-          batch_recs + static_cast<int64_t>(pr) * p.record_stride);  // 8-byte aligned
-#pragma unroll
-      for (int k = 0; k < 3; ++k)
-        if (lane + 32 * k < 81) cp_async8(st + r * 82 + lane + 32 * k, rec + lane + 32 * k);
-    }
-    if (r == kDecRecs / 2 - 1 || r == kDecRecs - 1)
-      asm volatile("cp.async.commit_group;" ::: "memory");
+  const char* rec = batch_recs + static_cast<int64_t>(mine >= 0 ? mine : 0) * p.record_stride;
+  const int off = static_cast<int>(reinterpret_cast<uintptr_t>(rec) & 15u);
+  // bytes expected per half: lanes 0-3 hold half 0's records, lanes 4-7 half 1's
+  uint32_t tot = (mine >= 0) ? static_cast<uint32_t>(kDecSlot) : 0u;
+  tot += __shfl_xor_sync(0xffffffffu, tot, 1);
+  tot += __shfl_xor_sync(0xffffffffu, tot, 2);
+  const uint32_t tot1 = __shfl_sync(0xffffffffu, tot, 4);
+  if (lane == 0) {
+    mbar_arrive_expect_tx(&bars[0], tot);
+    mbar_arrive_expect_tx(&bars[1], tot1);
   }
+  __syncwarp();
+  if (mine >= 0) bulk_g2s(st + lane * kDecSlot, rec - off, kDecSlot, &bars[lane >> 2]);
+  uint4* out0 = reinterpret_cast<uint4*>(p.kdec + row0 * kD);  // rows of 72 x 16 bytes
+  bool landed[2] = {true, true};
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    if (half == 0) asm volatile("cp.async.wait_group 1;" ::: "memory");
-    else asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncwarp();
-#pragma unroll 1
-    for (int r = half * (kDecRecs / 2); r < (half + 1) * (kDecRecs / 2); ++r) {
-      const int64_t row = row0 + r;
-      if (row >= p.rows) break;
-      uint4* out = reinterpret_cast<uint4*>(p.kdec + row * kD);  // 72 x 16 bytes
-      if (__shfl_sync(0xffffffffu, mine, r) < 0) {
-        for (int i = lane; i < kRowBytes / 16; i += 32) out[i] = make_uint4(0u, 0u, 0u, 0u);
-      } else {
-        decode_row(st + r * 82, out, lane);
-      }
+    landed[half] = mbar_wait(&bars[half], 0u);
+#pragma unroll
+    for (int rr = 0; rr < kDecRecs / 2; ++rr) {
+      const int r = half * (kDecRecs / 2) + rr;
+      const bool valid = __shfl_sync(0xffffffffu, mine, r) >= 0;
+      const int ro = __shfl_sync(0xffffffffu, off, r);
+      decode_row(st + r * kDecSlot, ro, out0 + r * (kRowBytes / 16), lane, valid);
     }
+  }
+  if (!landed[0] || !landed[1]) {
+    // a copy that never landed: report it, and give the copies still in
+    // flight one more bounded wait before the warp's shared memory is released
+    if (lane == 0 && p.err_word) atomicOr(p.err_word, SA_ERRBIT_TIMEOUT);
+    if (!landed[0]) mbar_wait(&bars[0], 0u);
+    if (!landed[1]) mbar_wait(&bars[1], 0u);
   }
 }
 
@@ -901,8 +922,9 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   d.n_cand_pad = g.n_cand_pad;
   d.Sq = static_cast<int>(g.Sq);
   d.kdec = static_cast<__nv_bfloat16*>(g.fp8_kdec);
+  d.err_word = g.err_word;
   const int64_t per_cta = 8 * kDecRecs;
-  const size_t dsmem = 8 * kDecRecs * 82 * sizeof(uint2);
+  const size_t dsmem = kDecSmem;
   if (cudaFuncSetAttribute(fp8_gather_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(dsmem)) != cudaSuccess ||
       launch_pdl(fp8_gather_decode_kernel, static_cast<unsigned>((rows + per_cta - 1) / per_cta), 256,
