@@ -499,14 +499,14 @@ class CsaFp8Decode:
 # kernel exists.
 TRAFFIC: dict = {
     # gather_stream_kernel (TMA gather4), one launch, ncu dram read + write
-    "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 271466338,
+    "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 271420645,
     # fp8_tc05_kernel, one launch, ncu dram read + write (ncu flushes caches between
     # kernels, so the 40 MB of decoded rows count from DRAM; live they come from L2)
     "csa_fp8_b16_h128_d576_t65536_k2048_w128": 42660960,
     # gather_stream_kernel (paged, TMA boxes), one launch: the 16-sequence capture
-    # (1,160.1 MB read + write over 282,062 context tokens) scaled by the context
+    # (1,156.8 MB read + write over 282,062 context tokens) scaled by the context
     # tokens of the full workload (2,171,044); the traffic grows with them
-    "paged_fp16_b128_h32_kv8_d128_ctx1k-32k_p16": 8929659221,
+    "paged_fp16_b128_h32_kv8_d128_ctx1k-32k_p16": 8903872744,
     # prefill_tc05_kernel, one launch (Q, K, V read; Y and present K/V written)
     "prefill_bf16_b4_s4096_h32_kv8_d128_causal_softcap50": 441644032,
 }
