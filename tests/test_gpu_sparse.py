@@ -420,6 +420,29 @@ def test_fp8_tc05_head_blocks_match_oracle(cuda_lib, over):
     assert_close(to64(y), ref, y.dtype, f"fp8 tc05 {over}")
 
 
+@pytest.mark.parametrize("stride,shift", [(664, 0), (648, 8), (656, 8), (704, 8)])
+def test_fp8_tc05_record_windows_match_oracle(cuda_lib, stride, shift):
+    # Records are 8-byte aligned; the decoder fetches each as the 16-byte-aligned
+    # window around it, which starts 0 or 8 bytes before the record.  Strides and
+    # a cache base 8 bytes past a 16-byte boundary cover both starts.
+    c = _fp8_case(Hq=128, record_stride=stride)
+    inp = synth.make_sparse_inputs(c, seed=95)
+    rec = inp["kv_records"]
+    buf = torch.zeros(rec.numel() + 16, dtype=torch.uint8, device=DEV)
+    dev_rec = buf[shift:shift + rec.numel()].view(rec.shape)
+    dev_rec.copy_(rec.to(DEV))
+    assert dev_rec.data_ptr() % 16 == shift
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = cuda_lib.sparse_attn_decode(inp["q"].to(DEV), dev_rec, None, inp["idx"].to(DEV),
+                                    scale=c.eff_scale(), window=c.window, n_rope=c.n_rope,
+                                    err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.sparse_attention(inp["q"], inp["idx"], records=rec, n_rope=c.n_rope,
+                                  scale=c.eff_scale(), window=c.window)
+    assert_close(to64(y), ref, y.dtype, f"fp8 tc05 stride {stride} shift {shift}")
+
+
 @pytest.mark.parametrize("over", [dict(B=16, T=3000, K=1000),   # 3 splits of 3 tiles
                                   dict(B=52, T=900, K=400)])    # 1 split of 5 tiles
 def test_fp8_tc05_several_tiles_per_cta(cuda_lib, over):
