@@ -277,4 +277,41 @@ __device__ __forceinline__ int64_t load_index(const void* idx, int64_t off, int 
                 : static_cast<int64_t>(static_cast<const int32_t*>(idx)[off]);
 }
 
+// ---- candidate positions of an index row ------------------------------------------
+// Row (b, ih, i) attends to the `window` most recent cache positions
+// [len - window, len) first, then to its selected indices.  A candidate is
+// masked (-1) past the causal limit (past_len + i), outside [0, len) with len
+// the batch's valid length (kv_len, clipped to the cache), or, for a selected
+// index, inside the window (each key counts once).
+struct CandRule {
+  int64_t len, wstart, causal_lim, window;
+};
+
+__device__ __forceinline__ CandRule cand_rule(const int64_t* kv_len, int64_t b, int64_t T,
+                                              int64_t window, int causal, int64_t past_len,
+                                              int64_t i) {
+  CandRule r;
+  int64_t len = kv_len ? __ldg(kv_len + b) : T;
+  if (len > T) len = T;
+  if (len < 0) len = 0;
+  r.len = len;
+  r.window = window;
+  r.wstart = len - window;
+  r.causal_lim = causal ? past_len + i : INT64_MAX;
+  return r;
+}
+
+// Window candidate c (< window).
+__device__ __forceinline__ int32_t window_pos(const CandRule& r, int64_t c) {
+  const int64_t t = r.wstart + c;
+  return (t >= 0 && t <= r.causal_lim) ? static_cast<int32_t>(t) : -1;
+}
+
+// Selected index t.
+__device__ __forceinline__ int32_t selected_pos(const CandRule& r, int64_t t) {
+  bool keep = t >= 0 && t < r.len && t <= r.causal_lim;
+  if (r.window > 0 && t >= r.wstart) keep = false;
+  return keep ? static_cast<int32_t>(t) : -1;
+}
+
 }  // namespace sa

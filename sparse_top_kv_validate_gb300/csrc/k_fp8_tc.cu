@@ -126,6 +126,17 @@ struct DecodeParams {
   int Sq;
   __nv_bfloat16* kdec;       // [units, n_cand_pad, 576]
   uint32_t* err_word;        // nullable: SA_ERRBIT_TIMEOUT if a copy never lands
+  // own_positions: the kernel plans its candidates from the index rows (one
+  // latent head, one index head: unit u = b * Sq + i is index row u) and writes
+  // them to pos for the attention kernel; else it reads the planned pos.
+  int own_positions;
+  int after_plan;            // a validation-only plan kernel runs just before this one
+  int32_t* pos_out;
+  const void* idx;           // [B, 1, Sq, K]
+  int idx_is_i64;
+  int causal;
+  int64_t K, window, past_len;
+  const int64_t* kv_len;     // nullable
 };
 
 // The ring's entries, in order: the nine score chunks of tile 0, then for
@@ -278,7 +289,14 @@ __global__ void __launch_bounds__(256, 4) fp8_gather_decode_kernel(const DecodeP
   const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
   // rows = units * n_cand_pad is a multiple of kDecRecs: a warp's rows are all in range
   const int64_t row0 = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * kDecRecs;
-  if (row0 >= p.rows) return;
+  // With own positions after the plan kernel, nothing here reads what that
+  // kernel writes (the validation); the wait moves to the end, so that this
+  // grid completes only after it (the attention kernel waits on this grid).
+  const bool wait_late = p.own_positions && p.after_plan;
+  if (row0 >= p.rows) {
+    if (wait_late) pdl_wait();
+    return;
+  }
   unsigned char* st = stage + warp * kDecRecs * kDecSlot;
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage + 8 * kDecRecs * kDecSlot) + 2 * warp;
   if (lane == 0) {
@@ -288,12 +306,27 @@ __global__ void __launch_bounds__(256, 4) fp8_gather_decode_kernel(const DecodeP
   fence_proxy_async_smem();
   fence_mbar_init();
   __syncwarp();
-  pdl_wait();                // the planned positions
-  pdl_launch_dependents();   // the attention kernel may start its set-up
-  const int32_t mine = (lane < kDecRecs) ? __ldg(p.pos + row0 + lane) : -1;
+  if (!wait_late) pdl_wait();  // the planned positions, or the work before the call
+  pdl_launch_dependents();       // the attention kernel may start its set-up
   // The warp's rows share one unit (kDecRecs divides n_cand_pad, a multiple
   // of 128, and row0 is a multiple of kDecRecs): one division per warp.
-  const char* batch_recs = p.recs + ((row0 / p.n_cand_pad) / p.Sq) * p.T * p.record_stride;
+  const int64_t unit = row0 / p.n_cand_pad;
+  const int64_t b = unit / p.Sq;
+  int32_t mine = -1;
+  if (p.own_positions) {
+    if (lane < kDecRecs) {
+      const int64_t c = row0 - unit * p.n_cand_pad + lane;
+      const CandRule rule =
+          cand_rule(p.kv_len, b, p.T, p.window, p.causal, p.past_len, unit - b * p.Sq);
+      if (c < p.window) mine = window_pos(rule, c);
+      else if (c < p.window + p.K)
+        mine = selected_pos(rule, load_index(p.idx, unit * p.K + (c - p.window), p.idx_is_i64));
+      p.pos_out[row0 + lane] = mine;
+    }
+  } else if (lane < kDecRecs) {
+    mine = __ldg(p.pos + row0 + lane);
+  }
+  const char* batch_recs = p.recs + b * p.T * p.record_stride;
   const char* rec = batch_recs + static_cast<int64_t>(mine >= 0 ? mine : 0) * p.record_stride;
   const int off = static_cast<int>(reinterpret_cast<uintptr_t>(rec) & 15u);
   // bytes expected per half: lanes 0-3 hold half 0's records, lanes 4-7 half 1's
@@ -327,6 +360,7 @@ __global__ void __launch_bounds__(256, 4) fp8_gather_decode_kernel(const DecodeP
     if (!landed[0]) mbar_wait(&bars[0], 0u);
     if (!landed[1]) mbar_wait(&bars[1], 0u);
   }
+  if (wait_late) pdl_wait();
 }
 
 }  // namespace
@@ -923,6 +957,17 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   d.Sq = static_cast<int>(g.Sq);
   d.kdec = static_cast<__nv_bfloat16*>(g.fp8_kdec);
   d.err_word = g.err_word;
+  d.own_positions = g.fp8_own_positions;
+  d.after_plan = g.fp8_after_plan;
+  d.pos_out = const_cast<int32_t*>(g.pos);
+  d.idx = g.idx;
+  d.idx_is_i64 = g.idx_is_i64;
+  d.causal = g.causal;
+  d.K = g.K;
+  d.window = g.window;
+  d.past_len = g.past_len;
+  d.kv_len = g.kv_len;
+  if (g.fp8_own_positions && (g.I != 1 || g.Hkv != 1 || (g.K > 0 && !g.idx))) return -1;
   const int64_t per_cta = 8 * kDecRecs;
   const size_t dsmem = kDecSmem;
   if (cudaFuncSetAttribute(fp8_gather_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

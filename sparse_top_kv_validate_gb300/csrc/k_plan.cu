@@ -65,21 +65,17 @@ __global__ void __launch_bounds__(256) plan_rows_kernel(PlanArgs a) {
   const int64_t irow = blockIdx.x;
   const int64_t i = irow % a.Sq;
   const int64_t b = irow / (a.I * a.Sq);
-  int64_t len = a.kv_len ? a.kv_len[b] : a.T;
-  if (len > a.T) len = a.T;
-  if (len < 0) len = 0;
-  const int64_t wstart = len - a.window;
-  const int64_t causal_lim = a.causal ? a.past_len + i : INT64_MAX;
+  const CandRule rule = cand_rule(a.kv_len, b, a.T, a.window, a.causal, a.past_len, i);
+  const int64_t len = rule.len;
   int32_t* pos = a.pos + irow * a.n_cand_pad;
   const int64_t ncand = a.window + a.K;
 
-  // window candidates
-  for (int64_t c = threadIdx.x; c < a.window; c += blockDim.x) {
-    const int64_t t = wstart + c;
-    pos[c] = (t >= 0 && t <= causal_lim) ? static_cast<int32_t>(t) : -1;
+  if (a.write_positions) {
+    // window candidates
+    for (int64_t c = threadIdx.x; c < a.window; c += blockDim.x) pos[c] = window_pos(rule, c);
+    // padding of the last tile
+    for (int64_t c = ncand + threadIdx.x; c < a.n_cand_pad; c += blockDim.x) pos[c] = -1;
   }
-  // padding of the last tile
-  for (int64_t c = ncand + threadIdx.x; c < a.n_cand_pad; c += blockDim.x) pos[c] = -1;
 
   // selected columns: 8 consecutive per thread per step, every load of the
   // step issued before any is used
@@ -125,10 +121,9 @@ __global__ void __launch_bounds__(256) plan_rows_kernel(PlanArgs a) {
           best = best > key ? best : key;
         }
       }
-      bool keep = t >= 0 && t < len && t <= causal_lim;
-      if (a.window > 0 && t >= wstart) keep = false;  // already a window candidate
-      out[e] = keep ? static_cast<int32_t>(t) : -1;
+      out[e] = selected_pos(rule, t);
     }
+    if (!a.write_positions) continue;
     int32_t* dst = pos + a.window + c0;
     if (c0 + 8 <= a.K && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
       reinterpret_cast<int4*>(dst)[0] = make_int4(out[0], out[1], out[2], out[3]);

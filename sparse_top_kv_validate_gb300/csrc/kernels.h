@@ -43,6 +43,7 @@ struct PlanArgs {
   int idx_is_i64;
   int vec_ok;                 // 16-byte vector loads are legal
   int plan_rows;              // 0: append blocks only
+  int write_positions;        // write pos (0: the consumer plans its own positions)
   int validate;               // write row_status / err_word
   int causal;
   int64_t B, I, Sq, K, T, window, past_len;
@@ -112,6 +113,8 @@ struct GatherArgs {
   // FP8 hybrid records (sparse source)
   int64_t record_stride;      // bytes between records
   void* fp8_kdec;             // tcgen05 FP8 path: decoded rows [units, n_cand_pad, 576] bf16
+  int fp8_own_positions;      // tcgen05 FP8 path: the decode kernel writes pos itself
+  int fp8_after_plan;         //   and the plan kernel (validation only) runs just before it
   void* ev_before;            // nullable cudaEvent_t pair recorded around the dominant kernel
   void* ev_after;
   // math

@@ -506,6 +506,15 @@ int sparse_attn_decode(const sa_sparse_params* p, void* stream) {
   const size_t iesz = p->idx_is_i64 ? 8 : 4;
   pa.vec_ok = p->idx && aligned16(p->idx) && ((p->K * static_cast<int64_t>(iesz)) % 16 == 0);
   pa.plan_rows = (pl.stream || pl.fp8) ? 1 : 0;
+  pa.write_positions = 1;
+  if (pl.fp8_tc) {
+    // the FP8 decode kernel plans its own positions: the plan kernel only
+    // validates, beside it, when a status output is asked for
+    pa.write_positions = 0;
+    pa.plan_rows = (p->K > 0 && (p->err_word || p->row_status)) ? 1 : 0;
+    pl.g.fp8_own_positions = 1;
+    pl.g.fp8_after_plan = pa.plan_rows;
+  }
   pa.validate = pa.plan_rows && p->K > 0 && (p->err_word || p->row_status);
   pa.causal = p->causal;
   pa.B = p->B;

@@ -420,6 +420,40 @@ def test_fp8_tc05_head_blocks_match_oracle(cuda_lib, over):
     assert_close(to64(y), ref, y.dtype, f"fp8 tc05 {over}")
 
 
+def test_fp8_tc05_malformed_rows_status_and_outputs(cuda_lib):
+    # The tcgen05 FP8 path plans its candidates inside the decode kernel while
+    # the plan kernel only validates beside it: statuses must equal the
+    # oracle's, valid rows must match the oracle (a malformed row's output is
+    # only required to be finite), and the output must not depend on whether
+    # a status output was asked for.
+    c = _fp8_case(B=5, Hq=128, T=2000, K=300, pad_prob=0.0)
+    inp = synth.make_sparse_inputs(c, seed=96)
+    idx = inp["idx"].clone()
+    idx[0, 0, 0, 7] = 5_000                 # out of range
+    idx[1, 0, 0, 10] = idx[1, 0, 0, 9]      # duplicate
+    idx[2, 0, 0, 20:] = -1                  # valid trailing padding
+    idx[2, 0, 0, 25] = 3                    # after padding
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    st = torch.full((c.B,), 255, dtype=torch.uint8, device=DEV)
+    dev = dict(q=inp["q"].to(DEV), rec=inp["kv_records"].to(DEV), idx=idx.to(DEV))
+    y = cuda_lib.sparse_attn_decode(dev["q"], dev["rec"], None, dev["idx"], scale=c.eff_scale(),
+                                    window=c.window, n_rope=c.n_rope, err_word=err, row_status=st)
+    y_plain = cuda_lib.sparse_attn_decode(dev["q"], dev["rec"], None, dev["idx"],
+                                          scale=c.eff_scale(), window=c.window, n_rope=c.n_rope)
+    torch.cuda.synchronize()
+    status, e = oracle.validate_indices(idx, bound=c.T)
+    assert st.cpu().tolist() == status.tolist()
+    assert int(err.item()) == e and e != 0
+    assert torch.equal(y, y_plain)
+    assert torch.isfinite(y.float()).all()
+    ok = [b for b in range(c.B) if status[b] == 0]
+    assert ok == [3, 4]
+    rows = [b * c.Hq + h for b in ok for h in range(c.Hq)]
+    ref = oracle.sparse_attention(inp["q"], idx, records=inp["kv_records"], n_rope=c.n_rope,
+                                  scale=c.eff_scale(), window=c.window, rows=rows)
+    assert_close(to64(y.reshape(-1, c.D)[rows]), ref, y.dtype, "fp8 tc05 valid rows")
+
+
 @pytest.mark.parametrize("stride,shift", [(664, 0), (648, 8), (656, 8), (704, 8)])
 def test_fp8_tc05_record_windows_match_oracle(cuda_lib, stride, shift):
     # Records are 8-byte aligned; the decoder fetches each as the 16-byte-aligned
