@@ -287,7 +287,7 @@ class PagedDecode:
         self.tokens = tokens
         self.decode_bytes = (tokens * c.Hkv * c.D * es * 2 + inp["block_table"].numel() * 4
                              + 2 * self.q.numel() * es + 2 * inp["k_new"].numel() * es * 2)
-        self.launches_per_step = 4  # append, gather, combine (+ nothing else)
+        self.launches_per_step = 3  # paged append, gather, combine
 
     def step(self, ev=None):
         i = self.inp
@@ -437,8 +437,9 @@ class CsaFp8Decode:
         self.decode_bytes = (self.keys * c.record_stride + self.idx.numel() * 4
                              + 2 * self.q.numel() * 2)
         self.flops = 4.0 * c.Hq * c.D * self.keys
-        # plan, gather-decode, tcgen05 attention, combine (when the splits are not
-        # merged on chip; 128-head blocks) -- else plan, warp-MMA kernel, combine
+        # plan (validation only), gather-decode (positions, records), tcgen05
+        # attention, combine (when the splits are not merged on chip; 128-head
+        # blocks) -- else plan, warp-MMA kernel, combine
         self.launches_per_step = 4 if c.Hq % 128 == 0 else 3
 
     def step(self, ev=None):
