@@ -454,6 +454,25 @@ def test_fp8_tc05_malformed_rows_status_and_outputs(cuda_lib):
     assert_close(to64(y.reshape(-1, c.D)[rows]), ref, y.dtype, "fp8 tc05 valid rows")
 
 
+@pytest.mark.parametrize("kv_len", [None, [700, 300, 90]])
+def test_fp8_tc05_window_only_matches_oracle(cuda_lib, kv_len):
+    # No index rows (K = 0): the candidates are the window alone, and no plan
+    # kernel runs before the decode.
+    c = _fp8_case(B=3, Hq=128, T=700, K=8, window=128, pad_prob=0.0)
+    inp = synth.make_sparse_inputs(c, seed=97)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kl = None if kv_len is None else torch.tensor(kv_len, dtype=torch.int64)
+    y = cuda_lib.sparse_attn_decode(inp["q"].to(DEV), inp["kv_records"].to(DEV), None, None,
+                                    scale=c.eff_scale(), window=c.window, n_rope=c.n_rope,
+                                    err_word=err, kv_len=None if kl is None else kl.to(DEV))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    idx0 = torch.empty((c.B, 1, 1, 0), dtype=torch.int32)
+    ref = oracle.sparse_attention(inp["q"], idx0, records=inp["kv_records"], n_rope=c.n_rope,
+                                  scale=c.eff_scale(), window=c.window, kv_len=kl)
+    assert_close(to64(y), ref, y.dtype, f"fp8 tc05 window only kv_len={kv_len}")
+
+
 @pytest.mark.parametrize("stride,shift", [(664, 0), (648, 8), (656, 8), (704, 8)])
 def test_fp8_tc05_record_windows_match_oracle(cuda_lib, stride, shift):
     # Records are 8-byte aligned; the decoder fetches each as the 16-byte-aligned
