@@ -168,11 +168,6 @@ __device__ __forceinline__ void entry_of(int e, int nt, int part, int& j, int& c
   }
 }
 
-// Barrier `id` over the first `threads` threads that reach it (a warpgroup).
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // ---- thread-block cluster helpers ----
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -226,6 +221,8 @@ namespace {
 
 constexpr int kDecRecs = 8;  // records per warp, all in flight together
 static_assert(128 % kDecRecs == 0, "a warp's rows must lie in one unit");
+static_assert(kDecRecs >= 2 && kDecRecs <= 32 && (kDecRecs & (kDecRecs - 1)) == 0,
+              "two halves of lanes, a power of two");
 // A record is fetched as the 16-byte-aligned window around it: records are
 // 8-byte aligned (checked on the host), so the window starts 0 or 8 bytes
 // before the record and is 656 bytes long; it never leaves the 16-byte
@@ -329,25 +326,27 @@ __global__ void __launch_bounds__(256, 4) fp8_gather_decode_kernel(const DecodeP
   const char* batch_recs = p.recs + b * p.T * p.record_stride;
   const char* rec = batch_recs + static_cast<int64_t>(mine >= 0 ? mine : 0) * p.record_stride;
   const int off = static_cast<int>(reinterpret_cast<uintptr_t>(rec) & 15u);
-  // bytes expected per half: lanes 0-3 hold half 0's records, lanes 4-7 half 1's
+  // bytes expected per half: lanes [0, kHalf) hold half 0's records, lanes
+  // [kHalf, 2 kHalf) half 1's
+  constexpr int kHalf = kDecRecs / 2;
   uint32_t tot = (mine >= 0) ? static_cast<uint32_t>(kDecSlot) : 0u;
-  tot += __shfl_xor_sync(0xffffffffu, tot, 1);
-  tot += __shfl_xor_sync(0xffffffffu, tot, 2);
-  const uint32_t tot1 = __shfl_sync(0xffffffffu, tot, 4);
+#pragma unroll
+  for (int sh = 1; sh < kHalf; sh <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, sh);
+  const uint32_t tot1 = __shfl_sync(0xffffffffu, tot, kHalf);
   if (lane == 0) {
     mbar_arrive_expect_tx(&bars[0], tot);
     mbar_arrive_expect_tx(&bars[1], tot1);
   }
   __syncwarp();
-  if (mine >= 0) bulk_g2s(st + lane * kDecSlot, rec - off, kDecSlot, &bars[lane >> 2]);
+  if (mine >= 0) bulk_g2s(st + lane * kDecSlot, rec - off, kDecSlot, &bars[lane / kHalf]);
   uint4* out0 = reinterpret_cast<uint4*>(p.kdec + row0 * kD);  // rows of 72 x 16 bytes
   bool landed[2] = {true, true};
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     landed[half] = mbar_wait(&bars[half], 0u);
 #pragma unroll
-    for (int rr = 0; rr < kDecRecs / 2; ++rr) {
-      const int r = half * (kDecRecs / 2) + rr;
+    for (int rr = 0; rr < kHalf; ++rr) {
+      const int r = half * kHalf + rr;
       const bool valid = __shfl_sync(0xffffffffu, mine, r) >= 0;
       const int ro = __shfl_sync(0xffffffffu, off, r);
       decode_row(st + r * kDecSlot, ro, out0 + r * (kRowBytes / 16), lane, valid);
