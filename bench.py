@@ -668,6 +668,20 @@ def run_gpu(args):
         e_e[i].record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / e2e_steps, dev)
+    # hot-L2 leg: the same step back to back with no flush in between (what a
+    # workload smaller than L2 sees when it repeats); reported beside the
+    # flushed figure, never as the value
+    hot_steps = max(3, min(steps, 50))
+    h_s, h_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h_s.record(stream)
+    for _ in range(hot_steps):
+        if graph is not None:
+            graph.replay()
+        else:
+            wl.step()
+    h_e.record(stream)
+    torch.cuda.synchronize(dev)
+    hot_ms = max_over_ranks(h_s.elapsed_time(h_e) / hot_steps, dev)
     # dominant-kernel leg: the library records events around its dominant
     # kernel (sa.kernel_events); same flush protocol, separate from the timed
     # steps because recording between kernels removes their launch overlap
@@ -711,6 +725,8 @@ def run_gpu(args):
                     "launch": "CUDA graph replay of the H2D copy, the library call and "
                               "the D2H copy per step" if e2e_graph is not None
                               else "direct copies and library call per step"},
+            "hot_l2": {"ms_per_step": round(hot_ms, 5), "steps": hot_steps,
+                       "note": "steps back to back, L2 not flushed"},
             "gpu_launches": wl.launches_per_step * steps,
             "clocks": clk.summary(),
             "wall_s_timed_region": round(wall, 4),
