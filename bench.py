@@ -765,7 +765,8 @@ def cpu_baseline(wl, args, budget_s: float = 10.0):
     t0 = time.perf_counter()
     _oracle_threads(wl, rows_all[:n], cores)
     dt = time.perf_counter() - t0
-    # grow the sample toward the time budget, capped at the whole step
+    # grow the sample toward the time budget: first within the step's rows,
+    # then whole passes over them when one pass is shorter than the budget
     if dt < budget_s and n < len(rows_all):
         n2 = min(len(rows_all), max(n, int(n * budget_s / max(dt, 1e-3))))
         t0 = time.perf_counter()
@@ -773,9 +774,18 @@ def cpu_baseline(wl, args, budget_s: float = 10.0):
         dt = time.perf_counter() - t0
         n = n2
     unit = "tokens/s" if isinstance(wl, Prefill) else "query-rows/s"
+    what = unit.split('/')[0]
+    sample = f"{n} of {wl.rows} {what} of one step"
+    if dt < budget_s and n == len(rows_all):
+        passes = min(1000, max(2, math.ceil(budget_s / max(dt, 1e-3))))
+        t0 = time.perf_counter()
+        for _ in range(passes):
+            _oracle_threads(wl, rows_all, cores)
+        dt = time.perf_counter() - t0
+        n = passes * len(rows_all)
+        sample = f"{passes} passes over all {wl.rows} {what} of one step"
     return {"value": round(n / dt, 2), "unit": unit, "cores": cores,
-            "kind": "oracle", "sample": f"{n} of {wl.rows} {unit.split('/')[0]} of one step",
-            "seconds": round(dt, 3)}
+            "kind": "oracle", "sample": sample, "seconds": round(dt, 3)}
 
 
 # ---------------------------------------------------------------------------
