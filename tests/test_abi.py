@@ -122,6 +122,38 @@ def test_host_checks_reject_bad_requests_without_launching(lib):
     assert lib.paged_attn_decode(C.byref(g), None) == -1
 
 
+def test_empty_sizes_are_shape_errors_without_launching(lib):
+    # An empty batch, sequence, head or index width is SA_ERR_SHAPE, returned by
+    # the host checks (the pointers below are never dereferenced).
+    fake, word = C.c_void_p(0x1000), C.c_void_p(0x2000)
+    assert lib.validate_indices(fake, 0, 1, 1, 1, 0, None, 10, None, word, None) == -2
+    assert lib.build_present_kv(None, fake, C.c_void_p(0x9000), None, None, None,
+                                sa.BF16, 0, 1, 0, 4, 8, 4, None, None, None) == -2
+    for field in ("B", "Hq", "Sq", "D", "T"):
+        p = sa.SparseParams()
+        p.q, p.k_cache, p.v_cache, p.y, p.idx = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+        p.B, p.Hq, p.Hkv, p.Sq, p.D, p.Dv, p.T, p.I, p.K = 1, 4, 2, 1, 64, 64, 32, 2, 8
+        p.q_dtype = p.kv_dtype = sa.BF16
+        setattr(p, field, 0)
+        assert lib.sparse_attn_decode(C.byref(p), None) == -2, field
+        assert lib.sparse_attn_decode_workspace(C.byref(p)) == 0, field
+    for field in ("B", "S", "Hq"):
+        q = sa.PrefillParams()
+        q.q, q.k, q.v, q.y = 0x10000, 0x20000, 0x30000, 0x40000
+        q.dtype = sa.BF16
+        q.B, q.Hq, q.Hkv, q.S, q.D = 1, 4, 2, 16, 64
+        setattr(q, field, 0)
+        assert lib.attn_prefill(C.byref(q), None) == -2, field
+    for field in ("B", "max_pages", "page_tokens"):
+        g = sa.PagedParams()
+        g.q, g.k_pool, g.v_pool, g.y = 0x10000, 0x20000, 0x30000, 0x40000
+        g.block_table, g.ctx_len = 0x50000, 0x60000
+        g.dtype = sa.F16
+        g.B, g.Hq, g.Hkv, g.D, g.page_tokens, g.max_pages, g.num_pages = 1, 4, 2, 64, 16, 2, 4
+        setattr(g, field, 0)
+        assert lib.paged_attn_decode(C.byref(g), None) == -2, field
+
+
 def test_workspace_query_needs_no_output_pointer(lib):
     p = sa.SparseParams()
     p.q, p.k_cache, p.v_cache, p.idx = 0x10000, 0x20000, 0x30000, 0x50000
