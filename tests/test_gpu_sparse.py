@@ -533,6 +533,25 @@ def test_fp8_tc05_options_kv_len_softcap_sink_and_query_positions(cuda_lib):
         assert_close(to64(y), ref, y.dtype, f"fp8 tc05 options softcap={softcap}")
 
 
+@pytest.mark.parametrize("past_len", [2400, 2450])
+def test_fp8_tc05_causal_frontier_matches_oracle(cuda_lib, past_len):
+    # Query position i sees keys <= past_len + i: the frontier cuts through the
+    # 128-token window [2372, 2500) and through the selected indices.
+    c = _fp8_case(B=2, Hq=128, T=2500, K=400)
+    inp = synth.make_sparse_inputs(c, seed=99)
+    q2 = synth.normal((c.B, c.Hq, 2, c.D), "bf16", 100)
+    idx2 = inp["idx"].repeat(1, 1, 2, 1)
+    inp2 = dict(inp, q=q2, idx=idx2)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = _run_fp8(cuda_lib, c, inp2, causal=True, past_len=past_len, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.sparse_attention(q2, idx2, records=inp["kv_records"], n_rope=c.n_rope,
+                                  scale=c.eff_scale(), window=c.window, causal=True,
+                                  past_len=past_len)
+    assert_close(to64(y), ref, y.dtype, f"fp8 tc05 causal past_len={past_len}")
+
+
 def test_fp8_tc05_is_deterministic(cuda_lib):
     c = _fp8_case(B=2, Hq=128, T=6000, K=1500)
     inp = synth.make_sparse_inputs(c, seed=97)
