@@ -23,7 +23,8 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
                        text, flags=re.M)
@@ -54,7 +55,8 @@ def _c_layout(struct_name, fields):
     with tempfile.TemporaryDirectory() as d:
         c = os.path.join(d, "t.c")
         exe = os.path.join(d, "t")
-        open(c, "w").write("\n".join(src))
+        with open(c, "w") as f:
+            f.write("\n".join(src))
         subprocess.run(["gcc", "-o", exe, c], check=True)
         vals = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
                                                check=True).stdout.split()]

@@ -168,7 +168,9 @@ def test_validation_brute_force_all_small_rows():
 def test_validation_messages_golden():
     path = os.path.join(GOLDEN, "validation_messages.txt")
     cases = 0
-    for line in open(path):
+    with open(path) as f:
+        text = f.read()
+    for line in text.splitlines():
         line = line.strip()
         if not line or line.startswith("#"):
             continue
@@ -246,8 +248,8 @@ def _one_row(q, k, v, keys, scale, softcap=0.0, **kw):
 
 
 def test_golden_two_token_examples():
-    lines = [l.split() for l in open(os.path.join(GOLDEN, "two_token_softmax.txt"))
-             if l.strip() and not l.startswith("#")]
+    with open(os.path.join(GOLDEN, "two_token_softmax.txt")) as f:
+        lines = [l.split() for l in f if l.strip() and not l.startswith("#")]
     assert [l[0] for l in lines] == ["plain", "softcap"]
     # plain: k1 = ln 3 as stored in f32; closed form with the stored value
     k1 = float(np.float32(math.log(3.0)))

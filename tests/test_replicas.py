@@ -36,7 +36,7 @@ def _rank(rank, world, port, out):
 
 def test_two_replicas_take_the_slowest_rank_and_count_every_rank():
     world, port = 2, _free_port()
-    with mp.Manager() as man:
+    with mp.get_context("spawn").Manager() as man:  # no fork of this threaded process
         out = man.dict()
         mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
