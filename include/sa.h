@@ -168,8 +168,10 @@ int build_present_kv(const void* past_k, const void* cur_k, void* present_k,
  *   sink: nullable device float [Hq] (natural-log logits).
  * scale: 0 means 1/sqrt(D).  Index rows are validated on the device against
  * len_b when err_word != NULL (row_status nullable, as in validate_indices);
- * malformed rows never fault: negative entries are skipped and entries
- * >= len_b are masked.
+ * malformed rows never fault: negative entries are skipped, entries >= len_b
+ * are masked, and the other entries of such a row (after padding, repeated or
+ * out of order) are attended as they stand.  A malformed row's output is
+ * finite; only a well-formed row's output is the definition above.
  * Fused append (dense cache only): when k_cur != NULL, the current token(s)
  * k_cur / v_cur [B, Hkv, cur_len, D] are first written into the cache at
  * positions write_pos[b] .. write_pos[b] + cur_len - 1 (write_pos: nullable
