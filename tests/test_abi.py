@@ -22,6 +22,17 @@ def lib():
     return sa.load()
 
 
+@pytest.fixture(scope="module")
+def host_lib(lib):
+    """The library, for calls on fake device addresses that the host checks
+    must refuse.  Skipped where a GPU is present: a request that passed the
+    checks by mistake must never reach a real device."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("fake-address checks run on hosts without a GPU")
+    return lib
+
+
 def declared_functions():
     with open(HEADER) as f:
         text = f.read()
@@ -85,67 +96,67 @@ def test_kernel_event_hook_needs_both_events_or_none(lib):
     assert lib.sa_set_kernel_events(None, None) == 0
 
 
-def test_host_checks_reject_bad_requests_without_launching(lib):
+def test_host_checks_reject_bad_requests_without_launching(host_lib):
     # validate_indices: null pointers, bad shapes
-    assert lib.validate_indices(None, 0, 1, 1, 1, 4, None, 10, None, None, None) == -1
+    assert host_lib.validate_indices(None, 0, 1, 1, 1, 4, None, 10, None, None, None) == -1
     fake = C.c_void_p(0x1000)
     word = C.c_void_p(0x2000)
-    assert lib.validate_indices(fake, 0, 0, 1, 1, 4, None, 10, None, word, None) == -2
-    assert lib.validate_indices(C.c_void_p(0x1002), 0, 1, 1, 1, 4, None, 10, None, word,
-                                None) == -4
+    assert host_lib.validate_indices(fake, 0, 0, 1, 1, 4, None, 10, None, word, None) == -2
+    assert host_lib.validate_indices(C.c_void_p(0x1002), 0, 1, 1, 1, 4, None, 10, None, word,
+                                     None) == -4
     # sparse decode
     p = sa.SparseParams()
-    assert lib.sparse_attn_decode(C.byref(p), None) == -1
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -1
     p.q, p.k_cache, p.v_cache, p.y, p.idx = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
     p.B, p.Hq, p.Hkv, p.Sq, p.D, p.Dv, p.T, p.I, p.K = 1, 6, 4, 1, 64, 64, 32, 4, 8
     p.q_dtype = p.kv_dtype = sa.BF16
-    assert lib.sparse_attn_decode(C.byref(p), None) == -2   # Hq % Hkv
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -2   # Hq % Hkv
     p.Hkv = 2
     p.I = 3
-    assert lib.sparse_attn_decode(C.byref(p), None) == -2   # I not in {1, Hkv, Hq}
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -2   # I not in {1, Hkv, Hq}
     p.I = 2
     p.kv_dtype = sa.F16
-    assert lib.sparse_attn_decode(C.byref(p), None) == -3   # q/kv dtype mismatch
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -3   # q/kv dtype mismatch
     p.kv_dtype = sa.BF16
     p.y = 0x10000 + 64                                       # y overlaps q
-    assert lib.sparse_attn_decode(C.byref(p), None) == -6
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -6
     p.y = 0x40000
     p.K, p.window = 0, 0
-    assert lib.sparse_attn_decode(C.byref(p), None) == -2   # no candidates at all
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -2   # no candidates at all
     # present: concat output overlapping an input
-    assert lib.build_present_kv(None, C.c_void_p(0x1000), C.c_void_p(0x1000), None, None, None,
-                                sa.BF16, 1, 1, 0, 4, 8, 4, None, None, None) == -6
-    assert lib.build_present_kv(None, C.c_void_p(0x1000), C.c_void_p(0x9000), None, None, None,
-                                7, 1, 1, 0, 4, 8, 4, None, None, None) == -3
+    assert host_lib.build_present_kv(None, C.c_void_p(0x1000), C.c_void_p(0x1000), None, None,
+                                     None, sa.BF16, 1, 1, 0, 4, 8, 4, None, None, None) == -6
+    assert host_lib.build_present_kv(None, C.c_void_p(0x1000), C.c_void_p(0x9000), None, None,
+                                     None, 7, 1, 1, 0, 4, 8, 4, None, None, None) == -3
     # prefill / paged
     q = sa.PrefillParams()
-    assert lib.attn_prefill(C.byref(q), None) == -1
+    assert host_lib.attn_prefill(C.byref(q), None) == -1
     g = sa.PagedParams()
-    assert lib.paged_attn_decode(C.byref(g), None) == -1
+    assert host_lib.paged_attn_decode(C.byref(g), None) == -1
 
 
-def test_empty_sizes_are_shape_errors_without_launching(lib):
+def test_empty_sizes_are_shape_errors_without_launching(host_lib):
     # An empty batch, sequence, head or index width is SA_ERR_SHAPE, returned by
     # the host checks (the pointers below are never dereferenced).
     fake, word = C.c_void_p(0x1000), C.c_void_p(0x2000)
-    assert lib.validate_indices(fake, 0, 1, 1, 1, 0, None, 10, None, word, None) == -2
-    assert lib.build_present_kv(None, fake, C.c_void_p(0x9000), None, None, None,
-                                sa.BF16, 0, 1, 0, 4, 8, 4, None, None, None) == -2
+    assert host_lib.validate_indices(fake, 0, 1, 1, 1, 0, None, 10, None, word, None) == -2
+    assert host_lib.build_present_kv(None, fake, C.c_void_p(0x9000), None, None, None,
+                                     sa.BF16, 0, 1, 0, 4, 8, 4, None, None, None) == -2
     for field in ("B", "Hq", "Sq", "D", "T"):
         p = sa.SparseParams()
         p.q, p.k_cache, p.v_cache, p.y, p.idx = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
         p.B, p.Hq, p.Hkv, p.Sq, p.D, p.Dv, p.T, p.I, p.K = 1, 4, 2, 1, 64, 64, 32, 2, 8
         p.q_dtype = p.kv_dtype = sa.BF16
         setattr(p, field, 0)
-        assert lib.sparse_attn_decode(C.byref(p), None) == -2, field
-        assert lib.sparse_attn_decode_workspace(C.byref(p)) == 0, field
+        assert host_lib.sparse_attn_decode(C.byref(p), None) == -2, field
+        assert host_lib.sparse_attn_decode_workspace(C.byref(p)) == 0, field
     for field in ("B", "S", "Hq"):
         q = sa.PrefillParams()
         q.q, q.k, q.v, q.y = 0x10000, 0x20000, 0x30000, 0x40000
         q.dtype = sa.BF16
         q.B, q.Hq, q.Hkv, q.S, q.D = 1, 4, 2, 16, 64
         setattr(q, field, 0)
-        assert lib.attn_prefill(C.byref(q), None) == -2, field
+        assert host_lib.attn_prefill(C.byref(q), None) == -2, field
     for field in ("B", "max_pages", "page_tokens"):
         g = sa.PagedParams()
         g.q, g.k_pool, g.v_pool, g.y = 0x10000, 0x20000, 0x30000, 0x40000
@@ -153,7 +164,68 @@ def test_empty_sizes_are_shape_errors_without_launching(lib):
         g.dtype = sa.F16
         g.B, g.Hq, g.Hkv, g.D, g.page_tokens, g.max_pages, g.num_pages = 1, 4, 2, 64, 16, 2, 4
         setattr(g, field, 0)
-        assert lib.paged_attn_decode(C.byref(g), None) == -2, field
+        assert host_lib.paged_attn_decode(C.byref(g), None) == -2, field
+
+
+def _fp8_params():
+    # A well-formed FP8 request on fake, non-overlapping, aligned addresses; the
+    # tests below only ever call the library after breaking one field of it,
+    # so every call is refused by the host checks and nothing is launched.
+    p = sa.SparseParams()
+    p.q, p.k_cache, p.v_cache, p.y, p.idx = 0x100000, 0x10000000, None, 0x200000, 0x300000
+    p.B, p.Hq, p.Hkv, p.Sq, p.D, p.Dv, p.T, p.I, p.K = 2, 128, 1, 1, 576, 576, 1000, 1, 64
+    p.q_dtype, p.kv_dtype = sa.BF16, sa.FP8_E4M3_B64
+    p.record_stride, p.n_rope, p.window = 648, 64, 128
+    return p
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("q_dtype", sa.F16, -3),            # FP8 records take bf16 queries
+    ("D", 512, -7), ("n_rope", 32, -7),  # 512 E4M3 + 64 bf16 dims only
+    ("Dv", 512, -7),                     # V is the whole record
+    ("I", 128, -7),                      # one index head
+    ("Hq", 48, -7),                      # query heads in blocks of 32
+    ("record_stride", 644, -2), ("record_stride", 652, -2),
+    ("k_cache", 0x10000004, -4),         # records must be 8-byte aligned
+    ("y", 0x10000000 + 4096, -6),        # the output overlaps the records
+    ("softcap", -1.0, -2), ("scale", float("inf"), -2),
+])
+def test_fp8_requests_the_library_does_not_serve_are_refused(host_lib, field, value, status):
+    p = _fp8_params()
+    setattr(p, field, value)
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == status
+
+
+def test_fp8_refuses_a_fused_append_and_a_second_latent_head(host_lib):
+    p = _fp8_params()
+    p.k_cur = 0x400000
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -7
+    p = _fp8_params()
+    p.Hkv = 2
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -7
+
+
+def _paged_params():
+    g = sa.PagedParams()
+    g.q, g.k_pool, g.v_pool, g.y = 0x100000, 0x10000000, 0x20000000, 0x200000
+    g.block_table, g.ctx_len = 0x300000, 0x400000
+    g.dtype = sa.F16
+    g.B, g.Hq, g.Hkv, g.D, g.page_tokens, g.max_pages, g.num_pages = 2, 8, 2, 128, 16, 4, 8
+    return g
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("dtype", 7, -3),
+    ("Hq", 7, -2),                                  # Hq % Hkv
+    ("num_pages", 1 << 27, -7),                     # pool rows beyond 2^31
+    ("v_pool", 0x10000000 + 512, -6),               # the pools overlap
+    ("y", 0x100000 + 64, -6),                       # the output overlaps q
+    ("scale", float("nan"), -2),
+])
+def test_paged_requests_the_library_does_not_serve_are_refused(host_lib, field, value, status):
+    g = _paged_params()
+    setattr(g, field, value)
+    assert host_lib.paged_attn_decode(C.byref(g), None) == status
 
 
 def test_workspace_query_needs_no_output_pointer(lib):
