@@ -83,6 +83,22 @@ def test_paged_row_copy_path_matches_oracle(cuda_lib, monkeypatch):
     assert_close(to64(y), ref, y.dtype, "paged row copies")
 
 
+def test_paged_batches_past_the_stream_limit_use_the_split_kernel(cuda_lib):
+    """2,050 sequences (the stream kernel keeps a per-sequence prefix for at most
+    2,048): the split-K kernel and its combine serve the call; contexts of 1 to
+    40 tokens include single-token sequences and partial last pages."""
+    c, inp = _paged_small("f16", seed=8, B=2050, Hq=8, Hkv=2, D=64, ctx_low=1, ctx_high=40)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = cuda_lib.paged_attn_decode(inp["q"].to(DEV), inp["k_pool"].to(DEV), inp["v_pool"].to(DEV),
+                                   inp["block_table"].to(DEV), inp["ctx_len"].to(DEV),
+                                   scale=c.eff_scale(), err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.paged_decode(inp["q"], inp["k_pool"], inp["v_pool"], inp["block_table"],
+                              inp["ctx_len"], page_tokens=c.page_tokens, scale=c.eff_scale())
+    assert_close(to64(y), ref, y.dtype, "paged B=2050")
+
+
 def test_paged_bad_table_entry_latches_and_skips(cuda_lib):
     c, inp = _paged_small("f16", seed=4)
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
