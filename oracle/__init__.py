@@ -61,6 +61,7 @@ class _SparseArgs(C.Structure):
         ("kv_len", _p), ("past_len", _i64), ("causal", C.c_int),
         ("scale", C.c_double), ("softcap", C.c_double), ("window", _i64), ("sink", _p),
         ("record_bytes", _i64), ("n_rope", _i64),
+        ("bias", _p), ("bias_rank", _i64), ("bias_dims", _i64 * 4),
     ]
 
 
@@ -214,12 +215,14 @@ def present_append(cache, cur, write_pos):
 def sparse_attention(q, idx, k=None, v=None, records=None, *, scale: float,
                      softcap: float = 0.0, window: int = 0, kv_len=None,
                      past_len: int = 0, causal: bool = False, sink=None,
-                     n_rope: int = 0, Dv=None, rows=None) -> np.ndarray:
+                     n_rope: int = 0, Dv=None, rows=None, bias=None) -> np.ndarray:
     """Selected-token attention; see ``orc_sparse_attention``.
 
     Dense cache: ``k``/``v`` ``[B, Hkv, T, D]``.  FP8: ``records``
     ``[B, Hkv, T, record_bytes]`` uint8 (K and V are the decoded record),
-    ``n_rope`` the bf16 tail width, logical ``D = 64*blocks + n_rope``."""
+    ``n_rope`` the bf16 tail width, logical ``D = 64*blocks + n_rope``.
+    ``bias``: optional float32 tensor of rank <= 4, broadcast right-aligned
+    against ``[B, Hq, Sq, T]`` and added to the score of cache position j."""
     qh = _host(q)
     B, Hq, Sq, D = qh.shape
     ih = _host(idx)
@@ -250,6 +253,14 @@ def sparse_attention(q, idx, k=None, v=None, records=None, *, scale: float,
     a.scale, a.softcap, a.window = scale, softcap, window
     sk = None if sink is None else _host(torch.as_tensor(sink, dtype=torch.float64))
     a.sink = _ptr(sk)
+    bh = None
+    if bias is not None:
+        bh = _host(torch.as_tensor(bias)).to(torch.float32)
+        if bh.dim() > 4:
+            raise ValueError("bias rank exceeds 4")
+        a.bias, a.bias_rank = bh.data_ptr(), bh.dim()
+        for r_, e_ in enumerate(bh.shape):
+            a.bias_dims[r_] = e_
     r, nr = _rows_arg(rows)
     n = nr if r is not None else B * Hq * Sq
     y = np.zeros((n, a.Dv), dtype=np.float64)

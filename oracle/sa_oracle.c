@@ -21,6 +21,9 @@
  *         `csa_ratio128_sink_attention` (dense window + records, sink).
  *   [PG]  ferrum-kernels, vnext_ops/transformer/causal_attention.rs --
  *         16-token KV blocks addressed through a table.
+ *   [IS] `bias_at` and `validate_bias_shape`: the optional additive bias of a
+ *         selected-token score, a tensor of rank <= 4 broadcast right-aligned
+ *         against [batch, q_head, query, cache position].
  *   OCP 8-bit floating point specification (E4M3FN) and the OCP MX
  *   specification (E8M0 scale) for the FP8 record decode.
  *
@@ -307,6 +310,7 @@ static void get_v(const orc_kv* kv, int64_t b, int64_t h, int64_t t, double* out
 /* One output row ([SA] Semantics; [IS] index_share_row):
  *   s_j = scale * sum_d q_d k_{j,d}
  *   s_j = softcap * tanh(s_j / softcap)            if softcap != 0
+ *   s_j = s_j + bias[j]                              if a bias is given
  *   s_j = -inf  if masked[j]                         (causal / pad / not a key)
  *   M = max_j s_j;  M == -inf  =>  y = 0
  *   L = sum_j exp(s_j - M)  (+ exp(sink - M) if a sink logit is given)
@@ -315,7 +319,7 @@ static void get_v(const orc_kv* kv, int64_t b, int64_t h, int64_t t, double* out
  */
 static void attend_row(const orc_kv* kv, int64_t b, int64_t kvh, const double* q,
                        const int64_t* keys, const int* masked, int64_t n, double scale,
-                       double softcap, const double* sink, double* y) {
+                       double softcap, const double* bias, const double* sink, double* y) {
   double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
   double* krow = (double*)malloc(sizeof(double) * (size_t)kv->D);
   double* vrow = (double*)malloc(sizeof(double) * (size_t)kv->D);
@@ -334,6 +338,9 @@ static void attend_row(const orc_kv* kv, int64_t b, int64_t kvh, const double* q
     double sj = scale * dot;
     if (softcap != 0.0) {
       sj = softcap * tanh(sj / softcap);
+    }
+    if (bias) {
+      sj += bias[j];
     }
     s[j] = sj;
     if (sj > M) {
@@ -397,13 +404,52 @@ typedef struct {
   const double* sink;   /* nullable: per-query-head logit added to the denominator */
   int64_t record_bytes; /* FP8 only */
   int64_t n_rope;       /* FP8 only */
+  const float* bias;    /* nullable: additive bias of rank bias_rank (<= 4) */
+  int64_t bias_rank;
+  int64_t bias_dims[4]; /* its shape, the first bias_rank entries */
 } orc_sparse_args;
+
+/* [IS] bias_at: the bias entry of logical element (b, h, i, j).  The bias
+ * shape lines up with [B, Hq, Sq, T] from the right; an axis of extent 1 is
+ * broadcast (index 0), any other axis is indexed by the logical coordinate;
+ * the offset is row-major over the bias's own shape. */
+static double orc_bias_at(const float* bias, int64_t rank, const int64_t* dims, int64_t b,
+                          int64_t h, int64_t i, int64_t j) {
+  int64_t logical[4] = {b, h, i, j};
+  int64_t off = 0;
+  for (int64_t r = 0; r < rank; ++r) {
+    int64_t axis = 4 - rank + r;
+    int64_t extent = dims[r];
+    int64_t index = (extent == 1) ? 0 : logical[axis];
+    off = off * extent + index;
+  }
+  return (double)bias[off];
+}
+
+/* [IS] validate_bias_shape: rank <= 4 and every axis 1 or equal to the
+ * matching axis of [B, Hq, Sq, T] counted from the right. */
+static int orc_bias_shape_ok(const orc_sparse_args* a) {
+  int64_t target[4] = {a->B, a->Hq, a->Sq, a->T};
+  if (a->bias_rank < 0 || a->bias_rank > 4) {
+    return 0;
+  }
+  for (int64_t r = 0; r < a->bias_rank; ++r) {
+    int64_t want = target[4 - a->bias_rank + r];
+    if (a->bias_dims[r] != 1 && a->bias_dims[r] != want) {
+      return 0;
+    }
+  }
+  return 1;
+}
 
 /* Candidate set of one row:
  *   the valid prefix of idx[b, ih, i, :] (take while != -1), and with a
  *   window W additionally every t in [len_b - W, len_b), the selected entries
  *   then being kept only below len_b - W so that each key counts once.
  * A kept key is masked when causal and j > past_len + i, or when j >= len_b.
+ * With a bias, the score of key j gains bias(b, h, i, j) after the softcap
+ * ([IS] index_share_row adds it to the scaled score; the key is the cache
+ * position); a -inf entry masks the key.
  * Rows are flattened (b, h, i); `rows` selects which to compute (NULL: all),
  * y gets one Dv-vector per computed row.  Returns 0, or -1 on a bad shape. */
 int orc_sparse_attention(const orc_sparse_args* a, const int64_t* rows, int64_t nrows,
@@ -414,6 +460,9 @@ int orc_sparse_attention(const orc_sparse_args* a, const int64_t* rows, int64_t 
   if (!(a->I == 1 || a->I == a->Hkv || a->I == a->Hq)) {
     return -1;
   }
+  if (a->bias && !orc_bias_shape_ok(a)) {
+    return -1;
+  }
   int64_t g = a->Hq / a->Hkv;
   int64_t total = a->B * a->Hq * a->Sq;
   int64_t count = rows ? nrows : total;
@@ -422,6 +471,7 @@ int orc_sparse_attention(const orc_sparse_args* a, const int64_t* rows, int64_t 
   int64_t cap = a->K + a->window;
   int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)(cap > 0 ? cap : 1));
   int* masked = (int*)malloc(sizeof(int) * (size_t)(cap > 0 ? cap : 1));
+  double* brow = (double*)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1));
   double* q = (double*)malloc(sizeof(double) * (size_t)a->D);
   for (int64_t r = 0; r < count; ++r) {
     int64_t row = rows ? rows[r] : r;
@@ -462,12 +512,17 @@ int orc_sparse_attention(const orc_sparse_args* a, const int64_t* rows, int64_t 
         m = 1;
       }
       masked[j] = m;
+      brow[j] = 0.0;
+      if (a->bias && !m) {
+        brow[j] = orc_bias_at(a->bias, a->bias_rank, a->bias_dims, b, h, i, keys[j]);
+      }
     }
-    attend_row(&kv, b, kvh, q, keys, masked, n, a->scale, a->softcap,
+    attend_row(&kv, b, kvh, q, keys, masked, n, a->scale, a->softcap, a->bias ? brow : NULL,
                a->sink ? &a->sink[h] : NULL, y + r * a->Dv);
   }
   free(keys);
   free(masked);
+  free(brow);
   free(q);
   return 0;
 }
@@ -503,7 +558,7 @@ int orc_prefill(const void* q, const void* k, const void* v, int dtype, int64_t 
       keys[j] = j;
       masked[j] = (causal && j > i) ? 1 : 0;
     }
-    attend_row(&kv, b, h / g, qr, keys, masked, S, scale, softcap, NULL, y + r * D);
+    attend_row(&kv, b, h / g, qr, keys, masked, S, scale, softcap, NULL, NULL, y + r * D);
   }
   free(keys);
   free(masked);
@@ -558,7 +613,7 @@ int orc_paged_decode(const void* q, const void* k_pool, const void* v_pool, int 
     for (int64_t t = 0; t < n; ++t) {
       keys[t] = t;
     }
-    attend_row(&kv, 0, 0, qr, keys, masked, n, scale, 0.0, NULL, y + r * D);
+    attend_row(&kv, 0, 0, qr, keys, masked, n, scale, 0.0, NULL, NULL, y + r * D);
     free(keys);
     free(masked);
     free(kc);

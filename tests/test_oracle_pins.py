@@ -331,6 +331,116 @@ def test_sparse_matches_brute_force_masked_dense(I_kind, dt):
             assert np.allclose(y[b * Hq + h], exp, rtol=1e-12, atol=1e-12)
 
 
+def test_golden_bias_two_token_examples():
+    with open(os.path.join(GOLDEN, "bias_two_token.txt")) as f:
+        lines = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    assert [l[0] for l in lines] == ["plain", "softcap", "neginf"]
+    ln3, ln2 = float(np.float32(math.log(3.0))), float(np.float32(math.log(2.0)))
+    y = _one_row([1.0], [[0.0], [0.0]], [[0.0], [4.0]], [0, 1], scale=1.0,
+                 bias=torch.tensor([0.0, ln3]))
+    assert abs(y[0] - 4.0 * math.exp(ln3) / (1.0 + math.exp(ln3))) < 1e-15
+    assert abs(y[0] - 3.0) < 1e-6
+    # the bias comes after the softcap: tanh is not applied to it
+    y = _one_row([1.0], [[0.0], [1.0]], [[0.0], [1.0]], [0, 1], scale=1.0, softcap=1.0,
+                 bias=torch.tensor([ln2, 0.0]))
+    e = math.exp(math.tanh(1.0))
+    assert abs(y[0] - e / (math.exp(ln2) + e)) < 1e-15
+    # a -inf entry masks its key
+    y = _one_row([1.0], [[0.0], [5.0]], [[7.0], [4.0]], [0, 1], scale=1.0,
+                 bias=torch.tensor([0.0, -math.inf]))
+    assert y[0] == 7.0
+
+
+def _broadcast_bias(shape, B, Hq, Sq, T, seed):
+    """A float32 bias of the given shape and its numpy broadcast to [B, Hq, Sq, T]."""
+    g = torch.Generator().manual_seed(seed)
+    bias = (torch.randn(shape, generator=g) * 0.7).to(torch.float32)
+    full = np.broadcast_to(bias.double().numpy(), (B, Hq, Sq, T))
+    return bias, full
+
+
+@pytest.mark.parametrize("shape_kind", ["full", "h1t", "b11t", "t", "st", "scalar1"])
+def test_bias_broadcast_matches_brute_force(shape_kind):
+    B, Hq, Hkv, Sq, T, D, K = 2, 4, 2, 2, 30, 8, 7
+    shape = {"full": (B, Hq, Sq, T), "h1t": (Hq, 1, T), "b11t": (B, 1, 1, T), "t": (T,),
+             "st": (Sq, T), "scalar1": (1, 1, 1, 1)}[shape_kind]
+    q = synth.normal((B, Hq, Sq, D), "f32", 61)
+    k = synth.normal((B, Hkv, T, D), "f32", 62)
+    v = synth.normal((B, Hkv, T, D), "f32", 63)
+    idx = synth.sorted_sample_rows(B * Hkv * Sq, 0, T, K, 64).reshape(B, Hkv, Sq, K)
+    bias, full = _broadcast_bias(shape, B, Hq, Sq, T, 65)
+    scale, cap = 0.4, 3.0
+    y = oracle.sparse_attention(q, idx, k, v, scale=scale, softcap=cap, bias=bias)
+    g = Hq // Hkv
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Sq):
+                sel = idx[b, h // g, i].tolist()
+                kk, vv = as64(k[b, h // g]), as64(v[b, h // g])
+                s = cap * np.tanh((kk @ as64(q[b, h, i])) * scale / cap) + full[b, h, i]
+                allowed = np.zeros(T, dtype=bool)
+                allowed[sel] = True
+                s = np.where(allowed, s, -np.inf)
+                w = np.exp(s - s.max())
+                exp = (w / w.sum()) @ vv
+                row = (b * Hq + h) * Sq + i
+                assert np.allclose(y[row], exp, rtol=1e-12, atol=1e-12)
+
+
+def test_bias_neg_inf_equals_dropping_the_key_and_constant_bias_changes_nothing():
+    B, Hq, T, D, K = 1, 3, 24, 8, 6
+    q = synth.normal((B, Hq, 1, D), "bf16", 71)
+    k = synth.normal((B, 1, T, D), "bf16", 72)
+    v = synth.normal((B, 1, T, D), "bf16", 73)
+    idx = torch.tensor([[[[1, 5, 8, 13, 20, 22]]]], dtype=torch.int32)
+    base = oracle.sparse_attention(q, idx, k, v, scale=0.3)
+    # the same bias for every key of a row is a shift: softmax is unchanged
+    shift = torch.tensor([[[1.5]], [[-2.0]], [[0.25]]], dtype=torch.float32)  # [Hq, 1, 1]
+    y = oracle.sparse_attention(q, idx, k, v, scale=0.3, bias=shift)
+    assert np.allclose(y, base, rtol=0, atol=1e-14)
+    # -inf at cache position 8 removes that key
+    bias = torch.zeros(T, dtype=torch.float32)
+    bias[8] = -math.inf
+    y = oracle.sparse_attention(q, idx, k, v, scale=0.3, bias=bias)
+    dropped = torch.tensor([[[[1, 5, 13, 20, 22, -1]]]], dtype=torch.int32)
+    assert np.array_equal(y, oracle.sparse_attention(q, dropped, k, v, scale=0.3))
+    # -inf everywhere: a fully masked row gives 0
+    y = oracle.sparse_attention(q, idx, k, v, scale=0.3, bias=torch.full((T,), -math.inf))
+    assert np.array_equal(y, np.zeros_like(y))
+
+
+def test_bias_with_window_and_fp8_records_keys_by_cache_position():
+    # window ∪ selected over FP8 records: brute force over the decoded cache
+    B, Hq, T, W, K = 1, 2, 40, 6, 5
+    nope = synth.normal((B, 1, T, 512), "f32", 81)
+    rope = synth.normal((B, 1, T, 64), "bf16", 84)
+    rec = synth.quantize_fp8_block64_records(nope, rope)
+    q = synth.normal((B, Hq, 1, 576), "bf16", 82)
+    idx = torch.tensor([[[[3, 9, 17, 35, 38]]]], dtype=torch.int32)
+    bias, full = _broadcast_bias((Hq, 1, T), B, Hq, 1, T, 83)
+    y = oracle.sparse_attention(q, idx, records=rec, n_rope=64, scale=0.05, window=W,
+                                bias=bias)
+    dec = np.stack([oracle.decode_fp8_record(rec[0, 0, t], 512, 64) for t in range(T)])
+    keys = sorted(set(range(T - W, T)) | {3, 9, 17})
+    for h in range(Hq):
+        allowed = np.zeros(T, dtype=bool)
+        allowed[keys] = True
+        s = (dec @ as64(q[0, h, 0])) * 0.05 + full[0, h, 0]
+        s = np.where(allowed, s, -np.inf)
+        w = np.exp(s - s.max())
+        assert np.allclose(y[h], (w / w.sum()) @ dec, rtol=1e-12, atol=1e-12)
+
+
+def test_bias_shape_not_broadcastable_is_rejected():
+    q = synth.normal((1, 2, 1, 4), "f32", 91)
+    k = synth.normal((1, 1, 10, 4), "f32", 92)
+    idx = torch.tensor([[[[1, 2]]]], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        oracle.sparse_attention(q, idx, k, k, scale=1.0, bias=torch.zeros(9))
+    with pytest.raises(ValueError):
+        oracle.sparse_attention(q, idx, k, k, scale=1.0, bias=torch.zeros(3, 1, 10))
+
+
 def test_window_union_matches_brute_force_and_counts_each_key_once():
     B, T, D, K, W = 2, 50, 8, 6, 10
     q = synth.normal((B, 3, 1, D), "f32", 51)
