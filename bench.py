@@ -259,7 +259,7 @@ class SparseDecode:
         es = self.q.element_size()
         kbytes = self.valid * 2 * self.c.D * es + self.q.numel() * es + self.y.numel() * es
         return hbm_roofline("gather_stream_kernel", kbytes, kernel_ms, self.decode_bytes,
-                            decode_ms, peaks, TRAFFIC.get(self.c.name))
+                            decode_ms, peaks, traffic_for(self.c.name, "gather_stream_kernel"))
 
 
 class PagedDecode:
@@ -340,7 +340,7 @@ class PagedDecode:
         kbytes = (self.tokens * self.c.Hkv * self.c.D * es * 2 + self.inp["block_table"].numel() * 4
                   + 2 * self.q.numel() * es)
         return hbm_roofline("gather_stream_kernel (paged)", kbytes, kernel_ms, self.decode_bytes,
-                            decode_ms, peaks, TRAFFIC.get(self.c.name))
+                            decode_ms, peaks, traffic_for(self.c.name, "gather_stream_kernel"))
 
 
 class Prefill:
@@ -406,7 +406,7 @@ class Prefill:
 
     def roofline(self, ms, kernel_ms, peaks):
         return tensor_roofline("prefill_tc05_kernel", self.flops, kernel_ms, ms, peaks,
-                               TRAFFIC.get(self.c.name))
+                               traffic_for(self.c.name, "prefill_tc05_kernel"))
 
 
 class CsaFp8Decode:
@@ -487,30 +487,50 @@ class CsaFp8Decode:
 
     def roofline(self, ms, kernel_ms, peaks):
         # every flop of the call is in the tensor-core attention kernel
-        line = tensor_roofline("fp8_tc05_kernel" if self.c.Hq % 128 == 0 else "fp8_decode_kernel",
-                               self.flops, kernel_ms, ms, peaks, TRAFFIC.get(self.c.name))
+        kern = "fp8_tc05_kernel" if self.c.Hq % 128 == 0 else "fp8_decode_kernel"
+        line = tensor_roofline(kern, self.flops, kernel_ms, ms, peaks,
+                               traffic_for(self.c.name, kern))
         gbs = self.decode_bytes / (ms * 1e-3) / 1e9
         line.update(algorithmic_bytes=int(self.decode_bytes), call_hbm_gbs=round(gbs, 1),
                     call_hbm_frac=round(gbs / peaks["hbm_gbs"], 4))
         return line
 
 
-# DRAM bytes (read + write) per decode launch from an ncu capture of the
-# dominant kernel, keyed by workload; None until a capture of the current
-# kernel exists.
-TRAFFIC: dict = {
-    # gather_stream_kernel (TMA gather4), one launch, ncu dram read + write
-    "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": 271420645,
-    # fp8_tc05_kernel, one launch, ncu dram read + write (ncu flushes caches between
-    # kernels, so the 40 MB of decoded rows count from DRAM; live they come from L2)
-    "csa_fp8_b16_h128_d576_t65536_k2048_w128": 42660960,
-    # gather_stream_kernel (paged, TMA boxes), one launch: the 16-sequence capture
-    # (1,156.8 MB read + write over 282,062 context tokens) scaled by the context
-    # tokens of the full workload (2,171,044); the traffic grows with them
-    "paged_fp16_b128_h32_kv8_d128_ctx1k-32k_p16": 8903872744,
-    # prefill_tc05_kernel, one launch (Q, K, V read; Y and present K/V written)
-    "prefill_bf16_b4_s4096_h32_kv8_d128_causal_softcap50": 441644032,
+# DRAM bytes (read + write) per launch of the dominant kernel from an ncu
+# capture, keyed by workload, each with the hash of the kernel's source files
+# at capture time (kernel_source_hash): a value whose hash no longer matches
+# the current sources is reported as null (stale), never as a measurement.
+KERNEL_SOURCES = {
+    "gather_stream_kernel": ["k_stream.cu", "gather_common.cuh", "common.cuh", "tc05.cuh",
+                             "kernels.h"],
+    "fp8_tc05_kernel": ["k_fp8_tc.cu", "gather_common.cuh", "common.cuh", "tc05.cuh",
+                        "kernels.h"],
+    "fp8_decode_kernel": ["k_fp8.cu", "gather_common.cuh", "common.cuh", "kernels.h"],
+    "prefill_tc05_kernel": ["k_prefill.cu", "common.cuh", "tc05.cuh", "kernels.h"],
 }
+
+TRAFFIC: dict = {
+    # workload: (kernel, bytes per launch, source hash at capture, how)
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_top_kv_validate_gb300", "csrc")
+    for name in KERNEL_SOURCES.get(kernel, []):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload: str, kernel: str):
+    """ncu DRAM bytes per launch for this workload's dominant kernel, or None
+    when no capture of the current kernel source exists."""
+    rec = TRAFFIC.get(workload)
+    if not rec or rec[0] != kernel or rec[2] != kernel_source_hash(kernel):
+        return None
+    return rec[1]
 
 
 def hbm_roofline(kernel, kbytes, kernel_ms, call_bytes, call_ms, peaks, traffic):
@@ -739,38 +759,40 @@ def run_gpu(args):
         torch.distributed.destroy_process_group()
 
 
-def _oracle_threads(wl, rows, threads):
-    chunks = [rows[i::threads] for i in range(threads)]
-    out = [None] * threads
+class OraclePool:
+    """A persistent pool of host threads, one per core, each running the C
+    oracle (ctypes releases the GIL) on its share of the rows."""
 
-    def work(k):
-        if chunks[k]:
-            out[k] = wl.oracle_rows(chunks[k])
+    def __init__(self, wl, threads):
+        import concurrent.futures as cf
+        self.wl, self.threads = wl, threads
+        self.ex = cf.ThreadPoolExecutor(max_workers=threads)
 
-    ts = [threading.Thread(target=work, args=(k,)) for k in range(threads)]
-    for t in ts:
-        t.start()
-    for t in ts:
-        t.join()
+    def run(self, rows):
+        chunks = [rows[i::self.threads] for i in range(self.threads)]
+        list(self.ex.map(self.wl.oracle_rows, [ch for ch in chunks if ch]))
+
+    def close(self):
+        self.ex.shutdown(wait=True)
 
 
 def cpu_baseline(wl, args, budget_s: float = 10.0):
     """The fp64 oracle as it stands, on the host cores, over a bounded sample
-    of the same workload's rows (ctypes releases the GIL, so one Python thread
-    per core runs the C oracle in parallel)."""
+    of the same workload's rows (a persistent pool of one thread per core):
+    part of the step's rows, or whole passes over all of them repeated when
+    one pass is shorter than the budget."""
     cores = os.cpu_count() or 1
+    pool = OraclePool(wl, cores)
     wl.oracle_rows([0])  # stage host copies outside the timing
     rows_all = list(range(wl.rows))
     n = min(len(rows_all), cores * 4)
     t0 = time.perf_counter()
-    _oracle_threads(wl, rows_all[:n], cores)
+    pool.run(rows_all[:n])
     dt = time.perf_counter() - t0
-    # grow the sample toward the time budget: first within the step's rows,
-    # then whole passes over them when one pass is shorter than the budget
     if dt < budget_s and n < len(rows_all):
         n2 = min(len(rows_all), max(n, int(n * budget_s / max(dt, 1e-3))))
         t0 = time.perf_counter()
-        _oracle_threads(wl, rows_all[:n2], cores)
+        pool.run(rows_all[:n2])
         dt = time.perf_counter() - t0
         n = n2
     unit = "tokens/s" if isinstance(wl, Prefill) else "query-rows/s"
@@ -780,10 +802,11 @@ def cpu_baseline(wl, args, budget_s: float = 10.0):
         passes = min(1000, max(2, math.ceil(budget_s / max(dt, 1e-3))))
         t0 = time.perf_counter()
         for _ in range(passes):
-            _oracle_threads(wl, rows_all, cores)
+            pool.run(rows_all)
         dt = time.perf_counter() - t0
         n = passes * len(rows_all)
         sample = f"{passes} passes over all {wl.rows} {what} of one step"
+    pool.close()
     return {"value": round(n / dt, 2), "unit": unit, "cores": cores,
             "kind": "oracle", "sample": sample, "seconds": round(dt, 3)}
 
@@ -810,16 +833,30 @@ def run_reference(args):
 
     wl = HostWL(c)
     cores = os.cpu_count() or 1
-    per_step = cores  # one (batch, head) row per core per step: a bounded sample
+    pool = OraclePool(wl, cores)
     rows = list(range(wl.rows))
+    wl.oracle_rows([0])  # host copies staged outside the timing
+    # a step is one whole pass over the step's query rows; if K + W such passes
+    # would take more than about two minutes, each step takes an equal share
+    t0 = time.perf_counter()
+    pool.run(rows)
+    t_pass = time.perf_counter() - t0
+    per_step = len(rows)
+    budget = 120.0
+    if t_pass * (args.steps + args.warmup) > budget:
+        per_step = max(cores, int(len(rows) * budget / (t_pass * (args.steps + args.warmup))))
     for i in range(args.warmup):
-        _oracle_threads(wl, rows[(i * per_step) % wl.rows:][:per_step], cores)
+        s = (i * per_step) % wl.rows
+        pool.run((rows[s:] + rows[:s])[:per_step])
     t0 = time.perf_counter()
     for i in range(args.steps):
         s = (i * per_step) % wl.rows
-        _oracle_threads(wl, rows[s:s + per_step], cores)
+        pool.run((rows[s:] + rows[:s])[:per_step])
     dt = time.perf_counter() - t0
+    pool.close()
     value = args.steps * per_step / dt
+    sample = (f"{per_step} of the {wl.rows} query rows of the step per step" if per_step < wl.rows
+              else f"every step a whole pass over all {wl.rows} query rows")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "query-rows/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -828,8 +865,7 @@ def run_reference(args):
         "config": {"workload": c.name, "batch": c.B, "q_heads": c.Hq, "kv_heads": c.Hkv,
                    "head_dim": c.D, "cache_tokens": c.T, "top_k": c.K},
         "cpu_baseline": {"value": round(value, 2), "unit": "query-rows/s", "cores": cores,
-                         "kind": "oracle",
-                         "sample": f"{per_step} query rows of the workload per step"},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "query-rows/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

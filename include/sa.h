@@ -78,6 +78,12 @@ extern "C" {
 #define SA_ERRBIT_PAGE 128       /* paged: ctx_len or block-table entry invalid */
 #define SA_ERRBIT_TIMEOUT 256    /* a kernel's bounded wait for a copy ran out  */
 
+/* ---- sa_sparse_params.options bits ------------------------------------- */
+#define SA_OPT_ROW_COPIES 1u     /* dense f16/bf16 caches: fetch each K/V row with
+                                    its own bulk copy instead of TMA tensor maps */
+#define SA_OPT_FP8_WARP_MMA 2u   /* FP8 records: the warp-level MMA kernel (32-head
+                                    blocks) for every head count */
+
 /* Human-readable name of a status code (static string). */
 const char* sa_status_string(int status);
 
@@ -153,6 +159,8 @@ int build_present_kv(const void* past_k, const void* cur_k, void* present_k,
  *   C = valid prefix of idx[b, ih, i, :] (entries before the first -1);
  *   with window W > 0: C = [len_b - W, len_b) united with {j in C : j < len_b - W};
  *   s_j = scale * q . k_j;  s_j = softcap * tanh(s_j / softcap) if softcap != 0;
+ *   s_j += bias(b, h, i, j) when bias != NULL ([IS] index_share_row / bias_at:
+ *         keyed by the cache position j);
  *   s_j = -inf when j >= len_b (len_b = kv_len[b], or T), or causal and
  *         j > past_len + i;
  *   y = sum_j softmax(s)_j v_j, with exp(sink[h] - max) added to the
@@ -166,6 +174,14 @@ int build_present_kv(const void* past_k, const void* cur_k, void* present_k,
  *     V is the same decoded record (its first Dv dims); v_cache is ignored.
  *   idx [B, I, Sq, K] int32 or int64.  kv_len: nullable device int64 [B].
  *   sink: nullable device float [Hq] (natural-log logits).
+ *   bias: nullable device float32, dense row-major of shape
+ *     bias_dims[0 .. bias_rank-1] with 0 <= bias_rank <= 4, broadcast against
+ *     [B, Hq, Sq, T] from the right ([IS] validate_bias_shape: every axis is 1
+ *     or the extent it lines up with; otherwise SA_ERR_SHAPE).  Entries are
+ *     finite or -inf (a -inf masks its key); the bias counts only for the
+ *     candidate keys, each read at its cache position.
+ * options: 0, or SA_OPT_* bits choosing a kernel variant (the result is the
+ * same operation; tests use them to cover every path).
  * scale: 0 means 1/sqrt(D).  Index rows are validated on the device against
  * len_b when err_word != NULL (row_status nullable, as in validate_indices);
  * malformed rows never fault: negative entries are skipped, entries >= len_b
@@ -213,6 +229,11 @@ typedef struct {
   int64_t cur_len;
   void* workspace;
   size_t workspace_bytes;
+  const float* bias;
+  int64_t bias_rank;
+  int64_t bias_dims[4];
+  uint32_t options;
+  uint32_t reserved_;   /* must be 0 */
 } sa_sparse_params;
 
 size_t sparse_attn_decode_workspace(const sa_sparse_params* p);
@@ -234,11 +255,13 @@ int sparse_attn_decode(const sa_sparse_params* p, void* stream);
  * SA_ERR_SCRATCH_LIMIT before anything is enqueued.  Nothing is allocated or
  * freed.  The first call on each device looks up that buffer's device
  * address (once, with that device current); make that first call before any
- * stream capture.  Every call shares the buffer and it keeps the last call's
- * contents (the call needs none of it cleared: all scratch is written before
- * it is read), so calls that overlap on the GPU -- on different streams, or
- * from different threads, of the same device -- race and must be serialised
- * by the caller.
+ * stream capture.  The address is kept for the life of the process: a device
+ * reset (cudaDeviceReset) while the library is loaded is not supported by this
+ * entry point, since the kept address would then be stale.  Every call
+ * shares the buffer and it keeps the last call's contents (the call needs
+ * none of it cleared: all scratch is written before it is read), so calls
+ * that overlap on the GPU -- on different streams, or from different
+ * threads, of the same device -- race and must be serialised by the caller.
  */
 #define SA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int sparse_attn_decode_noalloc(const sa_sparse_params* p, void* stream);
@@ -299,7 +322,7 @@ typedef struct {
   const int32_t* ctx_len;
   void* y;
   int32_t dtype;
-  int32_t pad_;
+  uint32_t options;     /* 0, or SA_OPT_ROW_COPIES (pages fetched row by row) */
   int64_t B, Hq, Hkv, D, page_tokens, max_pages, num_pages;
   float scale;
   float pad2_;

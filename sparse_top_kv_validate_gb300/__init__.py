@@ -23,7 +23,7 @@ __all__ = [
     "validate_indices", "build_present_kv", "sparse_attn_decode", "attn_prefill",
     "paged_attn_decode", "sparse_attn_decode_workspace", "attn_prefill_workspace",
     "paged_attn_decode_workspace", "new_workspace", "sparse_attn_decode_noalloc",
-    "NOALLOC_SCRATCH_BYTES", "ERR_SCRATCH_LIMIT",
+    "NOALLOC_SCRATCH_BYTES", "ERR_SCRATCH_LIMIT", "OPT_ROW_COPIES", "OPT_FP8_WARP_MMA",
     "F32", "F16", "BF16", "FP8_E4M3_B64",
     "IDX_BELOW_SENTINEL", "IDX_AFTER_PADDING", "IDX_OUT_OF_RANGE", "IDX_NOT_INCREASING",
     "IDX_DUPLICATE", "IDX_ALL_PADDING", "ERRBIT_WRITE_POS", "ERRBIT_PAGE", "ERRBIT_TIMEOUT",
@@ -39,6 +39,7 @@ IDX_NOT_INCREASING, IDX_DUPLICATE, IDX_ALL_PADDING = 8, 16, 32
 ERRBIT_WRITE_POS, ERRBIT_PAGE, ERRBIT_TIMEOUT = 64, 128, 256
 ERR_SCRATCH_LIMIT = -9
 NOALLOC_SCRATCH_BYTES = 16 << 20
+OPT_ROW_COPIES, OPT_FP8_WARP_MMA = 1, 2
 
 _p = C.c_void_p
 _i64 = C.c_int64
@@ -57,6 +58,8 @@ class SparseParams(C.Structure):
         ("err_word", _p), ("row_status", _p),
         ("k_cur", _p), ("v_cur", _p), ("write_pos", _p), ("cur_len", _i64),
         ("workspace", _p), ("workspace_bytes", C.c_size_t),
+        ("bias", _p), ("bias_rank", _i64), ("bias_dims", _i64 * 4),
+        ("options", C.c_uint32), ("reserved_", C.c_uint32),
     ]
 
 
@@ -74,7 +77,7 @@ class PagedParams(C.Structure):
     _fields_ = [
         ("q", _p), ("k_pool", _p), ("v_pool", _p), ("k_new", _p), ("v_new", _p),
         ("block_table", _p), ("ctx_len", _p), ("y", _p),
-        ("dtype", _i32), ("pad_", _i32),
+        ("dtype", _i32), ("options", C.c_uint32),
         ("B", _i64), ("Hq", _i64), ("Hkv", _i64), ("D", _i64), ("page_tokens", _i64),
         ("max_pages", _i64), ("num_pages", _i64),
         ("scale", C.c_float), ("pad2_", C.c_float),
@@ -272,7 +275,7 @@ def build_present_kv(cur_k, present_k, past_k=None, cur_v=None, present_v=None, 
 
 def _sparse_params(q, k_cache, v_cache, idx, y, *, scale, softcap, window, kv_len, past_len,
                    causal, sink, err_word, row_status, n_rope=0, Dv=None, k_cur=None,
-                   v_cur=None, write_pos=None):
+                   v_cur=None, write_pos=None, bias=None, options=0):
     p = SparseParams()
     B, Hq, Sq, D = q.shape
     p.q, p.y = q.data_ptr(), _ptr(y)
@@ -307,6 +310,13 @@ def _sparse_params(q, k_cache, v_cache, idx, y, *, scale, softcap, window, kv_le
     p.row_status = _ptr(row_status)
     p.k_cur, p.v_cur, p.write_pos = _ptr(k_cur), _ptr(v_cur), _ptr(write_pos)
     p.cur_len = 0 if k_cur is None else k_cur.shape[2]
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.dim() > 4:
+            raise ValueError("bias must be float32 of rank <= 4")
+        p.bias, p.bias_rank = bias.data_ptr(), bias.dim()
+        for r, e in enumerate(bias.shape):
+            p.bias_dims[r] = e
+    p.options = int(options)
     return p
 
 
@@ -318,7 +328,7 @@ def sparse_attn_decode_workspace(q, k_cache, v_cache, idx, **kw) -> int:
 def _sparse_defaults(kw):
     d = dict(scale=0.0, softcap=0.0, window=0, kv_len=None, past_len=0, causal=False, sink=None,
              err_word=None, row_status=None, n_rope=0, Dv=None, k_cur=None, v_cur=None,
-             write_pos=None)
+             write_pos=None, bias=None, options=0)
     d.update(kw)
     return d
 
@@ -330,14 +340,16 @@ def sparse_attn_decode(q, k_cache, v_cache, idx, *, y=None, workspace=None, stre
     ``n_rope``); ``idx [B,I,Sq,K]`` int32/int64.  Keyword options: scale,
     softcap, window, kv_len (int64 [B]), past_len, causal, sink (float32
     [Hq]), err_word (int32 [1], caller-zeroed), row_status (uint8 [B*I*Sq]),
-    n_rope, Dv, and the fused append k_cur / v_cur ([B,Hkv,C,D]) with
-    write_pos (int64 [B], default T - C).  Returns ``y [B,Hq,Sq,Dv]``."""
+    n_rope, Dv, the fused append k_cur / v_cur ([B,Hkv,C,D]) with
+    write_pos (int64 [B], default T - C), bias (float32, rank <= 4,
+    broadcast against [B,Hq,Sq,T]: added to the score of cache position j)
+    and options (OPT_* bits).  Returns ``y [B,Hq,Sq,Dv]``."""
     L = load()
     kw = _sparse_defaults(kw)
     for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("idx", idx),
                  ("kv_len", kw["kv_len"]), ("sink", kw["sink"]), ("err_word", kw["err_word"]),
                  ("row_status", kw["row_status"]), ("k_cur", kw["k_cur"]), ("v_cur", kw["v_cur"]),
-                 ("write_pos", kw["write_pos"])):
+                 ("write_pos", kw["write_pos"]), ("bias", kw["bias"])):
         _dev(t, n)
     B, Hq, Sq, D = q.shape
     Dv = kw["Dv"] if k_cache.dtype == torch.uint8 else v_cache.shape[3]
@@ -388,7 +400,8 @@ def attn_prefill(q, k, v, *, causal=True, scale=0.0, softcap=0.0, y=None, presen
     return y
 
 
-def _paged_params(q, k_pool, v_pool, block_table, ctx_len, y, k_new, v_new, scale, err_word):
+def _paged_params(q, k_pool, v_pool, block_table, ctx_len, y, k_new, v_new, scale, err_word,
+                  options=0):
     p = PagedParams()
     B, Hq = q.shape[0], q.shape[1]
     D = q.shape[-1]
@@ -400,6 +413,7 @@ def _paged_params(q, k_pool, v_pool, block_table, ctx_len, y, k_new, v_new, scal
     p.page_tokens, p.max_pages, p.num_pages = k_pool.shape[2], block_table.shape[1], k_pool.shape[0]
     p.scale = float(scale)
     p.err_word = _ptr(err_word)
+    p.options = int(options)
     return p
 
 
@@ -409,7 +423,8 @@ def paged_attn_decode_workspace(q, k_pool, v_pool, block_table, ctx_len, scale=0
 
 
 def paged_attn_decode(q, k_pool, v_pool, block_table, ctx_len, *, k_new=None, v_new=None,
-                      scale=0.0, err_word=None, y=None, workspace=None, stream=None):
+                      scale=0.0, err_word=None, y=None, workspace=None, stream=None,
+                      options=0):
     """Paged causal decode: ``q [B,Hq,1,D]`` (or ``[B,Hq,D]``), pools
     ``[num_pages,Hkv,page_tokens,D]``, ``block_table int32 [B,max_pages]``,
     ``ctx_len int32 [B]``; optional ``k_new/v_new [B,Hkv,D]`` written at token
@@ -423,7 +438,8 @@ def paged_attn_decode(q, k_pool, v_pool, block_table, ctx_len, *, k_new=None, v_
         raise TypeError("block_table and ctx_len must be int32")
     if y is None:
         y = torch.empty_like(q)
-    p = _paged_params(q, k_pool, v_pool, block_table, ctx_len, y, k_new, v_new, scale, err_word)
+    p = _paged_params(q, k_pool, v_pool, block_table, ctx_len, y, k_new, v_new, scale, err_word,
+                      options)
     need = int(L.paged_attn_decode_workspace(C.byref(p)))
     ws, nb = _workspace(need, q.device, workspace)
     p.workspace, p.workspace_bytes = _ptr(ws), nb
@@ -440,7 +456,7 @@ def sparse_attn_decode_noalloc(q, k_cache, v_cache, idx, *, y=None, stream=None,
     for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("idx", idx),
                  ("kv_len", kw["kv_len"]), ("sink", kw["sink"]), ("err_word", kw["err_word"]),
                  ("row_status", kw["row_status"]), ("k_cur", kw["k_cur"]), ("v_cur", kw["v_cur"]),
-                 ("write_pos", kw["write_pos"])):
+                 ("write_pos", kw["write_pos"]), ("bias", kw["bias"])):
         _dev(t, n)
     B, Hq, Sq, D = q.shape
     Dv = kw["Dv"] if k_cache.dtype == torch.uint8 else v_cache.shape[3]

@@ -133,6 +133,12 @@ __global__ void __launch_bounds__(128) gather_simt_kernel(GatherArgs a) {
     float x;
     if (a.softcap != 0.f) x = a.softcap * tanhf(dot * (sl2 / kLog2e) * a.inv_softcap) * kLog2e;
     else x = dot * sl2;
+    if (a.bias) {  // [IS] bias_at, keyed by the cache position (sparse source only)
+      const int64_t j = row - (u.b * a.Hkv + u.kvh) * a.T;
+      x += kLog2e * __ldg(a.bias + u.b * a.bias_sb + h * a.bias_sh + u.i * a.bias_si +
+                          j * a.bias_sk);
+      if (x == SA_NEG_INF) continue;  // a -inf entry masks the key
+    }
     const float mn = fmaxf(m, x);
     const float al = exp2f(m - mn);  // m == -inf -> 0
     const float p = exp2f(x - mn);

@@ -843,17 +843,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side -----------------------------------------------------------------------------
 
-// SA_FP8_KERNEL=mma selects the warp-level MMA kernel for every head count.
-static bool tc_disabled() {
-  const char* v = std::getenv("SA_FP8_KERNEL");
-  return v && std::strcmp(v, "mma") == 0;
-}
-
 int fp8_tc_max_tiles() { return kMaxTiles; }
 size_t fp8_tc_decoded_row_bytes() { return kRowBytes; }
 
 bool fp8_tc_supported(const GatherArgs& g) {
-  if (tc_disabled()) return false;
+  if (g.fp8_warp_mma) return false;  // the caller asked for the warp-level MMA kernel
+  if (g.bias) return false;          // an additive bias runs on the warp-level MMA kernel
   if (g.D != kD || g.Dv != kD || g.Hkv != 1 || g.Hq % kHeads != 0) return false;
   if (!(g.scale_log2 > 0.0f) || !std::isfinite(g.scale_log2)) return false;  // monotone logits
   if (g.n_cand < 1 || g.record_stride < 648 || g.record_stride % 8 != 0) return false;

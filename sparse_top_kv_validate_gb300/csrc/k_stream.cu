@@ -494,6 +494,14 @@ __global__ void __launch_bounds__(SGeo<D, kTma>::kThreads, 1)
           mma16816<T>(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
       }
     }
+    // additive bias ([IS] bias_at): keyed by the cache positions of this
+    // lane's accumulator rows (keys gid and gid + 8 of the tile)
+    int32_t j_lo = -1, j_hi = -1;
+    if (a.bias) {
+      const int64_t c0 = cur.prow + (t - cur.tu.off) * 16 + gid;
+      if (v_lo) j_lo = __ldg(a.pos + c0);
+      if (v_hi) j_hi = __ldg(a.pos + c0 + 8);
+    }
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -502,6 +510,13 @@ __global__ void __launch_bounds__(SGeo<D, kTma>::kThreads, 1)
         float x = s[nt][e];
         if (cap != 0.f) x = cap * tanh_fast(x * (sl2 * (1.0f / kLog2e)) * inv_cap) * kLog2e;
         else x = x * sl2;
+        if (a.bias) {
+          const int32_t j = (e < 2) ? j_lo : j_hi;
+          const int hh = nt * 8 + 2 * tig + (e & 1);
+          if (j >= 0 && hh < a.hpu)
+            x += kLog2e * __ldg(a.bias + cur.ui.b * a.bias_sb + (cur.ui.h0 + hh) * a.bias_sh +
+                                cur.ui.i * a.bias_si + j * a.bias_sk);
+        }
         s[nt][e] = ((e < 2) ? v_lo : v_hi) ? x : SA_NEG_INF;
       }
       float tm0 = fmaxf(s[nt][0], s[nt][2]);
@@ -743,8 +758,7 @@ static int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t
 // boxes one row high for tile::gather4.  All in the 128-byte swizzle.  False
 // when the tensors cannot be described (then the per-row copies are used).
 static bool kv_maps(const GatherArgs& a, int dtype, CUtensorMap* tk, CUtensorMap* tv) {
-  const char* env = std::getenv("SA_STREAM_TMA");  // "0": the per-row copies for every source
-  if (env && std::strcmp(env, "0") == 0) return false;
+  if (a.row_copies) return false;  // the caller asked for the per-row copies
   if (a.D != 64 && a.D != 128 && a.D != 256) return false;
   if (a.source == kPaged && a.page_tokens % 16 != 0) return false;
   const int64_t rows =

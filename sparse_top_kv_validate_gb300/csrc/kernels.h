@@ -74,6 +74,9 @@ struct GatherArgs {
   const void* v;
   void* y;                    // [B, Hq, Sq, Dv]
   const float* sink;          // nullable [Hq]
+  const float* bias;          // nullable: additive bias, element (b,h,i,j) at
+  int64_t bias_sb, bias_sh;   //   b*bias_sb + h*bias_sh + i*bias_si + j*bias_sk
+  int64_t bias_si, bias_sk;   //   (broadcast axes have stride 0)
   float* part_o;              // unnormalised partial outputs (layout per kernel)
   float* part_ml;             // partial running max (log2 units) and sum
   uint32_t* err_word;
@@ -115,6 +118,8 @@ struct GatherArgs {
   void* fp8_kdec;             // tcgen05 FP8 path: decoded rows [units, n_cand_pad, 576] bf16
   int fp8_own_positions;      // tcgen05 FP8 path: the decode kernel writes pos itself
   int fp8_after_plan;         //   and the plan kernel (validation only) runs just before it
+  int row_copies;             // stream kernel: per-row bulk copies, no tensor maps
+  int fp8_warp_mma;           // FP8 records: the warp-level MMA kernel only
   void* ev_before;            // nullable cudaEvent_t pair recorded around the dominant kernel
   void* ev_after;
   // math

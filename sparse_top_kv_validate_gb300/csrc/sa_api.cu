@@ -269,9 +269,38 @@ int run_plan(Plan& pl, int dtype, cudaStream_t st) {
 
 // ---- sparse decode: checks + plan ----------------------------------------------
 
+// [IS] validate_bias_shape: rank <= 4, each axis 1 or the extent of the axis
+// of [B, Hq, Sq, T] it lines up with from the right.  On success the element
+// strides of the four logical axes (0 on broadcast axes) go to st.
+bool bias_strides(const sa_sparse_params* p, int64_t st[4]) {
+  const int64_t target[4] = {p->B, p->Hq, p->Sq, p->T};
+  if (p->bias_rank < 0 || p->bias_rank > 4) return false;
+  const int r = static_cast<int>(p->bias_rank);
+  int64_t run = 1;
+  for (int ax = 3; ax >= 0; --ax) {
+    const int k = ax - (4 - r);  // index into bias_dims, < 0 for a missing leading axis
+    if (k < 0) {
+      st[ax] = 0;
+      continue;
+    }
+    const int64_t e = p->bias_dims[k];
+    if (e != 1 && e != target[ax]) return false;
+    st[ax] = (e == 1) ? 0 : run;
+    run *= e;
+  }
+  return true;
+}
+
 // `query` = 1 for a workspace-size query, which needs no output pointer.
 int check_sparse(const sa_sparse_params* p, int query = 0) {
   if (!p || !p->q || !p->k_cache || (!p->y && !query)) return SA_ERR_NULL;
+  if (p->reserved_ != 0 || (p->options & ~(SA_OPT_ROW_COPIES | SA_OPT_FP8_WARP_MMA)))
+    return SA_ERR_UNSUPPORTED;
+  if (p->bias) {
+    int64_t st[4];
+    if (!bias_strides(p, st)) return SA_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(p->bias) % 4) return SA_ERR_ALIGN;
+  }
   if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->Sq <= 0 || p->D <= 0 || p->T <= 0)
     return SA_ERR_SHAPE;
   if (p->Hq % p->Hkv != 0) return SA_ERR_SHAPE;
@@ -328,6 +357,17 @@ int sparse_plan(const sa_sparse_params* p, Plan& pl) {
   g.sink = p->sink;
   g.err_word = p->err_word;
   g.source = sa::kSparse;
+  if (p->bias) {
+    int64_t st[4];
+    bias_strides(p, st);  // checked by check_sparse
+    g.bias = p->bias;
+    g.bias_sb = st[0];
+    g.bias_sh = st[1];
+    g.bias_si = st[2];
+    g.bias_sk = st[3];
+  }
+  g.row_copies = (p->options & SA_OPT_ROW_COPIES) ? 1 : 0;
+  g.fp8_warp_mma = (p->options & SA_OPT_FP8_WARP_MMA) ? 1 : 0;
   g.B = p->B;
   g.Hq = p->Hq;
   g.Hkv = p->Hkv;
@@ -704,6 +744,7 @@ static int check_paged(const sa_paged_params* p, int query = 0) {
     return SA_ERR_SHAPE;
   if (p->Hq % p->Hkv != 0) return SA_ERR_SHAPE;
   if (dtype_bytes(p->dtype) == 0) return SA_ERR_DTYPE;
+  if (p->options & ~SA_OPT_ROW_COPIES) return SA_ERR_UNSUPPORTED;
   if (p->num_pages * p->Hkv * p->page_tokens >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
   if (!std::isfinite(p->scale)) return SA_ERR_SHAPE;
   const size_t es = dtype_bytes(p->dtype);
@@ -736,6 +777,7 @@ static void paged_args(const sa_paged_params* p, sa::GatherArgs& g) {
   g.max_pages = p->max_pages;
   g.num_pages = p->num_pages;
   g.n_cand = p->max_pages * p->page_tokens;
+  g.row_copies = (p->options & SA_OPT_ROW_COPIES) ? 1 : 0;
   const float scale = p->scale != 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->D));
   g.scale_log2 = scale * 1.4426950408889634f;
 }

@@ -303,11 +303,9 @@ def make_sparse_inputs(c: SparseCase, seed: int, device="cpu") -> dict:
         out["k_cur"] = out["k_cache"][:, :, c.T - c.cur:, :].clone()
         out["v_cur"] = out["v_cache"][:, :, c.T - c.cur:, :].clone()
     rows = c.B * c.I
-    if c.window:
-        high = c.T - c.window
-    else:
-        high = c.T
-    idx = sorted_sample_rows(rows, 0, high, c.K, seed * 7919 + 4, device)
+    # the selected indices are drawn from the whole cache, also with a window:
+    # entries inside the window overlap it (about K * window / T per row)
+    idx = sorted_sample_rows(rows, 0, c.T, c.K, seed * 7919 + 4, device)
     if c.pad_prob > 0 and c.pad_max > 0:
         idx = pad_tails(idx, seed * 7919 + 5, c.pad_prob, c.pad_max, c.pad_min)
     idx = idx.reshape(c.B, c.I, 1, c.K)

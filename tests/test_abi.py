@@ -234,3 +234,43 @@ def test_workspace_query_needs_no_output_pointer(lib):
     p.B, p.Hq, p.Hkv, p.Sq, p.D, p.Dv, p.T, p.I, p.K = 4, 64, 8, 1, 128, 128, 8192, 8, 2048
     p.q_dtype = p.kv_dtype = sa.BF16
     assert lib.sparse_attn_decode_workspace(C.byref(p)) > 0
+
+
+def _dense_params():
+    p = sa.SparseParams()
+    p.q, p.k_cache, p.v_cache, p.y, p.idx = 0x100000, 0x10000000, 0x20000000, 0x200000, 0x300000
+    p.B, p.Hq, p.Hkv, p.Sq, p.D, p.Dv, p.T, p.I, p.K = 2, 8, 2, 1, 128, 128, 100, 2, 16
+    p.q_dtype = p.kv_dtype = sa.BF16
+    p.bias = 0x400000
+    return p
+
+
+@pytest.mark.parametrize("dims,status", [
+    ((9,), -2),               # the last axis lines up with T = 100
+    ((3, 1, 100), -2),        # 3 is neither 1 nor Hq = 8
+    ((2, 8, 1, 100, 1), -2),  # rank 5
+    ((2, 8, 2, 100), -2),     # Sq is 1
+])
+def test_bias_shapes_that_do_not_broadcast_are_refused(host_lib, dims, status):
+    # [IS] validate_bias_shape: rank <= 4, every axis 1 or its target extent.
+    p = _dense_params()
+    p.bias_rank = len(dims)
+    for r, e in enumerate(dims[:4]):
+        p.bias_dims[r] = e
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == status
+    assert host_lib.sparse_attn_decode_workspace(C.byref(p)) == 0
+
+
+def test_unknown_option_bits_and_misaligned_bias_are_refused(host_lib):
+    p = _dense_params()
+    p.bias_rank, p.bias_dims[0] = 1, 100
+    p.options = 4
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -7
+    p.options, p.reserved_ = 0, 1
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -7
+    p.reserved_ = 0
+    p.bias = 0x400002
+    assert host_lib.sparse_attn_decode(C.byref(p), None) == -4
+    g = _paged_params()
+    g.options = 2
+    assert host_lib.paged_attn_decode(C.byref(g), None) == -7

@@ -70,13 +70,12 @@ def test_paged_slots_past_the_context_never_reach_the_output(cuda_lib, dt, page_
     assert_close(to64(y), ref, y.dtype, f"paged NaN tail {dt} p{page_tokens}")
 
 
-def test_paged_row_copy_path_matches_oracle(cuda_lib, monkeypatch):
-    """SA_STREAM_TMA=0: pages fetched row by row instead of as TMA boxes."""
-    monkeypatch.setenv("SA_STREAM_TMA", "0")
+def test_paged_row_copy_path_matches_oracle(cuda_lib):
+    """OPT_ROW_COPIES: pages fetched row by row instead of as TMA boxes."""
     c, inp = _paged_small("f16", seed=7, page_tokens=32, ctx_high=600)
     y = cuda_lib.paged_attn_decode(inp["q"].to(DEV), inp["k_pool"].to(DEV), inp["v_pool"].to(DEV),
                                    inp["block_table"].to(DEV), inp["ctx_len"].to(DEV),
-                                   scale=c.eff_scale())
+                                   scale=c.eff_scale(), options=cuda_lib.OPT_ROW_COPIES)
     torch.cuda.synchronize()
     ref = oracle.paged_decode(inp["q"], inp["k_pool"], inp["v_pool"], inp["block_table"],
                               inp["ctx_len"], page_tokens=c.page_tokens, scale=c.eff_scale())

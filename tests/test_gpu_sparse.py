@@ -320,14 +320,14 @@ def test_workspace_contents_on_entry_do_not_matter(cuda_lib):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
-def test_stream_row_copy_path_matches_oracle(cuda_lib, dt, monkeypatch):
-    """SA_STREAM_TMA=0: the stream kernel's per-row bulk copies (the path taken
+def test_stream_row_copy_path_matches_oracle(cuda_lib, dt):
+    """OPT_ROW_COPIES: the stream kernel's per-row bulk copies (the path taken
     when the caches cannot be described by tensor maps) for selected rows."""
-    monkeypatch.setenv("SA_STREAM_TMA", "0")
     c = synth.sparse_bf16(B=3, T=2000, K=500, dtype=dt, pad_prob=0.5, pad_max=100)
     inp = synth.make_sparse_inputs(c, seed=33)
     y = cuda_lib.sparse_attn_decode(inp["q"].to(DEV), inp["k_cache"].to(DEV), inp["v_cache"].to(DEV),
-                                    inp["idx"].to(DEV), scale=c.eff_scale())
+                                    inp["idx"].to(DEV), scale=c.eff_scale(),
+                                    options=cuda_lib.OPT_ROW_COPIES)
     torch.cuda.synchronize()
     ref = oracle.sparse_attention(inp["q"], inp["idx"], inp["k_cache"], inp["v_cache"],
                                   scale=c.eff_scale())
@@ -572,7 +572,12 @@ def test_full_size_fp8_sampled_rows(cuda_lib):
                                     err_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    for b in (0, 11):
+    # the sampled batches' rows hold selected entries inside the window, which
+    # the union must count once
+    inside = (inp["idx"][:, 0, 0] >= c.T - c.window).sum(dim=1).cpu()
+    overlapping = [b for b in range(c.B) if int(inside[b]) > 0]
+    assert overlapping
+    for b in sorted({0, 11, overlapping[0]}):
         heads = list(range(0, c.Hq, 9))
         ref = oracle.sparse_attention(inp["q"][b:b + 1].cpu(), inp["idx"][b:b + 1].cpu(),
                                       records=inp["kv_records"][b:b + 1].cpu(), n_rope=c.n_rope,

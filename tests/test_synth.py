@@ -73,3 +73,18 @@ def test_fp8_records_layout_and_block_exponents():
     err = (vals - x).abs()
     assert bool((err <= x.abs() * 2.0 ** -4 + torch.exp2(e.double() - 9)[:, :, None]).all())
     assert np.isfinite(vals.numpy()).all()
+
+
+def test_window_workload_index_rows_overlap_the_window():
+    # The FP8 latent workload unites a 128-token window with 2,048 indices
+    # drawn from all 65,536 positions: about 2048 * 128 / 65536 = 4 selected
+    # entries per row fall inside the window and must be counted once.
+    c = synth.csa_fp8()
+    idx = synth.sorted_sample_rows(c.B * c.I, 0, c.T, c.K, seed=1 * 7919 + 4)
+    inside = (idx >= c.T - c.window).sum(dim=1)
+    assert int(inside.sum()) > 0
+    assert 1.0 <= float(inside.double().mean()) <= 10.0
+    # make_sparse_inputs draws them that way
+    small = synth.csa_fp8(B=4, T=600, K=300)
+    inp = synth.make_sparse_inputs(small, seed=2)
+    assert int((inp["idx"] >= small.T - small.window).sum()) > 0
