@@ -189,7 +189,9 @@ __device__ __forceinline__ int64_t key_row(const GatherArgs& a, const KeyRef& k)
   return static_cast<int64_t>(k.raw) * a.Hkv * a.page_tokens + k.base;
 }
 
-template <typename T, int D, int NT, bool kTma>
+// kBias: the request carries an additive bias (a separate instance, so that
+// the common bias-free kernel keeps its registers).
+template <typename T, int D, int NT, bool kTma, bool kBias>
 __global__ void __launch_bounds__(SGeo<D, kTma>::kThreads, 1)
     gather_stream_kernel(const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, GatherArgs a) {
@@ -497,7 +499,7 @@ __global__ void __launch_bounds__(SGeo<D, kTma>::kThreads, 1)
     // additive bias ([IS] bias_at): keyed by the cache positions of this
     // lane's accumulator rows (keys gid and gid + 8 of the tile)
     int32_t j_lo = -1, j_hi = -1;
-    if (a.bias) {
+    if (kBias) {
       const int64_t c0 = cur.prow + (t - cur.tu.off) * 16 + gid;
       if (v_lo) j_lo = __ldg(a.pos + c0);
       if (v_hi) j_hi = __ldg(a.pos + c0 + 8);
@@ -510,7 +512,7 @@ __global__ void __launch_bounds__(SGeo<D, kTma>::kThreads, 1)
         float x = s[nt][e];
         if (cap != 0.f) x = cap * tanh_fast(x * (sl2 * (1.0f / kLog2e)) * inv_cap) * kLog2e;
         else x = x * sl2;
-        if (a.bias) {
+        if (kBias) {
           const int32_t j = (e < 2) ? j_lo : j_hi;
           const int hh = nt * 8 + 2 * tig + (e & 1);
           if (j >= 0 && hh < a.hpu)
@@ -783,27 +785,34 @@ static bool kv_maps(const GatherArgs& a, int dtype, CUtensorMap* tk, CUtensorMap
   return true;
 }
 
-template <typename T, int D, int NT>
-static int launch_stream_t(const GatherArgs& a, int dtype, int grid, cudaStream_t st) {
+template <typename T, int D, int NT, bool kBias>
+static int launch_stream_b(const GatherArgs& a, int dtype, int grid, cudaStream_t st) {
   CUtensorMap tk, tv;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
   if (kv_maps(a, dtype, &tk, &tv)) {
     const size_t smem = smem_bytes_t<D, true>(a.source, a.B);
-    if (cudaFuncSetAttribute(gather_stream_kernel<T, D, NT, true>,
+    if (cudaFuncSetAttribute(gather_stream_kernel<T, D, NT, true, kBias>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return -1;
-    return launch_pdl(gather_stream_kernel<T, D, NT, true>, dim3(grid),
+    return launch_pdl(gather_stream_kernel<T, D, NT, true, kBias>, dim3(grid),
                       dim3(SGeo<D, true>::kThreads), smem, st, tk, tv, a);
   }
   const size_t smem = smem_bytes_t<D, false>(a.source, a.B);
-  if (cudaFuncSetAttribute(gather_stream_kernel<T, D, NT, false>,
+  if (cudaFuncSetAttribute(gather_stream_kernel<T, D, NT, false, kBias>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return -1;
-  return launch_pdl(gather_stream_kernel<T, D, NT, false>, dim3(grid),
+  return launch_pdl(gather_stream_kernel<T, D, NT, false, kBias>, dim3(grid),
                     dim3(SGeo<D, false>::kThreads), smem, st, tk, tv, a);
+}
+
+template <typename T, int D, int NT>
+static int launch_stream_t(const GatherArgs& a, int dtype, int grid, cudaStream_t st) {
+  // the bias is keyed by planned positions: selected-token requests only
+  if (a.bias && a.source == kSparse) return launch_stream_b<T, D, NT, true>(a, dtype, grid, st);
+  return launch_stream_b<T, D, NT, false>(a, dtype, grid, st);
 }
 
 int launch_gather_stream(const GatherArgs& a, int dtype, int grid, cudaStream_t st) {
