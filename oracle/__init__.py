@@ -46,7 +46,8 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp,
+                    _SRC, "-lm"],
                    check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -63,6 +64,18 @@ class _SparseArgs(C.Structure):
         ("record_bytes", _i64), ("n_rope", _i64),
         ("bias", _p), ("bias_rank", _i64), ("bias_dims", _i64 * 4),
     ]
+
+
+class _SelectArgs(C.Structure):
+    _fields_ = [
+        ("query", _p), ("weight", _p), ("keys", _p),
+        ("B", _i64), ("S", _i64), ("IH", _i64), ("ID", _i64), ("R", _i64), ("topk", _i64),
+        ("key_stride", _i64), ("query_start", _i64), ("query_start_b", _p),
+        ("out_heads", _i64), ("ascending", C.c_int),
+    ]
+
+
+SEL_TIE, SEL_NONFINITE = 1, 2
 
 
 def lib():
@@ -95,6 +108,20 @@ def lib():
             L.orc_prefill.restype = C.c_int
             L.orc_prefill.argtypes = [_p, _p, _p, C.c_int, _i64, _i64, _i64, _i64, _i64,
                                       C.c_int, C.c_double, C.c_double, _p, _i64, _p]
+            L.orc_e2m1_to_double.restype = C.c_double
+            L.orc_e2m1_to_double.argtypes = [C.c_uint8]
+            L.orc_round_bf16.restype = C.c_float
+            L.orc_round_bf16.argtypes = [C.c_float]
+            L.orc_fp4_quantize_block.restype = None
+            L.orc_fp4_quantize_block.argtypes = [_p, _p, _p]
+            L.orc_fp4_element.restype = C.c_float
+            L.orc_fp4_element.argtypes = [C.c_uint8, _p, C.c_int]
+            L.orc_hadamard_bf16.restype = None
+            L.orc_hadamard_bf16.argtypes = [_p, _i64]
+            L.orc_index_query_finalize.restype = None
+            L.orc_index_query_finalize.argtypes = [_p, _i64, _p]
+            L.orc_index_select.restype = C.c_int
+            L.orc_index_select.argtypes = [C.POINTER(_SelectArgs), _p, _p, _p, _p]
             L.orc_paged_decode.restype = C.c_int
             L.orc_paged_decode.argtypes = [_p, _p, _p, C.c_int, _p, _p, _i64, _i64, _i64,
                                            _i64, _i64, _i64, C.c_double, _p, _i64, _p]
@@ -303,3 +330,76 @@ def paged_decode(q, k_pool, v_pool, block_table, ctx_len, *, page_tokens: int,
     if rc != 0:
         raise ValueError("oracle rejected the paged shape")
     return y
+
+
+# ---------------------------------------------------------------------------
+# ratio-4 index scoring and top-k selection
+# ---------------------------------------------------------------------------
+
+def e2m1_to_double(nibble: int) -> float:
+    return lib().orc_e2m1_to_double(nibble)
+
+
+def round_bf16(x: float) -> float:
+    return lib().orc_round_bf16(x)
+
+
+def fp4_quantize_block(x):
+    """32 float32 values -> (E8M0 scale byte, 16 packed bytes, the 32
+    dequantized values as float32)."""
+    xh = _host(torch.as_tensor(x, dtype=torch.float32))
+    assert xh.numel() == 32
+    sb = C.c_uint8(0)
+    packed = (C.c_uint8 * 16)()
+    lib().orc_fp4_quantize_block(xh.data_ptr(), C.addressof(sb), C.addressof(packed))
+    vals = np.array([lib().orc_fp4_element(sb.value, C.addressof(packed), i) for i in range(32)],
+                    dtype=np.float32)
+    return sb.value, bytes(packed), vals
+
+
+def hadamard_bf16(x) -> np.ndarray:
+    v = np.array(x, dtype=np.float32).copy()
+    lib().orc_hadamard_bf16(v.ctypes.data, v.size)
+    return v
+
+
+def index_query_finalize(x) -> np.ndarray:
+    v = np.array(x, dtype=np.float32).copy()
+    out = np.zeros_like(v)
+    lib().orc_index_query_finalize(v.ctypes.data, v.size, out.ctypes.data)
+    return out
+
+
+def index_select(query, weight, keys, *, topk: int, query_start: int = 0,
+                 query_start_b=None, out_heads: int = 1, ascending: bool = False,
+                 want_scores: bool = False):
+    """Ratio-4 index selection; see ``orc_index_select``.
+
+    query float32 ``[B, S, IH, ID]``, weight float32 ``[B, S, IH]``, keys uint8
+    ``[B, R, key_stride]``.  Returns ``(selected int32 [B, out_heads, S, topk],
+    status uint8 [B*S], err)`` and, with ``want_scores``, float32 scores
+    ``[B, S, R]``."""
+    qh = _host(torch.as_tensor(query, dtype=torch.float32))
+    wh = _host(torch.as_tensor(weight, dtype=torch.float32))
+    kh = _host(torch.as_tensor(keys, dtype=torch.uint8))
+    B, S, IH, ID = qh.shape
+    R, stride = kh.shape[1], kh.shape[2]
+    a = _SelectArgs()
+    a.query, a.weight, a.keys = qh.data_ptr(), wh.data_ptr(), kh.data_ptr()
+    a.B, a.S, a.IH, a.ID, a.R, a.topk, a.key_stride = B, S, IH, ID, R, topk, stride
+    a.query_start = int(query_start)
+    qsb = None if query_start_b is None else _host(torch.as_tensor(query_start_b,
+                                                                   dtype=torch.int64))
+    a.query_start_b = _ptr(qsb)
+    a.out_heads, a.ascending = int(out_heads), int(bool(ascending))
+    sel = np.zeros((B, out_heads, S, topk), dtype=np.int32)
+    status = np.zeros(B * S, dtype=np.uint8)
+    err = C.c_uint32(0)
+    scores = np.zeros((B, S, R), dtype=np.float32) if want_scores else None
+    rc = lib().orc_index_select(C.byref(a), sel.ctypes.data, status.ctypes.data,
+                                C.addressof(err), None if scores is None else scores.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle rejected the index selection shape")
+    if want_scores:
+        return sel, status, err.value, scores
+    return sel, status, err.value

@@ -622,3 +622,337 @@ int orc_paged_decode(const void* q, const void* k_pool, const void* v_pool, int 
   free(qr);
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Ratio-4 index scoring and top-k selection.                                */
+/*                                                                          */
+/* [CSA-CPU] onnx-runtime-ep-cpu compressed_sparse_attention.rs:            */
+/*   finalize_index_query, hadamard_bf16, fp4_roundtrip, select_ratio4_topk; */
+/* [CSA] onnx-runtime-ep-cuda compressed_sparse_attention.rs:               */
+/*   csa_ratio4_index_select (same steps on the device),                    */
+/*   csa_ratio4_index_replicate (one shared set per index head).            */
+/* OCP MX specification v1.0: E2M1 element encoding and the conversion of   */
+/* a block of 32 scalars to an E8M0 scale plus elements.                    */
+/*                                                                          */
+/* The pages carry these steps out in binary32 arithmetic (plain f32 adds   */
+/* and multiplies, bf16 rounding after the Hadamard transform), and the      */
+/* results are integer decisions (FP4 codes, the order of scores), so this   */
+/* section computes in float, in the pages' order, and does not widen to    */
+/* double.  The build passes -ffp-contract=off: no step is fused.           */
+/* ------------------------------------------------------------------------ */
+
+#define ORC_SEL_TIE 1       /* two scores of the row compare equal           */
+#define ORC_SEL_NONFINITE 2 /* a score is NaN or infinite                    */
+
+/* OCP E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa bit; exponent field 0
+ * is subnormal m * 0.5.  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double orc_e2m1_to_double(uint8_t nibble) {
+  int sign = (nibble >> 3) & 1;
+  int ex = (nibble >> 1) & 3;
+  int m = nibble & 1;
+  double v;
+  if (ex == 0) {
+    v = 0.5 * m;
+  } else {
+    v = ldexp(1.0 + 0.5 * m, ex - 1);
+  }
+  return sign ? -v : v;
+}
+
+/* Round a binary32 value to the nearest bfloat16 (ties to the even
+ * neighbour), returned as binary32.  The two candidates are the value with
+ * its low 16 bits cleared and the next bfloat16 away from zero. */
+float orc_round_bf16(float x) {
+  uint32_t u;
+  memcpy(&u, &x, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u) { /* inf stays inf, NaN a quiet NaN */
+    if (u & 0x007fffffu) {
+      u |= 0x00400000u;
+    }
+    u &= 0xffff0000u;
+    memcpy(&x, &u, 4);
+    return x;
+  }
+  uint32_t low = u & 0xffffu;
+  uint32_t down = u & 0xffff0000u;
+  int take_up = 0;
+  if (low > 0x8000u) {
+    take_up = 1;
+  } else if (low == 0x8000u && ((down >> 16) & 1u)) {
+    take_up = 1;
+  }
+  uint32_t r = take_up ? down + 0x10000u : down;
+  float y;
+  memcpy(&y, &r, 4);
+  return y;
+}
+
+/* The nearest E2M1 magnitude code (0..7) to v >= 0, ties to the even code,
+ * values beyond 6 saturating to 6 (code 7). */
+static int orc_e2m1_nearest_code(double v) {
+  int best = 0;
+  double best_err = INFINITY;
+  if (v > 6.0) {
+    return 7;
+  }
+  for (int c = 0; c < 8; ++c) {
+    double err = fabs(v - orc_e2m1_to_double((uint8_t)c));
+    if (err < best_err || (err == best_err && (c % 2) == 0)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return best;
+}
+
+/* OCP MX conversion of one block of 32 binary32 scalars to FP4 E2M1 with an
+ * E8M0 scale: X = 2^(floor(log2(amax)) - 2) (2 = the largest E2M1 exponent),
+ * clamped to [2^-127, 2^127]; element i is the E2M1 value nearest x_i / X,
+ * ties to even, saturating at +-6.  An all-zero block takes scale byte 0; a
+ * block holding inf or NaN takes the NaN scale byte 0xFF and zero codes.
+ * packed[j] holds element 2j in its low nibble and 2j+1 in its high nibble. */
+void orc_fp4_quantize_block(const float* x, uint8_t* scale_byte, uint8_t* packed) {
+  double amax = 0.0;
+  int finite = 1;
+  for (int i = 0; i < 32; ++i) {
+    double a = fabs((double)x[i]);
+    if (!isfinite(a)) {
+      finite = 0;
+    }
+    if (a > amax) {
+      amax = a;
+    }
+  }
+  for (int j = 0; j < 16; ++j) {
+    packed[j] = 0;
+  }
+  if (!finite) {
+    *scale_byte = 0xff;
+    return;
+  }
+  if (amax == 0.0) {
+    *scale_byte = 0;
+    return;
+  }
+  int k;
+  frexp(amax, &k); /* amax = f * 2^k, f in [0.5, 1): floor(log2 amax) = k - 1 */
+  int e = (k - 1) - 2;
+  if (e < -127) {
+    e = -127;
+  }
+  if (e > 127) {
+    e = 127;
+  }
+  *scale_byte = (uint8_t)(e + 127);
+  for (int i = 0; i < 32; ++i) {
+    double v = ldexp((double)x[i], -e);
+    int code = orc_e2m1_nearest_code(fabs(v));
+    if (v < 0.0 && code != 0) {
+      code |= 8;
+    }
+    packed[i / 2] |= (uint8_t)((i % 2) ? (code << 4) : code);
+  }
+}
+
+/* Element i of an FP4 block: e2m1(code) * 2^(scale - 127), NaN for 0xFF. */
+float orc_fp4_element(uint8_t scale_byte, const uint8_t* packed, int i) {
+  uint8_t nib = (uint8_t)((i % 2) ? (packed[i / 2] >> 4) : (packed[i / 2] & 0xf));
+  if (scale_byte == 0xff) {
+    return NAN;
+  }
+  return (float)ldexp(orc_e2m1_to_double(nib), (int)scale_byte - 127);
+}
+
+/* [CSA-CPU] hadamard_bf16: the unnormalised Walsh-Hadamard transform by
+ * butterflies (span 1, 2, 4, ...: a + b, a - b in binary32), then every value
+ * times 1/sqrt(n) (binary32) and rounded to bfloat16.  n a power of two. */
+void orc_hadamard_bf16(float* v, int64_t n) {
+  for (int64_t span = 1; span < n; span *= 2) {
+    for (int64_t start = 0; start < n; start += 2 * span) {
+      for (int64_t off = 0; off < span; ++off) {
+        float a = v[start + off];
+        float b = v[start + off + span];
+        v[start + off] = a + b;
+        v[start + off + span] = a - b;
+      }
+    }
+  }
+  float scale = 1.0f / sqrtf((float)n);
+  for (int64_t i = 0; i < n; ++i) {
+    float p = v[i] * scale;
+    v[i] = orc_round_bf16(p);
+  }
+}
+
+/* [CSA-CPU] finalize_index_query: bfloat16 rounding of the query head, then
+ * (RoPE of its last components is applied by the caller before this step)
+ * the Hadamard transform and an FP4 round trip per block of 32 (quantize,
+ * then dequantize in place).  out may equal src. */
+void orc_index_query_finalize(const float* src, int64_t n, float* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    out[i] = orc_round_bf16(src[i]);
+  }
+  orc_hadamard_bf16(out, n);
+  for (int64_t blk = 0; blk < n / 32; ++blk) {
+    uint8_t sb, packed[16];
+    orc_fp4_quantize_block(out + 32 * blk, &sb, packed);
+    for (int i = 0; i < 32; ++i) {
+      out[32 * blk + i] = orc_fp4_element(sb, packed, i);
+    }
+  }
+}
+
+/* Rust's f32::total_cmp as a signed integer key: for negative values every
+ * bit but the sign is flipped, so the signed order of the keys is the total
+ * order (-NaN < -inf < ... < -0 < +0 < ... < +inf < +NaN). */
+static int32_t orc_total_key(float f) {
+  int32_t k;
+  memcpy(&k, &f, 4);
+  if (k < 0) {
+    k ^= 0x7fffffff;
+  }
+  return k;
+}
+
+typedef struct {
+  int32_t record;
+  float score;
+} orc_scored;
+
+/* Higher score first (total order), then the lower record. */
+static int orc_rank_cmp(const void* pa, const void* pb) {
+  const orc_scored* a = (const orc_scored*)pa;
+  const orc_scored* b = (const orc_scored*)pb;
+  int32_t ka = orc_total_key(a->score), kb = orc_total_key(b->score);
+  if (ka != kb) {
+    return ka > kb ? -1 : 1;
+  }
+  return (a->record > b->record) - (a->record < b->record);
+}
+
+static int orc_int_cmp(const void* pa, const void* pb) {
+  int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+  return (a > b) - (a < b);
+}
+
+typedef struct {
+  const float* query;    /* [B, S, IH, ID] */
+  const float* weight;   /* [B, S, IH] */
+  const uint8_t* keys;   /* [B, R, key_stride]: ID/32 blocks of [scale, 16 packed bytes] */
+  int64_t B, S, IH, ID, R, topk, key_stride;
+  int64_t query_start;           /* position of query s is query_start + s ... */
+  const int64_t* query_start_b;  /* ... or query_start_b[b] + s when given */
+  int64_t out_heads;             /* copies of the set: selected [B, out_heads, S, topk] */
+  int ascending;                 /* 0: score order; 1: ascending record order */
+} orc_select_args;
+
+/* [CSA-CPU] select_ratio4_topk.  For row (b, s) at position p, the causal
+ * records are r < min(R, (p + 1) / 4).  Each record's score is
+ *   sum over heads h (ascending) of relu(q_h . k_r) * w_h * c,
+ *   c = (1/sqrt(ID)) / sqrt(IH), q_h the finalized query head,
+ * the dot product summed in ascending dimension order, every operation in
+ * binary32 and unfused.  The records are ranked by score (higher first,
+ * Rust total_cmp) and then by record index; the first topk fill the row,
+ * -1 the rest.  Two equal scores in a row set SEL_TIE (the pages refuse such
+ * input; the ranking still orders them by record), a non-finite score sets
+ * SEL_NONFINITE.  scores (nullable) receives [B, S, R] (0 past the causal
+ * limit).  Returns 0, or -1 on a bad shape. */
+int orc_index_select(const orc_select_args* a, int32_t* selected, uint8_t* status,
+                     uint32_t* err, float* scores) {
+  if (a->ID <= 0 || a->ID % 32 != 0 || (a->ID & (a->ID - 1)) != 0 || a->IH <= 0 ||
+      a->topk <= 0 || a->key_stride < a->ID / 32 * 17 || a->out_heads <= 0) {
+    return -1;
+  }
+  uint32_t acc = 0;
+  float* q = (float*)malloc(sizeof(float) * (size_t)(a->IH * a->ID));
+  float* k = (float*)malloc(sizeof(float) * (size_t)a->ID);
+  orc_scored* rank = (orc_scored*)malloc(sizeof(orc_scored) * (size_t)(a->R > 0 ? a->R : 1));
+  int32_t* row = (int32_t*)malloc(sizeof(int32_t) * (size_t)a->topk);
+  float c = 1.0f / sqrtf((float)a->ID);
+  c = c / sqrtf((float)a->IH);
+  for (int64_t b = 0; b < a->B; ++b) {
+    for (int64_t s = 0; s < a->S; ++s) {
+      int64_t pos = (a->query_start_b ? a->query_start_b[b] : a->query_start) + s;
+      int64_t limit = pos >= 0 ? (pos + 1) / 4 : 0;
+      if (limit > a->R) {
+        limit = a->R;
+      }
+      for (int64_t h = 0; h < a->IH; ++h) {
+        const float* src = a->query + ((b * a->S + s) * a->IH + h) * a->ID;
+        orc_index_query_finalize(src, a->ID, q + h * a->ID);
+      }
+      const float* w = a->weight + (b * a->S + s) * a->IH;
+      int code = 0;
+      for (int64_t r = 0; r < limit; ++r) {
+        const uint8_t* rec = a->keys + (b * a->R + r) * a->key_stride;
+        for (int64_t d = 0; d < a->ID; ++d) {
+          const uint8_t* blk = rec + (d / 32) * 17;
+          k[d] = orc_fp4_element(blk[0], blk + 1, (int)(d % 32));
+        }
+        float score = 0.0f;
+        for (int64_t h = 0; h < a->IH; ++h) {
+          float dot = 0.0f;
+          for (int64_t d = 0; d < a->ID; ++d) {
+            float p = q[h * a->ID + d] * k[d];
+            dot = dot + p;
+          }
+          float relu = fmaxf(dot, 0.0f);
+          float t = relu * w[h];
+          t = t * c;
+          score = score + t;
+        }
+        if (!isfinite(score)) {
+          code |= ORC_SEL_NONFINITE;
+        }
+        rank[r].record = (int32_t)r;
+        rank[r].score = score;
+      }
+      if (scores) {
+        for (int64_t r = 0; r < a->R; ++r) {
+          scores[(b * a->S + s) * a->R + r] = r < limit ? rank[r].score : 0.0f;
+        }
+      }
+      /* equal scores: sort a copy of the scores, compare neighbours with == */
+      {
+        float* sorted = (float*)malloc(sizeof(float) * (size_t)(limit > 0 ? limit : 1));
+        orc_scored* tmp = (orc_scored*)malloc(sizeof(orc_scored) * (size_t)(limit > 0 ? limit : 1));
+        memcpy(tmp, rank, sizeof(orc_scored) * (size_t)limit);
+        qsort(tmp, (size_t)limit, sizeof(orc_scored), orc_rank_cmp);
+        for (int64_t r = 0; r < limit; ++r) {
+          sorted[r] = tmp[r].score;
+        }
+        for (int64_t r = 1; r < limit; ++r) {
+          if (sorted[r] == sorted[r - 1]) {
+            code |= ORC_SEL_TIE;
+          }
+        }
+        free(sorted);
+        free(tmp);
+      }
+      qsort(rank, (size_t)limit, sizeof(orc_scored), orc_rank_cmp);
+      int64_t n = limit < a->topk ? limit : a->topk;
+      for (int64_t j = 0; j < a->topk; ++j) {
+        row[j] = j < n ? rank[j].record : -1;
+      }
+      if (a->ascending) {
+        qsort(row, (size_t)n, sizeof(int32_t), orc_int_cmp);
+      }
+      for (int64_t o = 0; o < a->out_heads; ++o) {
+        memcpy(selected + ((b * a->out_heads + o) * a->S + s) * a->topk, row,
+               sizeof(int32_t) * (size_t)a->topk);
+      }
+      if (status) {
+        status[b * a->S + s] = (uint8_t)code;
+      }
+      acc |= (uint32_t)code;
+    }
+  }
+  free(q);
+  free(k);
+  free(rank);
+  free(row);
+  if (err) {
+    *err = acc;
+  }
+  return 0;
+}

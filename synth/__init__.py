@@ -42,6 +42,10 @@ __all__ = [
     "make_sparse_inputs",
     "make_prefill_inputs",
     "make_paged_inputs",
+    "IndexCase",
+    "index_select_fp4",
+    "fp4_index_records",
+    "make_index_inputs",
 ]
 
 _TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -341,4 +345,72 @@ def make_paged_inputs(c: PagedCase, seed: int, device="cpu") -> dict:
         "q": normal((c.B, c.Hq, 1, c.D), c.dtype, seed * 15485863 + 4, device),
         "k_pool": k_pool, "v_pool": v_pool, "k_new": k_new, "v_new": v_new,
         "ctx_len": ctx_d, "block_table": table_d, "num_pages": num_pages,
+    }
+
+
+# --------------------------------------------------------------------------
+# Ratio-4 index selection inputs
+# --------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class IndexCase:
+    name: str
+    B: int
+    S: int                 # query positions per batch
+    IH: int                # index heads
+    ID: int                # index head dim (a power of two, a multiple of 32)
+    R: int                 # compressed index records per batch (capacity)
+    topk: int
+    query_start: int       # position of query 0 (the last S positions of the context)
+    key_stride: int = 0    # bytes between records (0: ID / 32 * 17)
+
+    @property
+    def stride(self) -> int:
+        return self.key_stride or self.ID // 32 * 17
+
+
+def index_select_fp4(**kw) -> IndexCase:
+    """B16 decode rows at the last position of a 65,536-token context: 16,384
+    ratio-4 index records of 128 FP4 dims (68 bytes), 64 index heads, top-k
+    2,048."""
+    base = IndexCase("index_select_b16_ih64_id128_r16384_k2048", B=16, S=1, IH=64, ID=128,
+                     R=16384, topk=2048, query_start=65535)
+    return replace(base, **kw)
+
+
+# E2M1 magnitude codes 0..7 (0, 0.5, 1, 1.5, 2, 3, 4, 6) drawn with roughly
+# the weights that Gaussian data scaled into [0, 6] per 32-block gives
+_E2M1_CODE_WEIGHTS = [0.20, 0.25, 0.20, 0.12, 0.10, 0.08, 0.04, 0.01]
+
+
+def fp4_index_records(B: int, R: int, ID: int, seed: int, stride: int = 0,
+                      device="cpu") -> torch.Tensor:
+    """Index-key records ``[B, R, stride]`` uint8: ID/32 blocks of [E8M0 scale
+    byte, 16 bytes of E2M1 codes, element 2j in the low nibble of byte j].
+    Codes and scale bytes are drawn directly (magnitudes from a fixed
+    categorical distribution, uniform signs, scale bytes 124..127); no
+    quantizer is involved."""
+    nb = ID // 32
+    width = nb * 17
+    stride = stride or width
+    g = _gen(seed, "cpu")
+    w = torch.tensor(_E2M1_CODE_WEIGHTS, dtype=torch.float64)
+    mag = torch.multinomial(w, B * R * ID, replacement=True, generator=g).to(torch.uint8)
+    sign = torch.randint(0, 2, (B * R * ID,), generator=g, dtype=torch.uint8) << 3
+    codes = (mag | sign).reshape(B, R, nb, 16, 2)
+    packed = codes[..., 0] | (codes[..., 1] << 4)
+    scale = torch.randint(124, 128, (B, R, nb, 1), generator=g, dtype=torch.uint8)
+    blocks = torch.cat([scale, packed], dim=3).reshape(B, R, width)
+    rec = torch.zeros((B, R, stride), dtype=torch.uint8)
+    rec[:, :, :width] = blocks
+    return rec.to(device)
+
+
+def make_index_inputs(c: IndexCase, seed: int, device="cpu") -> dict:
+    """Index queries float32 ``[B, S, IH, ID]`` and head weights float32
+    ``[B, S, IH]`` ~ N(0, 1), and the FP4 index-key records."""
+    return {
+        "query": normal((c.B, c.S, c.IH, c.ID), "f32", seed * 49157 + 1, device),
+        "weight": normal((c.B, c.S, c.IH), "f32", seed * 49157 + 2, device),
+        "keys": fp4_index_records(c.B, c.R, c.ID, seed * 49157 + 3, c.key_stride, device),
     }
