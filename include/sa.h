@@ -1,13 +1,14 @@
 /*
  * sa.h -- C ABI of the GB300 KV-cache attention library (libsa.so).
  *
- * Five operations, all computed on the GPU on the caller's stream:
+ * Six operations, all computed on the GPU on the caller's stream:
  *
  *   validate_indices     index-row validation with a device error word
  *   build_present_kv     present K/V = past ++ current (concat or in-place append)
  *   sparse_attn_decode   selected-token attention (dense or FP8 hybrid cache)
  *   attn_prefill         dense (causal) prefill with softcap, present K/V out
  *   paged_attn_decode    causal decode over a 16-token page table
+ *   sparse_index_select  ratio-4 index scoring + top-k (produces selected indices)
  *
  * Conventions shared by every call
  * --------------------------------
@@ -36,6 +37,8 @@
  *        compressed_sparse_attention.rs, csa_ratio128_sink_attention.
  *  [PG]  ferrum-kernels vnext_ops/transformer/causal_attention.rs: paged KV
  *        blocks of 16 tokens addressed through a table.
+ *  [CSA-CPU] onnx-runtime-ep-cpu compressed_sparse_attention.rs: the ratio-4
+ *        index stream (finalize_index_query, select_ratio4_topk).
  */
 #ifndef SA_H
 #define SA_H
@@ -265,6 +268,66 @@ int sparse_attn_decode(const sa_sparse_params* p, void* stream);
  */
 #define SA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int sparse_attn_decode_noalloc(const sa_sparse_params* p, void* stream);
+
+/*
+ * sparse_index_select -- ratio-4 index scoring and top-k selection, the step
+ * that produces the selected indices: [CSA-CPU] finalize_index_query,
+ * hadamard_bf16, fp4_roundtrip, select_ratio4_topk; [CSA]
+ * csa_ratio4_index_select, csa_ratio4_index_replicate.
+ *
+ * For each row (b, s), at position p = query_start (or query_start_b[b]) + s:
+ *   q_h = fp4_roundtrip(hadamard_bf16(bf16(query[b, s, h, :])))   per head h,
+ *     the Walsh-Hadamard transform with a 1/sqrt(ID) scale rounded to bf16,
+ *     then every block of 32 rounded to FP4 E2M1 with an E8M0 scale by the
+ *     OCP MX rule (scale 2^(floor(log2 amax) - 2), nearest value, ties to
+ *     even, saturating);
+ *   score_r = sum_h relu(q_h . k_r) * weight[b, s, h] * c,  c = (1/sqrt(ID))/sqrt(IH),
+ *     for the causal records r < min(R, (p + 1) / 4), in binary32: each dot
+ *     product summed in ascending dimension order, the heads in ascending
+ *     order, every multiply and add rounded on its own (the pages' order; the
+ *     result is that definition bit for bit);
+ *   the records ranked by score (Rust f32::total_cmp, higher first) and then
+ *   by record index; the first topk written, -1 after them.
+ * The compressed RoPE of the query's last components is the caller's: the
+ * query enters after it.
+ *
+ * query: float32 [B, S, IH, ID], ID in {32, 64, 128, 256}; weight: float32
+ * [B, S, IH]; keys: [B, R, key_stride] bytes, each record ID/32 blocks of
+ * [E8M0 scale byte, 16 bytes of E2M1 codes, element 2j in the low nibble of
+ * byte j] (68 bytes for ID 128), key_stride a multiple of 4, keys 4-byte
+ * aligned.  selected: int32 [B, out_heads, S, topk], the same row for every
+ * output head ([CSA] replicate); ascending = 1 writes the selected records
+ * in ascending record order instead of score order (the form
+ * sparse_attn_decode validates).  1 <= topk <= 4096, 1 <= IH <= 256.
+ * row_status (nullable uint8 [B*S]) and err_word (nullable): SA_SEL_TIE when
+ * two scores of the row are equal (the pages refuse such input; the ranking
+ * still orders them by record), SA_SEL_NONFINITE when a score is NaN or
+ * infinite; err_word receives them shifted into SA_ERRBIT_SEL_*.
+ * Workspace: sparse_index_select_workspace(p) bytes, 256-byte aligned,
+ * contents on entry irrelevant.  Deterministic.
+ */
+#define SA_SEL_TIE 1
+#define SA_SEL_NONFINITE 2
+#define SA_ERRBIT_SEL_TIE 512
+#define SA_ERRBIT_SEL_NONFINITE 1024
+typedef struct {
+  const float* query;
+  const float* weight;
+  const uint8_t* keys;
+  int32_t* selected;
+  uint8_t* row_status;
+  uint32_t* err_word;
+  int64_t B, S, IH, ID, R, topk, key_stride, out_heads;
+  int64_t query_start;
+  const int64_t* query_start_b;
+  int32_t ascending;
+  int32_t reserved_;    /* must be 0 */
+  void* workspace;
+  size_t workspace_bytes;
+} sa_index_select_params;
+
+size_t sparse_index_select_workspace(const sa_index_select_params* p);
+int sparse_index_select(const sa_index_select_params* p, void* stream);
 
 /*
  * attn_prefill -- [SA] Semantics with no past: q [B, Hq, S, D],

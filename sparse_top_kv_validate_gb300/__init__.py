@@ -8,7 +8,7 @@ falling back to anything else.
 
 Entry points (same names as the C ABI):
     validate_indices, build_present_kv, sparse_attn_decode, attn_prefill,
-    paged_attn_decode
+    paged_attn_decode, sparse_index_select
 """
 from __future__ import annotations
 
@@ -28,6 +28,8 @@ __all__ = [
     "IDX_BELOW_SENTINEL", "IDX_AFTER_PADDING", "IDX_OUT_OF_RANGE", "IDX_NOT_INCREASING",
     "IDX_DUPLICATE", "IDX_ALL_PADDING", "ERRBIT_WRITE_POS", "ERRBIT_PAGE", "ERRBIT_TIMEOUT",
     "SparseParams", "PrefillParams", "PagedParams", "kernel_events",
+    "IndexSelectParams", "sparse_index_select", "sparse_index_select_workspace",
+    "SEL_TIE", "SEL_NONFINITE", "ERRBIT_SEL_TIE", "ERRBIT_SEL_NONFINITE",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -40,6 +42,8 @@ ERRBIT_WRITE_POS, ERRBIT_PAGE, ERRBIT_TIMEOUT = 64, 128, 256
 ERR_SCRATCH_LIMIT = -9
 NOALLOC_SCRATCH_BYTES = 16 << 20
 OPT_ROW_COPIES, OPT_FP8_WARP_MMA = 1, 2
+SEL_TIE, SEL_NONFINITE = 1, 2
+ERRBIT_SEL_TIE, ERRBIT_SEL_NONFINITE = 512, 1024
 
 _p = C.c_void_p
 _i64 = C.c_int64
@@ -82,6 +86,17 @@ class PagedParams(C.Structure):
         ("max_pages", _i64), ("num_pages", _i64),
         ("scale", C.c_float), ("pad2_", C.c_float),
         ("err_word", _p), ("workspace", _p), ("workspace_bytes", C.c_size_t),
+    ]
+
+
+class IndexSelectParams(C.Structure):
+    _fields_ = [
+        ("query", _p), ("weight", _p), ("keys", _p), ("selected", _p), ("row_status", _p),
+        ("err_word", _p),
+        ("B", _i64), ("S", _i64), ("IH", _i64), ("ID", _i64), ("R", _i64), ("topk", _i64),
+        ("key_stride", _i64), ("out_heads", _i64), ("query_start", _i64),
+        ("query_start_b", _p), ("ascending", _i32), ("reserved_", _i32),
+        ("workspace", _p), ("workspace_bytes", C.c_size_t),
     ]
 
 
@@ -131,6 +146,10 @@ def load():
         L.attn_prefill_workspace.argtypes = [C.POINTER(PrefillParams)]
         L.attn_prefill.restype = C.c_int
         L.attn_prefill.argtypes = [C.POINTER(PrefillParams), _p]
+        L.sparse_index_select_workspace.restype = C.c_size_t
+        L.sparse_index_select_workspace.argtypes = [C.POINTER(IndexSelectParams)]
+        L.sparse_index_select.restype = C.c_int
+        L.sparse_index_select.argtypes = [C.POINTER(IndexSelectParams), _p]
         L.paged_attn_decode_workspace.restype = C.c_size_t
         L.paged_attn_decode_workspace.argtypes = [C.POINTER(PagedParams)]
         L.paged_attn_decode.restype = C.c_int
@@ -467,3 +486,56 @@ def sparse_attn_decode_noalloc(q, k_cache, v_cache, idx, *, y=None, stream=None,
     p = _sparse_params(q, k_cache, v_cache, idx, y, **kw)
     _check("sparse_attn_decode_noalloc", L.sparse_attn_decode_noalloc(C.byref(p), _stream(stream)))
     return y
+
+
+def _index_params(query, weight, keys, selected, *, topk, query_start, query_start_b,
+                  out_heads, ascending, row_status, err_word):
+    p = IndexSelectParams()
+    B, S, IH, ID = query.shape
+    p.query, p.weight, p.keys = query.data_ptr(), weight.data_ptr(), keys.data_ptr()
+    p.selected = _ptr(selected)
+    p.row_status, p.err_word = _ptr(row_status), _ptr(err_word)
+    p.B, p.S, p.IH, p.ID = B, S, IH, ID
+    p.R, p.key_stride = keys.shape[1], keys.shape[2]
+    p.topk, p.out_heads = int(topk), int(out_heads)
+    p.query_start = int(query_start)
+    p.query_start_b = _ptr(query_start_b)
+    p.ascending = int(bool(ascending))
+    return p
+
+
+def sparse_index_select_workspace(query, weight, keys, *, topk, out_heads=1) -> int:
+    p = _index_params(query, weight, keys, None, topk=topk, query_start=0, query_start_b=None,
+                      out_heads=out_heads, ascending=False, row_status=None, err_word=None)
+    return int(load().sparse_index_select_workspace(C.byref(p)))
+
+
+def sparse_index_select(query, weight, keys, *, topk, query_start=0, query_start_b=None,
+                        out_heads=1, ascending=False, row_status=None, err_word=None,
+                        selected=None, workspace=None, stream=None):
+    """Ratio-4 index scoring and top-k selection.  ``query`` float32
+    ``[B, S, IH, ID]``, ``weight`` float32 ``[B, S, IH]``, ``keys`` uint8
+    ``[B, R, key_stride]`` FP4 records; query s of batch b sits at position
+    ``query_start + s`` (or ``query_start_b[b] + s``, int64 ``[B]``).
+    Returns ``selected`` int32 ``[B, out_heads, S, topk]`` (score order, or
+    ascending records with ``ascending``), -1 past the causal records;
+    ``row_status`` (uint8 ``[B*S]``) / ``err_word`` receive the tie and
+    non-finite flags."""
+    L = load()
+    for n, t in (("query", query), ("weight", weight), ("keys", keys),
+                 ("query_start_b", query_start_b), ("row_status", row_status),
+                 ("err_word", err_word), ("selected", selected)):
+        _dev(t, n)
+    if query.dtype != torch.float32 or weight.dtype != torch.float32 or keys.dtype != torch.uint8:
+        raise TypeError("query and weight must be float32, keys uint8")
+    B, S = query.shape[0], query.shape[1]
+    if selected is None:
+        selected = torch.empty((B, out_heads, S, topk), dtype=torch.int32, device=query.device)
+    p = _index_params(query, weight, keys, selected, topk=topk, query_start=query_start,
+                      query_start_b=query_start_b, out_heads=out_heads, ascending=ascending,
+                      row_status=row_status, err_word=err_word)
+    need = int(L.sparse_index_select_workspace(C.byref(p)))
+    ws, nb = _workspace(need, query.device, workspace)
+    p.workspace, p.workspace_bytes = _ptr(ws), nb
+    _check("sparse_index_select", L.sparse_index_select(C.byref(p), _stream(stream)))
+    return selected

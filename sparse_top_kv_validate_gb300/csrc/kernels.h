@@ -180,6 +180,43 @@ struct PrefillTcArgs {
 bool prefill_tc_supported(const PrefillTcArgs& a);
 int launch_prefill_tc(const PrefillTcArgs& a, cudaStream_t st);
 
+// ---- ratio-4 index scoring and top-k selection ----------------------------------------
+constexpr int kQmetaZero = 1 << 30;       // index-query head whose codes are all zero
+constexpr int kQmetaNonfinite = 1 << 29;  // index-query head with a non-finite block
+constexpr int kSelTie = 1;                // row status: equal scores in the row
+constexpr int kSelNonfinite = 2;          // row status: a score is NaN or infinite
+constexpr int kSelErrShift = 9;           // row status << shift = err_word bits
+
+struct IndexArgs {
+  const float* query;         // [rows, IH, ID], rows = B * S
+  const float* weight;        // [rows, IH]
+  const uint8_t* keys;        // [B, R, key_stride]
+  int32_t* selected;          // [B, out_heads, S, topk]
+  uint8_t* row_status;        // nullable [rows]
+  uint32_t* err_word;         // nullable
+  int64_t rows, S, IH, ID, R, topk, key_stride, out_heads;
+  int64_t query_start;
+  const int64_t* query_start_b;  // nullable [B]
+  int ascending;              // 1: records in ascending order, else score order
+  float had_scale;            // 1 / sqrt(ID) in binary32
+  float weight_scale;         // (1 / sqrt(ID)) / sqrt(IH) in binary32
+  // workspace
+  int8_t* qcodes;             // [rows, IH, ID] signed 2 * E2M1 codes
+  int8_t* qexp;               // [rows, IH, ID / 32] block exponents (127: non-finite)
+  int32_t* qmeta;             // [rows, IH] exponent range / zero / non-finite
+  float* scores;              // [rows, R]
+  uint32_t* gkeys;            // [rows, R] when the top-k state is in global memory
+  uint32_t* ghash;            // [rows, hash_slots]
+  int topk_global;            // 1: top-k keys and hash in the workspace
+  int hash_slots;             // power of two >= 2 R and >= 2 next_pow2(topk)
+  int hash_log2;
+  void* ev_before;            // nullable measurement events around the score kernel
+  void* ev_after;
+};
+size_t index_topk_smem_bytes(int64_t R, int hash_slots);
+size_t index_score_smem_bytes(int64_t IH, int64_t ID, int64_t key_stride);
+int launch_index_select(const IndexArgs& a, cudaStream_t st);
+
 // ---- paged: write the new token into the pool -----------------------------------
 struct PagedAppendArgs {
   void* k_pool;

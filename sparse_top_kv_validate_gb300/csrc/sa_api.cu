@@ -823,6 +823,113 @@ int paged_attn_decode(const sa_paged_params* p, void* stream) {
   return run_plan(pl, p->dtype, st);
 }
 
+// ---- ratio-4 index selection -------------------------------------------------------
+
+static int check_index(const sa_index_select_params* p, int query = 0) {
+  if (!p || !p->query || !p->weight || !p->keys || (!p->selected && !query)) return SA_ERR_NULL;
+  if (p->reserved_ != 0) return SA_ERR_UNSUPPORTED;
+  if (p->B <= 0 || p->S <= 0 || p->IH <= 0 || p->R <= 0 || p->topk <= 0 || p->out_heads <= 0)
+    return SA_ERR_SHAPE;
+  if (!(p->ID == 32 || p->ID == 64 || p->ID == 128 || p->ID == 256)) return SA_ERR_UNSUPPORTED;
+  if (p->IH > 256 || p->topk > 4096) return SA_ERR_UNSUPPORTED;
+  if (p->key_stride < p->ID / 32 * 17 || p->key_stride % 4) return SA_ERR_SHAPE;
+  if (p->key_stride * 256 > 64 * 1024) return SA_ERR_UNSUPPORTED;
+  if (p->B * p->R >= (int64_t(1) << 31) || p->R >= (int64_t(1) << 28)) return SA_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(p->keys) % 4 || reinterpret_cast<uintptr_t>(p->query) % 4 ||
+      reinterpret_cast<uintptr_t>(p->weight) % 4 || reinterpret_cast<uintptr_t>(p->selected) % 4)
+    return SA_ERR_ALIGN;
+  const size_t sbytes = static_cast<size_t>(p->B * p->out_heads * p->S * p->topk) * 4;
+  const size_t qbytes = static_cast<size_t>(p->B * p->S * p->IH * p->ID) * 4;
+  const size_t kbytes = static_cast<size_t>(p->B * p->R * p->key_stride);
+  if (overlaps(p->selected, sbytes, p->query, qbytes) ||
+      overlaps(p->selected, sbytes, p->keys, kbytes) ||
+      overlaps(p->selected, sbytes, p->weight, static_cast<size_t>(p->B * p->S * p->IH) * 4))
+    return SA_ERR_OVERLAP;
+  return SA_OK;
+}
+
+// Workspace layout of the index selection; fills the pointers when ws != NULL.
+static size_t index_plan(const sa_index_select_params* p, sa::IndexArgs& a, char* ws) {
+  memset(&a, 0, sizeof(a));
+  a.rows = p->B * p->S;
+  a.S = p->S;
+  a.IH = p->IH;
+  a.ID = p->ID;
+  a.R = p->R;
+  a.topk = p->topk;
+  a.key_stride = p->key_stride;
+  a.out_heads = p->out_heads;
+  int64_t slots = 2;
+  while (slots < 2 * p->R) slots <<= 1;
+  int64_t kp = 1;
+  while (kp < p->topk) kp <<= 1;
+  if (slots < 2 * kp) slots = 2 * kp;
+  a.hash_slots = static_cast<int>(slots);
+  int lg = 0;
+  while ((int64_t(1) << lg) < slots) ++lg;
+  a.hash_log2 = lg;
+  a.topk_global = sa::index_topk_smem_bytes(p->R, a.hash_slots) > size_t(200) * 1024 ? 1 : 0;
+  size_t off = 0;
+  const size_t o_codes = off;
+  off += align_up(static_cast<size_t>(a.rows * p->IH * p->ID));
+  const size_t o_exp = off;
+  off += align_up(static_cast<size_t>(a.rows * p->IH * (p->ID / 32)));
+  const size_t o_meta = off;
+  off += align_up(static_cast<size_t>(a.rows * p->IH) * 4);
+  const size_t o_scores = off;
+  off += align_up(static_cast<size_t>(a.rows * p->R) * 4);
+  size_t o_keys = 0, o_hash = 0;
+  if (a.topk_global) {
+    o_keys = off;
+    off += align_up(static_cast<size_t>(a.rows * p->R) * 4);
+    o_hash = off;
+    off += align_up(static_cast<size_t>(a.rows) * static_cast<size_t>(slots) * 4);
+  }
+  if (ws) {
+    a.qcodes = reinterpret_cast<int8_t*>(ws + o_codes);
+    a.qexp = reinterpret_cast<int8_t*>(ws + o_exp);
+    a.qmeta = reinterpret_cast<int32_t*>(ws + o_meta);
+    a.scores = reinterpret_cast<float*>(ws + o_scores);
+    if (a.topk_global) {
+      a.gkeys = reinterpret_cast<uint32_t*>(ws + o_keys);
+      a.ghash = reinterpret_cast<uint32_t*>(ws + o_hash);
+    }
+  }
+  return off;
+}
+
+size_t sparse_index_select_workspace(const sa_index_select_params* p) {
+  if (check_index(p, 1) != SA_OK) return 0;
+  sa::IndexArgs a;
+  return index_plan(p, a, nullptr);
+}
+
+int sparse_index_select(const sa_index_select_params* p, void* stream) {
+  int rc = check_index(p);
+  if (rc != SA_OK) return rc;
+  sa::IndexArgs a;
+  const size_t need = index_plan(p, a, nullptr);
+  if (!p->workspace || p->workspace_bytes < need) return SA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(p->workspace) % kAlign) return SA_ERR_ALIGN;
+  index_plan(p, a, static_cast<char*>(p->workspace));
+  a.query = p->query;
+  a.weight = p->weight;
+  a.keys = p->keys;
+  a.selected = p->selected;
+  a.row_status = p->row_status;
+  a.err_word = p->err_word;
+  a.query_start = p->query_start;
+  a.query_start_b = p->query_start_b;
+  a.ascending = p->ascending ? 1 : 0;
+  // the pages' constants, binary32: 1/sqrt(ID), then (1/sqrt(ID))/sqrt(IH)
+  const float inv_sqrt_id = 1.0f / sqrtf(static_cast<float>(p->ID));
+  a.had_scale = inv_sqrt_id;
+  a.weight_scale = inv_sqrt_id / sqrtf(static_cast<float>(p->IH));
+  a.ev_before = t_ev_before;
+  a.ev_after = t_ev_after;
+  return sa::launch_index_select(a, as_stream(stream)) == 0 ? SA_OK : SA_ERR_LAUNCH;
+}
+
 }  // extern "C"
 
 // ---- sparse decode without caller-provided scratch ------------------------------------

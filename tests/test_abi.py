@@ -42,7 +42,7 @@ def declared_functions():
     return sorted(set(names))
 
 
-def test_header_declares_the_five_operations():
+def test_header_declares_the_six_operations():
     names = declared_functions()
     for n in ("validate_indices", "build_present_kv", "sparse_attn_decode", "attn_prefill",
               "paged_attn_decode"):
@@ -76,7 +76,8 @@ def _c_layout(struct_name, fields):
 
 @pytest.mark.parametrize("cname,py", [("sa_sparse_params", sa.SparseParams),
                                       ("sa_prefill_params", sa.PrefillParams),
-                                      ("sa_paged_params", sa.PagedParams)])
+                                      ("sa_paged_params", sa.PagedParams),
+                                      ("sa_index_select_params", sa.IndexSelectParams)])
 def test_struct_layout_matches_header(cname, py):
     fields = [f for f, _ in py._fields_]
     size, offs = _c_layout(cname, fields)
@@ -274,3 +275,36 @@ def test_unknown_option_bits_and_misaligned_bias_are_refused(host_lib):
     g = _paged_params()
     g.options = 2
     assert host_lib.paged_attn_decode(C.byref(g), None) == -7
+
+
+
+def _index_params():
+    p = sa.IndexSelectParams()
+    p.query, p.weight, p.keys, p.selected = 0x100000, 0x200000, 0x10000000, 0x300000
+    p.B, p.S, p.IH, p.ID, p.R, p.topk, p.key_stride, p.out_heads = 2, 1, 64, 128, 1000, 64, 68, 1
+    p.query_start = 4000
+    return p
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("ID", 96, -7), ("ID", 512, -7),        # 32, 64, 128 or 256 dims
+    ("topk", 0, -2), ("topk", 5000, -7),    # 1 .. 4096
+    ("IH", 0, -2), ("IH", 300, -7),
+    ("key_stride", 66, -2), ("key_stride", 70, -2),  # >= 68 and a multiple of 4
+    ("keys", 0x10000002, -4),
+    ("selected", 0x100000 + 64, -6),       # the output overlaps the queries
+    ("out_heads", 0, -2), ("reserved_", 1, -7),
+])
+def test_index_select_requests_the_library_does_not_serve_are_refused(host_lib, field, value,
+                                                                      status):
+    p = _index_params()
+    setattr(p, field, value)
+    assert host_lib.sparse_index_select(C.byref(p), None) == status
+
+
+def test_index_select_workspace_query_needs_no_output_pointer(lib):
+    p = _index_params()
+    p.selected = None
+    assert lib.sparse_index_select_workspace(C.byref(p)) > 0
+    p.ID = 100
+    assert lib.sparse_index_select_workspace(C.byref(p)) == 0
