@@ -178,18 +178,27 @@ __global__ void __launch_bounds__(128) index_query_kernel(const IndexArgs a) {
 
 namespace {
 
+// PTX prmt in its default mode: byte i of the result is byte (c_i & 7) of
+// {a, b}, or that byte's sign replicated when bit 3 of selector nibble c_i is
+// set (the __byte_perm intrinsic ignores that bit).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // Signed bytes 2 * E2M1 of the four nibble codes in the low 16 bits of x
 // (element i in bits 4i..4i+3, bit 3 of a code its sign): byte i of the result.
 __device__ __forceinline__ uint32_t nib4_to_s8(uint32_t x) {
-  // prmt selects byte (nibble & 7) of the 8-byte table; magnitudes
-  // 0 1 2 3 4 6 8 12 and their negations
+  // select byte (code & 7) of the 8-byte tables: magnitudes 0 1 2 3 4 6 8 12
+  // and their negations
   const uint32_t sel = x & 0x7777u;
-  const uint32_t pos = __byte_perm(0x03020100u, 0x0c080604u, sel);
-  const uint32_t neg = __byte_perm(0xfdfeff00u, 0xf4f8fafcu, sel);
-  // sign mask: selector 9 (bit 3 set: replicate the sign of byte 1 = 0x80)
-  // for a negative code, 0 (byte 0 = 0x00) otherwise
+  const uint32_t pos = prmt(0x03020100u, 0x0c080604u, sel);
+  const uint32_t neg = prmt(0xfdfeff00u, 0xf4f8fafcu, sel);
+  // sign mask: selector 9 (replicate the sign of byte 1 = 0x80) for a
+  // negative code, 0 (byte 0 = 0x00) otherwise
   const uint32_t sgn = x & 0x8888u;
-  const uint32_t sm = __byte_perm(0x00008000u, 0u, sgn | (sgn >> 3));
+  const uint32_t sm = prmt(0x00008000u, 0u, sgn | (sgn >> 3));
   return (pos & ~sm) | (neg & sm);
 }
 

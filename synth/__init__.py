@@ -366,7 +366,8 @@ class IndexCase:
 
     @property
     def stride(self) -> int:
-        return self.key_stride or self.ID // 32 * 17
+        # records padded to a multiple of 4 bytes (68 bytes at ID 128: packed)
+        return self.key_stride or (self.ID // 32 * 17 + 3) // 4 * 4
 
 
 def index_select_fp4(**kw) -> IndexCase:
@@ -386,13 +387,14 @@ _E2M1_CODE_WEIGHTS = [0.20, 0.25, 0.20, 0.12, 0.10, 0.08, 0.04, 0.01]
 def fp4_index_records(B: int, R: int, ID: int, seed: int, stride: int = 0,
                       device="cpu") -> torch.Tensor:
     """Index-key records ``[B, R, stride]`` uint8: ID/32 blocks of [E8M0 scale
-    byte, 16 bytes of E2M1 codes, element 2j in the low nibble of byte j].
+    byte, 16 bytes of E2M1 codes, element 2j in the low nibble of byte j],
+    the stride rounded up to a multiple of 4 bytes unless given.
     Codes and scale bytes are drawn directly (magnitudes from a fixed
     categorical distribution, uniform signs, scale bytes 124..127); no
     quantizer is involved."""
     nb = ID // 32
     width = nb * 17
-    stride = stride or width
+    stride = stride or (width + 3) // 4 * 4
     g = _gen(seed, "cpu")
     w = torch.tensor(_E2M1_CODE_WEIGHTS, dtype=torch.float64)
     mag = torch.multinomial(w, B * R * ID, replacement=True, generator=g).to(torch.uint8)
@@ -412,5 +414,5 @@ def make_index_inputs(c: IndexCase, seed: int, device="cpu") -> dict:
     return {
         "query": normal((c.B, c.S, c.IH, c.ID), "f32", seed * 49157 + 1, device),
         "weight": normal((c.B, c.S, c.IH), "f32", seed * 49157 + 2, device),
-        "keys": fp4_index_records(c.B, c.R, c.ID, seed * 49157 + 3, c.key_stride, device),
+        "keys": fp4_index_records(c.B, c.R, c.ID, seed * 49157 + 3, c.stride, device),
     }
