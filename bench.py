@@ -432,7 +432,9 @@ class CsaFp8Decode:
                                               row_status=self.status)
         self.ws = sa.new_workspace(nws, dev)
         self.rows = c.B * c.Hq
-        valid = int((self.idx >= 0).sum().item())       # selected below the window
+        # candidates: the window plus the selected entries below it (an entry
+        # inside the window is the same key, counted once)
+        valid = int(((self.idx >= 0) & (self.idx < c.T - c.window)).sum().item())
         self.keys = valid + c.B * c.window
         self.decode_bytes = (self.keys * c.record_stride + self.idx.numel() * 4
                              + 2 * self.q.numel() * 2)
@@ -496,6 +498,102 @@ class CsaFp8Decode:
         return line
 
 
+class IndexSelect:
+    """Ratio-4 index scoring and top-k selection (the producer of the selected
+    indices): B16 decode rows at position 65,535, 16,384 index records of 128
+    FP4 dims (68 bytes), 64 index heads, top-k 2,048."""
+
+    metric = "ratio-4 index-select query-rows/s (FP4 index scoring + top-k 2048) on 1 GB300"
+    dtype_name = "int8 (FP4 E2M1 codes, dp4a) + f32"
+    data_desc = ("synthetic (seeded N(0,1) index queries and head weights; FP4 index records "
+                 "with codes drawn from a fixed distribution, scale bytes 124..127)")
+
+    def __init__(self, sa, c: synth.IndexCase, dev, seed=1006):
+        self.sa, self.c, self.dev = sa, c, dev
+        inp = synth.make_index_inputs(c, seed, device=dev)
+        self.keys = inp["keys"]                     # resident, like the index-key cache
+        self.s_in = Staging([inp["query"], inp["weight"]], dev)
+        self.query, self.weight = self.s_in.views
+        self.s_out = Staging([torch.empty((c.B, 1, c.S, c.topk), dtype=torch.int32, device=dev),
+                              torch.zeros(1, dtype=torch.int32, device=dev)], dev)
+        self.sel, self.err = self.s_out.views
+        self.status = torch.empty(c.B * c.S, dtype=torch.uint8, device=dev)
+        nws = sa.sparse_index_select_workspace(self.query, self.weight, self.keys, topk=c.topk)
+        self.ws = sa.new_workspace(nws, dev)
+        self.rows = c.B * c.S
+        limits = [min(c.R, (c.query_start + s + 1) // 4) for s in range(c.S)] * c.B
+        self.records = int(sum(limits))
+        # integer multiply-adds of the exact dot products: one per (record, head, dim)
+        self.macs = float(self.records) * c.IH * c.ID
+        self.decode_bytes = (self.records * c.stride + self.query.numel() * 4
+                             + self.weight.numel() * 4 + self.sel.numel() * 4)
+        self.launches_per_step = 3  # query finalize, scores, top-k
+
+    def step(self, ev=None):
+        c = self.c
+        if ev is not None:
+            ev[0].record()
+        self.sa.sparse_index_select(self.query, self.weight, self.keys, topk=c.topk,
+                                    query_start=c.query_start, selected=self.sel,
+                                    workspace=self.ws, err_word=self.err,
+                                    row_status=self.status)
+        if ev is not None:
+            ev[1].record()
+
+    def h2d(self):
+        return self.s_in.h2d()  # index queries and head weights
+
+    def d2h(self):
+        return self.s_out.d2h()  # selected indices and the error word
+
+    def config(self):
+        c = self.c
+        return {"workload": c.name, "batch": c.B, "queries": c.S, "index_heads": c.IH,
+                "index_dim": c.ID, "records": c.R, "top_k": c.topk,
+                "query_position": c.query_start, "record_bytes": c.stride,
+                "step": "one sparse_index_select call: query finalize (bf16, Hadamard, FP4), "
+                        "scores (exact dp4a block dots), top-k (hash tie check, radix select, "
+                        "bitonic sort) -- 3 kernels"}
+
+    def oracle_rows(self, rows):
+        import oracle
+        c = self.c
+        if not hasattr(self, "_host"):
+            self._host = (self.query.cpu(), self.weight.cpu(), self.keys.cpu())
+        q, w, k = self._host
+        out = []
+        for r in rows:
+            b, s = divmod(r, c.S)
+            sel, _, _ = oracle.index_select(q[b:b + 1, s:s + 1], w[b:b + 1, s:s + 1],
+                                            k[b:b + 1], topk=c.topk, query_start=c.query_start + s)
+            out.append(sel[0, 0, 0])
+        return np.stack(out)
+
+    def roofline(self, ms, kernel_ms, peaks):
+        # the score kernel: integer dp4a, bound by the SMs' integer pipes
+        dp4a_peak = DP4A_PER_SM_PER_CLOCK * SMS * SM_MAX_GHZ * 1e9 * 4 * 2 / 1e12  # TOP/s
+        ops = 2.0 * self.macs
+        achieved = ops / (kernel_ms * 1e-3) / 1e12
+        call = ops / (ms * 1e-3) / 1e12
+        return {"bound": "alu", "kernel": "index_score_kernel", "achieved": round(achieved, 2),
+                "peak": round(dp4a_peak, 1), "unit": "TOP/s (int8 multiply + add)",
+                "frac": round(achieved / dp4a_peak, 4),
+                "traffic": traffic_for(self.c.name, "index_score_kernel"),
+                "peak_source": "derived: 152 SMs x %d dp4a per SM per clock x 2.07 GHz "
+                               "(measured dp4a issue rate) x 4 multiply-adds" %
+                               DP4A_PER_SM_PER_CLOCK,
+                "algorithmic_ops": ops, "kernel_us": round(kernel_ms * 1e3, 2),
+                "call_us": round(ms * 1e3, 2), "call_achieved": round(call, 2),
+                "call_frac": round(call / dp4a_peak, 4),
+                "algorithmic_bytes": int(self.decode_bytes),
+                "call_hbm_gbs": round(self.decode_bytes / (ms * 1e-3) / 1e9, 1)}
+
+
+SMS = 152
+SM_MAX_GHZ = 2.07
+DP4A_PER_SM_PER_CLOCK = 64  # placeholder until measured
+
+
 # DRAM bytes (read + write) per launch of the dominant kernel from an ncu
 # capture, keyed by workload, each with the hash of the kernel's source files
 # at capture time (kernel_source_hash): a value whose hash no longer matches
@@ -507,6 +605,7 @@ KERNEL_SOURCES = {
                         "kernels.h"],
     "fp8_decode_kernel": ["k_fp8.cu", "gather_common.cuh", "common.cuh", "kernels.h"],
     "prefill_tc05_kernel": ["k_prefill.cu", "common.cuh", "tc05.cuh", "kernels.h"],
+    "index_score_kernel": ["k_index.cu", "common.cuh", "kernels.h"],
 }
 
 TRAFFIC: dict = {
@@ -574,6 +673,8 @@ def make_workload(sa, name, dev):
         return CsaFp8Decode(sa, synth.csa_fp8(), dev)
     if name == "prefill_bf16":
         return Prefill(sa, synth.prefill_bf16(), dev)
+    if name == "index_select":
+        return IndexSelect(sa, synth.index_select_fp4(), dev)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -729,8 +830,10 @@ def run_gpu(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": str(wl.q.dtype).replace("torch.", "").replace("bfloat16", "bf16"),
-            "data": "synthetic (seeded N(0,1) Q/K/V, uniform sorted top-k indices)",
+            "dtype": getattr(wl, "dtype_name", None)
+            or str(wl.q.dtype).replace("torch.", "").replace("bfloat16", "bf16"),
+            "data": getattr(wl, "data_desc", None)
+            or "synthetic (seeded N(0,1) Q/K/V, uniform sorted top-k indices)",
             "config": dict(wl.config(), parallelism=f"replicas x{ws}" if ws > 1 else "single GPU",
                            l2="flushed between steps outside the step events: a 512 MB write, "
                               "then a 256 MB read that writes the flush's dirty lines back",

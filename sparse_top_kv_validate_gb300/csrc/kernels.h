@@ -181,8 +181,8 @@ bool prefill_tc_supported(const PrefillTcArgs& a);
 int launch_prefill_tc(const PrefillTcArgs& a, cudaStream_t st);
 
 // ---- ratio-4 index scoring and top-k selection ----------------------------------------
-constexpr int kQmetaZero = 1 << 30;       // index-query head whose codes are all zero
-constexpr int kQmetaNonfinite = 1 << 29;  // index-query head with a non-finite block
+constexpr int kQinfoZero = 1;             // index-query head whose codes are all zero
+constexpr int kQinfoNonfinite = 2;        // index-query head with a non-finite block
 constexpr int kSelTie = 1;                // row status: equal scores in the row
 constexpr int kSelNonfinite = 2;          // row status: a score is NaN or infinite
 constexpr int kSelErrShift = 9;           // row status << shift = err_word bits
@@ -203,17 +203,21 @@ struct IndexArgs {
   // workspace
   int8_t* qcodes;             // [rows, IH, ID] signed 2 * E2M1 codes
   int8_t* qexp;               // [rows, IH, ID / 32] block exponents (127: non-finite)
-  int32_t* qmeta;             // [rows, IH] exponent range / zero / non-finite
+  int4* qinfo;                // [rows, IH] {exponent range, min, max, zero / non-finite}
+  float* qscale;              // [rows, IH, ID / 32] 2^(block exponent)
   float* scores;              // [rows, R]
-  uint32_t* gkeys;            // [rows, R] when the top-k state is in global memory
-  uint32_t* ghash;            // [rows, hash_slots]
-  int topk_global;            // 1: top-k keys and hash in the workspace
-  int hash_slots;             // power of two >= 2 R and >= 2 next_pow2(topk)
+  uint32_t* hist;             // [rows, 2048] counts of the rank keys' top 11 bits
+  uint32_t* rowflags;         // [rows] SEL_TIE / SEL_NONFINITE found while scoring
+  uint32_t* done;             // [rows] CTAs of the selection kernel finished with the row
+  unsigned long long* bucket; // [rows, R] (rank key, record) of the threshold bin
+  int hash_slots;             // equal-score hash set: power of two >= 2 R, in parts
   int hash_log2;
+  int sel_slots;              // next power of two >= topk
   void* ev_before;            // nullable measurement events around the score kernel
   void* ev_after;
 };
-size_t index_topk_smem_bytes(int64_t R, int hash_slots);
+size_t index_topk_smem_bytes(int64_t sel_slots);
+size_t index_tie_smem_bytes(int hash_slots);
 size_t index_score_smem_bytes(int64_t IH, int64_t ID, int64_t key_stride);
 int launch_index_select(const IndexArgs& a, cudaStream_t st);
 

@@ -834,7 +834,9 @@ static int check_index(const sa_index_select_params* p, int query = 0) {
   if (p->IH > 256 || p->topk > 4096) return SA_ERR_UNSUPPORTED;
   if (p->key_stride < p->ID / 32 * 17 || p->key_stride % 4) return SA_ERR_SHAPE;
   if (p->key_stride * 256 > 64 * 1024) return SA_ERR_UNSUPPORTED;
-  if (p->B * p->R >= (int64_t(1) << 31) || p->R >= (int64_t(1) << 28)) return SA_ERR_UNSUPPORTED;
+  // rows up to 2^17 records (a 512K-token context at ratio 4): the
+  // equal-score hash set of a row (2 R slots in 8 parts) fits in shared memory
+  if (p->B * p->R >= (int64_t(1) << 31) || p->R > (int64_t(1) << 17)) return SA_ERR_UNSUPPORTED;
   if (reinterpret_cast<uintptr_t>(p->keys) % 4 || reinterpret_cast<uintptr_t>(p->query) % 4 ||
       reinterpret_cast<uintptr_t>(p->weight) % 4 || reinterpret_cast<uintptr_t>(p->selected) % 4)
     return SA_ERR_ALIGN;
@@ -861,39 +863,42 @@ static size_t index_plan(const sa_index_select_params* p, sa::IndexArgs& a, char
   a.out_heads = p->out_heads;
   int64_t slots = 2;
   while (slots < 2 * p->R) slots <<= 1;
-  int64_t kp = 1;
-  while (kp < p->topk) kp <<= 1;
-  if (slots < 2 * kp) slots = 2 * kp;
   a.hash_slots = static_cast<int>(slots);
   int lg = 0;
   while ((int64_t(1) << lg) < slots) ++lg;
   a.hash_log2 = lg;
-  a.topk_global = sa::index_topk_smem_bytes(p->R, a.hash_slots) > size_t(200) * 1024 ? 1 : 0;
+  int64_t sp = 1;
+  while (sp < p->topk) sp <<= 1;
+  a.sel_slots = static_cast<int>(sp);
   size_t off = 0;
   const size_t o_codes = off;
   off += align_up(static_cast<size_t>(a.rows * p->IH * p->ID));
   const size_t o_exp = off;
   off += align_up(static_cast<size_t>(a.rows * p->IH * (p->ID / 32)));
-  const size_t o_meta = off;
-  off += align_up(static_cast<size_t>(a.rows * p->IH) * 4);
+  const size_t o_info = off;
+  off += align_up(static_cast<size_t>(a.rows * p->IH) * 16);
+  const size_t o_qs = off;
+  off += align_up(static_cast<size_t>(a.rows * p->IH * (p->ID / 32)) * 4);
   const size_t o_scores = off;
   off += align_up(static_cast<size_t>(a.rows * p->R) * 4);
-  size_t o_keys = 0, o_hash = 0;
-  if (a.topk_global) {
-    o_keys = off;
-    off += align_up(static_cast<size_t>(a.rows * p->R) * 4);
-    o_hash = off;
-    off += align_up(static_cast<size_t>(a.rows) * static_cast<size_t>(slots) * 4);
-  }
+  const size_t o_hist = off;
+  off += align_up(static_cast<size_t>(a.rows) * 2048 * 4);
+  const size_t o_flags = off;
+  off += align_up(static_cast<size_t>(a.rows) * 4);
+  const size_t o_done = off;
+  off += align_up(static_cast<size_t>(a.rows) * 4);
+  const size_t o_bucket = off;
+  off += align_up(static_cast<size_t>(a.rows * p->R) * 8);
   if (ws) {
     a.qcodes = reinterpret_cast<int8_t*>(ws + o_codes);
     a.qexp = reinterpret_cast<int8_t*>(ws + o_exp);
-    a.qmeta = reinterpret_cast<int32_t*>(ws + o_meta);
+    a.qinfo = reinterpret_cast<int4*>(ws + o_info);
+    a.qscale = reinterpret_cast<float*>(ws + o_qs);
     a.scores = reinterpret_cast<float*>(ws + o_scores);
-    if (a.topk_global) {
-      a.gkeys = reinterpret_cast<uint32_t*>(ws + o_keys);
-      a.ghash = reinterpret_cast<uint32_t*>(ws + o_hash);
-    }
+    a.hist = reinterpret_cast<uint32_t*>(ws + o_hist);
+    a.rowflags = reinterpret_cast<uint32_t*>(ws + o_flags);
+    a.done = reinterpret_cast<uint32_t*>(ws + o_done);
+    a.bucket = reinterpret_cast<unsigned long long*>(ws + o_bucket);
   }
   return off;
 }

@@ -105,11 +105,11 @@ def test_nonfinite_key_scales(cuda_lib):
     _check(cuda_lib, c, inp, "non-finite scales")
 
 
-def test_topk_state_in_global_memory_for_long_rows(cuda_lib):
-    # 20,000 records: the hash set and keys no longer fit in shared memory
+def test_long_rows(cuda_lib):
+    # 20,000 records: a hash set of 65,536 slots in 8 parts, a large threshold bin
     c = _case(B=2, S=1, IH=4, ID=32, R=20000, topk=1000, query_start=100000)
     inp = synth.make_index_inputs(c, seed=26)
-    _check(cuda_lib, c, inp, "global top-k state", ascending=True)
+    _check(cuda_lib, c, inp, "long rows", ascending=True)
 
 
 def test_deterministic_and_independent_of_workspace_contents(cuda_lib):
