@@ -78,6 +78,14 @@ class _SelectArgs(C.Structure):
 SEL_TIE, SEL_NONFINITE = 1, 2
 
 
+class _PrefillMask(C.Structure):
+    _fields_ = [("mask", _p), ("kind", C.c_int), ("rank", _i64), ("dims", _i64 * 4),
+                ("nonpad", _p)]
+
+
+MASK_NONE, MASK_F32, MASK_F16, MASK_BF16, MASK_BOOL = 0, 1, 2, 3, 4
+
+
 def lib():
     global _lib
     with _lock:
@@ -122,6 +130,10 @@ def lib():
             L.orc_index_query_finalize.argtypes = [_p, _i64, _p]
             L.orc_index_select.restype = C.c_int
             L.orc_index_select.argtypes = [C.POINTER(_SelectArgs), _p, _p, _p, _p]
+            L.orc_prefill_masked.restype = C.c_int
+            L.orc_prefill_masked.argtypes = [_p, _p, _p, C.c_int, _i64, _i64, _i64, _i64, _i64,
+                                             C.c_int, C.c_double, C.c_double,
+                                             C.POINTER(_PrefillMask), _p, _i64, _p]
             L.orc_paged_decode.restype = C.c_int
             L.orc_paged_decode.argtypes = [_p, _p, _p, C.c_int, _p, _p, _i64, _i64, _i64,
                                            _i64, _i64, _i64, C.c_double, _p, _i64, _p]
@@ -298,16 +310,39 @@ def sparse_attention(q, idx, k=None, v=None, records=None, *, scale: float,
 
 
 def prefill(q, k, v, *, scale: float, causal: bool = True, softcap: float = 0.0,
-            rows=None) -> np.ndarray:
+            rows=None, attn_mask=None, nonpad_kv_seqlen=None) -> np.ndarray:
+    """Dense prefill; ``attn_mask`` (float32 / float16 / bfloat16 / bool, rank
+    <= 4, broadcast against ``[B, Hq, S, S]``) and ``nonpad_kv_seqlen`` (int64
+    ``[B]``) as in ``orc_prefill_masked``."""
     qh, kh, vh = _host(q), _host(k), _host(v)
     B, Hq, S, D = qh.shape
     Hkv = kh.shape[1]
     r, nr = _rows_arg(rows)
     n = nr if r is not None else B * Hq * S
     y = np.zeros((n, D), dtype=np.float64)
-    rc = lib().orc_prefill(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), _dtype_code(qh), B,
-                           Hq, Hkv, S, D, int(causal), scale, softcap, _ptr(r), nr,
-                           y.ctypes.data)
+    if attn_mask is None and nonpad_kv_seqlen is None:
+        rc = lib().orc_prefill(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), _dtype_code(qh), B,
+                               Hq, Hkv, S, D, int(causal), scale, softcap, _ptr(r), nr,
+                               y.ctypes.data)
+    else:
+        mk = _PrefillMask()
+        mh = None
+        if attn_mask is not None:
+            mh = _host(torch.as_tensor(attn_mask))
+            kinds = {torch.float32: MASK_F32, torch.float16: MASK_F16,
+                     torch.bfloat16: MASK_BF16, torch.bool: MASK_BOOL}
+            mk.kind = kinds[mh.dtype]
+            if mh.dtype == torch.bool:
+                mh = mh.to(torch.uint8)
+            mk.mask, mk.rank = mh.data_ptr(), mh.dim()
+            for i_, e_ in enumerate(mh.shape):
+                mk.dims[i_] = e_
+        npad = None if nonpad_kv_seqlen is None else _host(
+            torch.as_tensor(nonpad_kv_seqlen, dtype=torch.int64))
+        mk.nonpad = _ptr(npad)
+        rc = lib().orc_prefill_masked(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(),
+                                      _dtype_code(qh), B, Hq, Hkv, S, D, int(causal), scale,
+                                      softcap, C.byref(mk), _ptr(r), nr, y.ctypes.data)
     if rc != 0:
         raise ValueError("oracle rejected the prefill shape")
     return y

@@ -24,6 +24,8 @@
  *   [IS] `bias_at` and `validate_bias_shape`: the optional additive bias of a
  *         selected-token score, a tensor of rank <= 4 broadcast right-aligned
  *         against [batch, q_head, query, cache position].
+ *   [SA] `mask_bias` and the padding frontier (`nonpad_kv_seqlen`) of
+ *         `attention_row`: the attention mask and the causal offset.
  *   OCP 8-bit floating point specification (E4M3FN) and the OCP MX
  *   specification (E8M0 scale) for the FP8 record decode.
  *
@@ -530,6 +532,106 @@ int orc_sparse_attention(const orc_sparse_args* a, const int64_t* rows, int64_t 
 /* ------------------------------------------------------------------------ */
 /* Dense prefill ([SA] Semantics, attention_row), no past.                   */
 /* ------------------------------------------------------------------------ */
+
+/* [SA] mask_bias: the attention-mask term of logical element (b, h, i, j).
+ * The mask's shape lines up with [B, Hq, S, S] from the right (an axis of 1
+ * broadcasts).  The last axis is the key axis: a key j at or past its extent
+ * takes -inf (so a last axis shorter than S, 1 included, pads with -inf); a bool mask keeps a key where it is nonzero (term 0) and masks it
+ * where it is zero (-inf); f32 / f16 / bf16 masks add their value. */
+#define ORC_MASK_NONE 0
+#define ORC_MASK_F32 1
+#define ORC_MASK_F16 2
+#define ORC_MASK_BF16 3
+#define ORC_MASK_BOOL 4
+static double orc_mask_at(const void* mask, int kind, int64_t rank, const int64_t* dims,
+                          int64_t b, int64_t h, int64_t i, int64_t j) {
+  int64_t logical[4] = {b, h, i, j};
+  int64_t off = 0;
+  if (rank > 0 && j >= dims[rank - 1]) { /* (an extent of 1 included) */
+    return -INFINITY;
+  }
+  for (int64_t r = 0; r < rank; ++r) {
+    int64_t axis = 4 - rank + r;
+    int64_t extent = dims[r];
+    int64_t index = (extent == 1) ? 0 : logical[axis];
+    off = off * extent + index;
+  }
+  switch (kind) {
+    case ORC_MASK_F32:
+      return (double)((const float*)mask)[off];
+    case ORC_MASK_F16:
+      return orc_f16_to_double(((const uint16_t*)mask)[off]);
+    case ORC_MASK_BF16:
+      return orc_bf16_to_double(((const uint16_t*)mask)[off]);
+    case ORC_MASK_BOOL:
+      return ((const uint8_t*)mask)[off] != 0 ? 0.0 : -INFINITY;
+    default:
+      return 0.0;
+  }
+}
+
+typedef struct {
+  const void* mask;          /* nullable */
+  int kind;                  /* ORC_MASK_* */
+  int64_t rank;
+  int64_t dims[4];
+  const int64_t* nonpad;     /* nullable: per-batch valid key count */
+} orc_prefill_mask;
+
+/* Q [B, Hq, S, D], K/V [B, Hkv, S, D] ([SA] Semantics, attention_row, no
+ * past).  Keys j >= nonpad[b] are masked (the padding frontier) when nonpad
+ * is given; when causal, query i sees keys j <= i + offset with offset =
+ * nonpad[b] - S (0 without nonpad), so a row with i + offset < 0 is fully
+ * masked; the mask term is added after the softcap.  Rows flattened
+ * (b, h, i). */
+int orc_prefill_masked(const void* q, const void* k, const void* v, int dtype, int64_t B,
+                       int64_t Hq, int64_t Hkv, int64_t S, int64_t D, int causal, double scale,
+                       double softcap, const orc_prefill_mask* mk, const int64_t* rows,
+                       int64_t nrows, double* y) {
+  if (Hkv <= 0 || Hq % Hkv != 0) {
+    return -1;
+  }
+  int64_t g = Hq / Hkv;
+  int64_t total = B * Hq * S;
+  int64_t count = rows ? nrows : total;
+  orc_kv kv = {k, v, dtype, Hkv, S, D, D, 0, 0};
+  int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)S);
+  int* masked = (int*)malloc(sizeof(int) * (size_t)S);
+  double* brow = (double*)malloc(sizeof(double) * (size_t)S);
+  double* qr = (double*)malloc(sizeof(double) * (size_t)D);
+  int with_mask = mk && mk->mask && mk->kind != ORC_MASK_NONE;
+  for (int64_t r = 0; r < count; ++r) {
+    int64_t row = rows ? rows[r] : r;
+    int64_t i = row % S;
+    int64_t h = (row / S) % Hq;
+    int64_t b = row / (S * Hq);
+    int64_t pad = (mk && mk->nonpad) ? mk->nonpad[b] : -1;
+    int64_t offset = (mk && mk->nonpad) ? mk->nonpad[b] - S : 0;
+    for (int64_t d = 0; d < D; ++d) {
+      qr[d] = load_elem(q, ((b * Hq + h) * S + i) * D + d, dtype);
+    }
+    for (int64_t j = 0; j < S; ++j) {
+      keys[j] = j;
+      int m = 0;
+      if (pad >= 0 && j >= pad) {
+        m = 1;
+      }
+      if (causal && j > i + offset) {
+        m = 1;
+      }
+      masked[j] = m;
+      brow[j] = (with_mask && !m) ? orc_mask_at(mk->mask, mk->kind, mk->rank, mk->dims, b, h, i, j)
+                                  : 0.0;
+    }
+    attend_row(&kv, b, h / g, qr, keys, masked, S, scale, softcap, with_mask ? brow : NULL, NULL,
+               y + r * D);
+  }
+  free(keys);
+  free(masked);
+  free(brow);
+  free(qr);
+  return 0;
+}
 
 /* Q [B, Hq, S, D], K/V [B, Hkv, S, D]; query i sees keys 0..i when causal,
  * all S keys otherwise.  Rows flattened (b, h, i). */

@@ -441,6 +441,98 @@ def test_bias_shape_not_broadcastable_is_rejected():
         oracle.sparse_attention(q, idx, k, k, scale=1.0, bias=torch.zeros(3, 1, 10))
 
 
+def test_prefill_mask_and_padding_golden():
+    with open(os.path.join(GOLDEN, "prefill_mask_two_token.txt")) as f:
+        rows = {l.split()[0]: (float(l.split()[1]), float(l.split()[2]))
+                for l in f if l.strip() and not l.startswith("#")}
+    ln3 = float(np.float32(math.log(3.0)))
+    q = torch.tensor([1.0, 1.0], dtype=torch.float32).reshape(1, 1, 2, 1)
+    k = torch.tensor([0.0, ln3], dtype=torch.float32).reshape(1, 1, 2, 1)
+    v = torch.tensor([0.0, 4.0], dtype=torch.float32).reshape(1, 1, 2, 1)
+
+    def run(**kw):
+        return oracle.prefill(q, k, v, scale=1.0, **kw)[:, 0]
+
+    cases = {
+        "bool_full": run(causal=False, attn_mask=torch.tensor([[True, False], [True, True]])),
+        "f32_full": run(causal=False, attn_mask=torch.tensor([[0.0, 0.0], [ln3, 0.0]])),
+        "bool_short": run(causal=False, attn_mask=torch.tensor([[True], [True]])),
+        "causal_nonpad1": run(causal=True, nonpad_kv_seqlen=[1]),
+        "causal_nonpad2": run(causal=True, nonpad_kv_seqlen=[2]),
+    }
+    assert set(cases) == set(rows)
+    for name, y in cases.items():
+        assert np.allclose(y, rows[name], rtol=0, atol=1e-6), (name, y)
+
+
+def _brute_prefill(q, k, v, scale, causal, softcap, mask_full, nonpad):
+    """Masked dense attention in matrix form with numpy broadcasting."""
+    B, Hq, S, D = q.shape
+    g = Hq // k.shape[1]
+    y = np.zeros((B, Hq, S, D))
+    for b in range(B):
+        for h in range(Hq):
+            s = (as64(q[b, h]) @ as64(k[b, h // g]).T) * scale
+            if softcap:
+                s = softcap * np.tanh(s / softcap)
+            allowed = np.ones((S, S), dtype=bool)
+            off = 0
+            if nonpad is not None:
+                allowed[:, nonpad[b]:] = False
+                off = nonpad[b] - S
+            if causal:
+                allowed &= np.arange(S)[None, :] <= np.arange(S)[:, None] + off
+            if mask_full is not None:
+                s = s + np.where(allowed, mask_full[b, h], 0.0)
+            s = np.where(allowed, s, -np.inf)
+            for i in range(S):
+                if np.isneginf(s[i]).all():
+                    continue
+                w = np.exp(s[i] - s[i].max())
+                y[b, h, i] = (w / w.sum()) @ as64(v[b, h // g])
+    return y
+
+
+@pytest.mark.parametrize("kind", ["bool_ss", "f32_b1ss", "bf16_hss", "f16_s", "none"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_mask_and_padding_match_brute_force(kind, causal):
+    B, Hq, Hkv, S, D = 2, 4, 2, 12, 8
+    q = synth.normal((B, Hq, S, D), "f32", 101)
+    k = synth.normal((B, Hkv, S, D), "f32", 102)
+    v = synth.normal((B, Hkv, S, D), "f32", 103)
+    g = torch.Generator().manual_seed(104)
+    shape = {"bool_ss": (S, S), "f32_b1ss": (B, 1, S, S), "bf16_hss": (Hq, S, S),
+             "f16_s": (S,), "none": None}[kind]
+    mask = None
+    full = None
+    if shape is not None:
+        if kind.startswith("bool"):
+            mask = torch.rand(shape, generator=g) > 0.3
+            full = np.broadcast_to(np.where(mask.numpy(), 0.0, -np.inf), (B, Hq, S, S))
+        else:
+            dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[
+                kind.split("_")[0]]
+            mask = (torch.randn(shape, generator=g) * 2.0).to(dt)
+            full = np.broadcast_to(mask.double().numpy(), (B, Hq, S, S))
+    nonpad = [9, 12]
+    y = oracle.prefill(q, k, v, scale=0.35, causal=causal, softcap=4.0, attn_mask=mask,
+                       nonpad_kv_seqlen=nonpad).reshape(B, Hq, S, D)
+    exp = _brute_prefill(q, k, v, 0.35, causal, 4.0, full, nonpad)
+    assert np.allclose(y, exp, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_padding_to_full_length_and_zero_mask_change_nothing():
+    B, Hq, Hkv, S, D = 2, 4, 2, 10, 8
+    q = synth.normal((B, Hq, S, D), "bf16", 111)
+    k = synth.normal((B, Hkv, S, D), "bf16", 112)
+    v = synth.normal((B, Hkv, S, D), "bf16", 113)
+    base = oracle.prefill(q, k, v, scale=0.3, causal=True)
+    assert np.array_equal(oracle.prefill(q, k, v, scale=0.3, causal=True,
+                                         nonpad_kv_seqlen=[S, S]), base)
+    assert np.array_equal(oracle.prefill(q, k, v, scale=0.3, causal=True,
+                                         attn_mask=torch.zeros(S, S)), base)
+
+
 def test_window_union_matches_brute_force_and_counts_each_key_once():
     B, T, D, K, W = 2, 50, 8, 6, 10
     q = synth.normal((B, 3, 1, D), "f32", 51)
