@@ -329,6 +329,13 @@ typedef struct {
 size_t sparse_index_select_workspace(const sa_index_select_params* p);
 int sparse_index_select(const sa_index_select_params* p, void* stream);
 
+/* attention-mask element types of sa_prefill_params.mask_kind */
+#define SA_MASK_NONE 0
+#define SA_MASK_F32 1
+#define SA_MASK_F16 2
+#define SA_MASK_BF16 3
+#define SA_MASK_BOOL 4  /* one byte per element: nonzero keeps the key */
+
 /*
  * attn_prefill -- [SA] Semantics with no past: q [B, Hq, S, D],
  * k/v [B, Hkv, S, D] (GQA, Hq % Hkv == 0), y [B, Hq, S, D]; query i sees
@@ -341,6 +348,17 @@ int sparse_index_select(const sa_index_select_params* p, void* stream);
  * (a misaligned y there is SA_ERR_ALIGN); other shapes take the general
  * kernel.  err_word (nullable) receives SA_ERRBIT_TIMEOUT if the tensor-core
  * pipeline stalled, in which case y is unspecified.
+ * nonpad_kv_seqlen (nullable device int64 [B]; [SA] attention_row's padding
+ * frontier): keys j >= nonpad[b] are masked (a negative entry disables that),
+ * and a causal query i then sees keys j <= i + nonpad[b] - S; a row left with
+ * no key gives 0.  Served by the tcgen05 kernel.
+ * attn_mask (nullable device, [SA] mask_bias): mask_kind elements in a dense
+ * row-major tensor of shape mask_dims[0 .. mask_rank-1], rank <= 4, broadcast
+ * right-aligned against [B, Hq, S, S] (every axis but the last 1 or its
+ * target; the last is the key axis: keys at or past its extent take -inf);
+ * float masks add their value after the softcap, bool masks keep a key where
+ * nonzero.  A request with a mask runs on the per-row kernels (correct, not
+ * tuned) and writes present K/V by a separate copy.
  */
 typedef struct {
   const void* q;
@@ -357,6 +375,12 @@ typedef struct {
   void* workspace;
   size_t workspace_bytes;
   uint32_t* err_word;   /* nullable: SA_ERRBIT_TIMEOUT if a tensor-core pipeline stalled */
+  const void* attn_mask;
+  int32_t mask_kind;    /* SA_MASK_NONE / _F32 / _F16 / _BF16 / _BOOL */
+  int32_t reserved_;    /* must be 0 */
+  int64_t mask_rank;
+  int64_t mask_dims[4];
+  const int64_t* nonpad_kv_seqlen;
 } sa_prefill_params;
 
 size_t attn_prefill_workspace(const sa_prefill_params* p);

@@ -74,6 +74,8 @@ class PrefillParams(C.Structure):
         ("B", _i64), ("Hq", _i64), ("Hkv", _i64), ("S", _i64), ("D", _i64),
         ("scale", C.c_float), ("softcap", C.c_float),
         ("workspace", _p), ("workspace_bytes", C.c_size_t), ("err_word", _p),
+        ("attn_mask", _p), ("mask_kind", _i32), ("reserved_", _i32), ("mask_rank", _i64),
+        ("mask_dims", _i64 * 4), ("nonpad_kv_seqlen", _p),
     ]
 
 
@@ -384,7 +386,12 @@ def sparse_attn_decode(q, k_cache, v_cache, idx, *, y=None, workspace=None, stre
     return y
 
 
-def _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap, err_word=None):
+_MASK_KIND = {torch.float32: 1, torch.float16: 2, torch.bfloat16: 3, torch.bool: 4,
+              torch.uint8: 4}
+
+
+def _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap, err_word=None,
+                    attn_mask=None, nonpad_kv_seqlen=None):
     p = PrefillParams()
     B, Hq, S, D = q.shape
     p.q, p.k, p.v, p.y = q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(y)
@@ -393,25 +400,40 @@ def _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap, er
     p.B, p.Hq, p.Hkv, p.S, p.D = B, Hq, k.shape[1], S, D
     p.scale, p.softcap = float(scale), float(softcap)
     p.err_word = _ptr(err_word)
+    if attn_mask is not None:
+        if attn_mask.dtype not in _MASK_KIND or attn_mask.dim() > 4:
+            raise ValueError("attn_mask: float32/float16/bfloat16/bool of rank <= 4")
+        p.attn_mask, p.mask_kind = attn_mask.data_ptr(), _MASK_KIND[attn_mask.dtype]
+        p.mask_rank = attn_mask.dim()
+        for r, e in enumerate(attn_mask.shape):
+            p.mask_dims[r] = e
+    p.nonpad_kv_seqlen = _ptr(nonpad_kv_seqlen)
     return p
 
 
-def attn_prefill_workspace(q, k, v, causal=True, scale=0.0, softcap=0.0) -> int:
-    p = _prefill_params(q, k, v, None, None, None, causal, scale, softcap)
+def attn_prefill_workspace(q, k, v, causal=True, scale=0.0, softcap=0.0, attn_mask=None,
+                           nonpad_kv_seqlen=None) -> int:
+    p = _prefill_params(q, k, v, None, None, None, causal, scale, softcap, None, attn_mask,
+                        nonpad_kv_seqlen)
     return int(load().attn_prefill_workspace(C.byref(p)))
 
 
 def attn_prefill(q, k, v, *, causal=True, scale=0.0, softcap=0.0, y=None, present_k=None,
-                 present_v=None, err_word=None, workspace=None, stream=None):
+                 present_v=None, err_word=None, workspace=None, stream=None, attn_mask=None,
+                 nonpad_kv_seqlen=None):
     """Dense prefill, ``q [B,Hq,S,D]``, ``k/v [B,Hkv,S,D]``; optional exact
-    present K/V copies.  Returns ``y``."""
+    present K/V copies, ``attn_mask`` (float32/float16/bfloat16/bool, rank <=
+    4, broadcast against ``[B,Hq,S,S]``) and ``nonpad_kv_seqlen`` (int64
+    ``[B]``).  Returns ``y``."""
     L = load()
     for n, t in (("q", q), ("k", k), ("v", v), ("present_k", present_k),
-                 ("present_v", present_v)):
+                 ("present_v", present_v), ("attn_mask", attn_mask),
+                 ("nonpad_kv_seqlen", nonpad_kv_seqlen)):
         _dev(t, n)
     if y is None:
         y = torch.empty_like(q)
-    p = _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap, err_word)
+    p = _prefill_params(q, k, v, y, present_k, present_v, causal, scale, softcap, err_word,
+                        attn_mask, nonpad_kv_seqlen)
     need = int(L.attn_prefill_workspace(C.byref(p)))
     ws, nb = _workspace(need, q.device, workspace)
     p.workspace, p.workspace_bytes = _ptr(ws), nb

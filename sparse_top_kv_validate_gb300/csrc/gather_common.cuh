@@ -34,6 +34,35 @@ __device__ __forceinline__ UnitInfo unit_info(const GatherArgs& a, int64_t unit)
   return u;
 }
 
+// The additive term of logical element (b, h, i, j): an IndexShare bias or an
+// ONNX attention mask (bool: 0 where set, -inf where clear; a key at or past
+// a short key axis: -inf).
+__device__ __forceinline__ float bias_term(const GatherArgs& a, int64_t b, int64_t h, int64_t i,
+                                           int64_t j) {
+  if (a.bias_key_extent > 0 && j >= a.bias_key_extent) return SA_NEG_INF;
+  const int64_t off = b * a.bias_sb + h * a.bias_sh + i * a.bias_si + j * a.bias_sk;
+  switch (a.bias_kind) {
+    case kBiasF16: return __half2float(__ldg(static_cast<const __half*>(a.bias) + off));
+    case kBiasBF16:
+      return __bfloat162float(__ldg(static_cast<const __nv_bfloat16*>(a.bias) + off));
+    case kBiasBool: return __ldg(static_cast<const uint8_t*>(a.bias) + off) ? 0.0f : SA_NEG_INF;
+    default: return __ldg(static_cast<const float*>(a.bias) + off);
+  }
+}
+
+// Dense source: whether key c of query i of batch b is visible (causal frontier,
+// shifted by the padding frontier nonpad[b] - Sq when given; the frontier itself).
+__device__ __forceinline__ bool dense_visible(const GatherArgs& a, int64_t b, int64_t i,
+                                              int64_t c) {
+  int64_t off = a.past_len;
+  if (a.dense_nonpad) {
+    const int64_t np = __ldg(a.dense_nonpad + b);
+    if (np >= 0 && c >= np) return false;
+    off = np - a.Sq;
+  }
+  return !(a.causal && c > off + i);
+}
+
 // Per-batch write position of the fused current-token append.
 __device__ __forceinline__ int64_t write_pos_of(const GatherArgs& a, int64_t b) {
   return a.write_pos ? a.write_pos[b] : a.T - a.C;

@@ -63,7 +63,7 @@ __device__ __forceinline__ int32_t resolve_candidate(const GatherArgs& a, const 
                                 c % a.page_tokens);
   }
   if (a.source == kDense) {
-    if (a.causal && c > a.past_len + u.i) return -1;
+    if (!dense_visible(a, u.b, u.i, c)) return -1;
     return static_cast<int32_t>((u.b * a.Hkv + u.kvh) * a.T + c);
   }
   int64_t len = a.kv_len ? a.kv_len[u.b] : a.T;
@@ -133,11 +133,10 @@ __global__ void __launch_bounds__(128) gather_simt_kernel(GatherArgs a) {
     float x;
     if (a.softcap != 0.f) x = a.softcap * tanhf(dot * (sl2 / kLog2e) * a.inv_softcap) * kLog2e;
     else x = dot * sl2;
-    if (a.bias) {  // [IS] bias_at, keyed by the cache position (sparse source only)
+    if (a.bias) {  // [IS] bias_at / [SA] mask_bias, keyed by the cache position
       const int64_t j = row - (u.b * a.Hkv + u.kvh) * a.T;
-      x += kLog2e * __ldg(a.bias + u.b * a.bias_sb + h * a.bias_sh + u.i * a.bias_si +
-                          j * a.bias_sk);
-      if (x == SA_NEG_INF) continue;  // a -inf entry masks the key
+      x += kLog2e * bias_term(a, u.b, h, u.i, j);
+      if (x == SA_NEG_INF) continue;  // a -inf term masks the key
     }
     const float mn = fmaxf(m, x);
     const float al = exp2f(m - mn);  // m == -inf -> 0

@@ -242,9 +242,7 @@ __global__ void __launch_bounds__(256, 2) fp8_decode_kernel(GatherArgs a) {
         if (a.bias) {  // [IS] bias_at, keyed by the key's cache position
           const int32_t j = tp[n * 8 + 2 * tig + (e & 1)];
           const int64_t h = hb * kHeads + hg * 16 + gid + 8 * (e >> 1);
-          if (j >= 0)
-            x += kLog2e * __ldg(a.bias + b * a.bias_sb + h * a.bias_sh + qi * a.bias_si +
-                                j * a.bias_sk);
+          if (j >= 0) x += kLog2e * bias_term(a, b, h, qi, j);
         }
         s[n][e] = ((e & 1) ? v1 : v0) ? x : SA_NEG_INF;
       }

@@ -128,7 +128,23 @@ struct PrefillKParams {
   float k1;           // x = score * k1 (scale / softcap), or the raw score
   float c_log2;       // log2-domain multiplier of tanh(x) (softcap * log2e) or of x (scale * log2e)
   float tq[kTanhTerms];  // c_log2 * c_k: the tanh polynomial already in log2 units
+  const int64_t* nonpad;  // nullable [B]: padding frontier (keys >= nonpad masked, causal
+                          // offset nonpad - S)
 };
+
+// Last key query qi of batch b may see (< 0: none): S - 1, or the causal
+// frontier (shifted by the padding frontier's offset), or the padding frontier.
+__device__ __forceinline__ int last_key(const PrefillKParams& p, int b, int qi) {
+  int lim = p.S - 1;
+  int off = 0;
+  if (p.nonpad) {
+    const int64_t np = __ldg(p.nonpad + b);
+    if (np >= 0 && np - 1 < lim) lim = static_cast<int>(np - 1);
+    off = static_cast<int>(max(min(np - p.S, int64_t(1) << 30), -(int64_t(1) << 30)));
+  }
+  if (p.causal) lim = min(lim, qi + off);
+  return lim;
+}
 
 struct Item {
   int b, h, kvh, qt, n;   // n: KV tiles the query tile reads
@@ -144,7 +160,14 @@ __device__ __forceinline__ Item item_of(int w, const PrefillKParams& p) {
   it.b = bh / p.Hq;
   it.h = bh % p.Hq;
   it.kvh = it.h / p.g;
-  it.n = p.causal ? it.qt + 1 : p.nq;
+  if (!p.nonpad) {
+    it.n = p.causal ? it.qt + 1 : p.nq;
+  } else {
+    // tiles up to the tile's last visible key; at least one (its rows may all
+    // be masked, and then give 0)
+    const int lim = last_key(p, it.b, min(it.qt * kTile + kTile - 1, p.S - 1));
+    it.n = lim < 0 ? 1 : min(lim / kTile + 1, p.nq);
+  }
   return it;
 }
 
@@ -578,7 +601,8 @@ __device__ void prefill_softmax(const PrefillKParams& p, uint8_t* sm, uint64_t* 
     if (w >= p.n_items) break;
     const Item it = item_of(w, p);
     const int qi = it.qt * kTile + row;
-    const int lim = p.causal ? min(qi, p.S - 1) : p.S - 1;  // last visible key
+    const int lim = p.nonpad ? last_key(p, it.b, qi)                 // last visible key
+                             : (p.causal ? min(qi, p.S - 1) : p.S - 1);
     float m = SA_NEG_INF, l = 0.0f;
     for (int j = 0; j < it.n; ++j, ++g) {
       const int buf = static_cast<int>(g % kSBufs);
@@ -884,6 +908,7 @@ static int launch_prefill_t(const PrefillTcArgs& a, cudaStream_t st) {
   p.nq = static_cast<int>((a.S + kTile - 1) / kTile);
   p.n_items = p.B * p.Hq * p.nq;
   p.causal = a.causal ? 1 : 0;
+  p.nonpad = a.nonpad;
   const float log2e = 1.4426950408889634f;
   if (a.softcap != 0.0f) {
     const float cap = std::fabs(a.softcap);

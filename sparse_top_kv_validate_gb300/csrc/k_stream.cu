@@ -163,7 +163,7 @@ __device__ __forceinline__ KeyRef key_load(const GatherArgs& a, const Cursor& cu
     k.raw = __ldg(a.pos + cu.prow + c);
   } else if (a.source == kDense) {
     k.base = cu.rowbase;
-    k.raw = (c < cu.nc && !(a.causal && c > a.past_len + cu.ui.i)) ? static_cast<int32_t>(c) : -1;
+    k.raw = (c < cu.nc && dense_visible(a, cu.ui.b, cu.ui.i, c)) ? static_cast<int32_t>(c) : -1;
   } else {
     // c < max_pages * page_tokens < 2^31 (checked on the host): 32-bit division
     const uint32_t c32 = static_cast<uint32_t>(c), pt = static_cast<uint32_t>(a.page_tokens);
@@ -500,9 +500,14 @@ __global__ void __launch_bounds__(SGeo<D, kTma>::kThreads, 1)
     // lane's accumulator rows (keys gid and gid + 8 of the tile)
     int32_t j_lo = -1, j_hi = -1;
     if (kBias) {
-      const int64_t c0 = cur.prow + (t - cur.tu.off) * 16 + gid;
-      if (v_lo) j_lo = __ldg(a.pos + c0);
-      if (v_hi) j_hi = __ldg(a.pos + c0 + 8);
+      const int64_t c0 = (t - cur.tu.off) * 16 + gid;  // candidate of accumulator row gid
+      if (a.source == kSparse) {
+        if (v_lo) j_lo = __ldg(a.pos + cur.prow + c0);
+        if (v_hi) j_hi = __ldg(a.pos + cur.prow + c0 + 8);
+      } else {  // dense: the candidate is the key position
+        if (v_lo) j_lo = static_cast<int32_t>(c0);
+        if (v_hi) j_hi = static_cast<int32_t>(c0 + 8);
+      }
     }
     uint32_t pb[NT][2];
 #pragma unroll
@@ -516,8 +521,7 @@ __global__ void __launch_bounds__(SGeo<D, kTma>::kThreads, 1)
           const int32_t j = (e < 2) ? j_lo : j_hi;
           const int hh = nt * 8 + 2 * tig + (e & 1);
           if (j >= 0 && hh < a.hpu)
-            x += kLog2e * __ldg(a.bias + cur.ui.b * a.bias_sb + (cur.ui.h0 + hh) * a.bias_sh +
-                                cur.ui.i * a.bias_si + j * a.bias_sk);
+            x += kLog2e * bias_term(a, cur.ui.b, cur.ui.h0 + hh, cur.ui.i, j);
         }
         s[nt][e] = ((e < 2) ? v_lo : v_hi) ? x : SA_NEG_INF;
       }
@@ -810,8 +814,8 @@ static int launch_stream_b(const GatherArgs& a, int dtype, int grid, cudaStream_
 
 template <typename T, int D, int NT>
 static int launch_stream_t(const GatherArgs& a, int dtype, int grid, cudaStream_t st) {
-  // the bias is keyed by planned positions: selected-token requests only
-  if (a.bias && a.source == kSparse) return launch_stream_b<T, D, NT, true>(a, dtype, grid, st);
+  // an additive bias (selected tokens) or attention mask (dense prefill)
+  if (a.bias && a.source != kPaged) return launch_stream_b<T, D, NT, true>(a, dtype, grid, st);
   return launch_stream_b<T, D, NT, false>(a, dtype, grid, st);
 }
 

@@ -66,6 +66,7 @@ int launch_plan(const PlanArgs& a, cudaStream_t st);
 
 // ---- gather decode (sparse and paged) ------------------------------------------
 enum KeySource : int { kSparse = 0, kPaged = 1, kDense = 2 };
+enum BiasKind : int { kBiasF32 = 0, kBiasF16 = 1, kBiasBF16 = 2, kBiasBool = 3 };
 
 struct GatherArgs {
   // tensors
@@ -74,9 +75,12 @@ struct GatherArgs {
   const void* v;
   void* y;                    // [B, Hq, Sq, Dv]
   const float* sink;          // nullable [Hq]
-  const float* bias;          // nullable: additive bias, element (b,h,i,j) at
-  int64_t bias_sb, bias_sh;   //   b*bias_sb + h*bias_sh + i*bias_si + j*bias_sk
-  int64_t bias_si, bias_sk;   //   (broadcast axes have stride 0)
+  const void* bias;           // nullable: additive bias / attention mask, element
+  int64_t bias_sb, bias_sh;   //   (b,h,i,j) at b*bias_sb + h*bias_sh + i*bias_si +
+  int64_t bias_si, bias_sk;   //   j*bias_sk (broadcast axes have stride 0)
+  int bias_kind;              // kBiasF32 / kBiasF16 / kBiasBF16 / kBiasBool
+  int64_t bias_key_extent;    // > 0: keys j >= it take -inf (a short mask key axis)
+  const int64_t* dense_nonpad;  // dense source: nullable per-batch padding frontier
   float* part_o;              // unnormalised partial outputs (layout per kernel)
   float* part_ml;             // partial running max (log2 units) and sum
   uint32_t* err_word;
@@ -176,6 +180,7 @@ struct PrefillTcArgs {
   float scale;                // > 0
   float softcap;              // 0 = off
   uint32_t* err_word;         // nullable: SA_ERRBIT_TIMEOUT on a stalled pipeline
+  const int64_t* nonpad;      // nullable [B]: keys >= nonpad[b] masked, causal offset nonpad[b] - S
 };
 bool prefill_tc_supported(const PrefillTcArgs& a);
 int launch_prefill_tc(const PrefillTcArgs& a, cudaStream_t st);

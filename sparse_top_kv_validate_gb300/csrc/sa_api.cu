@@ -607,8 +607,42 @@ int sparse_attn_decode(const sa_sparse_params* p, void* stream) {
 
 // ---- prefill ---------------------------------------------------------------------
 
+// [SA] mask_bias: element strides of the mask's logical axes [B, Hq, S, S]
+// (0 on broadcast or missing axes) and the key-axis extent below which keys
+// are kept (0: no limit).  Every axis but the last is 1 or its target.
+static bool mask_layout(const sa_prefill_params* p, int64_t st[4], int64_t* key_extent) {
+  const int64_t target[4] = {p->B, p->Hq, p->S, p->S};
+  if (p->mask_rank < 0 || p->mask_rank > 4) return false;
+  const int r = static_cast<int>(p->mask_rank);
+  int64_t run = 1;
+  *key_extent = 0;
+  for (int ax = 3; ax >= 0; --ax) {
+    const int k = ax - (4 - r);
+    if (k < 0) {
+      st[ax] = 0;
+      continue;
+    }
+    const int64_t e = p->mask_dims[k];
+    if (e <= 0) return false;
+    if (ax < 3 && e != 1 && e != target[ax]) return false;
+    if (ax == 3 && e < p->S) *key_extent = e;
+    st[ax] = (e == 1) ? 0 : run;
+    run *= e;
+  }
+  return true;
+}
+
 static int check_prefill(const sa_prefill_params* p, int query = 0) {
   if (!p || !p->q || !p->k || !p->v || (!p->y && !query)) return SA_ERR_NULL;
+  if (p->reserved_ != 0) return SA_ERR_UNSUPPORTED;
+  if (p->mask_kind < SA_MASK_NONE || p->mask_kind > SA_MASK_BOOL) return SA_ERR_DTYPE;
+  if (p->mask_kind != SA_MASK_NONE) {
+    if (!p->attn_mask) return SA_ERR_NULL;
+    int64_t st[4], ke;
+    if (!mask_layout(p, st, &ke)) return SA_ERR_SHAPE;
+    const size_t es = p->mask_kind == SA_MASK_F32 ? 4 : p->mask_kind == SA_MASK_BOOL ? 1 : 2;
+    if (reinterpret_cast<uintptr_t>(p->attn_mask) % es) return SA_ERR_ALIGN;
+  }
   if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->S <= 0 || p->D <= 0) return SA_ERR_SHAPE;
   if (p->Hq % p->Hkv != 0) return SA_ERR_SHAPE;
   if (dtype_bytes(p->dtype) == 0) return SA_ERR_DTYPE;
@@ -653,6 +687,20 @@ static void prefill_args(const sa_prefill_params* p, sa::GatherArgs& g) {
   g.scale_log2 = scale * 1.4426950408889634f;
   g.softcap = p->softcap;
   g.inv_softcap = p->softcap != 0.f ? 1.0f / p->softcap : 0.f;
+  g.dense_nonpad = p->nonpad_kv_seqlen;
+  if (p->mask_kind != SA_MASK_NONE) {
+    int64_t st[4];
+    mask_layout(p, st, &g.bias_key_extent);  // checked by check_prefill
+    g.bias = p->attn_mask;
+    g.bias_kind = p->mask_kind == SA_MASK_F16    ? sa::kBiasF16
+                  : p->mask_kind == SA_MASK_BF16 ? sa::kBiasBF16
+                  : p->mask_kind == SA_MASK_BOOL ? sa::kBiasBool
+                                                 : sa::kBiasF32;
+    g.bias_sb = st[0];
+    g.bias_sh = st[1];
+    g.bias_si = st[2];
+    g.bias_sk = st[3];
+  }
 }
 
 static void prefill_tc_args(const sa_prefill_params* p, sa::PrefillTcArgs& a) {
@@ -673,6 +721,11 @@ static void prefill_tc_args(const sa_prefill_params* p, sa::PrefillTcArgs& a) {
   a.scale = p->scale != 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->D));
   a.softcap = p->softcap;
   a.err_word = p->err_word;
+  a.nonpad = p->nonpad_kv_seqlen;
+  if (a.nonpad) {  // present K/V then come from a separate copy (see attn_prefill)
+    a.present_k = nullptr;
+    a.present_v = nullptr;
+  }
 }
 
 // Whether the tcgen05 kernel serves this call (bf16/f16, D in {64, 128},
@@ -680,6 +733,7 @@ static void prefill_tc_args(const sa_prefill_params* p, sa::PrefillTcArgs& a) {
 // output's alignment is not part of the choice (the workspace query has no
 // output): a misaligned y on this path is SA_ERR_ALIGN.
 static bool prefill_on_tc(const sa_prefill_params* p) {
+  if (p->mask_kind != SA_MASK_NONE) return false;  // masks: the per-row kernels
   sa::PrefillTcArgs a;
   prefill_tc_args(p, a);
   a.y = const_cast<void*>(a.q);
@@ -713,8 +767,12 @@ int attn_prefill(const sa_prefill_params* p, void* stream) {
   if (prefill_on_tc(p)) {
     if (!aligned16(p->y) || !aligned16(p->present_k) || !aligned16(p->present_v))
       return SA_ERR_ALIGN;
-    sa::PrefillTcArgs a;  // present K/V are written by the kernel itself
+    sa::PrefillTcArgs a;  // present K/V are written by the kernel itself ...
     prefill_tc_args(p, a);
+    if (p->nonpad_kv_seqlen) {  // ... unless padded rows may skip their tiles
+      rc = copy_present(p, stream);
+      if (rc != SA_OK) return rc;
+    }
     sa::mark_event(t_ev_before, st);
     const int lrc = sa::launch_prefill_tc(a, st);
     sa::mark_event(t_ev_after, st);
