@@ -86,6 +86,17 @@ class _PrefillMask(C.Structure):
 MASK_NONE, MASK_F32, MASK_F16, MASK_BF16, MASK_BOOL = 0, 1, 2, 3, 4
 
 
+class _CsaArgs(C.Structure):
+    _fields_ = [
+        ("query", _p), ("q_dtype", C.c_int), ("window", _p), ("w_dtype", C.c_int),
+        ("records", _p), ("selected", _p), ("sink", _p), ("bias", _p), ("bias_rank", _i64),
+        ("bias_dims", _i64 * 4),
+        ("B", _i64), ("S", _i64), ("H", _i64), ("D", _i64), ("L", _i64), ("R", _i64),
+        ("topk", _i64), ("record_bytes", _i64), ("n_rope", _i64), ("total", _i64),
+        ("scale", C.c_double),
+    ]
+
+
 def lib():
     global _lib
     with _lock:
@@ -134,6 +145,8 @@ def lib():
             L.orc_prefill_masked.argtypes = [_p, _p, _p, C.c_int, _i64, _i64, _i64, _i64, _i64,
                                              C.c_int, C.c_double, C.c_double,
                                              C.POINTER(_PrefillMask), _p, _i64, _p]
+            L.orc_csa_ratio4_attention.restype = C.c_int
+            L.orc_csa_ratio4_attention.argtypes = [C.POINTER(_CsaArgs), _p, C.POINTER(C.c_int)]
             L.orc_paged_decode.restype = C.c_int
             L.orc_paged_decode.argtypes = [_p, _p, _p, C.c_int, _p, _p, _i64, _i64, _i64,
                                            _i64, _i64, _i64, C.c_double, _p, _i64, _p]
@@ -438,3 +451,41 @@ def index_select(query, weight, keys, *, topk: int, query_start: int = 0,
     if want_scores:
         return sel, status, err.value, scores
     return sel, status, err.value
+
+
+# ---------------------------------------------------------------------------
+# compressed sparse attention, ratio 4, the pages' own form
+# ---------------------------------------------------------------------------
+
+def csa_ratio4_attention(query, window, records, selected, *, total: int, n_rope: int,
+                         scale: float = 0.0, sink=None, bias=None):
+    """See ``orc_csa_ratio4_attention``.  query ``[B, S, H, D]`` and window
+    (current_kv) ``[B, L, D]`` float32 or bfloat16; records uint8
+    ``[B, R, record_bytes]``; selected int32 ``[B, S, topk]``; sink ``[H]``;
+    bias float32 of rank <= 4 broadcast against ``[B, H, S, C]``.  Returns
+    ``(y float64 [B, S, H, D], bad_record)``."""
+    qh, wh = _host(query), _host(window)
+    rh = _host(torch.as_tensor(records, dtype=torch.uint8))
+    sh = _host(torch.as_tensor(selected, dtype=torch.int32))
+    B, S, H, D = qh.shape
+    a = _CsaArgs()
+    a.query, a.q_dtype = qh.data_ptr(), _dtype_code(qh)
+    a.window, a.w_dtype = wh.data_ptr(), _dtype_code(wh)
+    a.records, a.selected = rh.data_ptr(), sh.data_ptr()
+    sk = None if sink is None else _host(torch.as_tensor(sink, dtype=torch.float64))
+    a.sink = _ptr(sk)
+    bh = None
+    if bias is not None:
+        bh = _host(torch.as_tensor(bias)).to(torch.float32)
+        a.bias, a.bias_rank = bh.data_ptr(), bh.dim()
+        for r_, e_ in enumerate(bh.shape):
+            a.bias_dims[r_] = e_
+    a.B, a.S, a.H, a.D = B, S, H, D
+    a.L, a.R, a.topk = wh.shape[1], rh.shape[1], sh.shape[2]
+    a.record_bytes, a.n_rope, a.total, a.scale = rh.shape[2], n_rope, int(total), float(scale)
+    y = np.zeros((B, S, H, D), dtype=np.float64)
+    bad = C.c_int(0)
+    rc = lib().orc_csa_ratio4_attention(C.byref(a), y.ctypes.data, C.byref(bad))
+    if rc != 0:
+        raise ValueError("oracle rejected the CSA shape")
+    return y, bad.value

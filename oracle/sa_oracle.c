@@ -1058,3 +1058,155 @@ int orc_index_select(const orc_select_args* a, int32_t* selected, uint8_t* statu
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Compressed sparse attention, ratio 4, in the pages' own form.             */
+/*                                                                          */
+/* [CSA-CPU] ratio4_attention and its call in execute_ratio4; [CSA]         */
+/* csa_ratio4_sink_attention.  A separate dense window store (current_kv,   */
+/* one latent head, K = V) of the most recent tokens and the selected       */
+/* compressed records (hybrid FP8, K = V = the decoded record) are the      */
+/* candidates; an optional additive bias is keyed by the candidate slot; a  */
+/* per-head sink logit joins the softmax denominator.                       */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const void* query;      /* [B, S, H, D] f32 or bf16 (q_dtype) */
+  int q_dtype;
+  const void* window;     /* [B, L, D] f32 or bf16 (w_dtype): current_kv */
+  int w_dtype;
+  const uint8_t* records; /* [B, R, record_bytes] hybrid FP8 records */
+  const int32_t* selected;/* [B, S, topk] record indices, -1 padded */
+  const double* sink;     /* nullable [H] */
+  const float* bias;      /* nullable: rank bias_rank, broadcast against [B, H, S, C] */
+  int64_t bias_rank;
+  int64_t bias_dims[4];
+  int64_t B, S, H, D, L, R, topk, record_bytes, n_rope;
+  int64_t total;          /* tokens so far (the current ones included) */
+  double scale;           /* 0: 1/sqrt(D) */
+} orc_csa_args;
+
+/* Returns 0, -1 on a bad shape; *bad_record = 1 when a selected entry is at
+ * or past the valid records (such a slot is skipped, as the device kernel of
+ * the pages does; their CPU reference refuses the input).  y [B, S, H, D]. */
+int orc_csa_ratio4_attention(const orc_csa_args* a, double* y, int* bad_record) {
+  int64_t query_start = a->total - a->S;
+  int64_t base = a->total - a->L; /* position of current_kv row 0 */
+  int64_t valid_records = a->total / 4;
+  if (valid_records > a->R) {
+    valid_records = a->R;
+  }
+  int64_t dense = 128;
+  if (query_start == 0) {
+    dense = a->L < 128 ? a->L : 128;
+  }
+  int64_t C = dense + a->topk;
+  if (a->bias) {
+    int64_t target[4] = {a->B, a->H, a->S, C};
+    if (a->bias_rank < 0 || a->bias_rank > 4) {
+      return -1;
+    }
+    for (int64_t r = 0; r < a->bias_rank; ++r) {
+      int64_t t = target[4 - a->bias_rank + r];
+      if (a->bias_dims[r] != 1 && a->bias_dims[r] != t) {
+        return -1;
+      }
+    }
+  }
+  double scale = a->scale != 0.0 ? a->scale : 1.0 / sqrt((double)a->D);
+  double* s = (double*)malloc(sizeof(double) * (size_t)C);
+  double* q = (double*)malloc(sizeof(double) * (size_t)a->D);
+  double* rows = (double*)malloc(sizeof(double) * (size_t)(C * a->D));
+  int* valid = (int*)malloc(sizeof(int) * (size_t)C);
+  *bad_record = 0;
+  for (int64_t b = 0; b < a->B; ++b) {
+    for (int64_t si = 0; si < a->S; ++si) {
+      int64_t pos = query_start + si;
+      int64_t wstart = pos + 1 - 128;
+      if (wstart < 0) {
+        wstart = 0;
+      }
+      int64_t dense_start = base > wstart ? base : wstart;
+      /* the candidates' rows, shared by every head */
+      for (int64_t c = 0; c < C; ++c) {
+        valid[c] = 0;
+        double* row = rows + c * a->D;
+        if (c < dense) {
+          int64_t absolute = dense_start + c;
+          int64_t rel = absolute - base;
+          if (absolute > pos || rel < 0 || rel >= a->L) {
+            continue;
+          }
+          for (int64_t d = 0; d < a->D; ++d) {
+            row[d] = load_elem(a->window, (b * a->L + rel) * a->D + d, a->w_dtype);
+          }
+          valid[c] = 1;
+        } else {
+          int32_t rec = a->selected[(b * a->S + si) * a->topk + (c - dense)];
+          if (rec < 0) {
+            continue;
+          }
+          if (rec >= valid_records) {
+            *bad_record = 1;
+            continue;
+          }
+          orc_decode_fp8_record(a->records + (b * a->R + rec) * a->record_bytes,
+                                a->D - a->n_rope, a->n_rope, row);
+          valid[c] = 1;
+        }
+      }
+      for (int64_t h = 0; h < a->H; ++h) {
+        double* out = y + ((b * a->S + si) * a->H + h) * a->D;
+        for (int64_t d = 0; d < a->D; ++d) {
+          q[d] = load_elem(a->query, ((b * a->S + si) * a->H + h) * a->D + d, a->q_dtype);
+          out[d] = 0.0;
+        }
+        double M = -INFINITY;
+        for (int64_t c = 0; c < C; ++c) {
+          s[c] = -INFINITY;
+          if (!valid[c]) {
+            continue;
+          }
+          double dot = 0.0;
+          for (int64_t d = 0; d < a->D; ++d) {
+            dot += q[d] * rows[c * a->D + d];
+          }
+          double sc = dot * scale;
+          if (a->bias) {
+            sc += orc_bias_at(a->bias, a->bias_rank, a->bias_dims, b, h, si, c);
+          }
+          s[c] = sc;
+          if (sc > M) {
+            M = sc;
+          }
+        }
+        if (M == -INFINITY) {
+          continue; /* no candidate: the row stays 0 */
+        }
+        double den = 0.0;
+        for (int64_t c = 0; c < C; ++c) {
+          if (s[c] != -INFINITY) {
+            den += exp(s[c] - M);
+          }
+        }
+        if (a->sink) {
+          den += exp(a->sink[h] - M);
+        }
+        for (int64_t c = 0; c < C; ++c) {
+          if (s[c] == -INFINITY) {
+            continue;
+          }
+          double p = exp(s[c] - M) / den;
+          for (int64_t d = 0; d < a->D; ++d) {
+            out[d] += p * rows[c * a->D + d];
+          }
+        }
+      }
+    }
+  }
+  free(s);
+  free(q);
+  free(rows);
+  free(valid);
+  return 0;
+}

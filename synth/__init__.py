@@ -46,6 +46,9 @@ __all__ = [
     "index_select_fp4",
     "fp4_index_records",
     "make_index_inputs",
+    "CsaCase",
+    "csa_ratio4_ref",
+    "make_csa_inputs",
 ]
 
 _TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -416,3 +419,62 @@ def make_index_inputs(c: IndexCase, seed: int, device="cpu") -> dict:
         "weight": normal((c.B, c.S, c.IH), "f32", seed * 49157 + 2, device),
         "keys": fp4_index_records(c.B, c.R, c.ID, seed * 49157 + 3, c.stride, device),
     }
+
+
+# --------------------------------------------------------------------------
+# Compressed sparse attention (ratio 4) in the pages' own form
+# --------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class CsaCase:
+    name: str
+    B: int
+    S: int                 # query positions per batch (the last S of the context)
+    H: int                 # query heads over one latent head
+    D: int                 # logical dims: (D - n_rope) FP8 + n_rope bf16
+    n_rope: int
+    L: int                 # current_kv rows (the most recent tokens, uncompressed)
+    total: int             # tokens so far
+    topk: int
+    dtype: str = "bf16"    # query and current_kv
+    record_stride: int = 0 # 0: packed (7 x 65 + 128 = 583 bytes at D 512)
+
+    @property
+    def R(self) -> int:
+        return self.total // 4
+
+    @property
+    def stride(self) -> int:
+        return self.record_stride or ((self.D - self.n_rope) // 64 * 65 + 2 * self.n_rope)
+
+
+def csa_ratio4_ref(**kw) -> CsaCase:
+    """B16 decode rows, 128 heads over one 512-dim latent head (448 E4M3 +
+    64 bf16, 583-byte records), a 128-token current_kv window, 65,536 tokens
+    (16,384 ratio-4 records), top-k 2,048."""
+    base = CsaCase("csa_ref_b16_h128_d512_l128_t65536_k2048", B=16, S=1, H=128, D=512,
+                   n_rope=64, L=128, total=65536, topk=2048)
+    return replace(base, **kw)
+
+
+def make_csa_inputs(c: CsaCase, seed: int, device="cpu") -> dict:
+    """query ``[B, S, H, D]`` and current_kv ``[B, L, D]`` ~ N(0, 1) in the
+    case dtype; ``[B, R, stride]`` hybrid FP8 records quantized from N(0, 1)
+    (with ``quantize_fp8_block64_records``); ``selected [B, S, topk]`` int32:
+    distinct records below ``(position + 1) / 4`` sampled uniformly (sorted,
+    as a top-k in record order), -1 where fewer exist."""
+    out = {
+        "query": normal((c.B, c.S, c.H, c.D), c.dtype, seed * 31337 + 1, device),
+        "window": normal((c.B, c.L, c.D), c.dtype, seed * 31337 + 2, device),
+    }
+    nope = normal((c.B, c.R, c.D - c.n_rope), "f32", seed * 31337 + 3, device)
+    rope = normal((c.B, c.R, c.n_rope), "bf16", seed * 31337 + 4, device)
+    out["records"] = quantize_fp8_block64_records(nope, rope, c.stride)
+    sel = torch.full((c.B, c.S, c.topk), -1, dtype=torch.int32)
+    for s in range(c.S):
+        valid = min(c.R, (c.total - c.S + s + 1) // 4)
+        k = min(valid, c.topk)
+        rows = sorted_sample_rows(c.B, 0, valid, k, seed * 31337 + 5 + s)
+        sel[:, s, :k] = rows.to(torch.int32)
+    out["selected"] = sel.to(device)
+    return out
