@@ -1,7 +1,7 @@
 /*
  * sa.h -- C ABI of the GB300 KV-cache attention library (libsa.so).
  *
- * Six operations, all computed on the GPU on the caller's stream:
+ * Seven operations, all computed on the GPU on the caller's stream:
  *
  *   validate_indices     index-row validation with a device error word
  *   build_present_kv     present K/V = past ++ current (concat or in-place append)
@@ -9,6 +9,7 @@
  *   attn_prefill         dense (causal) prefill with softcap, present K/V out
  *   paged_attn_decode    causal decode over a 16-token page table
  *   sparse_index_select  ratio-4 index scoring + top-k (produces selected indices)
+ *   csa_ratio4_attention compressed sparse attention: window store + records + sink
  *
  * Conventions shared by every call
  * --------------------------------
@@ -80,6 +81,8 @@ extern "C" {
 #define SA_ERRBIT_WRITE_POS 64   /* build_present_kv: write_pos[b] out of range */
 #define SA_ERRBIT_PAGE 128       /* paged: ctx_len or block-table entry invalid */
 #define SA_ERRBIT_TIMEOUT 256    /* a kernel's bounded wait for a copy ran out  */
+#define SA_ERRBIT_RECORD 2048    /* csa_ratio4_attention: a selected record at or
+                                    past the valid records (skipped)             */
 
 /* ---- sa_sparse_params.options bits ------------------------------------- */
 #define SA_OPT_ROW_COPIES 1u     /* dense f16/bf16 caches: fetch each K/V row with
@@ -328,6 +331,59 @@ typedef struct {
 
 size_t sparse_index_select_workspace(const sa_index_select_params* p);
 int sparse_index_select(const sa_index_select_params* p, void* stream);
+
+/*
+ * csa_ratio4_attention -- compressed sparse attention, ratio 4, in the pages'
+ * own form: [CSA-CPU] ratio4_attention (with its call in execute_ratio4),
+ * [CSA] csa_ratio4_sink_attention.
+ *
+ * For query s of batch b at position p = total - S + s, with base = total - L
+ * (the position of current_kv row 0):
+ *   dense slots c < dense (dense = 128, or min(L, 128) when total == S): the
+ *     current_kv row at position max(base, p + 1 - 128) + c when that is <= p
+ *     and stored (row < L), else no candidate;
+ *   slot dense + k: selected record selected[b, s, k] when it lies in
+ *     [0, min(R, total / 4)); a negative entry is no candidate, one at or past
+ *     that bound is skipped and sets SA_ERRBIT_RECORD (err_word nullable);
+ *   score = scale * q . row + bias(b, h, s, slot) (bias nullable, float32,
+ *     rank <= 4, broadcast right-aligned against [B, H, S, dense + topk]);
+ *   y = sum softmax(score) row, with exp(sink[h] - max) added to the
+ *     denominator (sink nullable); a query with no candidate gives 0.
+ * K = V = the row: current_kv is one latent head; a record decodes as
+ * (D - n_rope) / 64 blocks of [E8M0 scale, 64 E4M3FN] then n_rope LE bf16
+ * (583 bytes at D 512, n_rope 64; any byte alignment).
+ * Layouts: query / y [B, S, H, D] (q_dtype SA_F32 or SA_BF16, y the same);
+ * current_kv [B, L, D] (kv_dtype SA_F32 or SA_BF16); records [B, R,
+ * record_stride] bytes; selected int32 [B, S, topk].  D 128 or 512, H a
+ * multiple of 32, n_rope even with D - n_rope a positive multiple of 64.
+ * Arithmetic: rows and queries as bf16 (float inputs rounded; FP8 records
+ * exact) on the tensor cores with fp32 accumulation and softmax.
+ * Workspace: csa_ratio4_attention_workspace(p) bytes, 256-byte aligned,
+ * contents on entry irrelevant (the candidate rows, B * S * (dense + topk)
+ * rows of D bf16, and split partials).
+ */
+typedef struct {
+  const void* query;
+  const void* current_kv;
+  const uint8_t* records;
+  const int32_t* selected;
+  const float* sink;
+  const float* bias;
+  int64_t bias_rank;
+  int64_t bias_dims[4];
+  void* y;
+  int32_t q_dtype;
+  int32_t kv_dtype;
+  int64_t B, S, H, D, n_rope, L, R, topk, record_stride, total;
+  float scale;          /* 0: 1/sqrt(D) */
+  int32_t reserved_;    /* must be 0 */
+  uint32_t* err_word;
+  void* workspace;
+  size_t workspace_bytes;
+} sa_csa_params;
+
+size_t csa_ratio4_attention_workspace(const sa_csa_params* p);
+int csa_ratio4_attention(const sa_csa_params* p, void* stream);
 
 /* attention-mask element types of sa_prefill_params.mask_kind */
 #define SA_MASK_NONE 0

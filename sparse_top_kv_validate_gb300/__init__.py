@@ -8,7 +8,7 @@ falling back to anything else.
 
 Entry points (same names as the C ABI):
     validate_indices, build_present_kv, sparse_attn_decode, attn_prefill,
-    paged_attn_decode, sparse_index_select
+    paged_attn_decode, sparse_index_select, csa_ratio4_attention
 """
 from __future__ import annotations
 
@@ -30,6 +30,7 @@ __all__ = [
     "SparseParams", "PrefillParams", "PagedParams", "kernel_events",
     "IndexSelectParams", "sparse_index_select", "sparse_index_select_workspace",
     "SEL_TIE", "SEL_NONFINITE", "ERRBIT_SEL_TIE", "ERRBIT_SEL_NONFINITE",
+    "CsaParams", "csa_ratio4_attention", "csa_ratio4_attention_workspace", "ERRBIT_RECORD",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,6 +45,7 @@ NOALLOC_SCRATCH_BYTES = 16 << 20
 OPT_ROW_COPIES, OPT_FP8_WARP_MMA = 1, 2
 SEL_TIE, SEL_NONFINITE = 1, 2
 ERRBIT_SEL_TIE, ERRBIT_SEL_NONFINITE = 512, 1024
+ERRBIT_RECORD = 2048
 
 _p = C.c_void_p
 _i64 = C.c_int64
@@ -102,6 +104,18 @@ class IndexSelectParams(C.Structure):
     ]
 
 
+class CsaParams(C.Structure):
+    _fields_ = [
+        ("query", _p), ("current_kv", _p), ("records", _p), ("selected", _p), ("sink", _p),
+        ("bias", _p), ("bias_rank", _i64), ("bias_dims", _i64 * 4), ("y", _p),
+        ("q_dtype", _i32), ("kv_dtype", _i32),
+        ("B", _i64), ("S", _i64), ("H", _i64), ("D", _i64), ("n_rope", _i64), ("L", _i64),
+        ("R", _i64), ("topk", _i64), ("record_stride", _i64), ("total", _i64),
+        ("scale", C.c_float), ("reserved_", _i32), ("err_word", _p),
+        ("workspace", _p), ("workspace_bytes", C.c_size_t),
+    ]
+
+
 class SAError(RuntimeError):
     def __init__(self, call: str, status: int):
         super().__init__(f"{call}: status {status} ({status_string(status)})")
@@ -152,6 +166,10 @@ def load():
         L.sparse_index_select_workspace.argtypes = [C.POINTER(IndexSelectParams)]
         L.sparse_index_select.restype = C.c_int
         L.sparse_index_select.argtypes = [C.POINTER(IndexSelectParams), _p]
+        L.csa_ratio4_attention_workspace.restype = C.c_size_t
+        L.csa_ratio4_attention_workspace.argtypes = [C.POINTER(CsaParams)]
+        L.csa_ratio4_attention.restype = C.c_int
+        L.csa_ratio4_attention.argtypes = [C.POINTER(CsaParams), _p]
         L.paged_attn_decode_workspace.restype = C.c_size_t
         L.paged_attn_decode_workspace.argtypes = [C.POINTER(PagedParams)]
         L.paged_attn_decode.restype = C.c_int
@@ -561,3 +579,59 @@ def sparse_index_select(query, weight, keys, *, topk, query_start=0, query_start
     p.workspace, p.workspace_bytes = _ptr(ws), nb
     _check("sparse_index_select", L.sparse_index_select(C.byref(p), _stream(stream)))
     return selected
+
+
+def _csa_params(query, current_kv, records, selected, y, *, total, n_rope, scale, sink, bias,
+                err_word):
+    p = CsaParams()
+    B, S, H, D = query.shape
+    p.query, p.current_kv = query.data_ptr(), _ptr(current_kv)
+    p.records, p.selected, p.y = records.data_ptr(), selected.data_ptr(), _ptr(y)
+    p.sink, p.err_word = _ptr(sink), _ptr(err_word)
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.dim() > 4:
+            raise ValueError("bias must be float32 of rank <= 4")
+        p.bias, p.bias_rank = bias.data_ptr(), bias.dim()
+        for r, e in enumerate(bias.shape):
+            p.bias_dims[r] = e
+    p.q_dtype = _dt(query)
+    p.kv_dtype = _dt(current_kv) if current_kv is not None else _dt(query)
+    p.B, p.S, p.H, p.D = B, S, H, D
+    p.n_rope = int(n_rope)
+    p.L = current_kv.shape[1] if current_kv is not None else 0
+    p.R, p.record_stride = records.shape[1], records.shape[2]
+    p.topk, p.total, p.scale = selected.shape[2], int(total), float(scale)
+    return p
+
+
+def csa_ratio4_attention_workspace(query, current_kv, records, selected, *, total, n_rope,
+                                   scale=0.0, sink=None, bias=None) -> int:
+    p = _csa_params(query, current_kv, records, selected, None, total=total, n_rope=n_rope,
+                    scale=scale, sink=sink, bias=bias, err_word=None)
+    return int(load().csa_ratio4_attention_workspace(C.byref(p)))
+
+
+def csa_ratio4_attention(query, current_kv, records, selected, *, total, n_rope, scale=0.0,
+                         sink=None, bias=None, err_word=None, y=None, workspace=None,
+                         stream=None):
+    """Compressed sparse attention, ratio 4, in the pages' own form.  ``query``
+    ``[B, S, H, D]`` (float32 / bfloat16), ``current_kv`` ``[B, L, D]``,
+    ``records`` uint8 ``[B, R, record_stride]`` hybrid FP8, ``selected`` int32
+    ``[B, S, topk]``; ``total`` tokens so far; optional ``sink`` float32 ``[H]``
+    and ``bias`` float32 (rank <= 4, against ``[B, H, S, candidates]``).
+    Returns ``y`` shaped and typed like ``query``."""
+    L = load()
+    for n, t in (("query", query), ("current_kv", current_kv), ("records", records),
+                 ("selected", selected), ("sink", sink), ("bias", bias), ("err_word", err_word)):
+        _dev(t, n)
+    if selected.dtype != torch.int32 or records.dtype != torch.uint8:
+        raise TypeError("selected must be int32 and records uint8")
+    if y is None:
+        y = torch.empty_like(query)
+    p = _csa_params(query, current_kv, records, selected, y, total=total, n_rope=n_rope,
+                    scale=scale, sink=sink, bias=bias, err_word=err_word)
+    need = int(L.csa_ratio4_attention_workspace(C.byref(p)))
+    ws, nb = _workspace(need, query.device, workspace)
+    p.workspace, p.workspace_bytes = _ptr(ws), nb
+    _check("csa_ratio4_attention", L.csa_ratio4_attention(C.byref(p), _stream(stream)))
+    return y

@@ -2,6 +2,7 @@
 // points (sa_api.cu) and the kernel translation units.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -225,6 +226,35 @@ size_t index_topk_smem_bytes(int64_t sel_slots);
 size_t index_tie_smem_bytes(int hash_slots);
 size_t index_score_smem_bytes(int64_t IH, int64_t ID, int64_t key_stride);
 int launch_index_select(const IndexArgs& a, cudaStream_t st);
+
+// ---- compressed sparse attention (ratio 4), the pages' own form ------------------------
+struct CsaArgs {
+  const void* query;          // [B, S, H, D] (q_dtype)
+  const void* window;         // current_kv [B, L, D] (kv_dtype)
+  const uint8_t* records;     // [B, R, record_stride] hybrid FP8
+  const int32_t* selected;    // [B, S, topk]
+  const float* sink;          // nullable [H]
+  const float* bias;          // nullable: element (b,h,s,slot) at b*sb + h*sh + s*si + slot*sk
+  int64_t bias_sb, bias_sh, bias_si, bias_sk;
+  void* y;                    // [B, S, H, D] (q_dtype)
+  int q_dtype, kv_dtype;
+  int64_t B, S, H, D, n_rope, L, R, topk, record_stride, total;
+  int64_t dense;              // dense slots: 128, or min(L, 128) when the block starts at 0
+  int64_t valid_records;      // min(R, total / 4)
+  int64_t c_pad;              // candidate slots, rounded up to 16
+  int64_t splits, chunk_tiles;
+  float scale_log2;
+  uint32_t* err_word;
+  // workspace
+  __nv_bfloat16* rows;        // [B * S, c_pad, D] candidate rows
+  uint8_t* valid;             // [B * S, c_pad]
+  float* part_o;              // [B * S, splits, H, D] when splits > 1
+  float* part_ml;             // [B * S, splits, H, 2]
+  void* ev_before;            // nullable measurement events around the attention kernel
+  void* ev_after;
+};
+size_t csa_attn_smem_bytes(int64_t D);
+int launch_csa(const CsaArgs& a, cudaStream_t st);
 
 // ---- paged: write the new token into the pool -----------------------------------
 struct PagedAppendArgs {

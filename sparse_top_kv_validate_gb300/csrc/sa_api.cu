@@ -993,6 +993,142 @@ int sparse_index_select(const sa_index_select_params* p, void* stream) {
   return sa::launch_index_select(a, as_stream(stream)) == 0 ? SA_OK : SA_ERR_LAUNCH;
 }
 
+// ---- compressed sparse attention, ratio 4 (the pages' own form) ------------------------
+
+static int check_csa(const sa_csa_params* p, int query = 0) {
+  if (!p || !p->query || !p->records || !p->selected || (!p->y && !query)) return SA_ERR_NULL;
+  if (p->reserved_ != 0) return SA_ERR_UNSUPPORTED;
+  if (p->B <= 0 || p->S <= 0 || p->H <= 0 || p->D <= 0 || p->topk <= 0 || p->R <= 0 ||
+      p->L < 0 || p->total < p->S || p->n_rope < 0)
+    return SA_ERR_SHAPE;
+  if (p->L > 0 && !p->current_kv) return SA_ERR_NULL;
+  if ((p->q_dtype != SA_F32 && p->q_dtype != SA_BF16) ||
+      (p->kv_dtype != SA_F32 && p->kv_dtype != SA_BF16))
+    return SA_ERR_DTYPE;
+  if (!(p->D == 128 || p->D == 512) || p->H % 32 != 0) return SA_ERR_UNSUPPORTED;
+  if (p->n_rope % 2 || p->n_rope >= p->D || (p->D - p->n_rope) % 64) return SA_ERR_SHAPE;
+  if (p->record_stride < (p->D - p->n_rope) / 64 * 65 + 2 * p->n_rope) return SA_ERR_SHAPE;
+  if (!std::isfinite(p->scale)) return SA_ERR_SHAPE;
+  if (p->B * p->S * (128 + p->topk) >= (int64_t(1) << 31)) return SA_ERR_UNSUPPORTED;
+  const size_t qs = p->q_dtype == SA_F32 ? 4 : 2, ks = p->kv_dtype == SA_F32 ? 4 : 2;
+  if (!aligned16(p->query) || (p->current_kv && !aligned16(p->current_kv)) ||
+      (p->y && !aligned16(p->y)) || reinterpret_cast<uintptr_t>(p->selected) % 4 ||
+      (p->bias && reinterpret_cast<uintptr_t>(p->bias) % 4))
+    return SA_ERR_ALIGN;
+  if (p->bias) {
+    const int64_t dense = (p->total == p->S) ? (p->L < 128 ? p->L : 128) : 128;
+    const int64_t target[4] = {p->B, p->H, p->S, dense + p->topk};
+    if (p->bias_rank < 0 || p->bias_rank > 4) return SA_ERR_SHAPE;
+    for (int64_t r = 0; r < p->bias_rank; ++r) {
+      const int64_t e = p->bias_dims[r];
+      if (e != 1 && e != target[4 - p->bias_rank + r]) return SA_ERR_SHAPE;
+    }
+  }
+  const size_t yb = static_cast<size_t>(p->B * p->S * p->H * p->D) * qs;
+  if (overlaps(p->y, yb, p->query, yb) ||
+      overlaps(p->y, yb, p->current_kv, static_cast<size_t>(p->B * p->L * p->D) * ks) ||
+      overlaps(p->y, yb, p->records, static_cast<size_t>(p->B * p->R * p->record_stride)) ||
+      overlaps(p->y, yb, p->selected, static_cast<size_t>(p->B * p->S * p->topk) * 4))
+    return SA_ERR_OVERLAP;
+  return SA_OK;
+}
+
+static size_t csa_plan(const sa_csa_params* p, sa::CsaArgs& a, char* ws) {
+  memset(&a, 0, sizeof(a));
+  a.B = p->B;
+  a.S = p->S;
+  a.H = p->H;
+  a.D = p->D;
+  a.n_rope = p->n_rope;
+  a.L = p->L;
+  a.R = p->R;
+  a.topk = p->topk;
+  a.record_stride = p->record_stride;
+  a.total = p->total;
+  a.dense = (p->total == p->S) ? (p->L < 128 ? p->L : 128) : 128;
+  a.valid_records = p->total / 4 < p->R ? p->total / 4 : p->R;
+  const int64_t C = a.dense + p->topk;
+  a.c_pad = (C + 15) / 16 * 16;
+  const int64_t tiles = a.c_pad / 16;
+  const int64_t blocks = p->B * p->S * (p->H / 32);
+  const int64_t sms = device_shape().sms > 0 ? device_shape().sms : 152;
+  int64_t splits = (2 * sms + blocks - 1) / blocks;  // two CTAs per SM
+  if (splits > tiles) splits = tiles;
+  if (splits > 16) splits = 16;
+  if (splits < 1) splits = 1;
+  a.chunk_tiles = (tiles + splits - 1) / splits;
+  a.splits = (tiles + a.chunk_tiles - 1) / a.chunk_tiles;
+  const int64_t units = p->B * p->S;
+  size_t off = 0;
+  const size_t o_rows = off;
+  off += align_up(static_cast<size_t>(units * a.c_pad * p->D) * 2);
+  const size_t o_valid = off;
+  off += align_up(static_cast<size_t>(units * a.c_pad));
+  size_t o_po = 0, o_pml = 0;
+  if (a.splits > 1) {
+    o_po = off;
+    off += align_up(static_cast<size_t>(units * a.splits * p->H * p->D) * 4);
+    o_pml = off;
+    off += align_up(static_cast<size_t>(units * a.splits * p->H) * 8);
+  }
+  if (ws) {
+    a.rows = reinterpret_cast<__nv_bfloat16*>(ws + o_rows);
+    a.valid = reinterpret_cast<uint8_t*>(ws + o_valid);
+    if (a.splits > 1) {
+      a.part_o = reinterpret_cast<float*>(ws + o_po);
+      a.part_ml = reinterpret_cast<float*>(ws + o_pml);
+    }
+  }
+  return off;
+}
+
+size_t csa_ratio4_attention_workspace(const sa_csa_params* p) {
+  if (check_csa(p, 1) != SA_OK) return 0;
+  sa::CsaArgs a;
+  return csa_plan(p, a, nullptr);
+}
+
+int csa_ratio4_attention(const sa_csa_params* p, void* stream) {
+  int rc = check_csa(p);
+  if (rc != SA_OK) return rc;
+  sa::CsaArgs a;
+  const size_t need = csa_plan(p, a, nullptr);
+  if (!p->workspace || p->workspace_bytes < need) return SA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(p->workspace) % kAlign) return SA_ERR_ALIGN;
+  csa_plan(p, a, static_cast<char*>(p->workspace));
+  a.query = p->query;
+  a.window = p->current_kv;
+  a.records = p->records;
+  a.selected = p->selected;
+  a.sink = p->sink;
+  a.y = p->y;
+  a.q_dtype = p->q_dtype;
+  a.kv_dtype = p->kv_dtype;
+  a.err_word = p->err_word;
+  const float scale = p->scale != 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->D));
+  a.scale_log2 = scale * 1.4426950408889634f;
+  if (p->bias) {
+    // right-aligned strides against [B, H, S, C] (0 on broadcast or missing axes)
+    int64_t st[4] = {0, 0, 0, 0};
+    int64_t run = 1;
+    for (int ax = 3; ax >= 0; --ax) {
+      const int k = ax - (4 - static_cast<int>(p->bias_rank));
+      if (k < 0) continue;
+      const int64_t e = p->bias_dims[k];
+      st[ax] = (e == 1) ? 0 : run;
+      run *= e;
+    }
+    a.bias = p->bias;
+    a.bias_sb = st[0];
+    a.bias_sh = st[1];
+    a.bias_si = st[2];
+    a.bias_sk = st[3];
+  }
+  a.ev_before = t_ev_before;
+  a.ev_after = t_ev_after;
+  return sa::launch_csa(a, as_stream(stream)) == 0 ? SA_OK : SA_ERR_LAUNCH;
+}
+
 }  // extern "C"
 
 // ---- sparse decode without caller-provided scratch ------------------------------------

@@ -42,7 +42,7 @@ def declared_functions():
     return sorted(set(names))
 
 
-def test_header_declares_the_six_operations():
+def test_header_declares_the_seven_operations():
     names = declared_functions()
     for n in ("validate_indices", "build_present_kv", "sparse_attn_decode", "attn_prefill",
               "paged_attn_decode"):
@@ -77,7 +77,8 @@ def _c_layout(struct_name, fields):
 @pytest.mark.parametrize("cname,py", [("sa_sparse_params", sa.SparseParams),
                                       ("sa_prefill_params", sa.PrefillParams),
                                       ("sa_paged_params", sa.PagedParams),
-                                      ("sa_index_select_params", sa.IndexSelectParams)])
+                                      ("sa_index_select_params", sa.IndexSelectParams),
+                                      ("sa_csa_params", sa.CsaParams)])
 def test_struct_layout_matches_header(cname, py):
     fields = [f for f, _ in py._fields_]
     size, offs = _c_layout(cname, fields)
