@@ -589,6 +589,86 @@ class IndexSelect:
                 "call_hbm_gbs": round(self.decode_bytes / (ms * 1e-3) / 1e9, 1)}
 
 
+class CsaRef:
+    """Compressed sparse attention (ratio 4) in the pages' own form: B16 decode
+    rows, 128 heads over one 512-dim latent head, a 128-token current_kv window
+    plus 2,048 selected hybrid-FP8 records (583 bytes) of 16,384, sink."""
+
+    metric = METRIC
+    dtype_name = "bf16 (FP8 E4M3 records decoded exactly)"
+
+    def __init__(self, sa, c: synth.CsaCase, dev, seed=1007):
+        self.sa, self.c, self.dev = sa, c, dev
+        inp = synth.make_csa_inputs(c, seed, device=dev)
+        self.window, self.records = inp["window"], inp["records"]   # resident, like the caches
+        self.s_in = Staging([inp["query"], inp["selected"]], dev)
+        self.q, self.sel = self.s_in.views
+        self.sink = torch.linspace(-1.0, 1.0, c.H, dtype=torch.float32, device=dev)
+        self.s_out = Staging([torch.empty_like(self.q), torch.zeros(1, dtype=torch.int32,
+                                                                    device=dev)], dev)
+        self.y, self.err = self.s_out.views
+        nws = sa.csa_ratio4_attention_workspace(self.q, self.window, self.records, self.sel,
+                                                total=c.total, n_rope=c.n_rope, sink=self.sink)
+        self.ws = sa.new_workspace(nws, dev)
+        self.rows = c.B * c.S * c.H
+        valid_sel = int((self.sel >= 0).sum().item())
+        self.keys = valid_sel + c.B * c.S * min(c.L, 128)
+        es = self.q.element_size()
+        self.flops = 4.0 * c.H * c.D * self.keys
+        self.decode_bytes = (valid_sel * c.stride + c.B * c.S * min(c.L, 128) * c.D * es
+                             + 2 * self.q.numel() * es + self.sel.numel() * 4)
+        self.launches_per_step = 3  # assemble, attention, split merge
+
+    def step(self, ev=None):
+        c = self.c
+        if ev is not None:
+            ev[0].record()
+        self.sa.csa_ratio4_attention(self.q, self.window, self.records, self.sel, total=c.total,
+                                     n_rope=c.n_rope, sink=self.sink, y=self.y,
+                                     workspace=self.ws, err_word=self.err)
+        if ev is not None:
+            ev[1].record()
+
+    def h2d(self):
+        return self.s_in.h2d()  # queries and selected records
+
+    def d2h(self):
+        return self.s_out.d2h()  # y and the error word
+
+    def config(self):
+        c = self.c
+        return {"workload": c.name, "batch": c.B, "queries": c.S, "heads": c.H, "dim": c.D,
+                "rope_dims": c.n_rope, "window_rows": c.L, "tokens": c.total,
+                "records": c.R, "top_k": c.topk, "record_bytes": c.stride,
+                "step": "one csa_ratio4_attention call: candidate assembly (window rows, "
+                        "FP8 record decode), tensor-core attention with sink, split merge "
+                        "-- 3 kernels"}
+
+    def oracle_rows(self, rows):
+        import oracle
+        c = self.c
+        if not hasattr(self, "_host"):
+            self._host = (self.q.cpu(), self.window.cpu(), self.records.cpu(), self.sel.cpu(),
+                          self.sink.cpu().double())
+        q, w, rec, sel, sink = self._host
+        out = []
+        for r in rows:
+            bs, h = divmod(r, c.H)
+            b = bs // c.S
+            y, _ = oracle.csa_ratio4_attention(q[b:b + 1], w[b:b + 1], rec[b:b + 1],
+                                               sel[b:b + 1], total=c.total, n_rope=c.n_rope,
+                                               sink=sink)
+            out.append(y.reshape(-1, c.D)[(bs % c.S) * c.H + h])
+        return np.stack(out)
+
+    def roofline(self, ms, kernel_ms, peaks):
+        line = tensor_roofline("csa_attn_kernel", self.flops, kernel_ms, ms, peaks,
+                               traffic_for(self.c.name, "csa_attn_kernel"))
+        line.update(call_algorithmic_bytes=int(self.decode_bytes),
+                    call_hbm_gbs=round(self.decode_bytes / (ms * 1e-3) / 1e9, 1))
+        return line
+
+
 SMS = 152
 SM_MAX_GHZ = 2.07
 DP4A_PER_SM_PER_CLOCK = 64  # placeholder until measured
@@ -606,6 +686,7 @@ KERNEL_SOURCES = {
     "fp8_decode_kernel": ["k_fp8.cu", "gather_common.cuh", "common.cuh", "kernels.h"],
     "prefill_tc05_kernel": ["k_prefill.cu", "common.cuh", "tc05.cuh", "kernels.h"],
     "index_score_kernel": ["k_index.cu", "common.cuh", "kernels.h"],
+    "csa_attn_kernel": ["k_csa.cu", "gather_common.cuh", "common.cuh", "kernels.h"],
 }
 
 TRAFFIC: dict = {
@@ -675,6 +756,8 @@ def make_workload(sa, name, dev):
         return Prefill(sa, synth.prefill_bf16(), dev)
     if name == "index_select":
         return IndexSelect(sa, synth.index_select_fp4(), dev)
+    if name == "csa_ref":
+        return CsaRef(sa, synth.csa_ratio4_ref(), dev)
     raise SystemExit(f"unknown workload {name}")
 
 
