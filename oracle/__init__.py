@@ -97,6 +97,18 @@ class _CsaArgs(C.Structure):
     ]
 
 
+class _CompressArgs(C.Structure):
+    _fields_ = [
+        ("kv", _p), ("gate", _p), ("ape", _p), ("norm", _p), ("carry", _p),
+        ("records", _p), ("logical", _p),
+        ("B", _i64), ("S", _i64), ("D", _i64), ("n_rope", _i64), ("ratio", _i64),
+        ("kind", _i64), ("rows", _i64), ("record_stride", _i64), ("total", _i64),
+    ]
+
+
+COMPRESS_ATTN, COMPRESS_INDEX = 0, 1
+
+
 def lib():
     global _lib
     with _lock:
@@ -147,6 +159,18 @@ def lib():
                                              C.POINTER(_PrefillMask), _p, _i64, _p]
             L.orc_csa_ratio4_attention.restype = C.c_int
             L.orc_csa_ratio4_attention.argtypes = [C.POINTER(_CsaArgs), _p, C.POINTER(C.c_int)]
+            L.orc_pool_weight.restype = C.c_float
+            L.orc_pool_weight.argtypes = [C.c_float]
+            L.orc_rope_rotation.restype = None
+            L.orc_rope_rotation.argtypes = [_i64, _i64, _p, _p]
+            L.orc_fp8_quantize_block.restype = None
+            L.orc_fp8_quantize_block.argtypes = [_p, _p]
+            L.orc_pool_candidates.restype = C.c_int
+            L.orc_pool_candidates.argtypes = [_p, _p, _i64, _i64, _p]
+            L.orc_finalize_record.restype = C.c_int
+            L.orc_finalize_record.argtypes = [_p, _p, _i64, _i64, C.c_int, _i64, _p]
+            L.orc_csa_compress.restype = C.c_int
+            L.orc_csa_compress.argtypes = [C.POINTER(_CompressArgs), C.POINTER(_i64)]
             L.orc_paged_decode.restype = C.c_int
             L.orc_paged_decode.argtypes = [_p, _p, _p, C.c_int, _p, _p, _i64, _i64, _i64,
                                            _i64, _i64, _i64, C.c_double, _p, _i64, _p]
@@ -489,3 +513,89 @@ def csa_ratio4_attention(query, window, records, selected, *, total: int, n_rope
     if rc != 0:
         raise ValueError("oracle rejected the CSA shape")
     return y, bad.value
+
+
+# ---------------------------------------------------------------------------
+# CSA compression (ratio 128, ratio 4 attention records and index keys)
+# ---------------------------------------------------------------------------
+
+def _np(x):
+    return x.detach().cpu().numpy() if isinstance(x, torch.Tensor) else np.asarray(x)
+
+
+def pool_weight(t: float) -> float:
+    return lib().orc_pool_weight(float(t))
+
+
+def rope_rotation(position: int, n_rope: int):
+    """(cos, sin) float32 ``[n_rope / 2]`` of the compressed RoPE."""
+    cs = np.zeros(max(n_rope // 2, 1), dtype=np.float32)
+    sn = np.zeros_like(cs)
+    lib().orc_rope_rotation(int(position), int(n_rope), cs.ctypes.data, sn.ctypes.data)
+    return cs[: n_rope // 2], sn[: n_rope // 2]
+
+
+def fp8_quantize_block(x) -> bytes:
+    """64 float32 values -> 65 bytes: E8M0 scale byte, then 64 E4M3FN codes."""
+    v = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    assert v.size == 64
+    out = (C.c_uint8 * 65)()
+    lib().orc_fp8_quantize_block(v.ctypes.data, C.addressof(out))
+    return bytes(out)
+
+
+def pool_candidates(value, score):
+    """value, score float32 ``[n, D]`` -> (pooled float32 ``[D]``, ok)."""
+    v = np.ascontiguousarray(np.asarray(value, dtype=np.float32))
+    s = np.ascontiguousarray(np.asarray(score, dtype=np.float32))
+    n, D = v.shape
+    out = np.zeros(D, dtype=np.float32)
+    ok = lib().orc_pool_candidates(v.ctypes.data, s.ctypes.data, n, D, out.ctypes.data)
+    return out, bool(ok)
+
+
+def record_width(D: int, n_rope: int, kind: int) -> int:
+    return ((D - n_rope) // 64) * 65 + 2 * n_rope if kind == COMPRESS_ATTN else (D // 32) * 17
+
+
+def finalize_record(pooled, norm, *, n_rope: int, kind: int, block_start: int):
+    """-> (logical float32 ``[D]``, stored bytes, ok)."""
+    rec = np.array(pooled, dtype=np.float32).copy()
+    nm = np.ascontiguousarray(np.asarray(norm, dtype=np.float32))
+    D = rec.size
+    out = (C.c_uint8 * record_width(D, n_rope, kind))()
+    ok = lib().orc_finalize_record(rec.ctypes.data, nm.ctypes.data, D, n_rope, int(kind),
+                                   int(block_start), C.addressof(out))
+    return rec, bytes(out), bool(ok)
+
+
+def csa_compress(kv, gate, ape, norm, carry, *, ratio: int, kind: int, n_rope: int,
+                 total: int, rows: int, records=None, logical=None, record_stride=None):
+    """One call of the compression stream; see ``orc_csa_compress``.
+
+    kv, gate float32 ``[B, S, W]``; ape ``[ratio, W]``; norm ``[D]``; carry
+    ``[B, slots, 2, W]`` (a copy is updated and returned).  ``records`` uint8
+    ``[B, rows, stride]`` and ``logical`` float32 ``[B, rows, D]`` hold the
+    past records on entry (zeros when None).  Returns ``(records, logical,
+    carry, invalid)``."""
+    kvh, gh, ah, nh = (np.ascontiguousarray(_np(x), dtype=np.float32)
+                       for x in (kv, gate, ape, norm))
+    cy = np.array(_np(carry), dtype=np.float32, copy=True, order="C")
+    B, S, W = kvh.shape
+    D = W // 2 if ratio == 4 else W
+    width = record_width(D, n_rope, kind)
+    stride = width if record_stride is None else int(record_stride)
+    recs = (np.zeros((B, rows, stride), dtype=np.uint8) if records is None
+            else np.array(_np(records), dtype=np.uint8, copy=True, order="C"))
+    logi = (np.zeros((B, rows, D), dtype=np.float32) if logical is None
+            else np.array(_np(logical), dtype=np.float32, copy=True, order="C"))
+    a = _CompressArgs()
+    a.kv, a.gate, a.ape, a.norm = kvh.ctypes.data, gh.ctypes.data, ah.ctypes.data, nh.ctypes.data
+    a.carry, a.records, a.logical = cy.ctypes.data, recs.ctypes.data, logi.ctypes.data
+    a.B, a.S, a.D, a.n_rope, a.ratio, a.kind = B, S, D, n_rope, ratio, kind
+    a.rows, a.record_stride, a.total = rows, stride, int(total)
+    bad = _i64(0)
+    rc = lib().orc_csa_compress(C.byref(a), C.byref(bad))
+    if rc != 0:
+        raise ValueError("oracle rejected the compression shape")
+    return recs, logi, cy, bad.value

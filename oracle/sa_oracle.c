@@ -26,11 +26,17 @@
  *         against [batch, q_head, query, cache position].
  *   [SA] `mask_bias` and the padding frontier (`nonpad_kv_seqlen`) of
  *         `attention_row`: the attention mask and the causal offset.
+ *   [CSA-CPU] compress_ratio4_stream, pool_ratio4_record,
+ *         pool_ratio128_record, finalize_attention_record,
+ *         finalize_index_record, apply_compressed_rope: the compression
+ *         stages that produce the records.
  *   OCP 8-bit floating point specification (E4M3FN) and the OCP MX
  *   specification (E8M0 scale) for the FP8 record decode.
  *
- * Every floating-point step runs in double.  Inputs are widened exactly from
- * their storage type (f32, f16, bf16, FP8 record).
+ * Every floating-point step of the attention runs in double.  Inputs are
+ * widened exactly from their storage type (f32, f16, bf16, FP8 record).  The
+ * index selection and the compression stages produce bytes that the pages
+ * fix in binary32, so those sections follow the pages' binary32 steps.
  */
 #include <math.h>
 #include <stdint.h>
@@ -1208,5 +1214,369 @@ int orc_csa_ratio4_attention(const orc_csa_args* a, double* y, int* bad_record) 
   free(q);
   free(rows);
   free(valid);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* CSA compression: ratio 128 and ratio 4 (attention records, index keys).  */
+/*                                                                          */
+/* [CSA-CPU] compress_ratio4_stream, pool_ratio4_record,                    */
+/* pool_ratio128_record, finalize_attention_record, finalize_index_record,  */
+/* apply_compressed_rope; [CSA] csa_ratio128_compress,                      */
+/* csa_ratio4_main_compress, csa_ratio4_index_compress.  Binary32           */
+/* arithmetic, one rounding per operation, in the pages' order (the pages   */
+/* fix the record bytes, so the oracle reproduces their precision rather    */
+/* than widening to double).  Each transcendental value (the pool weight,   */
+/* the RoPE base frequency, sine and cosine) is the binary32 rounding of a  */
+/* double evaluation, the device page's own form for the pool weight.       */
+/* ------------------------------------------------------------------------ */
+
+#define ORC_COMPRESS_ATTN 0  /* hybrid FP8 attention record */
+#define ORC_COMPRESS_INDEX 1 /* FP4 index key (Hadamard first) */
+
+/* e^t rounded to binary32, t = score - max (<= 0): [CSA] ratio-4 pooling. */
+float orc_pool_weight(float t) {
+  return (float)exp((double)t);
+}
+
+/* Compressed RoPE rotation at `position` for n_rope/2 pairs ([CSA-CPU]
+ * apply_compressed_rope): base 160000, factor 16, ramp over pairs 15..25. */
+void orc_rope_rotation(int64_t position, int64_t n_rope, float* cs, float* sn) {
+  float p = (float)position;
+  for (int64_t pair = 0; pair < n_rope / 2; ++pair) {
+    float ramp = ((float)pair - 15.0f) / 10.0f;
+    if (ramp < 0.0f) {
+      ramp = 0.0f;
+    }
+    if (ramp > 1.0f) {
+      ramp = 1.0f;
+    }
+    float ex = -((float)(2 * pair)) / (float)n_rope;
+    float base = (float)pow(160000.0, (double)ex);
+    float t1 = base * (1.0f - ramp);
+    float t2 = (base / 16.0f) * ramp;
+    float freq = t1 + t2;
+    float angle = p * freq;
+    cs[pair] = (float)cos((double)angle);
+    sn[pair] = (float)sin((double)angle);
+  }
+}
+
+/* E4M3FN code nearest to v (|v| <= 448), ties to the even code, the sign of
+ * v kept (so -0 and negative values rounding to zero give 0x80). */
+static uint8_t orc_e4m3fn_nearest(double v) {
+  double mag = fabs(v);
+  int best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c < 0x7f; ++c) {
+    double err = fabs(mag - orc_e4m3fn_to_double((uint8_t)c));
+    if (err < best_err || (err == best_err && (c % 2) == 0)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(signbit(v) ? (0x80 | best) : best);
+}
+
+/* One FP8 block: out[0] = E8M0 byte of the smallest e with amax / 2^e <= 448
+ * (e = 0 for an all-zero block, clamped to [-127, 127]); out[1 + i] = the
+ * nearest E4M3FN code of x_i / 2^e.  The values must be finite. */
+void orc_fp8_quantize_block(const float* x, uint8_t* out) {
+  double amax = 0.0;
+  for (int i = 0; i < 64; ++i) {
+    double m = fabs((double)x[i]);
+    if (m > amax) {
+      amax = m;
+    }
+  }
+  int e = 0;
+  if (amax > 0.0) {
+    int k;
+    double f = frexp(amax, &k); /* amax = f * 2^k, f in [0.5, 1); 448 = 0.875 * 2^9 */
+    e = k - 9 + (f > 0.875 ? 1 : 0);
+    if (e < -127) {
+      e = -127;
+    }
+    if (e > 127) {
+      e = 127;
+    }
+  }
+  out[0] = (uint8_t)(e + 127);
+  for (int i = 0; i < 64; ++i) {
+    out[1 + i] = orc_e4m3fn_nearest(ldexp((double)x[i], -e));
+  }
+}
+
+static int orc_all_finite(const float* v, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) {
+    if (!isfinite(v[i])) {
+      return 0;
+    }
+  }
+  return 1;
+}
+
+/* Softmax pooling of one dimension over n candidates ([CSA-CPU]
+ * pool_ratio4_record / pool_ratio128_record): the maximum score, then in
+ * candidate order every score that is not -inf adds its weight to the
+ * denominator and weight * value to the numerator.  Returns 0 when the
+ * maximum is not finite or the sums are not usable. */
+static int orc_pool_dim(const float* value, const float* score, int64_t n, float* out) {
+  float m = -INFINITY;
+  for (int64_t c = 0; c < n; ++c) {
+    m = fmaxf(m, score[c]);
+  }
+  if (!isfinite(m)) {
+    return 0;
+  }
+  float num = 0.0f, den = 0.0f;
+  for (int64_t c = 0; c < n; ++c) {
+    if (score[c] == -INFINITY) {
+      continue;
+    }
+    float w = orc_pool_weight(score[c] - m);
+    num = num + w * value[c];
+    den = den + w;
+  }
+  if (den == 0.0f || !isfinite(den) || !isfinite(num)) {
+    return 0;
+  }
+  *out = num / den;
+  return 1;
+}
+
+/* The pooled candidates of one record, exported for the tests: value and
+ * score are [n, D]; out [D].  Returns 0 when a dimension fails to pool. */
+int orc_pool_candidates(const float* value, const float* score, int64_t n, int64_t D,
+                        float* out) {
+  float* v = (float*)malloc(sizeof(float) * (size_t)n);
+  float* s = (float*)malloc(sizeof(float) * (size_t)n);
+  int ok = 1;
+  for (int64_t d = 0; d < D; ++d) {
+    for (int64_t c = 0; c < n; ++c) {
+      v[c] = value[c * D + d];
+      s[c] = score[c * D + d];
+    }
+    if (!orc_pool_dim(v, s, n, out + d)) {
+      ok = 0;
+      out[d] = 0.0f;
+    }
+  }
+  free(v);
+  free(s);
+  return ok;
+}
+
+/* Finalize one pooled record ([CSA-CPU] finalize_attention_record /
+ * finalize_index_record): bfloat16 rounding; RMSNorm (binary32 square sum
+ * in dimension order, 1 / sqrt(sum / D + 1e-6)) times the learned scale,
+ * bfloat16; the compressed RoPE of the last n_rope dimensions at
+ * block_start, bfloat16 per component.  Attention records then quantize the
+ * first D - n_rope dimensions per block of 64 to FP8 and store the RoPE
+ * tail as little-endian bfloat16; index keys take the Hadamard transform and
+ * quantize per block of 32 to FP4.  `rec` holds the pooled values on entry
+ * and the logical (dequantized) record on return; `bytes` gets the stored
+ * record.  Returns 0 (and zeroes both) when a value is not finite. */
+int orc_finalize_record(float* rec, const float* norm, int64_t D, int64_t n_rope, int kind,
+                        int64_t block_start, uint8_t* bytes) {
+  int64_t width = kind == ORC_COMPRESS_ATTN ? ((D - n_rope) / 64) * 65 + 2 * n_rope
+                                            : (D / 32) * 17;
+  for (int64_t d = 0; d < D; ++d) {
+    rec[d] = orc_round_bf16(rec[d]);
+  }
+  float sum = 0.0f;
+  for (int64_t d = 0; d < D; ++d) {
+    sum = sum + rec[d] * rec[d];
+  }
+  int ok = isfinite(sum) && orc_all_finite(rec, D);
+  if (ok) {
+    float inv = 1.0f / sqrtf(sum / (float)D + 1.0e-6f);
+    for (int64_t d = 0; d < D; ++d) {
+      rec[d] = orc_round_bf16((rec[d] * inv) * norm[d]);
+    }
+    float* cs = (float*)malloc(sizeof(float) * (size_t)(n_rope / 2 + 1));
+    float* sn = (float*)malloc(sizeof(float) * (size_t)(n_rope / 2 + 1));
+    orc_rope_rotation(block_start, n_rope, cs, sn);
+    for (int64_t pair = 0; pair < n_rope / 2; ++pair) {
+      int64_t d = D - n_rope + 2 * pair;
+      float re = rec[d], im = rec[d + 1];
+      rec[d] = orc_round_bf16(re * cs[pair] - im * sn[pair]);
+      rec[d + 1] = orc_round_bf16(re * sn[pair] + im * cs[pair]);
+    }
+    free(cs);
+    free(sn);
+    if (kind == ORC_COMPRESS_INDEX) {
+      orc_hadamard_bf16(rec, D);
+    }
+    ok = orc_all_finite(rec, D);
+  }
+  if (!ok) {
+    for (int64_t d = 0; d < D; ++d) {
+      rec[d] = 0.0f;
+    }
+    memset(bytes, 0, (size_t)width);
+    return 0;
+  }
+  if (kind == ORC_COMPRESS_ATTN) {
+    int64_t nb = (D - n_rope) / 64;
+    for (int64_t blk = 0; blk < nb; ++blk) {
+      uint8_t* p = bytes + blk * 65;
+      orc_fp8_quantize_block(rec + blk * 64, p);
+      double s = orc_e8m0_to_double(p[0]);
+      for (int64_t i = 0; i < 64; ++i) {
+        rec[blk * 64 + i] = (float)(orc_e4m3fn_to_double(p[1 + i]) * s);
+      }
+    }
+    uint8_t* tail = bytes + nb * 65;
+    for (int64_t r = 0; r < n_rope; ++r) {
+      float v = rec[D - n_rope + r];
+      uint32_t u;
+      memcpy(&u, &v, 4);
+      tail[2 * r] = (uint8_t)((u >> 16) & 0xff);
+      tail[2 * r + 1] = (uint8_t)(u >> 24);
+    }
+  } else {
+    for (int64_t blk = 0; blk < D / 32; ++blk) {
+      uint8_t* p = bytes + blk * 17;
+      orc_fp4_quantize_block(rec + blk * 32, p, p + 1);
+      for (int i = 0; i < 32; ++i) {
+        rec[blk * 32 + i] = orc_fp4_element(p[0], p + 1, i);
+      }
+    }
+  }
+  return 1;
+}
+
+typedef struct {
+  const float* kv;   /* [B, S, W] the compressor's value source, W = D (ratio 128) or 2D */
+  const float* gate; /* [B, S, W] the compressor's score source */
+  const float* ape;  /* [ratio, W] positional score bias, by position within the block */
+  const float* norm; /* [D] RMSNorm scale */
+  float* carry;      /* [B, slots, 2, W], slots = 128 or 8; channel 0 value, 1 score */
+  uint8_t* records;  /* nullable [B, rows, record_stride] stored records */
+  float* logical;    /* nullable [B, rows, D] the dequantized records */
+  int64_t B, S, D, n_rope, ratio, kind, rows, record_stride, total;
+} orc_compress_args;
+
+/* The compression stream ([CSA-CPU] compress_ratio4_stream and the ratio-128
+ * loop; [CSA] csa_ratio*_compress), token by token: the token's value and
+ * gate + ape fill its carry slot (ratio 128: slot pos % 128; ratio 4: the
+ * current-window slot 4 + pos % 4); at the end of every block of `ratio`
+ * tokens the carry is pooled into one record (ratio 4: candidates 0..3 are
+ * the previous block's slots on the first D source dimensions, 4..7 the
+ * current block's on the last D), finalized at block_start = pos + 1 -
+ * ratio and stored as record pos / ratio; then the carry is cleared (ratio
+ * 128) or the current window moves into the previous one and is cleared
+ * (ratio 4).  A stream starting at position 0 starts from a cleared carry.
+ * A record that fails to pool or finalize is stored as zeros and counted in
+ * *invalid.  Returns -1 on a bad shape. */
+int orc_csa_compress(const orc_compress_args* a, int64_t* invalid) {
+  int64_t R = a->ratio, D = a->D;
+  if (R != 4 && R != 128) {
+    return -1;
+  }
+  if (a->kind == ORC_COMPRESS_INDEX && R != 4) {
+    return -1;
+  }
+  if (a->n_rope < 0 || a->n_rope > D || a->n_rope % 2) {
+    return -1;
+  }
+  if (a->kind == ORC_COMPRESS_ATTN && (D - a->n_rope) % 64) {
+    return -1;
+  }
+  if (a->kind == ORC_COMPRESS_INDEX && (D % 32 || (D & (D - 1)))) {
+    return -1;
+  }
+  int64_t start = a->total - a->S;
+  if (start < 0 || a->S < 0 || a->total / R > a->rows) {
+    return -1;
+  }
+  int64_t width = a->kind == ORC_COMPRESS_ATTN ? ((D - a->n_rope) / 64) * 65 + 2 * a->n_rope
+                                               : (D / 32) * 17;
+  if (a->records && a->record_stride < width) {
+    return -1;
+  }
+  int64_t slots = R == 128 ? 128 : 8;
+  int64_t W = R == 4 ? 2 * D : D;
+  int64_t ncand = R == 128 ? 128 : 8;
+  float* rec = (float*)malloc(sizeof(float) * (size_t)D);
+  float* cv = (float*)malloc(sizeof(float) * (size_t)ncand);
+  float* cscore = (float*)malloc(sizeof(float) * (size_t)ncand);
+  uint8_t* bytes = (uint8_t*)malloc((size_t)width);
+  *invalid = 0;
+  for (int64_t b = 0; b < a->B; ++b) {
+    float* cy = a->carry + b * slots * 2 * W;
+    if (start == 0) {
+      for (int64_t sl = 0; sl < slots; ++sl) {
+        for (int64_t d = 0; d < W; ++d) {
+          cy[(sl * 2) * W + d] = 0.0f;
+          cy[(sl * 2 + 1) * W + d] = -INFINITY;
+        }
+      }
+    }
+    for (int64_t s = 0; s < a->S; ++s) {
+      int64_t pos = start + s;
+      int64_t phase = pos % R;
+      int64_t slot = R == 4 ? 4 + phase : phase;
+      const float* kv = a->kv + (b * a->S + s) * W;
+      const float* gate = a->gate + (b * a->S + s) * W;
+      for (int64_t d = 0; d < W; ++d) {
+        cy[(slot * 2) * W + d] = kv[d];
+        cy[(slot * 2 + 1) * W + d] = gate[d] + a->ape[phase * W + d];
+      }
+      if ((pos + 1) % R != 0) {
+        continue;
+      }
+      int ok = 1;
+      for (int64_t d = 0; d < D; ++d) {
+        for (int64_t c = 0; c < ncand; ++c) {
+          int64_t sd = (R == 4 && c >= 4) ? D + d : d;
+          cv[c] = cy[(c * 2) * W + sd];
+          cscore[c] = cy[(c * 2 + 1) * W + sd];
+        }
+        if (!orc_pool_dim(cv, cscore, ncand, rec + d)) {
+          ok = 0;
+          rec[d] = 0.0f;
+        }
+      }
+      if (ok) {
+        ok = orc_finalize_record(rec, a->norm, D, a->n_rope, (int)a->kind, pos + 1 - R, bytes);
+      } else {
+        memset(rec, 0, sizeof(float) * (size_t)D);
+        memset(bytes, 0, (size_t)width);
+      }
+      if (!ok) {
+        *invalid += 1;
+      }
+      int64_t out = pos / R;
+      if (a->records) {
+        memcpy(a->records + (b * a->rows + out) * a->record_stride, bytes, (size_t)width);
+      }
+      if (a->logical) {
+        memcpy(a->logical + (b * a->rows + out) * D, rec, sizeof(float) * (size_t)D);
+      }
+      if (R == 128) {
+        for (int64_t sl = 0; sl < 128; ++sl) {
+          for (int64_t d = 0; d < W; ++d) {
+            cy[(sl * 2) * W + d] = 0.0f;
+            cy[(sl * 2 + 1) * W + d] = -INFINITY;
+          }
+        }
+      } else {
+        for (int64_t prev = 0; prev < 4; ++prev) {
+          for (int64_t ch = 0; ch < 2; ++ch) {
+            for (int64_t d = 0; d < W; ++d) {
+              cy[(prev * 2 + ch) * W + d] = cy[((4 + prev) * 2 + ch) * W + d];
+              cy[((4 + prev) * 2 + ch) * W + d] = ch == 0 ? 0.0f : -INFINITY;
+            }
+          }
+        }
+      }
+    }
+  }
+  free(rec);
+  free(cv);
+  free(cscore);
+  free(bytes);
   return 0;
 }

@@ -49,6 +49,10 @@ __all__ = [
     "CsaCase",
     "csa_ratio4_ref",
     "make_csa_inputs",
+    "CompressCase",
+    "compress_r4",
+    "compress_r128",
+    "make_compress_inputs",
 ]
 
 _TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -477,4 +481,92 @@ def make_csa_inputs(c: CsaCase, seed: int, device="cpu") -> dict:
         rows = sorted_sample_rows(c.B, 0, valid, k, seed * 31337 + 5 + s)
         sel[:, s, :k] = rows.to(torch.int32)
     out["selected"] = sel.to(device)
+    return out
+
+
+# --------------------------------------------------------------------------
+# CSA compression streams (ratio 4 attention records / index keys, ratio 128)
+# --------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class CompressCase:
+    name: str
+    B: int
+    S: int          # new tokens per sequence in this call
+    D: int          # record dims (ratio 4 sources are 2 * D wide)
+    n_rope: int
+    ratio: int      # 4 or 128
+    kind: int       # 0 attention record (FP8 + bf16 tail), 1 index key (FP4)
+    total: int      # tokens so far, these S included
+    rows: int = 0   # record rows per sequence (0: total / ratio)
+
+    @property
+    def W(self) -> int:
+        return 2 * self.D if self.ratio == 4 else self.D
+
+    @property
+    def slots(self) -> int:
+        return 8 if self.ratio == 4 else 128
+
+    @property
+    def start(self) -> int:
+        return self.total - self.S
+
+    @property
+    def R(self) -> int:
+        return self.rows or self.total // self.ratio
+
+    @property
+    def width(self) -> int:
+        if self.kind == 0:
+            return (self.D - self.n_rope) // 64 * 65 + 2 * self.n_rope
+        return self.D // 32 * 17
+
+
+def compress_r4(kind: int = 0, **kw) -> CompressCase:
+    """One ratio-4 layer's chunk: B16, 4,096 new tokens ending at 65,536;
+    attention records D 512 (448 E4M3 + 64 bf16 RoPE, 583 bytes) or index
+    keys D 128 (64 RoPE, FP4, 68 bytes)."""
+    D = 512 if kind == 0 else 128
+    base = CompressCase(f"compress_r4_{'attn' if kind == 0 else 'index'}_b16_s4096_t65536_d{D}",
+                        B=16, S=4096, D=D, n_rope=64, ratio=4, kind=kind, total=65536)
+    return replace(base, **kw)
+
+
+def compress_r128(**kw) -> CompressCase:
+    """A ratio-128 layer's chunk: B16, 4,096 new tokens ending at 65,536,
+    D 512 records (583 bytes)."""
+    base = CompressCase("compress_r128_b16_s4096_t65536_d512", B=16, S=4096, D=512,
+                        n_rope=64, ratio=128, kind=0, total=65536)
+    return replace(base, **kw)
+
+
+def make_compress_inputs(c: CompressCase, seed: int, device="cpu") -> dict:
+    """kv, gate ``[B, S, W]`` ~ N(0, 1); ape ``[ratio, W]`` ~ N(0, 1) / 2;
+    norm ``[D]`` = 1 + N(0, 1) / 10 (all float32), and a carry ``[B, slots,
+    2, W]`` in the state a stream at position ``start`` holds: the slots of
+    the positions already seen in the open block (and, for ratio 4, the
+    previous block's four slots once a block has closed) carry N(0, 1)
+    values and scores, every other slot value 0 and score -inf."""
+    out = {
+        "kv": normal((c.B, c.S, c.W), "f32", seed * 7919 + 1, device),
+        "gate": normal((c.B, c.S, c.W), "f32", seed * 7919 + 2, device),
+        "ape": normal((c.ratio, c.W), "f32", seed * 7919 + 3, device) * 0.5,
+        "norm": 1.0 + normal((c.D,), "f32", seed * 7919 + 4, device) * 0.1,
+    }
+    carry = torch.zeros((c.B, c.slots, 2, c.W), dtype=torch.float32)
+    carry[:, :, 1, :] = float("-inf")
+    vals = normal((c.B, c.slots, 2, c.W), "f32", seed * 7919 + 5)
+    st = c.start
+    open_from = st - st % c.ratio
+    live = []
+    if c.ratio == 4:
+        live += [4 + (p % 4) for p in range(open_from, st)]
+        if open_from >= 4:
+            live += [0, 1, 2, 3]
+    else:
+        live += [p % 128 for p in range(open_from, st)]
+    for sl in live:
+        carry[:, sl] = vals[:, sl]
+    out["carry"] = carry.to(device)
     return out
