@@ -669,9 +669,120 @@ class CsaRef:
         return line
 
 
+class Compress:
+    """One ratio-4 layer's compression stages over a prefill chunk: B16, 4,096
+    new tokens per sequence ending at position 65,536; the attention-record
+    stream (D 512: 448 E4M3 + 64 bf16 RoPE, 583-byte records) and the
+    index-key stream (D 128, 64 RoPE, FP4, 68-byte keys)."""
+
+    metric = "CSA compression tokens/s (ratio-4 attention records + index keys) on 1 GB300"
+    unit = "tokens/s"
+    dtype_name = "f32 (binary32 pooling and RMSNorm; E4M3 / E2M1 records)"
+    data_desc = ("synthetic (seeded N(0,1) compressor values and gates, N(0,1)/2 positional "
+                 "score biases, 1 + N(0,1)/10 norm scales; carry in the state of position "
+                 "61,440)")
+    chunk = 64  # tokens per oracle unit of the CPU baseline
+
+    def __init__(self, sa, dev, seed=1008):
+        self.sa, self.dev = sa, dev
+        self.cm, self.ci = synth.compress_r4(0), synth.compress_r4(1)
+        im = synth.make_compress_inputs(self.cm, seed, device=dev)
+        ii = synth.make_compress_inputs(self.ci, seed + 1, device=dev)
+        self.s_in = Staging([im["kv"], im["gate"], ii["kv"], ii["gate"]], dev)
+        self.kv_m, self.g_m, self.kv_i, self.g_i = self.s_in.views
+        self.ape_m, self.norm_m, self.carry_m = im["ape"], im["norm"], im["carry"]
+        self.ape_i, self.norm_i, self.carry_i = ii["ape"], ii["norm"], ii["carry"]
+        cm, ci = self.cm, self.ci
+        self.rec_m = torch.zeros((cm.B, cm.R, cm.width), dtype=torch.uint8, device=dev)
+        self.rec_i = torch.zeros((ci.B, ci.R, ci.width), dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.k0 = cm.start // 4
+        self.nk = cm.total // 4 - self.k0
+        self.h_rec_m = torch.empty((cm.B, self.nk, cm.width), dtype=torch.uint8).pin_memory()
+        self.h_rec_i = torch.empty((ci.B, self.nk, ci.width), dtype=torch.uint8).pin_memory()
+        self.h_err = torch.empty(1, dtype=torch.int32).pin_memory()
+        self.rows = cm.B * cm.S  # tokens per step
+        self.oracle_row_count = cm.B * cm.S // self.chunk
+        self.oracle_row_units = self.chunk
+        # algorithmic bytes: every new token's value and gate rows once, the
+        # previous block's four carry slots, the records written, the carry
+        # rewritten (8 slots x 2 channels x W per sequence); ape and norm
+        # (a few KB, cache resident) left out
+        def stream_bytes(c):
+            src = c.B * c.S * 2 * c.W * 4
+            rec = c.B * self.nk * c.width
+            return src, rec, c.B * 4 * 2 * c.W * 4, c.B * 8 * 2 * c.W * 4
+        sm, rm, pm, cym = stream_bytes(cm)
+        si, ri, pi, cyi = stream_bytes(ci)
+        self.kernel_bytes = sm + rm + pm // 2  # the records kernel reads half of each slot
+        self.call_bytes = sm + rm + pm // 2 + cym + si + ri + pi // 2 + cyi
+        self.launches_per_step = 4  # two streams: records kernel + carry kernel each
+
+    def step(self, ev=None):
+        sa, cm, ci = self.sa, self.cm, self.ci
+        if ev is not None:
+            ev[0].record()
+        # the index stream first, so that the library's measurement events
+        # (recorded around each call's record kernel) end on the main stream's
+        sa.csa_ratio4_index_compress(self.kv_i, self.g_i, self.ape_i, self.norm_i, self.carry_i,
+                                     n_rope=ci.n_rope, total=ci.total, records=self.rec_i,
+                                     err_word=self.err)
+        sa.csa_ratio4_main_compress(self.kv_m, self.g_m, self.ape_m, self.norm_m, self.carry_m,
+                                    n_rope=cm.n_rope, total=cm.total, records=self.rec_m,
+                                    err_word=self.err)
+        if ev is not None:
+            ev[1].record()
+
+    def h2d(self):
+        return self.s_in.h2d()  # the chunk's value and gate rows of both streams
+
+    def d2h(self):
+        # the records this step wrote (rows k0.. of every sequence) and the error word
+        for b in range(self.cm.B):
+            self.h_rec_m[b].copy_(self.rec_m[b, self.k0:], non_blocking=True)
+            self.h_rec_i[b].copy_(self.rec_i[b, self.k0:], non_blocking=True)
+        self.h_err.copy_(self.err, non_blocking=True)
+        return self.h_rec_m.numel() + self.h_rec_i.numel() + 4
+
+    def config(self):
+        cm, ci = self.cm, self.ci
+        return {"workload": cm.name.replace("_attn", "") + "_main_and_index",
+                "batch": cm.B, "new_tokens": cm.S, "position_end": cm.total, "ratio": 4,
+                "record_dim": cm.D, "record_rope_dims": cm.n_rope, "record_bytes": cm.width,
+                "index_dim": ci.D, "index_rope_dims": ci.n_rope, "index_key_bytes": ci.width,
+                "records_per_sequence": self.nk,
+                "step": "csa_ratio4_index_compress + csa_ratio4_main_compress: per stream a "
+                        "record kernel (softmax pool of 8 candidates, RMSNorm, RoPE, "
+                        "FP8 / Hadamard + FP4) and a carry kernel -- 4 kernels"}
+
+    def oracle_rows(self, rows):
+        import oracle
+        if not hasattr(self, "_host"):
+            self._host = [(c, tuple(t.cpu() for t in ts)) for c, ts in (
+                (self.cm, (self.kv_m, self.g_m, self.ape_m, self.norm_m, self.carry_m)),
+                (self.ci, (self.kv_i, self.g_i, self.ape_i, self.norm_i, self.carry_i)))]
+        n = self.chunk
+        per_b = self.cm.S // n
+        for r in rows:
+            b, ch = divmod(r, per_b)
+            lo, hi = ch * n, ch * n + n
+            # one 64-token chunk of both streams from the carry (positions from
+            # the chunk's start: the same work as at the step's own positions)
+            for c, (kv, g, ape, norm, cy) in self._host:
+                oracle.csa_compress(kv[b:b + 1, lo:hi], g[b:b + 1, lo:hi], ape, norm,
+                                    cy[b:b + 1], ratio=4, kind=c.kind, n_rope=c.n_rope,
+                                    total=hi, rows=hi // 4)
+
+    def roofline(self, ms, kernel_ms, peaks):
+        return hbm_roofline("compress_r4_kernel", self.kernel_bytes, kernel_ms, self.call_bytes,
+                            ms, peaks, traffic_for("compress_r4", "compress_r4_kernel"))
+
+
 SMS = 152
 SM_MAX_GHZ = 2.07
-DP4A_PER_SM_PER_CLOCK = 64  # placeholder until measured
+# dp4a issue rate: 16 per SM sub-partition per clock (a probe kernel measured
+# about 60 per SM per clock on this part)
+DP4A_PER_SM_PER_CLOCK = 64
 
 
 # DRAM bytes (read + write) per launch of the dominant kernel from an ncu
@@ -685,7 +796,8 @@ KERNEL_SOURCES = {
                         "kernels.h"],
     "fp8_decode_kernel": ["k_fp8.cu", "gather_common.cuh", "common.cuh", "kernels.h"],
     "prefill_tc05_kernel": ["k_prefill.cu", "common.cuh", "tc05.cuh", "kernels.h"],
-    "index_score_kernel": ["k_index.cu", "common.cuh", "kernels.h"],
+    "index_score_kernel": ["k_index.cu", "codes.cuh", "common.cuh", "kernels.h"],
+    "compress_r4_kernel": ["k_compress.cu", "codes.cuh", "common.cuh", "kernels.h"],
     "csa_attn_kernel": ["k_csa.cu", "gather_common.cuh", "common.cuh", "kernels.h"],
 }
 
@@ -740,6 +852,11 @@ def tensor_roofline(kernel, flops, kernel_ms, call_ms, peaks, traffic):
             "call_frac": round(call / peaks["bf16_tflops"], 4)}
 
 
+def unit_of(wl) -> str:
+    return getattr(wl, "unit", None) or ("tokens/s" if isinstance(wl, Prefill)
+                                         else "query-rows/s")
+
+
 def make_workload(sa, name, dev):
     if name in ("sparse_bf16", "default"):
         return SparseDecode(sa, synth.sparse_bf16(), dev)
@@ -758,6 +875,8 @@ def make_workload(sa, name, dev):
         return IndexSelect(sa, synth.index_select_fp4(), dev)
     if name == "csa_ref":
         return CsaRef(sa, synth.csa_ratio4_ref(), dev)
+    if name == "compress_r4":
+        return Compress(sa, dev)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -905,7 +1024,7 @@ def run_gpu(args):
         line = {
             "metric": wl.metric,
             "value": round(value, 1),
-            "unit": "tokens/s" if isinstance(wl, Prefill) else "query-rows/s",
+            "unit": unit_of(wl),
             "n_gpus": ws,
             "steps": steps,
             "warmup": max(args.warmup, 3),
@@ -925,7 +1044,7 @@ def run_gpu(args):
                            if graph is not None else "direct library call per step"),
             "roofline": wl.roofline(statistics.median(dec_ms), kernel_ms, peaks),
             "e2e": {"value": round(job_rate(wl.rows, ws, 1, e2e_ms), 1),
-                    "unit": "tokens/s" if isinstance(wl, Prefill) else "query-rows/s",
+                    "unit": unit_of(wl),
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "ms_per_step": round(e2e_ms, 5),
                     "launch": "CUDA graph replay of the H2D copy, the library call and "
@@ -970,7 +1089,8 @@ def cpu_baseline(wl, args, budget_s: float = 10.0):
     cores = os.cpu_count() or 1
     pool = OraclePool(wl, cores)
     wl.oracle_rows([0])  # stage host copies outside the timing
-    rows_all = list(range(wl.rows))
+    per_row = getattr(wl, "oracle_row_units", 1)  # workload units one oracle row covers
+    rows_all = list(range(getattr(wl, "oracle_row_count", wl.rows)))
     n = min(len(rows_all), cores * 4)
     t0 = time.perf_counter()
     pool.run(rows_all[:n])
@@ -981,9 +1101,9 @@ def cpu_baseline(wl, args, budget_s: float = 10.0):
         pool.run(rows_all[:n2])
         dt = time.perf_counter() - t0
         n = n2
-    unit = "tokens/s" if isinstance(wl, Prefill) else "query-rows/s"
+    unit = unit_of(wl)
     what = unit.split('/')[0]
-    sample = f"{n} of {wl.rows} {what} of one step"
+    sample = f"{n * per_row} of {len(rows_all) * per_row} {what} of one step"
     if dt < budget_s and n == len(rows_all):
         passes = min(1000, max(2, math.ceil(budget_s / max(dt, 1e-3))))
         t0 = time.perf_counter()
@@ -991,9 +1111,9 @@ def cpu_baseline(wl, args, budget_s: float = 10.0):
             pool.run(rows_all)
         dt = time.perf_counter() - t0
         n = passes * len(rows_all)
-        sample = f"{passes} passes over all {wl.rows} {what} of one step"
+        sample = f"{passes} passes over all {len(rows_all) * per_row} {what} of one step"
     pool.close()
-    return {"value": round(n / dt, 2), "unit": unit, "cores": cores,
+    return {"value": round(n * per_row / dt, 2), "unit": unit, "cores": cores,
             "kind": "oracle", "sample": sample, "seconds": round(dt, 3)}
 
 

@@ -1,7 +1,7 @@
 /*
  * sa.h -- C ABI of the GB300 KV-cache attention library (libsa.so).
  *
- * Seven operations, all computed on the GPU on the caller's stream:
+ * Eight operations, all computed on the GPU on the caller's stream:
  *
  *   validate_indices     index-row validation with a device error word
  *   build_present_kv     present K/V = past ++ current (concat or in-place append)
@@ -10,6 +10,8 @@
  *   paged_attn_decode    causal decode over a 16-token page table
  *   sparse_index_select  ratio-4 index scoring + top-k (produces selected indices)
  *   csa_ratio4_attention compressed sparse attention: window store + records + sink
+ *   csa_*_compress       the compression stages that produce the CSA records
+ *                        (ratio 128, ratio-4 attention records, ratio-4 index keys)
  *
  * Conventions shared by every call
  * --------------------------------
@@ -39,7 +41,10 @@
  *  [PG]  ferrum-kernels vnext_ops/transformer/causal_attention.rs: paged KV
  *        blocks of 16 tokens addressed through a table.
  *  [CSA-CPU] onnx-runtime-ep-cpu compressed_sparse_attention.rs: the ratio-4
- *        index stream (finalize_index_query, select_ratio4_topk).
+ *        index stream (finalize_index_query, select_ratio4_topk) and the
+ *        compression stream (compress_ratio4_stream, pool_ratio4_record,
+ *        pool_ratio128_record, finalize_attention_record,
+ *        finalize_index_record, apply_compressed_rope).
  */
 #ifndef SA_H
 #define SA_H
@@ -83,6 +88,8 @@ extern "C" {
 #define SA_ERRBIT_TIMEOUT 256    /* a kernel's bounded wait for a copy ran out  */
 #define SA_ERRBIT_RECORD 2048    /* csa_ratio4_attention: a selected record at or
                                     past the valid records (skipped)             */
+#define SA_ERRBIT_COMPRESS 4096  /* csa_*_compress: a record met a non-finite
+                                    value and was stored as zeros                */
 
 /* ---- sa_sparse_params.options bits ------------------------------------- */
 #define SA_OPT_ROW_COPIES 1u     /* dense f16/bf16 caches: fetch each K/V row with
@@ -384,6 +391,83 @@ typedef struct {
 
 size_t csa_ratio4_attention_workspace(const sa_csa_params* p);
 int csa_ratio4_attention(const sa_csa_params* p, void* stream);
+
+/*
+ * csa_ratio128_compress / csa_ratio4_main_compress / csa_ratio4_index_compress
+ * -- the compression stages that produce the CSA records: [CSA-CPU]
+ * compress_ratio4_stream, pool_ratio4_record, pool_ratio128_record,
+ * finalize_attention_record, finalize_index_record, apply_compressed_rope;
+ * [CSA] csa_ratio128_compress, csa_ratio4_main_compress,
+ * csa_ratio4_index_compress.
+ *
+ * One call appends S tokens per sequence at positions start = total - S ..
+ * total - 1.  Token p's score row is gate + ape[p % ratio].  Every block of
+ * `ratio` tokens that closes in [start, total) emits record k = p / ratio
+ * (p its last token), computed at block_start = k * ratio:
+ *   pool: per dimension d, over the candidates in order -- ratio 128: the
+ *     block's 128 tokens; ratio 4: the previous block's 4 tokens on source
+ *     dim d, then the block's 4 tokens on source dim D + d (a token before
+ *     position 0 is no candidate) -- the weighted mean sum(w v) / sum(w)
+ *     with w = e^(score - max score) (the binary32 rounding of the exact
+ *     value), candidates of score -inf left out; then bf16;
+ *   RMSNorm: binary32 square sum in dimension order, times
+ *     1 / sqrt(sum / D + 1e-6), times norm[d], bf16;
+ *   compressed RoPE of the last n_rope dims, pair i = dims (D - n_rope + 2i,
+ *     +1): frequency f = b (1 - r) + (b / 16) r with b = 160000^(-2i/n_rope)
+ *     and r = clamp((i - 15) / 10, 0, 1), angle = block_start * f (binary32),
+ *     cos and sin rounded from their exact values; each component bf16;
+ *   attention records (main, ratio 128): (D - n_rope) / 64 blocks of
+ *     [E8M0 byte, 64 E4M3FN codes] -- the block exponent is the smallest e
+ *     with amax / 2^e <= 448 (0 for a zero block), codes the nearest-even
+ *     E4M3FN of x / 2^e -- then the n_rope dims as little-endian bf16:
+ *     (D - n_rope) / 64 * 65 + 2 n_rope bytes (583 at D 512, n_rope 64);
+ *   index keys: the Walsh-Hadamard transform (butterflies of span 1, 2, 4,
+ *     ..., then times 1 / sqrt(D), bf16), then D / 32 blocks of [E8M0 byte,
+ *     16 bytes of FP4 E2M1 codes, even element in the low nibble] with the
+ *     OCP MX scale 2^(floor(log2 amax) - 2) (byte 0 for a zero block):
+ *     D / 32 * 17 bytes (68 at D 128).
+ * Every step is one binary32 operation rounded to nearest, in this order.
+ * A record that meets a non-finite value (no finite score in a dimension,
+ * an unusable sum, a non-finite square sum or result) is stored as zeros and
+ * sets SA_ERRBIT_COMPRESS in err_word (nullable).
+ *
+ * Layouts (float32 unless stated): kv, gate [B, S, W] with W = D (ratio
+ * 128) or 2 D (ratio 4); ape [ratio, W]; norm [D]; carry [B, slots, 2, W]
+ * with slots 128 (ratio 128) or 8 (ratio 4), channel 0 the value and 1 the
+ * score, read and rewritten in place: it holds the open block's tokens (slot
+ * p % 128, or 4 + p % 4) and, at ratio 4, the last closed block's (slots
+ * 0..3); empty slots hold (0, -inf).  A call with start == 0 ignores the
+ * carry's contents.  records [B, rows, record_stride] bytes and logical
+ * [B, rows, D] (the record's dequantized values), each nullable but not
+ * both: row k is written, the others untouched.  rows >= total / ratio.
+ * Shapes: attention records need D % 4 == 0, D <= 1024, (D - n_rope) % 64
+ * == 0; index keys D in {32, 64, 128, 256}; n_rope even, <= min(D, 128).
+ * kv, gate, ape and carry 16-byte aligned.  No workspace.
+ */
+typedef struct {
+  const float* kv;
+  const float* gate;
+  const float* ape;
+  const float* norm;
+  float* carry;
+  uint8_t* records;
+  float* logical;
+  uint32_t* err_word;
+  int64_t B, S, D, n_rope, rows, record_stride, total;
+  int64_t reserved_;  /* must be 0 */
+} sa_compress_params;
+
+int csa_ratio128_compress(const sa_compress_params* p, void* stream);
+int csa_ratio4_main_compress(const sa_compress_params* p, void* stream);
+int csa_ratio4_index_compress(const sa_compress_params* p, void* stream);
+
+/*
+ * csa_pool_weight -- w[i] = e^t[i] rounded to binary32 (nearest even), the
+ * pool weight of the compression stages, for checking that rounding on its
+ * own: t, w device float32 [n] (t <= 0 is the compression's domain; any
+ * value is accepted).  Returns SA_OK or an argument error.
+ */
+int csa_pool_weight(const float* t, float* w, int64_t n, void* stream);
 
 /* attention-mask element types of sa_prefill_params.mask_kind */
 #define SA_MASK_NONE 0

@@ -8,7 +8,9 @@ falling back to anything else.
 
 Entry points (same names as the C ABI):
     validate_indices, build_present_kv, sparse_attn_decode, attn_prefill,
-    paged_attn_decode, sparse_index_select, csa_ratio4_attention
+    paged_attn_decode, sparse_index_select, csa_ratio4_attention,
+    csa_ratio128_compress, csa_ratio4_main_compress, csa_ratio4_index_compress,
+    csa_pool_weight
 """
 from __future__ import annotations
 
@@ -31,6 +33,8 @@ __all__ = [
     "IndexSelectParams", "sparse_index_select", "sparse_index_select_workspace",
     "SEL_TIE", "SEL_NONFINITE", "ERRBIT_SEL_TIE", "ERRBIT_SEL_NONFINITE",
     "CsaParams", "csa_ratio4_attention", "csa_ratio4_attention_workspace", "ERRBIT_RECORD",
+    "CompressParams", "csa_ratio128_compress", "csa_ratio4_main_compress",
+    "csa_ratio4_index_compress", "csa_pool_weight", "ERRBIT_COMPRESS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -46,6 +50,7 @@ OPT_ROW_COPIES, OPT_FP8_WARP_MMA = 1, 2
 SEL_TIE, SEL_NONFINITE = 1, 2
 ERRBIT_SEL_TIE, ERRBIT_SEL_NONFINITE = 512, 1024
 ERRBIT_RECORD = 2048
+ERRBIT_COMPRESS = 4096
 
 _p = C.c_void_p
 _i64 = C.c_int64
@@ -116,6 +121,15 @@ class CsaParams(C.Structure):
     ]
 
 
+class CompressParams(C.Structure):
+    _fields_ = [
+        ("kv", _p), ("gate", _p), ("ape", _p), ("norm", _p), ("carry", _p), ("records", _p),
+        ("logical", _p), ("err_word", _p),
+        ("B", _i64), ("S", _i64), ("D", _i64), ("n_rope", _i64), ("rows", _i64),
+        ("record_stride", _i64), ("total", _i64), ("reserved_", _i64),
+    ]
+
+
 class SAError(RuntimeError):
     def __init__(self, call: str, status: int):
         super().__init__(f"{call}: status {status} ({status_string(status)})")
@@ -170,6 +184,13 @@ def load():
         L.csa_ratio4_attention_workspace.argtypes = [C.POINTER(CsaParams)]
         L.csa_ratio4_attention.restype = C.c_int
         L.csa_ratio4_attention.argtypes = [C.POINTER(CsaParams), _p]
+        for name in ("csa_ratio128_compress", "csa_ratio4_main_compress",
+                     "csa_ratio4_index_compress"):
+            fn = getattr(L, name)
+            fn.restype = C.c_int
+            fn.argtypes = [C.POINTER(CompressParams), _p]
+        L.csa_pool_weight.restype = C.c_int
+        L.csa_pool_weight.argtypes = [_p, _p, _i64, _p]
         L.paged_attn_decode_workspace.restype = C.c_size_t
         L.paged_attn_decode_workspace.argtypes = [C.POINTER(PagedParams)]
         L.paged_attn_decode.restype = C.c_int
@@ -635,3 +656,76 @@ def csa_ratio4_attention(query, current_kv, records, selected, *, total, n_rope,
     p.workspace, p.workspace_bytes = _ptr(ws), nb
     _check("csa_ratio4_attention", L.csa_ratio4_attention(C.byref(p), _stream(stream)))
     return y
+
+
+# ---- CSA compression stages ---------------------------------------------------------------
+
+def _compress(name, ratio, D, kv, gate, ape, norm, carry, *, n_rope, total, records, logical,
+              err_word, stream):
+    L = load()
+    for n, t in (("kv", kv), ("gate", gate), ("ape", ape), ("norm", norm), ("carry", carry),
+                 ("records", records), ("logical", logical), ("err_word", err_word)):
+        _dev(t, n)
+    for n, t in (("kv", kv), ("gate", gate), ("ape", ape), ("norm", norm), ("carry", carry),
+                 ("logical", logical)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise TypeError(f"{n} must be a contiguous float32 tensor")
+    if records is not None and (records.dtype != torch.uint8 or not records.is_contiguous()):
+        raise TypeError("records must be a contiguous uint8 tensor")
+    B, S = kv.shape[0], kv.shape[1]
+    p = CompressParams()
+    p.kv, p.gate, p.ape, p.norm = kv.data_ptr(), gate.data_ptr(), ape.data_ptr(), norm.data_ptr()
+    p.carry, p.records, p.logical = carry.data_ptr(), _ptr(records), _ptr(logical)
+    p.err_word = _ptr(err_word)
+    p.B, p.S, p.D, p.n_rope, p.total = B, S, D, int(n_rope), int(total)
+    if records is not None:
+        p.rows, p.record_stride = records.shape[1], records.shape[2]
+    else:
+        p.rows, p.record_stride = logical.shape[1], 0
+    _check(name, getattr(L, name)(C.byref(p), _stream(stream)))
+
+
+def csa_ratio128_compress(kv, gate, ape, norm, carry, *, n_rope, total, records=None,
+                          logical=None, err_word=None, stream=None):
+    """Append ``S`` tokens to a ratio-128 compression stream.  ``kv``, ``gate``
+    float32 ``[B, S, D]``, ``ape`` ``[128, D]``, ``norm`` ``[D]``, ``carry``
+    ``[B, 128, 2, D]`` (updated in place); every block of 128 tokens that
+    closes is written to ``records`` (uint8 ``[B, rows, stride]``, hybrid
+    FP8) and/or ``logical`` (float32 ``[B, rows, D]``) at row ``p // 128``."""
+    _compress("csa_ratio128_compress", 128, kv.shape[2], kv, gate, ape, norm, carry,
+              n_rope=n_rope, total=total, records=records, logical=logical,
+              err_word=err_word, stream=stream)
+
+
+def csa_ratio4_main_compress(kv, gate, ape, norm, carry, *, n_rope, total, records=None,
+                             logical=None, err_word=None, stream=None):
+    """Append ``S`` tokens to a ratio-4 attention-record stream.  ``kv``,
+    ``gate`` float32 ``[B, S, 2D]``, ``ape`` ``[4, 2D]``, ``norm`` ``[D]``,
+    ``carry`` ``[B, 8, 2, 2D]`` (updated in place); records as for ratio 128,
+    at row ``p // 4``."""
+    _compress("csa_ratio4_main_compress", 4, kv.shape[2] // 2, kv, gate, ape, norm, carry,
+              n_rope=n_rope, total=total, records=records, logical=logical,
+              err_word=err_word, stream=stream)
+
+
+def csa_ratio4_index_compress(kv, gate, ape, norm, carry, *, n_rope, total, records=None,
+                              logical=None, err_word=None, stream=None):
+    """Append ``S`` tokens to a ratio-4 index-key stream (FP4 keys of
+    ``D / 32 * 17`` bytes, Hadamard-transformed); shapes as for
+    ``csa_ratio4_main_compress``."""
+    _compress("csa_ratio4_index_compress", 4, kv.shape[2] // 2, kv, gate, ape, norm, carry,
+              n_rope=n_rope, total=total, records=records, logical=logical,
+              err_word=err_word, stream=stream)
+
+
+def csa_pool_weight(t, *, w=None, stream=None):
+    """``e^t`` rounded to binary32 as the compression pool computes it;
+    ``t`` a contiguous float32 CUDA tensor."""
+    _dev(t, "t")
+    if t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError("t must be a contiguous float32 tensor")
+    if w is None:
+        w = torch.empty_like(t)
+    _check("csa_pool_weight", load().csa_pool_weight(t.data_ptr(), w.data_ptr(), t.numel(),
+                                                      _stream(stream)))
+    return w

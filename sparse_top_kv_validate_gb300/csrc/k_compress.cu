@@ -1,0 +1,600 @@
+// k_compress.cu -- the CSA compression stages: ratio-4 attention records,
+// ratio-4 index keys and ratio-128 attention records, produced from the
+// compressor's value and gate rows and the carry of the open block.
+//
+// Semantics: onnx-runtime-ep-cpu src/kernels/compressed_sparse_attention.rs,
+// compress_ratio4_stream / pool_ratio4_record / pool_ratio128_record /
+// finalize_attention_record / finalize_index_record / apply_compressed_rope,
+// and onnx-runtime-ep-cuda compressed_sparse_attention.rs,
+// csa_ratio128_compress / csa_ratio4_main_compress / csa_ratio4_index_compress.
+// A record is the per-dimension softmax pool of its candidates (score = gate
+// + ape), rounded to bf16, RMS-normalised times a learned scale (bf16), its
+// last n_rope dimensions rotated by the compressed RoPE at the block start
+// (bf16 per component), then stored as FP8 blocks + a bf16 tail (attention)
+// or Hadamard-transformed and stored as FP4 blocks (index keys).
+//
+// GB300 design.  The pages run one serial thread per sequence that walks the
+// carry token by token.  A record depends only on the tokens of its block
+// (ratio 4: and of the block before), each found either in this call's rows
+// or in the carry, so every record a call closes is computed independently:
+//  * compress_r4_kernel: one warp per record; the 8 warps of a CTA take 8
+//    sequences at the same record index, so the RoPE rotation (one double
+//    sine and cosine per pair) is evaluated once per CTA.  Lanes pool four
+//    dimensions at a time from 16-byte loads of the 8 candidates' values and
+//    scores, stage the pooled record in shared memory and finalize it there.
+//  * compress_r128_kernel: one CTA per record, a thread per dimension pooling
+//    the block's 128 tokens, then warp 0 finalizes.
+//  * compress_carry_kernel: one thread per (sequence, source dimension)
+//    writes the carry the stream holds after the call (runs after the record
+//    kernel, which reads the carry of before the call).
+// Bit-exactness: every step is the pages' binary32 operation, rounded once,
+// in their order (no contraction; RMSNorm's square sum runs in dimension
+// order in one lane).  The pool weight e^t is the correctly rounded binary32
+// value: Tang's table-driven exponential (ACM TOMS 15(2), 1989) in
+// float-float arithmetic, accepted by Ziv's rounding test and otherwise
+// evaluated in double and rounded.
+#include <cmath>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "codes.cuh"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sa {
+
+namespace {
+
+// ---- e^t, t <= 0, correctly rounded to binary32 ------------------------------------------
+//
+// t = (256 m + j) ln2/256 + r with |r| <= ln2/512: e^t = 2^m 2^(j/256) e^r.
+// 2^(j/256) is held as hi + lo (binary32 pair, ~2^-48 relative); r as
+// r_hi + r_lo from a three-part ln2/256 (k L1 exact through an FMA residual);
+// e^r - 1 - r = r^2/2 + r^3/6 (the r^4 term is below 2^-42).  The error of
+// the float-float value is below 2^-38.4 of the result (the largest seen
+// over a dense sample is 2^-39.3); it is rounded once and accepted when its
+// residual stays 2^-37 clear of a rounding boundary, about 1 input in 8000
+// falling back to the double evaluation.
+
+struct ExpTable {
+  float hi[256];
+  float lo[256];
+};
+
+__host__ __device__ constexpr double exp_series(double x) {
+  double term[32] = {};
+  term[0] = 1.0;
+  for (int n = 1; n < 32; ++n) term[n] = term[n - 1] * x / n;
+  double s = 0.0;
+  for (int n = 31; n >= 0; --n) s += term[n];  // smallest terms first
+  return s;
+}
+
+__host__ __device__ constexpr ExpTable make_exp_table() {
+  ExpTable t{};
+  for (int j = 0; j < 256; ++j) {
+    const double v = exp_series(j * (0.69314718055994530942 / 256.0));
+    t.hi[j] = static_cast<float>(v);
+    t.lo[j] = static_cast<float>(v - static_cast<double>(t.hi[j]));
+  }
+  return t;
+}
+
+__device__ const ExpTable g_exp_table = make_exp_table();
+
+constexpr float kInvL = 0x1.7153b2p+8f;   // 256 / ln 2
+constexpr float kL1 = 0x1.62e43p-9f;      // ln2/256 = kL1 + kL2 + O(2^-61)
+constexpr float kL2 = -0x1.05c61p-37f;
+constexpr float kSixth = 0x1.555556p-3f;
+constexpr float kMargin = 0x1p-37f;
+
+// Error-free sum: the rounding error of s = a + b.
+__device__ __forceinline__ float two_sum_err(float a, float b, float s) {
+  const float bb = __fsub_rn(s, a);
+  return __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __noinline__ float exp_double(float t) {
+  return static_cast<float>(exp(static_cast<double>(t)));
+}
+
+__device__ __forceinline__ float pool_weight(float t, const float* thi, const float* tlo) {
+  if (t == 0.0f) return 1.0f;
+  // NaN, positive t, and t < -87 (subnormal or zero results) take the double path
+  if (!(t >= -87.0f && t <= 0.0f)) return exp_double(t);
+  const float kf = rintf(__fmul_rn(t, kInvL));
+  const int k = __float2int_rn(kf);
+  const float p1 = __fmul_rn(kf, kL1);
+  const float e1 = __fmaf_rn(kf, kL1, -p1);
+  const float a_hi = __fsub_rn(t, p1);
+  const float a_lo = two_sum_err(t, -p1, a_hi);
+  const float bsum = __fmaf_rn(kf, kL2, e1);
+  const float r_hi = __fsub_rn(a_hi, bsum);
+  const float r_lo = __fadd_rn(two_sum_err(a_hi, -bsum, r_hi), a_lo);
+  const float q = __fmul_rn(__fmul_rn(r_hi, r_hi), __fmaf_rn(r_hi, kSixth, 0.5f));
+  const float u = __fadd_rn(r_lo, q);
+  const int j = k & 255, m = k >> 8;
+  const float th = thi[j], tl = tlo[j];
+  const float p_hi = __fmul_rn(th, r_hi);
+  const float p_lo = __fmaf_rn(th, r_hi, -p_hi);
+  const float w = __fadd_rn(__fmaf_rn(th, u, p_lo), __fmaf_rn(tl, r_hi, tl));
+  const float z_hi = __fadd_rn(p_hi, w);
+  const float z_lo = two_sum_err(p_hi, w, z_hi);
+  const float y = __fadd_rn(th, z_hi);
+  const float err = __fadd_rn(__fsub_rn(z_hi, __fsub_rn(y, th)), z_lo);
+  // The exact value is y + err within kMargin.  h = half the spacing from y
+  // towards err (y in [0.99, 2.01]; below a power of two the spacing halves).
+  // |err| clear below h: y is the rounding; clear above h: the neighbour on
+  // err's side is (|err| <= h + ulp(z_hi) / 2, far from the next midpoint).
+  const uint32_t yb = __float_as_uint(y);
+  float h = __uint_as_float((yb & 0x7f800000u) - (24u << 23));
+  if ((yb & 0x007fffffu) == 0 && err < 0.0f) h = __fmul_rn(h, 0.5f);
+  const float ae = fabsf(err);
+  float r;
+  if (__fadd_rn(ae, kMargin) < h)
+    r = y;
+  else if (__fsub_rn(ae, kMargin) > h)
+    r = __uint_as_float(err > 0.0f ? yb + 1u : yb - 1u);
+  else
+    return exp_double(t);
+  return __fmul_rn(r, pow2f(m));  // exact: the result is a normal number
+}
+
+// ---- shared pieces -------------------------------------------------------------------------
+
+constexpr int kR4Warps = 8;
+constexpr int kTableFloats = 512 + 128;  // exp table + up to 64 (cos, sin) pairs
+
+__device__ __forceinline__ void load_exp_table(float* thi, float* tlo) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+    thi[i] = g_exp_table.hi[i];
+    tlo[i] = g_exp_table.lo[i];
+  }
+}
+
+// The compressed RoPE rotation at block_start, one (cos, sin) per pair:
+// frequency = base (1 - ramp) + (base / 16) ramp, ramp = clamp((i - 15) / 10),
+// angle = position * frequency in binary32; sine and cosine of the binary32
+// angle are evaluated in double and rounded.
+__device__ void rope_rotation(const CompressArgs& a, int64_t block_start, float2* rot,
+                              int lane) {
+  const float p = __ll2float_rn(block_start);
+  for (int i = lane; i < a.n_rope / 2; i += 32) {
+    float ramp = __fdiv_rn(__fsub_rn(static_cast<float>(i), 15.0f), 10.0f);
+    ramp = fminf(1.0f, fmaxf(0.0f, ramp));
+    const float base = a.rope_base[i];
+    const float f = __fadd_rn(__fmul_rn(base, __fsub_rn(1.0f, ramp)),
+                              __fmul_rn(__fdiv_rn(base, 16.0f), ramp));
+    const float ang = __fmul_rn(p, f);
+    double s, c;
+    sincos(static_cast<double>(ang), &s, &c);
+    rot[i] = make_float2(static_cast<float>(c), static_cast<float>(s));
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Exponent of an FP8 block: the smallest e with amax / 2^e <= 448 (0 for
+// amax 0), clamped to [-127, 127].  448 = 1.75 * 2^8.
+__device__ __forceinline__ int fp8_block_exponent(float amax) {
+  if (amax == 0.0f) return 0;
+  const uint32_t u = __float_as_uint(amax);
+  const bool above = (u & 0x7f800000u) && (u & 0x7fffffu) > 0x600000u;
+  const int e = floor_log2(amax) - 8 + (above ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+__device__ __forceinline__ float e4m3_value(uint8_t c) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));
+}
+
+// Finalize one record held (pooled, bf16-rounded) in shared memory rec[D],
+// by one warp: RMSNorm, RoPE, (index: Hadamard), validity, quantize, store.
+template <int KIND>
+__device__ void finalize_warp(const CompressArgs& a, float* rec, const float2* rot, int64_t b,
+                              int64_t k, bool ok, int lane) {
+  const int D = a.D;
+  // RMSNorm: the binary32 square sum in dimension order, in one lane
+  float inv = 0.0f;
+  int sum_ok = 0;
+  if (lane == 0) {
+    float sum = 0.0f;
+    for (int d = 0; d < D; d += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(rec + d);
+      sum = __fadd_rn(sum, __fmul_rn(x.x, x.x));
+      sum = __fadd_rn(sum, __fmul_rn(x.y, x.y));
+      sum = __fadd_rn(sum, __fmul_rn(x.z, x.z));
+      sum = __fadd_rn(sum, __fmul_rn(x.w, x.w));
+    }
+    sum_ok = isfinite(sum) ? 1 : 0;
+    inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(sum, static_cast<float>(D)), 1.0e-6f)));
+  }
+  inv = __shfl_sync(0xffffffffu, inv, 0);
+  ok = ok && __shfl_sync(0xffffffffu, sum_ok, 0);
+  for (int d = lane; d < D; d += 32)
+    rec[d] = round_bf16(__fmul_rn(__fmul_rn(rec[d], inv), __ldg(a.norm + d)));
+  __syncwarp();
+  for (int i = lane; i < a.n_rope / 2; i += 32) {
+    const int d = D - a.n_rope + 2 * i;
+    const float re = rec[d], im = rec[d + 1];
+    const float2 cs = rot[i];
+    rec[d] = round_bf16(__fsub_rn(__fmul_rn(re, cs.x), __fmul_rn(im, cs.y)));
+    rec[d + 1] = round_bf16(__fadd_rn(__fmul_rn(re, cs.y), __fmul_rn(im, cs.x)));
+  }
+  __syncwarp();
+  if (KIND == kCompressIndex) {
+    // Walsh-Hadamard butterflies, span 1, 2, 4, ...: a level's pairs are disjoint
+    for (int span = 1; span < D; span *= 2) {
+      for (int q = lane; q < D / 2; q += 32) {
+        const int i = (q / span) * 2 * span + (q % span);
+        const float l = rec[i], r = rec[i + span];
+        rec[i] = __fadd_rn(l, r);
+        rec[i + span] = __fsub_rn(l, r);
+      }
+      __syncwarp();
+    }
+    const float hs = __frcp_rn(__fsqrt_rn(static_cast<float>(D)));
+    for (int d = lane; d < D; d += 32) rec[d] = round_bf16(__fmul_rn(rec[d], hs));
+    __syncwarp();
+  }
+  bool fin = true;
+  for (int d = lane; d < D; d += 32) fin = fin && isfinite(rec[d]);
+  ok = __all_sync(0xffffffffu, ok && fin);
+
+  uint8_t* dst = a.records ? a.records + (b * a.rows + k) * a.record_stride : nullptr;
+  float* lg = a.logical ? a.logical + (b * a.rows + k) * static_cast<int64_t>(D) : nullptr;
+  if (!ok) {
+    if (dst)
+      for (int i = lane; i < a.width; i += 32) dst[i] = 0;
+    if (lg)
+      for (int d = lane; d < D; d += 32) lg[d] = 0.0f;
+    if (lane == 0 && a.err_word) atomicOr(a.err_word, static_cast<uint32_t>(SA_ERRBIT_COMPRESS));
+    return;
+  }
+  if (KIND == kCompressAttn) {
+    const int nb = (D - a.n_rope) / 64;
+    for (int blk = 0; blk < nb; ++blk) {
+      const float x0 = rec[64 * blk + lane], x1 = rec[64 * blk + 32 + lane];
+      const int e = fp8_block_exponent(warp_max(fmaxf(fabsf(x0), fabsf(x1))));
+      const float sc = pow2f(-e);
+      const uint8_t c0 = __nv_cvt_float_to_fp8(__fmul_rn(x0, sc), __NV_SATFINITE, __NV_E4M3);
+      const uint8_t c1 = __nv_cvt_float_to_fp8(__fmul_rn(x1, sc), __NV_SATFINITE, __NV_E4M3);
+      if (dst) {
+        if (lane == 0) dst[blk * 65] = static_cast<uint8_t>(e + 127);
+        dst[blk * 65 + 1 + lane] = c0;
+        dst[blk * 65 + 33 + lane] = c1;
+      }
+      if (lg) {
+        const float s = pow2f(e);
+        lg[64 * blk + lane] = __fmul_rn(e4m3_value(c0), s);
+        lg[64 * blk + 32 + lane] = __fmul_rn(e4m3_value(c1), s);
+      }
+    }
+    for (int r = lane; r < a.n_rope; r += 32) {
+      const float v = rec[D - a.n_rope + r];
+      const uint32_t bits = __float_as_uint(v) >> 16;  // v is a bf16 value
+      if (dst) {
+        dst[nb * 65 + 2 * r] = static_cast<uint8_t>(bits & 0xffu);
+        dst[nb * 65 + 2 * r + 1] = static_cast<uint8_t>(bits >> 8);
+      }
+      if (lg) lg[D - a.n_rope + r] = v;
+    }
+  } else {
+    for (int blk = 0; blk < D / 32; ++blk) {
+      const float x = rec[32 * blk + lane];
+      const float amax = warp_max(fabsf(x));
+      int e = -127;  // an all-zero block: scale byte 0
+      if (amax > 0.0f) {
+        e = floor_log2(amax) - 2;
+        e = e < -127 ? -127 : (e > 127 ? 127 : e);
+      }
+      const float xs = __fmul_rn(x, pow2f(-e));
+      const int tw = e2m1_twice(fabsf(xs));
+      int code = e2m1_code(tw);
+      if (xs < 0.0f && code) code |= 8;
+      const int hi = __shfl_down_sync(0xffffffffu, code, 1);
+      if (dst) {
+        if (lane == 0) dst[blk * 17] = static_cast<uint8_t>(e + 127);
+        if (!(lane & 1)) dst[blk * 17 + 1 + lane / 2] = static_cast<uint8_t>(code | (hi << 4));
+      }
+      if (lg) {
+        const float mag = __fmul_rn(0.5f * static_cast<float>(tw), pow2f(e));
+        lg[32 * blk + lane] = (code & 8) ? -mag : mag;
+      }
+    }
+  }
+}
+
+// ---- ratio 4 -------------------------------------------------------------------------------
+
+// Source rows of candidate c of record k (ratio 4): c < 4 the previous
+// block's token 4k - 4 + c on source dims [0, D), c >= 4 the block's token
+// 4k + c - 4 on [D, 2D).  A token of this call is read from kv / gate (+ the
+// ape row of its phase); an earlier one from its carry slot (the open block's
+// tokens in slots 4 + phase, the closed block before it in slots 0..3).
+struct Cand {
+  const float* v;
+  const float* s;
+  const float* ape;  // nullptr: the score is stored (carry)
+};
+
+__device__ __forceinline__ Cand r4_candidate(const CompressArgs& a, int64_t b, int64_t k, int c) {
+  const int64_t P = c < 4 ? 4 * k - 4 + c : 4 * k + c - 4;
+  const int64_t half = c < 4 ? 0 : a.D;
+  Cand x{nullptr, nullptr, nullptr};
+  if (P < 0) return x;
+  if (P >= a.start) {
+    const int64_t off = (b * a.S + (P - a.start)) * a.W + half;
+    x.v = a.kv + off;
+    x.s = a.gate + off;
+    x.ape = a.ape + (P & 3) * a.W + half;
+  } else {
+    const int64_t open_from = a.start - (a.start & 3);
+    const int64_t slot = P >= open_from ? 4 + (P & 3) : (P & 3);
+    const float* base = a.carry + ((b * 8 + slot) * 2) * a.W + half;
+    x.v = base;
+    x.s = base + a.W;
+  }
+  return x;
+}
+
+__device__ __forceinline__ float4 ld4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+__device__ __forceinline__ float4 add4(float4 x, float4 y) {
+  return make_float4(__fadd_rn(x.x, y.x), __fadd_rn(x.y, y.y), __fadd_rn(x.z, y.z),
+                     __fadd_rn(x.w, y.w));
+}
+
+// One dimension's pool over 8 candidates, in candidate order.
+__device__ __forceinline__ float pool8(const float (&s)[8], const float (&v)[8], bool& ok,
+                                       const float* thi, const float* tlo) {
+  float m = SA_NEG_INF;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) m = fmaxf(m, s[c]);
+  ok = ok && isfinite(m);
+  float num = 0.0f, den = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    if (s[c] == SA_NEG_INF) continue;
+    const float w = pool_weight(__fsub_rn(s[c], m), thi, tlo);
+    num = __fadd_rn(num, __fmul_rn(w, v[c]));
+    den = __fadd_rn(den, w);
+  }
+  ok = ok && den != 0.0f && isfinite(den) && isfinite(num);
+  return round_bf16(__fdiv_rn(num, den));
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kR4Warps * 32) compress_r4_kernel(const CompressArgs a) {
+  extern __shared__ __align__(16) float smem[];
+  float* thi = smem;
+  float* tlo = smem + 256;
+  float2* rot = reinterpret_cast<float2*>(smem + 512);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t k = a.k0 + blockIdx.x;
+  load_exp_table(thi, tlo);
+  if (warp == 0) rope_rotation(a, 4 * k, rot, lane);
+  __syncthreads();
+  const int64_t b = static_cast<int64_t>(blockIdx.y) * kR4Warps + warp;
+  if (b >= a.B) return;
+  float* rec = smem + kTableFloats + warp * a.D;
+  bool ok = true;
+  for (int d0 = 4 * lane; d0 < a.D; d0 += 128) {
+    float s[4][8], v[4][8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const Cand x = r4_candidate(a, b, k, c);
+      float4 sv = make_float4(SA_NEG_INF, SA_NEG_INF, SA_NEG_INF, SA_NEG_INF);
+      float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (x.v) {
+        vv = ld4(x.v + d0);
+        sv = ld4(x.s + d0);
+        if (x.ape) sv = add4(sv, ld4(x.ape + d0));
+      }
+      s[0][c] = sv.x, s[1][c] = sv.y, s[2][c] = sv.z, s[3][c] = sv.w;
+      v[0][c] = vv.x, v[1][c] = vv.y, v[2][c] = vv.z, v[3][c] = vv.w;
+    }
+    float4 out;
+    out.x = pool8(s[0], v[0], ok, thi, tlo);
+    out.y = pool8(s[1], v[1], ok, thi, tlo);
+    out.z = pool8(s[2], v[2], ok, thi, tlo);
+    out.w = pool8(s[3], v[3], ok, thi, tlo);
+    *reinterpret_cast<float4*>(rec + d0) = out;
+  }
+  ok = __all_sync(0xffffffffu, ok);
+  __syncwarp();
+  finalize_warp<KIND>(a, rec, rot, b, k, ok, lane);
+}
+
+// ---- ratio 128 -----------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(1024) compress_r128_kernel(const CompressArgs a) {
+  extern __shared__ __align__(16) float smem[];
+  float* thi = smem;
+  float* tlo = smem + 256;
+  float2* rot = reinterpret_cast<float2*>(smem + 512);
+  float* rec = smem + kTableFloats;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t k = a.k0 + blockIdx.x;
+  const int64_t b = blockIdx.y;
+  load_exp_table(thi, tlo);
+  if (warp == 0) rope_rotation(a, 128 * k, rot, lane);
+  __syncthreads();
+  // candidates: the block's tokens 128k + j; those of this call from kv /
+  // gate + ape[j], the earlier ones from carry slot j
+  const int64_t first_new = a.start - 128 * k;  // j >= first_new: this call's rows
+  const int64_t W = a.W;
+  const float* cy = a.carry + b * 128 * 2 * W;
+  const float* src_v = a.kv + (b * a.S - a.start + 128 * k) * W;
+  const float* src_g = a.gate + (b * a.S - a.start + 128 * k) * W;
+  bool ok = true;
+  for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+    float m = SA_NEG_INF;
+    for (int j = 0; j < 128; ++j) {
+      const float s = j >= first_new
+                          ? __fadd_rn(__ldg(src_g + j * W + d), __ldg(a.ape + j * W + d))
+                          : cy[(2 * j + 1) * W + d];
+      m = fmaxf(m, s);
+    }
+    ok = ok && isfinite(m);
+    float num = 0.0f, den = 0.0f;
+    for (int j = 0; j < 128; ++j) {
+      float s, v;
+      if (j >= first_new) {
+        s = __fadd_rn(__ldg(src_g + j * W + d), __ldg(a.ape + j * W + d));
+        v = __ldg(src_v + j * W + d);
+      } else {
+        s = cy[(2 * j + 1) * W + d];
+        v = cy[(2 * j) * W + d];
+      }
+      if (s == SA_NEG_INF) continue;
+      const float w = pool_weight(__fsub_rn(s, m), thi, tlo);
+      num = __fadd_rn(num, __fmul_rn(w, v));
+      den = __fadd_rn(den, w);
+    }
+    ok = ok && den != 0.0f && isfinite(den) && isfinite(num);
+    rec[d] = round_bf16(__fdiv_rn(num, den));
+  }
+  ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  if (warp == 0) finalize_warp<kCompressAttn>(a, rec, rot, b, k, ok, lane);
+}
+
+// ---- the carry after the call --------------------------------------------------------------
+
+__device__ __forceinline__ void carry_from_row(const CompressArgs& a, int64_t b, int64_t q,
+                                               int64_t d, float& v, float& s) {
+  const int64_t off = (b * a.S + (q - a.start)) * a.W + d;
+  v = __ldg(a.kv + off);
+  s = __fadd_rn(__ldg(a.gate + off), __ldg(a.ape + (q % a.ratio) * a.W + d));
+}
+
+__global__ void __launch_bounds__(256) compress_carry_kernel(const CompressArgs a) {
+  const int64_t d = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t b = blockIdx.y;
+  if (d >= a.W) return;
+  const int64_t W = a.W;
+  float* cy = a.carry + b * (a.ratio == 128 ? 128 : 8) * 2 * W;
+  const int64_t open_end = a.total - a.total % a.ratio;
+  if (a.ratio == 128) {
+    for (int j = 0; j < 128; ++j) {
+      const int64_t q = open_end + j;
+      float v = 0.0f, s = SA_NEG_INF;
+      if (q < a.total) {
+        if (q < a.start) continue;  // already in its slot
+        carry_from_row(a, b, q, d, v, s);
+      }
+      cy[(2 * j) * W + d] = v;
+      cy[(2 * j + 1) * W + d] = s;
+    }
+    return;
+  }
+  const int64_t open_from = a.start - a.start % 4;
+  float pv[4], ps[4];
+  bool pw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // previous-block slots: read everything first
+    pv[i] = 0.0f;
+    ps[i] = SA_NEG_INF;
+    pw[i] = true;
+    if (open_end == 0) continue;
+    const int64_t q = open_end - 4 + i;
+    if (q >= a.start) {
+      carry_from_row(a, b, q, d, pv[i], ps[i]);
+    } else if (q >= open_from) {  // the block was open before the call: it moves
+      pv[i] = cy[((4 + i) * 2) * W + d];
+      ps[i] = cy[((4 + i) * 2 + 1) * W + d];
+    } else {
+      pw[i] = false;  // the closed block before the call stays
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (!pw[i]) continue;
+    cy[(i * 2) * W + d] = pv[i];
+    cy[(i * 2 + 1) * W + d] = ps[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t q = open_end + i;
+    float v = 0.0f, s = SA_NEG_INF;
+    if (q < a.total) {
+      if (q < a.start) continue;
+      carry_from_row(a, b, q, d, v, s);
+    }
+    cy[((4 + i) * 2) * W + d] = v;
+    cy[((4 + i) * 2 + 1) * W + d] = s;
+  }
+}
+
+__global__ void pool_weight_kernel(const float* t, float* w, int64_t n) {
+  __shared__ float thi[256], tlo[256];
+  load_exp_table(thi, tlo);
+  __syncthreads();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += stride)
+    w[i] = pool_weight(__ldg(t + i), thi, tlo);
+}
+
+}  // namespace
+
+// ---- host side ------------------------------------------------------------------------------
+
+size_t compress_smem_bytes(int ratio, int64_t D) {
+  const int64_t recs = ratio == 4 ? kR4Warps * D : D;
+  return static_cast<size_t>(kTableFloats + recs) * sizeof(float);
+}
+
+template <typename K>
+static int set_smem(K kernel, size_t smem) {
+  if (smem <= 48 * 1024) return 0;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(smem)) == cudaSuccess
+             ? 0
+             : -1;
+}
+
+int launch_compress(const CompressArgs& a, cudaStream_t st) {
+  if (a.nk > 0) {
+    const size_t smem = compress_smem_bytes(static_cast<int>(a.ratio), a.D);
+    mark_event(a.ev_before, st);
+    if (a.ratio == 4) {
+      const dim3 grid(static_cast<unsigned>(a.nk),
+                      static_cast<unsigned>((a.B + kR4Warps - 1) / kR4Warps));
+      if (a.kind == kCompressAttn) {
+        if (set_smem(compress_r4_kernel<kCompressAttn>, smem) != 0) return -1;
+        compress_r4_kernel<kCompressAttn><<<grid, kR4Warps * 32, smem, st>>>(a);
+      } else {
+        if (set_smem(compress_r4_kernel<kCompressIndex>, smem) != 0) return -1;
+        compress_r4_kernel<kCompressIndex><<<grid, kR4Warps * 32, smem, st>>>(a);
+      }
+    } else {
+      const int threads = static_cast<int>((a.D + 31) / 32 * 32);
+      if (set_smem(compress_r128_kernel, smem) != 0) return -1;
+      compress_r128_kernel<<<dim3(static_cast<unsigned>(a.nk), static_cast<unsigned>(a.B)),
+                             threads, smem, st>>>(a);
+    }
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    mark_event(a.ev_after, st);
+  }
+  compress_carry_kernel<<<dim3(static_cast<unsigned>((a.W + 255) / 256),
+                               static_cast<unsigned>(a.B)),
+                          256, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_pool_weight(const float* t, float* w, int64_t n, cudaStream_t st) {
+  if (n <= 0) return 0;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  pool_weight_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(t, w, n);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace sa

@@ -256,6 +256,30 @@ struct CsaArgs {
 size_t csa_attn_smem_bytes(int64_t D);
 int launch_csa(const CsaArgs& a, cudaStream_t st);
 
+// ---- CSA compression stages (ratio 4 records / index keys, ratio 128) -------------------
+constexpr int kCompressAttn = 0;   // hybrid FP8 attention record
+constexpr int kCompressIndex = 1;  // FP4 index key
+
+struct CompressArgs {
+  const float* kv;            // [B, S, W] source values (W = D at ratio 128, 2 D at ratio 4)
+  const float* gate;          // [B, S, W] source scores
+  const float* ape;           // [ratio, W]
+  const float* norm;          // [D]
+  float* carry;               // [B, slots, 2, W], slots 128 or 8
+  uint8_t* records;           // nullable [B, rows, record_stride]
+  float* logical;             // nullable [B, rows, D]
+  uint32_t* err_word;         // nullable
+  int64_t B, S, W, rows, record_stride, start, total, ratio;
+  int64_t k0, nk;             // the records this call closes: k0 .. k0 + nk - 1
+  int D, n_rope, kind, width;
+  float rope_base[64];        // 160000^(-2i / n_rope) per RoPE pair, binary32
+  void* ev_before;            // nullable measurement events around the record kernel
+  void* ev_after;
+};
+size_t compress_smem_bytes(int ratio, int64_t D);
+int launch_compress(const CompressArgs& a, cudaStream_t st);
+int launch_pool_weight(const float* t, float* w, int64_t n, cudaStream_t st);
+
 // ---- paged: write the new token into the pool -----------------------------------
 struct PagedAppendArgs {
   void* k_pool;

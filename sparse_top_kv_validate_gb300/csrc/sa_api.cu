@@ -1129,6 +1129,109 @@ int csa_ratio4_attention(const sa_csa_params* p, void* stream) {
   return sa::launch_csa(a, as_stream(stream)) == 0 ? SA_OK : SA_ERR_LAUNCH;
 }
 
+// ---- CSA compression stages ------------------------------------------------------------
+
+static int check_compress(const sa_compress_params* p, int ratio, int kind) {
+  if (!p || !p->ape || !p->norm || !p->carry) return SA_ERR_NULL;
+  if (!p->records && !p->logical) return SA_ERR_NULL;
+  if (p->reserved_ != 0) return SA_ERR_UNSUPPORTED;
+  if (p->B <= 0 || p->S < 0 || p->D <= 0 || p->total < p->S || p->n_rope < 0 || p->rows < 0)
+    return SA_ERR_SHAPE;
+  if (p->S > 0 && (!p->kv || !p->gate)) return SA_ERR_NULL;
+  if (p->n_rope % 2 || p->n_rope > p->D || p->n_rope > 128) return SA_ERR_SHAPE;
+  if (kind == sa::kCompressAttn) {
+    if (p->D % 4 || p->D > 1024 || (p->D - p->n_rope) % 64) return SA_ERR_SHAPE;
+  } else if (!(p->D == 32 || p->D == 64 || p->D == 128 || p->D == 256)) {
+    return SA_ERR_SHAPE;
+  }
+  if (p->rows < p->total / ratio) return SA_ERR_SHAPE;
+  const int64_t width = kind == sa::kCompressAttn
+                            ? (p->D - p->n_rope) / 64 * 65 + 2 * p->n_rope
+                            : p->D / 32 * 17;
+  if (p->records && p->record_stride < width) return SA_ERR_SHAPE;
+  const int64_t W = ratio == 4 ? 2 * p->D : p->D;
+  const int64_t slots = ratio == 4 ? 8 : 128;
+  // index arithmetic stays in 64 bits; grids need the counts below 2^31
+  if (p->total / ratio - (p->total - p->S) / ratio >= (int64_t(1) << 31) ||
+      p->B >= (int64_t(1) << 31) || p->total >= (int64_t(1) << 53))
+    return SA_ERR_UNSUPPORTED;
+  if (!aligned16(p->kv) || !aligned16(p->gate) || !aligned16(p->ape) || !aligned16(p->carry) ||
+      reinterpret_cast<uintptr_t>(p->norm) % 4 || reinterpret_cast<uintptr_t>(p->logical) % 4 ||
+      reinterpret_cast<uintptr_t>(p->err_word) % 4)
+    return SA_ERR_ALIGN;
+  const size_t carry_b = static_cast<size_t>(p->B * slots * 2 * W) * 4;
+  const size_t src_b = static_cast<size_t>(p->B * p->S * W) * 4;
+  const size_t rec_b = p->records ? static_cast<size_t>(p->B * p->rows * p->record_stride) : 0;
+  const size_t log_b = p->logical ? static_cast<size_t>(p->B * p->rows * p->D) * 4 : 0;
+  if (overlaps(p->carry, carry_b, p->kv, src_b) || overlaps(p->carry, carry_b, p->gate, src_b) ||
+      overlaps(p->records, rec_b, p->carry, carry_b) ||
+      overlaps(p->logical, log_b, p->carry, carry_b) ||
+      overlaps(p->records, rec_b, p->logical, log_b) ||
+      overlaps(p->records, rec_b, p->kv, src_b) || overlaps(p->logical, log_b, p->kv, src_b) ||
+      overlaps(p->records, rec_b, p->gate, src_b) || overlaps(p->logical, log_b, p->gate, src_b))
+    return SA_ERR_OVERLAP;
+  return SA_OK;
+}
+
+static int compress_entry(const sa_compress_params* p, void* stream, int ratio, int kind) {
+  const int rc = check_compress(p, ratio, kind);
+  if (rc != SA_OK) return rc;
+  sa::CompressArgs a;
+  memset(&a, 0, sizeof(a));
+  a.kv = p->kv;
+  a.gate = p->gate;
+  a.ape = p->ape;
+  a.norm = p->norm;
+  a.carry = p->carry;
+  a.records = p->records;
+  a.logical = p->logical;
+  a.err_word = p->err_word;
+  a.B = p->B;
+  a.S = p->S;
+  a.D = static_cast<int>(p->D);
+  a.W = ratio == 4 ? 2 * p->D : p->D;
+  a.rows = p->rows;
+  a.record_stride = p->record_stride;
+  a.total = p->total;
+  a.start = p->total - p->S;
+  a.ratio = ratio;
+  a.kind = kind;
+  a.n_rope = static_cast<int>(p->n_rope);
+  a.width = static_cast<int>(kind == sa::kCompressAttn
+                                 ? (p->D - p->n_rope) / 64 * 65 + 2 * p->n_rope
+                                 : p->D / 32 * 17);
+  a.k0 = a.start / ratio;
+  a.nk = p->total / ratio - a.k0;
+  for (int64_t i = 0; i < p->n_rope / 2; ++i) {
+    // the base frequency of pair i: a binary32 exponent, the power rounded once
+    const float ex = -static_cast<float>(2 * i) / static_cast<float>(p->n_rope);
+    a.rope_base[i] = static_cast<float>(std::pow(160000.0, static_cast<double>(ex)));
+  }
+  a.ev_before = t_ev_before;
+  a.ev_after = t_ev_after;
+  return sa::launch_compress(a, as_stream(stream)) == 0 ? SA_OK : SA_ERR_LAUNCH;
+}
+
+int csa_ratio128_compress(const sa_compress_params* p, void* stream) {
+  return compress_entry(p, stream, 128, sa::kCompressAttn);
+}
+
+int csa_ratio4_main_compress(const sa_compress_params* p, void* stream) {
+  return compress_entry(p, stream, 4, sa::kCompressAttn);
+}
+
+int csa_ratio4_index_compress(const sa_compress_params* p, void* stream) {
+  return compress_entry(p, stream, 4, sa::kCompressIndex);
+}
+
+int csa_pool_weight(const float* t, float* w, int64_t n, void* stream) {
+  if (n < 0) return SA_ERR_SHAPE;
+  if (n > 0 && (!t || !w)) return SA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(t) % 4 || reinterpret_cast<uintptr_t>(w) % 4)
+    return SA_ERR_ALIGN;
+  return sa::launch_pool_weight(t, w, n, as_stream(stream)) == 0 ? SA_OK : SA_ERR_LAUNCH;
+}
+
 }  // extern "C"
 
 // ---- sparse decode without caller-provided scratch ------------------------------------

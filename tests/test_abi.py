@@ -78,7 +78,8 @@ def _c_layout(struct_name, fields):
                                       ("sa_prefill_params", sa.PrefillParams),
                                       ("sa_paged_params", sa.PagedParams),
                                       ("sa_index_select_params", sa.IndexSelectParams),
-                                      ("sa_csa_params", sa.CsaParams)])
+                                      ("sa_csa_params", sa.CsaParams),
+                                      ("sa_compress_params", sa.CompressParams)])
 def test_struct_layout_matches_header(cname, py):
     fields = [f for f, _ in py._fields_]
     size, offs = _c_layout(cname, fields)
@@ -309,3 +310,34 @@ def test_index_select_workspace_query_needs_no_output_pointer(lib):
     assert lib.sparse_index_select_workspace(C.byref(p)) > 0
     p.ID = 100
     assert lib.sparse_index_select_workspace(C.byref(p)) == 0
+
+
+def test_compress_host_checks(host_lib):
+    def params(**kw):
+        p = sa.CompressParams()
+        p.kv, p.gate, p.ape, p.norm = 0x100000, 0x200000, 0x300000, 0x400000
+        p.carry, p.records = 0x500000, 0x600000
+        p.B, p.S, p.D, p.n_rope, p.total = 2, 8, 512, 64, 8
+        p.rows, p.record_stride = 2, 583
+        for k, v in kw.items():
+            setattr(p, k, v)
+        return p
+
+    main, index, r128 = (host_lib.csa_ratio4_main_compress, host_lib.csa_ratio4_index_compress,
+                         host_lib.csa_ratio128_compress)
+    assert main(C.byref(sa.CompressParams()), None) == -1
+    assert main(C.byref(params(records=None)), None) == -1          # no output at all
+    assert main(C.byref(params(kv=None)), None) == -1               # S > 0 needs rows
+    assert main(C.byref(params(reserved_=1)), None) == -7
+    assert main(C.byref(params(total=7)), None) == -2               # total < S
+    assert main(C.byref(params(n_rope=63)), None) == -2             # odd RoPE width
+    assert main(C.byref(params(D=520, n_rope=64)), None) == -2      # 456 not a multiple of 64
+    assert main(C.byref(params(rows=1)), None) == -2                # 8 / 4 records need 2 rows
+    assert main(C.byref(params(record_stride=582)), None) == -2     # 583-byte records
+    assert index(C.byref(params(D=96, n_rope=64, record_stride=51)), None) == -2
+    assert index(C.byref(params(D=128, n_rope=64, record_stride=67)), None) == -2  # 68 bytes
+    assert r128(C.byref(params(rows=0, total=200, S=200)), None) == -2  # one 128-block closes
+    assert main(C.byref(params(kv=0x100004)), None) == -4           # 16-byte alignment
+    assert main(C.byref(params(records=0x500000 + 64)), None) == -6  # records inside the carry
+    assert host_lib.csa_pool_weight(None, None, 4, None) == -1
+    assert host_lib.csa_pool_weight(None, None, -1, None) == -2
