@@ -87,57 +87,58 @@ constexpr float kL1 = 0x1.62e43p-9f;      // ln2/256 = kL1 + kL2 + O(2^-61)
 constexpr float kL2 = -0x1.05c61p-37f;
 constexpr float kSixth = 0x1.555556p-3f;
 constexpr float kMargin = 0x1p-37f;
-
-// Error-free sum: the rounding error of s = a + b.
-__device__ __forceinline__ float two_sum_err(float a, float b, float s) {
-  const float bb = __fsub_rn(s, a);
-  return __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
+constexpr float kShifter = 0x1.8p23f;     // x + 1.5 * 2^23 rounds x to an integer
 
 __device__ __noinline__ float exp_double(float t) {
   return static_cast<float>(exp(static_cast<double>(t)));
 }
 
-__device__ __forceinline__ float pool_weight(float t, const float* thi, const float* tlo) {
-  if (t == 0.0f) return 1.0f;
-  // NaN, positive t, and t < -87 (subnormal or zero results) take the double path
-  if (!(t >= -87.0f && t <= 0.0f)) return exp_double(t);
-  const float kf = rintf(__fmul_rn(t, kInvL));
-  const int k = __float2int_rn(kf);
+// The table evaluation, without branches (so that a caller's independent
+// evaluations interleave).  `ok` comes back false when the rounding is not
+// certified or t is outside [-87, 0] (NaN included); the caller then takes
+// exp_double(t) instead.
+__device__ __forceinline__ float exp_table(float t, const float* thi, const float* tlo,
+                                           bool& ok) {
+  ok = t >= -87.0f && t <= 0.0f;
+  const float tc = fminf(fmaxf(t, -87.0f), 0.0f);
+  const float kb = __fmaf_rn(tc, kInvL, kShifter);
+  const int k = __float_as_int(kb) - __float_as_int(kShifter);
+  const float kf = __fsub_rn(kb, kShifter);
+  // a = t - k L1 is exact (t and k L1 within a factor of two for k != 0)
   const float p1 = __fmul_rn(kf, kL1);
   const float e1 = __fmaf_rn(kf, kL1, -p1);
-  const float a_hi = __fsub_rn(t, p1);
-  const float a_lo = two_sum_err(t, -p1, a_hi);
-  const float bsum = __fmaf_rn(kf, kL2, e1);
-  const float r_hi = __fsub_rn(a_hi, bsum);
-  const float r_lo = __fadd_rn(two_sum_err(a_hi, -bsum, r_hi), a_lo);
-  const float q = __fmul_rn(__fmul_rn(r_hi, r_hi), __fmaf_rn(r_hi, kSixth, 0.5f));
-  const float u = __fadd_rn(r_lo, q);
+  const float a = __fsub_rn(tc, p1);
+  const float bsum = __fmaf_rn(kf, kL2, e1);  // r = a - bsum
+  const float r = __fsub_rn(a, bsum);
+  const float q = __fmul_rn(__fmul_rn(r, r), __fmaf_rn(r, kSixth, 0.5f));
+  const float u = __fsub_rn(q, bsum);           // e^r = 1 + a + u
   const int j = k & 255, m = k >> 8;
   const float th = thi[j], tl = tlo[j];
-  const float p_hi = __fmul_rn(th, r_hi);
-  const float p_lo = __fmaf_rn(th, r_hi, -p_hi);
-  const float w = __fadd_rn(__fmaf_rn(th, u, p_lo), __fmaf_rn(tl, r_hi, tl));
-  const float z_hi = __fadd_rn(p_hi, w);
-  const float z_lo = two_sum_err(p_hi, w, z_hi);
-  const float y = __fadd_rn(th, z_hi);
-  const float err = __fadd_rn(__fsub_rn(z_hi, __fsub_rn(y, th)), z_lo);
+  const float p_hi = __fmul_rn(th, a);
+  const float p_lo = __fmaf_rn(th, a, -p_hi);
+  const float w = __fadd_rn(__fmaf_rn(th, u, p_lo), __fmaf_rn(tl, a, tl));
+  // y + err = th + p_hi + w: two error-free (fast) sums
+  const float y1 = __fadd_rn(th, p_hi);
+  const float c = __fadd_rn(__fsub_rn(p_hi, __fsub_rn(y1, th)), w);
+  const float y = __fadd_rn(y1, c);
+  const float err = __fsub_rn(c, __fsub_rn(y, y1));
   // The exact value is y + err within kMargin.  h = half the spacing from y
   // towards err (y in [0.99, 2.01]; below a power of two the spacing halves).
   // |err| clear below h: y is the rounding; clear above h: the neighbour on
-  // err's side is (|err| <= h + ulp(z_hi) / 2, far from the next midpoint).
+  // err's side is (|err| <= h + ulp(c) / 2, far from the next midpoint).
   const uint32_t yb = __float_as_uint(y);
   float h = __uint_as_float((yb & 0x7f800000u) - (24u << 23));
   if ((yb & 0x007fffffu) == 0 && err < 0.0f) h = __fmul_rn(h, 0.5f);
-  const float ae = fabsf(err);
-  float r;
-  if (__fadd_rn(ae, kMargin) < h)
-    r = y;
-  else if (__fsub_rn(ae, kMargin) > h)
-    r = __uint_as_float(err > 0.0f ? yb + 1u : yb - 1u);
-  else
-    return exp_double(t);
-  return __fmul_rn(r, pow2f(m));  // exact: the result is a normal number
+  const float d = __fsub_rn(fabsf(err), h);
+  ok = ok && fabsf(d) > kMargin;
+  const uint32_t rb = d < 0.0f ? yb : (err > 0.0f ? yb + 1u : yb - 1u);
+  return __uint_as_float(rb + (static_cast<uint32_t>(m) << 23));  // 2^m: a normal result
+}
+
+__device__ __forceinline__ float pool_weight(float t, const float* thi, const float* tlo) {
+  bool ok;
+  const float w = exp_table(t, thi, tlo, ok);
+  return ok ? w : exp_double(t);
 }
 
 // ---- shared pieces -------------------------------------------------------------------------
@@ -311,67 +312,87 @@ __device__ void finalize_warp(const CompressArgs& a, float* rec, const float2* r
 
 // ---- ratio 4 -------------------------------------------------------------------------------
 
-// Source rows of candidate c of record k (ratio 4): c < 4 the previous
-// block's token 4k - 4 + c on source dims [0, D), c >= 4 the block's token
-// 4k + c - 4 on [D, 2D).  A token of this call is read from kv / gate (+ the
-// ape row of its phase); an earlier one from its carry slot (the open block's
-// tokens in slots 4 + phase, the closed block before it in slots 0..3).
-struct Cand {
-  const float* v;
-  const float* s;
-  const float* ape;  // nullptr: the score is stored (carry)
-};
-
-__device__ __forceinline__ Cand r4_candidate(const CompressArgs& a, int64_t b, int64_t k, int c) {
-  const int64_t P = c < 4 ? 4 * k - 4 + c : 4 * k + c - 4;
-  const int64_t half = c < 4 ? 0 : a.D;
-  Cand x{nullptr, nullptr, nullptr};
-  if (P < 0) return x;
-  if (P >= a.start) {
-    const int64_t off = (b * a.S + (P - a.start)) * a.W + half;
-    x.v = a.kv + off;
-    x.s = a.gate + off;
-    x.ape = a.ape + (P & 3) * a.W + half;
-  } else {
-    const int64_t open_from = a.start - (a.start & 3);
-    const int64_t slot = P >= open_from ? 4 + (P & 3) : (P & 3);
-    const float* base = a.carry + ((b * 8 + slot) * 2) * a.W + half;
-    x.v = base;
-    x.s = base + a.W;
-  }
-  return x;
-}
-
-__device__ __forceinline__ float4 ld4(const float* p) {
-  return __ldg(reinterpret_cast<const float4*>(p));
-}
-
-__device__ __forceinline__ float4 add4(float4 x, float4 y) {
-  return make_float4(__fadd_rn(x.x, y.x), __fadd_rn(x.y, y.y), __fadd_rn(x.z, y.z),
-                     __fadd_rn(x.w, y.w));
-}
-
-// One dimension's pool over 8 candidates, in candidate order.
-__device__ __forceinline__ float pool8(const float (&s)[8], const float (&v)[8], bool& ok,
-                                       const float* thi, const float* tlo) {
+// Softmax pool of one dimension over n candidates (scores s, values v), in
+// candidate order, -inf scores left out: the weights first (independent, so
+// they interleave), the rare uncertified ones redone in double, then the sums.
+template <int N>
+__device__ __forceinline__ float pool_dim(const float (&s)[N], const float (&v)[N], bool& ok,
+                                          const float* thi, const float* tlo) {
   float m = SA_NEG_INF;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) m = fmaxf(m, s[c]);
+  for (int c = 0; c < N; ++c) m = fmaxf(m, s[c]);
   ok = ok && isfinite(m);
+  float w[N];
+  bool cert = true;
+#pragma unroll
+  for (int c = 0; c < N; ++c) {
+    bool okc;
+    w[c] = exp_table(__fsub_rn(s[c], m), thi, tlo, okc);
+    cert = cert && (okc || s[c] == SA_NEG_INF);
+  }
+  if (!cert) {
+#pragma unroll
+    for (int c = 0; c < N; ++c) {
+      bool okc;
+      exp_table(__fsub_rn(s[c], m), thi, tlo, okc);
+      if (!okc && s[c] != SA_NEG_INF) w[c] = exp_double(__fsub_rn(s[c], m));
+    }
+  }
   float num = 0.0f, den = 0.0f;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    if (s[c] == SA_NEG_INF) continue;
-    const float w = pool_weight(__fsub_rn(s[c], m), thi, tlo);
-    num = __fadd_rn(num, __fmul_rn(w, v[c]));
-    den = __fadd_rn(den, w);
+  for (int c = 0; c < N; ++c) {
+    const bool use = s[c] != SA_NEG_INF;
+    const float n2 = __fadd_rn(num, __fmul_rn(w[c], v[c]));
+    const float d2 = __fadd_rn(den, w[c]);
+    num = use ? n2 : num;
+    den = use ? d2 : den;
   }
   ok = ok && den != 0.0f && isfinite(den) && isfinite(num);
   return round_bf16(__fdiv_rn(num, den));
 }
 
+// Source rows of record k's candidates (ratio 4): c < 4 the previous
+// block's token 4k - 4 + c on source dims [0, D), c >= 4 the block's token
+// 4k + c - 4 on [D, 2D).  A token of this call is read from kv / gate (+ the
+// ape row of its phase); an earlier one from its carry slot (the open block's
+// tokens in slots 4 + phase, the closed block before it in slots 0..3); a
+// token before position 0 is no candidate.
+struct R4Sources {
+  const float* v[8];
+  const float* s[8];
+  uint32_t from_rows;  // bit c: candidate c is a token of this call (add its ape row)
+  uint32_t present;    // bit c: candidate c exists
+};
+
+__device__ __forceinline__ void r4_sources(const CompressArgs& a, int64_t b, int64_t k,
+                                           R4Sources& x) {
+  x.from_rows = 0;
+  x.present = 0;
+  const int64_t open_from = a.start - (a.start & 3);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int64_t P = c < 4 ? 4 * k - 4 + c : 4 * k + c - 4;
+    const int64_t half = c < 4 ? 0 : a.D;
+    x.v[c] = a.kv;  // any valid address for an absent candidate
+    x.s[c] = a.kv;
+    if (P < 0) continue;
+    x.present |= 1u << c;
+    if (P >= a.start) {
+      const int64_t off = (b * a.S + (P - a.start)) * a.W + half;
+      x.v[c] = a.kv + off;
+      x.s[c] = a.gate + off;
+      x.from_rows |= 1u << c;
+    } else {
+      const int64_t slot = P >= open_from ? 4 + (P & 3) : (P & 3);
+      const float* base = a.carry + ((b * 8 + slot) * 2) * a.W + half;
+      x.v[c] = base;
+      x.s[c] = base + a.W;
+    }
+  }
+}
+
 template <int KIND>
-__global__ void __launch_bounds__(kR4Warps * 32) compress_r4_kernel(const CompressArgs a) {
+__global__ void __launch_bounds__(kR4Warps * 32, 3) compress_r4_kernel(const CompressArgs a) {
   extern __shared__ __align__(16) float smem[];
   float* thi = smem;
   float* tlo = smem + 256;
@@ -379,36 +400,39 @@ __global__ void __launch_bounds__(kR4Warps * 32) compress_r4_kernel(const Compre
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t k = a.k0 + blockIdx.x;
   load_exp_table(thi, tlo);
-  if (warp == 0) rope_rotation(a, 4 * k, rot, lane);
   __syncthreads();
   const int64_t b = static_cast<int64_t>(blockIdx.y) * kR4Warps + warp;
-  if (b >= a.B) return;
+  const bool active = b < a.B;
   float* rec = smem + kTableFloats + warp * a.D;
   bool ok = true;
-  for (int d0 = 4 * lane; d0 < a.D; d0 += 128) {
-    float s[4][8], v[4][8];
+  if (active) {
+    R4Sources x;
+    r4_sources(a, b, k, x);
+    // ape rows of the candidates' phases: c < 4 phase c on [0, D), c >= 4 phase c - 4 on [D, 2D)
+    for (int d0 = 0; d0 < a.D; d0 += 32) {
+      const int d = d0 + lane < a.D ? d0 + lane : a.D - 1;  // every lane takes part
+      float s[8], v[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const Cand x = r4_candidate(a, b, k, c);
-      float4 sv = make_float4(SA_NEG_INF, SA_NEG_INF, SA_NEG_INF, SA_NEG_INF);
-      float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (x.v) {
-        vv = ld4(x.v + d0);
-        sv = ld4(x.s + d0);
-        if (x.ape) sv = add4(sv, ld4(x.ape + d0));
+      for (int c = 0; c < 8; ++c) {
+        const int64_t ape_off = c < 4 ? c * a.W + d : (c - 4) * a.W + a.D + d;
+        const float sv = __ldg(x.s[c] + d);
+        const float av = __ldg(a.ape + ape_off);
+        v[c] = __ldg(x.v[c] + d);
+        s[c] = (x.from_rows >> c) & 1u ? __fadd_rn(sv, av) : sv;
+        if (!((x.present >> c) & 1u)) {
+          s[c] = SA_NEG_INF;
+          v[c] = 0.0f;
+        }
       }
-      s[0][c] = sv.x, s[1][c] = sv.y, s[2][c] = sv.z, s[3][c] = sv.w;
-      v[0][c] = vv.x, v[1][c] = vv.y, v[2][c] = vv.z, v[3][c] = vv.w;
+      const float out = pool_dim<8>(s, v, ok, thi, tlo);
+      if (d0 + lane < a.D) rec[d0 + lane] = out;
     }
-    float4 out;
-    out.x = pool8(s[0], v[0], ok, thi, tlo);
-    out.y = pool8(s[1], v[1], ok, thi, tlo);
-    out.z = pool8(s[2], v[2], ok, thi, tlo);
-    out.w = pool8(s[3], v[3], ok, thi, tlo);
-    *reinterpret_cast<float4*>(rec + d0) = out;
   }
+  // the RoPE rotation of this record index, once per CTA, off the pooling path
+  if (warp == 0) rope_rotation(a, 4 * k, rot, lane);
+  __syncthreads();
+  if (!active) return;
   ok = __all_sync(0xffffffffu, ok);
-  __syncwarp();
   finalize_warp<KIND>(a, rec, rot, b, k, ok, lane);
 }
 
@@ -424,43 +448,60 @@ __global__ void __launch_bounds__(1024) compress_r128_kernel(const CompressArgs 
   const int64_t k = a.k0 + blockIdx.x;
   const int64_t b = blockIdx.y;
   load_exp_table(thi, tlo);
-  if (warp == 0) rope_rotation(a, 128 * k, rot, lane);
   __syncthreads();
-  // candidates: the block's tokens 128k + j; those of this call from kv /
-  // gate + ape[j], the earlier ones from carry slot j
-  const int64_t first_new = a.start - 128 * k;  // j >= first_new: this call's rows
+  // candidates: the block's tokens 128k + j; those of this call (j >=
+  // first_new) from kv / gate + ape[j], the earlier ones from carry slot j
+  const int64_t first_new = a.start - 128 * k;
   const int64_t W = a.W;
   const float* cy = a.carry + b * 128 * 2 * W;
-  const float* src_v = a.kv + (b * a.S - a.start + 128 * k) * W;
-  const float* src_g = a.gate + (b * a.S - a.start + 128 * k) * W;
+  const int64_t row0 = b * a.S - a.start + 128 * k;  // row of token 128k (may be < b S)
   bool ok = true;
   for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+    auto score = [&](int j) {
+      return j >= first_new ? __fadd_rn(__ldg(a.gate + (row0 + j) * W + d),
+                                        __ldg(a.ape + j * W + d))
+                            : cy[(2 * j + 1) * W + d];
+    };
+    auto value = [&](int j) {
+      return j >= first_new ? __ldg(a.kv + (row0 + j) * W + d) : cy[(2 * j) * W + d];
+    };
     float m = SA_NEG_INF;
-    for (int j = 0; j < 128; ++j) {
-      const float s = j >= first_new
-                          ? __fadd_rn(__ldg(src_g + j * W + d), __ldg(a.ape + j * W + d))
-                          : cy[(2 * j + 1) * W + d];
-      m = fmaxf(m, s);
-    }
+#pragma unroll 8
+    for (int j = 0; j < 128; ++j) m = fmaxf(m, score(j));
     ok = ok && isfinite(m);
     float num = 0.0f, den = 0.0f;
-    for (int j = 0; j < 128; ++j) {
-      float s, v;
-      if (j >= first_new) {
-        s = __fadd_rn(__ldg(src_g + j * W + d), __ldg(a.ape + j * W + d));
-        v = __ldg(src_v + j * W + d);
-      } else {
-        s = cy[(2 * j + 1) * W + d];
-        v = cy[(2 * j) * W + d];
+    for (int j0 = 0; j0 < 128; j0 += 8) {
+      float sc[8], v[8], w[8];
+      bool cert = true;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        sc[c] = score(j0 + c);
+        v[c] = value(j0 + c);
+        bool okc;
+        w[c] = exp_table(__fsub_rn(sc[c], m), thi, tlo, okc);
+        cert = cert && (okc || sc[c] == SA_NEG_INF);
       }
-      if (s == SA_NEG_INF) continue;
-      const float w = pool_weight(__fsub_rn(s, m), thi, tlo);
-      num = __fadd_rn(num, __fmul_rn(w, v));
-      den = __fadd_rn(den, w);
+      if (!cert) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          bool okc;
+          exp_table(__fsub_rn(sc[c], m), thi, tlo, okc);
+          if (!okc && sc[c] != SA_NEG_INF) w[c] = exp_double(__fsub_rn(sc[c], m));
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const bool use = sc[c] != SA_NEG_INF;
+        const float n2 = __fadd_rn(num, __fmul_rn(w[c], v[c]));
+        const float d2 = __fadd_rn(den, w[c]);
+        num = use ? n2 : num;
+        den = use ? d2 : den;
+      }
     }
     ok = ok && den != 0.0f && isfinite(den) && isfinite(num);
     rec[d] = round_bf16(__fdiv_rn(num, den));
   }
+  if (warp == 0) rope_rotation(a, 128 * k, rot, lane);
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
   if (warp == 0) finalize_warp<kCompressAttn>(a, rec, rot, b, k, ok, lane);
 }
