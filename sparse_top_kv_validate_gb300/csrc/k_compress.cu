@@ -391,41 +391,84 @@ __device__ __forceinline__ void r4_sources(const CompressArgs& a, int64_t b, int
   }
 }
 
+// One warp's pipeline stage: 8 candidates x (value, score) x 32 dimensions.
+constexpr int kStageFloats = 8 * 2 * 32;
+
+__device__ __forceinline__ void cp_async16(float* dst, const float* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+               "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+// Stage dims [32 it, 32 it + 32) of the 8 candidates: 128 16-byte chunks, 4
+// per lane; chunk q holds candidate q / 16, array (q / 8) % 2 (0 value, 1
+// score), dims 4 (q % 8) .. + 3.  Absent candidates and dims past D are
+// zero-filled (no global read).
+__device__ __forceinline__ void r4_stage(const CompressArgs& a, const R4Sources& x, int it,
+                                         float* stage, int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = lane + 32 * i;
+    const int c_lo = 2 * i, c_hi = 2 * i + 1;       // q / 16 is one of these two
+    const bool upper = lane >= 16;
+    const int c = upper ? c_hi : c_lo;
+    const bool score = (q >> 3) & 1;
+    const int part = q & 7;
+    const float* base = upper ? (score ? x.s[c_hi] : x.v[c_hi]) : (score ? x.s[c_lo] : x.v[c_lo]);
+    const int d = 32 * it + 4 * part;
+    const bool valid = ((x.present >> c) & 1u) && d < a.D;
+    cp_async16(stage + (c * 2 + (score ? 1 : 0)) * 32 + 4 * part, valid ? base + d : a.ape, valid);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(kR4Warps * 32, 3) compress_r4_kernel(const CompressArgs a) {
   extern __shared__ __align__(16) float smem[];
   float* thi = smem;
   float* tlo = smem + 256;
   float2* rot = reinterpret_cast<float2*>(smem + 512);
+  float* ape_s = smem + kTableFloats;          // [4, W]
+  float* recs = ape_s + 4 * a.W;               // [warps, D]
+  float* stages = recs + kR4Warps * a.D;       // [warps, 2, kStageFloats]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t k = a.k0 + blockIdx.x;
   load_exp_table(thi, tlo);
+  for (int i = threadIdx.x; i < a.W; i += blockDim.x)  // 4 rows of W floats, as float4
+    reinterpret_cast<float4*>(ape_s)[i] = __ldg(reinterpret_cast<const float4*>(a.ape) + i);
   __syncthreads();
   const int64_t b = static_cast<int64_t>(blockIdx.y) * kR4Warps + warp;
   const bool active = b < a.B;
-  float* rec = smem + kTableFloats + warp * a.D;
+  float* rec = recs + warp * a.D;
   bool ok = true;
   if (active) {
     R4Sources x;
     r4_sources(a, b, k, x);
-    // ape rows of the candidates' phases: c < 4 phase c on [0, D), c >= 4 phase c - 4 on [D, 2D)
-    for (int d0 = 0; d0 < a.D; d0 += 32) {
-      const int d = d0 + lane < a.D ? d0 + lane : a.D - 1;  // every lane takes part
+    float* stg = stages + warp * 2 * kStageFloats;
+    const int niter = (a.D + 31) / 32;
+    r4_stage(a, x, 0, stg, lane);
+    for (int it = 0; it < niter; ++it) {
+      if (it + 1 < niter)
+        r4_stage(a, x, it + 1, stg + ((it + 1) & 1) * kStageFloats, lane);
+      else
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      __syncwarp();
+      const float* cur = stg + (it & 1) * kStageFloats;
+      const int d = 32 * it + lane < a.D ? 32 * it + lane : a.D - 1;
       float s[8], v[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const int64_t ape_off = c < 4 ? c * a.W + d : (c - 4) * a.W + a.D + d;
-        const float sv = __ldg(x.s[c] + d);
-        const float av = __ldg(a.ape + ape_off);
-        v[c] = __ldg(x.v[c] + d);
+        // ape row of the candidate's phase: c < 4 phase c on [0, D), else phase c - 4 on [D, 2D)
+        const float av = ape_s[(c & 3) * a.W + (c < 4 ? 0 : a.D) + d];
+        const float sv = cur[(c * 2 + 1) * 32 + lane];
+        v[c] = cur[(c * 2) * 32 + lane];
         s[c] = (x.from_rows >> c) & 1u ? __fadd_rn(sv, av) : sv;
-        if (!((x.present >> c) & 1u)) {
-          s[c] = SA_NEG_INF;
-          v[c] = 0.0f;
-        }
+        if (!((x.present >> c) & 1u)) s[c] = SA_NEG_INF;
       }
       const float out = pool_dim<8>(s, v, ok, thi, tlo);
-      if (d0 + lane < a.D) rec[d0 + lane] = out;
+      if (32 * it + lane < a.D) rec[32 * it + lane] = out;
+      __syncwarp();  // every lane has read this stage before it is refilled
     }
   }
   // the RoPE rotation of this record index, once per CTA, off the pooling path
@@ -588,8 +631,10 @@ __global__ void pool_weight_kernel(const float* t, float* w, int64_t n) {
 // ---- host side ------------------------------------------------------------------------------
 
 size_t compress_smem_bytes(int ratio, int64_t D) {
-  const int64_t recs = ratio == 4 ? kR4Warps * D : D;
-  return static_cast<size_t>(kTableFloats + recs) * sizeof(float);
+  if (ratio == 4)  // tables, ape rows (4 x 2D), pooled records, pipeline stages
+    return static_cast<size_t>(kTableFloats + 8 * D + kR4Warps * D +
+                               kR4Warps * 2 * kStageFloats) * sizeof(float);
+  return static_cast<size_t>(kTableFloats + D) * sizeof(float);
 }
 
 template <typename K>
