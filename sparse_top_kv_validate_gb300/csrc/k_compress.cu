@@ -57,8 +57,7 @@ namespace {
 // falling back to the double evaluation.
 
 struct ExpTable {
-  float hi[256];
-  float lo[256];
+  float2 e[256];  // (hi, lo)
 };
 
 __host__ __device__ constexpr double exp_series(double x) {
@@ -74,8 +73,8 @@ __host__ __device__ constexpr ExpTable make_exp_table() {
   ExpTable t{};
   for (int j = 0; j < 256; ++j) {
     const double v = exp_series(j * (0.69314718055994530942 / 256.0));
-    t.hi[j] = static_cast<float>(v);
-    t.lo[j] = static_cast<float>(v - static_cast<double>(t.hi[j]));
+    t.e[j].x = static_cast<float>(v);
+    t.e[j].y = static_cast<float>(v - static_cast<double>(t.e[j].x));
   }
   return t;
 }
@@ -94,63 +93,51 @@ __device__ __noinline__ float exp_double(float t) {
 }
 
 // The table evaluation, without branches (so that a caller's independent
-// evaluations interleave).  `ok` comes back false when the rounding is not
-// certified or t is outside [-87, 0] (NaN included); the caller then takes
-// exp_double(t) instead.
-__device__ __forceinline__ float exp_table(float t, const float* thi, const float* tlo,
-                                           bool& ok) {
-  ok = t >= -87.0f && t <= 0.0f;
-  const float tc = fminf(fmaxf(t, -87.0f), 0.0f);
-  const float kb = __fmaf_rn(tc, kInvL, kShifter);
-  const int k = __float_as_int(kb) - __float_as_int(kShifter);
+// evaluations interleave).  The float-float value y1 + c is within 2^-37 of
+// e^t / 2^m; rounding it with c raised and lowered by 2^-37 gives the same
+// binary32 number exactly when that number is the correct rounding of e^t /
+// 2^m (rounding is monotone), and then `ok` is true.  `ok` is false for t
+// outside [-87, 0] (NaN and -inf included); the caller then takes
+// exp_double(t).
+__device__ __forceinline__ float exp_table(float t, const float2* tab, bool& ok) {
+  const float kb = __fmaf_rn(t, kInvL, kShifter);
+  const uint32_t kbits = __float_as_uint(kb);  // 0x4b400000 + k, k = round(t 256 / ln 2)
   const float kf = __fsub_rn(kb, kShifter);
   // a = t - k L1 is exact (t and k L1 within a factor of two for k != 0)
   const float p1 = __fmul_rn(kf, kL1);
   const float e1 = __fmaf_rn(kf, kL1, -p1);
-  const float a = __fsub_rn(tc, p1);
+  const float a = __fsub_rn(t, p1);
   const float bsum = __fmaf_rn(kf, kL2, e1);  // r = a - bsum
   const float r = __fsub_rn(a, bsum);
   const float q = __fmul_rn(__fmul_rn(r, r), __fmaf_rn(r, kSixth, 0.5f));
   const float u = __fsub_rn(q, bsum);           // e^r = 1 + a + u
-  const int j = k & 255, m = k >> 8;
-  const float th = thi[j], tl = tlo[j];
-  const float p_hi = __fmul_rn(th, a);
-  const float p_lo = __fmaf_rn(th, a, -p_hi);
-  const float w = __fadd_rn(__fmaf_rn(th, u, p_lo), __fmaf_rn(tl, a, tl));
-  // y + err = th + p_hi + w: two error-free (fast) sums
-  const float y1 = __fadd_rn(th, p_hi);
-  const float c = __fadd_rn(__fsub_rn(p_hi, __fsub_rn(y1, th)), w);
-  const float y = __fadd_rn(y1, c);
-  const float err = __fsub_rn(c, __fsub_rn(y, y1));
-  // The exact value is y + err within kMargin.  h = half the spacing from y
-  // towards err (y in [0.99, 2.01]; below a power of two the spacing halves).
-  // |err| clear below h: y is the rounding; clear above h: the neighbour on
-  // err's side is (|err| <= h + ulp(c) / 2, far from the next midpoint).
-  const uint32_t yb = __float_as_uint(y);
-  float h = __uint_as_float((yb & 0x7f800000u) - (24u << 23));
-  if ((yb & 0x007fffffu) == 0 && err < 0.0f) h = __fmul_rn(h, 0.5f);
-  const float d = __fsub_rn(fabsf(err), h);
-  ok = ok && fabsf(d) > kMargin;
-  const uint32_t rb = d < 0.0f ? yb : (err > 0.0f ? yb + 1u : yb - 1u);
-  return __uint_as_float(rb + (static_cast<uint32_t>(m) << 23));  // 2^m: a normal result
+  const float2 T = tab[kbits & 255u];          // 2^(j/256), j = k mod 256
+  const float p_hi = __fmul_rn(T.x, a);
+  const float p_lo = __fmaf_rn(T.x, a, -p_hi);
+  const float w = __fadd_rn(__fmaf_rn(T.x, u, p_lo), __fmaf_rn(T.y, a, T.y));
+  const float y1 = __fadd_rn(T.x, p_hi);
+  const float c = __fadd_rn(__fsub_rn(p_hi, __fsub_rn(y1, T.x)), w);  // exact low part + w
+  const float ya = __fadd_rn(y1, __fadd_rn(c, kMargin));
+  const float yb = __fadd_rn(y1, __fsub_rn(c, kMargin));
+  ok = t >= -87.0f && ya == yb;
+  // times 2^m, m = floor(k / 256), on the exponent field (the result is normal)
+  const uint32_t m23 = (kbits & ~255u) << 15;  // (k + 0x4b400000) / 256 * 2^23
+  return __uint_as_float(__float_as_uint(ya) + m23 - (__float_as_uint(kShifter) << 15));
 }
 
-__device__ __forceinline__ float pool_weight(float t, const float* thi, const float* tlo) {
+__device__ __forceinline__ float pool_weight(float t, const float2* tab) {
   bool ok;
-  const float w = exp_table(t, thi, tlo, ok);
+  const float w = exp_table(t, tab, ok);
   return ok ? w : exp_double(t);
 }
 
 // ---- shared pieces -------------------------------------------------------------------------
 
 constexpr int kR4Warps = 8;
-constexpr int kTableFloats = 512 + 128;  // exp table + up to 64 (cos, sin) pairs
+constexpr int kTableFloats = 512 + 128 + 16;  // exp table, 64 (cos, sin) pairs, scales
 
-__device__ __forceinline__ void load_exp_table(float* thi, float* tlo) {
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-    thi[i] = g_exp_table.hi[i];
-    tlo[i] = g_exp_table.lo[i];
-  }
+__device__ __forceinline__ void load_exp_table(float2* tab) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) tab[i] = g_exp_table.e[i];
 }
 
 // The compressed RoPE rotation at block_start, one (cos, sin) per pair:
@@ -193,29 +180,30 @@ __device__ __forceinline__ float e4m3_value(uint8_t c) {
   return __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));
 }
 
+// RMSNorm's scale of one pooled record rec[D]: the binary32 square sum in
+// dimension order (a serial chain, one thread), then 1 / sqrt(sum / D +
+// 1e-6).  Returns a negative value when the sum is not finite.
+__device__ __forceinline__ float rms_inverse(const float* rec, int D) {
+  float sum = 0.0f;
+  for (int d = 0; d < D; d += 4) {
+    const float4 x = *reinterpret_cast<const float4*>(rec + d);
+    sum = __fadd_rn(sum, __fmul_rn(x.x, x.x));
+    sum = __fadd_rn(sum, __fmul_rn(x.y, x.y));
+    sum = __fadd_rn(sum, __fmul_rn(x.z, x.z));
+    sum = __fadd_rn(sum, __fmul_rn(x.w, x.w));
+  }
+  if (!isfinite(sum)) return -1.0f;
+  return __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(sum, static_cast<float>(D)), 1.0e-6f)));
+}
+
 // Finalize one record held (pooled, bf16-rounded) in shared memory rec[D],
-// by one warp: RMSNorm, RoPE, (index: Hadamard), validity, quantize, store.
+// by one warp, given its RMSNorm scale: normalisation, RoPE, (index:
+// Hadamard), validity, quantize, store.
 template <int KIND>
 __device__ void finalize_warp(const CompressArgs& a, float* rec, const float2* rot, int64_t b,
-                              int64_t k, bool ok, int lane) {
+                              int64_t k, bool ok, float inv, int lane) {
   const int D = a.D;
-  // RMSNorm: the binary32 square sum in dimension order, in one lane
-  float inv = 0.0f;
-  int sum_ok = 0;
-  if (lane == 0) {
-    float sum = 0.0f;
-    for (int d = 0; d < D; d += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(rec + d);
-      sum = __fadd_rn(sum, __fmul_rn(x.x, x.x));
-      sum = __fadd_rn(sum, __fmul_rn(x.y, x.y));
-      sum = __fadd_rn(sum, __fmul_rn(x.z, x.z));
-      sum = __fadd_rn(sum, __fmul_rn(x.w, x.w));
-    }
-    sum_ok = isfinite(sum) ? 1 : 0;
-    inv = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(sum, static_cast<float>(D)), 1.0e-6f)));
-  }
-  inv = __shfl_sync(0xffffffffu, inv, 0);
-  ok = ok && __shfl_sync(0xffffffffu, sum_ok, 0);
+  ok = ok && inv >= 0.0f;
   for (int d = lane; d < D; d += 32)
     rec[d] = round_bf16(__fmul_rn(__fmul_rn(rec[d], inv), __ldg(a.norm + d)));
   __syncwarp();
@@ -312,12 +300,14 @@ __device__ void finalize_warp(const CompressArgs& a, float* rec, const float2* r
 
 // ---- ratio 4 -------------------------------------------------------------------------------
 
-// Softmax pool of one dimension over n candidates (scores s, values v), in
+// Softmax pool of one dimension over N candidates (scores s, values v), in
 // candidate order, -inf scores left out: the weights first (independent, so
-// they interleave), the rare uncertified ones redone in double, then the sums.
+// they interleave), the rare uncertified ones redone in double (e^-inf = 0
+// there), then the sums.  A left-out candidate adds a weight of 0 to the
+// denominator, which leaves it unchanged (it is never -0).
 template <int N>
 __device__ __forceinline__ float pool_dim(const float (&s)[N], const float (&v)[N], bool& ok,
-                                          const float* thi, const float* tlo) {
+                                          const float2* tab) {
   float m = SA_NEG_INF;
 #pragma unroll
   for (int c = 0; c < N; ++c) m = fmaxf(m, s[c]);
@@ -327,25 +317,23 @@ __device__ __forceinline__ float pool_dim(const float (&s)[N], const float (&v)[
 #pragma unroll
   for (int c = 0; c < N; ++c) {
     bool okc;
-    w[c] = exp_table(__fsub_rn(s[c], m), thi, tlo, okc);
-    cert = cert && (okc || s[c] == SA_NEG_INF);
+    w[c] = exp_table(__fsub_rn(s[c], m), tab, okc);
+    cert = cert && okc;
   }
   if (!cert) {
 #pragma unroll
     for (int c = 0; c < N; ++c) {
       bool okc;
-      exp_table(__fsub_rn(s[c], m), thi, tlo, okc);
-      if (!okc && s[c] != SA_NEG_INF) w[c] = exp_double(__fsub_rn(s[c], m));
+      exp_table(__fsub_rn(s[c], m), tab, okc);
+      if (!okc) w[c] = exp_double(__fsub_rn(s[c], m));
     }
   }
   float num = 0.0f, den = 0.0f;
 #pragma unroll
   for (int c = 0; c < N; ++c) {
-    const bool use = s[c] != SA_NEG_INF;
     const float n2 = __fadd_rn(num, __fmul_rn(w[c], v[c]));
-    const float d2 = __fadd_rn(den, w[c]);
-    num = use ? n2 : num;
-    den = use ? d2 : den;
+    num = s[c] != SA_NEG_INF ? n2 : num;
+    den = __fadd_rn(den, w[c]);
   }
   ok = ok && den != 0.0f && isfinite(den) && isfinite(num);
   return round_bf16(__fdiv_rn(num, den));
@@ -425,21 +413,22 @@ __device__ __forceinline__ void r4_stage(const CompressArgs& a, const R4Sources&
 template <int KIND>
 __global__ void __launch_bounds__(kR4Warps * 32, 3) compress_r4_kernel(const CompressArgs a) {
   extern __shared__ __align__(16) float smem[];
-  float* thi = smem;
-  float* tlo = smem + 256;
+  float2* tab = reinterpret_cast<float2*>(smem);
   float2* rot = reinterpret_cast<float2*>(smem + 512);
+  float* invs = smem + 640;                    // [warps] RMSNorm scales
   float* ape_s = smem + kTableFloats;          // [4, W]
-  float* recs = ape_s + 4 * a.W;               // [warps, D]
-  float* stages = recs + kR4Warps * a.D;       // [warps, 2, kStageFloats]
+  const int rs = a.D + 4;                      // record stride: the RMS lanes hit distinct banks
+  float* recs = ape_s + 4 * a.W;               // [warps, D + 4]
+  float* stages = recs + kR4Warps * rs;        // [warps, 2, kStageFloats]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t k = a.k0 + blockIdx.x;
-  load_exp_table(thi, tlo);
+  load_exp_table(tab);
   for (int i = threadIdx.x; i < a.W; i += blockDim.x)  // 4 rows of W floats, as float4
     reinterpret_cast<float4*>(ape_s)[i] = __ldg(reinterpret_cast<const float4*>(a.ape) + i);
   __syncthreads();
   const int64_t b = static_cast<int64_t>(blockIdx.y) * kR4Warps + warp;
   const bool active = b < a.B;
-  float* rec = recs + warp * a.D;
+  float* rec = recs + warp * rs;
   bool ok = true;
   if (active) {
     R4Sources x;
@@ -466,31 +455,36 @@ __global__ void __launch_bounds__(kR4Warps * 32, 3) compress_r4_kernel(const Com
         s[c] = (x.from_rows >> c) & 1u ? __fadd_rn(sv, av) : sv;
         if (!((x.present >> c) & 1u)) s[c] = SA_NEG_INF;
       }
-      const float out = pool_dim<8>(s, v, ok, thi, tlo);
+      const float out = pool_dim<8>(s, v, ok, tab);
       if (32 * it + lane < a.D) rec[32 * it + lane] = out;
       __syncwarp();  // every lane has read this stage before it is refilled
     }
   }
-  // the RoPE rotation of this record index, once per CTA, off the pooling path
+  __syncthreads();
+  // off the pooling path, once per CTA: warp 0 the RoPE rotation of this
+  // record index, warp 1 the RMSNorm square sums (serial chains, one lane per
+  // record, in parallel)
   if (warp == 0) rope_rotation(a, 4 * k, rot, lane);
+  if (warp == 1 && lane < kR4Warps && static_cast<int64_t>(blockIdx.y) * kR4Warps + lane < a.B)
+    invs[lane] = rms_inverse(recs + lane * rs, a.D);
   __syncthreads();
   if (!active) return;
   ok = __all_sync(0xffffffffu, ok);
-  finalize_warp<KIND>(a, rec, rot, b, k, ok, lane);
+  finalize_warp<KIND>(a, rec, rot, b, k, ok, invs[warp], lane);
 }
 
 // ---- ratio 128 -----------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(1024) compress_r128_kernel(const CompressArgs a) {
   extern __shared__ __align__(16) float smem[];
-  float* thi = smem;
-  float* tlo = smem + 256;
+  float2* tab = reinterpret_cast<float2*>(smem);
   float2* rot = reinterpret_cast<float2*>(smem + 512);
+  float* inv = smem + 640;
   float* rec = smem + kTableFloats;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t k = a.k0 + blockIdx.x;
   const int64_t b = blockIdx.y;
-  load_exp_table(thi, tlo);
+  load_exp_table(tab);
   __syncthreads();
   // candidates: the block's tokens 128k + j; those of this call (j >=
   // first_new) from kv / gate + ape[j], the earlier ones from carry slot j
@@ -521,24 +515,22 @@ __global__ void __launch_bounds__(1024) compress_r128_kernel(const CompressArgs 
         sc[c] = score(j0 + c);
         v[c] = value(j0 + c);
         bool okc;
-        w[c] = exp_table(__fsub_rn(sc[c], m), thi, tlo, okc);
-        cert = cert && (okc || sc[c] == SA_NEG_INF);
+        w[c] = exp_table(__fsub_rn(sc[c], m), tab, okc);
+        cert = cert && okc;
       }
       if (!cert) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           bool okc;
-          exp_table(__fsub_rn(sc[c], m), thi, tlo, okc);
-          if (!okc && sc[c] != SA_NEG_INF) w[c] = exp_double(__fsub_rn(sc[c], m));
+          exp_table(__fsub_rn(sc[c], m), tab, okc);
+          if (!okc) w[c] = exp_double(__fsub_rn(sc[c], m));
         }
       }
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const bool use = sc[c] != SA_NEG_INF;
+      for (int c = 0; c < 8; ++c) {  // a -inf score adds w = 0 to den: no change
         const float n2 = __fadd_rn(num, __fmul_rn(w[c], v[c]));
-        const float d2 = __fadd_rn(den, w[c]);
-        num = use ? n2 : num;
-        den = use ? d2 : den;
+        num = sc[c] != SA_NEG_INF ? n2 : num;
+        den = __fadd_rn(den, w[c]);
       }
     }
     ok = ok && den != 0.0f && isfinite(den) && isfinite(num);
@@ -546,7 +538,10 @@ __global__ void __launch_bounds__(1024) compress_r128_kernel(const CompressArgs 
   }
   if (warp == 0) rope_rotation(a, 128 * k, rot, lane);
   ok = __syncthreads_and(ok ? 1 : 0) != 0;
-  if (warp == 0) finalize_warp<kCompressAttn>(a, rec, rot, b, k, ok, lane);
+  if (warp != 0) return;
+  if (lane == 0) *inv = rms_inverse(rec, a.D);
+  __syncwarp();
+  finalize_warp<kCompressAttn>(a, rec, rot, b, k, ok, *inv, lane);
 }
 
 // ---- the carry after the call --------------------------------------------------------------
@@ -617,13 +612,13 @@ __global__ void __launch_bounds__(256) compress_carry_kernel(const CompressArgs 
 }
 
 __global__ void pool_weight_kernel(const float* t, float* w, int64_t n) {
-  __shared__ float thi[256], tlo[256];
-  load_exp_table(thi, tlo);
+  __shared__ float2 tab[256];
+  load_exp_table(tab);
   __syncthreads();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += stride)
-    w[i] = pool_weight(__ldg(t + i), thi, tlo);
+    w[i] = pool_weight(__ldg(t + i), tab);
 }
 
 }  // namespace
@@ -632,7 +627,7 @@ __global__ void pool_weight_kernel(const float* t, float* w, int64_t n) {
 
 size_t compress_smem_bytes(int ratio, int64_t D) {
   if (ratio == 4)  // tables, ape rows (4 x 2D), pooled records, pipeline stages
-    return static_cast<size_t>(kTableFloats + 8 * D + kR4Warps * D +
+    return static_cast<size_t>(kTableFloats + 8 * D + kR4Warps * (D + 4) +
                                kR4Warps * 2 * kStageFloats) * sizeof(float);
   return static_cast<size_t>(kTableFloats + D) * sizeof(float);
 }
