@@ -92,43 +92,80 @@ __device__ __noinline__ float exp_double(float t) {
   return static_cast<float>(exp(static_cast<double>(t)));
 }
 
-// The table evaluation, without branches (so that a caller's independent
-// evaluations interleave).  The float-float value y1 + c is within 2^-37 of
-// e^t / 2^m; rounding it with c raised and lowered by 2^-37 gives the same
-// binary32 number exactly when that number is the correct rounding of e^t /
-// 2^m (rounding is monotone), and then `ok` is true.  `ok` is false for t
-// outside [-87, 0] (NaN and -inf included); the caller then takes
-// exp_double(t).
-__device__ __forceinline__ float exp_table(float t, const float2* tab, bool& ok) {
-  const float kb = __fmaf_rn(t, kInvL, kShifter);
-  const uint32_t kbits = __float_as_uint(kb);  // 0x4b400000 + k, k = round(t 256 / ln 2)
-  const float kf = __fsub_rn(kb, kShifter);
-  // a = t - k L1 is exact (t and k L1 within a factor of two for k != 0)
-  const float p1 = __fmul_rn(kf, kL1);
-  const float e1 = __fmaf_rn(kf, kL1, -p1);
-  const float a = __fsub_rn(t, p1);
-  const float bsum = __fmaf_rn(kf, kL2, e1);  // r = a - bsum
-  const float r = __fsub_rn(a, bsum);
-  const float q = __fmul_rn(__fmul_rn(r, r), __fmaf_rn(r, kSixth, 0.5f));
-  const float u = __fsub_rn(q, bsum);           // e^r = 1 + a + u
-  const float2 T = tab[kbits & 255u];          // 2^(j/256), j = k mod 256
-  const float p_hi = __fmul_rn(T.x, a);
-  const float p_lo = __fmaf_rn(T.x, a, -p_hi);
-  const float w = __fadd_rn(__fmaf_rn(T.x, u, p_lo), __fmaf_rn(T.y, a, T.y));
-  const float y1 = __fadd_rn(T.x, p_hi);
-  const float c = __fadd_rn(__fsub_rn(p_hi, __fsub_rn(y1, T.x)), w);  // exact low part + w
-  const float ya = __fadd_rn(y1, __fadd_rn(c, kMargin));
-  const float yb = __fadd_rn(y1, __fsub_rn(c, kMargin));
-  ok = t >= -87.0f && ya == yb;
-  // times 2^m, m = floor(k / 256), on the exponent field (the result is normal)
-  const uint32_t m23 = (kbits & ~255u) << 15;  // (k + 0x4b400000) / 256 * 2^23
-  return __uint_as_float(__float_as_uint(ya) + m23 - (__float_as_uint(kShifter) << 15));
+// Two binary32 values in one 64-bit register, for the sm_100+ packed
+// instructions: each element is the IEEE binary32 operation, rounded to
+// nearest, exactly as its scalar form.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
+__device__ __forceinline__ void upk2(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t splat2(float x) { return pk2(x, x); }
 
-__device__ __forceinline__ float pool_weight(float t, const float2* tab) {
-  bool ok;
-  const float w = exp_table(t, tab, ok);
-  return ok ? w : exp_double(t);
+// The table evaluation of two arguments at once, without branches (so that
+// a caller's independent evaluations interleave).  The float-float value
+// y1 + c is within 2^-37 of e^t / 2^m; rounding it with c raised and
+// lowered by 2^-37 gives the same binary32 number exactly when that number
+// is the correct rounding of e^t / 2^m (rounding is monotone), and then the
+// element's `ok` is true.  `ok` is false for t outside [-87, 0] (NaN and
+// -inf included); the caller then takes exp_double(t).
+__device__ __forceinline__ void exp_table2(float t0, float t1, const float2* tab, float& w0,
+                                           float& w1, bool& ok0, bool& ok1) {
+  const uint64_t t = pk2(t0, t1);
+  const uint64_t kb = fma2(t, splat2(kInvL), splat2(kShifter));
+  const uint64_t kf = sub2(kb, splat2(kShifter));
+  // a = t - k L1 is exact (t and k L1 within a factor of two for k != 0)
+  const uint64_t p1n = mul2(kf, splat2(-kL1));            // -k L1 rounded
+  const uint64_t e1 = fma2(kf, splat2(kL1), p1n);         // k L1 - p1, exact
+  const uint64_t a = add2(t, p1n);
+  const uint64_t bsum = fma2(kf, splat2(kL2), e1);        // r = a - bsum
+  const uint64_t r = sub2(a, bsum);
+  const uint64_t q = mul2(mul2(r, r), fma2(r, splat2(kSixth), splat2(0.5f)));
+  const uint64_t u = sub2(q, bsum);                        // e^r = 1 + a + u
+  float kb0, kb1;
+  upk2(kb, kb0, kb1);
+  const uint32_t kbits0 = __float_as_uint(kb0), kbits1 = __float_as_uint(kb1);
+  const float2 T0 = tab[kbits0 & 255u], T1 = tab[kbits1 & 255u];  // 2^(j/256)
+  const uint64_t th = pk2(T0.x, T1.x), tl = pk2(T0.y, T1.y);
+  const uint64_t p_hi = mul2(th, a);
+  const uint64_t p_lo = fma2(th, a, sub2(splat2(0.0f), p_hi));
+  const uint64_t w = add2(fma2(th, u, p_lo), fma2(tl, a, tl));
+  const uint64_t y1 = add2(th, p_hi);
+  const uint64_t c = add2(sub2(p_hi, sub2(y1, th)), w);   // exact low part + w
+  const uint64_t ya = add2(y1, add2(c, splat2(kMargin)));
+  const uint64_t yb = add2(y1, sub2(c, splat2(kMargin)));
+  float ya0, ya1, yb0, yb1;
+  upk2(ya, ya0, ya1);
+  upk2(yb, yb0, yb1);
+  ok0 = t0 >= -87.0f && ya0 == yb0;
+  ok1 = t1 >= -87.0f && ya1 == yb1;
+  // times 2^m, m = floor(k / 256), on the exponent field (the result is normal)
+  const uint32_t bias = __float_as_uint(kShifter) << 15;
+  w0 = __uint_as_float(__float_as_uint(ya0) + ((kbits0 & ~255u) << 15) - bias);
+  w1 = __uint_as_float(__float_as_uint(ya1) + ((kbits1 & ~255u) << 15) - bias);
 }
 
 // ---- shared pieces -------------------------------------------------------------------------
@@ -300,83 +337,57 @@ __device__ void finalize_warp(const CompressArgs& a, float* rec, const float2* r
 
 // ---- ratio 4 -------------------------------------------------------------------------------
 
-// Softmax pool of one dimension over N candidates (scores s, values v), in
-// candidate order, -inf scores left out: the weights first (independent, so
-// they interleave), the rare uncertified ones redone in double (e^-inf = 0
-// there), then the sums.  A left-out candidate adds a weight of 0 to the
-// denominator, which leaves it unchanged (it is never -0).
-template <int N>
-__device__ __forceinline__ float pool_dim(const float (&s)[N], const float (&v)[N], bool& ok,
-                                          const float2* tab) {
-  float m = SA_NEG_INF;
+// The weights e^t[c] of 8 candidates, two per packed evaluation; the rare
+// uncertified ones are redone in double (e^-inf = 0 there).
+__device__ __forceinline__ void weights8(const float (&t)[8], const float2* tab, float (&w)[8]) {
+  bool ok[8];
 #pragma unroll
-  for (int c = 0; c < N; ++c) m = fmaxf(m, s[c]);
-  ok = ok && isfinite(m);
-  float w[N];
-  bool cert = true;
+  for (int p = 0; p < 4; ++p)
+    exp_table2(t[2 * p], t[2 * p + 1], tab, w[2 * p], w[2 * p + 1], ok[2 * p], ok[2 * p + 1]);
+  bool all = true;
 #pragma unroll
-  for (int c = 0; c < N; ++c) {
-    bool okc;
-    w[c] = exp_table(__fsub_rn(s[c], m), tab, okc);
-    cert = cert && okc;
+  for (int c = 0; c < 8; ++c) all = all && ok[c];
+  if (!all) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (!ok[c]) w[c] = exp_double(t[c]);
   }
-  if (!cert) {
+}
+
+// Adds 8 candidates' terms to the pool sums in candidate order: num += w v,
+// den += w; a -inf score leaves num unchanged and adds w = 0 to den, which
+// leaves it unchanged too (den is never -0).
+__device__ __forceinline__ void pool_sums8(const float (&s)[8], const float (&v)[8],
+                                           const float (&w)[8], float& num, float& den) {
+  float wv[8];
 #pragma unroll
-    for (int c = 0; c < N; ++c) {
-      bool okc;
-      exp_table(__fsub_rn(s[c], m), tab, okc);
-      if (!okc) w[c] = exp_double(__fsub_rn(s[c], m));
-    }
-  }
-  float num = 0.0f, den = 0.0f;
+  for (int p = 0; p < 4; ++p)
+    upk2(mul2(pk2(w[2 * p], w[2 * p + 1]), pk2(v[2 * p], v[2 * p + 1])), wv[2 * p],
+         wv[2 * p + 1]);
 #pragma unroll
-  for (int c = 0; c < N; ++c) {
-    const float n2 = __fadd_rn(num, __fmul_rn(w[c], v[c]));
+  for (int c = 0; c < 8; ++c) {
+    const float n2 = __fadd_rn(num, wv[c]);
     num = s[c] != SA_NEG_INF ? n2 : num;
     den = __fadd_rn(den, w[c]);
   }
-  ok = ok && den != 0.0f && isfinite(den) && isfinite(num);
-  return round_bf16(__fdiv_rn(num, den));
 }
 
-// Source rows of record k's candidates (ratio 4): c < 4 the previous
-// block's token 4k - 4 + c on source dims [0, D), c >= 4 the block's token
-// 4k + c - 4 on [D, 2D).  A token of this call is read from kv / gate (+ the
-// ape row of its phase); an earlier one from its carry slot (the open block's
-// tokens in slots 4 + phase, the closed block before it in slots 0..3); a
-// token before position 0 is no candidate.
-struct R4Sources {
-  const float* v[8];
-  const float* s[8];
-  uint32_t from_rows;  // bit c: candidate c is a token of this call (add its ape row)
-  uint32_t present;    // bit c: candidate c exists
-};
-
-__device__ __forceinline__ void r4_sources(const CompressArgs& a, int64_t b, int64_t k,
-                                           R4Sources& x) {
-  x.from_rows = 0;
-  x.present = 0;
-  const int64_t open_from = a.start - (a.start & 3);
+// Softmax pool of one dimension over 8 candidates (scores s, values v), in
+// candidate order, -inf scores left out; then bf16.
+__device__ __forceinline__ float pool_dim8(const float (&s)[8], const float (&v)[8], bool& ok,
+                                           const float2* tab) {
+  float m = SA_NEG_INF;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const int64_t P = c < 4 ? 4 * k - 4 + c : 4 * k + c - 4;
-    const int64_t half = c < 4 ? 0 : a.D;
-    x.v[c] = a.kv;  // any valid address for an absent candidate
-    x.s[c] = a.kv;
-    if (P < 0) continue;
-    x.present |= 1u << c;
-    if (P >= a.start) {
-      const int64_t off = (b * a.S + (P - a.start)) * a.W + half;
-      x.v[c] = a.kv + off;
-      x.s[c] = a.gate + off;
-      x.from_rows |= 1u << c;
-    } else {
-      const int64_t slot = P >= open_from ? 4 + (P & 3) : (P & 3);
-      const float* base = a.carry + ((b * 8 + slot) * 2) * a.W + half;
-      x.v[c] = base;
-      x.s[c] = base + a.W;
-    }
-  }
+  for (int c = 0; c < 8; ++c) m = fmaxf(m, s[c]);
+  ok = ok && isfinite(m);
+  float t[8], w[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) t[c] = __fsub_rn(s[c], m);
+  weights8(t, tab, w);
+  float num = 0.0f, den = 0.0f;
+  pool_sums8(s, v, w, num, den);
+  ok = ok && den != 0.0f && isfinite(den) && isfinite(num);
+  return round_bf16(__fdiv_rn(num, den));
 }
 
 // One warp's pipeline stage: 8 candidates x (value, score) x 32 dimensions.
@@ -388,24 +399,69 @@ __device__ __forceinline__ void cp_async16(float* dst, const float* src, bool va
                : "memory");
 }
 
-// Stage dims [32 it, 32 it + 32) of the 8 candidates: 128 16-byte chunks, 4
-// per lane; chunk q holds candidate q / 16, array (q / 8) % 2 (0 value, 1
-// score), dims 4 (q % 8) .. + 3.  Absent candidates and dims past D are
-// zero-filled (no global read).
-__device__ __forceinline__ void r4_stage(const CompressArgs& a, const R4Sources& x, int it,
+// Record k's candidates (ratio 4): c < 4 the previous block's token 4k - 4 +
+// c on source dims [0, D), c >= 4 the block's token 4k + c - 4 on [D, 2D).
+// A token of this call is read from kv / gate and scores gate + its phase's
+// ape row; an earlier one from its carry slot (the open block's tokens in
+// slots 4 + phase, the closed block before it in slots 0..3), its score as
+// stored; a token before position 0 is no candidate (value 0, score -inf).
+//
+// Each lane stages 4 of a stage's 128 16-byte chunks: chunk q = lane + 32 i
+// holds candidate q / 16, array (q / 8) % 2 (0 value, 1 score), dims
+// 4 (q % 8) .. + 3 of the stage's 32.  `src` are those chunks' sources at
+// dim 0 (absent candidates read nothing: zero-filled), `ape_off` per
+// candidate the row in the shared ape table whose dim d is added to the
+// staged score: the phase row (+ D for c >= 4), a zero row (carry) or a
+// -inf row (absent).
+struct R4Plan {
+  const float* src[4];
+  uint32_t valid;  // bit i: chunk i has a source
+  int ape_off[8];
+};
+
+__device__ __forceinline__ void r4_plan(const CompressArgs& a, int64_t b, int64_t k, int lane,
+                                        R4Plan& pl) {
+  const int64_t open_from = a.start - (a.start & 3);
+  const int W = static_cast<int>(a.W);
+  pl.valid = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pl.src[i] = a.kv;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int64_t P = c < 4 ? 4 * k - 4 + c : 4 * k + c - 4;
+    const int half = c < 4 ? 0 : a.D;
+    const float* v = nullptr;
+    const float* sc = nullptr;
+    if (P < 0) {
+      pl.ape_off[c] = 4 * W + a.D;  // the -inf row
+    } else if (P >= a.start) {
+      const int64_t off = (b * a.S + (P - a.start)) * a.W + half;
+      v = a.kv + off;
+      sc = a.gate + off;
+      pl.ape_off[c] = static_cast<int>(P & 3) * W + half;
+    } else {
+      const int64_t slot = P >= open_from ? 4 + (P & 3) : (P & 3);
+      v = a.carry + ((b * 8 + slot) * 2) * a.W + half;
+      sc = v + a.W;
+      pl.ape_off[c] = 4 * W;  // the zero row
+    }
+    // this lane's chunks of candidate c: i with 2 i + (lane >= 16) == c
+    if ((c & 1) == (lane >= 16 ? 1 : 0) && v) {
+      const int i = c >> 1;
+      pl.src[i] = (((lane >> 3) & 1) ? sc : v) + 4 * (lane & 7);
+      pl.valid |= 1u << i;
+    }
+  }
+}
+
+__device__ __forceinline__ void r4_stage(const CompressArgs& a, const R4Plan& pl, int it,
                                          float* stage, int lane) {
+  const int dst = ((lane >= 16 ? 1 : 0) * 2 + ((lane >> 3) & 1)) * 32 + 4 * (lane & 7);
+  const bool in_d = 32 * it + 4 * (lane & 7) < a.D;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int q = lane + 32 * i;
-    const int c_lo = 2 * i, c_hi = 2 * i + 1;       // q / 16 is one of these two
-    const bool upper = lane >= 16;
-    const int c = upper ? c_hi : c_lo;
-    const bool score = (q >> 3) & 1;
-    const int part = q & 7;
-    const float* base = upper ? (score ? x.s[c_hi] : x.v[c_hi]) : (score ? x.s[c_lo] : x.v[c_lo]);
-    const int d = 32 * it + 4 * part;
-    const bool valid = ((x.present >> c) & 1u) && d < a.D;
-    cp_async16(stage + (c * 2 + (score ? 1 : 0)) * 32 + 4 * part, valid ? base + d : a.ape, valid);
+    const bool valid = ((pl.valid >> i) & 1u) && in_d;
+    cp_async16(stage + dst + 128 * i, valid ? pl.src[i] + 32 * it : a.ape, valid);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -416,29 +472,32 @@ __global__ void __launch_bounds__(kR4Warps * 32, 3) compress_r4_kernel(const Com
   float2* tab = reinterpret_cast<float2*>(smem);
   float2* rot = reinterpret_cast<float2*>(smem + 512);
   float* invs = smem + 640;                    // [warps] RMSNorm scales
-  float* ape_s = smem + kTableFloats;          // [4, W]
+  float* ape_s = smem + kTableFloats;          // [4, W] phase rows, then D zeros, D -inf
+  const int W = static_cast<int>(a.W);
   const int rs = a.D + 4;                      // record stride: the RMS lanes hit distinct banks
-  float* recs = ape_s + 4 * a.W;               // [warps, D + 4]
+  float* recs = ape_s + 5 * W;                 // [warps, D + 4]
   float* stages = recs + kR4Warps * rs;        // [warps, 2, kStageFloats]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t k = a.k0 + blockIdx.x;
   load_exp_table(tab);
-  for (int i = threadIdx.x; i < a.W; i += blockDim.x)  // 4 rows of W floats, as float4
+  for (int i = threadIdx.x; i < W; i += blockDim.x)  // 4 rows of W floats, as float4
     reinterpret_cast<float4*>(ape_s)[i] = __ldg(reinterpret_cast<const float4*>(a.ape) + i);
+  for (int i = threadIdx.x; i < W; i += blockDim.x)
+    ape_s[4 * W + i] = i < a.D ? 0.0f : SA_NEG_INF;
   __syncthreads();
   const int64_t b = static_cast<int64_t>(blockIdx.y) * kR4Warps + warp;
   const bool active = b < a.B;
   float* rec = recs + warp * rs;
   bool ok = true;
   if (active) {
-    R4Sources x;
-    r4_sources(a, b, k, x);
+    R4Plan pl;
+    r4_plan(a, b, k, lane, pl);
     float* stg = stages + warp * 2 * kStageFloats;
     const int niter = (a.D + 31) / 32;
-    r4_stage(a, x, 0, stg, lane);
+    r4_stage(a, pl, 0, stg, lane);
     for (int it = 0; it < niter; ++it) {
       if (it + 1 < niter)
-        r4_stage(a, x, it + 1, stg + ((it + 1) & 1) * kStageFloats, lane);
+        r4_stage(a, pl, it + 1, stg + ((it + 1) & 1) * kStageFloats, lane);
       else
         asm volatile("cp.async.commit_group;" ::: "memory");
       asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -448,14 +507,10 @@ __global__ void __launch_bounds__(kR4Warps * 32, 3) compress_r4_kernel(const Com
       float s[8], v[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        // ape row of the candidate's phase: c < 4 phase c on [0, D), else phase c - 4 on [D, 2D)
-        const float av = ape_s[(c & 3) * a.W + (c < 4 ? 0 : a.D) + d];
-        const float sv = cur[(c * 2 + 1) * 32 + lane];
         v[c] = cur[(c * 2) * 32 + lane];
-        s[c] = (x.from_rows >> c) & 1u ? __fadd_rn(sv, av) : sv;
-        if (!((x.present >> c) & 1u)) s[c] = SA_NEG_INF;
+        s[c] = __fadd_rn(cur[(c * 2 + 1) * 32 + lane], ape_s[pl.ape_off[c] + d]);
       }
-      const float out = pool_dim<8>(s, v, ok, tab);
+      const float out = pool_dim8(s, v, ok, tab);
       if (32 * it + lane < a.D) rec[32 * it + lane] = out;
       __syncwarp();  // every lane has read this stage before it is refilled
     }
@@ -508,30 +563,15 @@ __global__ void __launch_bounds__(1024) compress_r128_kernel(const CompressArgs 
     ok = ok && isfinite(m);
     float num = 0.0f, den = 0.0f;
     for (int j0 = 0; j0 < 128; j0 += 8) {
-      float sc[8], v[8], w[8];
-      bool cert = true;
+      float sc[8], v[8], t[8], w[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         sc[c] = score(j0 + c);
         v[c] = value(j0 + c);
-        bool okc;
-        w[c] = exp_table(__fsub_rn(sc[c], m), tab, okc);
-        cert = cert && okc;
+        t[c] = __fsub_rn(sc[c], m);
       }
-      if (!cert) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          bool okc;
-          exp_table(__fsub_rn(sc[c], m), tab, okc);
-          if (!okc) w[c] = exp_double(__fsub_rn(sc[c], m));
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {  // a -inf score adds w = 0 to den: no change
-        const float n2 = __fadd_rn(num, __fmul_rn(w[c], v[c]));
-        num = sc[c] != SA_NEG_INF ? n2 : num;
-        den = __fadd_rn(den, w[c]);
-      }
+      weights8(t, tab, w);
+      pool_sums8(sc, v, w, num, den);
     }
     ok = ok && den != 0.0f && isfinite(den) && isfinite(num);
     rec[d] = round_bf16(__fdiv_rn(num, den));
@@ -616,9 +656,17 @@ __global__ void pool_weight_kernel(const float* t, float* w, int64_t n) {
   load_exp_table(tab);
   __syncthreads();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += stride)
-    w[i] = pool_weight(__ldg(t + i), tab);
+  // pairs (2 i, 2 i + 1) through the packed evaluation the pools use
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; 2 * i < n;
+       i += stride) {
+    const bool two = 2 * i + 1 < n;
+    const float t0 = __ldg(t + 2 * i), t1 = two ? __ldg(t + 2 * i + 1) : 0.0f;
+    float w0, w1;
+    bool ok0, ok1;
+    exp_table2(t0, t1, tab, w0, w1, ok0, ok1);
+    w[2 * i] = ok0 ? w0 : exp_double(t0);
+    if (two) w[2 * i + 1] = ok1 ? w1 : exp_double(t1);
+  }
 }
 
 }  // namespace
@@ -626,8 +674,8 @@ __global__ void pool_weight_kernel(const float* t, float* w, int64_t n) {
 // ---- host side ------------------------------------------------------------------------------
 
 size_t compress_smem_bytes(int ratio, int64_t D) {
-  if (ratio == 4)  // tables, ape rows (4 x 2D), pooled records, pipeline stages
-    return static_cast<size_t>(kTableFloats + 8 * D + kR4Warps * (D + 4) +
+  if (ratio == 4)  // tables, ape rows (4 x 2D + a zero and a -inf row), records, stages
+    return static_cast<size_t>(kTableFloats + 10 * D + kR4Warps * (D + 4) +
                                kR4Warps * 2 * kStageFloats) * sizeof(float);
   return static_cast<size_t>(kTableFloats + D) * sizeof(float);
 }
