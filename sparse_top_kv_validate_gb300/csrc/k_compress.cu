@@ -92,80 +92,38 @@ __device__ __noinline__ float exp_double(float t) {
   return static_cast<float>(exp(static_cast<double>(t)));
 }
 
-// Two binary32 values in one 64-bit register, for the sm_100+ packed
-// instructions: each element is the IEEE binary32 operation, rounded to
-// nearest, exactly as its scalar form.
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void upk2(uint64_t x, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t splat2(float x) { return pk2(x, x); }
-
-// The table evaluation of two arguments at once, without branches (so that
-// a caller's independent evaluations interleave).  The float-float value
-// y1 + c is within 2^-37 of e^t / 2^m; rounding it with c raised and
-// lowered by 2^-37 gives the same binary32 number exactly when that number
-// is the correct rounding of e^t / 2^m (rounding is monotone), and then the
-// element's `ok` is true.  `ok` is false for t outside [-87, 0] (NaN and
-// -inf included); the caller then takes exp_double(t).
-__device__ __forceinline__ void exp_table2(float t0, float t1, const float2* tab, float& w0,
-                                           float& w1, bool& ok0, bool& ok1) {
-  const uint64_t t = pk2(t0, t1);
-  const uint64_t kb = fma2(t, splat2(kInvL), splat2(kShifter));
-  const uint64_t kf = sub2(kb, splat2(kShifter));
+// The table evaluation, without branches (so that a caller's independent
+// evaluations interleave).  The float-float value y1 + c is within 2^-37 of
+// e^t / 2^m; rounding it with c raised and lowered by 2^-37 gives the same
+// binary32 number exactly when that number is the correct rounding of e^t /
+// 2^m (rounding is monotone), and then `ok` is true.  `ok` is false for t
+// outside [-87, 0] (NaN and -inf included); the caller then takes
+// exp_double(t).  (Kept scalar: a packed two-lane form of these steps gave
+// certified results one ulp off under some instruction schedules.)
+__device__ __forceinline__ float exp_table(float t, const float2* tab, bool& ok) {
+  const float kb = __fmaf_rn(t, kInvL, kShifter);
+  const uint32_t kbits = __float_as_uint(kb);  // 0x4b400000 + k, k = round(t 256 / ln 2)
+  const float kf = __fsub_rn(kb, kShifter);
   // a = t - k L1 is exact (t and k L1 within a factor of two for k != 0)
-  const uint64_t p1n = mul2(kf, splat2(-kL1));            // -k L1 rounded
-  const uint64_t e1 = fma2(kf, splat2(kL1), p1n);         // k L1 - p1, exact
-  const uint64_t a = add2(t, p1n);
-  const uint64_t bsum = fma2(kf, splat2(kL2), e1);        // r = a - bsum
-  const uint64_t r = sub2(a, bsum);
-  const uint64_t q = mul2(mul2(r, r), fma2(r, splat2(kSixth), splat2(0.5f)));
-  const uint64_t u = sub2(q, bsum);                        // e^r = 1 + a + u
-  float kb0, kb1;
-  upk2(kb, kb0, kb1);
-  const uint32_t kbits0 = __float_as_uint(kb0), kbits1 = __float_as_uint(kb1);
-  const float2 T0 = tab[kbits0 & 255u], T1 = tab[kbits1 & 255u];  // 2^(j/256)
-  const uint64_t th = pk2(T0.x, T1.x), tl = pk2(T0.y, T1.y);
-  const uint64_t p_hi = mul2(th, a);
-  const uint64_t p_lo = fma2(th, a, sub2(splat2(0.0f), p_hi));
-  const uint64_t w = add2(fma2(th, u, p_lo), fma2(tl, a, tl));
-  const uint64_t y1 = add2(th, p_hi);
-  const uint64_t c = add2(sub2(p_hi, sub2(y1, th)), w);   // exact low part + w
-  const uint64_t ya = add2(y1, add2(c, splat2(kMargin)));
-  const uint64_t yb = add2(y1, sub2(c, splat2(kMargin)));
-  float ya0, ya1, yb0, yb1;
-  upk2(ya, ya0, ya1);
-  upk2(yb, yb0, yb1);
-  ok0 = t0 >= -87.0f && ya0 == yb0;
-  ok1 = t1 >= -87.0f && ya1 == yb1;
+  const float p1 = __fmul_rn(kf, kL1);
+  const float e1 = __fmaf_rn(kf, kL1, -p1);
+  const float a = __fsub_rn(t, p1);
+  const float bsum = __fmaf_rn(kf, kL2, e1);  // r = a - bsum
+  const float r = __fsub_rn(a, bsum);
+  const float q = __fmul_rn(__fmul_rn(r, r), __fmaf_rn(r, kSixth, 0.5f));
+  const float u = __fsub_rn(q, bsum);           // e^r = 1 + a + u
+  const float2 T = tab[kbits & 255u];          // 2^(j/256), j = k mod 256
+  const float p_hi = __fmul_rn(T.x, a);
+  const float p_lo = __fmaf_rn(T.x, a, -p_hi);
+  const float w = __fadd_rn(__fmaf_rn(T.x, u, p_lo), __fmaf_rn(T.y, a, T.y));
+  const float y1 = __fadd_rn(T.x, p_hi);
+  const float c = __fadd_rn(__fsub_rn(p_hi, __fsub_rn(y1, T.x)), w);  // exact low part + w
+  const float ya = __fadd_rn(y1, __fadd_rn(c, kMargin));
+  const float yb = __fadd_rn(y1, __fsub_rn(c, kMargin));
+  ok = t >= -87.0f && t <= 0.0f && ya == yb;
   // times 2^m, m = floor(k / 256), on the exponent field (the result is normal)
-  const uint32_t bias = __float_as_uint(kShifter) << 15;
-  w0 = __uint_as_float(__float_as_uint(ya0) + ((kbits0 & ~255u) << 15) - bias);
-  w1 = __uint_as_float(__float_as_uint(ya1) + ((kbits1 & ~255u) << 15) - bias);
+  const uint32_t m23 = (kbits & ~255u) << 15;  // (k + 0x4b400000) / 256 * 2^23
+  return __uint_as_float(__float_as_uint(ya) + m23 - (__float_as_uint(kShifter) << 15));
 }
 
 // ---- shared pieces -------------------------------------------------------------------------
@@ -337,13 +295,12 @@ __device__ void finalize_warp(const CompressArgs& a, float* rec, const float2* r
 
 // ---- ratio 4 -------------------------------------------------------------------------------
 
-// The weights e^t[c] of 8 candidates, two per packed evaluation; the rare
+// The weights e^t[c] of 8 candidates (independent evaluations); the rare
 // uncertified ones are redone in double (e^-inf = 0 there).
 __device__ __forceinline__ void weights8(const float (&t)[8], const float2* tab, float (&w)[8]) {
   bool ok[8];
 #pragma unroll
-  for (int p = 0; p < 4; ++p)
-    exp_table2(t[2 * p], t[2 * p + 1], tab, w[2 * p], w[2 * p + 1], ok[2 * p], ok[2 * p + 1]);
+  for (int c = 0; c < 8; ++c) w[c] = exp_table(t[c], tab, ok[c]);
   bool all = true;
 #pragma unroll
   for (int c = 0; c < 8; ++c) all = all && ok[c];
@@ -359,14 +316,9 @@ __device__ __forceinline__ void weights8(const float (&t)[8], const float2* tab,
 // leaves it unchanged too (den is never -0).
 __device__ __forceinline__ void pool_sums8(const float (&s)[8], const float (&v)[8],
                                            const float (&w)[8], float& num, float& den) {
-  float wv[8];
-#pragma unroll
-  for (int p = 0; p < 4; ++p)
-    upk2(mul2(pk2(w[2 * p], w[2 * p + 1]), pk2(v[2 * p], v[2 * p + 1])), wv[2 * p],
-         wv[2 * p + 1]);
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    const float n2 = __fadd_rn(num, wv[c]);
+    const float n2 = __fadd_rn(num, __fmul_rn(w[c], v[c]));
     num = s[c] != SA_NEG_INF ? n2 : num;
     den = __fadd_rn(den, w[c]);
   }
@@ -656,16 +608,12 @@ __global__ void pool_weight_kernel(const float* t, float* w, int64_t n) {
   load_exp_table(tab);
   __syncthreads();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  // pairs (2 i, 2 i + 1) through the packed evaluation the pools use
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; 2 * i < n;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += stride) {
-    const bool two = 2 * i + 1 < n;
-    const float t0 = __ldg(t + 2 * i), t1 = two ? __ldg(t + 2 * i + 1) : 0.0f;
-    float w0, w1;
-    bool ok0, ok1;
-    exp_table2(t0, t1, tab, w0, w1, ok0, ok1);
-    w[2 * i] = ok0 ? w0 : exp_double(t0);
-    if (two) w[2 * i + 1] = ok1 ? w1 : exp_double(t1);
+    const float x = __ldg(t + i);
+    bool ok;
+    const float y = exp_table(x, tab, ok);
+    w[i] = ok ? y : exp_double(x);
   }
 }
 
