@@ -803,6 +803,9 @@ KERNEL_SOURCES = {
 
 TRAFFIC: dict = {
     # workload: (kernel, bytes per launch, source hash at capture, how)
+    "compress_r4": ("compress_r4_kernel", 547_078_912, "cd7022a0e814742c",
+                    "ncu --set full, one launch of the bench's own workload (537.01 MB read, "
+                    "10.07 MB written)"),
 }
 
 
