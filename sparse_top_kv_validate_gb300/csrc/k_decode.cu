@@ -10,24 +10,26 @@
 // a fixed order; paged addressing as in ferrum-kernels causal_attention.rs
 // (16-token blocks through a table).
 //
-// GB300 design (not the pages' row-per-block kernel):
-//  * A work unit is (batch, KV head or index head, query), serving every query
-//    head that shares its index row and KV head, so each gathered K/V row is
-//    read from HBM once for the whole GQA group.  Units are cut into splits of
-//    `chunk` candidates (one CTA each).
-//  * Candidate -> cache-row resolution (index row, window, masks, page table)
-//    happens once per CTA into shared memory.
-//  * K and V rows are fetched by bulk async copies (one 16-byte-aligned row per
-//    copy, completion counted on an mbarrier) into a 3-deep ring of 64-key
-//    stages; rows are padded by 16 bytes so ldmatrix reads are conflict-free.
-//  * Each warp owns 16 keys of a stage and runs the tensor-core m16n8k16 MMA
-//    with KEYS as the M dimension: S^T = K . Q^T (heads as N, so a GQA group of
-//    8 fills N exactly), then O^T += V^T . P^T where P^T is produced from the
-//    S^T accumulator by an in-register 8x8 transpose (movmatrix).  The online
-//    softmax state of a head lives in the same lanes as its O^T columns, so
-//    rescaling is thread-local.
-//  * Warps merge in shared memory in warp order; splits merge in split order.
-//    Results are deterministic run to run.
+// What this file holds (the tensor-core gather is gather_stream_kernel in
+// k_stream.cu):
+//  * unit / candidate resolution shared by the gather kernels: a work unit is
+//    (batch, KV head or index head, query) serving every query head that
+//    shares its index row and KV head; resolve_candidate maps a candidate to a
+//    cache row (index row, window, masks, page table) or -1, never out of
+//    bounds.
+//  * gather_simt_kernel: the general path for fp32 storage and the shapes the
+//    tensor-core kernel does not take.  One CTA per (unit, head, split of
+//    `chunk` candidates); warps stride over the candidates, each lane holding
+//    DPL dims (d = lane + 32 k); fp32 FMA and an online softmax; the bias and
+//    mask terms of gather_common.cuh.  Warps merge in shared memory in warp
+//    order.
+//  * combine_kernel and combine_flat_kernel: the fixed-order log-sum-exp merge
+//    of split partials (max, sum, unnormalised P.V), with the sink logit in
+//    the denominator; combine_flat_kernel is one thread per four output dims
+//    with every split's partials loaded at once (the FP8 paths).
+//  * paged_append_kernel: writes the new token into its page before a paged
+//    decode.
+// Results are deterministic run to run (fixed warp and split order).
 #include "gather_common.cuh"
 
 namespace sa {
