@@ -1010,16 +1010,40 @@ def run_gpu(args):
     hot_ms = max_over_ranks(h_s.elapsed_time(h_e) / hot_steps, dev)
     # dominant-kernel leg: the library records events around its dominant
     # kernel (sa.kernel_events); same flush protocol, separate from the timed
-    # steps because recording between kernels removes their launch overlap
+    # steps because recording between kernels removes their launch overlap.
+    # With a graph the events are nodes of a second captured step, so that no
+    # host launch latency falls between them.
     k_steps = max(3, min(steps, 50))
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(k_steps)]
-    for i in range(k_steps):
-        flush_l2()
-        with sa.kernel_events(*kev[i]):
-            wl.step()
-    torch.cuda.synchronize(dev)
-    kernel_ms = statistics.median(a.elapsed_time(b) for a, b in kev)
+    kernel_samples = []
+    kgraph = None
+    if graph is not None:
+        kb, ka = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        try:
+            with sa.kernel_events(kb, ka):
+                kgraph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(kgraph):
+                    wl.step()
+            torch.cuda.synchronize(dev)
+        except Exception as exc:
+            print(f"# kernel-event graph capture failed ({exc}); timing direct calls",
+                  file=sys.stderr)
+            kgraph = None
+    if kgraph is not None:
+        for i in range(k_steps):
+            flush_l2()
+            kgraph.replay()
+            torch.cuda.synchronize(dev)
+            kernel_samples.append(kb.elapsed_time(ka))
+    else:
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(k_steps)]
+        for i in range(k_steps):
+            flush_l2()
+            with sa.kernel_events(*kev[i]):
+                wl.step()
+        torch.cuda.synchronize(dev)
+        kernel_samples = [a.elapsed_time(b) for a, b in kev]
+    kernel_ms = statistics.median(kernel_samples)
     err = int(wl.err.item())
 
     if rank == 0:

@@ -169,7 +169,13 @@ int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st);
 // ---- dense prefill on the fifth-generation tensor cores (tcgen05 + TMEM + TMA) ------
 // Records ev (a cudaEvent_t, nullable) on st: the measurement hook.
 inline void mark_event(void* ev, cudaStream_t st) {
-  if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev), st);
+  if (!ev) return;
+  // under stream capture only an external record becomes a node of the graph
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(static_cast<cudaEvent_t>(ev), st);
 }
 
 struct PrefillTcArgs {
