@@ -267,7 +267,7 @@ def test_bias_shapes_that_do_not_broadcast_are_refused(host_lib, dims, status):
 def test_unknown_option_bits_and_misaligned_bias_are_refused(host_lib):
     p = _dense_params()
     p.bias_rank, p.bias_dims[0] = 1, 100
-    p.options = 8  # the first bit no option uses
+    p.options = 4
     assert host_lib.sparse_attn_decode(C.byref(p), None) == -7
     p.options, p.reserved_ = 0, 1
     assert host_lib.sparse_attn_decode(C.byref(p), None) == -7
