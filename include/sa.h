@@ -96,11 +96,6 @@ extern "C" {
                                     its own bulk copy instead of TMA tensor maps */
 #define SA_OPT_FP8_WARP_MMA 2u   /* FP8 records: the warp-level MMA kernel (32-head
                                     blocks) for every head count */
-#define SA_OPT_FP8_DIM_PARTS 4u  /* FP8 records, 128-head blocks: the tensor-core
-                                    kernel in which each of three CTAs computes the
-                                    scores itself and owns a third of the output
-                                    dims (instead of one score CTA feeding three
-                                    output CTAs) */
 
 /* Human-readable name of a status code (static string). */
 const char* sa_status_string(int status);

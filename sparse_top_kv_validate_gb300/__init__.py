@@ -26,7 +26,6 @@ __all__ = [
     "paged_attn_decode", "sparse_attn_decode_workspace", "attn_prefill_workspace",
     "paged_attn_decode_workspace", "new_workspace", "sparse_attn_decode_noalloc",
     "NOALLOC_SCRATCH_BYTES", "ERR_SCRATCH_LIMIT", "OPT_ROW_COPIES", "OPT_FP8_WARP_MMA",
-    "OPT_FP8_DIM_PARTS",
     "F32", "F16", "BF16", "FP8_E4M3_B64",
     "IDX_BELOW_SENTINEL", "IDX_AFTER_PADDING", "IDX_OUT_OF_RANGE", "IDX_NOT_INCREASING",
     "IDX_DUPLICATE", "IDX_ALL_PADDING", "ERRBIT_WRITE_POS", "ERRBIT_PAGE", "ERRBIT_TIMEOUT",
@@ -47,7 +46,7 @@ IDX_NOT_INCREASING, IDX_DUPLICATE, IDX_ALL_PADDING = 8, 16, 32
 ERRBIT_WRITE_POS, ERRBIT_PAGE, ERRBIT_TIMEOUT = 64, 128, 256
 ERR_SCRATCH_LIMIT = -9
 NOALLOC_SCRATCH_BYTES = 16 << 20
-OPT_ROW_COPIES, OPT_FP8_WARP_MMA, OPT_FP8_DIM_PARTS = 1, 2, 4
+OPT_ROW_COPIES, OPT_FP8_WARP_MMA = 1, 2
 SEL_TIE, SEL_NONFINITE = 1, 2
 ERRBIT_SEL_TIE, ERRBIT_SEL_NONFINITE = 512, 1024
 ERRBIT_RECORD = 2048

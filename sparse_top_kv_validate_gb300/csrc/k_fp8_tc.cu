@@ -103,7 +103,6 @@ constexpr uint32_t kColS = 0, kColO = 2 * kKeys, kTmemCols = 512;
 static_assert(kColO + kPartDims <= kTmemCols, "tensor memory");
 
 struct Fp8TcParams {
-  const void* q;             // [B, Hq, Sq, 576] bf16 (read directly by the role-split kernel)
   const int32_t* pos;        // [units, n_cand_pad] planned cache positions or -1
   int64_t n_cand_pad;        // multiple of 128
   void* y;                   // [B, Hq, Sq, 576] bf16
@@ -842,553 +841,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---- role-split attention kernel ---------------------------------------------------------
-//
-// fp8_rs_kernel: a cluster of four CTAs per (unit, 128-head block, key split).
-// Rank 0 (the score CTA) keeps Q in tensor memory (the A operand of the score
-// MMA, so only K is read from shared memory), computes each 128 x 128 score
-// tile once, and turns it into P = 2^(logit - m) as bf16.  Ranks 1..3 (the PV
-// CTAs) each own 192 output dims (three 64-dim chunks) in their tensor memory
-// and accumulate O += P V with P from shared memory.  P travels to the PV CTAs
-// as bulk copies between the CTAs' shared memories (two P slots per PV CTA),
-// with a header per slot: each head's rescale factor when the lazy running
-// maximum was raised.  At the end the score CTA sends each head's (max, sum).
-// Barriers live at the same offsets in every CTA of the cluster, so a remote
-// one is this CTA's address mapped to the peer.
-namespace {
-
-constexpr int kRsCtas = 4;               // cluster: score CTA + three PV CTAs
-constexpr int kRsRing = 9;               // K chunk ring of the score CTA: one tile
-constexpr int kRsPBytes = 2 * kChunkBytes;  // P tile: 128 heads x 128 keys bf16, two slabs
-constexpr int kRsHdrBytes = kHeads * 4 + 16;  // alpha[128] + 4 rescale flags (one per warp)
-
-// barriers (same indices, same offsets in every CTA; each role uses its own)
-constexpr int kRbQ = 0;                          // S: Q in tensor memory (128)
-constexpr int kRbFullK = 1;                      // S: [9] K chunk landed (tx)
-constexpr int kRbEmptyK = kRbFullK + kRsRing;    // S: [9] chunk read by the score MMAs
-constexpr int kRbSFull = kRbEmptyK + kRsRing;    // S: score tile complete
-constexpr int kRbSFree = kRbSFull + 1;           // S: scores loaded to registers (128)
-constexpr int kRbPLocal = kRbSFree + 1;          // S: [2] local P slot written (128)
-constexpr int kRbLocalFree = kRbPLocal + 2;      // S: [2] local P slot copied out (1)
-constexpr int kRbPEmpty = kRbLocalFree + 2;      // S: [2] P slot free in all PV CTAs (3)
-constexpr int kRbFinLocal = kRbPEmpty + 2;       // S: local (max, sum) written (128)
-constexpr int kRbVFull = kRbFinLocal + 1;        // PV: [2] V tile landed (tx)
-constexpr int kRbPFull = kRbVFull + 2;           // PV: [2] P slot landed (tx)
-constexpr int kRbPvDone = kRbPFull + 2;          // PV: [2] the slot's MMAs complete
-constexpr int kRbResc = kRbPvDone + 2;           // PV: rescale O requested (1)
-constexpr int kRbRescDone = kRbResc + 1;         // PV: rescale done (128)
-constexpr int kRbFinal = kRbRescDone + 1;        // PV: (max, sum) landed (tx)
-constexpr int kRbDrain = kRbFinal + 1;           // both: an MMA lane's last commit
-constexpr int kRsNumBars = kRbDrain + 1;
-constexpr int kRsOffTmem = kRsNumBars * 8;
-constexpr int kRsOffAbort = kRsOffTmem + 4;
-constexpr int kRsOffRescSlot = kRsOffAbort + 4;  // PV: the slot whose alphas to apply, -1 = end
-constexpr int kRsOffValid = 512;                 // S: [kMaxTiles][4] u32 bit masks
-constexpr int kRsOffHdr = 1280;                  // [2] slot headers
-constexpr int kRsOffFinal = 2560;                // [128] (max, sum)
-constexpr int kRsOffData = 4096;
-// score CTA: the K ring, then its two local P slots
-constexpr int kRsOffRing = kRsOffData;
-constexpr int kRsOffP = kRsOffRing + kRsRing * kChunkBytes;
-constexpr int kRsEndS = kRsOffP + 2 * kRsPBytes;
-// PV CTA: two P slots, two V tiles of three chunks; the epilogue stages rows over both
-constexpr int kRsOffPSlot = kRsOffData;
-constexpr int kRsOffV = kRsOffPSlot + 2 * kRsPBytes;
-constexpr int kRsEndPv = kRsOffV + 2 * kPartChunks * kChunkBytes;
-constexpr int kRsSmem = (kRsEndS > kRsEndPv ? kRsEndS : kRsEndPv) + 1024;
-static_assert(kRsOffValid >= kRsOffRescSlot + 4 && kRsOffValid + kMaxTiles * 16 <= kRsOffHdr, "low");
-static_assert(kRsOffHdr + 2 * kRsHdrBytes <= kRsOffFinal && kRsOffFinal + kHeads * 8 <= kRsOffData,
-              "headers");
-static_assert(kHeads * kOStride * 4 <= kRsEndPv - kRsOffData, "staging");
-static_assert(kRsSmem <= 232448, "shared memory");
-// tensor memory: score CTA -- S tile, then Q (576 bf16 = 288 columns); PV CTA -- O
-constexpr uint32_t kRsColS = 0, kRsColQ = 128, kRsColsS = 512;
-constexpr uint32_t kRsColO = 0, kRsColsPv = 256;
-
-// Remote mbarrier arrive (release at cluster scope) on a peer CTA's barrier.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// Bulk copy from this CTA's shared memory to a peer's, completing on the
-// peer's barrier (both cluster addresses; 16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_s2peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
-                                            uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];" ::"r"(dst_cluster),
-      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
-
-// ---- score CTA roles ----
-
-__device__ void rs_k_producer(const CUtensorMap* tk, const Fp8TcParams& p, int unit, int t0,
-                              int nt, uint8_t* sm, uint64_t* bars, volatile int* abort_flag) {
-  tc05::prefetch_tmap(tk);
-  // tiles [0, jend) fully requested, and chunks [0, cpart) of tile jend
-  int jend = nt, cpart = 0;
-  for (int j = 0; j < nt && jend == nt; ++j) {
-    for (int c = 0; c < kChunks; ++c) {
-      if (j > 0 && !wait_or_abort(&bars[kRbEmptyK + c], (j - 1) & 1, abort_flag, p.err_word)) {
-        jend = j;
-        cpart = c;
-        break;
-      }
-      mbar_arrive_expect_tx(&bars[kRbFullK + c], kChunkBytes);
-      tc05::tma_load3(sm + kRsOffRing + c * kChunkBytes, tk, 64 * c, (t0 + j) * kKeys, unit,
-                      &bars[kRbFullK + c]);
-    }
-  }
-  // no copy may still be landing when the CTA exits: each chunk's last request
-  for (int c = 0; c < kChunks; ++c) {
-    const int last = c < cpart ? jend : jend - 1;
-    if (last >= 0) mbar_wait(&bars[kRbFullK + c], last & 1);
-  }
-}
-
-__device__ void rs_score_lane(const Fp8TcParams& p, int nt, uint8_t* sm, uint64_t* bars,
-                              uint32_t tmem, volatile int* abort_flag) {
-  constexpr uint32_t id_s = tc05::idesc_f16(kHeads, kKeys, true, false, false);
-  const uint64_t dK = tc05::sw128_desc(smem_u32(sm + kRsOffRing), 16, 1024);
-  bool ok = wait_or_abort(&bars[kRbQ], 0, abort_flag, p.err_word);
-  for (int j = 0; ok && j < nt; ++j) {
-    // the previous tile's scores must have left the tensor memory
-    if (j > 0 && !wait_or_abort(&bars[kRbSFree], (j - 1) & 1, abort_flag, p.err_word)) break;
-    for (int c = 0; c < kChunks; ++c) {
-      if (!wait_or_abort(&bars[kRbFullK + c], j & 1, abort_flag, p.err_word)) {
-        ok = false;
-        break;
-      }
-      tc05::fence_after_sync();
-      const uint64_t b0 = dK + ((static_cast<uint32_t>(c) * kChunkBytes) >> 4);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc05::mma_ts(tmem + kRsColS, tmem + kRsColQ + 8 * (4 * c + kk), b0 + kk * 2, id_s,
-                     (c > 0 || kk > 0) ? 1u : 0u);
-      tc05::commit(&bars[kRbEmptyK + c]);
-    }
-    if (!ok) break;
-    tc05::commit(&bars[kRbSFull]);
-  }
-  drain_lane(&bars[kRbDrain]);
-}
-
-// Copies each P slot (and its header) to the three PV CTAs once the softmax
-// warps have written it and every PV CTA has freed that slot; at the end the
-// (max, sum) rows.
-__device__ void rs_sender(const Fp8TcParams& p, int nt, uint8_t* sm, uint64_t* bars,
-                          volatile int* abort_flag) {
-  const uint32_t bar0 = smem_u32(bars);
-  for (int j = 0; j < nt; ++j) {
-    const int s = j & 1;
-    if (!wait_or_abort(&bars[kRbPLocal + s], (j >> 1) & 1, abort_flag, p.err_word)) break;
-    if (j >= 2 && !wait_or_abort(&bars[kRbPEmpty + s], ((j - 2) >> 1) & 1, abort_flag, p.err_word))
-      break;
-    for (uint32_t r = 1; r < kRsCtas; ++r) {
-      const uint32_t bar = map_rank(bar0 + 8u * (kRbPFull + s), r);
-      bulk_s2peer(map_rank(smem_u32(sm + kRsOffPSlot + s * kRsPBytes), r),
-                  sm + kRsOffP + s * kRsPBytes, kRsPBytes, bar);
-      bulk_s2peer(map_rank(smem_u32(sm + kRsOffHdr + s * kRsHdrBytes), r),
-                  sm + kRsOffHdr + s * kRsHdrBytes, kRsHdrBytes, bar);
-    }
-    tc05::bulk_commit_group();
-    tc05::bulk_wait_group_read0();  // the local slot may be written again
-    mbar_arrive(&bars[kRbLocalFree + s]);
-  }
-  if (wait_or_abort(&bars[kRbFinLocal], 0, abort_flag, p.err_word)) {
-    for (uint32_t r = 1; r < kRsCtas; ++r)
-      bulk_s2peer(map_rank(smem_u32(sm + kRsOffFinal), r), sm + kRsOffFinal, kHeads * 8,
-                  map_rank(bar0 + 8u * kRbFinal, r));
-    tc05::bulk_commit_group();
-  }
-  tc05::bulk_wait_group0();
-}
-
-// Softmax warps of the score CTA (warps 4-7; thread r = head r = TMEM lane r).
-template <bool kCap>
-__device__ void rs_softmax(const Fp8TcParams& p, int unit, int hb, int split, int nt,
-                           const uint32_t* valid, uint8_t* sm, uint64_t* bars, uint32_t tmem,
-                           volatile int* abort_flag) {
-  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
-  const int quarter = warp & 3;
-  const int row = quarter * 32 + lane;
-  const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-  float m_run = SA_NEG_INF, l_run = 0.0f;
-  bool ok = true;
-  for (int j = 0; j < nt; ++j) {
-    const int s = j & 1;
-    if (!wait_or_abort_warp(&bars[kRbSFull], j & 1, abort_flag, p.err_word)) {
-      ok = false;
-      break;
-    }
-    tc05::fence_after_sync();
-    uint32_t sc[4][32];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) tc05::tmem_ld32(tl + kRsColS + 32 * k, sc[k]);
-    tc05::tmem_ld_wait();
-    tc05::fence_before_sync();
-    mbar_arrive(&bars[kRbSFree]);  // the next tile's score MMAs may start
-    const uint4 vm = reinterpret_cast<const uint4*>(valid)[j];
-    const uint32_t vw[4] = {vm.x, vm.y, vm.z, vm.w};
-    float mx = SA_NEG_INF;
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if ((vw[k] >> i) & 1u) mx = fmaxf(mx, __uint_as_float(sc[k][i]));
-    const float mt = mx == SA_NEG_INF ? SA_NEG_INF : logit2<kCap>(mx, p);
-    float alpha = 1.0f;
-    if (mt > m_run + kRescaleLog2) {  // also the first finite maximum
-      alpha = ex2(m_run - mt);
-      m_run = mt;
-    }
-    const float mu = m_run == SA_NEG_INF ? 0.0f : m_run;
-    // the local P slot must have been copied out (tile j - 2)
-    if (j >= 2 && !wait_or_abort_warp(&bars[kRbLocalFree + s], ((j - 2) >> 1) & 1, abort_flag,
-                                      p.err_word)) {
-      ok = false;
-      break;
-    }
-    uint8_t* prow = sm + kRsOffP + s * kRsPBytes + row * 128;
-    float ls = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      // keys 32k .. 32k + 31: slab k / 2, 16-byte chunks 4 (k % 2) .. + 3
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i0 = 8 * q + 2 * e;
-          float p0 = ex2(logit2<kCap>(__uint_as_float(sc[k][i0]), p) - mu);
-          float p1 = ex2(logit2<kCap>(__uint_as_float(sc[k][i0 + 1]), p) - mu);
-          if (!((vw[k] >> i0) & 1u)) p0 = 0.0f;
-          if (!((vw[k] >> (i0 + 1)) & 1u)) p1 = 0.0f;
-          ls += p0 + p1;
-          w[e] = pack2<__nv_bfloat16>(p0, p1);
-        }
-        const int chunk = 4 * (k & 1) + q;
-        *reinterpret_cast<uint4*>(prow + (k >> 1) * kChunkBytes + ((chunk ^ (row & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-    float* hdr = reinterpret_cast<float*>(sm + kRsOffHdr + s * kRsHdrBytes);
-    hdr[row] = alpha;
-    const bool any = __any_sync(0xffffffffu, alpha != 1.0f);
-    if (lane == 0) reinterpret_cast<uint32_t*>(hdr + kHeads)[quarter] = any ? 1u : 0u;
-    l_run = l_run * alpha + ls;
-    fence_proxy_async_smem();  // the bulk copies read these through the async proxy
-    mbar_arrive(&bars[kRbPLocal + s]);
-  }
-  // (max, sum) of the head: to the PV CTAs, and to the combine for key splits
-  float2* fin = reinterpret_cast<float2*>(sm + kRsOffFinal);
-  const float m_out = ok ? m_run : SA_NEG_INF, l_out = ok ? l_run : 0.0f;
-  fin[row] = make_float2(m_out, l_out);
-  fence_proxy_async_smem();
-  mbar_arrive(&bars[kRbFinLocal]);
-  if (p.splits > 1) {
-    const int h = hb * kHeads + row;
-    const int64_t pidx = (static_cast<int64_t>(unit) * p.splits + split) * p.Hq + h;
-    p.part_ml[2 * pidx] = m_out;
-    p.part_ml[2 * pidx + 1] = l_out;
-  }
-}
-
-// ---- PV CTA roles ----
-
-__device__ void rs_v_producer(const CUtensorMap* tk, const Fp8TcParams& p, int unit, int t0,
-                              int nt, int part, uint8_t* sm, uint64_t* bars,
-                              volatile int* abort_flag) {
-  tc05::prefetch_tmap(tk);
-  int issued = 0;
-  for (int j = 0; j < nt; ++j) {
-    const int s = j & 1;
-    if (j >= 2 && !wait_or_abort(&bars[kRbPvDone + s], ((j - 2) >> 1) & 1, abort_flag, p.err_word))
-      break;
-    mbar_arrive_expect_tx(&bars[kRbVFull + s], kPartChunks * kChunkBytes);
-    for (int k = 0; k < kPartChunks; ++k)
-      tc05::tma_load3(sm + kRsOffV + (s * kPartChunks + k) * kChunkBytes, tk,
-                      64 * (part * kPartChunks + k), (t0 + j) * kKeys, unit, &bars[kRbVFull + s]);
-    issued = j + 1;
-  }
-  for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-    mbar_wait(&bars[kRbVFull + (j & 1)], (j >> 1) & 1);
-}
-
-// O[:, 0 .. 192) += P_j V_j, one N = 192 MMA per 16 keys; P from the slot's
-// two K-major slabs, V MN-major (the three chunks of the tile, 16 KB apart).
-__device__ void rs_pv_lane(const Fp8TcParams& p, int nt, uint8_t* sm, uint64_t* bars,
-                           uint32_t tmem, volatile int* abort_flag) {
-  constexpr uint32_t id_o = tc05::idesc_f16(kHeads, kPartDims, true, false, true);
-  volatile int* resc_slot = reinterpret_cast<volatile int*>(sm + kRsOffRescSlot);
-  int rescales = 0;
-  for (int s = 0; s < 2 && s < nt; ++s)  // the first phase of each P slot
-    mbar_arrive_expect_tx(&bars[kRbPFull + s], kRsPBytes + kRsHdrBytes);
-  for (int j = 0; j < nt; ++j) {
-    const int s = j & 1;
-    if (!wait_or_abort(&bars[kRbPFull + s], (j >> 1) & 1, abort_flag, p.err_word)) break;
-    if (j + 2 < nt) mbar_arrive_expect_tx(&bars[kRbPFull + s], kRsPBytes + kRsHdrBytes);
-    const uint32_t* flags =
-        reinterpret_cast<const uint32_t*>(sm + kRsOffHdr + s * kRsHdrBytes + kHeads * 4);
-    if (j > 0 && (flags[0] | flags[1] | flags[2] | flags[3])) {
-      // O is rescaled once the previous tile's MMAs have landed in it
-      if (!wait_or_abort(&bars[kRbPvDone + (s ^ 1)], ((j - 1) >> 1) & 1, abort_flag, p.err_word))
-        break;
-      *resc_slot = s;
-      mbar_arrive(&bars[kRbResc]);
-      if (!wait_or_abort(&bars[kRbRescDone], rescales & 1, abort_flag, p.err_word)) break;
-      ++rescales;
-    }
-    if (!wait_or_abort(&bars[kRbVFull + s], (j >> 1) & 1, abort_flag, p.err_word)) break;
-    tc05::fence_after_sync();
-    const uint64_t dP = tc05::sw128_desc(smem_u32(sm + kRsOffPSlot + s * kRsPBytes), 16, 1024);
-    const uint64_t dV = tc05::sw128_desc(smem_u32(sm + kRsOffV + s * kPartChunks * kChunkBytes),
-                                         kChunkBytes, 1024);
-#pragma unroll
-    for (int ks = 0; ks < kKeys / 16; ++ks)
-      tc05::mma_ss(tmem + kRsColO,
-                   dP + (((ks >> 2) * kChunkBytes + (ks & 3) * 32) >> 4),
-                   dV + ((ks * 2048) >> 4), id_o, (j > 0 || ks > 0) ? 1u : 0u);
-    tc05::commit(&bars[kRbPvDone + s]);
-  }
-  *resc_slot = -1;  // the rescale warps' end marker
-  mbar_arrive(&bars[kRbResc]);
-  drain_lane(&bars[kRbDrain]);
-}
-
-// Frees each P slot in the score CTA once this CTA's MMAs on it are done.
-__device__ void rs_relay(const Fp8TcParams& p, int nt, uint64_t* bars, volatile int* abort_flag) {
-  const uint32_t bar0 = smem_u32(bars);
-  for (int j = 0; j + 2 < nt; ++j) {  // slots of the last two tiles are never refilled
-    const int s = j & 1;
-    if (!wait_or_abort(&bars[kRbPvDone + s], (j >> 1) & 1, abort_flag, p.err_word)) break;
-    mbar_arrive_remote(map_rank(bar0 + 8u * (kRbPEmpty + s), 0));
-  }
-}
-
-// PV warps 4-7 (thread r = head r): rescale O on request, then the epilogue.
-__device__ void rs_pv_rows(const Fp8TcParams& p, int unit, int hb, int split, int nt, int part,
-                           uint8_t* sm, uint64_t* bars, uint32_t tmem, volatile int* abort_flag) {
-  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
-  const int quarter = warp & 3;
-  const int row = quarter * 32 + lane;
-  const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-  volatile int* resc_slot = reinterpret_cast<volatile int*>(sm + kRsOffRescSlot);
-  bool ok = true;
-  for (int n = 0;; ++n) {
-    if (!wait_or_abort_warp(&bars[kRbResc], n & 1, abort_flag, p.err_word)) {
-      ok = false;
-      break;
-    }
-    const int s = *resc_slot;
-    if (s < 0) break;
-    tc05::fence_after_sync();
-    const float alpha = reinterpret_cast<const float*>(sm + kRsOffHdr + s * kRsHdrBytes)[row];
-    if (__any_sync(0xffffffffu, alpha != 1.0f)) rescale_o(tl + kRsColO, alpha);
-    tc05::fence_before_sync();
-    mbar_arrive(&bars[kRbRescDone]);
-  }
-  // the head's (max, sum) and the last tile's MMAs
-  bool have = ok && wait_or_abort_warp(&bars[kRbFinal], 0, abort_flag, p.err_word);
-  if (have && nt > 0)
-    have = wait_or_abort_warp(&bars[kRbPvDone + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag,
-                              p.err_word);
-  if (have) tc05::fence_after_sync();
-  const float2 ml = have ? reinterpret_cast<const float2*>(sm + kRsOffFinal)[row]
-                         : make_float2(SA_NEG_INF, 0.0f);
-  const bool any_tile = have && nt > 0 && ml.x != SA_NEG_INF;
-  const int h = hb * kHeads + row;
-  const int b = unit / p.Sq, i = unit % p.Sq;
-  float* orow = reinterpret_cast<float*>(sm + kRsOffData) + row * kOStride;  // staging
-  if (p.splits == 1) {
-    float L = ml.y;
-    if (p.sink && ml.x != SA_NEG_INF) L += ex2(p.sink[h] * kLog2e - ml.x);
-    const float inv = (!any_tile || L == 0.0f) ? 0.0f : 1.0f / L;
-    uint32_t* yrow = reinterpret_cast<uint32_t*>(orow);
-#pragma unroll 1
-    for (int c = 0; c < kPartDims / 32; ++c) {
-      uint32_t o[32];
-      if (any_tile) {
-        tc05::tmem_ld32(tl + kRsColO + c * 32, o);
-        tc05::tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w[e] = pack2<__nv_bfloat16>(__uint_as_float(o[8 * q + 2 * e]) * inv,
-                                      __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
-        *reinterpret_cast<uint4*>(yrow + c * 16 + 4 * q) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-    fence_proxy_async_smem();
-    tc05::bulk_s2g(static_cast<__nv_bfloat16*>(p.y) +
-                       ((static_cast<int64_t>(b) * p.Hq + h) * p.Sq + i) * kD + part * kPartDims,
-                   yrow, kPartDims * 2);
-    tc05::bulk_commit_group();
-    tc05::bulk_wait_group_read0();
-    return;
-  }
-#pragma unroll 1
-  for (int c = 0; c < kPartDims / 32; ++c) {
-    uint32_t o[32];
-    if (any_tile) {
-      tc05::tmem_ld32(tl + kRsColO + c * 32, o);
-      tc05::tmem_ld_wait();
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = 0u;
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      *reinterpret_cast<uint4*>(orow + c * 32 + 4 * q) =
-          make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-  }
-  const int64_t pidx = (static_cast<int64_t>(unit) * p.splits + split) * p.Hq + h;
-  fence_proxy_async_smem();
-  tc05::bulk_s2g(p.part_o + pidx * kD + part * kPartDims, orow, kPartDims * 4);
-  tc05::bulk_commit_group();
-  tc05::bulk_wait_group_read0();
-}
-
-}  // namespace
-
-// One cluster of four CTAs per (unit, 128-head block, key split):
-// blockIdx.x = ((unit * hblocks + hb) * splits + split) * 4 + rank.
-template <bool kCap>
-__global__ void __launch_bounds__(kThreads, 1)
-    fp8_rs_kernel(const __grid_constant__ CUtensorMap tk, const Fp8TcParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kRsOffTmem);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kRsOffAbort);
-  uint32_t* valid = reinterpret_cast<uint32_t*>(sm + kRsOffValid);
-  const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
-  const int rank = static_cast<int>(cluster_rank());
-  int cl = static_cast<int>(blockIdx.x) / kRsCtas;
-  const int split = cl % p.splits;
-  cl /= p.splits;
-  const int hb = cl % p.hblocks;
-  const int unit = cl / p.hblocks;
-  const int t0 = split * p.chunk_tiles;
-  int nt = p.tiles - t0;
-  if (nt > p.chunk_tiles) nt = p.chunk_tiles;  // chunk_tiles <= kMaxTiles (host)
-  if (nt < 0) nt = 0;
-  const bool score = rank == 0;
-  const uint32_t cols = score ? kRsColsS : kRsColsPv;
-
-  if (warp == 1) {
-    tc05::tmem_alloc(tslot, cols);
-    tc05::tmem_relinquish();
-  }
-  if (threadIdx.x == 0) {
-    if (score) {
-      mbar_init(&bars[kRbQ], kHeads);
-      for (int c = 0; c < kRsRing; ++c) {
-        mbar_init(&bars[kRbFullK + c], 1);
-        mbar_init(&bars[kRbEmptyK + c], 1);
-      }
-      mbar_init(&bars[kRbSFull], 1);
-      mbar_init(&bars[kRbSFree], kHeads);
-      for (int s = 0; s < 2; ++s) {
-        mbar_init(&bars[kRbPLocal + s], kHeads);
-        mbar_init(&bars[kRbLocalFree + s], 1);
-        mbar_init(&bars[kRbPEmpty + s], kRsCtas - 1);
-      }
-      mbar_init(&bars[kRbFinLocal], kHeads);
-    } else {
-      for (int s = 0; s < 2; ++s) {
-        mbar_init(&bars[kRbVFull + s], 1);
-        mbar_init(&bars[kRbPFull + s], 1);
-        mbar_init(&bars[kRbPvDone + s], 1);
-      }
-      mbar_init(&bars[kRbResc], 1);
-      mbar_init(&bars[kRbRescDone], kHeads);
-      mbar_init(&bars[kRbFinal], 1);
-    }
-    mbar_init(&bars[kRbDrain], 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  tc05::fence_after_sync();
-  const uint32_t tmem = *tslot;
-  if (!score && threadIdx.x == 0)  // the (max, sum) rows arrive by one copy
-    mbar_arrive_expect_tx(&bars[kRbFinal], kHeads * 8);
-  // Q -> tensor memory (an input of the call: before waiting for the decode)
-  if (score && warp >= kWarpSoftmax) {
-    const int quarter = warp & 3, row = quarter * 32 + lane;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int b = unit / p.Sq, i = unit % p.Sq;
-    const uint4* qrow = reinterpret_cast<const uint4*>(
-        static_cast<const __nv_bfloat16*>(p.q) +
-        ((static_cast<int64_t>(b) * p.Hq + hb * kHeads + row) * p.Sq + i) * kD);
-#pragma unroll 1
-    for (int c = 0; c < kD / 64; ++c) {  // 32 columns = 64 bf16 per store
-      uint32_t w[32];
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const uint4 x = __ldg(qrow + 8 * c + v);
-        w[4 * v] = x.x;
-        w[4 * v + 1] = x.y;
-        w[4 * v + 2] = x.z;
-        w[4 * v + 3] = x.w;
-      }
-      tc05::tmem_st32(tl + kRsColQ + 32 * c, w);
-    }
-    tc05::tmem_st_wait();
-    tc05::fence_before_sync();
-    mbar_arrive(&bars[kRbQ]);
-  }
-  cluster_sync();  // every CTA's barriers exist before any peer uses them
-  pdl_wait();      // the planned positions and the decoded keys
-  if (score) {
-    const int32_t* prow = p.pos + static_cast<int64_t>(unit) * p.n_cand_pad +
-                          static_cast<int64_t>(t0) * kKeys;
-    for (int w = warp; w < 4 * nt; w += kThreads / 32) {
-      const uint32_t m = __ballot_sync(0xffffffffu, __ldg(prow + 32 * w + lane) >= 0);
-      if (lane == 0) valid[w] = m;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      if (lane == 0) rs_k_producer(&tk, p, unit, t0, nt, sm, bars, abort_flag);
-    } else if (warp == 1) {
-      if (lane == 0) rs_score_lane(p, nt, sm, bars, tmem, abort_flag);
-    } else if (warp == 3) {
-      if (lane == 0) rs_sender(p, nt, sm, bars, abort_flag);
-    } else if (warp >= kWarpSoftmax) {
-      rs_softmax<kCap>(p, unit, hb, split, nt, valid, sm, bars, tmem, abort_flag);
-    }
-  } else {
-    const int part = rank - 1;
-    if (warp == 0) {
-      if (lane == 0) rs_v_producer(&tk, p, unit, t0, nt, part, sm, bars, abort_flag);
-    } else if (warp == 1) {
-      if (lane == 0) rs_pv_lane(p, nt, sm, bars, tmem, abort_flag);
-    } else if (warp == 2) {
-      if (lane == 0) rs_relay(p, nt, bars, abort_flag);
-    } else if (warp >= kWarpSoftmax) {
-      rs_pv_rows(p, unit, hb, split, nt, part, sm, bars, tmem, abort_flag);
-    }
-  }
-  pdl_launch_dependents();
-  tc05::fence_before_sync();
-  __syncwarp();
-  cluster_sync();  // no CTA leaves while a peer may still copy into or signal it
-  if (warp == 1) {
-    tc05::fence_after_sync();
-    tc05::tmem_dealloc(tmem, cols);
-  }
-}
-
 // ---- host side -----------------------------------------------------------------------------
 
 int fp8_tc_max_tiles() { return kMaxTiles; }
@@ -1481,41 +933,9 @@ bool fp8_tc_cluster_merge(int64_t splits, int64_t blocks) {
   return max_active_clusters(static_cast<int>(splits)) >= blocks;
 }
 
-template <bool kCap>
-static bool set_smem_rs() {
-  return cudaFuncSetAttribute(fp8_rs_kernel<kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kRsSmem) == cudaSuccess &&
-         cudaFuncSetAttribute(fp8_rs_kernel<kCap>, cudaFuncAttributeNonPortableClusterSizeAllowed,
-                              0) == cudaSuccess;
-}
-
-int fp8_rs_max_clusters() {
-  static std::once_flag once;
-  static int n = 0;
-  std::call_once(once, [] {
-    if (!set_smem_rs<false>() || !set_smem_rs<true>()) return;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kRsCtas);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kRsSmem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kRsCtas;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, fp8_rs_kernel<false>, &cfg) == cudaSuccess) n = c;
-    cudaGetLastError();  // a refused query leaves no sticky error behind
-  });
-  return n;
-}
-
 int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   if (!fp8_tc_supported(g) || !g.fp8_kdec) return -1;
-  const bool cluster =
-      !g.fp8_rs && fp8_tc_cluster_merge(g.splits, g.units * (g.Hq / kHeads) * kParts);
+  const bool cluster = fp8_tc_cluster_merge(g.splits, g.units * (g.Hq / kHeads) * kParts);
   if (g.splits > 1 && !cluster && (!g.part_o || !g.part_ml)) return -1;
   if (g.n_cand_pad % kKeys != 0 || g.chunk > kMaxTiles || g.chunk < 1) return -1;
   const int64_t rows = g.units * g.n_cand_pad;
@@ -1565,7 +985,6 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   if (!bf16_map(&tq, g.q, qdims, qstr, qbox) || !bf16_map(&tk, g.fp8_kdec, kdims, kstr, kbox))
     return -1;
   Fp8TcParams p;
-  p.q = g.q;
   p.pos = g.pos;
   p.n_cand_pad = g.n_cand_pad;
   p.y = g.y;
@@ -1585,17 +1004,6 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   const float log2e = 1.4426950408889634f;
   p.k1 = g.softcap != 0.0f ? (g.scale_log2 / log2e) * g.inv_softcap : 0.0f;
   p.c_log2 = g.softcap * log2e;
-  if (g.fp8_rs) {
-    const unsigned grid = static_cast<unsigned>(g.units * p.hblocks * g.splits * kRsCtas);
-    if (!(g.softcap != 0.0f ? set_smem_rs<true>() : set_smem_rs<false>())) return -1;
-    mark_event(g.ev_before, st);
-    const int rc =
-        g.softcap != 0.0f
-            ? launch_pdl(fp8_rs_kernel<true>, grid, kThreads, kRsSmem, st, kRsCtas, tk, p)
-            : launch_pdl(fp8_rs_kernel<false>, grid, kThreads, kRsSmem, st, kRsCtas, tk, p);
-    mark_event(g.ev_after, st);
-    return rc;
-  }
   const unsigned grid = static_cast<unsigned>(g.units * p.hblocks * kParts * g.splits);
   const unsigned cl = cluster ? static_cast<unsigned>(g.splits) : 1u;
   if (!(g.softcap != 0.0f ? set_smem<true>() : set_smem<false>())) return -1;

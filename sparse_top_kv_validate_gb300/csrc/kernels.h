@@ -125,7 +125,6 @@ struct GatherArgs {
   int fp8_after_plan;         //   and the plan kernel (validation only) runs just before it
   int row_copies;             // stream kernel: per-row bulk copies, no tensor maps
   int fp8_warp_mma;           // FP8 records: the warp-level MMA kernel only
-  int fp8_rs;                 // tcgen05 FP8 path: the role-split attention kernel
   void* ev_before;            // nullable cudaEvent_t pair recorded around the dominant kernel
   void* ev_after;
   // math
@@ -159,9 +158,6 @@ size_t fp8_tc_decoded_row_bytes();
 // CTAs per output block, `blocks` such clusters resident at once); otherwise
 // partials for launch_combine.
 bool fp8_tc_cluster_merge(int64_t splits, int64_t blocks);
-// Clusters of the role-split attention kernel (a score CTA and three output
-// CTAs per (unit, head block, key split)) resident at once; 0 if it cannot run.
-int fp8_rs_max_clusters();
 int launch_fp8_tc(const GatherArgs& a, cudaStream_t st);
 // Merge of the units the stream kernel split across warps.
 int launch_stream_combine(const GatherArgs& a, int dtype, cudaStream_t st);

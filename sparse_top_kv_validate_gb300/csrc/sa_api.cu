@@ -153,15 +153,11 @@ int plan_fp8(Plan& pl) {
   pl.fp8_tc = sa::fp8_tc_supported(g);
   const int64_t sms = device_shape().sms > 0 ? device_shape().sms : 152;
   if (pl.fp8_tc) {
-    // 128-key tiles; one CTA per SM.  Role split: a cluster of four CTAs (scores
-    // + three output parts) per (unit, 128-head block, split), as many clusters
-    // as can be resident at once; otherwise three dim-part CTAs per block.
+    // 128-key tiles; (unit, 128-head block, split) x 3 dim parts, one CTA per SM
     g.tiles_per_unit = (g.n_cand + 127) / 128;
     g.n_cand_pad = g.tiles_per_unit * 128;
-    const int rs_clusters = g.fp8_rs ? sa::fp8_rs_max_clusters() : 0;
-    g.fp8_rs = rs_clusters > 0 ? 1 : 0;
-    const int64_t blocks = g.units * (g.Hq / 128) * (g.fp8_rs ? 1 : 3);
-    int64_t splits = (g.fp8_rs ? rs_clusters : sms) / (blocks > 0 ? blocks : 1);
+    const int64_t blocks = g.units * (g.Hq / 128) * 3;
+    int64_t splits = sms / (blocks > 0 ? blocks : 1);
     const int64_t min_splits = (g.tiles_per_unit + sa::fp8_tc_max_tiles() - 1) / sa::fp8_tc_max_tiles();
     if (splits < min_splits) splits = min_splits;
     if (splits < 1) splits = 1;
@@ -188,8 +184,7 @@ int plan_fp8(Plan& pl) {
   size_t off = 0;
   pl.off_pos = off;
   off += align_up(static_cast<size_t>(irows * g.n_cand_pad) * sizeof(int32_t));
-  pl.fp8_combine = g.splits > 1 && !(pl.fp8_tc && !g.fp8_rs &&
-                                      sa::fp8_tc_cluster_merge(g.splits, g.units * (g.Hq / 128) * 3));
+  pl.fp8_combine = g.splits > 1 && !(pl.fp8_tc && sa::fp8_tc_cluster_merge(g.splits, g.units * (g.Hq / 128) * 3));
   if (pl.fp8_combine) {
     const size_t parts = static_cast<size_t>(g.units * g.splits * g.hpu);
     pl.off_part_o = off;
@@ -299,8 +294,7 @@ bool bias_strides(const sa_sparse_params* p, int64_t st[4]) {
 // `query` = 1 for a workspace-size query, which needs no output pointer.
 int check_sparse(const sa_sparse_params* p, int query = 0) {
   if (!p || !p->q || !p->k_cache || (!p->y && !query)) return SA_ERR_NULL;
-  if (p->reserved_ != 0 ||
-      (p->options & ~(SA_OPT_ROW_COPIES | SA_OPT_FP8_WARP_MMA | SA_OPT_FP8_DIM_PARTS)))
+  if (p->reserved_ != 0 || (p->options & ~(SA_OPT_ROW_COPIES | SA_OPT_FP8_WARP_MMA)))
     return SA_ERR_UNSUPPORTED;
   if (p->bias) {
     int64_t st[4];
@@ -374,7 +368,6 @@ int sparse_plan(const sa_sparse_params* p, Plan& pl) {
   }
   g.row_copies = (p->options & SA_OPT_ROW_COPIES) ? 1 : 0;
   g.fp8_warp_mma = (p->options & SA_OPT_FP8_WARP_MMA) ? 1 : 0;
-  g.fp8_rs = (p->options & SA_OPT_FP8_DIM_PARTS) ? 0 : 1;  // narrowed by plan_fp8
   g.B = p->B;
   g.Hq = p->Hq;
   g.Hkv = p->Hkv;

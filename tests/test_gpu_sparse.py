@@ -583,42 +583,3 @@ def test_full_size_fp8_sampled_rows(cuda_lib):
                                       records=inp["kv_records"][b:b + 1].cpu(), n_rope=c.n_rope,
                                       scale=c.eff_scale(), window=c.window, rows=heads)
         assert_close(to64(y[b, heads]), ref, y.dtype, f"fp8 full b={b}")
-
-
-# The same requests on the dim-part tensor-core kernel (SA_OPT_FP8_DIM_PARTS:
-# three CTAs that each compute the scores and own a third of the output dims)
-# and, by default, on the role-split kernel (one score CTA feeding three output
-# CTAs of a cluster): both against the oracle, and against each other.
-@pytest.mark.parametrize("over", [dict(Hq=128), dict(Hq=256, B=1, T=4000, K=900),
-                                  dict(Hq=128, B=16, T=3000, K=1000),
-                                  dict(Hq=128, B=1, T=30000, K=6000)])
-def test_fp8_tc05_both_kernels_match_oracle(cuda_lib, over):
-    c = _fp8_case(**over)
-    inp = synth.make_sparse_inputs(c, seed=101)
-    rows = list(range(0, c.B * c.Hq, 3))
-    ref = oracle.sparse_attention(inp["q"], inp["idx"], records=inp["kv_records"],
-                                  n_rope=c.n_rope, scale=c.eff_scale(), window=c.window,
-                                  rows=rows)
-    ys = []
-    for opt in (0, cuda_lib.OPT_FP8_DIM_PARTS):
-        err = torch.zeros(1, dtype=torch.int32, device=DEV)
-        y = _run_fp8(cuda_lib, c, inp, err_word=err, options=opt)
-        torch.cuda.synchronize()
-        assert int(err.item()) == 0, f"options {opt}: err_word {int(err.item())}"
-        assert_close(to64(y.reshape(-1, c.D)[rows]), ref, y.dtype, f"fp8 tc05 {over} opt {opt}")
-        ys.append(y)
-    assert_close(to64(ys[0]), to64(ys[1]), ys[0].dtype, f"fp8 kernels agree {over}")
-
-
-def test_fp8_tc05_dim_parts_options_softcap_sink(cuda_lib):
-    c = _fp8_case(B=2, Hq=128, T=2500, K=400)
-    inp = synth.make_sparse_inputs(c, seed=102)
-    sink = torch.linspace(-2.0, 1.0, c.Hq, dtype=torch.float32)
-    for softcap in (0.0, 4.0):
-        y = _run_fp8(cuda_lib, c, inp, softcap=softcap, sink=sink.to(DEV),
-                     options=cuda_lib.OPT_FP8_DIM_PARTS)
-        torch.cuda.synchronize()
-        ref = oracle.sparse_attention(inp["q"], inp["idx"], records=inp["kv_records"],
-                                      n_rope=c.n_rope, scale=c.eff_scale(), window=c.window,
-                                      softcap=softcap, sink=sink.double())
-        assert_close(to64(y), ref, y.dtype, f"fp8 dim parts softcap={softcap}")
