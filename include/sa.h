@@ -114,10 +114,35 @@ int sa_version(void);
  * immediately after it, so that the events bracket that one kernel.  The
  * handles are not owned; the caller keeps them alive while the hook is set.
  * Recording between two kernels removes their launch overlap, so timings of
- * whole calls are taken with the hook off.
+ * whole calls are taken with the hook off.  Under stream capture the records
+ * become event-record nodes of the graph (cudaEventRecordExternal), so a
+ * replayed graph brackets the kernel the same way.
  * Returns SA_OK, or SA_ERR_NULL if exactly one of the two is NULL.
  */
 int sa_set_kernel_events(void* before, void* after);
+
+/*
+ * sa_check_wait_timeout -- diagnostic (no counterpart on the pages): runs the
+ * library's bounded-wait timeout path on purpose, without a fault.
+ *
+ * Every pipelined kernel waits on its shared-memory barriers for at most about
+ * 2e9 SM cycles (about one second), then ORs SA_ERRBIT_TIMEOUT into the
+ * caller's error word, sets its CTA's abort flag and returns, leaving the
+ * context usable.  A correct call never takes that path; this call makes one
+ * warp wait on a barrier that nothing arrives on (no copy or MMA in flight),
+ * then wait once more on the abort flag the first wait set.
+ *
+ * err_word: device pointer to one uint32 (zeroed by the caller), receives
+ *           SA_ERRBIT_TIMEOUT.
+ * out:      device pointer to four uint32: [0] 1 if the first wait gave up,
+ *           [1] 1 if the second returned at once, [2], [3] the first wait's
+ *           SM cycles (low, high word).
+ * stream:   cudaStream_t or NULL.  Asynchronous; about one second of device
+ *           time on one SM.
+ * Returns SA_OK, SA_ERR_NULL, SA_ERR_ALIGN (a pointer not 4-byte aligned) or
+ * SA_ERR_LAUNCH.
+ */
+int sa_check_wait_timeout(uint32_t* err_word, uint32_t* out, void* stream);
 
 /*
  * validate_indices -- [IS] validate_indices / validate_index_rows.

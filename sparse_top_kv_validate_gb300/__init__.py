@@ -21,7 +21,7 @@ import threading
 import torch
 
 __all__ = [
-    "load", "lib_path", "SAError", "status_string",
+    "load", "lib_path", "SAError", "status_string", "check_wait_timeout",
     "validate_indices", "build_present_kv", "sparse_attn_decode", "attn_prefill",
     "paged_attn_decode", "sparse_attn_decode_workspace", "attn_prefill_workspace",
     "paged_attn_decode_workspace", "new_workspace", "sparse_attn_decode_noalloc",
@@ -191,6 +191,8 @@ def load():
             fn.argtypes = [C.POINTER(CompressParams), _p]
         L.csa_pool_weight.restype = C.c_int
         L.csa_pool_weight.argtypes = [_p, _p, _i64, _p]
+        L.sa_check_wait_timeout.restype = C.c_int
+        L.sa_check_wait_timeout.argtypes = [_p, _p, _p]
         L.paged_attn_decode_workspace.restype = C.c_size_t
         L.paged_attn_decode_workspace.argtypes = [C.POINTER(PagedParams)]
         L.paged_attn_decode.restype = C.c_int
@@ -716,6 +718,17 @@ def csa_ratio4_index_compress(kv, gate, ape, norm, carry, *, n_rope, total, reco
     _compress("csa_ratio4_index_compress", 4, kv.shape[2] // 2, kv, gate, ape, norm, carry,
               n_rope=n_rope, total=total, records=records, logical=logical,
               err_word=err_word, stream=stream)
+
+
+def check_wait_timeout(device="cuda", stream=None):
+    """Runs the library's bounded-wait timeout path once (one warp waits on a
+    barrier nothing arrives on, about a second); returns ``(err_word, out)``,
+    int32 CUDA tensors of 1 and 4 entries (see ``sa_check_wait_timeout``)."""
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    out = torch.zeros(4, dtype=torch.int32, device=device)
+    _check("sa_check_wait_timeout",
+           load().sa_check_wait_timeout(err.data_ptr(), out.data_ptr(), _stream(stream)))
+    return err, out
 
 
 def csa_pool_weight(t, *, w=None, stream=None):

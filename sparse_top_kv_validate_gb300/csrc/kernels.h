@@ -153,6 +153,9 @@ int launch_fp8_decode(const GatherArgs& a, cudaStream_t st);
 // 128-key tiles, at most fp8_tc_max_tiles() tiles per key split).
 bool fp8_tc_supported(const GatherArgs& a);
 int fp8_tc_max_tiles();
+
+// One warp waits on a barrier that nothing arrives on (k_diag.cu).
+int launch_wait_timeout(uint32_t* err_word, uint32_t* out, cudaStream_t st);
 size_t fp8_tc_decoded_row_bytes();
 // Key splits that the attention kernel merges itself (a cluster of `splits`
 // CTAs per output block, `blocks` such clusters resident at once); otherwise

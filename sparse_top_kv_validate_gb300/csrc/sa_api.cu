@@ -416,6 +416,15 @@ int sa_set_kernel_events(void* before, void* after) {
   return SA_OK;
 }
 
+int sa_check_wait_timeout(uint32_t* err_word, uint32_t* out, void* stream) {
+  if (!err_word || !out) return SA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(out) % 4 || reinterpret_cast<uintptr_t>(err_word) % 4)
+    return SA_ERR_ALIGN;
+  return sa::launch_wait_timeout(err_word, out, static_cast<cudaStream_t>(stream)) == 0
+             ? SA_OK
+             : SA_ERR_LAUNCH;
+}
+
 const char* sa_status_string(int status) {
   switch (status) {
     case SA_OK: return "ok";
