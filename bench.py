@@ -641,8 +641,8 @@ class CsaRef:
                 "rope_dims": c.n_rope, "window_rows": c.L, "tokens": c.total,
                 "records": c.R, "top_k": c.topk, "record_bytes": c.stride,
                 "step": "one csa_ratio4_attention call: candidate assembly (window rows, "
-                        "FP8 record decode), tensor-core attention with sink, split merge "
-                        "-- 3 kernels"}
+                        "FP8 record decode), tcgen05 attention with sink (128-head blocks, "
+                        "two CTAs of 256 output dims), split merge -- 3 kernels"}
 
     def oracle_rows(self, rows):
         import oracle
@@ -662,8 +662,10 @@ class CsaRef:
         return np.stack(out)
 
     def roofline(self, ms, kernel_ms, peaks):
-        line = tensor_roofline("csa_attn_kernel", self.flops, kernel_ms, ms, peaks,
-                               traffic_for(self.c.name, "csa_attn_kernel"))
+        # 128-head blocks of bf16 queries run on the tcgen05 attention kernel
+        # (fp8_tc05_kernel in its 512-dim geometry)
+        line = tensor_roofline("fp8_tc05_kernel", self.flops, kernel_ms, ms, peaks,
+                               traffic_for(self.c.name, "fp8_tc05_kernel"))
         line.update(call_algorithmic_bytes=int(self.decode_bytes),
                     call_hbm_gbs=round(self.decode_bytes / (ms * 1e-3) / 1e9, 1))
         return line

@@ -19,7 +19,12 @@
 //    aligned, so a warp reads them with byte loads, a block's 64 codes in one
 //    coalesced pass), with a validity byte; the rows stay in L2 for the
 //    attention kernel.
-//  * csa_attn_kernel: CTA = (query, block of 32 heads, key split); 8 warps =
+//  * bf16 queries in blocks of 128 heads (D 512): the tcgen05 attention kernel
+//    of k_fp8_tc.cu in its 512-dim geometry reads the assembled rows by TMA in
+//    128-slot tiles (two CTAs per head block, each owning 256 output dims;
+//    the validity bytes mask the slots; the slot bias is added to the log2
+//    logits in tensor memory before the maximum is taken).
+//  * otherwise csa_attn_kernel: CTA = (query, block of 32 heads, key split); 8 warps =
 //    2 head groups of 16 x 4 quarters of the dims.  Candidate tiles of 16 rows
 //    arrive by 16-byte cp.async, double-buffered; S over each warp's quarter
 //    on the m16n8k16 tensor-core MMA (heads as M, keys as N), the quarters
@@ -445,6 +450,13 @@ static int launch_csa_t(const CsaArgs& a, cudaStream_t st) {
   csa_assemble_kernel<D><<<dim3(static_cast<unsigned>(a.c_pad / 8),
                                static_cast<unsigned>(a.B * a.S)), 256, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return -1;
+  if (a.tc) {  // the tcgen05 kernel over the same rows (k_fp8_tc.cu)
+    if (launch_csa_tc(a, st) != 0) return -1;
+    if (a.splits > 1)
+      return launch_pdl(csa_combine_kernel<D>, dim3(static_cast<unsigned>(a.B * a.S * a.H)),
+                        dim3(128), 0, st, a);
+    return 0;
+  }
   if (cudaFuncSetAttribute(csa_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            G::kSmem) != cudaSuccess)
     return -1;

@@ -40,6 +40,10 @@
 //      * Every mbarrier wait is bounded: a stalled pipeline sets
 //        SA_ERRBIT_TIMEOUT, stops every role and still frees the tensor
 //        memory.
+//  The same attention kernel, in a 512-dim geometry (eight chunks, two CTAs
+//  of 256 output dims), serves the compressed sparse attention rows that
+//  k_csa.cu assembles: validity from bytes instead of planned positions, and
+//  an optional additive bias per candidate slot (launch_csa_tc).
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -55,14 +59,10 @@ namespace sa {
 
 namespace {
 
-constexpr int kD = 576;
+constexpr int kD = 576;                  // FP8 latent record: 512 FP8 dims + 64 RoPE dims
 constexpr int kRowBytes = kD * 2;        // decoded row: 576 bf16
-constexpr int kChunks = 9;               // 64-dim chunks: 8 FP8 blocks + the RoPE tail
 constexpr int kHeads = 128;              // M of every MMA
 constexpr int kKeys = 128;               // keys per tile (N of the score MMA)
-constexpr int kParts = 3;                // CTAs sharing a head block's output dims
-constexpr int kPartChunks = kChunks / kParts;  // 64-dim output chunks per CTA
-constexpr int kPartDims = kPartChunks * 64;    // 192
 constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 bf16, 128-byte swizzled
 constexpr int kStages = 5;               // ring of key chunks
 constexpr int kWarpLoad = 0, kWarpS = 1, kWarpPv = 2, kWarpSoftmax = 4;
@@ -70,12 +70,6 @@ constexpr int kThreads = 256;
 constexpr int kMaxTiles = 48;            // tiles per CTA (validity staged in shared memory)
 constexpr int kRecRope = 8 * 65;         // byte offset of the RoPE tail in a record
 constexpr float kRescaleLog2 = 8.0f;
-
-// shared memory (bytes)
-constexpr int kOffQ = 0;                                    // 9 slabs [128 heads][64 dims]
-constexpr int kOffRing = kChunks * kChunkBytes;             // [kStages] key chunks
-constexpr int kOffValid = kOffRing + kStages * kChunkBytes; // [kMaxTiles][4] u32 bit masks
-constexpr int kOffBar = kOffValid + kMaxTiles * 16;
 // barriers: q_full, full_s[kStages], full_pv[kStages], empty[kStages],
 // s_full[2], p_full[2], pv_free[2], o_full, done[2].  A filled slot is
 // announced on full_s or full_pv by the lane that will read it: each of those
@@ -86,27 +80,55 @@ constexpr int kBarQ = 0, kBarFullS = 1, kBarFullPv = kBarFullS + kStages,
               kBarEmpty = kBarFullPv + kStages, kBarS = kBarEmpty + kStages,
               kBarP = kBarS + 2, kBarPv = kBarP + 2, kBarO = kBarPv + 2, kBarDone = kBarO + 1,
               kNumBars = kBarDone + 2;
-constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr int kOffAbort = kOffTmemSlot + 4;
-constexpr int kSmem = kOffAbort + 4 + 1024;                 // + alignment slack
-// The split merge reuses the Q area once every score MMA has completed: the
-// CTA's O rows (fp32, padded rows), its (max, sum) per row, the merge weights.
 constexpr int kMaxClusterSplits = 8;
-constexpr int kOStride = kPartDims + 4;                     // floats per O row
-constexpr int kOffMO = kOffQ;
-constexpr int kOffMMl = kOffMO + kHeads * kOStride * 4;
-constexpr int kOffMW = kOffMMl + kHeads * 8;
-static_assert(kOffMW + kHeads * kMaxClusterSplits * 4 <= kOffRing, "merge area");
-static_assert(kSmem <= 232448, "shared memory");
 // tensor memory: score buffers 0 and 1, then this CTA's output dims
 constexpr uint32_t kColS = 0, kColO = 2 * kKeys, kTmemCols = 512;
-static_assert(kColO + kPartDims <= kTmemCols, "tensor memory");
+
+// Geometry of the attention kernel for a row width D (576: the FP8 latent
+// record, three CTAs of 192 output dims per head block; 512: the compressed
+// sparse attention rows, two CTAs of 256 output dims).
+template <int D>
+struct TcGeo {
+  static constexpr int kD = D;
+  static constexpr int kChunks = D / 64;                       // 64-dim chunks of a row
+  static constexpr int kParts = D == 576 ? 3 : 2;              // CTAs sharing the output dims
+  static constexpr int kPartChunks = kChunks / kParts;         // output chunks per CTA
+  static constexpr int kPartDims = kPartChunks * 64;
+  static constexpr int kEntries = kChunks + kPartChunks;       // ring entries per tile
+  // shared memory (bytes)
+  static constexpr int kOffQ = 0;                              // kChunks slabs [128 heads][64]
+  static constexpr int kOffRing = kChunks * kChunkBytes;       // [kStages] key chunks
+  static constexpr int kOffValid = kOffRing + kStages * kChunkBytes;  // [kMaxTiles][4] masks
+  static constexpr int kOffBar = kOffValid + kMaxTiles * 16;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kSmem = kOffAbort + 4 + 1024;           // + alignment slack
+  // The epilogue and the split merge reuse the Q area and the ring once every
+  // MMA has completed: the CTA's O rows (fp32, padded rows), its (max, sum)
+  // per row, the merge weights.
+  static constexpr int kOStride = kPartDims + 4;               // floats per O row
+  static constexpr int kOffMO = kOffQ;
+  static constexpr int kOffMMl = kOffMO + kHeads * kOStride * 4;
+  static constexpr int kOffMW = kOffMMl + kHeads * 8;
+  static_assert(kChunks * 64 == D && kPartChunks * kParts == kChunks, "row geometry");
+  static_assert(kOffMW + kHeads * kMaxClusterSplits * 4 <= kOffValid, "merge area");
+  static_assert(kSmem <= 232448, "shared memory");
+  static_assert(kColO + kPartDims <= kTmemCols, "tensor memory");
+};
+using GeoFp8 = TcGeo<576>;
+using GeoCsa = TcGeo<512>;
 
 struct Fp8TcParams {
   const int32_t* pos;        // [units, n_cand_pad] planned cache positions or -1
+  const uint8_t* valid_u8;   // or, when set: [units, n_cand_pad] 1 = a valid candidate
+  // nullable additive bias of candidate slot k (natural-log units), unit = b * bias_S + s:
+  // element (b, h, s, k) at b * bias_sb + h * bias_sh + s * bias_si + k * bias_sk
+  const float* bias;
+  int64_t bias_sb, bias_sh, bias_si, bias_sk;
+  int bias_S;
   int64_t n_cand_pad;        // multiple of 128
-  void* y;                   // [B, Hq, Sq, 576] bf16
-  float* part_o;             // splits > 1: [units * splits * Hq, 576] partial outputs
+  void* y;                   // [B, Hq, Sq, D] bf16
+  float* part_o;             // splits > 1: [units * splits * Hq, D] partial outputs
   float* part_ml;            //             [units * splits * Hq, 2] (max, sum)
   const float* sink;         // nullable [Hq]
   uint32_t* err_word;
@@ -142,29 +164,33 @@ struct DecodeParams {
 // The ring's entries, in order: the nine score chunks of tile 0, then for
 // each tile j: the nine score chunks of tile j + 1 (if any) and the CTA's
 // three output chunks of tile j.
+template <class G>
 __device__ __forceinline__ uint32_t s_entry(int j, int c) {
-  return j == 0 ? static_cast<uint32_t>(c) : static_cast<uint32_t>(9 + 12 * (j - 1) + c);
+  return j == 0 ? static_cast<uint32_t>(c)
+                : static_cast<uint32_t>(G::kChunks + G::kEntries * (j - 1) + c);
 }
+template <class G>
 __device__ __forceinline__ uint32_t pv_entry(int j, int k, int nt) {
-  return static_cast<uint32_t>(9 + 12 * j + (j + 1 < nt ? 9 : 0) + k);
+  return static_cast<uint32_t>(G::kChunks + G::kEntries * j + (j + 1 < nt ? G::kChunks : 0) + k);
 }
 // Entry e -> (tile j, chunk c, read by the score lane?).
+template <class G>
 __device__ __forceinline__ void entry_of(int e, int nt, int part, int& j, int& c, bool& score) {
-  if (e < 9) {
+  if (e < G::kChunks) {
     j = 0;
     c = e;
     score = true;
     return;
   }
-  const int q = e - 9, blk = q / 12, rr = q % 12;
+  const int q = e - G::kChunks, blk = q / G::kEntries, rr = q % G::kEntries;
   const bool more = blk + 1 < nt;
-  score = more && rr < 9;
+  score = more && rr < G::kChunks;
   if (score) {
     j = blk + 1;
     c = rr;
   } else {
     j = blk;
-    c = part * kPartChunks + (rr - (more ? 9 : 0));
+    c = part * G::kPartChunks + (rr - (more ? G::kChunks : 0));
   }
 }
 
@@ -370,6 +396,7 @@ namespace {
 
 // The ring entries in order, each a 128-key x 64-dim box of the decoded buffer
 // (Q's nine slabs were requested in the prologue).
+template <class G>
 __device__ void fp8tc_producer(const CUtensorMap* tk, const Fp8TcParams& p,
                                int unit, int t0, int nt, int part, uint8_t* sm,
                                uint64_t* bars, volatile int* abort_flag) {
@@ -377,11 +404,11 @@ __device__ void fp8tc_producer(const CUtensorMap* tk, const Fp8TcParams& p,
   // per slot: armed at all, last fill read by the score lane, its parity;
   // and the parity of the next phase of full_s / full_pv
   uint32_t armed = 0, last_score = 0, last_par = 0, par_s = 0, par_pv = 0;
-  const int total = 12 * nt;
+  const int total = G::kEntries * nt;
   for (int e = 0; e < total; ++e) {
     int j, c;
     bool score;
-    entry_of(e, nt, part, j, c, score);
+    entry_of<G>(e, nt, part, j, c, score);
     const uint32_t slot = static_cast<uint32_t>(e) % kStages, use = static_cast<uint32_t>(e) / kStages;
     if (use > 0 && !wait_or_abort(&bars[kBarEmpty + slot], (use - 1) & 1, abort_flag, p.err_word))
       break;
@@ -393,7 +420,7 @@ __device__ void fp8tc_producer(const CUtensorMap* tk, const Fp8TcParams& p,
     last_par = (last_par & ~(1u << slot)) | (ph << slot);
     uint64_t* full = &bars[(score ? kBarFullS : kBarFullPv) + slot];
     mbar_arrive_expect_tx(full, kChunkBytes);
-    tc05::tma_load3(sm + kOffRing + slot * kChunkBytes, tk, 64 * c, (t0 + j) * kKeys, unit, full);
+    tc05::tma_load3(sm + G::kOffRing + slot * kChunkBytes, tk, 64 * c, (t0 + j) * kKeys, unit, full);
   }
   // no copy may still be landing when the CTA exits
   mbar_wait(&bars[kBarQ], 0);
@@ -409,11 +436,12 @@ __device__ __forceinline__ void drain_lane(uint64_t* done) {
 }
 
 // S_j = Q K_j^T into score buffer j & 1, one 64-dim chunk (4 k-steps) at a time.
+template <class G>
 __device__ void fp8tc_score_lane(const Fp8TcParams& p, int nt, uint8_t* sm, uint64_t* bars,
                                  uint32_t tmem, volatile int* abort_flag) {
   constexpr uint32_t id_s = tc05::idesc_f16(kHeads, kKeys, true, false, false);
-  const uint64_t dQ = tc05::sw128_desc(smem_u32(sm + kOffQ), 16, 1024);
-  const uint64_t dK = tc05::sw128_desc(smem_u32(sm + kOffRing), 16, 1024);
+  const uint64_t dQ = tc05::sw128_desc(smem_u32(sm + G::kOffQ), 16, 1024);
+  const uint64_t dK = tc05::sw128_desc(smem_u32(sm + G::kOffRing), 16, 1024);
   bool ok = wait_or_abort(&bars[kBarQ], 0, abort_flag, p.err_word);
   uint32_t par = 0;  // bit s: parity of the next awaited phase of full_s[s]
   for (int j = 0; ok && j < nt; ++j) {
@@ -421,8 +449,8 @@ __device__ void fp8tc_score_lane(const Fp8TcParams& p, int nt, uint8_t* sm, uint
     // the buffer's previous P (tile j - 2) must have been read by its PV
     if (j >= 2 && !wait_or_abort(&bars[kBarPv + buf], ((j - 2) >> 1) & 1, abort_flag, p.err_word))
       break;
-    for (int c = 0; c < kChunks; ++c) {
-      const uint32_t e = s_entry(j, c), slot = e % kStages;
+    for (int c = 0; c < G::kChunks; ++c) {
+      const uint32_t e = s_entry<G>(j, c), slot = e % kStages;
       if (!wait_or_abort(&bars[kBarFullS + slot], (par >> slot) & 1, abort_flag, p.err_word)) {
         ok = false;
         break;
@@ -446,18 +474,19 @@ __device__ void fp8tc_score_lane(const Fp8TcParams& p, int nt, uint8_t* sm, uint
 // O[:, 64k .. 64k + 64) += P_j V_j[:, chunk part * 3 + k] for the CTA's three
 // output chunks; P_j is the bf16 pairs over score buffer j & 1's first 64
 // columns (keys 2i, 2i + 1 in column i).
+template <class G>
 __device__ void fp8tc_pv_lane(const Fp8TcParams& p, int nt, uint8_t* sm, uint64_t* bars,
                               uint32_t tmem, volatile int* abort_flag) {
   constexpr uint32_t id_o = tc05::idesc_f16(kHeads, 64, true, false, true);
-  const uint64_t dV = tc05::sw128_desc(smem_u32(sm + kOffRing), kChunkBytes, 1024);
+  const uint64_t dV = tc05::sw128_desc(smem_u32(sm + G::kOffRing), kChunkBytes, 1024);
   bool ok = true;
   uint32_t par = 0;  // bit s: parity of the next awaited phase of full_pv[s]
   for (int j = 0; ok && j < nt; ++j) {
     const int buf = j & 1;
     if (!wait_or_abort(&bars[kBarP + buf], (j >> 1) & 1, abort_flag, p.err_word)) break;
     tc05::fence_after_sync();
-    for (int k = 0; k < kPartChunks; ++k) {
-      const uint32_t e = pv_entry(j, k, nt), slot = e % kStages;
+    for (int k = 0; k < G::kPartChunks; ++k) {
+      const uint32_t e = pv_entry<G>(j, k, nt), slot = e % kStages;
       if (!wait_or_abort(&bars[kBarFullPv + slot], (par >> slot) & 1, abort_flag, p.err_word)) {
         ok = false;
         break;
@@ -485,10 +514,11 @@ namespace {
 // ---- kernel 2 role: softmax warpgroup (warps 4-7; thread r = head r = TMEM lane r) -------
 
 // kCols columns of this thread's O row *= alpha, in tensor memory (warp-collective).
+template <class G>
 __device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
   const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-  for (int c = 0; c < kPartDims / 32; ++c) {
+  for (int c = 0; c < G::kPartDims / 32; ++c) {
     uint32_t o[32];
     tc05::tmem_ld32(tO + c * 32, o);
     tc05::tmem_ld_wait();
@@ -511,7 +541,7 @@ __device__ __forceinline__ float logit2(float s, const Fp8TcParams& p) {
   return kCap ? p.c_log2 * tanh_approx(s * p.k1) : s * p.scale_log2;
 }
 
-template <bool kCap>
+template <class G, bool kCap, bool kBias>
 __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split, int nt,
                               int part, const uint32_t* valid, uint64_t* bars, uint32_t tmem,
                               volatile int* abort_flag) {
@@ -521,6 +551,14 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
   const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   float m_run = SA_NEG_INF, l_run = 0.0f;
   bool ok = true;
+  // kBias: this head's bias row at candidate slot 0
+  const float* brow = nullptr;
+  if constexpr (kBias) {
+    const int bb = unit / p.bias_S, ss = unit % p.bias_S;
+    brow = p.bias + bb * p.bias_sb + static_cast<int64_t>(hb * kHeads + row) * p.bias_sh +
+           ss * p.bias_si;
+  }
+  const int64_t slot_t0 = static_cast<int64_t>(split) * p.chunk_tiles * kKeys;
   for (int j = 0; j < nt; ++j) {
     const int buf = j & 1;
     // validity of the tile's keys 32k + bit (kept in scalars: the loops over k
@@ -542,7 +580,19 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
       tc05::tmem_ld32(tS + 32 * k, s);
       tc05::tmem_ld_wait();
       const uint32_t vk = valid_bits(k);
-      if (vk == 0xffffffffu) {
+      if constexpr (kBias) {
+        // the biased log2 logits replace the raw scores in tensor memory
+        const float* bk = brow + (slot_t0 + j * kKeys + 32 * k) * p.bias_sk;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float x = SA_NEG_INF;
+          if ((vk >> i) & 1u)
+            x = logit2<kCap>(__uint_as_float(s[i]), p) + kLog2e * __ldg(bk + i * p.bias_sk);
+          s[i] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+        tc05::tmem_st32(tS + 32 * k, s);
+      } else if (vk == 0xffffffffu) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) mx = max3(mx, __uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
       } else {
@@ -554,8 +604,9 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
         }
       }
     }
+    if constexpr (kBias) tc05::tmem_st_wait();
     // the lazy running maximum (log2 units): raised only past 2^8
-    const float mt = mx == SA_NEG_INF ? SA_NEG_INF : logit2<kCap>(mx, p);
+    const float mt = (kBias || mx == SA_NEG_INF) ? mx : logit2<kCap>(mx, p);
     float alpha = 1.0f;
     if (mt > m_run + kRescaleLog2) {  // also the first finite maximum
       alpha = ex2(m_run - mt);
@@ -570,7 +621,7 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
         break;
       }
       tc05::fence_after_sync();
-      rescale_o(tl + kColO, alpha);
+      rescale_o<G>(tl + kColO, alpha);
     }
     // pass 2: P = 2^(logit - mu) as bf16 pairs over the buffer's first 64 columns
     float ls0 = 0.0f, ls1 = 0.0f;
@@ -583,8 +634,11 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        float p0 = ex2(logit2<kCap>(__uint_as_float(s[2 * i]), p) - mu);
-        float p1 = ex2(logit2<kCap>(__uint_as_float(s[2 * i + 1]), p) - mu);
+        const float x0 = kBias ? __uint_as_float(s[2 * i]) : logit2<kCap>(__uint_as_float(s[2 * i]), p);
+        const float x1 =
+            kBias ? __uint_as_float(s[2 * i + 1]) : logit2<kCap>(__uint_as_float(s[2 * i + 1]), p);
+        float p0 = ex2(x0 - mu);
+        float p1 = ex2(x1 - mu);
         if (!((vk >> (2 * i)) & 1u)) p0 = 0.0f;
         if (!((vk >> (2 * i + 1)) & 1u)) p1 = 0.0f;
         ls0 += p0;
@@ -609,15 +663,15 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
   const bool have = nt > 0 && ok && wait_or_abort_warp(&bars[kBarO], 0, abort_flag, p.err_word);
   if (have) tc05::fence_after_sync();
   mbar_wait(&bars[kBarQ], 0);  // (no tile at all: Q's load must have landed before its area is reused)
-  uint8_t* sm = reinterpret_cast<uint8_t*>(bars) - kOffBar;
-  float* orow = reinterpret_cast<float*>(sm + kOffMO) + row * kOStride;
+  uint8_t* sm = reinterpret_cast<uint8_t*>(bars) - G::kOffBar;
+  float* orow = reinterpret_cast<float*>(sm + G::kOffMO) + row * G::kOStride;
   if (p.splits == 1) {
     float L = l_run;
     if (p.sink && m_run != SA_NEG_INF) L += ex2(p.sink[h] * kLog2e - m_run);
     const float inv = (!have || m_run == SA_NEG_INF || L == 0.0f) ? 0.0f : 1.0f / L;
     uint32_t* yrow = reinterpret_cast<uint32_t*>(orow);  // 192 bf16 = 384 bytes
 #pragma unroll 1
-    for (int c = 0; c < kPartDims / 32; ++c) {
+    for (int c = 0; c < G::kPartDims / 32; ++c) {
       uint32_t o[32];
       if (have) {
         tc05::tmem_ld32(tl + kColO + c * 32, o);
@@ -638,15 +692,15 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
     }
     fence_proxy_async_smem();
     tc05::bulk_s2g(static_cast<__nv_bfloat16*>(p.y) +
-                       ((static_cast<int64_t>(b) * p.Hq + h) * p.Sq + i) * kD + part * kPartDims,
-                   yrow, kPartDims * 2);
+                       ((static_cast<int64_t>(b) * p.Hq + h) * p.Sq + i) * G::kD + part * G::kPartDims,
+                   yrow, G::kPartDims * 2);
     tc05::bulk_commit_group();
     tc05::bulk_wait_group_read0();
     return;
   }
   // splits > 1: the row's unnormalised O and (max, sum)
 #pragma unroll 1
-  for (int c = 0; c < kPartDims / 32; ++c) {
+  for (int c = 0; c < G::kPartDims / 32; ++c) {
     uint32_t o[32];
     if (have) {
       tc05::tmem_ld32(tl + kColO + c * 32, o);
@@ -662,14 +716,14 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
   }
   const float m_out = have ? m_run : SA_NEG_INF, l_out = have ? l_run : 0.0f;
   if (p.cluster_merge) {  // merged on chip after the cluster barrier
-    float* ml = reinterpret_cast<float*>(sm + kOffMMl);
+    float* ml = reinterpret_cast<float*>(sm + G::kOffMMl);
     ml[2 * row] = m_out;
     ml[2 * row + 1] = l_out;
     return;
   }
   const int64_t pidx = (static_cast<int64_t>(unit) * p.splits + split) * p.Hq + h;
   fence_proxy_async_smem();
-  tc05::bulk_s2g(p.part_o + pidx * kD + part * kPartDims, orow, kPartDims * 4);
+  tc05::bulk_s2g(p.part_o + pidx * G::kD + part * G::kPartDims, orow, G::kPartDims * 4);
   tc05::bulk_commit_group();
   if (part == 0) {  // the same (max, sum) in every part: the combine kernel's layout
     p.part_ml[2 * pidx] = m_out;
@@ -683,12 +737,13 @@ __device__ void fp8tc_softmax(const Fp8TcParams& p, int unit, int hb, int split,
 // part's dims, reading every CTA's staged O rows and (max, sum) through
 // distributed shared memory:
 //   y = sum_c 2^(m_c - M) O_c / (sum_c 2^(m_c - M) l_c [+ 2^(sink - M)]).
+template <class G>
 __device__ void fp8tc_cluster_merge(const Fp8TcParams& p, int unit, int hb, int part, uint8_t* sm) {
   const int C = p.splits;
   const uint32_t rank = cluster_rank();
   const int r0 = static_cast<int>(rank) * kHeads / C, r1 = (static_cast<int>(rank) + 1) * kHeads / C;
-  const uint32_t o_base = smem_u32(sm + kOffMO), ml_base = smem_u32(sm + kOffMMl);
-  float* wts = reinterpret_cast<float*>(sm + kOffMW);  // [128][kMaxClusterSplits]
+  const uint32_t o_base = smem_u32(sm + G::kOffMO), ml_base = smem_u32(sm + G::kOffMMl);
+  float* wts = reinterpret_cast<float*>(sm + G::kOffMW);  // [128][kMaxClusterSplits]
   const int tid = static_cast<int>(threadIdx.x);
   const int b = unit / p.Sq, i = unit % p.Sq;
   if (tid < r1 - r0) {
@@ -718,10 +773,10 @@ __device__ void fp8tc_cluster_merge(const Fp8TcParams& p, int unit, int hb, int 
     for (int c = 0; c < kMaxClusterSplits; ++c) wts[r * kMaxClusterSplits + c] = m[c] * inv;
   }
   __syncthreads();
-  const int n = (r1 - r0) * (kPartDims / 4);
+  const int n = (r1 - r0) * (G::kPartDims / 4);
   for (int it = tid; it < n; it += kThreads) {
-    const int r = r0 + it / (kPartDims / 4), k = it % (kPartDims / 4);
-    const uint32_t src = o_base + static_cast<uint32_t>((r * kOStride + 4 * k) * 4);
+    const int r = r0 + it / (G::kPartDims / 4), k = it % (G::kPartDims / 4);
+    const uint32_t src = o_base + static_cast<uint32_t>((r * G::kOStride + 4 * k) * 4);
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
     for (int c = 0; c < kMaxClusterSplits; ++c) {
@@ -735,8 +790,8 @@ __device__ void fp8tc_cluster_merge(const Fp8TcParams& p, int unit, int hb, int 
       acc.w = fmaf(v.w, w, acc.w);
     }
     __nv_bfloat16* yp = static_cast<__nv_bfloat16*>(p.y) +
-                        ((static_cast<int64_t>(b) * p.Hq + hb * kHeads + r) * p.Sq + i) * kD +
-                        part * kPartDims + 4 * k;
+                        ((static_cast<int64_t>(b) * p.Hq + hb * kHeads + r) * p.Sq + i) * G::kD +
+                        part * G::kPartDims + 4 * k;
     *reinterpret_cast<uint2*>(yp) =
         make_uint2(pack2<__nv_bfloat16>(acc.x, acc.y), pack2<__nv_bfloat16>(acc.z, acc.w));
   }
@@ -749,23 +804,23 @@ __device__ void fp8tc_cluster_merge(const Fp8TcParams& p, int unit, int hb, int 
 // output dims, key split): blockIdx.x = ((unit * hblocks + hb) * 3 + part) *
 // splits + split, the splits of one output block adjacent (a cluster when
 // they merge on chip).
-template <bool kCap>
+template <class G, bool kCap, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_tc05_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const Fp8TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffTmemSlot);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffAbort);
-  uint32_t* valid = reinterpret_cast<uint32_t*>(sm + kOffValid);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + G::kOffBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + G::kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + G::kOffAbort);
+  uint32_t* valid = reinterpret_cast<uint32_t*>(sm + G::kOffValid);
   const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
   int cta = static_cast<int>(blockIdx.x);
   const int split = cta % p.splits;
   cta /= p.splits;
-  const int part = cta % kParts;
-  cta /= kParts;
+  const int part = cta % G::kParts;
+  cta /= G::kParts;
   const int hb = cta % p.hblocks;
   const int unit = cta / p.hblocks;
   const int t0 = split * p.chunk_tiles;
@@ -796,19 +851,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q is an input of the call: its load may start before the kernels this
     // one depends on have finished
     tc05::prefetch_tmap(&tq);
-    mbar_arrive_expect_tx(&bars[kBarQ], kChunks * kChunkBytes);
+    mbar_arrive_expect_tx(&bars[kBarQ], G::kChunks * kChunkBytes);
     const int b = unit / p.Sq, i = unit % p.Sq;
 #pragma unroll 1
-    for (int c = 0; c < kChunks; ++c)
-      tc05::tma_load3(sm + kOffQ + c * kChunkBytes, &tq, 64 * c, i, b * p.Hq + hb * kHeads,
+    for (int c = 0; c < G::kChunks; ++c)
+      tc05::tma_load3(sm + G::kOffQ + c * kChunkBytes, &tq, 64 * c, i, b * p.Hq + hb * kHeads,
                       &bars[kBarQ]);
   }
   pdl_wait();  // the planned positions and the decoded keys
   // validity bit masks of this split's tiles: word 4j + k, bit i = key 32k + i
-  const int32_t* prow = p.pos + static_cast<int64_t>(unit) * p.n_cand_pad +
-                        static_cast<int64_t>(t0) * kKeys;
+  const int64_t vbase = static_cast<int64_t>(unit) * p.n_cand_pad + static_cast<int64_t>(t0) * kKeys;
   for (int w = warp; w < 4 * nt; w += kThreads / 32) {
-    const uint32_t m = __ballot_sync(0xffffffffu, __ldg(prow + 32 * w + lane) >= 0);
+    const bool v = p.valid_u8 ? __ldg(p.valid_u8 + vbase + 32 * w + lane) != 0
+                              : __ldg(p.pos + vbase + 32 * w + lane) >= 0;
+    const uint32_t m = __ballot_sync(0xffffffffu, v);
     if (lane == 0) valid[w] = m;
   }
   tc05::fence_before_sync();
@@ -817,20 +873,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tslot;
 
   if (warp == kWarpLoad) {
-    if (lane == 0) fp8tc_producer(&tk, p, unit, t0, nt, part, sm, bars, abort_flag);
+    if (lane == 0) fp8tc_producer<G>(&tk, p, unit, t0, nt, part, sm, bars, abort_flag);
   } else if (warp == kWarpS) {
-    if (lane == 0) fp8tc_score_lane(p, nt, sm, bars, tmem, abort_flag);
+    if (lane == 0) fp8tc_score_lane<G>(p, nt, sm, bars, tmem, abort_flag);
   } else if (warp == kWarpPv) {
-    if (lane == 0) fp8tc_pv_lane(p, nt, sm, bars, tmem, abort_flag);
+    if (lane == 0) fp8tc_pv_lane<G>(p, nt, sm, bars, tmem, abort_flag);
   } else if (warp >= kWarpSoftmax) {
-    fp8tc_softmax<kCap>(p, unit, hb, split, nt, part, valid, bars, tmem, abort_flag);
+    fp8tc_softmax<G, kCap, kBias>(p, unit, hb, split, nt, part, valid, bars, tmem, abort_flag);
   }
 
   tc05::fence_before_sync();
   __syncwarp();
   if (p.splits > 1 && p.cluster_merge) {
     cluster_sync();  // every CTA's O rows staged
-    fp8tc_cluster_merge(p, unit, hb, part, sm);
+    fp8tc_cluster_merge<G>(p, unit, hb, part, sm);
     cluster_sync();  // no CTA leaves while another reads its shared memory
   } else {
     __syncthreads();
@@ -893,10 +949,10 @@ static int launch_pdl(K kernel, unsigned grid, unsigned block, size_t smem, cuda
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? 0 : -1;
 }
 
-template <bool kCap>
+template <class G, bool kCap, bool kBias>
 static bool set_smem() {
-  return cudaFuncSetAttribute(fp8_tc05_kernel<kCap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmem) == cudaSuccess;
+  return cudaFuncSetAttribute(fp8_tc05_kernel<G, kCap, kBias>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem) == cudaSuccess;
 }
 
 // How many clusters of `c` CTAs of the attention kernel can be resident at
@@ -906,11 +962,11 @@ static int max_active_clusters(int c) {
   static int ok[kMaxClusterSplits + 1];
   std::call_once(once[c], [c] {
     ok[c] = 0;
-    if (!set_smem<false>() || !set_smem<true>()) return;
+    if (!set_smem<GeoFp8, false, false>() || !set_smem<GeoFp8, true, false>()) return;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = GeoFp8::kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(c);
@@ -919,7 +975,9 @@ static int max_active_clusters(int c) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_tc05_kernel<false>, &cfg) == cudaSuccess) ok[c] = n;
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_tc05_kernel<GeoFp8, false, false>, &cfg) ==
+        cudaSuccess)
+      ok[c] = n;
     cudaGetLastError();  // a refused query leaves no sticky error behind
   });
   return ok[c];
@@ -935,7 +993,7 @@ bool fp8_tc_cluster_merge(int64_t splits, int64_t blocks) {
 
 int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   if (!fp8_tc_supported(g) || !g.fp8_kdec) return -1;
-  const bool cluster = fp8_tc_cluster_merge(g.splits, g.units * (g.Hq / kHeads) * kParts);
+  const bool cluster = fp8_tc_cluster_merge(g.splits, g.units * (g.Hq / kHeads) * GeoFp8::kParts);
   if (g.splits > 1 && !cluster && (!g.part_o || !g.part_ml)) return -1;
   if (g.n_cand_pad % kKeys != 0 || g.chunk > kMaxTiles || g.chunk < 1) return -1;
   const int64_t rows = g.units * g.n_cand_pad;
@@ -984,7 +1042,7 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   const cuuint32_t kbox[3] = {64, static_cast<cuuint32_t>(kKeys), 1};
   if (!bf16_map(&tq, g.q, qdims, qstr, qbox) || !bf16_map(&tk, g.fp8_kdec, kdims, kstr, kbox))
     return -1;
-  Fp8TcParams p;
+  Fp8TcParams p = {};
   p.pos = g.pos;
   p.n_cand_pad = g.n_cand_pad;
   p.y = g.y;
@@ -1004,15 +1062,83 @@ int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
   const float log2e = 1.4426950408889634f;
   p.k1 = g.softcap != 0.0f ? (g.scale_log2 / log2e) * g.inv_softcap : 0.0f;
   p.c_log2 = g.softcap * log2e;
-  const unsigned grid = static_cast<unsigned>(g.units * p.hblocks * kParts * g.splits);
+  using G = GeoFp8;
+  const unsigned grid = static_cast<unsigned>(g.units * p.hblocks * G::kParts * g.splits);
   const unsigned cl = cluster ? static_cast<unsigned>(g.splits) : 1u;
-  if (!(g.softcap != 0.0f ? set_smem<true>() : set_smem<false>())) return -1;
+  if (!(g.softcap != 0.0f ? set_smem<G, true, false>() : set_smem<G, false, false>())) return -1;
   mark_event(g.ev_before, st);
   const int rc =
       g.softcap != 0.0f
-          ? launch_pdl(fp8_tc05_kernel<true>, grid, kThreads, kSmem, st, cl, tq, tk, p)
-          : launch_pdl(fp8_tc05_kernel<false>, grid, kThreads, kSmem, st, cl, tq, tk, p);
+          ? launch_pdl(fp8_tc05_kernel<G, true, false>, grid, kThreads, G::kSmem, st, cl, tq, tk, p)
+          : launch_pdl(fp8_tc05_kernel<G, false, false>, grid, kThreads, G::kSmem, st, cl, tq, tk,
+                       p);
   mark_event(g.ev_after, st);
+  return rc;
+}
+
+// ---- compressed sparse attention rows (D = 512) on the same kernel -------------------------
+
+bool csa_tc_supported(int64_t D, int64_t H, int q_dtype) {
+  return D == GeoCsa::kD && H % kHeads == 0 && q_dtype == SA_BF16 && encode_tiled() != nullptr;
+}
+
+int csa_tc_max_tiles() { return kMaxTiles; }
+
+// The assembled candidate rows [units, c_pad, 512] bf16 with their validity
+// bytes: a (query, head block, half of the output dims, key split) per CTA,
+// the query block read as [units * H][512] (one query position per unit).
+int launch_csa_tc(const CsaArgs& a, cudaStream_t st) {
+  using G = GeoCsa;
+  const int64_t units = a.B * a.S;
+  if (!csa_tc_supported(a.D, a.H, a.q_dtype) || a.c_pad % kKeys != 0 || a.chunk_tiles < 1 ||
+      a.chunk_tiles > kMaxTiles || (a.splits > 1 && (!a.part_o || !a.part_ml)))
+    return -1;
+  CUtensorMap tq, tk;
+  const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(G::kD), 1,
+                               static_cast<cuuint64_t>(units * a.H)};
+  const cuuint64_t qstr[2] = {static_cast<cuuint64_t>(G::kD * 2),
+                              static_cast<cuuint64_t>(G::kD * 2)};
+  const cuuint32_t qbox[3] = {64, 1, static_cast<cuuint32_t>(kHeads)};
+  const cuuint64_t kdims[3] = {static_cast<cuuint64_t>(G::kD), static_cast<cuuint64_t>(a.c_pad),
+                               static_cast<cuuint64_t>(units)};
+  const cuuint64_t kstr[2] = {static_cast<cuuint64_t>(G::kD * 2),
+                              static_cast<cuuint64_t>(a.c_pad * G::kD * 2)};
+  const cuuint32_t kbox[3] = {64, static_cast<cuuint32_t>(kKeys), 1};
+  if (!bf16_map(&tq, a.query, qdims, qstr, qbox) || !bf16_map(&tk, a.rows, kdims, kstr, kbox))
+    return -1;
+  Fp8TcParams p = {};
+  p.pos = nullptr;
+  p.valid_u8 = a.valid;
+  p.bias = a.bias;
+  p.bias_sb = a.bias_sb;
+  p.bias_sh = a.bias_sh;
+  p.bias_si = a.bias_si;
+  p.bias_sk = a.bias_sk;
+  p.bias_S = static_cast<int>(a.S);
+  p.n_cand_pad = a.c_pad;
+  p.y = a.y;
+  p.part_o = a.part_o;
+  p.part_ml = a.part_ml;
+  p.sink = a.sink;
+  p.err_word = a.err_word;
+  p.B = static_cast<int>(units);
+  p.Sq = 1;
+  p.Hq = static_cast<int>(a.H);
+  p.hblocks = static_cast<int>(a.H / kHeads);
+  p.splits = static_cast<int>(a.splits);
+  p.chunk_tiles = static_cast<int>(a.chunk_tiles);
+  p.tiles = static_cast<int>(a.c_pad / kKeys);
+  p.cluster_merge = 0;
+  p.scale_log2 = a.scale_log2;
+  const unsigned grid = static_cast<unsigned>(units * p.hblocks * G::kParts * a.splits);
+  const bool bias = a.bias != nullptr;
+  if (!(bias ? set_smem<G, false, true>() : set_smem<G, false, false>())) return -1;
+  mark_event(a.ev_before, st);
+  const int rc =
+      bias ? launch_pdl(fp8_tc05_kernel<G, false, true>, grid, kThreads, G::kSmem, st, 1u, tq, tk, p)
+           : launch_pdl(fp8_tc05_kernel<G, false, false>, grid, kThreads, G::kSmem, st, 1u, tq, tk,
+                        p);
+  mark_event(a.ev_after, st);
   return rc;
 }
 

@@ -250,8 +250,9 @@ struct CsaArgs {
   int64_t B, S, H, D, n_rope, L, R, topk, record_stride, total;
   int64_t dense;              // dense slots: 128, or min(L, 128) when the block starts at 0
   int64_t valid_records;      // min(R, total / 4)
-  int64_t c_pad;              // candidate slots, rounded up to 16
-  int64_t splits, chunk_tiles;
+  int64_t c_pad;              // candidate slots, rounded up to 16 (128 on the tensor-core path)
+  int64_t splits, chunk_tiles;  // chunk_tiles: 16-slot tiles, or 128-slot tiles when tc
+  int tc;                     // the tcgen05 attention kernel (k_fp8_tc.cu) instead of csa_attn_kernel
   float scale_log2;
   uint32_t* err_word;
   // workspace
@@ -264,6 +265,10 @@ struct CsaArgs {
 };
 size_t csa_attn_smem_bytes(int64_t D);
 int launch_csa(const CsaArgs& a, cudaStream_t st);
+// tcgen05 attention over the assembled rows (D = 512, 128-head blocks, bf16 queries)
+bool csa_tc_supported(int64_t D, int64_t H, int q_dtype);
+int csa_tc_max_tiles();
+int launch_csa_tc(const CsaArgs& a, cudaStream_t st);
 
 // ---- CSA compression stages (ratio 4 records / index keys, ratio 128) -------------------
 constexpr int kCompressAttn = 0;   // hybrid FP8 attention record

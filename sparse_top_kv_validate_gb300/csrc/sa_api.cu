@@ -1057,13 +1057,27 @@ static size_t csa_plan(const sa_csa_params* p, sa::CsaArgs& a, char* ws) {
   a.dense = (p->total == p->S) ? (p->L < 128 ? p->L : 128) : 128;
   a.valid_records = p->total / 4 < p->R ? p->total / 4 : p->R;
   const int64_t C = a.dense + p->topk;
-  a.c_pad = (C + 15) / 16 * 16;
-  const int64_t tiles = a.c_pad / 16;
-  const int64_t blocks = p->B * p->S * (p->H / 32);
   const int64_t sms = device_shape().sms > 0 ? device_shape().sms : 152;
-  int64_t splits = (2 * sms + blocks - 1) / blocks;  // two CTAs per SM
+  int64_t tiles, splits;
+  a.tc = sa::csa_tc_supported(p->D, p->H, p->q_dtype) ? 1 : 0;
+  if (a.tc) {
+    // 128-slot tiles; two CTAs (halves of the output dims) per (query, 128-head
+    // block, key split), one CTA per SM
+    a.c_pad = (C + 127) / 128 * 128;
+    tiles = a.c_pad / 128;
+    const int64_t blocks = p->B * p->S * (p->H / 128) * 2;
+    splits = sms / blocks;
+    const int64_t min_splits = (tiles + sa::csa_tc_max_tiles() - 1) / sa::csa_tc_max_tiles();
+    if (splits < min_splits) splits = min_splits;
+    if (splits > 16) splits = 16 > min_splits ? 16 : min_splits;
+  } else {
+    a.c_pad = (C + 15) / 16 * 16;
+    tiles = a.c_pad / 16;
+    const int64_t blocks = p->B * p->S * (p->H / 32);
+    splits = (2 * sms + blocks - 1) / blocks;  // two CTAs per SM
+    if (splits > 16) splits = 16;
+  }
   if (splits > tiles) splits = tiles;
-  if (splits > 16) splits = 16;
   if (splits < 1) splits = 1;
   a.chunk_tiles = (tiles + splits - 1) / splits;
   a.splits = (tiles + a.chunk_tiles - 1) / a.chunk_tiles;

@@ -51,8 +51,22 @@ CASES = [
 ]
 
 
+# 128-head blocks with bf16 queries run on the tcgen05 kernel (128-slot tiles,
+# two CTAs per head block, key splits merged by the combine kernel); the
+# f32 versions of the same shapes run on the warp-level MMA kernel.
+CASES_TC = [
+    ("tc_mid", dict(B=2, S=1, H=128, D=512, n_rope=64, L=128, total=3000, topk=300)),
+    ("tc_multi_query", dict(B=2, S=3, H=128, D=512, n_rope=64, L=128, total=2048, topk=100)),
+    ("tc_short_window_h256", dict(B=3, S=2, H=256, D=512, n_rope=64, L=40, total=900, topk=64)),
+    ("tc_block_at_zero", dict(B=1, S=50, H=128, D=512, n_rope=64, L=50, total=50, topk=12)),
+    ("tc_long_16_splits", dict(B=1, S=1, H=128, D=512, n_rope=64, L=128, total=40000,
+                               topk=6000)),
+    ("tc_one_tile", dict(B=2, S=20, H=128, D=512, n_rope=64, L=20, total=20, topk=4)),
+]
+
+
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
-@pytest.mark.parametrize("name,over", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("name,over", CASES + CASES_TC, ids=[c[0] for c in CASES + CASES_TC])
 def test_csa_matches_oracle(cuda_lib, dt, name, over):
     c = synth.CsaCase(name, dtype=dt, **over)
     inp = synth.make_csa_inputs(c, seed=41)
@@ -63,9 +77,10 @@ def test_csa_matches_oracle(cuda_lib, dt, name, over):
     _close(y, ref, f"{name} {dt}")
 
 
+@pytest.mark.parametrize("H", [32, 128])
 @pytest.mark.parametrize("shape_kind", ["h1c", "b11c", "c", "full"])
-def test_slot_bias(cuda_lib, shape_kind):
-    c = synth.CsaCase("bias", B=2, S=2, H=32, D=512, n_rope=64, L=128, total=1200, topk=80)
+def test_slot_bias(cuda_lib, shape_kind, H):
+    c = synth.CsaCase("bias", B=2, S=2, H=H, D=512, n_rope=64, L=128, total=1200, topk=80)
     inp = synth.make_csa_inputs(c, seed=42)
     C = 128 + c.topk
     shape = {"h1c": (c.H, 1, C), "b11c": (c.B, 1, 1, C), "c": (C,),
@@ -78,8 +93,9 @@ def test_slot_bias(cuda_lib, shape_kind):
     _close(y, ref, f"bias {shape_kind}")
 
 
-def test_invalid_records_are_skipped_and_flagged(cuda_lib):
-    c = synth.CsaCase("bad", B=2, S=1, H=32, D=512, n_rope=64, L=128, total=1000, topk=40)
+@pytest.mark.parametrize("H", [32, 128])
+def test_invalid_records_are_skipped_and_flagged(cuda_lib, H):
+    c = synth.CsaCase("bad", B=2, S=1, H=H, D=512, n_rope=64, L=128, total=1000, topk=40)
     inp = synth.make_csa_inputs(c, seed=44)
     sel = inp["selected"].clone()
     sel[0, 0, 5] = 250          # 250 >= 1000 / 4: skipped, flagged
@@ -91,8 +107,9 @@ def test_invalid_records_are_skipped_and_flagged(cuda_lib):
     _close(y, ref, "bad records")
 
 
-def test_deterministic(cuda_lib):
-    c = synth.CsaCase("det", B=2, S=1, H=64, D=512, n_rope=64, L=128, total=4000, topk=500)
+@pytest.mark.parametrize("H", [64, 128])
+def test_deterministic(cuda_lib, H):
+    c = synth.CsaCase("det", B=2, S=1, H=H, D=512, n_rope=64, L=128, total=4000, topk=500)
     inp = synth.make_csa_inputs(c, seed=45, device=DEV)
     ys = [_run(cuda_lib, c, inp)[0] for _ in range(2)]
     assert torch.equal(ys[0], ys[1])
