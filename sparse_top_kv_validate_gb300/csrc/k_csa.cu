@@ -451,8 +451,9 @@ static int launch_csa_t(const CsaArgs& a, cudaStream_t st) {
                                static_cast<unsigned>(a.B * a.S)), 256, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return -1;
   if (a.tc) {  // the tcgen05 kernel over the same rows (k_fp8_tc.cu)
-    if (launch_csa_tc(a, st) != 0) return -1;
-    if (a.splits > 1)
+    bool merged = false;
+    if (launch_csa_tc(a, st, &merged) != 0) return -1;
+    if (!merged)
       return launch_pdl(csa_combine_kernel<D>, dim3(static_cast<unsigned>(a.B * a.S * a.H)),
                         dim3(128), 0, st, a);
     return 0;

@@ -955,18 +955,22 @@ static bool set_smem() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem) == cudaSuccess;
 }
 
-// How many clusters of `c` CTAs of the attention kernel can be resident at
-// once on this device (a cluster needs c SMs of one GPC)?  Asked once per size.
+// How many clusters of `c` CTAs of the attention kernel (geometry G) can be
+// resident at once on this device (a cluster needs c SMs of one GPC)?  Asked
+// once per geometry and size.
+template <class G>
 static int max_active_clusters(int c) {
   static std::once_flag once[kMaxClusterSplits + 1];
   static int ok[kMaxClusterSplits + 1];
   std::call_once(once[c], [c] {
     ok[c] = 0;
-    if (!set_smem<GeoFp8, false, false>() || !set_smem<GeoFp8, true, false>()) return;
+    if (!set_smem<G, false, false>() || !set_smem<G, true, false>() ||
+        !set_smem<G, false, true>())
+      return;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = GeoFp8::kSmem;
+    cfg.dynamicSmemBytes = G::kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(c);
@@ -975,8 +979,7 @@ static int max_active_clusters(int c) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_tc05_kernel<GeoFp8, false, false>, &cfg) ==
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_tc05_kernel<G, false, false>, &cfg) == cudaSuccess)
       ok[c] = n;
     cudaGetLastError();  // a refused query leaves no sticky error behind
   });
@@ -988,7 +991,7 @@ static int max_active_clusters(int c) {
 // would cost more than the separate combine).
 bool fp8_tc_cluster_merge(int64_t splits, int64_t blocks) {
   if (splits < 2 || splits > kMaxClusterSplits) return false;
-  return max_active_clusters(static_cast<int>(splits)) >= blocks;
+  return max_active_clusters<GeoFp8>(static_cast<int>(splits)) >= blocks;
 }
 
 int launch_fp8_tc(const GatherArgs& g, cudaStream_t st) {
@@ -1087,11 +1090,16 @@ int csa_tc_max_tiles() { return kMaxTiles; }
 // The assembled candidate rows [units, c_pad, 512] bf16 with their validity
 // bytes: a (query, head block, half of the output dims, key split) per CTA,
 // the query block read as [units * H][512] (one query position per unit).
-int launch_csa_tc(const CsaArgs& a, cudaStream_t st) {
+int launch_csa_tc(const CsaArgs& a, cudaStream_t st, bool* merged) {
   using G = GeoCsa;
   const int64_t units = a.B * a.S;
+  // the splits of an output block merge on chip when all blocks' clusters are resident at once
+  const int64_t blocks = units * (a.H / kHeads) * G::kParts;
+  const bool cluster = a.splits >= 2 && a.splits <= kMaxClusterSplits &&
+                       max_active_clusters<G>(static_cast<int>(a.splits)) >= blocks;
+  *merged = cluster || a.splits == 1;
   if (!csa_tc_supported(a.D, a.H, a.q_dtype) || a.c_pad % kKeys != 0 || a.chunk_tiles < 1 ||
-      a.chunk_tiles > kMaxTiles || (a.splits > 1 && (!a.part_o || !a.part_ml)))
+      a.chunk_tiles > kMaxTiles || (a.splits > 1 && !cluster && (!a.part_o || !a.part_ml)))
     return -1;
   CUtensorMap tq, tk;
   const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(G::kD), 1,
@@ -1128,15 +1136,16 @@ int launch_csa_tc(const CsaArgs& a, cudaStream_t st) {
   p.splits = static_cast<int>(a.splits);
   p.chunk_tiles = static_cast<int>(a.chunk_tiles);
   p.tiles = static_cast<int>(a.c_pad / kKeys);
-  p.cluster_merge = 0;
+  p.cluster_merge = cluster ? 1 : 0;
   p.scale_log2 = a.scale_log2;
   const unsigned grid = static_cast<unsigned>(units * p.hblocks * G::kParts * a.splits);
+  const unsigned cl = cluster ? static_cast<unsigned>(a.splits) : 1u;
   const bool bias = a.bias != nullptr;
   if (!(bias ? set_smem<G, false, true>() : set_smem<G, false, false>())) return -1;
   mark_event(a.ev_before, st);
   const int rc =
-      bias ? launch_pdl(fp8_tc05_kernel<G, false, true>, grid, kThreads, G::kSmem, st, 1u, tq, tk, p)
-           : launch_pdl(fp8_tc05_kernel<G, false, false>, grid, kThreads, G::kSmem, st, 1u, tq, tk,
+      bias ? launch_pdl(fp8_tc05_kernel<G, false, true>, grid, kThreads, G::kSmem, st, cl, tq, tk, p)
+           : launch_pdl(fp8_tc05_kernel<G, false, false>, grid, kThreads, G::kSmem, st, cl, tq, tk,
                         p);
   mark_event(a.ev_after, st);
   return rc;

@@ -268,7 +268,8 @@ int launch_csa(const CsaArgs& a, cudaStream_t st);
 // tcgen05 attention over the assembled rows (D = 512, 128-head blocks, bf16 queries)
 bool csa_tc_supported(int64_t D, int64_t H, int q_dtype);
 int csa_tc_max_tiles();
-int launch_csa_tc(const CsaArgs& a, cudaStream_t st);
+// *merged: the key splits were merged on chip (no combine kernel needed)
+int launch_csa_tc(const CsaArgs& a, cudaStream_t st, bool* merged);
 
 // ---- CSA compression stages (ratio 4 records / index keys, ratio 128) -------------------
 constexpr int kCompressAttn = 0;   // hybrid FP8 attention record
