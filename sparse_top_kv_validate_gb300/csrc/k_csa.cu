@@ -13,12 +13,13 @@
 // with exp(sink[h] - max) added to the denominator; y = sum p * row (K = V).
 //
 // GB300 design:
-//  * csa_assemble_kernel: one warp per (query, candidate slot) writes the
-//    slot's row as bf16 into a candidate buffer (window rows converted,
+//  * csa_assemble_kernel: one warp per (query, four candidate slots) writes
+//    the slots' rows as bf16 into a candidate buffer (window rows converted,
 //    hybrid FP8 records decoded exactly: 583-byte records are not even 2-byte
-//    aligned, so a warp reads them with byte loads, a block's 64 codes in one
-//    coalesced pass), with a validity byte; the rows stay in L2 for the
-//    attention kernel.
+//    aligned, so a warp stages each one in shared memory -- 16-byte loads for
+//    its aligned interior, byte loads for the ends, the four records' loads in
+//    flight together -- and decodes it from there), with a validity byte; the
+//    rows stay in L2 for the attention kernel.
 //  * bf16 queries in blocks of 128 heads (D 512): the tcgen05 attention kernel
 //    of k_fp8_tc.cu in its 512-dim geometry reads the assembled rows by TMA in
 //    128-slot tiles (two CTAs per head block, each owning 256 output dims;
@@ -99,76 +100,125 @@ __device__ __forceinline__ CsaRow csa_row(const CsaArgs& a, int64_t s) {
 
 // ---- candidate rows ------------------------------------------------------------------------
 // grid (c_pad / 8, units), 8 warps: warp w writes candidate slot blockIdx.x * 8 + w.
+// Each warp assembles kSlotsPerWarp consecutive candidate slots.  It first
+// stages every selected record among them in shared memory -- the 16-byte
+// aligned interior with vector loads, the unaligned head and tail (under 16
+// bytes each) with byte loads, all issued together and none outside the
+// record; byte j of a record sits at stage[(address % 16) + j] -- and then
+// decodes and writes the slots in turn.
+constexpr int kSlotsPerWarp = 4;
+
+// Shared-memory bytes a warp stages one record in: the record and up to 15
+// bytes before it, rounded to 16 (dynamic: the CTA then holds 8 warps x 4).
+__host__ __device__ __forceinline__ int csa_stage_bytes(int64_t D, int64_t n_rope) {
+  const int nbytes = static_cast<int>((D - n_rope) / 64 * 65 + 2 * n_rope);
+  return (15 + nbytes + 15) / 16 * 16;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) csa_assemble_kernel(const CsaArgs a) {
+  extern __shared__ __align__(16) uint8_t stage_all[];
   const int lane = threadIdx.x & 31;
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int kStageBytes = csa_stage_bytes(D, a.n_rope);
+  uint8_t* stage = stage_all + (threadIdx.x >> 5) * kSlotsPerWarp * kStageBytes;
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kSlotsPerWarp;
   const int64_t unit = blockIdx.y;  // b * S + s
   const int64_t b = unit / a.S, s = unit % a.S;
   const CsaRow r = csa_row(a, s);
-  __nv_bfloat16* dst = a.rows + (unit * a.c_pad + c) * D;
-  bool valid = false;
-  if (c < r.dense) {
-    const int64_t absolute = r.dense_start + c;
-    const int64_t rel = absolute - r.base;
-    valid = absolute <= r.pos && rel < a.L;
-    if (valid) {
-      // lane l: dims [l * D / 32, (l + 1) * D / 32)
-      constexpr int kPer = D / 32;
-      uint32_t w[kPer / 2];
-      if (a.kv_dtype == SA_BF16) {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(
-            static_cast<const __nv_bfloat16*>(a.window) + (b * a.L + rel) * D + lane * kPer);
+  const int nb = static_cast<int>((D - a.n_rope) / 64);
+  const int nbytes = 65 * nb + 2 * static_cast<int>(a.n_rope);
+  // the slots' selected records (lane i < kSlotsPerWarp reads slot c0 + i's)
+  int32_t mine = -1;
+  if (lane < kSlotsPerWarp) {
+    const int64_t c = c0 + lane;
+    if (c < a.c_pad && c >= r.dense && c < r.dense + a.topk)
+      mine = __ldg(a.selected + unit * a.topk + (c - r.dense));
+  }
+  // phase 1: stage every valid record
 #pragma unroll
-        for (int i = 0; i < kPer / 2; ++i) w[i] = __ldg(src + i);
-      } else {
-        const float2* src = reinterpret_cast<const float2*>(
-            static_cast<const float*>(a.window) + (b * a.L + rel) * D + lane * kPer);
+  for (int i = 0; i < kSlotsPerWarp; ++i) {
+    const int32_t rec = __shfl_sync(0xffffffffu, mine, i);
+    if (rec < 0 || rec >= a.valid_records) continue;
+    const uint8_t* src = a.records + (b * a.R + rec) * a.record_stride;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), s1 = s0 + nbytes;
+    const uintptr_t a0 = (s0 + 15) & ~static_cast<uintptr_t>(15);
+    const uintptr_t a1 = s1 & ~static_cast<uintptr_t>(15);
+    uint8_t* st = stage + i * kStageBytes + (s0 & 15);
+    const int head = static_cast<int>((a0 < s1 ? a0 : s1) - s0);   // bytes before the interior
+    const int body = a1 > a0 ? static_cast<int>((a1 - a0) / 16) : 0;  // 16-byte words
+    const int tail0 = head + 16 * body;                              // first tail byte
+    for (int w = lane; w < body; w += 32)
+      *reinterpret_cast<uint4*>(st + head + 16 * w) = __ldg(reinterpret_cast<const uint4*>(a0) + w);
+    if (lane < head) st[lane] = __ldg(src + lane);
+    if (tail0 + lane < nbytes) st[tail0 + lane] = __ldg(src + tail0 + lane);
+  }
+  __syncwarp();
+  // phase 2: each slot's bf16 row and validity byte
+  for (int i = 0; i < kSlotsPerWarp; ++i) {
+    const int64_t c = c0 + i;
+    if (c >= a.c_pad) break;
+    __nv_bfloat16* dst = a.rows + (unit * a.c_pad + c) * D;
+    bool valid = false;
+    if (c < r.dense) {
+      const int64_t absolute = r.dense_start + c;
+      const int64_t rel = absolute - r.base;
+      valid = absolute <= r.pos && rel < a.L;
+      if (valid) {
+        // lane l: dims [l * D / 32, (l + 1) * D / 32)
+        constexpr int kPer = D / 32;
+        uint32_t w[kPer / 2];
+        if (a.kv_dtype == SA_BF16) {
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(
+              static_cast<const __nv_bfloat16*>(a.window) + (b * a.L + rel) * D + lane * kPer);
 #pragma unroll
-        for (int i = 0; i < kPer / 2; ++i) {
-          const float2 f = __ldg(src + i);
-          w[i] = pack2<__nv_bfloat16>(f.x, f.y);
+          for (int e = 0; e < kPer / 2; ++e) w[e] = __ldg(src + e);
+        } else {
+          const float2* src = reinterpret_cast<const float2*>(
+              static_cast<const float*>(a.window) + (b * a.L + rel) * D + lane * kPer);
+#pragma unroll
+          for (int e = 0; e < kPer / 2; ++e) {
+            const float2 f = __ldg(src + e);
+            w[e] = pack2<__nv_bfloat16>(f.x, f.y);
+          }
+        }
+        if (kPer >= 8) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + lane * kPer);
+#pragma unroll
+          for (int e = 0; e < kPer / 8; ++e)
+            d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        } else {
+          *reinterpret_cast<uint2*>(dst + lane * kPer) = make_uint2(w[0], w[1]);
         }
       }
-      if (kPer >= 8) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + lane * kPer);
-#pragma unroll
-        for (int i = 0; i < kPer / 8; ++i)
-          d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      } else {
-        *reinterpret_cast<uint2*>(dst + lane * kPer) = make_uint2(w[0], w[1]);
+    } else if (c < r.dense + a.topk) {
+      const int32_t rec = __shfl_sync(0xffffffffu, mine, i);
+      if (rec >= a.valid_records && lane == 0 && a.err_word) atomicOr(a.err_word, SA_ERRBIT_RECORD);
+      valid = rec >= 0 && rec < a.valid_records;
+      if (valid) {
+        const uint8_t* src = a.records + (b * a.R + rec) * a.record_stride;
+        const uint8_t* st = stage + i * kStageBytes + (reinterpret_cast<uintptr_t>(src) & 15);
+        uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
+        for (int k = 0; k < nb; ++k) {
+          const uint8_t* blk = st + 65 * k;
+          const float sc = e8m0(blk[0]);
+          const uint32_t two = static_cast<uint32_t>(blk[1 + 2 * lane]) |
+                               (static_cast<uint32_t>(blk[2 + 2 * lane]) << 8);
+          const float2 f = e4m3_pair(two);
+          d32[32 * k + lane] = pack2<__nv_bfloat16>(f.x * sc, f.y * sc);
+        }
+        // the RoPE dims: little-endian bf16, copied
+        const uint8_t* tl = st + 65 * nb;
+        uint16_t* d16 = reinterpret_cast<uint16_t*>(dst + 64 * nb);
+        for (int e = lane; e < a.n_rope; e += 32)
+          d16[e] = static_cast<uint16_t>(tl[2 * e] | (tl[2 * e + 1] << 8));
       }
     }
-  } else if (c < r.dense + a.topk) {
-    const int32_t rec = __ldg(a.selected + unit * a.topk + (c - r.dense));
-    if (rec >= a.valid_records) {
-      if (lane == 0 && a.err_word) atomicOr(a.err_word, SA_ERRBIT_RECORD);
+    if (!valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      for (int e = lane; e < D / 8; e += 32) d4[e] = make_uint4(0u, 0u, 0u, 0u);
     }
-    valid = rec >= 0 && rec < a.valid_records;
-    if (valid) {
-      const uint8_t* src = a.records + (b * a.R + rec) * a.record_stride;
-      uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
-      const int nb = static_cast<int>((D - a.n_rope) / 64);
-      for (int k = 0; k < nb; ++k) {
-        const uint8_t* blk = src + 65 * k;
-        const float sc = e8m0(__ldg(blk));
-        const uint32_t two = static_cast<uint32_t>(__ldg(blk + 1 + 2 * lane)) |
-                             (static_cast<uint32_t>(__ldg(blk + 2 + 2 * lane)) << 8);
-        const float2 f = e4m3_pair(two);
-        d32[32 * k + lane] = pack2<__nv_bfloat16>(f.x * sc, f.y * sc);
-      }
-      // the RoPE dims: little-endian bf16, copied
-      const uint8_t* tail = src + 65 * nb;
-      uint16_t* d16 = reinterpret_cast<uint16_t*>(dst + 64 * nb);
-      for (int e = lane; e < a.n_rope; e += 32)
-        d16[e] = static_cast<uint16_t>(__ldg(tail + 2 * e) | (__ldg(tail + 2 * e + 1) << 8));
-    }
+    if (lane == 0) a.valid[unit * a.c_pad + c] = valid ? 1 : 0;
   }
-  if (!valid) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-    for (int i = lane; i < D / 8; i += 32) d4[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  if (lane == 0) a.valid[unit * a.c_pad + c] = valid ? 1 : 0;
   pdl_launch_dependents();
 }
 
@@ -447,8 +497,10 @@ static int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t
 template <int D>
 static int launch_csa_t(const CsaArgs& a, cudaStream_t st) {
   using G = CsaGeo<D>;
-  csa_assemble_kernel<D><<<dim3(static_cast<unsigned>(a.c_pad / 8),
-                               static_cast<unsigned>(a.B * a.S)), 256, 0, st>>>(a);
+  constexpr int kSlotsPerCta = 8 * kSlotsPerWarp;
+  const size_t stage_smem = static_cast<size_t>(kSlotsPerCta) * csa_stage_bytes(D, a.n_rope);
+  csa_assemble_kernel<D><<<dim3(static_cast<unsigned>((a.c_pad + kSlotsPerCta - 1) / kSlotsPerCta),
+                               static_cast<unsigned>(a.B * a.S)), 256, stage_smem, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return -1;
   if (a.tc) {  // the tcgen05 kernel over the same rows (k_fp8_tc.cu)
     bool merged = false;
