@@ -805,6 +805,19 @@ KERNEL_SOURCES = {
 
 TRAFFIC: dict = {
     # workload: (kernel, bytes per launch, source hash at capture, how)
+    "csa_fp8_b16_h128_d576_t65536_k2048_w128": (
+        "fp8_tc05_kernel", 42_666_240, "799adc77e5673050",
+        "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the bench's own "
+        "workload (42.67 MB read, 0 written; ncu starts each kernel with cold caches, so the "
+        "decoded rows are read from DRAM here and from L2 in a live call)"),
+    "index_select_b16_ih64_id128_r16384_k2048": (
+        "index_score_kernel", 18_047_232, "4f9a40538fc99c73",
+        "ncu --set full, one launch of the bench's own workload (18.05 MB read, 0 written: the "
+        "index records once)"),
+    "csa_ref_b16_h128_d512_l128_t65536_k2048": (
+        "fp8_tc05_kernel", 37_857_536, "799adc77e5673050",
+        "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the bench's own "
+        "workload (37.86 MB read, 768 B written; cold caches under ncu, as above)"),
     "compress_r4": ("compress_r4_kernel", 547_078_912, "cd7022a0e814742c",
                     "ncu --set full, one launch of the bench's own workload (537.01 MB read, "
                     "10.07 MB written)"),
