@@ -30,8 +30,9 @@
 //    head sum runs serially in ascending head order.
 //  * index_topk_kernel: one CTA per row.  Equal scores are found with an
 //    open-addressing hash set; an MSB-first radix select over the total-order
-//    keys finds the k-th; the selected (key, record) pairs are bitonic-sorted
-//    into score order (or record order).
+//    keys finds the k-th; the selected (key, record) pairs are sorted into
+//    score order (or record order): runs of 64 by a bitonic network in each
+//    warp's registers, then merge levels found by binary search (merge path).
 #include <cmath>
 
 #include "codes.cuh"
@@ -387,22 +388,19 @@ __global__ void __launch_bounds__(kScoreRecords / RPT) index_score_kernel(const 
 
 namespace {
 
-// Bitonic steps of stride max_stride .. 1 (all below 64) for sorted-run size
-// `size`, inside each aligned 64-key chunk: warp w takes chunks w, w + warps,
-// ...; lane l holds keys l and l + 32 of the chunk.  With first_pass, every
-// run size from 2 to 64 (the chunk sorted from scratch).
-__device__ void warp_bitonic(unsigned long long* k, int n, int size, int max_stride,
-                             bool first_pass) {
+// Each warp sorts runs of 64 keys ascending in registers (two keys a lane:
+// run positions lane and lane + 32), a bitonic network over the run.
+__device__ void warp_sort64(unsigned long long* k, int n) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int c = warp; c < n / 64; c += nw) {
     const int base = c * 64;
     unsigned long long x[2] = {k[base + lane], k[base + 32 + lane]};
-    const int s0 = first_pass ? 2 : size, s1 = first_pass ? 64 : size;
-    for (int sz = s0; sz <= s1; sz <<= 1) {
-      for (int stride = first_pass ? sz >> 1 : max_stride; stride > 0; stride >>= 1) {
-        if (stride == 32) {
-          const bool up = ((base + lane) & sz) == 0;
-          if ((x[0] > x[1]) == up) {
+#pragma unroll
+    for (int sz = 2; sz <= 64; sz <<= 1) {
+#pragma unroll
+      for (int stride = sz >> 1; stride > 0; stride >>= 1) {
+        if (stride == 32) {  // sz == 64: the run's final merge, ascending
+          if (x[0] > x[1]) {
             const unsigned long long t = x[0];
             x[0] = x[1];
             x[1] = t;
@@ -411,8 +409,9 @@ __device__ void warp_bitonic(unsigned long long* k, int n, int size, int max_str
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const unsigned long long o = __shfl_xor_sync(0xffffffffu, x[h], stride);
-            const int e = base + 32 * h + lane;
-            const bool keep_min = ((e & stride) == 0) == ((e & sz) == 0);
+            const int e = 32 * h + lane;  // position in the run
+            const bool up = sz == 64 || (e & sz) == 0;
+            const bool keep_min = ((e & stride) == 0) == up;
             x[h] = keep_min ? (x[h] < o ? x[h] : o) : (x[h] < o ? o : x[h]);
           }
         }
@@ -423,32 +422,53 @@ __device__ void warp_bitonic(unsigned long long* k, int n, int size, int max_str
   }
 }
 
-// Ascending bitonic sort of n (a power of two) 64-bit keys in shared memory:
-// strides of 64 and more across the block (a barrier each), the smaller ones
-// inside warps in registers.
-__device__ void bitonic_sort(unsigned long long* k, int n) {
-  if (n < 64) {
-    for (int size = 2; size <= n; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
-          const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1));
-          const int hi = lo + stride;
-          const bool up = (lo & size) == 0;
-          const unsigned long long x = k[lo], y = k[hi];
-          if ((x > y) == up) {
-            k[lo] = y;
-            k[hi] = x;
-          }
-        }
-        __syncthreads();
-      }
+// One merge level: the sorted runs of L keys in src, taken in pairs, become
+// sorted runs of 2 L in dst.  Output rank r of a pair is found by a binary
+// search for the number i of keys of the first run among the pair's first r
+// outputs (equal keys -- only the padding -- take the second run's first).
+__device__ void merge_level(const unsigned long long* src, unsigned long long* dst, int n, int L) {
+  for (int o = threadIdx.x; o < n; o += blockDim.x) {
+    const int base = o & ~(2 * L - 1), r = o - base;
+    const unsigned long long* A = src + base;
+    const unsigned long long* Bv = A + L;
+    int lo = r > L ? r - L : 0, hi = r < L ? r : L;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (A[mid] < Bv[r - mid - 1]) lo = mid + 1;
+      else hi = mid;
     }
-    return;
+    const int j = r - lo;
+    const bool take_a = j >= L || (lo < L && A[lo] < Bv[j]);
+    dst[o] = take_a ? A[lo] : Bv[j];
   }
-  warp_bitonic(k, n, 64, 32, true);
+}
+
+// Ascending sort of n (a power of two, >= 64) 64-bit keys in shared memory:
+// runs of 64 sorted in registers, then log2(n / 64) merge levels between k
+// and tmp (n keys of scratch), the result back in k.
+__device__ void merge_sort(unsigned long long* k, unsigned long long* tmp, int n) {
+  warp_sort64(k, n);
   __syncthreads();
-  for (int size = 128; size <= n; size <<= 1) {
-    for (int stride = size >> 1; stride >= 64; stride >>= 1) {
+  unsigned long long* src = k;
+  unsigned long long* dst = tmp;
+  for (int L = 64; L < n; L <<= 1) {
+    merge_level(src, dst, n, L);
+    __syncthreads();
+    unsigned long long* t = src;
+    src = dst;
+    dst = t;
+  }
+  if (src != k) {
+    for (int o = threadIdx.x; o < n; o += blockDim.x) k[o] = src[o];
+    __syncthreads();
+  }
+}
+
+// Ascending bitonic sort of n (a power of two, below 64) 64-bit keys in
+// shared memory, a barrier per stage.
+__device__ void bitonic_sort(unsigned long long* k, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
         const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1));
         const int hi = lo + stride;
@@ -461,8 +481,6 @@ __device__ void bitonic_sort(unsigned long long* k, int n) {
       }
       __syncthreads();
     }
-    warp_bitonic(k, n, size, 32, false);
-    __syncthreads();
   }
 }
 
@@ -780,7 +798,10 @@ __device__ void topk_row(const IndexArgs& a, int64_t row, unsigned long long* se
   while (npad < kcount) npad <<= 1;
   for (int i = kcount + tid; i < npad; i += kTopkThreads) sel[i] = ~0ull;
   __syncthreads();
-  if (kcount > 1) bitonic_sort(sel, npad);
+  if (kcount > 1) {
+    if (npad >= 64) merge_sort(sel, sel + a.sel_slots, npad);
+    else bitonic_sort(sel, npad);
+  }
   // ---- write the row (replicated per output head), -1 past the selection ----
   const int64_t b = row / a.S, s = row % a.S;
   for (int o = 0; o < a.out_heads; ++o) {
@@ -822,7 +843,8 @@ __global__ void __launch_bounds__(kTopkThreads) index_select_kernel(const IndexA
 
 // ---- host side ---------------------------------------------------------------------------
 
-size_t index_topk_smem_bytes(int64_t sel_slots) { return static_cast<size_t>(sel_slots) * 8; }
+// the selection and the merge sort's scratch
+size_t index_topk_smem_bytes(int64_t sel_slots) { return static_cast<size_t>(sel_slots) * 16; }
 
 size_t index_tie_smem_bytes(int hash_slots) {
   return static_cast<size_t>(hash_slots / kTieParts) * 4;

@@ -57,7 +57,8 @@ def test_index_select_bit_exact(cuda_lib, ID, ascending):
                                   dict(IH=64, R=3000, topk=2048, query_start=20000),
                                   dict(IH=3, R=257, topk=300, query_start=900),    # topk > limit
                                   dict(S=5, R=128, topk=33, query_start=200),       # several queries
-                                  dict(IH=130, R=500, topk=1, query_start=10000)])  # topk 1
+                                  dict(IH=130, R=500, topk=1, query_start=10000),   # topk 1
+                                  dict(IH=8, R=5000, topk=4096, query_start=40000)])  # largest k
 def test_index_select_shapes(cuda_lib, over):
     c = _case(**over)
     inp = synth.make_index_inputs(c, seed=21)
