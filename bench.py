@@ -553,7 +553,7 @@ class IndexSelect:
                 "query_position": c.query_start, "record_bytes": c.stride,
                 "step": "one sparse_index_select call: query finalize (bf16, Hadamard, FP4), "
                         "scores (exact dp4a block dots), top-k (hash tie check, radix select, "
-                        "bitonic sort) -- 3 kernels"}
+                        "merge sort) -- 3 kernels"}
 
     def oracle_rows(self, rows):
         import oracle
