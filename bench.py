@@ -818,9 +818,23 @@ TRAFFIC: dict = {
         "fp8_tc05_kernel", 37_857_536, "799adc77e5673050",
         "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the bench's own "
         "workload (37.86 MB read, 768 B written; cold caches under ncu, as above)"),
-    "compress_r4": ("compress_r4_kernel", 547_078_912, "cd7022a0e814742c",
-                    "ncu --set full, one launch of the bench's own workload (537.01 MB read, "
-                    "10.07 MB written)"),
+    "compress_r4": ("compress_r4_kernel", 546_426_624, "89fe5929934292d9",
+                    "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the "
+                    "bench's own workload (536.98 MB read, 9.45 MB written)"),
+    "sparse_bf16_b32_h64_kv8_d128_t8192_k2048": (
+        "gather_stream_kernel", 274_255_872, "96f01ec1f92b7531",
+        "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the bench's own "
+        "workload (270.69 MB read, 3.57 MB written)"),
+    "paged_fp16_b128_h32_kv8_d128_ctx1k-32k_p16": (
+        "gather_stream_kernel", 8_926_250_739, "96f01ec1f92b7531",
+        "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the same "
+        "sequences' distribution at 16 sequences (workload paged_fp16_b16: 1,159.68 MB, 1.0034 x "
+        "its algorithmic bytes), scaled by the algorithmic bytes to the 128-sequence batch"),
+    "prefill_bf16_b4_s4096_h32_kv8_d128_causal_softcap50": (
+        "prefill_tc05_kernel", 427_458_048, "b003441e58206e07",
+        "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the bench's own "
+        "workload (272.07 MB read, 155.39 MB written: part of Y and the present K/V is still in "
+        "L2 when the kernel ends)"),
 }
 
 
