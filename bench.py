@@ -811,7 +811,7 @@ TRAFFIC: dict = {
         "workload (42.67 MB read, 0 written; ncu starts each kernel with cold caches, so the "
         "decoded rows are read from DRAM here and from L2 in a live call)"),
     "index_select_b16_ih64_id128_r16384_k2048": (
-        "index_score_kernel", 18_047_232, "4f9a40538fc99c73",
+        "index_score_kernel", 18_047_232, "7b8479ac54a89ab1",
         "ncu --set full, one launch of the bench's own workload (18.05 MB read, 0 written: the "
         "index records once)"),
     "csa_ref_b16_h128_d512_l128_t65536_k2048": (
