@@ -794,19 +794,19 @@ DP4A_PER_SM_PER_CLOCK = 64
 KERNEL_SOURCES = {
     "gather_stream_kernel": ["k_stream.cu", "gather_common.cuh", "common.cuh", "tc05.cuh",
                              "kernels.h"],
-    "fp8_tc05_kernel": ["k_fp8_tc.cu", "gather_common.cuh", "common.cuh", "tc05.cuh",
+    "fp8_tc05_kernel": ["k_fp8_tc.cu", "e4m3.cuh", "gather_common.cuh", "common.cuh", "tc05.cuh",
                         "kernels.h"],
-    "fp8_decode_kernel": ["k_fp8.cu", "gather_common.cuh", "common.cuh", "kernels.h"],
+    "fp8_decode_kernel": ["k_fp8.cu", "e4m3.cuh", "gather_common.cuh", "common.cuh", "kernels.h"],
     "prefill_tc05_kernel": ["k_prefill.cu", "common.cuh", "tc05.cuh", "kernels.h"],
     "index_score_kernel": ["k_index.cu", "codes.cuh", "common.cuh", "kernels.h"],
     "compress_r4_kernel": ["k_compress.cu", "codes.cuh", "common.cuh", "kernels.h"],
-    "csa_attn_kernel": ["k_csa.cu", "gather_common.cuh", "common.cuh", "kernels.h"],
+    "csa_attn_kernel": ["k_csa.cu", "e4m3.cuh", "gather_common.cuh", "common.cuh", "kernels.h"],
 }
 
 TRAFFIC: dict = {
     # workload: (kernel, bytes per launch, source hash at capture, how)
     "csa_fp8_b16_h128_d576_t65536_k2048_w128": (
-        "fp8_tc05_kernel", 42_666_240, "799adc77e5673050",
+        "fp8_tc05_kernel", 42_666_496, "4d5499920cc78155",
         "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the bench's own "
         "workload (42.67 MB read, 0 written; ncu starts each kernel with cold caches, so the "
         "decoded rows are read from DRAM here and from L2 in a live call)"),
@@ -815,9 +815,9 @@ TRAFFIC: dict = {
         "ncu --set full, one launch of the bench's own workload (18.05 MB read, 0 written: the "
         "index records once)"),
     "csa_ref_b16_h128_d512_l128_t65536_k2048": (
-        "fp8_tc05_kernel", 37_857_536, "799adc77e5673050",
+        "fp8_tc05_kernel", 37_858_048, "4d5499920cc78155",
         "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the bench's own "
-        "workload (37.86 MB read, 768 B written; cold caches under ncu, as above)"),
+        "workload (37.86 MB read, 1,280 B written; cold caches under ncu, as above)"),
     "compress_r4": ("compress_r4_kernel", 546_426_624, "89fe5929934292d9",
                     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch of the "
                     "bench's own workload (536.98 MB read, 9.45 MB written)"),

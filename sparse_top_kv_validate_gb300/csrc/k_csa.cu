@@ -32,9 +32,9 @@
 //    summed through shared memory, an online softmax in the log2 domain with
 //    the slot bias, then O += P . V from the same rows.
 //  * csa_combine_kernel merges key splits in split order (deterministic).
+#include "e4m3.cuh"
 #include "gather_common.cuh"
 
-#include <cuda_fp8.h>
 
 namespace sa {
 
@@ -64,13 +64,8 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Two E4M3FN codes (low byte first) -> two floats, exactly (via f16x2).
-__device__ __forceinline__ float2 e4m3_pair(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two),
-                                                   __NV_E4M3);
-  __half2 hh = *reinterpret_cast<const __half2*>(&h);
-  return __half22float2(hh);
-}
+// Two E4M3FN codes (low byte first) -> two floats, exactly.
+__device__ __forceinline__ float2 e4m3_pair(uint32_t two) { return e4m3x2_to_float2(two); }
 
 // E8M0 scale byte -> 2^(b - 127) (0xFF, NaN in the format, maps to NaN).
 __device__ __forceinline__ float e8m0(uint32_t b) {

@@ -23,9 +23,9 @@
 //    Then each warp does O += P . V over its quarter, P taken straight from
 //    the S accumulators, V through ldmatrix.trans.
 //  * Key chunks merge in the fixed-order combine kernel.
+#include "e4m3.cuh"
 #include "gather_common.cuh"
 
-#include <cuda_fp8.h>
 
 namespace sa {
 
@@ -55,15 +55,6 @@ __device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
 
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Two E4M3FN codes -> two floats, exactly (via the f16x2 conversion).
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two),
-                                                   __NV_E4M3);
-  __half2 hh;
-  hh = *reinterpret_cast<const __half2*>(&h);
-  return __half22float2(hh);
 }
 
 // E8M0 scale byte -> 2^(b - 127) (255 is NaN in the format; it maps to NaN).

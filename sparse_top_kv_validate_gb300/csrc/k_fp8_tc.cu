@@ -45,13 +45,13 @@
 //  k_csa.cu assembles: validity from bytes instead of planned positions, and
 //  an optional additive bias per candidate slot (launch_csa_tc).
 #include <cuda.h>
-#include <cuda_fp8.h>
 
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 
+#include "e4m3.cuh"
 #include "kernels.h"
 #include "tc05.cuh"
 
@@ -226,11 +226,7 @@ __device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
 }
 
 // Two E4M3FN codes -> two floats, exactly (via the f16x2 conversion).
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
-  const __half2_raw h =
-      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) { return e4m3x2_to_float2(two); }
 
 // E8M0 scale byte -> 2^(b - 127); 255 is NaN in the format.
 __device__ __forceinline__ float e8m0_scale(uint32_t b) {
