@@ -67,3 +67,25 @@ def test_cpu_baseline_repeats_whole_passes_up_to_the_budget():
     passes = int(r["sample"].split()[0])
     assert passes >= 2
     assert r["value"] == pytest.approx(passes * wl.rows / r["seconds"], rel=0.02)
+
+
+def test_traffic_entries_name_known_workloads_and_kernels():
+    """Every recorded DRAM-traffic figure belongs to a workload the bench runs
+    and to a kernel whose sources it hashes."""
+    import synth
+    names = {synth.sparse_bf16().name, synth.paged_fp16().name, synth.prefill_bf16().name,
+             synth.csa_fp8().name, synth.csa_ratio4_ref().name, synth.index_select_fp4().name,
+             "compress_r4"}
+    for workload, (kernel, nbytes, digest, how) in bench.TRAFFIC.items():
+        assert workload in names, workload
+        assert kernel in bench.KERNEL_SOURCES, kernel
+        assert nbytes > 0 and len(digest) == 16 and how
+
+
+def test_traffic_is_withheld_when_the_sources_change(monkeypatch):
+    workload, (kernel, nbytes, digest, _) = next(iter(bench.TRAFFIC.items()))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: digest)
+    assert bench.traffic_for(workload, kernel) == nbytes
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
+    assert bench.traffic_for(workload, kernel) is None
+    assert bench.traffic_for("no_such_workload", kernel) is None
