@@ -617,7 +617,7 @@ class CsaRef:
         self.flops = 4.0 * c.H * c.D * self.keys
         self.decode_bytes = (valid_sel * c.stride + c.B * c.S * min(c.L, 128) * c.D * es
                              + 2 * self.q.numel() * es + self.sel.numel() * 4)
-        self.launches_per_step = 3  # assemble, attention, split merge
+        self.launches_per_step = 3  # assemble, attention, split merge (2 when merged on chip)
 
     def step(self, ev=None):
         c = self.c
@@ -959,6 +959,17 @@ def run_gpu(args):
             print(f"# CUDA graph capture failed ({exc}); timing direct calls", file=sys.stderr)
             graph = None
 
+    # the library's kernels in one step: counted from the captured graph's
+    # kernel nodes (the step is one library call, nothing else), else stated
+    launches = wl.launches_per_step
+    launches_how = "stated by the workload"
+    if graph is not None:
+        try:
+            launches = sa.graph_kernel_count(graph)
+            launches_how = "kernel nodes of the captured step"
+        except Exception as exc:  # no graph introspection: the stated count
+            print(f"# graph kernel count failed ({exc}); using the stated count", file=sys.stderr)
+
     steps = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -1108,7 +1119,8 @@ def run_gpu(args):
                               else "direct copies and library call per step"},
             "hot_l2": {"ms_per_step": round(hot_ms, 5), "steps": hot_steps,
                        "note": "steps back to back, L2 not flushed"},
-            "gpu_launches": wl.launches_per_step * steps,
+            "gpu_launches": launches * steps,
+            "launches_per_step": {"value": launches, "how": launches_how},
             "clocks": clk.summary(),
             "wall_s_timed_region": round(wall, 4),
             "err_word": err,

@@ -122,6 +122,16 @@ int sa_version(void);
 int sa_set_kernel_events(void* before, void* after);
 
 /*
+ * sa_graph_kernel_count -- measurement hook (no counterpart on the pages): the
+ * number of kernel nodes in a CUDA graph (a cudaGraph_t, not owned), e.g. one
+ * library call captured from a stream, so that a benchmark can state how many
+ * of the library's kernels one call launches.  Returns the count, or a
+ * negative status (SA_ERR_NULL for a NULL graph, SA_ERR_LAUNCH if the graph
+ * cannot be read).
+ */
+int sa_graph_kernel_count(void* graph);
+
+/*
  * sa_check_wait_timeout -- diagnostic (no counterpart on the pages): runs the
  * library's bounded-wait timeout path on purpose, without a fault.
  *

@@ -21,7 +21,7 @@ import threading
 import torch
 
 __all__ = [
-    "load", "lib_path", "SAError", "status_string", "check_wait_timeout",
+    "load", "lib_path", "SAError", "status_string", "check_wait_timeout", "graph_kernel_count",
     "validate_indices", "build_present_kv", "sparse_attn_decode", "attn_prefill",
     "paged_attn_decode", "sparse_attn_decode_workspace", "attn_prefill_workspace",
     "paged_attn_decode_workspace", "new_workspace", "sparse_attn_decode_noalloc",
@@ -193,6 +193,8 @@ def load():
         L.csa_pool_weight.argtypes = [_p, _p, _i64, _p]
         L.sa_check_wait_timeout.restype = C.c_int
         L.sa_check_wait_timeout.argtypes = [_p, _p, _p]
+        L.sa_graph_kernel_count.restype = C.c_int
+        L.sa_graph_kernel_count.argtypes = [_p]
         L.paged_attn_decode_workspace.restype = C.c_size_t
         L.paged_attn_decode_workspace.argtypes = [C.POINTER(PagedParams)]
         L.paged_attn_decode.restype = C.c_int
@@ -718,6 +720,14 @@ def csa_ratio4_index_compress(kv, gate, ape, norm, carry, *, n_rope, total, reco
     _compress("csa_ratio4_index_compress", 4, kv.shape[2] // 2, kv, gate, ape, norm, carry,
               n_rope=n_rope, total=total, records=records, logical=logical,
               err_word=err_word, stream=stream)
+
+
+def graph_kernel_count(graph) -> int:
+    """Kernel nodes in a captured ``torch.cuda.CUDAGraph`` (measurement hook:
+    how many kernels one captured call launches)."""
+    n = load().sa_graph_kernel_count(C.c_void_p(graph.raw_cuda_graph()))
+    _check("sa_graph_kernel_count", min(n, 0))
+    return n
 
 
 def check_wait_timeout(device="cuda", stream=None):

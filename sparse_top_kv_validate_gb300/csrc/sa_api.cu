@@ -9,6 +9,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <vector>
+
 #include "../../include/sa.h"
 #include "kernels.h"
 
@@ -414,6 +416,22 @@ int sa_set_kernel_events(void* before, void* after) {
   t_ev_before = before;
   t_ev_after = after;
   return SA_OK;
+}
+
+int sa_graph_kernel_count(void* graph) {
+  if (!graph) return SA_ERR_NULL;
+  cudaGraph_t g = static_cast<cudaGraph_t>(graph);
+  size_t n = 0;
+  if (cudaGraphGetNodes(g, nullptr, &n) != cudaSuccess) return SA_ERR_LAUNCH;
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (n > 0 && cudaGraphGetNodes(g, nodes.data(), &n) != cudaSuccess) return SA_ERR_LAUNCH;
+  int kernels = 0;
+  for (size_t i = 0; i < n; ++i) {
+    cudaGraphNodeType t;
+    if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess) return SA_ERR_LAUNCH;
+    if (t == cudaGraphNodeTypeKernel) ++kernels;
+  }
+  return kernels;
 }
 
 int sa_check_wait_timeout(uint32_t* err_word, uint32_t* out, void* stream) {
