@@ -964,9 +964,14 @@ def run_gpu(args):
     launches = wl.launches_per_step
     launches_how = "stated by the workload"
     if graph is not None:
-        try:
-            launches = sa.graph_kernel_count(graph)
+        try:  # a second capture of the step, kept as a graph to read, never replayed
+            cg = torch.cuda.CUDAGraph(keep_graph=True)
+            with torch.cuda.graph(cg):
+                wl.step()
+            torch.cuda.synchronize(dev)
+            launches = sa.graph_kernel_count(cg)
             launches_how = "kernel nodes of the captured step"
+            del cg
         except Exception as exc:  # no graph introspection: the stated count
             print(f"# graph kernel count failed ({exc}); using the stated count", file=sys.stderr)
 
