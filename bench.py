@@ -642,7 +642,8 @@ class CsaRef:
                 "records": c.R, "top_k": c.topk, "record_bytes": c.stride,
                 "step": "one csa_ratio4_attention call: candidate assembly (window rows, "
                         "FP8 record decode), tcgen05 attention with sink (128-head blocks, "
-                        "two CTAs of 256 output dims), split merge -- 3 kernels"}
+                        "two CTAs of 256 output dims; key splits merged on chip in clusters, "
+                        "else by a split-merge kernel) -- 2 or 3 kernels"}
 
     def oracle_rows(self, rows):
         import oracle
