@@ -551,6 +551,9 @@ class IndexSelect:
         return {"workload": c.name, "batch": c.B, "queries": c.S, "index_heads": c.IH,
                 "index_dim": c.ID, "records": c.R, "top_k": c.topk,
                 "query_position": c.query_start, "record_bytes": c.stride,
+                "equal_scores": "the synthetic FP4 keys give equal scores in some rows: the "
+                                "device ranks them by record and flags them (err_word "
+                                "SA_ERRBIT_SEL_TIE = 512), as the oracle does",
                 "step": "one sparse_index_select call: query finalize (bf16, Hadamard, FP4), "
                         "scores (exact dp4a block dots), top-k (hash tie check, radix select, "
                         "merge sort) -- 3 kernels"}
@@ -917,6 +920,63 @@ def make_workload(sa, name, dev):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+# The other workloads, measured after the headline in the default run (one GPU)
+# so that one bench line carries every workload's figures.
+SECONDARY = ["csa_fp8", "paged_fp16", "prefill_bf16", "index_select", "csa_ref", "compress_r4"]
+
+
+def measure_secondary(sa, name, dev, flush_l2, peaks, steps=20):
+    """One more workload in the same process by the headline's protocol at fewer
+    steps: CUDA graph replay of one step, L2 flushed between steps outside the
+    events, the dominant kernel timed by events captured as graph nodes.  Its
+    buffers are released afterwards."""
+    wl = make_workload(sa, name, dev)
+    graph = kgraph = None
+    try:
+        stream = torch.cuda.current_stream(dev)
+        for _ in range(3):
+            flush_l2()
+            wl.step()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            wl.step()
+        torch.cuda.synchronize(dev)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush_l2()
+            st[i].record(stream)
+            graph.replay()
+            en[i].record(stream)
+        torch.cuda.synchronize(dev)
+        step_ms = [a.elapsed_time(b) for a, b in zip(st, en)]
+        kb, ka = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with sa.kernel_events(kb, ka):
+            kgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(kgraph):
+                wl.step()
+        torch.cuda.synchronize(dev)
+        ks = []
+        for _ in range(min(steps, 10)):
+            flush_l2()
+            kgraph.replay()
+            torch.cuda.synchronize(dev)
+            ks.append(kb.elapsed_time(ka))
+        rl = wl.roofline(statistics.median(step_ms), statistics.median(ks), peaks)
+        keep = ("bound", "kernel", "achieved", "peak", "unit", "frac", "traffic", "kernel_us",
+                "call_us")
+        return {"value": round(job_rate(wl.rows, 1, steps, sum(step_ms)), 1),
+                "unit": unit_of(wl), "ms_per_step": round(sum(step_ms) / steps, 5),
+                "steps": steps, "workload": wl.config()["workload"],
+                "roofline": {k: rl.get(k) for k in keep}, "err_word": int(wl.err.item())}
+    finally:
+        del graph, kgraph, wl
+        torch.cuda.empty_cache()
+
+
 def run_gpu(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -1133,6 +1193,19 @@ def run_gpu(args):
         }
         if ws == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, args)
+        if ws == 1 and args.workload in ("sparse_bf16", "default") and not args.no_secondary:
+            # after the headline's timed region; each workload's own events
+            others = {}
+            del graph, e2e_graph, kgraph
+            with ClockSampler(dev) as clk2:
+                for name in SECONDARY:
+                    try:
+                        others[name] = measure_secondary(sa, name, dev, flush_l2, peaks)
+                    except Exception as exc:  # one failed workload leaves the line intact
+                        others[name] = {"error": f"{type(exc).__name__}: {exc}"[:200]}
+            line["other_workloads"] = dict(others, clocks=clk2.summary(),
+                                           note="measured after the headline by the same "
+                                                "protocol at 20 steps; not part of value")
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -1260,6 +1333,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sparse_bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="default workload only: skip the other workloads' figures")
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct library calls instead of a CUDA graph of one call")
     args = ap.parse_args()
