@@ -20,9 +20,9 @@
 //  * gather_simt_kernel: the general path for fp32 storage and the shapes the
 //    tensor-core kernel does not take.  One CTA per (unit, head, split of
 //    `chunk` candidates); warps stride over the candidates, each lane holding
-//    DPL dims (d = lane + 32 k); fp32 FMA and an online softmax; the bias and
-//    mask terms of gather_common.cuh.  Warps merge in shared memory in warp
-//    order.
+//    DPL dims (d = lane + 32 k), a few candidates' rows loaded at once; fp32
+//    FMA and an online softmax; the bias and mask terms of gather_common.cuh.
+//    Warps merge in shared memory in warp order.
 //  * combine_kernel and combine_flat_kernel: the fixed-order log-sum-exp merge
 //    of split partials (max, sum, unnormalised P.V), with the sink logit in
 //    the denominator; combine_flat_kernel is one thread per four output dims
@@ -120,37 +120,61 @@ __global__ void __launch_bounds__(128) gather_simt_kernel(GatherArgs a) {
   const T* kp = static_cast<const T*>(a.k);
   const T* vp = static_cast<const T*>(a.v);
   const float sl2 = a.scale_log2;
-  for (int64_t c = c0 + warp; c < c1; c += 4) {
-    const int32_t row = resolve_candidate(a, u, c);
-    if (row < 0) continue;
-    const T* kr = kp + static_cast<int64_t>(row) * D;
-    float dot = 0.f;
+  // Warp w takes candidates c0 + w, c0 + w + 4, ... in that order, kU at a
+  // time: the kU rows are resolved and their K and V values loaded together
+  // (independent loads in flight), then the online softmax takes them in turn.
+  constexpr int kU = DPL <= 2 ? 4 : (DPL <= 4 ? 2 : 1);
+  for (int64_t cb = c0 + warp; cb < c1; cb += 4 * kU) {
+    int32_t rows[kU];
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) {
-      const int64_t d = lane + 32 * k;
-      if (d < D) dot = fmaf(q[k], to_f32<T>(kr[d]), dot);
+    for (int t = 0; t < kU; ++t) {
+      const int64_t c = cb + 4 * t;
+      rows[t] = c < c1 ? resolve_candidate(a, u, c) : -1;
+    }
+    float kv[kU][DPL], vv[kU][DPL];
+#pragma unroll
+    for (int t = 0; t < kU; ++t) {
+      const T* kr = kp + static_cast<int64_t>(rows[t] < 0 ? 0 : rows[t]) * D;
+      const T* vr = vp + static_cast<int64_t>(rows[t] < 0 ? 0 : rows[t]) * D;
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) {
+        const int64_t d = lane + 32 * k;
+        const bool in = rows[t] >= 0 && d < D;
+        kv[t][k] = in ? to_f32<T>(kr[d]) : 0.f;
+        vv[t][k] = in ? to_f32<T>(vr[d]) : 0.f;
+      }
     }
 #pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
-    float x;
-    if (a.softcap != 0.f) x = a.softcap * tanhf(dot * (sl2 / kLog2e) * a.inv_softcap) * kLog2e;
-    else x = dot * sl2;
-    if (a.bias) {  // [IS] bias_at / [SA] mask_bias, keyed by the cache position
-      const int64_t j = row - (u.b * a.Hkv + u.kvh) * a.T;
-      x += kLog2e * bias_term(a, u.b, h, u.i, j);
-      if (x == SA_NEG_INF) continue;  // a -inf term masks the key
-    }
-    const float mn = fmaxf(m, x);
-    const float al = exp2f(m - mn);  // m == -inf -> 0
-    const float p = exp2f(x - mn);
-    l = l * al + p;
-    const T* vr = vp + static_cast<int64_t>(row) * D;
+    for (int t = 0; t < kU; ++t) {
+      const int32_t row = rows[t];
+      if (row < 0) continue;
+      float dot = 0.f;
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) {
-      const int64_t d = lane + 32 * k;
-      o[k] = o[k] * al + (d < D ? p * to_f32<T>(vr[d]) : 0.f);
+      for (int k = 0; k < DPL; ++k) {
+        const int64_t d = lane + 32 * k;
+        if (d < D) dot = fmaf(q[k], kv[t][k], dot);
+      }
+#pragma unroll
+      for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+      float x;
+      if (a.softcap != 0.f) x = a.softcap * tanhf(dot * (sl2 / kLog2e) * a.inv_softcap) * kLog2e;
+      else x = dot * sl2;
+      if (a.bias) {  // [IS] bias_at / [SA] mask_bias, keyed by the cache position
+        const int64_t j = row - (u.b * a.Hkv + u.kvh) * a.T;
+        x += kLog2e * bias_term(a, u.b, h, u.i, j);
+        if (x == SA_NEG_INF) continue;  // a -inf term masks the key
+      }
+      const float mn = fmaxf(m, x);
+      const float al = exp2f(m - mn);  // m == -inf -> 0
+      const float p = exp2f(x - mn);
+      l = l * al + p;
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) {
+        const int64_t d = lane + 32 * k;
+        o[k] = o[k] * al + (d < D ? p * vv[t][k] : 0.f);
+      }
+      m = mn;
     }
-    m = mn;
   }
 #pragma unroll
   for (int k = 0; k < DPL; ++k) sm_o[warp][lane + 32 * k] = o[k];
