@@ -77,7 +77,7 @@ def test_csa_matches_oracle(cuda_lib, dt, name, over):
     _close(y, ref, f"{name} {dt}")
 
 
-@pytest.mark.parametrize("H", [32, 128])
+@pytest.mark.parametrize("H", [32, 128, 384])
 @pytest.mark.parametrize("shape_kind", ["h1c", "b11c", "c", "full"])
 def test_slot_bias(cuda_lib, shape_kind, H):
     c = synth.CsaCase("bias", B=2, S=2, H=H, D=512, n_rope=64, L=128, total=1200, topk=80)
